@@ -1,0 +1,28 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+HERE = os.path.dirname(os.path.abspath(__file__))
+if HERE not in sys.path:
+    sys.path.insert(0, HERE)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a)")
+    config.addinivalue_line("markers", "slow: long-running CPU oracle case")
+
+
+def golden_path(name: str) -> str:
+    return os.path.join(HERE, "golden", name)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built_cpu_side():
+    import oracle
+    import synth
+    oracle.build()
+    synth.build(device=False)

@@ -1,0 +1,43 @@
+"""The seeded input generator: Philox known answers and the workload recipes."""
+import numpy as np
+
+import synth
+
+
+def test_philox4x32_10_known_answers():
+    # Known-answer vectors published with the Random123 library (Salmon et al.,
+    # SC'11) for philox4x32 with 10 rounds.
+    kat = [
+        ([0, 0, 0, 0], [0, 0], [0x6627e8d5, 0xe169c58d, 0xbc57ac4c, 0x9b00dbd8]),
+        ([0xffffffff] * 4, [0xffffffff] * 2, [0x408f276d, 0x41c83b0e, 0xa20bc7c6, 0x6d5451fd]),
+        ([0x243f6a88, 0x85a308d3, 0x13198a2e, 0x03707344], [0xa4093822, 0x299f31d0],
+         [0xd16cfe09, 0x94fdcceb, 0x5001e420, 0x24126ea1]),
+    ]
+    for ctr, key, out in kat:
+        assert synth.philox(ctr, key) == out
+
+
+def test_weight_distributions():
+    q = synth.mx_codes(0, synth.GATE_Q, 3, 256, 512)
+    codes = np.concatenate([q & 15, q >> 4]).ravel()
+    cnt = np.bincount(codes, minlength=16)
+    assert cnt.min() > 0.9 * codes.size / 16 and cnt.max() < 1.1 * codes.size / 16
+    s = synth.mx_scales(0, synth.GATE_S, 3, 256, 512)
+    assert set(np.unique(s).tolist()) == {123, 124, 125, 126, 127}
+
+
+def test_streams_are_keyed_by_expert_and_tensor():
+    a = synth.mx_codes(0, synth.GATE_Q, 0, 4, 64)
+    assert not np.array_equal(a, synth.mx_codes(0, synth.GATE_Q, 1, 4, 64))
+    assert not np.array_equal(a, synth.mx_codes(0, synth.UP_Q, 0, 4, 64))
+    np.testing.assert_array_equal(a, synth.mx_codes(0, synth.GATE_Q, 0, 4, 64))
+    # rows are independent of how many rows are drawn
+    np.testing.assert_array_equal(a[:2], synth.mx_codes(0, synth.GATE_Q, 0, 2, 64))
+
+
+def test_normals():
+    x = synth.normal_f32(1, synth.X, 200, 1000)
+    assert abs(x.mean()) < 0.01 and abs(x.std() - 1) < 0.01
+    b = synth.normal_bf16(1, synth.X, 200, 1000)
+    xf = (b.astype(np.uint32) << 16).view(np.float32)
+    assert np.max(np.abs(xf - x)) <= np.max(np.abs(x)) * 2.0 ** -8
