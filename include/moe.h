@@ -1,0 +1,172 @@
+/*
+ * moe.h — C ABI of the routed-expert FFN library (libmoe.so), GB300 / sm_103a.
+ *
+ * The operation is one routed-MoE layer of a Kimi-K3-style model: every token
+ * selects top_k of n_experts experts (16 of 896 in K3: MoonTail, intro;
+ * Moonshine README, "How the engine works"), all rows selecting each expert
+ * are grouped and only the unique selected experts are read (Moonshine README,
+ * "How the engine works", prefill paragraph; Moonshine GitHub README,
+ * "Prefill"), each selected expert runs its SwiGLU FFN on MXFP4 weights
+ * (MoonTail, requester/volunteer table: "Routed expert FFN"; Moonshine GitHub
+ * README, MiMo section: "MXFP4 kernels"), and the weighted expert outputs are
+ * reduced back to token order (Moonshine README, "Run layer-major prefill":
+ * the MoE tail's weighted reduction). Decode is token-major and prefill
+ * layer-major (Moonshine README, "How the engine works"); here that split is
+ * moe_decode (CUDA-core streaming of the selected experts) versus
+ * moe_forward (grouped block-scaled tensor-core GEMMs).
+ *
+ * Conventions for every call below:
+ *  - Pointers are DEVICE pointers unless marked "host". All calls are
+ *    asynchronous on `stream` (a cudaStream_t passed as void*; NULL = legacy
+ *    default stream) except moe_create, moe_destroy, moe_status and the
+ *    size queries, which are host-only.
+ *  - No call allocates or frees device memory, except moe_create (one 4-byte
+ *    device status word) and moe_destroy (frees it). Scratch memory is the
+ *    caller's `ws` buffer, sized by moe_workspace_bytes.
+ *  - The caller owns every buffer; the handle keeps the weight pointers it was
+ *    given (it does not copy weights), so they must outlive the handle.
+ *  - Return value: MOE_OK (0) or a negative MOE_ERR_* code. Argument errors are
+ *    detected on the host before anything is launched. Data errors found on
+ *    the device (NaN logits, out-of-range indices in a caller-supplied plan,
+ *    an expired device-side wait) are recorded in the handle's status word and
+ *    reported by moe_status; the kernels skip the offending element instead of
+ *    faulting.
+ *
+ * Data layouts (row-major, C order):
+ *   x        bf16 [T][d_model]               (uint16 bit patterns)
+ *   logits   fp32 [T][n_experts]
+ *   out      bf16 [T][d_model]
+ *   MXFP4 matrix with N rows and reduction length K (K % 32 == 0):
+ *     codes  uint8 [N][K/2]   element kk in byte kk/2, even element in the low
+ *                             nibble; each nibble an OCP E2M1 code
+ *     scales uint8 [N][K/32]  OCP E8M0 (2^(b-127)), one per 32 elements along K
+ *   gate, up  per expert N = d_ff,    K = d_model   -> [E][d_ff][d_model/2] ...
+ *   down      per expert N = d_model, K = d_ff      -> [E][d_model][d_ff/2] ...
+ *   w_router  fp32 [n_experts][d_model]   (router_mode MOE_ROUTER_XWR only)
+ *   sh_gate, sh_up bf16 [d_ff][d_model]; sh_down bf16 [d_model][d_ff]
+ *                                         (has_shared only)
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum moe_status_code {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,     /* null pointer, negative size, bad desc field */
+    MOE_ERR_UNSUPPORTED = -2,     /* shape outside the supported envelope, or no sm_103 GPU */
+    MOE_ERR_WORKSPACE = -3,       /* ws_bytes smaller than moe_workspace_bytes() */
+    MOE_ERR_CUDA = -4,            /* a CUDA runtime call or launch failed */
+    MOE_ERR_DEVICE_TIMEOUT = -5,  /* a device-side wait hit its iteration limit */
+    MOE_ERR_NAN_LOGIT = -6,       /* a router logit was NaN (treated as -inf) */
+    MOE_ERR_BAD_INDEX = -7        /* out-of-range expert / row index in a plan */
+};
+
+enum moe_router_mode {
+    MOE_ROUTER_LOGITS = 0,  /* moe_plan takes fp32 logits [T][E] */
+    MOE_ROUTER_XWR = 1      /* moe_plan computes logits = x . W_r^T in fp32 */
+};
+
+enum moe_op {
+    MOE_OP_PLAN = 0,
+    MOE_OP_FORWARD = 1,
+    MOE_OP_DECODE = 2
+};
+
+/* Layer shape. Supported envelope: d_model and d_ff multiples of 128,
+ * d_model <= 16384, d_ff <= 8192, 1 <= top_k <= 32, top_k <= n_experts <= 1024. */
+typedef struct moe_desc {
+    int32_t d_model;
+    int32_t d_ff;
+    int32_t n_experts;
+    int32_t top_k;
+    int32_t router_mode;  /* enum moe_router_mode */
+    int32_t has_shared;   /* 1: one always-on bf16 SwiGLU shared expert, weight 1.0 */
+} moe_desc;
+
+/* Device pointers to the layer's weights (see layouts above). Unused fields NULL. */
+typedef struct moe_weights {
+    const uint8_t *gate_q, *gate_s;
+    const uint8_t *up_q, *up_s;
+    const uint8_t *down_q, *down_s;
+    const float *w_router;
+    const uint16_t *sh_gate, *sh_up, *sh_down;
+} moe_weights;
+
+/* Route plan, caller-allocated device buffers, written by moe_plan:
+ *   topk_idx int32 [T][top_k]  selected experts, descending logit, ties to the
+ *                              lower expert index (+0 == -0)
+ *   topk_w   fp32  [T][top_k]  exp(l_j - l_max) / sum over the selected
+ *   counts   int32 [E]         rows routed to each expert
+ *   offsets  int32 [E+1]       exclusive scan of counts; offsets[E] = T*top_k
+ *   perm     int32 [T*top_k]   flat indices t*top_k+j sorted by (expert, flat)
+ *   inv      int32 [T*top_k]   inv[perm[p]] = p
+ *   active   int32 [E+1]       active[0] = number of experts with rows,
+ *                              active[1..] = those experts, ascending
+ * moe_forward and moe_decode read topk_w, offsets, perm, inv and active. */
+typedef struct moe_plan_buf {
+    int32_t *topk_idx;
+    float *topk_w;
+    int32_t *counts;
+    int32_t *offsets;
+    int32_t *perm;
+    int32_t *inv;
+    int32_t *active;
+} moe_plan_buf;
+
+typedef struct moe_handle moe_handle;
+
+/* Host. Validates the shape against the supported envelope and the current
+ * device (must be compute capability 10.3), records the weight pointers and
+ * allocates the 4-byte device status word. *out is NULL on failure. */
+int moe_create(const moe_desc *desc, const moe_weights *weights, moe_handle **out);
+
+/* Host. Frees the status word and the handle. NULL is a no-op. */
+void moe_destroy(moe_handle *h);
+
+/* Host. Bytes of one expert's three MXFP4 matrices (codes + scales):
+ * 3 * (d_model*d_ff/2 + d_model*d_ff/32). 17,547,264 for d_model=7168,
+ * d_ff=1536. Returns -1 if either size is not a positive multiple of 32. */
+int64_t moe_expert_bytes(int32_t d_model, int32_t d_ff);
+
+/* Host. Scratch bytes `op` (enum moe_op) needs for T tokens; 0 for T == 0. */
+size_t moe_workspace_bytes(const moe_handle *h, int32_t T, int32_t op);
+
+/* Route T tokens: top-k + weights, then the stable per-expert plan.
+ * logits: fp32 [T][E] (MOE_ROUTER_LOGITS; x may be NULL) or NULL with x given
+ * (MOE_ROUTER_XWR). ws: >= moe_workspace_bytes(h, T, MOE_OP_PLAN).
+ * T == 0 is a no-op returning MOE_OK. */
+int moe_plan(moe_handle *h, int32_t T, const float *logits, const uint16_t *x,
+             const moe_plan_buf *plan, void *ws, size_t ws_bytes, void *stream);
+
+/* Layer-major expert FFN for a planned batch (prefill): grouped block-scaled
+ * MXFP4 GEMMs on tcgen05 tensor cores (gate/up with SwiGLU, then down with
+ * the weighted scatter), finalised to bf16 out [T][d_model].
+ * ws: >= moe_workspace_bytes(h, T, MOE_OP_FORWARD). */
+int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
+                uint16_t *out, void *ws, size_t ws_bytes, void *stream);
+
+/* Token-major expert FFN (decode, any T; intended for T <= 16): streams only
+ * the active experts' packed codes with 128-bit loads and reduces on CUDA
+ * cores in fp32, then combines deterministically in top-k order.
+ * ws: >= moe_workspace_bytes(h, T, MOE_OP_DECODE). */
+int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
+               uint16_t *out, void *ws, size_t ws_bytes, void *stream);
+
+/* Host. Synchronises `stream`, returns the first device-side error recorded
+ * since the last call (MOE_OK if none) and clears it. */
+int moe_status(moe_handle *h, void *stream);
+
+/* Host. Static description of a status code. */
+const char *moe_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,158 @@
+"""Python binding of libmoe.so, the GB300 routed-expert FFN library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/moe.h``. The functions keep the
+C names (``moe_create``, ``moe_plan``, ``moe_forward``, ``moe_decode``, ...);
+tensors are passed as device pointers and PyTorch only provides device memory
+and streams. Importing this module fails loudly if the library is missing;
+there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED = -2
+MOE_ERR_WORKSPACE = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_DEVICE_TIMEOUT = -5
+MOE_ERR_NAN_LOGIT = -6
+MOE_ERR_BAD_INDEX = -7
+
+MOE_ROUTER_LOGITS = 0
+MOE_ROUTER_XWR = 1
+
+MOE_OP_PLAN = 0
+MOE_OP_FORWARD = 1
+MOE_OP_DECODE = 2
+
+# Every symbol include/moe.h declares.
+EXPORTS = ("moe_create", "moe_destroy", "moe_expert_bytes", "moe_workspace_bytes", "moe_plan",
+           "moe_forward", "moe_decode", "moe_status", "moe_strerror")
+
+
+class moe_desc(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("router_mode", ctypes.c_int32), ("has_shared", ctypes.c_int32)]
+
+
+class moe_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q",
+                                                "down_s", "w_router", "sh_gate", "sh_up",
+                                                "sh_down")]
+
+
+class moe_plan_buf(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("topk_idx", "topk_w", "counts", "offsets", "perm",
+                                                "inv", "active")]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str = ""):
+        self.code = code
+        super().__init__(f"{where}: {moe_strerror(code)} ({code})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe.so (raises OSError if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise OSError(f"{LIB_PATH} is missing: build it with "
+                          "mxfp4_routed_expert_03_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        p, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        L.moe_create.argtypes = [ctypes.POINTER(moe_desc), ctypes.POINTER(moe_weights),
+                                 ctypes.POINTER(p)]
+        L.moe_create.restype = ctypes.c_int
+        L.moe_destroy.argtypes = [p]
+        L.moe_destroy.restype = None
+        L.moe_expert_bytes.argtypes = [i32, i32]
+        L.moe_expert_bytes.restype = i64
+        L.moe_workspace_bytes.argtypes = [p, i32, i32]
+        L.moe_workspace_bytes.restype = sz
+        L.moe_plan.argtypes = [p, i32, p, p, ctypes.POINTER(moe_plan_buf), p, sz, p]
+        L.moe_plan.restype = ctypes.c_int
+        for fn in (L.moe_forward, L.moe_decode):
+            fn.argtypes = [p, i32, p, ctypes.POINTER(moe_plan_buf), p, p, sz, p]
+            fn.restype = ctypes.c_int
+        L.moe_status.argtypes = [p, p]
+        L.moe_status.restype = ctypes.c_int
+        L.moe_strerror.argtypes = [ctypes.c_int]
+        L.moe_strerror.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _ptr(t) -> int | None:
+    """Device pointer of a tensor (or an int pointer, or None)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def moe_strerror(code: int) -> str:
+    return lib().moe_strerror(code).decode()
+
+
+def moe_expert_bytes(d_model: int, d_ff: int) -> int:
+    return lib().moe_expert_bytes(d_model, d_ff)
+
+
+def moe_create(desc: moe_desc, weights: moe_weights) -> int:
+    h = ctypes.c_void_p()
+    rc = lib().moe_create(ctypes.byref(desc), ctypes.byref(weights), ctypes.byref(h))
+    if rc != MOE_OK:
+        raise MoeError(rc, "moe_create")
+    return h.value
+
+
+def moe_destroy(h: int) -> None:
+    lib().moe_destroy(h)
+
+
+def moe_workspace_bytes(h: int, T: int, op: int) -> int:
+    return lib().moe_workspace_bytes(h, T, op)
+
+
+def moe_plan(h, T, logits, x, plan: moe_plan_buf, ws, ws_bytes, stream=None) -> int:
+    return lib().moe_plan(h, T, _ptr(logits), _ptr(x), ctypes.byref(plan), _ptr(ws), ws_bytes,
+                          _stream(stream))
+
+
+def moe_forward(h, T, x, plan: moe_plan_buf, out, ws, ws_bytes, stream=None) -> int:
+    return lib().moe_forward(h, T, _ptr(x), ctypes.byref(plan), _ptr(out), _ptr(ws), ws_bytes,
+                             _stream(stream))
+
+
+def moe_decode(h, T, x, plan: moe_plan_buf, out, ws, ws_bytes, stream=None) -> int:
+    return lib().moe_decode(h, T, _ptr(x), ctypes.byref(plan), _ptr(out), _ptr(ws), ws_bytes,
+                            _stream(stream))
+
+
+def moe_status(h, stream=None) -> int:
+    return lib().moe_status(h, _stream(stream))
+
+
+def check(rc: int, where: str = "") -> None:
+    if rc != MOE_OK:
+        raise MoeError(rc, where)

@@ -1,0 +1,315 @@
+// C ABI of the routed-expert FFN library: argument validation, workspace
+// carving and kernel launches. See include/moe.h for the contract.
+#include <stdlib.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+struct moe_handle {
+    moe_desc desc;
+    moe_weights w;
+    int device;
+    int num_sms;
+    int *status;  // device word: first error code recorded by a kernel
+    CUtensorMap map_gate, map_up, map_down;  // TMA views of the packed E2M1 weights
+};
+
+// Device-side waits give up after this many SM clocks (about one second).
+static const long long kTimeoutCycles = 2000000000LL;
+
+// cuTensorMapEncodeTiled, looked up through the runtime so the library does
+// not link the driver library directly (it must load on hosts without a GPU).
+typedef CUresult (*encode_tiled_fn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static encode_tiled_fn encode_tiled() {
+    static encode_tiled_fn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (encode_tiled_fn)p;
+    }
+    return fn;
+}
+
+// 2D tensor map over a row-major byte matrix [rows][cols(elements)].
+static bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t cols,
+                        uint64_t rows, uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows) {
+    encode_tiled_fn enc = encode_tiled();
+    if (!enc) return false;
+    cuuint64_t gd[2] = {cols, rows};
+    cuuint64_t gs[1] = {row_bytes};
+    cuuint32_t bd[2] = {box_cols, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, dt, 2, const_cast<void *>(base), gd, gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Workspace of moe_forward, carved in this order (each region 1 KB aligned).
+struct FwdLayout {
+    size_t xq_hi, xq_lo, xs_hi, xs_lo, hq_hi, hq_lo, hs_hi, hs_lo, acc, prefix, total;
+};
+
+static FwdLayout fwd_layout(int T, int D, int F, int E, int k) {
+    FwdLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += (bytes + 1023) / 1024 * 1024;
+        return o;
+    };
+    size_t rows = (size_t)T * k;
+    L.xq_hi = take((size_t)T * D);
+    L.xq_lo = take((size_t)T * D);
+    L.xs_hi = take((size_t)T * D / 32);
+    L.xs_lo = take((size_t)T * D / 32);
+    L.hq_hi = take(rows * F);
+    L.hq_lo = take(rows * F);
+    L.hs_hi = take(rows * F / 32);
+    L.hs_lo = take(rows * F / 32);
+    L.acc = take((size_t)T * D * sizeof(float));
+    L.prefix = take((size_t)(E + 1) * sizeof(int32_t));
+    L.total = off;
+    return L;
+}
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+MOE_API int64_t moe_expert_bytes(int32_t d_model, int32_t d_ff) {
+    if (d_model <= 0 || d_ff <= 0 || d_model % 32 || d_ff % 32) return -1;
+    int64_t n = (int64_t)d_model * d_ff;
+    return 3 * (n / 2 + n / 32);
+}
+
+MOE_API const char *moe_strerror(int code) {
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape or device";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+        case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case MOE_ERR_NAN_LOGIT: return "NaN router logit";
+        case MOE_ERR_BAD_INDEX: return "out-of-range index in plan";
+        default: return "unknown status code";
+    }
+}
+
+MOE_API int moe_create(const moe_desc *d, const moe_weights *w, moe_handle **out) {
+    if (!out) return MOE_ERR_INVALID_ARG;
+    *out = NULL;
+    if (!d || !w) return MOE_ERR_INVALID_ARG;
+    if (d->d_model <= 0 || d->d_ff <= 0 || d->n_experts <= 0 || d->top_k <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (d->router_mode != MOE_ROUTER_LOGITS && d->router_mode != MOE_ROUTER_XWR)
+        return MOE_ERR_INVALID_ARG;
+    if (d->has_shared != 0 && d->has_shared != 1) return MOE_ERR_INVALID_ARG;
+    if (d->top_k > d->n_experts) return MOE_ERR_INVALID_ARG;
+    if (d->d_model % 128 || d->d_ff % 128 || d->d_model > MOE_MAX_DMODEL ||
+        d->d_ff > MOE_MAX_DFF || d->top_k > MOE_MAX_TOPK || d->n_experts > MOE_MAX_EXPERTS)
+        return MOE_ERR_UNSUPPORTED;
+    if (moe_decode_per_lane(d->d_model) == 0 || moe_decode_per_lane(d->d_ff) == 0)
+        return MOE_ERR_UNSUPPORTED;
+    const void *req[] = {w->gate_q, w->gate_s, w->up_q, w->up_s, w->down_q, w->down_s};
+    for (const void *p : req)
+        if (!p) return MOE_ERR_INVALID_ARG;
+    if (((uintptr_t)w->gate_q | (uintptr_t)w->up_q | (uintptr_t)w->down_q) & 31u)
+        return MOE_ERR_INVALID_ARG;  // TMA of packed E2M1 needs 32-byte aligned bases
+    if (d->router_mode == MOE_ROUTER_XWR && !w->w_router) return MOE_ERR_INVALID_ARG;
+    if (d->has_shared && (!w->sh_gate || !w->sh_up || !w->sh_down)) return MOE_ERR_INVALID_ARG;
+    if (d->router_mode == MOE_ROUTER_XWR || d->has_shared) return MOE_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;
+
+    moe_handle *h = (moe_handle *)calloc(1, sizeof(moe_handle));
+    if (!h) return MOE_ERR_INVALID_ARG;
+    h->desc = *d;
+    h->w = *w;
+    h->device = dev;
+    if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        free(h);
+        return MOE_ERR_CUDA;
+    }
+    {
+        const uint64_t D = d->d_model, F = d->d_ff, E = d->n_experts;
+        const CUtensorMapDataType fp4 = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
+        if (!make_map_2d(&h->map_gate, fp4, w->gate_q, D, E * F, D / 2, 128, 128) ||
+            !make_map_2d(&h->map_up, fp4, w->up_q, D, E * F, D / 2, 128, 128) ||
+            !make_map_2d(&h->map_down, fp4, w->down_q, F, E * D, F / 2, 128, 128)) {
+            free(h);
+            return MOE_ERR_CUDA;
+        }
+    }
+    if (cudaMalloc(&h->status, sizeof(int)) != cudaSuccess) {
+        free(h);
+        return MOE_ERR_CUDA;
+    }
+    if (cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess) {
+        cudaFree(h->status);
+        free(h);
+        return MOE_ERR_CUDA;
+    }
+    *out = h;
+    return MOE_OK;
+}
+
+MOE_API void moe_destroy(moe_handle *h) {
+    if (!h) return;
+    cudaFree(h->status);
+    free(h);
+}
+
+MOE_API size_t moe_workspace_bytes(const moe_handle *h, int32_t T, int32_t op) {
+    if (!h || T <= 0) return 0;
+    const moe_desc &d = h->desc;
+    switch (op) {
+        case MOE_OP_PLAN: return align_up(moe_plan_ws_bytes(T, d.n_experts), 256);
+        case MOE_OP_DECODE: return align_up(moe_decode_ws_bytes(T, d.d_model, d.d_ff, d.top_k), 256);
+        case MOE_OP_FORWARD:
+            return fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k).total;
+        default: return 0;
+    }
+}
+
+static bool plan_ok(const moe_plan_buf *p) {
+    return p && p->topk_idx && p->topk_w && p->counts && p->offsets && p->perm && p->inv &&
+           p->active;
+}
+
+MOE_API int moe_plan(moe_handle *h, int32_t T, const float *logits, const uint16_t *x,
+                     const moe_plan_buf *plan, void *ws, size_t ws_bytes, void *stream) {
+    if (!h || T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!plan_ok(plan)) return MOE_ERR_INVALID_ARG;
+    if (h->desc.router_mode == MOE_ROUTER_LOGITS && !logits) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)T * h->desc.top_k > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    size_t need = moe_workspace_bytes(h, T, MOE_OP_PLAN);
+    if (ws_bytes < need || (need && !ws)) return MOE_ERR_WORKSPACE;
+    (void)x;
+    cudaError_t err = moe_launch_plan(T, h->desc.n_experts, h->desc.top_k, logits, plan, ws,
+                                      h->status, (cudaStream_t)stream);
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+MOE_API int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
+                       uint16_t *out, void *ws, size_t ws_bytes, void *stream) {
+    if (!h || T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !out || !plan_ok(plan)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)T * h->desc.top_k > INT32_MAX / 2 || T > 65535) return MOE_ERR_UNSUPPORTED;
+    size_t need = moe_workspace_bytes(h, T, MOE_OP_DECODE);
+    if (ws_bytes < need || !ws || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+    const moe_desc &d = h->desc;
+    cudaError_t err = moe_launch_decode(T, d.d_model, d.d_ff, d.n_experts, d.top_k, x, plan, &h->w,
+                                        out, ws, h->status, (cudaStream_t)stream);
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
+                        uint16_t *out, void *ws, size_t ws_bytes, void *stream) {
+    if (!h || T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !out || !plan_ok(plan)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)T * h->desc.top_k > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    const moe_desc &d = h->desc;
+    const FwdLayout L = fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k);
+    if (ws_bytes < L.total || !ws || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    unsigned char *base = (unsigned char *)ws;
+    const int D = d.d_model, F = d.d_ff, E = d.n_experts, k = d.top_k, rows = T * k;
+    uint8_t *xq_hi = base + L.xq_hi, *xq_lo = base + L.xq_lo;
+    uint8_t *xs_hi = base + L.xs_hi, *xs_lo = base + L.xs_lo;
+    uint8_t *hq_hi = base + L.hq_hi, *hq_lo = base + L.hq_lo;
+    uint8_t *hs_hi = base + L.hs_hi, *hs_lo = base + L.hs_lo;
+    float *acc = (float *)(base + L.acc);
+    int32_t *prefix = (int32_t *)(base + L.prefix);
+
+    CUtensorMap mx_hi, mx_lo, mh_hi, mh_lo;
+    if (!make_map_2d(&mx_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq_hi, D, T, D, 128, 1) ||
+        !make_map_2d(&mx_lo, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq_lo, D, T, D, 128, 1) ||
+        !make_map_2d(&mh_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, hq_hi, F, rows, F, 128, 16) ||
+        !make_map_2d(&mh_lo, CU_TENSOR_MAP_DATA_TYPE_UINT8, hq_lo, F, rows, F, 128, 16))
+        return MOE_ERR_CUDA;
+
+    cudaError_t err = moe_launch_quant_x(T, D, x, xq_hi, xq_lo, xs_hi, xs_lo, st);
+    if (err == cudaSuccess)
+        err = moe_launch_schedule(E, MOE_GEMM_NTMAX, plan->offsets, plan->active, prefix,
+                                  h->status, st);
+    MoeGemmArgs a;
+    memset(&a, 0, sizeof(a));
+    a.E = E;
+    a.k = k;
+    a.n_rows = rows;
+    a.Dout = D;
+    a.offsets = plan->offsets;
+    a.perm = plan->perm;
+    a.active = plan->active;
+    a.tt_prefix = prefix;
+    a.topk_w = plan->topk_w;
+    a.status = h->status;
+    a.timeout_cycles = kTimeoutCycles;
+    if (err == cudaSuccess) {
+        MoeGemmArgs g1 = a;
+        g1.M = F;
+        g1.MT = F / 128;
+        g1.K = D;
+        g1.KC = D / 128;
+        g1.a_s = h->w.gate_s;
+        g1.a2_s = h->w.up_s;
+        g1.b_s_hi = xs_hi;
+        g1.b_s_lo = xs_lo;
+        g1.h_hi = hq_hi;
+        g1.h_lo = hq_lo;
+        g1.hs_hi = hs_hi;
+        g1.hs_lo = hs_lo;
+        err = moe_launch_gemm(MOE_GEMM_GATEUP, &h->map_gate, &h->map_up, &mx_hi, &mx_lo, &g1,
+                              h->num_sms, st);
+    }
+    if (err == cudaSuccess) err = cudaMemsetAsync(acc, 0, (size_t)T * D * sizeof(float), st);
+    if (err == cudaSuccess) {
+        MoeGemmArgs g2 = a;
+        g2.M = D;
+        g2.MT = D / 128;
+        g2.K = F;
+        g2.KC = F / 128;
+        g2.a_s = h->w.down_s;
+        g2.a2_s = nullptr;
+        g2.b_s_hi = hs_hi;
+        g2.b_s_lo = hs_lo;
+        g2.acc = acc;
+        err = moe_launch_gemm(MOE_GEMM_DOWN, &h->map_down, &h->map_down, &mh_hi, &mh_lo, &g2,
+                              h->num_sms, st);
+    }
+    if (err == cudaSuccess) err = moe_launch_finalize(T, D, acc, out, st);
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+MOE_API int moe_status(moe_handle *h, void *stream) {
+    if (!h) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (v != 0 && cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+    return v;
+}

@@ -1,0 +1,42 @@
+// Shared device helpers of the routed-expert FFN library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+#define MOE_MAX_TOPK 32
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_DMODEL 16384
+#define MOE_MAX_DFF 8192
+
+// Record the first device-side error; later errors keep the first one.
+__device__ __forceinline__ void moe_flag(int *status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+    return __uint_as_float(((uint32_t)b) << 16);
+}
+
+// fp32 -> bf16 bits, round to nearest even (NaN kept quiet).
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x40);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+// 2^(b - 127) for an E8M0 scale byte b (255 -> NaN).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+    if (b == 255u) return __uint_as_float(0x7FC00000u);
+    if (b == 0u) return __uint_as_float(0x00400000u);  // 2^-127 (fp32 subnormal)
+    return __uint_as_float(b << 23);
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}

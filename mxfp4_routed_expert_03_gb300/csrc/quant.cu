@@ -1,0 +1,143 @@
+// Small kernels around the grouped GEMMs: the activation split-quantiser
+// (bf16 -> two-term MXFP8), the per-expert token-tile schedule, and the final
+// fp32 -> bf16 cast of the combined output.
+#include "common.cuh"
+#include "kernels.h"
+#include "mx8.cuh"
+
+#define FULL_MASK 0xFFFFFFFFu
+
+// One thread per 32-element block of x: hi/lo E4M3 bytes and their E8M0 scales.
+__global__ void __launch_bounds__(256) moe_quant_x_kernel(int64_t n_blocks, int D,
+                                                          const uint16_t *__restrict__ x,
+                                                          uint8_t *__restrict__ q_hi,
+                                                          uint8_t *__restrict__ q_lo,
+                                                          uint8_t *__restrict__ s_hi,
+                                                          uint8_t *__restrict__ s_lo) {
+    int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (b >= n_blocks) return;
+    const uint4 *src = (const uint4 *)(x + b * 32);
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint4 u = src[i];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+            v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    int sh = mx8::scale_exp(amax);
+    float inv_h = mx8::exp2i(-sh), sc_h = mx8::exp2i(sh);
+    uint32_t hw[8];
+    float r[32];
+    float ramax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        uint32_t p = mx8::to_e4m3x2(v[2 * i] * inv_h, v[2 * i + 1] * inv_h);
+        float2 back = mx8::from_e4m3x2(p);
+        r[2 * i] = v[2 * i] - back.x * sc_h;
+        r[2 * i + 1] = v[2 * i + 1] - back.y * sc_h;
+        ramax = fmaxf(ramax, fmaxf(fabsf(r[2 * i]), fabsf(r[2 * i + 1])));
+        if (i % 2 == 0) hw[i / 2] = p;
+        else hw[i / 2] |= p << 16;
+    }
+    int sl = mx8::scale_exp(ramax);
+    float inv_l = mx8::exp2i(-sl);
+    uint32_t lw[8];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        uint32_t p = mx8::to_e4m3x2(r[2 * i] * inv_l, r[2 * i + 1] * inv_l);
+        if (i % 2 == 0) lw[i / 2] = p;
+        else lw[i / 2] |= p << 16;
+    }
+    uint4 *dh = (uint4 *)(q_hi + b * 32), *dl = (uint4 *)(q_lo + b * 32);
+    dh[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    dh[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+    dl[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    dl[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+    s_hi[b] = (uint8_t)(sh + 127);
+    s_lo[b] = (uint8_t)(sl + 127);
+}
+
+// tt_prefix[a] = token tiles of active experts before a; tt_prefix[n] = total.
+__global__ void __launch_bounds__(1024) moe_schedule_kernel(int E, int ntmax,
+                                                            const int32_t *__restrict__ offsets,
+                                                            const int32_t *__restrict__ active,
+                                                            int32_t *__restrict__ tt_prefix,
+                                                            int *status) {
+    __shared__ int s_tot[33];
+    int a = threadIdx.x, lane = a & 31, wid = a >> 5;
+    int n = active[0];
+    if (n < 0 || n > E) {
+        if (a == 0) { moe_flag(status, MOE_ERR_BAD_INDEX); tt_prefix[0] = 0; }
+        n = 0;
+    }
+    int ntt = 0;
+    if (a < n) {
+        int e = active[1 + a];
+        if (e >= 0 && e < E) {
+            int c = offsets[e + 1] - offsets[e];
+            ntt = c > 0 ? (c + ntmax - 1) / ntmax : 0;
+        } else {
+            moe_flag(status, MOE_ERR_BAD_INDEX);
+        }
+    }
+    int inc = ntt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int o = __shfl_up_sync(FULL_MASK, inc, off);
+        if (lane >= off) inc += o;
+    }
+    if (lane == 31) s_tot[wid] = inc;
+    __syncthreads();
+    if (wid == 0) {
+        int t = s_tot[lane], ti = t;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int o = __shfl_up_sync(FULL_MASK, ti, off);
+            if (lane >= off) ti += o;
+        }
+        s_tot[lane] = ti - t;
+        if (lane == 31) s_tot[32] = ti;
+    }
+    __syncthreads();
+    int excl = s_tot[wid] + inc - ntt;
+    if (a < n) tt_prefix[a] = excl;
+    if (a == 0) tt_prefix[n] = s_tot[32];
+}
+
+__global__ void __launch_bounds__(256) moe_finalize_kernel(int64_t n4, const float *__restrict__ acc,
+                                                           uint16_t *__restrict__ out) {
+    int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i >= n4) return;
+    float4 v = ((const float4 *)acc)[i];
+    uint2 o;
+    o.x = (uint32_t)f32_to_bf16_bits(v.x) | ((uint32_t)f32_to_bf16_bits(v.y) << 16);
+    o.y = (uint32_t)f32_to_bf16_bits(v.z) | ((uint32_t)f32_to_bf16_bits(v.w) << 16);
+    ((uint2 *)out)[i] = o;
+}
+
+cudaError_t moe_launch_quant_x(int T, int D, const uint16_t *x, uint8_t *q_hi, uint8_t *q_lo,
+                               uint8_t *s_hi, uint8_t *s_lo, cudaStream_t st) {
+    int64_t nb = (int64_t)T * D / 32;
+    moe_quant_x_kernel<<<(unsigned)((nb + 255) / 256), 256, 0, st>>>(nb, D, x, q_hi, q_lo, s_hi,
+                                                                       s_lo);
+    return cudaGetLastError();
+}
+
+cudaError_t moe_launch_schedule(int E, int ntmax, const int32_t *offsets, const int32_t *active,
+                                int32_t *tt_prefix, int *status, cudaStream_t st) {
+    moe_schedule_kernel<<<1, 1024, 0, st>>>(E, ntmax, offsets, active, tt_prefix, status);
+    return cudaGetLastError();
+}
+
+cudaError_t moe_launch_finalize(int T, int D, const float *acc, uint16_t *out, cudaStream_t st) {
+    int64_t n4 = (int64_t)T * D / 4;
+    moe_finalize_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(n4, acc, out);
+    return cudaGetLastError();
+}

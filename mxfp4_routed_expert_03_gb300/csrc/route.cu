@@ -1,0 +1,296 @@
+// Routing: per-token top-k with softmax weights (K1) and the per-expert route
+// plan (K2: histogram, exclusive scan, stable counting-sort scatter).
+//
+// Each token selects top_k of n_experts experts (MoonTail, intro; Moonshine
+// README, "How the engine works"). All rows selecting each expert are then
+// grouped and only the experts with rows are touched (Moonshine README,
+// "How the engine works", prefill paragraph; Moonshine GitHub README,
+// "Prefill"). Order: descending logit, ties to the lower expert index; the
+// weights are the softmax over the selected logits. The plan orders the flat
+// indices t*k+j by (expert, flat index), so it is unique and bit-exact.
+#include "common.cuh"
+#include "kernels.h"
+
+#define FULL_MASK 0xFFFFFFFFu
+
+namespace {
+
+// Warp-cooperative top-k of one token's logits. On return lane j < k holds
+// the j-th selection (expert index, logit). NaN logits count as -inf and set
+// *nan_seen. Lane l owns experts l, l+32, ... (coalesced loads).
+__device__ __forceinline__ void warp_topk(const float *row, int E, int k, int lane, int &my_e,
+                                          float &my_v, bool &nan_seen) {
+    float v[32];
+    uint32_t taken = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        int e = lane + 32 * i;
+        float t = -INFINITY;
+        if (e < E) {
+            t = row[e];
+            if (t != t) { nan_seen = true; t = -INFINITY; }
+        } else {
+            taken |= 1u << i;
+        }
+        v[i] = t;
+    }
+    my_e = -1;
+    my_v = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int be = -1;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            // Within a lane the expert index grows with i, so a strict '>'
+            // keeps the lowest index among equal logits (+0 == -0 here).
+            if (!((taken >> i) & 1u) && (be < 0 || v[i] > bv)) { bv = v[i]; be = lane + 32 * i; }
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            float ov = __shfl_xor_sync(FULL_MASK, bv, off);
+            int oe = __shfl_xor_sync(FULL_MASK, be, off);
+            bool better = oe >= 0 && (be < 0 || ov > bv || (ov == bv && oe < be));
+            if (better) { bv = ov; be = oe; }
+        }
+        if (be >= 0 && (be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == j) { my_e = be; my_v = bv; }
+    }
+}
+
+// Softmax over the k selected logits held by lanes 0..k-1.
+__device__ __forceinline__ float warp_select_weight(float my_v, int k, int lane) {
+    float vmax = __shfl_sync(FULL_MASK, my_v, 0);
+    float ex = (lane < k) ? expf(my_v - vmax) : 0.f;
+    float s = ex;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(FULL_MASK, s, off);
+    return ex / s;
+}
+
+// Exclusive block scan of one int per thread (blockDim.x == 1024).
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &total) {
+    int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int o = __shfl_up_sync(FULL_MASK, inc, off);
+        if (lane >= off) inc += o;
+    }
+    if (lane == 31) warp_tot[wid] = inc;
+    __syncthreads();
+    if (wid == 0) {
+        int t = warp_tot[lane];
+        int ti = t;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int o = __shfl_up_sync(FULL_MASK, ti, off);
+            if (lane >= off) ti += o;
+        }
+        warp_tot[lane] = ti - t;  // exclusive prefix of warp totals
+        if (lane == 31) warp_tot[32] = ti;
+    }
+    __syncthreads();
+    int r = warp_tot[wid] + inc - v;
+    total = warp_tot[32];
+    __syncthreads();
+    return r;
+}
+
+// Stable scatter of the flat entries [f0, f1) in flat order by one warp.
+// cnt[e] holds the next free position of expert e and is advanced.
+__device__ __forceinline__ void warp_stable_scatter(const int32_t *idx, int64_t f0, int64_t f1,
+                                                    int E, int *cnt, int32_t *perm, int32_t *inv,
+                                                    int *status) {
+    int lane = threadIdx.x & 31;
+    for (int64_t base = f0; base < f1; base += 32) {
+        int64_t f = base + lane;
+        bool valid = f < f1;
+        int e = valid ? idx[f] : -1;
+        if (valid && (e < 0 || e >= E)) { moe_flag(status, MOE_ERR_BAD_INDEX); e = -1; }
+        uint32_t m = __match_any_sync(FULL_MASK, e);
+        if (e >= 0) {
+            int rank = __popc(m & lanemask_lt());
+            int pos = cnt[e] + rank;
+            perm[pos] = (int32_t)f;
+            inv[f] = pos;
+        }
+        __syncwarp();
+        if (e >= 0 && lane == 31 - __clz(m)) cnt[e] += __popc(m);
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Small batches: one CTA does top-k, histogram, scan and the stable scatter.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) moe_plan_small_kernel(
+    int T, int E, int k, const float *__restrict__ logits, int32_t *topk_idx, float *topk_w,
+    int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *active, int *status) {
+    __shared__ int s_cnt[MOE_MAX_EXPERTS];
+    __shared__ int s_tot[33];
+    __shared__ int s_nan;
+    int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    s_cnt[tid] = 0;
+    if (tid == 0) s_nan = 0;
+    __syncthreads();
+    for (int t = wid; t < T; t += 32) {
+        int my_e;
+        float my_v;
+        bool nan_seen = false;
+        warp_topk(logits + (int64_t)t * E, E, k, lane, my_e, my_v, nan_seen);
+        float w = warp_select_weight(my_v, k, lane);
+        if (lane < k) {
+            topk_idx[(int64_t)t * k + lane] = my_e;
+            topk_w[(int64_t)t * k + lane] = w;
+            atomicAdd(&s_cnt[my_e], 1);
+        }
+        if (__any_sync(FULL_MASK, nan_seen) && lane == 0) s_nan = 1;
+    }
+    __syncthreads();
+    if (tid == 0 && s_nan) moe_flag(status, MOE_ERR_NAN_LOGIT);
+    int c = tid < E ? s_cnt[tid] : 0;
+    int total;
+    int off = block_exclusive_scan(c, s_tot, total);
+    int a = block_exclusive_scan(c > 0 ? 1 : 0, s_tot, total);
+    if (tid < E) {
+        counts[tid] = c;
+        offsets[tid] = off;
+        if (c > 0) active[1 + a] = tid;
+    }
+    if (tid == 0) {
+        offsets[E] = T * k;
+        active[0] = total;
+    }
+    __syncthreads();
+    if (tid < E) s_cnt[tid] = off;
+    __syncthreads();
+    if (wid == 0) warp_stable_scatter(topk_idx, 0, (int64_t)T * k, E, s_cnt, perm, inv, status);
+}
+
+// ---------------------------------------------------------------------------
+// Large batches: four kernels.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) moe_topk_kernel(int T, int E, int k,
+                                                       const float *__restrict__ logits,
+                                                       int32_t *topk_idx, float *topk_w,
+                                                       int *status) {
+    int lane = threadIdx.x & 31;
+    int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int my_e;
+    float my_v;
+    bool nan_seen = false;
+    warp_topk(logits + (int64_t)t * E, E, k, lane, my_e, my_v, nan_seen);
+    float w = warp_select_weight(my_v, k, lane);
+    if (lane < k) {
+        topk_idx[(int64_t)t * k + lane] = my_e;
+        topk_w[(int64_t)t * k + lane] = w;
+    }
+    if (__any_sync(FULL_MASK, nan_seen) && lane == 0) moe_flag(status, MOE_ERR_NAN_LOGIT);
+}
+
+// chunk_counts[c][e]: rows of expert e among tokens [c*CH, (c+1)*CH).
+__global__ void __launch_bounds__(256) moe_plan_count_kernel(int T, int E, int k, int CH,
+                                                             const int32_t *__restrict__ idx,
+                                                             int32_t *chunk_counts, int *status) {
+    extern __shared__ int s_hist[];  // 8 warps x E
+    int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int c = blockIdx.x * 8 + wid;
+    int nchunks = (T + CH - 1) / CH;
+    int *h = s_hist + wid * E;
+    for (int e = lane; e < E; e += 32) h[e] = 0;
+    __syncwarp();
+    if (c < nchunks) {
+        int64_t f0 = (int64_t)c * CH * k;
+        int64_t f1 = min((int64_t)(c + 1) * CH, (int64_t)T) * k;
+        for (int64_t f = f0 + lane; f < f1; f += 32) {
+            int e = idx[f];
+            if (e >= 0 && e < E) atomicAdd(&h[e], 1);
+            else moe_flag(status, MOE_ERR_BAD_INDEX);
+        }
+        __syncwarp();
+        for (int e = lane; e < E; e += 32) chunk_counts[(int64_t)c * E + e] = h[e];
+    }
+}
+
+// Column scan of chunk_counts (in place -> chunk bases), counts, offsets, active.
+__global__ void __launch_bounds__(1024) moe_plan_scan_kernel(int T, int E, int k, int nchunks,
+                                                             int32_t *chunk_counts,
+                                                             int32_t *counts, int32_t *offsets,
+                                                             int32_t *active) {
+    __shared__ int s_tot[33];
+    int e = threadIdx.x;
+    int run = 0;
+    if (e < E) {
+        for (int c = 0; c < nchunks; ++c) {
+            int v = chunk_counts[(int64_t)c * E + e];
+            chunk_counts[(int64_t)c * E + e] = run;
+            run += v;
+        }
+    }
+    int total;
+    int off = block_exclusive_scan(run, s_tot, total);
+    int a = block_exclusive_scan(run > 0 ? 1 : 0, s_tot, total);
+    if (e < E) {
+        counts[e] = run;
+        offsets[e] = off;
+        if (run > 0) active[1 + a] = e;
+    }
+    if (e == 0) {
+        offsets[E] = T * k;
+        active[0] = total;
+    }
+}
+
+__global__ void __launch_bounds__(256) moe_plan_scatter_kernel(int T, int E, int k, int CH,
+                                                               const int32_t *__restrict__ idx,
+                                                               const int32_t *chunk_base,
+                                                               const int32_t *offsets,
+                                                               int32_t *perm, int32_t *inv,
+                                                               int *status) {
+    extern __shared__ int s_next[];  // 8 warps x E
+    int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int c = blockIdx.x * 8 + wid;
+    int nchunks = (T + CH - 1) / CH;
+    if (c >= nchunks) return;
+    int *nx = s_next + wid * E;
+    for (int e = lane; e < E; e += 32) nx[e] = offsets[e] + chunk_base[(int64_t)c * E + e];
+    __syncwarp();
+    int64_t f0 = (int64_t)c * CH * k;
+    int64_t f1 = min((int64_t)(c + 1) * CH, (int64_t)T) * k;
+    warp_stable_scatter(idx, f0, f1, E, nx, perm, inv, status);
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers.
+// ---------------------------------------------------------------------------
+size_t moe_plan_ws_bytes(int T, int E) {
+    if (T <= 0 || moe_plan_is_small(T)) return 0;
+    int nchunks = (T + MOE_PLAN_CHUNK - 1) / MOE_PLAN_CHUNK;
+    return (size_t)nchunks * E * sizeof(int32_t);
+}
+
+cudaError_t moe_launch_plan(int T, int E, int k, const float *logits, const moe_plan_buf *p,
+                            void *ws, int *status, cudaStream_t st) {
+    if (moe_plan_is_small(T)) {
+        moe_plan_small_kernel<<<1, 1024, 0, st>>>(T, E, k, logits, p->topk_idx, p->topk_w,
+                                                  p->counts, p->offsets, p->perm, p->inv,
+                                                  p->active, status);
+        return cudaGetLastError();
+    }
+    int CH = MOE_PLAN_CHUNK;
+    int nchunks = (T + CH - 1) / CH;
+    int32_t *chunk = (int32_t *)ws;
+    moe_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(T, E, k, logits, p->topk_idx, p->topk_w, status);
+    size_t sm = (size_t)8 * E * sizeof(int);
+    moe_plan_count_kernel<<<(nchunks + 7) / 8, 256, sm, st>>>(T, E, k, CH, p->topk_idx, chunk,
+                                                              status);
+    moe_plan_scan_kernel<<<1, 1024, 0, st>>>(T, E, k, nchunks, chunk, p->counts, p->offsets,
+                                             p->active);
+    moe_plan_scatter_kernel<<<(nchunks + 7) / 8, 256, sm, st>>>(T, E, k, CH, p->topk_idx, chunk,
+                                                                p->offsets, p->perm, p->inv,
+                                                                status);
+    return cudaGetLastError();
+}

@@ -1,0 +1,94 @@
+"""Buffer bookkeeping around the C ABI for one routed layer.
+
+Holds torch-owned device buffers (weights, plan, workspace) and calls the C
+entry points; it computes nothing itself.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (MOE_OP_DECODE, MOE_OP_FORWARD, MOE_OP_PLAN, check, moe_create, moe_decode,
+               moe_desc, moe_destroy, moe_forward, moe_plan, moe_plan_buf, moe_status,
+               moe_weights, moe_workspace_bytes)
+
+WEIGHT_NAMES = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
+
+
+def alloc_weights(E: int, D: int, F: int, device="cuda") -> dict:
+    """Uninitialised uint8 weight tensors in the library's layout."""
+    return {
+        "gate_q": torch.empty((E, F, D // 2), dtype=torch.uint8, device=device),
+        "gate_s": torch.empty((E, F, D // 32), dtype=torch.uint8, device=device),
+        "up_q": torch.empty((E, F, D // 2), dtype=torch.uint8, device=device),
+        "up_s": torch.empty((E, F, D // 32), dtype=torch.uint8, device=device),
+        "down_q": torch.empty((E, D, F // 2), dtype=torch.uint8, device=device),
+        "down_s": torch.empty((E, D, F // 32), dtype=torch.uint8, device=device),
+    }
+
+
+class Plan:
+    def __init__(self, T: int, E: int, k: int, device="cuda"):
+        dev = device
+        self.T, self.E, self.k = T, E, k
+        n = max(T * k, 1)
+        self.topk_idx = torch.empty((max(T, 1), k), dtype=torch.int32, device=dev)
+        self.topk_w = torch.empty((max(T, 1), k), dtype=torch.float32, device=dev)
+        self.counts = torch.empty(E, dtype=torch.int32, device=dev)
+        self.offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        self.perm = torch.empty(n, dtype=torch.int32, device=dev)
+        self.inv = torch.empty(n, dtype=torch.int32, device=dev)
+        self.active = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        self.buf = moe_plan_buf(*[t.data_ptr() for t in (self.topk_idx, self.topk_w, self.counts,
+                                                         self.offsets, self.perm, self.inv,
+                                                         self.active)])
+
+
+class Layer:
+    """One routed layer: weights (device tensors) + the library handle."""
+
+    def __init__(self, D: int, F: int, E: int, k: int, weights: dict, router_mode: int = 0,
+                 w_router=None, shared=None):
+        self.D, self.F, self.E, self.k = D, F, E, k
+        self.weights = weights
+        self.w_router = w_router
+        self.shared = shared
+        ptr = lambda t: None if t is None else t.data_ptr()
+        sh = shared or {}
+        self.desc = moe_desc(D, F, E, k, router_mode, 1 if shared else 0)
+        self.wdesc = moe_weights(*[weights[n].data_ptr() for n in WEIGHT_NAMES], ptr(w_router),
+                                 ptr(sh.get("sh_gate")), ptr(sh.get("sh_up")),
+                                 ptr(sh.get("sh_down")))
+        self.h = moe_create(self.desc, self.wdesc)
+        self._ws = None
+
+    def close(self):
+        if self.h:
+            moe_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def workspace(self, T: int, op: int) -> tuple:
+        n = moe_workspace_bytes(self.h, T, op)
+        if self._ws is None or self._ws.numel() < n:
+            self._ws = torch.empty(max(n, 256), dtype=torch.uint8, device="cuda")
+        return self._ws, n
+
+    def plan(self, T, logits, x, plan: Plan, stream=None) -> int:
+        ws, n = self.workspace(T, MOE_OP_PLAN)
+        return moe_plan(self.h, T, logits, x, plan.buf, ws, ws.numel(), stream)
+
+    def decode(self, T, x, plan: Plan, out, stream=None) -> int:
+        ws, n = self.workspace(T, MOE_OP_DECODE)
+        return moe_decode(self.h, T, x, plan.buf, out, ws, ws.numel(), stream)
+
+    def forward(self, T, x, plan: Plan, out, stream=None) -> int:
+        ws, n = self.workspace(T, MOE_OP_FORWARD)
+        return moe_forward(self.h, T, x, plan.buf, out, ws, ws.numel(), stream)
+
+    def status(self, stream=None) -> int:
+        return moe_status(self.h, stream)

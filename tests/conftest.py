@@ -26,3 +26,15 @@ def _built_cpu_side():
     import synth
     oracle.build()
     synth.build(device=False)
+
+
+@pytest.fixture(scope="session")
+def k3_layer():
+    """The full 896-expert K3-shaped layer (15.7 GB), generated on the GPU once."""
+    import torch
+    import synth
+    from harness import device_layer_weights
+    wts = device_layer_weights(synth.WORKLOADS["decode1"])
+    yield wts
+    del wts
+    torch.cuda.empty_cache()

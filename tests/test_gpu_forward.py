@@ -1,0 +1,94 @@
+"""GPU layer-major path (moe_plan + moe_forward, tcgen05 grouped GEMMs) vs the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from harness import assert_close, bf16_dev_to_f64, errors, host_layer_weights, to_dev_bf16
+from oracle.run import reference
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, weights, x_np, lg_np, path="forward"):
+    from mxfp4_routed_expert_03_gb300 import check
+    from mxfp4_routed_expert_03_gb300.layer import Layer, Plan
+    T = x_np.shape[0]
+    layer = Layer(w.D, w.F, w.E, w.k, weights)
+    plan = Plan(T, w.E, w.k)
+    x = to_dev_bf16(x_np)
+    check(layer.plan(T, torch.from_numpy(lg_np).cuda(), None, plan), "plan")
+    out = torch.empty((T, w.D), dtype=torch.int16, device="cuda")
+    fn = layer.forward if path == "forward" else layer.decode
+    check(fn(T, x, plan, out), path)
+    st = layer.status()
+    layer.close()
+    assert st == 0, st
+    return bf16_dev_to_f64(out), plan
+
+
+@pytest.fixture(scope="module")
+def tiny_weights():
+    return host_layer_weights(synth.WORKLOADS["tiny"])
+
+
+def test_tiny_layer_all_tokens(tiny_weights):
+    w = synth.WORKLOADS["tiny"]
+    x, lg = synth.make_x(w), synth.make_logits(w)
+    got, _ = _run(w, tiny_weights, x, lg)
+    e = assert_close(got, reference(w, x, lg)["out"])
+    print("tiny forward", e)
+
+
+@pytest.mark.parametrize("T", [1, 3, 17, 130, 1000])
+def test_tiny_shapes_ragged_and_multi_tile_segments(tiny_weights, T):
+    w = synth.WORKLOADS["tiny"]
+    x, lg = synth.make_x(w, 11, T=T), synth.make_logits(w, 11, T=T)
+    tok = np.arange(T) if T <= 130 else np.random.default_rng(T).choice(T, 48, replace=False)
+    got, plan = _run(w, tiny_weights, x, lg)
+    ref = reference(w, x, lg, tokens=tok)
+    if T == 1000:
+        assert plan.counts.cpu().numpy().max() > 112   # several token tiles per expert
+    e = assert_close(got[tok], ref["out"])
+    print("tiny forward T=%d" % T, e)
+
+
+def test_tiny_one_expert_holds_all_rows(tiny_weights):
+    w = synth.WORKLOADS["tiny"]
+    T = 500
+    x, lg = synth.make_x(w, 5, T=T), synth.make_logits(w, 5, T=T)
+    lg[:, 9] = 60.0
+    got, plan = _run(w, tiny_weights, x, lg)
+    assert plan.counts.cpu().numpy()[9] == T
+    tok = np.arange(0, T, 11)
+    assert_close(got[tok], reference(w, x, lg, tokens=tok)["out"])
+
+
+@pytest.mark.parametrize("name,n_check", [("prefill4k", 16), ("skewed8k", 16)])
+def test_k3_prefill_sampled_tokens(k3_layer, name, n_check):
+    w = synth.WORKLOADS[name]
+    x, lg = synth.make_x(w), synth.make_logits(w)
+    got, plan = _run(w, k3_layer, x, lg)
+    tok = np.random.default_rng(1).choice(w.T, n_check, replace=False)
+    ref = reference(w, x, lg, tokens=tok)
+    np.testing.assert_array_equal(plan.perm.cpu().numpy(), ref["plan"]["perm"])
+    e = assert_close(got[tok], ref["out"])
+    assert np.all(np.isfinite(got))
+    print(name, e)
+
+
+@pytest.mark.parametrize("T", [1, 4, 8, 16])
+def test_crossover_decode_and_forward_agree(k3_layer, T):
+    w = synth.WORKLOADS["decode16"]
+    x, lg = synth.make_x(w, 20 + T, T=T), synth.make_logits(w, 20 + T, T=T)
+    got_f, plan_f = _run(w, k3_layer, x, lg, "forward")
+    got_d, plan_d = _run(w, k3_layer, x, lg, "decode")
+    for name in ("topk_idx", "counts", "offsets", "perm", "inv"):
+        np.testing.assert_array_equal(getattr(plan_f, name).cpu().numpy(),
+                                      getattr(plan_d, name).cpu().numpy())
+    af, ad = plan_f.active.cpu().numpy(), plan_d.active.cpu().numpy()
+    np.testing.assert_array_equal(af[: 1 + af[0]], ad[: 1 + ad[0]])
+    ref = reference(w, x, lg)["out"]
+    ef = assert_close(got_f, ref)
+    ed = assert_close(got_d, ref)
+    print("crossover T=%d forward" % T, ef, "decode", ed)
