@@ -1,0 +1,404 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 routed-expert FFN library: prints one JSON line.
+
+Default workload: one K3-shaped routed layer (d_model 7168, d_ff 1536, 896
+experts, top-16, MXFP4 weights resident in HBM), decode batches of T = 1, 4
+and 16 tokens; one step = moe_plan + moe_decode for each of the three
+batches (21 tokens). `--workload prefill4k|skewed8k` times moe_plan +
+moe_forward on one prefill batch instead.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: CUDA events on the library's stream, barrier + synchronize on both
+sides, max over ranks. Each step's weight working set (>= 280 MB) exceeds L2
+and the router logits rotate through pre-generated sets, so the selected
+experts change every step. N > 1 runs independent replicas (the layer does
+not shard here): value = tokens of all ranks / slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s + % roofline (decode HBM GB/s; prefill FP4 TFLOP/s), 1xGB300"
+D_MODEL, D_FF, N_EXPERTS, TOP_K = 7168, 1536, 896, 16
+EXPERT_BYTES = 17547264            # one expert's three MXFP4 matrices (codes + scales)
+GATEUP_BYTES = 2 * (D_FF * D_MODEL // 2 + D_FF * D_MODEL // 32)
+DOWN_BYTES = D_MODEL * D_FF // 2 + D_MODEL * D_FF // 32
+N_SETS = 8
+
+BENCH_WORKLOADS = {
+    "decode": {"Ts": [1, 4, 16], "path": "decode",
+               "desc": "K3 routed layer decode, T=1,4,16 (d_model 7168, d_ff 1536, 896 experts, top-16, MXFP4)"},
+    "prefill4k": {"Ts": [4096], "path": "forward",
+                  "desc": "K3 routed layer prefill, T=4096, uniform routing"},
+    "skewed8k": {"Ts": [8192], "path": "forward",
+                 "desc": "K3 routed layer prefill, T=8192, Zipf(1.1)-skewed routing"},
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 1000 for decode, 60 for prefill)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default="decode")
+    ap.add_argument("--path", choices=["decode", "forward"], default=None,
+                    help="entry point for the batches (default: decode for decode, forward for prefill)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="wall-time budget of the CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (the reference arm and the cpu_baseline object)
+# ---------------------------------------------------------------------------
+def oracle_tokens_per_s(workload_name: str, budget_s: float):
+    """Time the CPU oracle, as it stands, one token at a time until the budget
+    is used (at least one token). Returns (tokens/s, tokens, seconds, threads)."""
+    import numpy as np
+    import synth
+    import oracle
+    from oracle.run import reference
+    oracle.build()
+    wl = BENCH_WORKLOADS[workload_name]
+    base = synth.WORKLOADS["decode1"] if workload_name == "decode" else synth.WORKLOADS[workload_name]
+    done, t0 = 0, time.perf_counter()
+    it = 0
+    while True:
+        T = wl["Ts"][it % len(wl["Ts"])]
+        w = synth.Workload(base.name, T=T, D=base.D, F=base.F, E=base.E, k=base.k, seed=base.seed,
+                           zipf_s=base.zipf_s)
+        x, lg = synth.make_x(w, it % N_SETS), synth.make_logits(w, it % N_SETS)
+        reference(w, x, lg, tokens=[it % T])
+        done += 1
+        it += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return done / el, done, el, threads
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    per_step = []
+    total_tok = 0
+    budget = 90.0 / max(args.steps + args.warmup, 1)   # at least one token per step
+    for i in range(args.warmup + args.steps):
+        tps, tok, el, threads = oracle_tokens_per_s(args.workload, budget)
+        if i >= args.warmup:
+            per_step.append(el)
+            total_tok += tok
+    el = sum(per_step)
+    value = total_tok / el
+    wl = BENCH_WORKLOADS[args.workload]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl["desc"], "sample": "one token per oracle call, full routing of its batch"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{total_tok} tokens of the {args.workload} workload, one at a time"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not inside:
+            inside = [p for (_, p) in self.samples]
+            window = "run"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        smax = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def kernel_traffic(name: str, source: str):
+    """dram bytes per launch of `name` from the committed ncu summary, or None
+    when the summary was taken on a different version of the kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "mxfp4_routed_expert_03_gb300", "csrc", source)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 4 and parts[0] == name and parts[1] == sha:
+            return float(parts[3])
+    return None
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import synth
+    from mxfp4_routed_expert_03_gb300 import (MOE_PROF_DECODE_GATEUP, MOE_PROF_FORWARD_GEMM1,
+                                              MOE_PROF_NONE, check, moe_profile_kernel)
+    from mxfp4_routed_expert_03_gb300.layer import Layer, Plan, alloc_weights
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = BENCH_WORKLOADS[args.workload]
+    path = args.path or wl["path"]
+    base = synth.WORKLOADS["decode1"] if args.workload == "decode" else synth.WORKLOADS[args.workload]
+
+    # weights: the full layer, generated in HBM by the device half of the generator
+    weights = alloc_weights(N_EXPERTS, D_MODEL, D_FF)
+    synth.dev_fill_layer(base.seed, N_EXPERTS, D_MODEL, D_FF,
+                         {k: v.data_ptr() for k, v in weights.items()},
+                         torch.cuda.current_stream().cuda_stream)
+    layer = Layer(D_MODEL, D_FF, N_EXPERTS, TOP_K, weights)
+    if path == "forward":
+        layer.prepare()
+    stream = torch.cuda.current_stream()
+
+    # inputs: N_SETS seeded (x, logits) sets per batch size, resident in HBM
+    batches = []
+    for T in wl["Ts"]:
+        w = synth.Workload(base.name, T=T, D=D_MODEL, F=D_FF, E=N_EXPERTS, k=TOP_K,
+                           seed=base.seed, zipf_s=base.zipf_s)
+        xs_h = [synth.make_x(w, rank * 97 + i) for i in range(N_SETS)]
+        ls_h = [synth.make_logits(w, rank * 97 + i) for i in range(N_SETS)]
+        xs = [torch.from_numpy(a.view(np.int16)).to(dev) for a in xs_h]
+        ls = [torch.from_numpy(a).to(dev) for a in ls_h]
+        pin_x = [torch.from_numpy(a.view(np.int16)).pin_memory() for a in xs_h]
+        pin_l = [torch.from_numpy(a).pin_memory() for a in ls_h]
+        batches.append({"T": T, "x": xs, "l": ls, "px": pin_x, "pl": pin_l,
+                        "plan": Plan(T, N_EXPERTS, TOP_K),
+                        "out": torch.empty((T, D_MODEL), dtype=torch.int16, device=dev),
+                        "dx": torch.empty((T, D_MODEL), dtype=torch.int16, device=dev),
+                        "dl": torch.empty((T, N_EXPERTS), dtype=torch.float32, device=dev),
+                        "hout": torch.empty((T, D_MODEL), dtype=torch.int16).pin_memory()})
+    for b in batches:  # size the workspace once for the largest call
+        layer.workspace(b["T"], 2 if path == "decode" else 1)
+    run = layer.decode if path == "decode" else layer.forward
+    prof_kind = MOE_PROF_DECODE_GATEUP if path == "decode" else MOE_PROF_FORWARD_GEMM1
+
+    def step(i, events=None, e2e=False):
+        for bi, b in enumerate(batches):
+            s = i % N_SETS
+            if events is not None:
+                ev0, ev1 = events[bi]
+                check(moe_profile_kernel(layer.h, prof_kind, ev0, ev1), "profile")
+            if e2e:
+                b["dx"].copy_(b["px"][s], non_blocking=True)
+                b["dl"].copy_(b["pl"][s], non_blocking=True)
+                x, lg = b["dx"], b["dl"]
+            else:
+                x, lg = b["x"][s], b["l"][s]
+            check(layer.plan(b["T"], lg, None, b["plan"], stream), "moe_plan")
+            check(run(b["T"], x, b["plan"], b["out"], stream), "moe_" + path)
+            if e2e:
+                b["hout"].copy_(b["out"], non_blocking=True)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(gpu_id)
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    # per-launch events of the dominant kernel over the timed region
+    n_b = len(batches)
+    kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(n_b)] for _ in range(args.steps)]
+    for row in kev:
+        for a, b in row:
+            a.record()
+            b.record()
+    torch.cuda.synchronize()
+    t_start = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        step(args.warmup + i, events=kev[i])
+    e1.record()
+    barrier()
+    t_end = time.time()
+    check(moe_profile_kernel(layer.h, MOE_PROF_NONE), "profile")
+    elapsed_ms = e0.elapsed_time(e1)
+    kern_ms = [[a.elapsed_time(b) for (a, b) in row] for row in kev]
+    check(layer.status(), "device status")
+
+    # end to end through the same calls with host buffers (copies inside the region)
+    for i in range(args.warmup):
+        step(i, e2e=True)
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record()
+    for i in range(args.steps):
+        step(args.warmup + i, e2e=True)
+    f1.record()
+    barrier()
+    e2e_ms = f0.elapsed_time(f1)
+    sampler.stop()
+    clocks = sampler.summary(t_start, t_end)
+
+    times = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    elapsed_ms, e2e_ms = times.tolist()
+    tokens_step = sum(wl["Ts"])
+    value = world * tokens_step * args.steps / (elapsed_ms * 1e-3)
+    e2e_value = world * tokens_step * args.steps / (e2e_ms * 1e-3)
+
+    # roofline of the dominant kernel (algorithmic bytes or flops per launch)
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    act = [int(b["plan"].active[0].item()) for b in batches]
+    tot_k_ms = float(np.sum(kern_ms))
+    n_launch = args.steps * n_b
+    if path == "decode":
+        # gate/up kernel: active experts' gate+up codes and scales, f16 x rows read,
+        # f16 h and its exponents written. Active counts vary per step; the
+        # expected count is taken from the last step's plans.
+        per_launch = [a * GATEUP_BYTES + T * D_MODEL * 2 + T * TOP_K * (D_FF * 2 + D_FF // 32)
+                      for a, T in zip(act, wl["Ts"])]
+        achieved = sum(per_launch) / len(per_launch) / (tot_k_ms / n_launch * 1e-3) / 1e9
+        peak = peaks.get("hbm_gbs", 6800.0)
+        roof = {"bound": "hbm", "kernel": "moe_decode_gateup_kernel", "achieved": achieved,
+                "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
+                "bytes_per_launch": sum(per_launch) / len(per_launch),
+                "traffic": kernel_traffic("moe_decode_gateup_kernel", "decode.cu")}
+    else:
+        flops = [2.0 * T * TOP_K * 2 * D_MODEL * D_FF for T in wl["Ts"]]
+        achieved = sum(flops) / len(flops) / (tot_k_ms / n_launch * 1e-3) / 1e12
+        # kind::mxf8f6f4 runs at the FP8 tensor rate: measured bf16 x (4.5 / 2.25 nominal)
+        peak = 2.0 * peaks.get("bf16_tflops", 1900.0)
+        roof = {"bound": "tensor", "kernel": "moe_grouped_gemm_kernel<gate/up>", "achieved": achieved,
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "frac_of_fp4_peak": achieved / (6.0 * peaks.get("bf16_tflops", 1900.0)),
+                "peak_source": ("measured bf16 x 2 (fp8 rate); the two-term activation split "
+                                "issues 2 MMAs per algorithmic one, so frac <= 0.5")
+                if "bf16_tflops" in peaks else "fallback",
+                "traffic": kernel_traffic("moe_grouped_gemm_kernel<0>", "grouped_gemm.cu")}
+
+    launches_per_call = 1 if max(wl["Ts"]) <= 64 else 4
+    launches_per_call += 4 if path == "decode" else 6
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "mxfp4 x f16 -> f32" if path == "decode" else "mxfp4 x 2-term e4m3 -> f32",
+        "data": "synthetic (seeded Philox weights, N(0,1) activations and logits)",
+        "config": {"workload": wl["desc"], "path": "moe_plan + moe_" + path,
+                   "tokens_per_step": tokens_step, "active_experts_last_step": act,
+                   "l2": "inputs larger than L2 (>=280 MB of expert weights per batch, "
+                         "8 rotating logit sets)", "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": "tokens/s",
+                "h2d_bytes_per_step": sum(T * D_MODEL * 2 + T * N_EXPERTS * 4 for T in wl["Ts"]),
+                "d2h_bytes_per_step": sum(T * D_MODEL * 2 for T in wl["Ts"])},
+        "gpu_launches": launches_per_call * len(wl["Ts"]) * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, tok, el, threads = oracle_tokens_per_s(args.workload, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"{tok} tokens of the {args.workload} workload "
+                                          f"in {el:.1f} s (full routing of each batch, expert FFN "
+                                          "of the sampled token, fp64)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    layer.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.steps is None:
+        args.steps = 1000 if args.workload == "decode" else 60
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -22,7 +22,8 @@
  *    size queries, which are host-only.
  *  - No call allocates or frees device memory, except moe_create (one 4-byte
  *    device status word) and moe_destroy (frees it). Scratch memory is the
- *    caller's `ws` buffer, sized by moe_workspace_bytes.
+ *    caller's `ws` buffer, sized by moe_workspace_bytes; the prepared weight
+ *    scales of moe_prepare live in a caller buffer too.
  *  - The caller owns every buffer; the handle keeps the weight pointers it was
  *    given (it does not copy weights), so they must outlive the handle.
  *  - Return value: MOE_OK (0) or a negative MOE_ERR_* code. Argument errors are
@@ -64,7 +65,8 @@ enum moe_status_code {
     MOE_ERR_CUDA = -4,            /* a CUDA runtime call or launch failed */
     MOE_ERR_DEVICE_TIMEOUT = -5,  /* a device-side wait hit its iteration limit */
     MOE_ERR_NAN_LOGIT = -6,       /* a router logit was NaN (treated as -inf) */
-    MOE_ERR_BAD_INDEX = -7        /* out-of-range expert / row index in a plan */
+    MOE_ERR_BAD_INDEX = -7,       /* out-of-range expert / row index in a plan */
+    MOE_ERR_NOT_PREPARED = -8     /* moe_forward before moe_prepare */
 };
 
 enum moe_router_mode {
@@ -76,6 +78,15 @@ enum moe_op {
     MOE_OP_PLAN = 0,
     MOE_OP_FORWARD = 1,
     MOE_OP_DECODE = 2
+};
+
+/* Kernels moe_profile_kernel can bracket with events. */
+enum moe_prof_kernel {
+    MOE_PROF_NONE = 0,
+    MOE_PROF_DECODE_GATEUP = 1,   /* moe_decode: gate/up + SwiGLU streaming kernel */
+    MOE_PROF_DECODE_DOWN = 2,     /* moe_decode: down-projection streaming kernel */
+    MOE_PROF_FORWARD_GEMM1 = 3,   /* moe_forward: grouped gate/up GEMM */
+    MOE_PROF_FORWARD_GEMM2 = 4    /* moe_forward: grouped down GEMM + weighted scatter */
 };
 
 /* Layer shape. Supported envelope: d_model and d_ff multiples of 128,
@@ -134,6 +145,21 @@ void moe_destroy(moe_handle *h);
  * d_ff=1536. Returns -1 if either size is not a positive multiple of 32. */
 int64_t moe_expert_bytes(int32_t d_model, int32_t d_ff);
 
+/* Host. Bytes of the buffer moe_prepare fills: the three weight-scale arrays
+ * (3 * n_experts * d_model * d_ff / 32 bytes, 924 MB for the 896-expert K3 layer). */
+size_t moe_prepared_bytes(const moe_handle *h);
+
+/* One-time weight-layout preparation for moe_forward (asynchronous on
+ * `stream`). Re-lays the E8M0 weight scales into the order the tensor cores
+ * consume them: for each (expert, 128-row tile, 128-wide K chunk) one
+ * contiguous 512-byte block, row m of the tile and 32-wide K block c at byte
+ * (m % 32) * 16 + (m / 32) * 4 + c. `buf` is caller-owned device memory of at
+ * least moe_prepared_bytes(h) bytes, 256-byte aligned; the handle keeps the
+ * pointer, so it must outlive the handle, and the weight scales must not
+ * change afterwards without calling moe_prepare again. moe_decode does not
+ * need it; moe_forward returns MOE_ERR_NOT_PREPARED without it. */
+int moe_prepare(moe_handle *h, void *buf, size_t bytes, void *stream);
+
 /* Host. Scratch bytes `op` (enum moe_op) needs for T tokens; 0 for T == 0. */
 size_t moe_workspace_bytes(const moe_handle *h, int32_t T, int32_t op);
 
@@ -147,7 +173,8 @@ int moe_plan(moe_handle *h, int32_t T, const float *logits, const uint16_t *x,
 /* Layer-major expert FFN for a planned batch (prefill): grouped block-scaled
  * MXFP4 GEMMs on tcgen05 tensor cores (gate/up with SwiGLU, then down with
  * the weighted scatter), finalised to bf16 out [T][d_model].
- * ws: >= moe_workspace_bytes(h, T, MOE_OP_FORWARD). */
+ * Requires moe_prepare. ws: >= moe_workspace_bytes(h, T, MOE_OP_FORWARD),
+ * 256-byte aligned. */
 int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
                 uint16_t *out, void *ws, size_t ws_bytes, void *stream);
 
@@ -157,6 +184,13 @@ int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf 
  * ws: >= moe_workspace_bytes(h, T, MOE_OP_DECODE). */
 int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
                uint16_t *out, void *ws, size_t ws_bytes, void *stream);
+
+/* Host. Instrumentation for timing one kernel on the library's own stream:
+ * while `which` names a kernel (enum moe_prof_kernel), every later call that
+ * launches it records ev_start (a cudaEvent_t) immediately before that launch
+ * and ev_stop immediately after it, on the call's stream. The caller owns the
+ * events and may swap them between calls; MOE_PROF_NONE turns it off. */
+int moe_profile_kernel(moe_handle *h, int32_t which, void *ev_start, void *ev_stop);
 
 /* Host. Synchronises `stream`, returns the first device-side error recorded
  * since the last call (MOE_OK if none) and clears it. */

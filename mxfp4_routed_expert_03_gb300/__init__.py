@@ -23,6 +23,7 @@ MOE_ERR_CUDA = -4
 MOE_ERR_DEVICE_TIMEOUT = -5
 MOE_ERR_NAN_LOGIT = -6
 MOE_ERR_BAD_INDEX = -7
+MOE_ERR_NOT_PREPARED = -8
 
 MOE_ROUTER_LOGITS = 0
 MOE_ROUTER_XWR = 1
@@ -32,8 +33,15 @@ MOE_OP_FORWARD = 1
 MOE_OP_DECODE = 2
 
 # Every symbol include/moe.h declares.
-EXPORTS = ("moe_create", "moe_destroy", "moe_expert_bytes", "moe_workspace_bytes", "moe_plan",
-           "moe_forward", "moe_decode", "moe_status", "moe_strerror")
+EXPORTS = ("moe_create", "moe_destroy", "moe_expert_bytes", "moe_prepared_bytes", "moe_prepare",
+           "moe_workspace_bytes", "moe_plan", "moe_forward", "moe_decode", "moe_profile_kernel",
+           "moe_status", "moe_strerror")
+
+MOE_PROF_NONE = 0
+MOE_PROF_DECODE_GATEUP = 1
+MOE_PROF_DECODE_DOWN = 2
+MOE_PROF_FORWARD_GEMM1 = 3
+MOE_PROF_FORWARD_GEMM2 = 4
 
 
 class moe_desc(ctypes.Structure):
@@ -78,6 +86,10 @@ def lib() -> ctypes.CDLL:
         L.moe_destroy.restype = None
         L.moe_expert_bytes.argtypes = [i32, i32]
         L.moe_expert_bytes.restype = i64
+        L.moe_prepared_bytes.argtypes = [p]
+        L.moe_prepared_bytes.restype = sz
+        L.moe_prepare.argtypes = [p, p, sz, p]
+        L.moe_prepare.restype = ctypes.c_int
         L.moe_workspace_bytes.argtypes = [p, i32, i32]
         L.moe_workspace_bytes.restype = sz
         L.moe_plan.argtypes = [p, i32, p, p, ctypes.POINTER(moe_plan_buf), p, sz, p]
@@ -85,6 +97,8 @@ def lib() -> ctypes.CDLL:
         for fn in (L.moe_forward, L.moe_decode):
             fn.argtypes = [p, i32, p, ctypes.POINTER(moe_plan_buf), p, p, sz, p]
             fn.restype = ctypes.c_int
+        L.moe_profile_kernel.argtypes = [p, i32, p, p]
+        L.moe_profile_kernel.restype = ctypes.c_int
         L.moe_status.argtypes = [p, p]
         L.moe_status.restype = ctypes.c_int
         L.moe_strerror.argtypes = [ctypes.c_int]
@@ -130,6 +144,14 @@ def moe_destroy(h: int) -> None:
     lib().moe_destroy(h)
 
 
+def moe_prepared_bytes(h: int) -> int:
+    return lib().moe_prepared_bytes(h)
+
+
+def moe_prepare(h, buf, nbytes, stream=None) -> int:
+    return lib().moe_prepare(h, _ptr(buf), nbytes, _stream(stream))
+
+
 def moe_workspace_bytes(h: int, T: int, op: int) -> int:
     return lib().moe_workspace_bytes(h, T, op)
 
@@ -147,6 +169,15 @@ def moe_forward(h, T, x, plan: moe_plan_buf, out, ws, ws_bytes, stream=None) -> 
 def moe_decode(h, T, x, plan: moe_plan_buf, out, ws, ws_bytes, stream=None) -> int:
     return lib().moe_decode(h, T, _ptr(x), ctypes.byref(plan), _ptr(out), _ptr(ws), ws_bytes,
                             _stream(stream))
+
+
+def moe_profile_kernel(h, which: int, ev_start=None, ev_stop=None) -> int:
+    """ev_start/ev_stop: torch.cuda.Event (already recorded once) or raw cudaEvent_t."""
+    def raw(e):
+        if e is None or isinstance(e, int):
+            return e
+        return e.cuda_event
+    return lib().moe_profile_kernel(h, which, raw(ev_start), raw(ev_stop))
 
 
 def moe_status(h, stream=None) -> int:

@@ -15,6 +15,8 @@ struct moe_handle {
     int num_sms;
     int *status;  // device word: first error code recorded by a kernel
     CUtensorMap map_gate, map_up, map_down;  // TMA views of the packed E2M1 weights
+    const uint8_t *atoms;  // caller buffer filled by moe_prepare (NULL until then)
+    MoeProf prof;          // optional timing events (moe_profile_kernel)
 };
 
 // Device-side waits give up after this many SM clocks (about one second).
@@ -54,9 +56,14 @@ static bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Workspace of moe_forward, carved in this order (each region 1 KB aligned).
+// Workspace of moe_forward, carved in this order (each region 1 KB aligned):
+// per-token two-term E4M3 activations and scales, the same rows gathered into
+// plan (slot) order with per-token-tile scale atoms, h in slot order with its
+// scale atoms, the fp32 output accumulator and the token-tile schedule.
 struct FwdLayout {
-    size_t xq_hi, xq_lo, xs_hi, xs_lo, hq_hi, hq_lo, hs_hi, hs_lo, acc, prefix, total;
+    size_t xq_hi, xq_lo, xs_hi, xs_lo, xg_hi, xg_lo, xa_hi, xa_lo, hq_hi, hq_lo, ha_hi, ha_lo,
+        acc, prefix, total;
+    int max_tt;
 };
 
 static FwdLayout fwd_layout(int T, int D, int F, int E, int k) {
@@ -67,15 +74,21 @@ static FwdLayout fwd_layout(int T, int D, int F, int E, int k) {
         off += (bytes + 1023) / 1024 * 1024;
         return o;
     };
-    size_t rows = (size_t)T * k;
+    const size_t rows = (size_t)T * k;
+    // each active expert contributes ceil(count / NTMAX) <= count / NTMAX + 1 tiles
+    L.max_tt = (int)(E + (rows + MOE_GEMM_NTMAX - 1) / MOE_GEMM_NTMAX);
     L.xq_hi = take((size_t)T * D);
     L.xq_lo = take((size_t)T * D);
     L.xs_hi = take((size_t)T * D / 32);
     L.xs_lo = take((size_t)T * D / 32);
+    L.xg_hi = take(rows * D);
+    L.xg_lo = take(rows * D);
+    L.xa_hi = take((size_t)L.max_tt * (D / 128) * 512);
+    L.xa_lo = take((size_t)L.max_tt * (D / 128) * 512);
     L.hq_hi = take(rows * F);
     L.hq_lo = take(rows * F);
-    L.hs_hi = take(rows * F / 32);
-    L.hs_lo = take(rows * F / 32);
+    L.ha_hi = take((size_t)L.max_tt * (F / 128) * 512);
+    L.ha_lo = take((size_t)L.max_tt * (F / 128) * 512);
     L.acc = take((size_t)T * D * sizeof(float));
     L.prefix = take((size_t)(E + 1) * sizeof(int32_t));
     L.total = off;
@@ -102,6 +115,7 @@ MOE_API const char *moe_strerror(int code) {
         case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
         case MOE_ERR_NAN_LOGIT: return "NaN router logit";
         case MOE_ERR_BAD_INDEX: return "out-of-range index in plan";
+        case MOE_ERR_NOT_PREPARED: return "moe_prepare has not been called on this handle";
         default: return "unknown status code";
     }
 }
@@ -219,7 +233,7 @@ MOE_API int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_pl
     if (ws_bytes < need || !ws || !aligned16(ws)) return MOE_ERR_WORKSPACE;
     const moe_desc &d = h->desc;
     cudaError_t err = moe_launch_decode(T, d.d_model, d.d_ff, d.n_experts, d.top_k, x, plan, &h->w,
-                                        out, ws, h->status, (cudaStream_t)stream);
+                                        out, ws, h->status, h->prof, (cudaStream_t)stream);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -230,6 +244,7 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     if (!x || !out || !plan_ok(plan)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
     if ((int64_t)T * h->desc.top_k > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    if (!h->atoms) return MOE_ERR_NOT_PREPARED;
     const moe_desc &d = h->desc;
     const FwdLayout L = fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k);
     if (ws_bytes < L.total || !ws || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
@@ -238,14 +253,16 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     const int D = d.d_model, F = d.d_ff, E = d.n_experts, k = d.top_k, rows = T * k;
     uint8_t *xq_hi = base + L.xq_hi, *xq_lo = base + L.xq_lo;
     uint8_t *xs_hi = base + L.xs_hi, *xs_lo = base + L.xs_lo;
+    uint8_t *xg_hi = base + L.xg_hi, *xg_lo = base + L.xg_lo;
+    uint8_t *xa_hi = base + L.xa_hi, *xa_lo = base + L.xa_lo;
     uint8_t *hq_hi = base + L.hq_hi, *hq_lo = base + L.hq_lo;
-    uint8_t *hs_hi = base + L.hs_hi, *hs_lo = base + L.hs_lo;
+    uint8_t *ha_hi = base + L.ha_hi, *ha_lo = base + L.ha_lo;
     float *acc = (float *)(base + L.acc);
     int32_t *prefix = (int32_t *)(base + L.prefix);
 
     CUtensorMap mx_hi, mx_lo, mh_hi, mh_lo;
-    if (!make_map_2d(&mx_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq_hi, D, T, D, 128, 1) ||
-        !make_map_2d(&mx_lo, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq_lo, D, T, D, 128, 1) ||
+    if (!make_map_2d(&mx_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, xg_hi, D, rows, D, 128, 16) ||
+        !make_map_2d(&mx_lo, CU_TENSOR_MAP_DATA_TYPE_UINT8, xg_lo, D, rows, D, 128, 16) ||
         !make_map_2d(&mh_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, hq_hi, F, rows, F, 128, 16) ||
         !make_map_2d(&mh_lo, CU_TENSOR_MAP_DATA_TYPE_UINT8, hq_lo, F, rows, F, 128, 16))
         return MOE_ERR_CUDA;
@@ -254,6 +271,10 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     if (err == cudaSuccess)
         err = moe_launch_schedule(E, MOE_GEMM_NTMAX, plan->offsets, plan->active, prefix,
                                   h->status, st);
+    if (err == cudaSuccess)
+        err = moe_launch_gather_x(L.max_tt, E, k, rows, D, MOE_GEMM_NTMAX, plan->offsets,
+                                  plan->perm, plan->active, prefix, xq_hi, xq_lo, xs_hi, xs_lo,
+                                  xg_hi, xg_lo, xa_hi, xa_lo, h->status, st);
     MoeGemmArgs a;
     memset(&a, 0, sizeof(a));
     a.E = E;
@@ -273,16 +294,18 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         g1.MT = F / 128;
         g1.K = D;
         g1.KC = D / 128;
-        g1.a_s = h->w.gate_s;
-        g1.a2_s = h->w.up_s;
-        g1.b_s_hi = xs_hi;
-        g1.b_s_lo = xs_lo;
+        g1.a_atoms = h->atoms;
+        g1.a2_atoms = h->atoms + (size_t)E * F * D / 32;
+        g1.b_atoms_hi = xa_hi;
+        g1.b_atoms_lo = xa_lo;
         g1.h_hi = hq_hi;
         g1.h_lo = hq_lo;
-        g1.hs_hi = hs_hi;
-        g1.hs_lo = hs_lo;
+        g1.h_atoms_hi = ha_hi;
+        g1.h_atoms_lo = ha_lo;
+        h->prof.before(MOE_PROF_FORWARD_GEMM1, st);
         err = moe_launch_gemm(MOE_GEMM_GATEUP, &h->map_gate, &h->map_up, &mx_hi, &mx_lo, &g1,
                               h->num_sms, st);
+        h->prof.after(MOE_PROF_FORWARD_GEMM1, st);
     }
     if (err == cudaSuccess) err = cudaMemsetAsync(acc, 0, (size_t)T * D * sizeof(float), st);
     if (err == cudaSuccess) {
@@ -291,16 +314,50 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         g2.MT = D / 128;
         g2.K = F;
         g2.KC = F / 128;
-        g2.a_s = h->w.down_s;
-        g2.a2_s = nullptr;
-        g2.b_s_hi = hs_hi;
-        g2.b_s_lo = hs_lo;
+        g2.a_atoms = h->atoms + 2 * ((size_t)E * F * D / 32);
+        g2.a2_atoms = nullptr;
+        g2.b_atoms_hi = ha_hi;
+        g2.b_atoms_lo = ha_lo;
         g2.acc = acc;
+        h->prof.before(MOE_PROF_FORWARD_GEMM2, st);
         err = moe_launch_gemm(MOE_GEMM_DOWN, &h->map_down, &h->map_down, &mh_hi, &mh_lo, &g2,
                               h->num_sms, st);
+        h->prof.after(MOE_PROF_FORWARD_GEMM2, st);
     }
     if (err == cudaSuccess) err = moe_launch_finalize(T, D, acc, out, st);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+MOE_API size_t moe_prepared_bytes(const moe_handle *h) {
+    if (!h) return 0;
+    const moe_desc &d = h->desc;
+    return 3 * ((size_t)d.n_experts * d.d_model * d.d_ff / 32);
+}
+
+MOE_API int moe_prepare(moe_handle *h, void *buf, size_t bytes, void *stream) {
+    if (!h || !buf) return MOE_ERR_INVALID_ARG;
+    if (bytes < moe_prepared_bytes(h)) return MOE_ERR_WORKSPACE;
+    if ((uintptr_t)buf & 255u) return MOE_ERR_INVALID_ARG;
+    const moe_desc &d = h->desc;
+    const int E = d.n_experts, D = d.d_model, F = d.d_ff;
+    uint8_t *out = (uint8_t *)buf;
+    const size_t per = (size_t)E * F * D / 32;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t err = moe_launch_prepare_atoms(E, F, D, h->w.gate_s, out, st);
+    if (err == cudaSuccess) err = moe_launch_prepare_atoms(E, F, D, h->w.up_s, out + per, st);
+    if (err == cudaSuccess) err = moe_launch_prepare_atoms(E, D, F, h->w.down_s, out + 2 * per, st);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    h->atoms = out;
+    return MOE_OK;
+}
+
+MOE_API int moe_profile_kernel(moe_handle *h, int32_t which, void *ev_start, void *ev_stop) {
+    if (!h || which < MOE_PROF_NONE || which > MOE_PROF_FORWARD_GEMM2) return MOE_ERR_INVALID_ARG;
+    if (which != MOE_PROF_NONE && (!ev_start || !ev_stop)) return MOE_ERR_INVALID_ARG;
+    h->prof.which = which;
+    h->prof.start = (cudaEvent_t)ev_start;
+    h->prof.stop = (cudaEvent_t)ev_stop;
+    return MOE_OK;
 }
 
 MOE_API int moe_status(moe_handle *h, void *stream) {

@@ -12,10 +12,15 @@
 // Arithmetic: an E2M1 pair is converted to f16x2 exactly (cvt.rn.f16x2.e2m1x2);
 // each 32-element block is reduced with exact f16 x f16 products accumulated
 // in fp32 (fma.rn.f32.f16), multiplied by its E8M0 scale and added to the
-// row's fp32 sum. The activation row is held in shared memory as f16 (bf16 ->
-// f16 is exact for |x| in [2^-14, 65504), the range of these inputs).
-// In the down projection the intermediate h stays fp32 and the codes are
-// widened to fp32.
+// row's fp32 sum. Activations enter as f16 (bf16 -> f16 is exact for |x| in
+// [2^-14, 65504), the range of these inputs). The intermediate h is stored as
+// f16 with one power-of-two exponent per 32 consecutive rows of F (so it
+// cannot overflow; 11 significant bits per element), which lets the down
+// projection use the same exact f16 x f16 -> fp32 inner loop.
+//
+// Work split: persistent grids, each CTA walking a contiguous range of the
+// (active expert, row) space, so every weight row is read exactly once and
+// the grid stays balanced for any number of active experts.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -33,30 +38,37 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
     return r;
 }
 
-// acc + lo(a)*lo(b) + hi(a)*hi(b), products exact, sums in fp32.
-__device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float acc) {
-    asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t"
-        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-        "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
-        "fma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+// acc + sum over the 8 codes of word w (element 2i in the low nibble of byte i)
+// times the 8 f16 activations in xa..xd: products exact, sums in fp32.
+__device__ __forceinline__ float word_dot(uint32_t w, uint32_t xa, uint32_t xb, uint32_t xc,
+                                          uint32_t xd, float acc) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .b32 h0, h1, h2, h3;\n\t"
+        ".reg .f16 wl, wh, al, ah;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 h0, b0;\n\tcvt.rn.f16x2.e2m1x2 h1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 h2, b2;\n\tcvt.rn.f16x2.e2m1x2 h3, b3;\n\t"
+        "mov.b32 {wl, wh}, h0;\n\tmov.b32 {al, ah}, %2;\n\t"
+        "fma.rn.f32.f16 %0, wl, al, %0;\n\tfma.rn.f32.f16 %0, wh, ah, %0;\n\t"
+        "mov.b32 {wl, wh}, h1;\n\tmov.b32 {al, ah}, %3;\n\t"
+        "fma.rn.f32.f16 %0, wl, al, %0;\n\tfma.rn.f32.f16 %0, wh, ah, %0;\n\t"
+        "mov.b32 {wl, wh}, h2;\n\tmov.b32 {al, ah}, %4;\n\t"
+        "fma.rn.f32.f16 %0, wl, al, %0;\n\tfma.rn.f32.f16 %0, wh, ah, %0;\n\t"
+        "mov.b32 {wl, wh}, h3;\n\tmov.b32 {al, ah}, %5;\n\t"
+        "fma.rn.f32.f16 %0, wl, al, %0;\n\tfma.rn.f32.f16 %0, wh, ah, %0;\n\t}"
         : "+f"(acc)
-        : "r"(a), "r"(b));
+        : "r"(w), "r"(xa), "r"(xb), "r"(xc), "r"(xd));
     return acc;
 }
 
 // Dot product of one 32-element MX block (16 code bytes) with 32 f16
-// activations (as 16 f16x2 words), fp32 result before the block scale.
+// activations held as four 16-byte chunks; fp32 result before the block scale.
 __device__ __forceinline__ float block_dot_f16(const uint4 &q, const uint4 *xs) {
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-    float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint4 xv = xs[i];  // elements 8i .. 8i+7
-        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-        for (int b = 0; b < 4; ++b) acc = fma2_f16_f32(e2m1x2_to_f16x2((w[i] >> (8 * b)) & 0xFF), xw[b], acc);
-    }
-    return acc;
+    const uint4 x0 = xs[0], x1 = xs[1], x2 = xs[2], x3 = xs[3];
+    float a0 = word_dot(q.x, x0.x, x0.y, x0.z, x0.w, 0.f);
+    float a1 = word_dot(q.y, x1.x, x1.y, x1.z, x1.w, 0.f);
+    a0 = word_dot(q.z, x2.x, x2.y, x2.z, x2.w, a0);
+    a1 = word_dot(q.w, x3.x, x3.y, x3.z, x3.w, a1);
+    return a0 + a1;
 }
 
 __device__ __forceinline__ float2 f16x2_to_float2(uint32_t v) {
@@ -82,94 +94,138 @@ __device__ __forceinline__ bool segment_of(int a, int E, int n_rows, const int32
 
 }  // namespace
 
+// Shared-memory activation rows: each 32-element block (64 bytes of f16) is
+// stored with 16 bytes of padding, so the 16-byte reads of eight consecutive
+// lanes (one block each) fall in distinct bank groups.
+constexpr int kBlkStride = 80;   // bytes per staged block
+constexpr int kStageTok = 4;     // tokens staged at once
+
 // ---------------------------------------------------------------------------
-// Gate/up + SwiGLU. grid = (F / ROWS, max active experts); each CTA handles
-// ROWS consecutive f of one expert for all of its tokens, NT tokens at a time.
-// Lanes are grouped LPR per row; each lane owns PER_LANE MX blocks of the row.
-// h[slot][f] = silu(g) * u (fp32), slot = position in the plan's perm order.
+// Gate/up + SwiGLU. The (active expert, 32-row block of F) steps are split
+// into contiguous ranges, one per CTA, so a CTA restages the activations
+// (bf16 -> f16 into shared memory) only when its expert changes. In a step
+// the 8 warps compute g, u for the 32 rows (lanes grouped LPR per row, each
+// lane owning PER_LANE MX blocks), then one warp per token stores the 32
+// values of h = silu(g) * u as f16 with their shared power-of-two exponent.
 // ---------------------------------------------------------------------------
-template <int PER_LANE, int NT>
-__global__ void __launch_bounds__(256) moe_decode_gateup_kernel(
-    int D, int F, int E, int k, int n_rows, int rows_per_cta, const uint16_t *__restrict__ x,
+template <int PER_LANE>
+__global__ void __launch_bounds__(256, 2) moe_decode_gateup_kernel(
+    int D, int F, int E, int k, int n_rows, const uint16_t *__restrict__ x,
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
     const int32_t *__restrict__ active, const uint8_t *__restrict__ gate_q,
     const uint8_t *__restrict__ gate_s, const uint8_t *__restrict__ up_q,
-    const uint8_t *__restrict__ up_s, float *__restrict__ h, int *status) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    __half *xs = (__half *)smem;  // [NT][D]
-    int e, s0, n;
-    if (!segment_of(blockIdx.y, E, n_rows, active, offsets, e, s0, n, status)) return;
+    const uint8_t *__restrict__ up_s, __half *__restrict__ h16, int8_t *__restrict__ hexp,
+    int *status) {
+    constexpr int NT = 2, NW = 8;
+    extern __shared__ __align__(16) unsigned char xs[];  // [kStageTok][nblk][kBlkStride]
+    __shared__ float s_h[kStageTok][32];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int nblk = D / 32;               // MX blocks per row
-    const int LPR = nblk / PER_LANE;       // lanes per row (power of two <= 32)
-    const int RPW = 32 / LPR;              // rows per warp pass
+    const int nblk = D / 32;
+    const int LPR = nblk / PER_LANE;
+    const int RPW = 32 / LPR;
     const int sub = lane % LPR, grp = lane / LPR;
-    const int f_begin = blockIdx.x * rows_per_cta;
-    const int f_end = min(F, f_begin + rows_per_cta);
     const size_t qrow = (size_t)D / 2, srow = (size_t)nblk;
-    const uint8_t *gq = gate_q + (size_t)e * F * qrow, *uq = up_q + (size_t)e * F * qrow;
-    const uint8_t *gs = gate_s + (size_t)e * F * srow, *us = up_s + (size_t)e * F * srow;
-
-    for (int g0 = 0; g0 < n; g0 += NT) {
-        const int nt = min(NT, n - g0);
-        __syncthreads();
-        // Stage the group's activation rows as f16.
-        for (int i = threadIdx.x; i < nt * (D / 2); i += blockDim.x) {
-            int tl = i / (D / 2), c = i % (D / 2);
-            int fl = perm[s0 + g0 + tl];
-            if (fl < 0 || fl >= n_rows) { moe_flag(status, MOE_ERR_BAD_INDEX); fl = 0; }
-            int t = fl / k;
-            uint32_t two = ((const uint32_t *)(x + (size_t)t * D))[c];
-            float2 v = make_float2(bf16_bits_to_f32(two & 0xFFFF), bf16_bits_to_f32(two >> 16));
-            ((__half2 *)xs)[(size_t)tl * (D / 2) + c] = __float22half2_rn(v);
-        }
-        __syncthreads();
-        for (int f = f_begin + wid * RPW + grp; f - grp < f_end; f += 8 * RPW) {
-            const bool row_ok = f < f_end;
-            uint4 gqv[PER_LANE], uqv[PER_LANE];
-            float gsc[PER_LANE], usc[PER_LANE];
+    int n_active = active[0];
+    if (n_active < 0 || n_active > E) {
+        if (threadIdx.x == 0) moe_flag(status, MOE_ERR_BAD_INDEX);
+        return;
+    }
+    const int spe = F / 32;  // steps per expert
+    const long long total = (long long)n_active * spe;
+    const long long b0 = total * blockIdx.x / gridDim.x, b1 = total * (blockIdx.x + 1) / gridDim.x;
+    int staged_a = -1, staged_g0 = -1;
+    for (long long step = b0; step < b1; ++step) {
+        const int a = (int)(step / spe), f_base = (int)(step % spe) * 32;
+        int e, s0, n;
+        if (!segment_of(a, E, n_rows, active, offsets, e, s0, n, status)) continue;
+        const uint8_t *gq = gate_q + (size_t)e * F * qrow, *uq = up_q + (size_t)e * F * qrow;
+        const uint8_t *gs = gate_s + (size_t)e * F * srow, *us = up_s + (size_t)e * F * srow;
+        for (int g0 = 0; g0 < n; g0 += kStageTok) {
+            const int ns = min(kStageTok, n - g0);
+            if (a != staged_a || g0 != staged_g0) {
+                __syncthreads();
+                // 8 bf16 -> 8 f16 per thread iteration; chunk c of block b of token j
+                for (int i = threadIdx.x; i < ns * nblk * 4; i += blockDim.x) {
+                    const int j = i / (nblk * 4), r = i % (nblk * 4);
+                    int fl = perm[s0 + g0 + j];
+                    if (fl < 0 || fl >= n_rows) { moe_flag(status, MOE_ERR_BAD_INDEX); fl = 0; }
+                    const uint4 v = __ldg((const uint4 *)(x + (size_t)(fl / k) * D) + r);
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t o[4];
 #pragma unroll
-            for (int p = 0; p < PER_LANE; ++p) {
-                int b = sub + LPR * p;
-                if (row_ok) {
+                    for (int q = 0; q < 4; ++q) {
+                        __half2 hh = __floats2half2_rn(__uint_as_float(w4[q] << 16),
+                                                       __uint_as_float(w4[q] & 0xFFFF0000u));
+                        o[q] = *reinterpret_cast<uint32_t *>(&hh);
+                    }
+                    *(uint4 *)(xs + ((size_t)j * nblk + r / 4) * kBlkStride + (r % 4) * 16) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                __syncthreads();
+                staged_a = a;
+                staged_g0 = g0;
+            }
+            for (int rl = wid * RPW + grp; rl - grp < 32; rl += NW * RPW) {
+                const bool row_ok = rl < 32;
+                const int f = f_base + (row_ok ? rl : 0);
+                uint4 gqv[PER_LANE], uqv[PER_LANE];
+                float gsc[PER_LANE], usc[PER_LANE];
+#pragma unroll
+                for (int p = 0; p < PER_LANE; ++p) {
+                    const int b = sub + LPR * p;
                     gqv[p] = __ldg((const uint4 *)(gq + (size_t)f * qrow) + b);
                     uqv[p] = __ldg((const uint4 *)(uq + (size_t)f * qrow) + b);
                     gsc[p] = e8m0_to_f32(__ldg(gs + (size_t)f * srow + b));
                     usc[p] = e8m0_to_f32(__ldg(us + (size_t)f * srow + b));
-                } else {
-                    gqv[p] = uqv[p] = make_uint4(0, 0, 0, 0);
-                    gsc[p] = usc[p] = 0.f;
                 }
-            }
-            float ag[NT], au[NT];
+                for (int j0 = 0; j0 < ns; j0 += NT) {
+                    const int nt = min(NT, ns - j0);
+                    float ag[NT], au[NT];
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                ag[j] = 0.f;
-                au[j] = 0.f;
-                if (j < nt) {
+                    for (int j = 0; j < NT; ++j) {
+                        ag[j] = 0.f;
+                        au[j] = 0.f;
+                        if (j < nt) {
 #pragma unroll
-                    for (int p = 0; p < PER_LANE; ++p) {
-                        int b = sub + LPR * p;
-                        const uint4 *xb = (const uint4 *)(xs + (size_t)j * D + 32 * b);
-                        ag[j] = fmaf(block_dot_f16(gqv[p], xb), gsc[p], ag[j]);
-                        au[j] = fmaf(block_dot_f16(uqv[p], xb), usc[p], au[j]);
+                            for (int p = 0; p < PER_LANE; ++p) {
+                                const uint4 *xb = (const uint4 *)(
+                                    xs + ((size_t)(j0 + j) * nblk + sub + LPR * p) * kBlkStride);
+                                ag[j] = fmaf(block_dot_f16(gqv[p], xb), gsc[p], ag[j]);
+                                au[j] = fmaf(block_dot_f16(uqv[p], xb), usc[p], au[j]);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+                        for (int off = 1; off < 32; off <<= 1) {
+                            if (off < LPR) {
+                                ag[j] += __shfl_xor_sync(FULL_MASK, ag[j], off);
+                                au[j] += __shfl_xor_sync(FULL_MASK, au[j], off);
+                            }
+                        }
+                    }
+                    if (row_ok && sub == 0) {
+#pragma unroll
+                        for (int j = 0; j < NT; ++j)
+                            if (j < nt) s_h[j0 + j][rl] = silu_f(ag[j]) * au[j];
                     }
                 }
             }
+            __syncthreads();
+            if (wid < ns) {
+                const float v = s_h[wid][lane];
+                float amax = fabsf(v);
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    if (off < LPR) {
-                        ag[j] += __shfl_xor_sync(FULL_MASK, ag[j], off);
-                        au[j] += __shfl_xor_sync(FULL_MASK, au[j], off);
-                    }
-                }
-            }
-            if (row_ok && sub == 0) {
-#pragma unroll
-                for (int j = 0; j < NT; ++j)
-                    if (j < nt) h[(size_t)(s0 + g0 + j) * F + f] = silu_f(ag[j]) * au[j];
+                for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, off));
+                // exponent so that amax / 2^ex lies in [2^14, 2^15): f16-safe, 11 significant bits
+                int ex = ((int)((__float_as_uint(amax) >> 23) & 0xFF)) - 127 - 14;
+                if (amax == 0.f || !(amax < INFINITY)) ex = 0;
+                ex = max(-126, min(127, ex));
+                const float sc = __uint_as_float((uint32_t)(127 - ex) << 23);  // 2^-ex
+                const size_t slot = (size_t)(s0 + g0 + wid);
+                h16[slot * F + f_base + lane] = __float2half_rn(v * sc);
+                if (lane == 0) hexp[slot * (F / 32) + f_base / 32] = (int8_t)ex;
             }
         }
     }
@@ -177,91 +233,113 @@ __global__ void __launch_bounds__(256) moe_decode_gateup_kernel(
 
 // ---------------------------------------------------------------------------
 // Down projection: y[slot][d] = sum_f W_down[e][d][f] * h[slot][f] (fp32).
+// Units of consecutive rows of one expert are split into contiguous ranges
+// per CTA; h of the expert's slots is staged (padded blocks) when the expert
+// changes. Each warp issues all loads of RG groups of RPW rows before any
+// arithmetic.
 // ---------------------------------------------------------------------------
-template <int PER_LANE, int NT>
-__global__ void __launch_bounds__(256) moe_decode_down_kernel(
-    int D, int F, int E, int n_rows, int rows_per_cta, const int32_t *__restrict__ offsets,
+template <int PER_LANE>
+__global__ void __launch_bounds__(256, 2) moe_decode_down_kernel(
+    int D, int F, int E, int n_rows, const int32_t *__restrict__ offsets,
     const int32_t *__restrict__ active, const uint8_t *__restrict__ down_q,
-    const uint8_t *__restrict__ down_s, const float *__restrict__ h, float *__restrict__ y,
-    int *status) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    float *hs = (float *)smem;  // [NT][F]
-    int e, s0, n;
-    if (!segment_of(blockIdx.y, E, n_rows, active, offsets, e, s0, n, status)) return;
+    const uint8_t *__restrict__ down_s, const __half *__restrict__ h16,
+    const int8_t *__restrict__ hexp, float *__restrict__ y, int *status) {
+    constexpr int NT = 2, NW = 8, RG = 2;
+    extern __shared__ __align__(16) unsigned char hs[];  // [kStageTok][nblk][kBlkStride]
+    __shared__ float s_hsc[kStageTok][MOE_MAX_DFF / 32];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int nblk = F / 32;
     const int LPR = nblk / PER_LANE;
     const int RPW = 32 / LPR;
     const int sub = lane % LPR, grp = lane / LPR;
-    const int d_begin = blockIdx.x * rows_per_cta;
-    const int d_end = min(D, d_begin + rows_per_cta);
     const size_t qrow = (size_t)F / 2, srow = (size_t)nblk;
-    const uint8_t *dq = down_q + (size_t)e * D * qrow;
-    const uint8_t *ds = down_s + (size_t)e * D * srow;
-
-    for (int g0 = 0; g0 < n; g0 += NT) {
-        const int nt = min(NT, n - g0);
-        __syncthreads();
-        for (int i = threadIdx.x; i < nt * (F / 4); i += blockDim.x) {
-            int tl = i / (F / 4), c = i % (F / 4);
-            ((float4 *)hs)[(size_t)tl * (F / 4) + c] =
-                ((const float4 *)(h + (size_t)(s0 + g0 + tl) * F))[c];
-        }
-        __syncthreads();
-        for (int d = d_begin + wid * RPW + grp; d - grp < d_end; d += 8 * RPW) {
-            const bool row_ok = d < d_end;
-            uint4 qv[PER_LANE];
-            float sc[PER_LANE];
+    int n_active = active[0];
+    if (n_active < 0 || n_active > E) {
+        if (threadIdx.x == 0) moe_flag(status, MOE_ERR_BAD_INDEX);
+        return;
+    }
+    const int unit = NW * RG * RPW;  // rows per unit (D is a multiple of 128)
+    const int upe = (D + unit - 1) / unit;
+    const long long total = (long long)n_active * upe;
+    const long long b0 = total * blockIdx.x / gridDim.x, b1 = total * (blockIdx.x + 1) / gridDim.x;
+    int staged_a = -1, staged_g0 = -1;
+    for (long long u = b0; u < b1; ++u) {
+        const int a = (int)(u / upe), d_base = (int)(u % upe) * unit;
+        int e, s0, n;
+        if (!segment_of(a, E, n_rows, active, offsets, e, s0, n, status)) continue;
+        const uint8_t *dq = down_q + (size_t)e * D * qrow;
+        const uint8_t *ds = down_s + (size_t)e * D * srow;
+        int drow[RG];
+        bool ok[RG];
+        uint4 qv[RG][PER_LANE];
+        float sc[RG][PER_LANE];
+#pragma unroll
+        for (int r = 0; r < RG; ++r) {
+            drow[r] = d_base + (wid * RG + r) * RPW + grp;
+            ok[r] = drow[r] < D;
+            const int d = ok[r] ? drow[r] : 0;
 #pragma unroll
             for (int p = 0; p < PER_LANE; ++p) {
-                int b = sub + LPR * p;
-                if (row_ok) {
-                    qv[p] = __ldg((const uint4 *)(dq + (size_t)d * qrow) + b);
-                    sc[p] = e8m0_to_f32(__ldg(ds + (size_t)d * srow + b));
-                } else {
-                    qv[p] = make_uint4(0, 0, 0, 0);
-                    sc[p] = 0.f;
-                }
+                const int b = sub + LPR * p;
+                qv[r][p] = __ldg((const uint4 *)(dq + (size_t)d * qrow) + b);
+                sc[r][p] = e8m0_to_f32(__ldg(ds + (size_t)d * srow + b));
             }
-            float acc[NT];
+        }
+        for (int g0 = 0; g0 < n; g0 += kStageTok) {
+            const int ns = min(kStageTok, n - g0);
+            if (a != staged_a || g0 != staged_g0) {
+                __syncthreads();
+                for (int i = threadIdx.x; i < ns * nblk * 4; i += blockDim.x) {
+                    const int j = i / (nblk * 4), r = i % (nblk * 4);
+                    const uint4 v = __ldg((const uint4 *)(h16 + (size_t)(s0 + g0 + j) * F) + r);
+                    *(uint4 *)(hs + ((size_t)j * nblk + r / 4) * kBlkStride + (r % 4) * 16) = v;
+                }
+                for (int i = threadIdx.x; i < ns * nblk; i += blockDim.x) {
+                    const int j = i / nblk, b = i % nblk;
+                    const int ex = __ldg(hexp + (size_t)(s0 + g0 + j) * nblk + b);
+                    s_hsc[j][b] = __uint_as_float((uint32_t)(ex + 127) << 23);  // 2^ex
+                }
+                __syncthreads();
+                staged_a = a;
+                staged_g0 = g0;
+            }
+            for (int j0 = 0; j0 < ns; j0 += NT) {
+                const int nt = min(NT, ns - j0);
+                float acc[RG][NT];
 #pragma unroll
-            for (int j = 0; j < NT; ++j) acc[j] = 0.f;
+                for (int r = 0; r < RG; ++r)
 #pragma unroll
-            for (int p = 0; p < PER_LANE; ++p) {
-                int b = sub + LPR * p;
-                const uint32_t w[4] = {qv[p].x, qv[p].y, qv[p].z, qv[p].w};
-                float part[NT];
+                    for (int j = 0; j < NT; ++j) acc[r][j] = 0.f;
 #pragma unroll
-                for (int j = 0; j < NT; ++j) part[j] = 0.f;
+                for (int j = 0; j < NT; ++j) {
+                    if (j < nt) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                        for (int p = 0; p < PER_LANE; ++p) {
+                            const int b = sub + LPR * p;
+                            const uint4 *hb =
+                                (const uint4 *)(hs + ((size_t)(j0 + j) * nblk + b) * kBlkStride);
+                            const float hsc = s_hsc[j0 + j][b];
 #pragma unroll
-                    for (int bb = 0; bb < 4; ++bb) {
-                        float2 wf = f16x2_to_float2(e2m1x2_to_f16x2((w[i] >> (8 * bb)) & 0xFF));
-                        int kk = 32 * b + 8 * i + 2 * bb;
-#pragma unroll
-                        for (int j = 0; j < NT; ++j) {
-                            if (j < nt) {
-                                float2 hv = *(const float2 *)(hs + (size_t)j * F + kk);
-                                part[j] = fmaf(wf.x, hv.x, part[j]);
-                                part[j] = fmaf(wf.y, hv.y, part[j]);
-                            }
+                            for (int r = 0; r < RG; ++r)
+                                acc[r][j] = fmaf(block_dot_f16(qv[r][p], hb), sc[r][p] * hsc, acc[r][j]);
                         }
                     }
                 }
 #pragma unroll
-                for (int j = 0; j < NT; ++j) acc[j] = fmaf(part[j], sc[p], acc[j]);
-            }
+                for (int r = 0; r < RG; ++r)
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
+                    for (int j = 0; j < NT; ++j)
 #pragma unroll
-                for (int off = 1; off < 32; off <<= 1)
-                    if (off < LPR) acc[j] += __shfl_xor_sync(FULL_MASK, acc[j], off);
-            }
-            if (row_ok && sub == 0) {
+                        for (int off = 1; off < 32; off <<= 1)
+                            if (off < LPR) acc[r][j] += __shfl_xor_sync(FULL_MASK, acc[r][j], off);
+                if (sub == 0) {
 #pragma unroll
-                for (int j = 0; j < NT; ++j)
-                    if (j < nt) y[(size_t)(s0 + g0 + j) * D + d] = acc[j];
+                    for (int r = 0; r < RG; ++r)
+                        if (ok[r])
+#pragma unroll
+                            for (int j = 0; j < NT; ++j)
+                                if (j < nt) y[(size_t)(s0 + g0 + j0 + j) * D + drow[r]] = acc[r][j];
+                }
             }
         }
     }
@@ -299,35 +377,6 @@ __global__ void __launch_bounds__(256) moe_combine_slots_kernel(int T, int D, in
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
-namespace {
-constexpr int kDecodeNT = 4;
-constexpr int kRowsPerCta = 16;
-
-template <int P>
-cudaError_t launch_gateup(dim3 g, size_t sm, cudaStream_t st, int D, int F, int E, int k,
-                          int n_rows, const uint16_t *x, const moe_plan_buf *p,
-                          const moe_weights *w, float *h, int *status) {
-    auto kern = moe_decode_gateup_kernel<P, kDecodeNT>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (err != cudaSuccess) return err;
-    kern<<<g, 256, sm, st>>>(D, F, E, k, n_rows, kRowsPerCta, x, p->offsets, p->perm, p->active,
-                             w->gate_q, w->gate_s, w->up_q, w->up_s, h, status);
-    return cudaGetLastError();
-}
-
-template <int P>
-cudaError_t launch_down(dim3 g, size_t sm, cudaStream_t st, int D, int F, int E, int n_rows,
-                        const moe_plan_buf *p, const moe_weights *w, const float *h, float *y,
-                        int *status) {
-    auto kern = moe_decode_down_kernel<P, kDecodeNT>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (err != cudaSuccess) return err;
-    kern<<<g, 256, sm, st>>>(D, F, E, n_rows, kRowsPerCta, p->offsets, p->active, w->down_q,
-                             w->down_s, h, y, status);
-    return cudaGetLastError();
-}
-}  // namespace
-
 // MX blocks per lane for a row of K elements: the smallest p <= 8 with
 // (K/32) % p == 0 and (K/32)/p a power of two <= 32; 0 if none.
 int moe_decode_per_lane(int K) {
@@ -340,51 +389,94 @@ int moe_decode_per_lane(int K) {
     return 0;
 }
 
-size_t moe_decode_ws_bytes(int T, int D, int F, int k) {
+namespace {
+struct DecodeLayout {
+    size_t h16, hexp, y, total;
+};
+
+DecodeLayout decode_layout(int T, int D, int F, int k) {
+    DecodeLayout L;
+    size_t off = 0;
+    auto take = [&](size_t b) {
+        size_t o = off;
+        off += (b + 255) / 256 * 256;
+        return o;
+    };
     size_t rows = (size_t)T * k;
-    return rows * F * sizeof(float) + rows * D * sizeof(float);
+    L.h16 = take(rows * F * 2);
+    L.hexp = take(rows * F / 32);
+    L.y = take(rows * D * sizeof(float));
+    L.total = off;
+    return L;
 }
+
+int g_num_sms = 0;
+int num_sms() {
+    if (!g_num_sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_num_sms <= 0) g_num_sms = 1;
+    }
+    return g_num_sms;
+}
+}  // namespace
+
+size_t moe_decode_ws_bytes(int T, int D, int F, int k) { return decode_layout(T, D, F, k).total; }
+
+namespace {
+template <int P>
+void launch_gateup(int grid, cudaStream_t st, int D, int F, int E, int k, int n_rows,
+                   const uint16_t *x, const moe_plan_buf *p, const moe_weights *w, __half *h16,
+                   int8_t *hexp, int *status) {
+    const size_t sm = (size_t)kStageTok * (D / 32) * kBlkStride;
+    cudaFuncSetAttribute(moe_decode_gateup_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sm);
+    moe_decode_gateup_kernel<P><<<grid, 256, sm, st>>>(D, F, E, k, n_rows, x, p->offsets, p->perm,
+                                                       p->active, w->gate_q, w->gate_s, w->up_q,
+                                                       w->up_s, h16, hexp, status);
+}
+
+template <int P>
+void launch_down(int grid, cudaStream_t st, int D, int F, int E, int n_rows, const moe_plan_buf *p,
+                 const moe_weights *w, const __half *h16, const int8_t *hexp, float *y,
+                 int *status) {
+    const size_t sm = (size_t)kStageTok * (F / 32) * kBlkStride;
+    cudaFuncSetAttribute(moe_decode_down_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sm);
+    moe_decode_down_kernel<P><<<grid, 256, sm, st>>>(D, F, E, n_rows, p->offsets, p->active,
+                                                     w->down_q, w->down_s, h16, hexp, y, status);
+}
+
+typedef void (*gateup_fn)(int, cudaStream_t, int, int, int, int, int, const uint16_t *,
+                          const moe_plan_buf *, const moe_weights *, __half *, int8_t *, int *);
+typedef void (*down_fn)(int, cudaStream_t, int, int, int, int, const moe_plan_buf *,
+                        const moe_weights *, const __half *, const int8_t *, float *, int *);
+const gateup_fn kGateup[9] = {nullptr, launch_gateup<1>, launch_gateup<2>, launch_gateup<3>,
+                              launch_gateup<4>, launch_gateup<5>, launch_gateup<6>,
+                              launch_gateup<7>, launch_gateup<8>};
+const down_fn kDown[9] = {nullptr, launch_down<1>, launch_down<2>, launch_down<3>, launch_down<4>,
+                          launch_down<5>, launch_down<6>, launch_down<7>, launch_down<8>};
+}  // namespace
 
 cudaError_t moe_launch_decode(int T, int D, int F, int E, int k, const uint16_t *x,
                               const moe_plan_buf *p, const moe_weights *w, uint16_t *out,
-                              void *ws, int *status, cudaStream_t st) {
+                              void *ws, int *status, const MoeProf &prof, cudaStream_t st) {
     const int n_rows = T * k;
-    float *h = (float *)ws;
-    float *y = h + (size_t)n_rows * F;
-    const int max_active = n_rows < E ? n_rows : E;
-    cudaError_t err;
-    {
-        dim3 g((F + kRowsPerCta - 1) / kRowsPerCta, max_active);
-        size_t sm = (size_t)kDecodeNT * D * sizeof(__half);
-        switch (moe_decode_per_lane(D)) {
-            case 1: err = launch_gateup<1>(g, sm, st, D, F, E, k, n_rows, x, p, w, h, status); break;
-            case 2: err = launch_gateup<2>(g, sm, st, D, F, E, k, n_rows, x, p, w, h, status); break;
-            case 3: err = launch_gateup<3>(g, sm, st, D, F, E, k, n_rows, x, p, w, h, status); break;
-            case 4: err = launch_gateup<4>(g, sm, st, D, F, E, k, n_rows, x, p, w, h, status); break;
-            case 5: err = launch_gateup<5>(g, sm, st, D, F, E, k, n_rows, x, p, w, h, status); break;
-            case 6: err = launch_gateup<6>(g, sm, st, D, F, E, k, n_rows, x, p, w, h, status); break;
-            case 7: err = launch_gateup<7>(g, sm, st, D, F, E, k, n_rows, x, p, w, h, status); break;
-            case 8: err = launch_gateup<8>(g, sm, st, D, F, E, k, n_rows, x, p, w, h, status); break;
-            default: return cudaErrorInvalidValue;
-        }
-        if (err != cudaSuccess) return err;
-    }
-    {
-        dim3 g((D + kRowsPerCta - 1) / kRowsPerCta, max_active);
-        size_t sm = (size_t)kDecodeNT * F * sizeof(float);
-        switch (moe_decode_per_lane(F)) {
-            case 1: err = launch_down<1>(g, sm, st, D, F, E, n_rows, p, w, h, y, status); break;
-            case 2: err = launch_down<2>(g, sm, st, D, F, E, n_rows, p, w, h, y, status); break;
-            case 3: err = launch_down<3>(g, sm, st, D, F, E, n_rows, p, w, h, y, status); break;
-            case 4: err = launch_down<4>(g, sm, st, D, F, E, n_rows, p, w, h, y, status); break;
-            case 5: err = launch_down<5>(g, sm, st, D, F, E, n_rows, p, w, h, y, status); break;
-            case 6: err = launch_down<6>(g, sm, st, D, F, E, n_rows, p, w, h, y, status); break;
-            case 7: err = launch_down<7>(g, sm, st, D, F, E, n_rows, p, w, h, y, status); break;
-            case 8: err = launch_down<8>(g, sm, st, D, F, E, n_rows, p, w, h, y, status); break;
-            default: return cudaErrorInvalidValue;
-        }
-        if (err != cudaSuccess) return err;
-    }
+    const DecodeLayout L = decode_layout(T, D, F, k);
+    unsigned char *base = (unsigned char *)ws;
+    __half *h16 = (__half *)(base + L.h16);
+    int8_t *hexp = (int8_t *)(base + L.hexp);
+    float *y = (float *)(base + L.y);
+    const int grid = 2 * num_sms();
+    const int pd = moe_decode_per_lane(D), pf = moe_decode_per_lane(F);
+    if (pd < 1 || pd > 8 || pf < 1 || pf > 8) return cudaErrorInvalidValue;
+    prof.before(MOE_PROF_DECODE_GATEUP, st);
+    kGateup[pd](grid, st, D, F, E, k, n_rows, x, p, w, h16, hexp, status);
+    prof.after(MOE_PROF_DECODE_GATEUP, st);
+    prof.before(MOE_PROF_DECODE_DOWN, st);
+    kDown[pf](grid, st, D, F, E, n_rows, p, w, h16, hexp, y, status);
+    prof.after(MOE_PROF_DECODE_DOWN, st);
     dim3 g((D / 4 + 255) / 256, T);
     moe_combine_slots_kernel<<<g, 256, 0, st>>>(T, D, k, n_rows, p->topk_w, p->inv, y, out, status);
     return cudaGetLastError();

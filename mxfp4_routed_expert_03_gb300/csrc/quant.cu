@@ -122,6 +122,85 @@ __global__ void __launch_bounds__(256) moe_finalize_kernel(int64_t n4, const flo
     ((uint2 *)out)[i] = o;
 }
 
+// Token tile tt -> its expert's active index a, first row r0 and row count n
+// (the same split the grouped GEMMs use: ntt = ceil(count / ntmax) tiles of
+// near-equal size per expert).
+__device__ __forceinline__ bool token_tile(int tt, int n_active, const int32_t *prefix,
+                                           const int32_t *active, const int32_t *offsets, int E,
+                                           int n_rows, int &e, int &sb, int &r0, int &n) {
+    if (n_active <= 0 || tt >= prefix[n_active]) return false;
+    int lo = 0, hi = n_active - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= tt) lo = mid;
+        else hi = mid - 1;
+    }
+    int ntt = prefix[lo + 1] - prefix[lo];
+    int j = tt - prefix[lo];
+    e = active[1 + lo];
+    if (ntt <= 0 || e < 0 || e >= E) return false;
+    sb = offsets[e];
+    int cnt = offsets[e + 1] - sb;
+    if (sb < 0 || cnt <= 0 || sb + cnt > n_rows) return false;
+    r0 = (int)((long long)j * cnt / ntt);
+    n = (int)((long long)(j + 1) * cnt / ntt) - r0;
+    return true;
+}
+
+// Copies the quantised activation rows of one token tile into plan (slot)
+// order and writes their scales as 512-byte tensor-core scale atoms, one per
+// 128-wide K chunk: row r of the tile, 32-wide block c of the chunk at byte
+// (r % 32) * 16 + (r / 32) * 4 + c.
+__global__ void __launch_bounds__(256) moe_gather_x_kernel(
+    int E, int k, int n_rows, int D, const int32_t *__restrict__ offsets,
+    const int32_t *__restrict__ perm, const int32_t *__restrict__ active,
+    const int32_t *__restrict__ prefix, const uint8_t *__restrict__ q_hi,
+    const uint8_t *__restrict__ q_lo, const uint8_t *__restrict__ s_hi,
+    const uint8_t *__restrict__ s_lo, uint8_t *__restrict__ g_hi, uint8_t *__restrict__ g_lo,
+    uint8_t *__restrict__ atoms_hi, uint8_t *__restrict__ atoms_lo, int *status) {
+    __shared__ int s_tok[MOE_GEMM_NTMAX];
+    const int tt = blockIdx.x;
+    int n_active = active[0];
+    if (n_active < 0 || n_active > E) return;
+    int e, sb, r0, n;
+    if (!token_tile(tt, n_active, prefix, active, offsets, E, n_rows, e, sb, r0, n)) return;
+    if (n > MOE_GEMM_NTMAX) { if (threadIdx.x == 0) moe_flag(status, MOE_ERR_BAD_INDEX); return; }
+    for (int r = threadIdx.x; r < n; r += blockDim.x) {
+        int fl = perm[sb + r0 + r];
+        if (fl < 0 || fl >= n_rows) { moe_flag(status, MOE_ERR_BAD_INDEX); fl = 0; }
+        s_tok[r] = fl / k;
+    }
+    __syncthreads();
+    const int chunks = D / 16;  // 16-byte chunks per row and term
+    for (int i = threadIdx.x; i < n * chunks; i += blockDim.x) {
+        const int r = i / chunks, c = i % chunks;
+        const size_t src = (size_t)s_tok[r] * D / 16 + c;
+        const size_t dst = (size_t)(sb + r0 + r) * D / 16 + c;
+        ((uint4 *)g_hi)[dst] = ((const uint4 *)q_hi)[src];
+        ((uint4 *)g_lo)[dst] = ((const uint4 *)q_lo)[src];
+    }
+    const int nb = D / 32, KC = D / 128;
+    for (int i = threadIdx.x; i < n * nb; i += blockDim.x) {
+        const int r = i / nb, b = i % nb;
+        const size_t at = ((size_t)tt * KC + b / 4) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (b & 3);
+        atoms_hi[at] = s_hi[(size_t)s_tok[r] * nb + b];
+        atoms_lo[at] = s_lo[(size_t)s_tok[r] * nb + b];
+    }
+}
+
+cudaError_t moe_launch_gather_x(int max_tt, int E, int k, int n_rows, int D, int ntmax,
+                                const int32_t *offsets, const int32_t *perm, const int32_t *active,
+                                const int32_t *tt_prefix, const uint8_t *q_hi, const uint8_t *q_lo,
+                                const uint8_t *s_hi, const uint8_t *s_lo, uint8_t *g_hi,
+                                uint8_t *g_lo, uint8_t *atoms_hi, uint8_t *atoms_lo, int *status,
+                                cudaStream_t st) {
+    (void)ntmax;
+    moe_gather_x_kernel<<<max_tt, 256, 0, st>>>(E, k, n_rows, D, offsets, perm, active, tt_prefix,
+                                                q_hi, q_lo, s_hi, s_lo, g_hi, g_lo, atoms_hi,
+                                                atoms_lo, status);
+    return cudaGetLastError();
+}
+
 cudaError_t moe_launch_quant_x(int T, int D, const uint16_t *x, uint8_t *q_hi, uint8_t *q_lo,
                                uint8_t *s_hi, uint8_t *s_lo, cudaStream_t st) {
     int64_t nb = (int64_t)T * D / 32;

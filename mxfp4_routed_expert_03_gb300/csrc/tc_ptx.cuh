@@ -97,6 +97,17 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
+// Contiguous bulk copy global -> shared (16-byte aligned, size multiple of 16),
+// completion counted on bar's transaction count.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
+                                              uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+        "[%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 __device__ __forceinline__ void cp_async_4(void *dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)

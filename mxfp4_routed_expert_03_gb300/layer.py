@@ -8,8 +8,8 @@ from __future__ import annotations
 import torch
 
 from . import (MOE_OP_DECODE, MOE_OP_FORWARD, MOE_OP_PLAN, check, moe_create, moe_decode,
-               moe_desc, moe_destroy, moe_forward, moe_plan, moe_plan_buf, moe_status,
-               moe_weights, moe_workspace_bytes)
+               moe_desc, moe_destroy, moe_forward, moe_plan, moe_plan_buf, moe_prepare,
+               moe_prepared_bytes, moe_status, moe_weights, moe_workspace_bytes)
 
 WEIGHT_NAMES = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
 
@@ -60,6 +60,14 @@ class Layer:
                                  ptr(sh.get("sh_down")))
         self.h = moe_create(self.desc, self.wdesc)
         self._ws = None
+        self.atoms = None
+
+    def prepare(self, stream=None) -> None:
+        """One-time weight-scale re-layout for the tensor-core path."""
+        if self.atoms is None:
+            n = moe_prepared_bytes(self.h)
+            self.atoms = torch.empty(n, dtype=torch.uint8, device="cuda")
+            check(moe_prepare(self.h, self.atoms, n, stream), "moe_prepare")
 
     def close(self):
         if self.h:
@@ -87,6 +95,7 @@ class Layer:
         return moe_decode(self.h, T, x, plan.buf, out, ws, ws.numel(), stream)
 
     def forward(self, T, x, plan: Plan, out, stream=None) -> int:
+        self.prepare(stream)
         ws, n = self.workspace(T, MOE_OP_FORWARD)
         return moe_forward(self.h, T, x, plan.buf, out, ws, ws.numel(), stream)
 
