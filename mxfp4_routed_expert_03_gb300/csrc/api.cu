@@ -57,12 +57,13 @@ static bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base
 }
 
 // Workspace of moe_forward, carved in this order (each region 1 KB aligned):
-// per-token two-term E4M3 activations and scales, the same rows gathered into
-// plan (slot) order with per-token-tile scale atoms, h in slot order with its
-// scale atoms, the fp32 output accumulator and the token-tile schedule.
+// per-token two-term E4M3 activations and scales, the same rows laid out as
+// the gate/up GEMM's B tiles (one block of 2 * NTMAX rows x 128 bytes per
+// token tile and 128-wide K chunk; only the rows a tile uses are written),
+// their scale blocks, h as the down GEMM's B tiles and its scale blocks, the
+// fp32 output accumulator and the token-tile schedule.
 struct FwdLayout {
-    size_t xq_hi, xq_lo, xs_hi, xs_lo, xg_hi, xg_lo, xa_hi, xa_lo, hq_hi, hq_lo, ha_hi, ha_lo,
-        acc, prefix, total;
+    size_t xq_hi, xq_lo, xs_hi, xs_lo, xb, xa, hb, ha, acc, prefix, total;
     int max_tt;
 };
 
@@ -81,14 +82,10 @@ static FwdLayout fwd_layout(int T, int D, int F, int E, int k) {
     L.xq_lo = take((size_t)T * D);
     L.xs_hi = take((size_t)T * D / 32);
     L.xs_lo = take((size_t)T * D / 32);
-    L.xg_hi = take(rows * D);
-    L.xg_lo = take(rows * D);
-    L.xa_hi = take((size_t)L.max_tt * (D / 128) * 512);
-    L.xa_lo = take((size_t)L.max_tt * (D / 128) * 512);
-    L.hq_hi = take(rows * F);
-    L.hq_lo = take(rows * F);
-    L.ha_hi = take((size_t)L.max_tt * (F / 128) * 512);
-    L.ha_lo = take((size_t)L.max_tt * (F / 128) * 512);
+    L.xb = take((size_t)L.max_tt * (D / 128) * MOE_GEMM_BTILE);
+    L.xa = take((size_t)L.max_tt * (D / 128) * 1024);
+    L.hb = take((size_t)L.max_tt * (F / 128) * MOE_GEMM_BTILE);
+    L.ha = take((size_t)L.max_tt * (F / 128) * 1024);
     L.acc = take((size_t)T * D * sizeof(float));
     L.prefix = take((size_t)(E + 1) * sizeof(int32_t));
     L.total = off;
@@ -164,8 +161,8 @@ MOE_API int moe_create(const moe_desc *d, const moe_weights *w, moe_handle **out
     {
         const uint64_t D = d->d_model, F = d->d_ff, E = d->n_experts;
         const CUtensorMapDataType fp4 = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
-        if (!make_map_2d(&h->map_gate, fp4, w->gate_q, D, E * F, D / 2, 128, 128) ||
-            !make_map_2d(&h->map_up, fp4, w->up_q, D, E * F, D / 2, 128, 128) ||
+        if (!make_map_2d(&h->map_gate, fp4, w->gate_q, D, E * F, D / 2, 128, 64) ||
+            !make_map_2d(&h->map_up, fp4, w->up_q, D, E * F, D / 2, 128, 64) ||
             !make_map_2d(&h->map_down, fp4, w->down_q, F, E * D, F / 2, 128, 128)) {
             free(h);
             return MOE_ERR_CUDA;
@@ -253,19 +250,9 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     const int D = d.d_model, F = d.d_ff, E = d.n_experts, k = d.top_k, rows = T * k;
     uint8_t *xq_hi = base + L.xq_hi, *xq_lo = base + L.xq_lo;
     uint8_t *xs_hi = base + L.xs_hi, *xs_lo = base + L.xs_lo;
-    uint8_t *xg_hi = base + L.xg_hi, *xg_lo = base + L.xg_lo;
-    uint8_t *xa_hi = base + L.xa_hi, *xa_lo = base + L.xa_lo;
-    uint8_t *hq_hi = base + L.hq_hi, *hq_lo = base + L.hq_lo;
-    uint8_t *ha_hi = base + L.ha_hi, *ha_lo = base + L.ha_lo;
+    uint8_t *xb = base + L.xb, *xa = base + L.xa, *hb = base + L.hb, *ha = base + L.ha;
     float *acc = (float *)(base + L.acc);
     int32_t *prefix = (int32_t *)(base + L.prefix);
-
-    CUtensorMap mx_hi, mx_lo, mh_hi, mh_lo;
-    if (!make_map_2d(&mx_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, xg_hi, D, rows, D, 128, 16) ||
-        !make_map_2d(&mx_lo, CU_TENSOR_MAP_DATA_TYPE_UINT8, xg_lo, D, rows, D, 128, 16) ||
-        !make_map_2d(&mh_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, hq_hi, F, rows, F, 128, 16) ||
-        !make_map_2d(&mh_lo, CU_TENSOR_MAP_DATA_TYPE_UINT8, hq_lo, F, rows, F, 128, 16))
-        return MOE_ERR_CUDA;
 
     cudaError_t err = moe_launch_quant_x(T, D, x, xq_hi, xq_lo, xs_hi, xs_lo, st);
     if (err == cudaSuccess)
@@ -274,7 +261,7 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     if (err == cudaSuccess)
         err = moe_launch_gather_x(L.max_tt, E, k, rows, D, MOE_GEMM_NTMAX, plan->offsets,
                                   plan->perm, plan->active, prefix, xq_hi, xq_lo, xs_hi, xs_lo,
-                                  xg_hi, xg_lo, xa_hi, xa_lo, h->status, st);
+                                  xb, xa, h->status, st);
     MoeGemmArgs a;
     memset(&a, 0, sizeof(a));
     a.E = E;
@@ -291,20 +278,16 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     if (err == cudaSuccess) {
         MoeGemmArgs g1 = a;
         g1.M = F;
-        g1.MT = F / 128;
         g1.K = D;
         g1.KC = D / 128;
+        g1.MT = F / 64;  // 64 gate rows + the same 64 up rows per weight tile
         g1.a_atoms = h->atoms;
-        g1.a2_atoms = h->atoms + (size_t)E * F * D / 32;
-        g1.b_atoms_hi = xa_hi;
-        g1.b_atoms_lo = xa_lo;
-        g1.h_hi = hq_hi;
-        g1.h_lo = hq_lo;
-        g1.h_atoms_hi = ha_hi;
-        g1.h_atoms_lo = ha_lo;
+        g1.b_tiles = xb;
+        g1.b_atoms = xa;
+        g1.h_tiles = hb;
+        g1.h_atoms = ha;
         h->prof.before(MOE_PROF_FORWARD_GEMM1, st);
-        err = moe_launch_gemm(MOE_GEMM_GATEUP, &h->map_gate, &h->map_up, &mx_hi, &mx_lo, &g1,
-                              h->num_sms, st);
+        err = moe_launch_gemm(MOE_GEMM_GATEUP, &h->map_gate, &h->map_up, &g1, h->num_sms, st);
         h->prof.after(MOE_PROF_FORWARD_GEMM1, st);
     }
     if (err == cudaSuccess) err = cudaMemsetAsync(acc, 0, (size_t)T * D * sizeof(float), st);
@@ -315,13 +298,11 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         g2.K = F;
         g2.KC = F / 128;
         g2.a_atoms = h->atoms + 2 * ((size_t)E * F * D / 32);
-        g2.a2_atoms = nullptr;
-        g2.b_atoms_hi = ha_hi;
-        g2.b_atoms_lo = ha_lo;
+        g2.b_tiles = hb;
+        g2.b_atoms = ha;
         g2.acc = acc;
         h->prof.before(MOE_PROF_FORWARD_GEMM2, st);
-        err = moe_launch_gemm(MOE_GEMM_DOWN, &h->map_down, &h->map_down, &mh_hi, &mh_lo, &g2,
-                              h->num_sms, st);
+        err = moe_launch_gemm(MOE_GEMM_DOWN, &h->map_down, &h->map_down, &g2, h->num_sms, st);
         h->prof.after(MOE_PROF_FORWARD_GEMM2, st);
     }
     if (err == cudaSuccess) err = moe_launch_finalize(T, D, acc, out, st);
@@ -343,9 +324,10 @@ MOE_API int moe_prepare(moe_handle *h, void *buf, size_t bytes, void *stream) {
     uint8_t *out = (uint8_t *)buf;
     const size_t per = (size_t)E * F * D / 32;
     cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t err = moe_launch_prepare_atoms(E, F, D, h->w.gate_s, out, st);
-    if (err == cudaSuccess) err = moe_launch_prepare_atoms(E, F, D, h->w.up_s, out + per, st);
-    if (err == cudaSuccess) err = moe_launch_prepare_atoms(E, D, F, h->w.down_s, out + 2 * per, st);
+    // gate/up tiles: 64 gate rows over the same 64 up rows; down tiles: 128 rows
+    cudaError_t err = moe_launch_prepare_atoms(E, F, D, 64, h->w.gate_s, h->w.up_s, out, st);
+    if (err == cudaSuccess)
+        err = moe_launch_prepare_atoms(E, D, F, 128, h->w.down_s, nullptr, out + 2 * per, st);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     h->atoms = out;
     return MOE_OK;

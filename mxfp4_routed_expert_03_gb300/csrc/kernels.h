@@ -42,15 +42,15 @@ cudaError_t moe_launch_finalize(int T, int D, const float *acc, uint16_t *out, c
 cudaError_t moe_launch_gather_x(int max_tt, int E, int k, int n_rows, int D, int ntmax,
                                 const int32_t *offsets, const int32_t *perm, const int32_t *active,
                                 const int32_t *tt_prefix, const uint8_t *q_hi, const uint8_t *q_lo,
-                                const uint8_t *s_hi, const uint8_t *s_lo, uint8_t *g_hi,
-                                uint8_t *g_lo, uint8_t *atoms_hi, uint8_t *atoms_lo, int *status,
-                                cudaStream_t st);
+                                const uint8_t *s_hi, const uint8_t *s_lo, uint8_t *tiles,
+                                uint8_t *atoms, int *status, cudaStream_t st);
 
 // grouped_gemm.cu
 #include <cuda.h>
 #define MOE_GEMM_GATEUP 0
 #define MOE_GEMM_DOWN 1
 #define MOE_GEMM_NTMAX 112
+#define MOE_GEMM_BTILE (2 * MOE_GEMM_NTMAX * 128)  // bytes of one activation B tile block
 
 struct MoeGemmArgs {
     int E, k, n_rows;        // experts, top-k, T*k
@@ -58,18 +58,20 @@ struct MoeGemmArgs {
     int Dout;                // row stride of the fp32 output accumulator (d_model)
     const int32_t *offsets, *perm, *active, *tt_prefix;
     const float *topk_w;
-    const uint8_t *a_atoms, *a2_atoms;  // weight scales as 512-byte atoms [E][M/128][K/128]
-    const uint8_t *b_atoms_hi, *b_atoms_lo;  // activation scale atoms [token tile][K/128]
-    uint8_t *h_hi, *h_lo;                    // GEMM1 outputs: h terms, slot order [T*k][M]
-    uint8_t *h_atoms_hi, *h_atoms_lo;        // GEMM1 outputs: h scale atoms [token tile][M/128]
+    const uint8_t *a_atoms;  // weight scale atoms [E][weight tiles][K/128][512 B]
+    const uint8_t *b_tiles;  // activation B tiles [token tile][K/128][2*NTMAX rows][128 B]:
+                             // rows [0, nmma) the hi term, [nmma, 2 nmma) the lo term,
+                             // each 128-byte row pre-swizzled (16-byte chunk c at c ^ row % 8)
+    const uint8_t *b_atoms;  // their scales [token tile][K/128][1 KB] (see bsf_off)
+    uint8_t *h_tiles;        // GEMM1 output: h as GEMM2's B tiles [token tile][M/128][...]
+    uint8_t *h_atoms;        // GEMM1 output: h scales [token tile][M/128][1 KB]
     float *acc;                        // GEMM2 output
     int *status;
     long long timeout_cycles;
 };
 
 size_t moe_gemm_smem_bytes(int mode);
-cudaError_t moe_launch_prepare_atoms(int E, int M, int K, const uint8_t *s, uint8_t *out,
-                                     cudaStream_t st);
+cudaError_t moe_launch_prepare_atoms(int E, int M, int K, int mrows, const uint8_t *s,
+                                     const uint8_t *s2, uint8_t *out, cudaStream_t st);
 cudaError_t moe_launch_gemm(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
-                            const CUtensorMap *mBhi, const CUtensorMap *mBlo,
                             const MoeGemmArgs *args, int grid, cudaStream_t st);

@@ -147,17 +147,23 @@ __device__ __forceinline__ bool token_tile(int tt, int n_active, const int32_t *
     return true;
 }
 
-// Copies the quantised activation rows of one token tile into plan (slot)
-// order and writes their scales as 512-byte tensor-core scale atoms, one per
-// 128-wide K chunk: row r of the tile, 32-wide block c of the chunk at byte
-// (r % 32) * 16 + (r / 32) * 4 + c.
+// Lays out the quantised activation rows of one token tile as the grouped
+// GEMM's B operand: for each 128-wide K chunk one block of 2 * NTMAX rows of
+// 128 bytes (row r = tile row r's hi term, row nmma + r = its lo term; nmma =
+// rows rounded up to 16), each row pre-swizzled for the 128-byte shared-memory
+// swizzle (16-byte chunk c stored at c ^ (row % 8)), so one contiguous bulk
+// copy per chunk lands a ready MMA tile. The scales go into a 1 KB block per
+// chunk: B row n, 32-wide block c at byte
+// (i / 8) * 256 + (j / 4) * 128 + (i % 8) * 16 + (j % 4) * 4 + c with
+// i = n % 32, j = n / 32 (32 lanes x 8 columns as tcgen05.cp.128x256b reads
+// K-major 8 x 16-byte core matrices).
 __global__ void __launch_bounds__(256) moe_gather_x_kernel(
     int E, int k, int n_rows, int D, const int32_t *__restrict__ offsets,
     const int32_t *__restrict__ perm, const int32_t *__restrict__ active,
     const int32_t *__restrict__ prefix, const uint8_t *__restrict__ q_hi,
     const uint8_t *__restrict__ q_lo, const uint8_t *__restrict__ s_hi,
-    const uint8_t *__restrict__ s_lo, uint8_t *__restrict__ g_hi, uint8_t *__restrict__ g_lo,
-    uint8_t *__restrict__ atoms_hi, uint8_t *__restrict__ atoms_lo, int *status) {
+    const uint8_t *__restrict__ s_lo, uint8_t *__restrict__ tiles, uint8_t *__restrict__ atoms,
+    int *status) {
     __shared__ int s_tok[MOE_GEMM_NTMAX];
     const int tt = blockIdx.x;
     int n_active = active[0];
@@ -171,33 +177,37 @@ __global__ void __launch_bounds__(256) moe_gather_x_kernel(
         s_tok[r] = fl / k;
     }
     __syncthreads();
-    const int chunks = D / 16;  // 16-byte chunks per row and term
-    for (int i = threadIdx.x; i < n * chunks; i += blockDim.x) {
-        const int r = i / chunks, c = i % chunks;
-        const size_t src = (size_t)s_tok[r] * D / 16 + c;
-        const size_t dst = (size_t)(sb + r0 + r) * D / 16 + c;
-        ((uint4 *)g_hi)[dst] = ((const uint4 *)q_hi)[src];
-        ((uint4 *)g_lo)[dst] = ((const uint4 *)q_lo)[src];
+    const int KC = D / 128, nmma = (n + 15) & ~15;
+    // 16-byte pieces: (row r, chunk kc, piece c) for hi and lo
+    for (int i = threadIdx.x; i < n * KC * 8; i += blockDim.x) {
+        const int r = i / (KC * 8), rem = i % (KC * 8), kc = rem / 8, c = rem % 8;
+        const size_t src = (size_t)s_tok[r] * D + kc * 128 + c * 16;
+        uint8_t *blk = tiles + ((size_t)tt * KC + kc) * MOE_GEMM_BTILE;
+        const int rl = nmma + r;
+        *(uint4 *)(blk + r * 128 + ((c ^ (r & 7)) * 16)) = *(const uint4 *)(q_hi + src);
+        *(uint4 *)(blk + rl * 128 + ((c ^ (rl & 7)) * 16)) = *(const uint4 *)(q_lo + src);
     }
-    const int nb = D / 32, KC = D / 128;
+    const int nb = D / 32;
+    auto off = [](int row, int c) {
+        const int i = row & 31, j = row >> 5;
+        return (i >> 3) * 256 + (j >> 2) * 128 + (i & 7) * 16 + (j & 3) * 4 + c;
+    };
     for (int i = threadIdx.x; i < n * nb; i += blockDim.x) {
-        const int r = i / nb, b = i % nb;
-        const size_t at = ((size_t)tt * KC + b / 4) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (b & 3);
-        atoms_hi[at] = s_hi[(size_t)s_tok[r] * nb + b];
-        atoms_lo[at] = s_lo[(size_t)s_tok[r] * nb + b];
+        const int r = i / nb, b = i % nb, c = b & 3;
+        const size_t at = ((size_t)tt * KC + b / 4) * 1024;
+        atoms[at + off(r, c)] = s_hi[(size_t)s_tok[r] * nb + b];
+        atoms[at + off(nmma + r, c)] = s_lo[(size_t)s_tok[r] * nb + b];
     }
 }
 
 cudaError_t moe_launch_gather_x(int max_tt, int E, int k, int n_rows, int D, int ntmax,
                                 const int32_t *offsets, const int32_t *perm, const int32_t *active,
                                 const int32_t *tt_prefix, const uint8_t *q_hi, const uint8_t *q_lo,
-                                const uint8_t *s_hi, const uint8_t *s_lo, uint8_t *g_hi,
-                                uint8_t *g_lo, uint8_t *atoms_hi, uint8_t *atoms_lo, int *status,
-                                cudaStream_t st) {
+                                const uint8_t *s_hi, const uint8_t *s_lo, uint8_t *tiles,
+                                uint8_t *atoms, int *status, cudaStream_t st) {
     (void)ntmax;
     moe_gather_x_kernel<<<max_tt, 256, 0, st>>>(E, k, n_rows, D, offsets, perm, active, tt_prefix,
-                                                q_hi, q_lo, s_hi, s_lo, g_hi, g_lo, atoms_hi,
-                                                atoms_lo, status);
+                                                q_hi, q_lo, s_hi, s_lo, tiles, atoms, status);
     return cudaGetLastError();
 }
 

@@ -175,6 +175,12 @@ __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t 
                  : "memory");
 }
 
+// 128 rows x 256 bits from smem (descriptor) into TMEM: row i -> lane i,
+// 8 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Each thread of the warp reads 16 consecutive 32-bit columns of its lane.
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
@@ -211,6 +217,18 @@ __device__ __forceinline__ uint64_t sdesc_plain_32x16(uint32_t saddr) {
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
     d |= (uint64_t)(128u >> 4) << 16;
     d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Descriptor of a plain (unswizzled) 128-row x 32-byte block for
+// tcgen05.cp.128x256b: K-major core matrices of 8 rows x 16 bytes, the two
+// 16-byte halves of a row 128 bytes apart, 8-row groups 256 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_plain_128x32(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128u >> 4) << 16;  // leading (K) byte offset
+    d |= (uint64_t)(256u >> 4) << 32;  // stride (row-group) byte offset
     d |= (uint64_t)1 << 46;
     return d;
 }
