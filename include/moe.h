@@ -89,7 +89,7 @@ enum moe_prof_kernel {
     MOE_PROF_FORWARD_GEMM2 = 4    /* moe_forward: grouped down GEMM + weighted scatter */
 };
 
-/* Layer shape. Supported envelope: d_model and d_ff multiples of 128,
+/* Layer shape. Supported envelope: d_model a multiple of 256, d_ff of 128,
  * d_model <= 16384, d_ff <= 8192, 1 <= top_k <= 32, top_k <= n_experts <= 1024. */
 typedef struct moe_desc {
     int32_t d_model;

@@ -127,7 +127,7 @@ MOE_API int moe_create(const moe_desc *d, const moe_weights *w, moe_handle **out
         return MOE_ERR_INVALID_ARG;
     if (d->has_shared != 0 && d->has_shared != 1) return MOE_ERR_INVALID_ARG;
     if (d->top_k > d->n_experts) return MOE_ERR_INVALID_ARG;
-    if (d->d_model % 128 || d->d_ff % 128 || d->d_model > MOE_MAX_DMODEL ||
+    if (d->d_model % 256 || d->d_ff % 128 || d->d_model > MOE_MAX_DMODEL ||
         d->d_ff > MOE_MAX_DFF || d->top_k > MOE_MAX_TOPK || d->n_experts > MOE_MAX_EXPERTS)
         return MOE_ERR_UNSUPPORTED;
     if (moe_decode_per_lane(d->d_model) == 0 || moe_decode_per_lane(d->d_ff) == 0)

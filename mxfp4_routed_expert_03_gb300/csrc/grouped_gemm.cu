@@ -23,6 +23,14 @@
 //     A tile (two 64-row TMA boxes), so one MMA per 32-wide K step covers
 //     gate and up; the epilogue pairs TMEM lanes r and 64 + r.
 //
+// CTAs run in clusters of CL = 2 on neighbouring SMs. The two CTAs of a
+// cluster take adjacent weight tiles of the same expert and token tile, so
+// they consume identical activation chunks: each CTA fetches half of every
+// chunk and multicasts it into both CTAs' shared memory, halving the L2
+// traffic of the activation operand; each CTA's MMA completion is multicast
+// to both CTAs' release barriers, so a stage is refilled only once both have
+// consumed it.
+//
 // One persistent CTA per SM, 7 warps:
 //   warp 0      weight producer (one thread): weight tile(s) by TMA (packed
 //               E2M1 expanded to the 8-bit MMA layout) and the prepared
@@ -54,6 +62,8 @@ constexpr int NUM_THREADS = 224;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 2 * NTMAX;  // [hi | lo] accumulator columns per buffer
 constexpr uint32_t SF_TMEM_COL = 448;     // scale atoms: 2 slots x (4 A + 8 B) columns
+constexpr int CL = MOE_GEMM_CLUSTER;      // CTAs per cluster sharing activation chunks
+constexpr uint16_t CL_MASK = (1u << CL) - 1;
 
 template <int MODE>
 struct Cfg {
@@ -90,27 +100,29 @@ struct Tile {
     int tt;     // global token-tile index (activation / h scale atoms)
 };
 
-// Tile `tile` of the schedule: active expert a owns MT * ntt(a) consecutive
-// tiles (weight tile major, token tile minor). s_prefix, s_expert and s_seg
-// are the shared-memory copies of the token-tile prefix, the active experts
-// and their (first slot, rows) segments.
-__device__ __forceinline__ bool tile_at(int tile, int n_active, int MT, const int *s_prefix,
-                                        const int *s_expert, const int2 *s_seg, Tile &t) {
+// Cluster tile `ct` of the schedule: active expert a owns MTG * ntt(a)
+// consecutive cluster tiles (weight tile group major, token tile minor); the
+// CTA of cluster rank `rank` takes weight tile mg * CL + rank of the group.
+// s_prefix, s_expert and s_seg are the shared-memory copies of the token-tile
+// prefix, the active experts and their (first slot, rows) segments.
+__device__ __forceinline__ bool tile_at(int ct, int n_active, int MTG, int rank,
+                                        const int *s_prefix, const int *s_expert,
+                                        const int2 *s_seg, Tile &t) {
     int lo = 0, hi = n_active - 1;
-    while (lo < hi) {  // last a with MT * prefix[a] <= tile
+    while (lo < hi) {  // last a with MTG * prefix[a] <= ct
         int mid = (lo + hi + 1) >> 1;
-        if (MT * s_prefix[mid] <= tile) lo = mid;
+        if (MTG * s_prefix[mid] <= ct) lo = mid;
         else hi = mid - 1;
     }
     const int a = lo;
     const int ntt = s_prefix[a + 1] - s_prefix[a];
     if (ntt <= 0 || s_expert[a] < 0) return false;
-    const int local = tile - MT * s_prefix[a];
-    const int m = local / ntt, j = local % ntt;
+    const int local = ct - MTG * s_prefix[a];
+    const int mg = local / ntt, j = local % ntt;
     const int2 seg = s_seg[a];
     const int r0 = (int)((long long)j * seg.y / ntt), r1 = (int)((long long)(j + 1) * seg.y / ntt);
     t.e = s_expert[a];
-    t.mt = m;
+    t.mt = mg * CL + rank;
     t.s0 = seg.x + r0;
     t.n = r1 - r0;
     t.nmma = (t.n + 15) & ~15;
@@ -186,7 +198,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
         }
         for (int s = 0; s < C::SB; ++s) {
             tc::mbar_init(&fullB[s], 1);
-            tc::mbar_init(&emptyB[s], 1);
+            tc::mbar_init(&emptyB[s], CL);  // released by every CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&tfull[b], 1);
@@ -200,10 +212,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
     }
     tc::tc_fence_before();
     __syncthreads();
+    tc::cluster_sync();  // peers' barriers are initialised before any multicast lands
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int MT = args.MT, KC = args.KC;
-    const int total_tiles = n_active > 0 ? s_prefix[n_active] * MT : 0;
+    const int MT = args.MT, KC = args.KC, MTG = MT / CL;
+    const int rank = (int)tc::cluster_ctarank();
+    const int cluster_id = blockIdx.x / CL, n_clusters = gridDim.x / CL;
+    const int total_tiles = n_active > 0 ? s_prefix[n_active] * MTG : 0;
     const long long LIMIT = args.timeout_cycles;
     volatile int *abort_p = abort_flag;
     auto fail = [&](void) {
@@ -217,9 +232,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
             const uint64_t pol_w = tc::policy_evict_first();
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+            for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
                 Tile t;
-                if (!tile_at(tile, n_active, MT, s_prefix, s_expert, s_seg, t)) {
+                if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, t)) {
                     moe_flag(args.status, MOE_ERR_BAD_INDEX);
                     continue;
                 }
@@ -248,9 +263,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
             const uint64_t pol_x = tc::policy_evict_last();
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+            for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
                 Tile t;
-                if (!tile_at(tile, n_active, MT, s_prefix, s_expert, s_seg, t)) continue;
+                if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, t)) continue;
                 const uint32_t tile_bytes = (uint32_t)(2 * t.nmma * BK);
                 const size_t blk0 = (size_t)t.tt * KC;
                 for (int kc = 0; kc < KC; ++kc, ++it) {
@@ -261,54 +276,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                         break;
                     }
                     unsigned char *st = smem + C::B_BASE + s * C::B_STAGE;
+                    // the whole chunk lands here; this CTA fetches its 1/CL share for all
                     tc::mbar_arrive_expect_tx(&fullB[s], tile_bytes + 4 * BSF_BYTES);
-                    tc::bulk_copy_g2s(st, args.b_tiles + (blk0 + kc) * MOE_GEMM_BTILE, tile_bytes,
-                                      &fullB[s], pol_x);
-                    for (int qd = 0; qd < 4; ++qd)  // one copy per TMEM lane quadrant
-                        tc::bulk_copy_g2s(st + C::B_SF + qd * BSF_BYTES,
-                                          args.b_atoms + (blk0 + kc) * BSF_BYTES, BSF_BYTES,
-                                          &fullB[s], pol_x);
+                    const uint32_t part = tile_bytes / CL;
+                    tc::bulk_copy_g2s_multicast(
+                        st + rank * part, args.b_tiles + (blk0 + kc) * MOE_GEMM_BTILE + rank * part,
+                        part, &fullB[s], CL_MASK, pol_x);
+                    for (int qd = rank; qd < 4; qd += CL)  // one copy per TMEM lane quadrant
+                        tc::bulk_copy_g2s_multicast(st + C::B_SF + qd * BSF_BYTES,
+                                                    args.b_atoms + (blk0 + kc) * BSF_BYTES,
+                                                    BSF_BYTES, &fullB[s], CL_MASK, pol_x);
                 }
             }
         }
     } else if (warp == 2) {
-        // ------------------------------------------ MMA issuer
-        int it = 0, lt = 0;
-        bool ok = true;
-        uint64_t *lastA = nullptr, *lastB = nullptr;
-        uint32_t parA = 0, parB = 0;
-        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-            Tile t;
-            if (!tile_at(tile, n_active, MT, s_prefix, s_expert, s_seg, t))
-                continue;
-            const int buf = lt & 1, use = lt >> 1;
-            ++lt;
-            if (use > 0 && !tc::mbar_wait(&tempty[buf], (use - 1) & 1, LIMIT, abort_p)) {
-                if (lane == 0) fail();
-                ok = false;
-                break;
-            }
-            tc::tc_fence_after();
-            const uint32_t acc = tmem + buf * ACC_COLS;
-            for (int kc = 0; kc < KC; ++kc, ++it) {
-                const int sa = it % C::SA, ra = it / C::SA;
-                const int sb = it % C::SB, rb = it / C::SB;
-                if (!tc::mbar_wait(&fullA[sa], ra & 1, LIMIT, abort_p) ||
-                    !tc::mbar_wait(&fullB[sb], rb & 1, LIMIT, abort_p)) {
-                    if (lane == 0) fail();
+        // ------------------------------------------ MMA issuer (one thread)
+        // The whole loop runs on one thread: reconverging the warp around every
+        // chunk's issue costs about as much as the chunk's MMAs themselves.
+        if (lane == 0) {
+            int it = 0, lt = 0;
+            bool ok = true;
+            uint64_t *lastA = nullptr, *lastB = nullptr;
+            uint32_t parA = 0, parB = 0;
+            for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
+                Tile t;
+                if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, t)) continue;
+                const int buf = lt & 1, use = lt >> 1;
+                ++lt;
+                if (use > 0 && !tc::mbar_wait(&tempty[buf], (use - 1) & 1, LIMIT, abort_p)) {
+                    fail();
                     ok = false;
                     break;
                 }
                 tc::tc_fence_after();
-                if (lane == 0) {
+                const uint32_t acc = tmem + buf * ACC_COLS;
+                for (int kc = 0; kc < KC; ++kc, ++it) {
+                    const int sa = it % C::SA, ra = it / C::SA;
+                    const int sb = it % C::SB, rb = it / C::SB;
+                    if (!tc::mbar_wait(&fullA[sa], ra & 1, LIMIT, abort_p) ||
+                        !tc::mbar_wait(&fullB[sb], rb & 1, LIMIT, abort_p)) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
                     unsigned char *sta = smem + sa * C::A_STAGE;
                     unsigned char *stb = smem + C::B_BASE + sb * C::B_STAGE;
                     const uint32_t sfa = tmem + SF_TMEM_COL + (uint32_t)(it & 1) * 12;
                     const uint32_t sfb = sfa + 4;
-                    const uint32_t sfa_s = tc::smem_u32(sta + C::A_SF);
-                    const uint32_t sfb_s = tc::smem_u32(stb + C::B_SF);
-                    tc::tmem_cp_32x128b_warpx4(sfa, tc::sdesc_plain_32x16(sfa_s));
-                    tc::tmem_cp_128x256b(sfb, tc::sdesc_plain_128x32(sfb_s));
+                    tc::tmem_cp_32x128b_warpx4(sfa, tc::sdesc_plain_32x16(tc::smem_u32(sta + C::A_SF)));
+                    tc::tmem_cp_128x256b(sfb, tc::sdesc_plain_128x32(tc::smem_u32(stb + C::B_SF)));
                     const uint32_t a_s = tc::smem_u32(sta), b_s = tc::smem_u32(stb);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -319,31 +335,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                                          (kc > 0 || k > 0) ? 1u : 0u);
                     }
                     tc::mma_commit(&emptyA[sa]);
-                    tc::mma_commit(&emptyB[sb]);
+                    tc::mma_commit_multicast(&emptyB[sb], CL_MASK);  // every CTA's copy is free
+                    lastA = &emptyA[sa];
+                    parA = ra & 1;
+                    lastB = &emptyB[sb];
+                    parB = rb & 1;
                 }
-                __syncwarp();
-                lastA = &emptyA[sa];
-                parA = ra & 1;
-                lastB = &emptyB[sb];
-                parB = rb & 1;
+                if (!ok) break;
+                tc::mma_commit(&tfull[buf]);
             }
-            if (!ok) break;
-            if (lane == 0) tc::mma_commit(&tfull[buf]);
-            __syncwarp();
+            // the last stage releases must land before the CTA can exit
+            if (ok && lastA &&
+                (!tc::mbar_wait(lastA, parA, LIMIT, abort_p) || !tc::mbar_wait(lastB, parB, LIMIT, abort_p)))
+                fail();
         }
-        // the last stage releases must land before the CTA can exit
-        if (ok && lastA &&
-            (!tc::mbar_wait(lastA, parA, LIMIT, abort_p) || !tc::mbar_wait(lastB, parB, LIMIT, abort_p))) {
-            if (lane == 0) fail();
-        }
+        __syncwarp();
     } else {
         // ------------------------------------------ epilogue (warps 3..6)
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         int lt = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        for (int tile = cluster_id; tile < total_tiles; tile += n_clusters) {
             Tile t;
-            if (!tile_at(tile, n_active, MT, s_prefix, s_expert, s_seg, t))
+            if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, t))
                 continue;
             const int buf = lt & 1, use = lt >> 1;
             ++lt;
@@ -456,6 +470,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, TMEM_COLS);
     }
+    tc::cluster_sync();  // no CTA leaves while a peer may still multicast into it
 }
 
 // Weight scales re-laid as 512-byte tensor-core scale atoms, one per
@@ -499,20 +514,43 @@ cudaError_t moe_launch_prepare_atoms(int E, int M, int K, int mrows, const uint8
     return cudaGetLastError();
 }
 
+namespace {
+template <int MODE>
+cudaError_t launch_clustered(const CUtensorMap *mA, const CUtensorMap *mA2,
+                             const MoeGemmArgs *args, int max_ctas, cudaStream_t st) {
+    auto kern = moe_grouped_gemm_kernel<MODE>;
+    const size_t sm = Cfg<MODE>::SMEM;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = sm;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static int clusters[2] = {0, 0};  // co-resident clusters, per mode
+    if (!clusters[MODE]) {
+        cfg.gridDim = dim3(max_ctas / CL * CL);
+        int n = 0;
+        err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (err != cudaSuccess) return err;
+        clusters[MODE] = n > 0 ? n : 1;
+    }
+    int grid = clusters[MODE] * CL;
+    if (grid > max_ctas / CL * CL) grid = max_ctas / CL * CL;
+    cfg.gridDim = dim3(grid);
+    return cudaLaunchKernelEx(&cfg, kern, *mA, *mA2, *args);
+}
+}  // namespace
+
 cudaError_t moe_launch_gemm(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
                             const MoeGemmArgs *args, int grid, cudaStream_t st) {
-    size_t sm = moe_gemm_smem_bytes(mode);
-    cudaError_t err;
-    if (mode == MOE_GEMM_GATEUP) {
-        err = cudaFuncSetAttribute(moe_grouped_gemm_kernel<MOE_GEMM_GATEUP>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        if (err != cudaSuccess) return err;
-        moe_grouped_gemm_kernel<MOE_GEMM_GATEUP><<<grid, NUM_THREADS, sm, st>>>(*mA, *mA2, *args);
-    } else {
-        err = cudaFuncSetAttribute(moe_grouped_gemm_kernel<MOE_GEMM_DOWN>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        if (err != cudaSuccess) return err;
-        moe_grouped_gemm_kernel<MOE_GEMM_DOWN><<<grid, NUM_THREADS, sm, st>>>(*mA, *mA, *args);
-    }
-    return cudaGetLastError();
+    if (args->MT % CL) return cudaErrorInvalidValue;
+    return mode == MOE_GEMM_GATEUP ? launch_clustered<MOE_GEMM_GATEUP>(mA, mA2, args, grid, st)
+                                   : launch_clustered<MOE_GEMM_DOWN>(mA, mA2, args, grid, st);
 }

@@ -50,6 +50,7 @@ cudaError_t moe_launch_gather_x(int max_tt, int E, int k, int n_rows, int D, int
 #define MOE_GEMM_GATEUP 0
 #define MOE_GEMM_DOWN 1
 #define MOE_GEMM_NTMAX 112
+#define MOE_GEMM_CLUSTER 2  // CTAs per cluster sharing the activation operand
 #define MOE_GEMM_BTILE (2 * MOE_GEMM_NTMAX * 128)  // bytes of one activation B tile block
 
 struct MoeGemmArgs {
