@@ -185,6 +185,24 @@ int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf 
 int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
                uint16_t *out, void *ws, size_t ws_bytes, void *stream);
 
+/* moe_decode without any device allocation, for callers that cannot call
+ * cudaMalloc (for example code running where the allocator is owned by
+ * someone else, or which must not allocate after start-up). No passage of the
+ * pages describes this entry point; it is an interface convenience with no
+ * counterpart there.
+ * The scratch moe_decode takes from `ws` lives instead in one fixed array
+ * inside the library (a static device array of about 9.5 MB that every GPU
+ * which loads the library holds until the process exits). It fits T * top_k
+ * <= 256 routed rows for d_ff <= 2048 and d_model <= 8192; larger calls
+ * return MOE_ERR_WORKSPACE. The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress), so make that first call before any
+ * stream capture. All calls share the array: calls whose kernels overlap on
+ * the GPU (other streams, other threads) race on it and must be serialised by
+ * the caller. Same inputs, outputs and results as moe_decode; the plan comes
+ * from moe_plan, which needs no workspace for T <= 64. */
+int moe_decode_noalloc(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
+                       uint16_t *out, void *stream);
+
 /* Host. Instrumentation for timing one kernel on the library's own stream:
  * while `which` names a kernel (enum moe_prof_kernel), every later call that
  * launches it records ev_start (a cudaEvent_t) immediately before that launch

@@ -34,8 +34,8 @@ MOE_OP_DECODE = 2
 
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_create", "moe_destroy", "moe_expert_bytes", "moe_prepared_bytes", "moe_prepare",
-           "moe_workspace_bytes", "moe_plan", "moe_forward", "moe_decode", "moe_profile_kernel",
-           "moe_status", "moe_strerror")
+           "moe_workspace_bytes", "moe_plan", "moe_forward", "moe_decode", "moe_decode_noalloc",
+           "moe_profile_kernel", "moe_status", "moe_strerror")
 
 MOE_PROF_NONE = 0
 MOE_PROF_DECODE_GATEUP = 1
@@ -97,6 +97,8 @@ def lib() -> ctypes.CDLL:
         for fn in (L.moe_forward, L.moe_decode):
             fn.argtypes = [p, i32, p, ctypes.POINTER(moe_plan_buf), p, p, sz, p]
             fn.restype = ctypes.c_int
+        L.moe_decode_noalloc.argtypes = [p, i32, p, ctypes.POINTER(moe_plan_buf), p, p]
+        L.moe_decode_noalloc.restype = ctypes.c_int
         L.moe_profile_kernel.argtypes = [p, i32, p, p]
         L.moe_profile_kernel.restype = ctypes.c_int
         L.moe_status.argtypes = [p, p]
@@ -178,6 +180,11 @@ def moe_profile_kernel(h, which: int, ev_start=None, ev_stop=None) -> int:
             return e
         return e.cuda_event
     return lib().moe_profile_kernel(h, which, raw(ev_start), raw(ev_stop))
+
+
+def moe_decode_noalloc(h, T, x, plan: moe_plan_buf, out, stream=None) -> int:
+    """moe_decode with the library's fixed scratch (no workspace argument)."""
+    return lib().moe_decode_noalloc(h, T, _ptr(x), ctypes.byref(plan), _ptr(out), _stream(stream))
 
 
 def moe_status(h, stream=None) -> int:

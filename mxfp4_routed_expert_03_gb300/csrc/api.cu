@@ -234,6 +234,27 @@ MOE_API int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_pl
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+MOE_API int moe_decode_noalloc(moe_handle *h, int32_t T, const uint16_t *x,
+                               const moe_plan_buf *plan, uint16_t *out, void *stream) {
+    if (!h || T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !out || !plan_ok(plan)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    const moe_desc &d = h->desc;
+    if ((int64_t)T * d.top_k > MOE_NOALLOC_MAX_ROWS || d.d_ff > MOE_NOALLOC_MAX_DFF ||
+        d.d_model > MOE_NOALLOC_MAX_DMODEL ||
+        moe_decode_ws_bytes(T, d.d_model, d.d_ff, d.top_k) > moe_noalloc_scratch_bytes())
+        return MOE_ERR_WORKSPACE;  // beyond the fixed scratch
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev != h->device) return MOE_ERR_INVALID_ARG;
+    void *scratch = nullptr;
+    if (moe_noalloc_scratch(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaError_t err = moe_launch_decode(T, d.d_model, d.d_ff, d.n_experts, d.top_k, x, plan, &h->w,
+                                        out, scratch, h->status, h->prof, (cudaStream_t)stream);
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
                         uint16_t *out, void *ws, size_t ws_bytes, void *stream) {
     if (!h || T < 0) return MOE_ERR_INVALID_ARG;

@@ -33,6 +33,13 @@ cudaError_t moe_launch_decode(int T, int D, int F, int E, int k, const uint16_t 
                               const moe_plan_buf *p, const moe_weights *w, uint16_t *out,
                               void *ws, int *status, const MoeProf &prof, cudaStream_t st);
 
+// noalloc.cu: fixed scratch of moe_decode_noalloc
+#define MOE_NOALLOC_MAX_ROWS 256     // tokens x top_k
+#define MOE_NOALLOC_MAX_DFF 2048
+#define MOE_NOALLOC_MAX_DMODEL 8192
+size_t moe_noalloc_scratch_bytes();
+cudaError_t moe_noalloc_scratch(void **ptr);
+
 // quant.cu
 cudaError_t moe_launch_quant_x(int T, int D, const uint16_t *x, uint8_t *q_hi, uint8_t *q_lo,
                                uint8_t *s_hi, uint8_t *s_lo, cudaStream_t st);
