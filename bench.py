@@ -5,7 +5,9 @@ Default workload: one K3-shaped routed layer (d_model 7168, d_ff 1536, 896
 experts, top-16, MXFP4 weights resident in HBM), decode batches of T = 1, 4
 and 16 tokens; one step = moe_plan + moe_decode for each of the three
 batches (21 tokens). `--workload prefill4k|skewed8k` times moe_plan +
-moe_forward on one prefill batch instead.
+moe_forward on one prefill batch instead; `--workload router16k` times the
+long prefill whose logits come from the library's own fp32 router (x . W_r)
+and which adds one bf16 shared expert.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -45,6 +47,9 @@ BENCH_WORKLOADS = {
                   "desc": "K3 routed layer prefill, T=4096, uniform routing"},
     "skewed8k": {"Ts": [8192], "path": "forward",
                  "desc": "K3 routed layer prefill, T=8192, Zipf(1.1)-skewed routing"},
+    "router16k": {"Ts": [16384], "path": "forward", "router": True, "sets": 2,
+                  "desc": "K3 routed layer long prefill, T=16384, in-library fp32 router "
+                          "(x . W_r) + one bf16 shared expert"},
 }
 
 
@@ -82,8 +87,9 @@ def oracle_tokens_per_s(workload_name: str, budget_s: float):
     while True:
         T = wl["Ts"][it % len(wl["Ts"])]
         w = synth.Workload(base.name, T=T, D=base.D, F=base.F, E=base.E, k=base.k, seed=base.seed,
-                           zipf_s=base.zipf_s)
-        x, lg = synth.make_x(w, it % N_SETS), synth.make_logits(w, it % N_SETS)
+                           zipf_s=base.zipf_s, router=base.router, shared=base.shared)
+        x = synth.make_x(w, it % N_SETS)
+        lg = None if w.router == "xwr" else synth.make_logits(w, it % N_SETS)
         reference(w, x, lg, tokens=[it % T])
         done += 1
         it += 1
@@ -202,8 +208,10 @@ def run_ours(args):
     import numpy as np
     import torch
     import synth
+    import mxfp4_routed_expert_03_gb300 as moe
     from mxfp4_routed_expert_03_gb300 import (MOE_PROF_DECODE_GATEUP, MOE_PROF_FORWARD_GEMM1,
-                                              MOE_PROF_NONE, check, moe_profile_kernel)
+                                              MOE_PROF_NONE, MOE_ROUTER_XWR, check,
+                                              moe_profile_kernel)
     from mxfp4_routed_expert_03_gb300.layer import Layer, Plan, alloc_weights
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -226,18 +234,28 @@ def run_ours(args):
     synth.dev_fill_layer(base.seed, N_EXPERTS, D_MODEL, D_FF,
                          {k: v.data_ptr() for k, v in weights.items()},
                          torch.cuda.current_stream().cuda_stream)
-    layer = Layer(D_MODEL, D_FF, N_EXPERTS, TOP_K, weights)
-    if path == "forward":
+    use_router = bool(wl.get("router"))
+    n_sets = wl.get("sets", N_SETS)
+    if use_router:
+        w_router = torch.from_numpy(synth.make_w_router(base)).to(dev)
+        shared = {k: torch.from_numpy(v.view(np.int16)).to(dev)
+                  for k, v in synth.make_shared(base).items()}
+        layer = Layer(D_MODEL, D_FF, N_EXPERTS, TOP_K, weights, MOE_ROUTER_XWR, w_router, shared)
+    else:
+        layer = Layer(D_MODEL, D_FF, N_EXPERTS, TOP_K, weights)
+    if path == "forward" or use_router:
         layer.prepare()
     stream = torch.cuda.current_stream()
 
-    # inputs: N_SETS seeded (x, logits) sets per batch size, resident in HBM
+    # inputs: seeded (x, logits) sets per batch size, resident in HBM (x only
+    # when the library computes the logits)
     batches = []
     for T in wl["Ts"]:
         w = synth.Workload(base.name, T=T, D=D_MODEL, F=D_FF, E=N_EXPERTS, k=TOP_K,
                            seed=base.seed, zipf_s=base.zipf_s)
-        xs_h = [synth.make_x(w, rank * 97 + i) for i in range(N_SETS)]
-        ls_h = [synth.make_logits(w, rank * 97 + i) for i in range(N_SETS)]
+        xs_h = [synth.make_x(w, rank * 97 + i) for i in range(n_sets)]
+        ls_h = [np.zeros((T, N_EXPERTS), np.float32) if use_router else
+                synth.make_logits(w, rank * 97 + i) for i in range(n_sets)]
         xs = [torch.from_numpy(a.view(np.int16)).to(dev) for a in xs_h]
         ls = [torch.from_numpy(a).to(dev) for a in ls_h]
         pin_x = [torch.from_numpy(a.view(np.int16)).pin_memory() for a in xs_h]
@@ -253,19 +271,23 @@ def run_ours(args):
     run = layer.decode if path == "decode" else layer.forward
     prof_kind = MOE_PROF_DECODE_GATEUP if path == "decode" else MOE_PROF_FORWARD_GEMM1
 
-    def step(i, events=None, e2e=False):
+    def step(i, events=None, e2e=False, prof_kind=prof_kind):
         for bi, b in enumerate(batches):
-            s = i % N_SETS
+            s = i % n_sets
             if events is not None:
                 ev0, ev1 = events[bi]
                 check(moe_profile_kernel(layer.h, prof_kind, ev0, ev1), "profile")
             if e2e:
                 b["dx"].copy_(b["px"][s], non_blocking=True)
-                b["dl"].copy_(b["pl"][s], non_blocking=True)
+                if not use_router:
+                    b["dl"].copy_(b["pl"][s], non_blocking=True)
                 x, lg = b["dx"], b["dl"]
             else:
                 x, lg = b["x"][s], b["l"][s]
-            check(layer.plan(b["T"], lg, None, b["plan"], stream), "moe_plan")
+            if use_router:
+                check(layer.plan(b["T"], None, x, b["plan"], stream), "moe_plan")
+            else:
+                check(layer.plan(b["T"], lg, None, b["plan"], stream), "moe_plan")
             check(run(b["T"], x, b["plan"], b["out"], stream), "moe_" + path)
             if e2e:
                 b["hout"].copy_(b["out"], non_blocking=True)
@@ -321,6 +343,28 @@ def run_ours(args):
     if dist is not None:
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
     elapsed_ms, e2e_ms = times.tolist()
+
+    # per-kernel breakdown (separate untimed pass, one kernel bracketed at a time)
+    breakdown = {}
+    kinds = ([("decode_gateup", moe.MOE_PROF_DECODE_GATEUP), ("decode_down", moe.MOE_PROF_DECODE_DOWN)]
+             if path == "decode" else
+             [("gemm1_gateup", moe.MOE_PROF_FORWARD_GEMM1), ("gemm2_down", moe.MOE_PROF_FORWARD_GEMM2)])
+    if use_router:
+        kinds += [("router", moe.MOE_PROF_ROUTER), ("shared_gateup", moe.MOE_PROF_SHARED_GATEUP),
+                  ("shared_down", moe.MOE_PROF_SHARED_DOWN)]
+    n_bd = min(args.steps, 5)
+    for name, kid in kinds:
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_b)] for _ in range(n_bd)]
+        for row in ev:
+            for a, b in row:
+                a.record()
+                b.record()
+        for i in range(n_bd):
+            step(i, events=ev[i], prof_kind=kid)
+        torch.cuda.synchronize()
+        breakdown[name] = float(np.mean([a.elapsed_time(b) for row in ev for (a, b) in row]))
+    check(moe_profile_kernel(layer.h, MOE_PROF_NONE), "profile")
     tokens_step = sum(wl["Ts"])
     value = world * tokens_step * args.steps / (elapsed_ms * 1e-3)
     e2e_value = world * tokens_step * args.steps / (e2e_ms * 1e-3)
@@ -357,21 +401,28 @@ def run_ours(args):
                 if "bf16_tflops" in peaks else "fallback",
                 "traffic": kernel_traffic("moe_grouped_gemm_kernel<0>", "grouped_gemm.cu")}
 
+    # plan: one fused kernel for T <= 64, else top-k, count, scan, scatter;
+    # decode: gate/up, down, combine; forward: quant, schedule, gather, two GEMMs, finalize
     launches_per_call = 1 if max(wl["Ts"]) <= 64 else 4
-    launches_per_call += 4 if path == "decode" else 6
+    launches_per_call += 3 if path == "decode" else 6
+    if use_router:
+        launches_per_call += 1 + 2   # router GEMM; shared gate/up and down GEMMs
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "mxfp4 x f16 -> f32" if path == "decode" else "mxfp4 x 2-term e4m3 -> f32",
         "data": "synthetic (seeded Philox weights, N(0,1) activations and logits)",
-        "config": {"workload": wl["desc"], "path": "moe_plan + moe_" + path,
+        "config": {"workload": wl["desc"],
+                   "path": ("moe_plan (router) + moe_" if use_router else "moe_plan + moe_") + path,
                    "tokens_per_step": tokens_step, "active_experts_last_step": act,
+                   "kernel_ms_per_call": breakdown,
                    "l2": "inputs larger than L2 (>=280 MB of expert weights per batch, "
                          "8 rotating logit sets)", "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "tokens/s",
-                "h2d_bytes_per_step": sum(T * D_MODEL * 2 + T * N_EXPERTS * 4 for T in wl["Ts"]),
+                "h2d_bytes_per_step": sum(T * D_MODEL * 2 + (0 if use_router else T * N_EXPERTS * 4)
+                                          for T in wl["Ts"]),
                 "d2h_bytes_per_step": sum(T * D_MODEL * 2 for T in wl["Ts"])},
         "gpu_launches": launches_per_call * len(wl["Ts"]) * args.steps,
         "clocks": clocks,

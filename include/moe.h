@@ -86,7 +86,10 @@ enum moe_prof_kernel {
     MOE_PROF_DECODE_GATEUP = 1,   /* moe_decode: gate/up + SwiGLU streaming kernel */
     MOE_PROF_DECODE_DOWN = 2,     /* moe_decode: down-projection streaming kernel */
     MOE_PROF_FORWARD_GEMM1 = 3,   /* moe_forward: grouped gate/up GEMM */
-    MOE_PROF_FORWARD_GEMM2 = 4    /* moe_forward: grouped down GEMM + weighted scatter */
+    MOE_PROF_FORWARD_GEMM2 = 4,   /* moe_forward: grouped down GEMM + weighted scatter */
+    MOE_PROF_ROUTER = 5,          /* moe_plan / moe_router_logits: x . W_r GEMM */
+    MOE_PROF_SHARED_GATEUP = 6,   /* shared expert: gate/up GEMM + SwiGLU */
+    MOE_PROF_SHARED_DOWN = 7      /* shared expert: down GEMM */
 };
 
 /* Layer shape. Supported envelope: d_model a multiple of 256, d_ff of 128,
@@ -146,7 +149,10 @@ void moe_destroy(moe_handle *h);
 int64_t moe_expert_bytes(int32_t d_model, int32_t d_ff);
 
 /* Host. Bytes of the buffer moe_prepare fills: the three weight-scale arrays
- * (3 * n_experts * d_model * d_ff / 32 bytes, 924 MB for the 896-expert K3 layer). */
+ * (3 * n_experts * d_model * d_ff / 32 bytes, 924 MB for the 896-expert K3
+ * layer, rounded up to 256) plus, for router_mode MOE_ROUTER_XWR, three bf16
+ * copies of W_r's shape (3 * n_experts * d_model * 2 bytes, each rounded up to
+ * 256; 38.5 MB for K3). */
 size_t moe_prepared_bytes(const moe_handle *h);
 
 /* One-time weight-layout preparation for moe_forward (asynchronous on
@@ -157,22 +163,45 @@ size_t moe_prepared_bytes(const moe_handle *h);
  * least moe_prepared_bytes(h) bytes, 256-byte aligned; the handle keeps the
  * pointer, so it must outlive the handle, and the weight scales must not
  * change afterwards without calling moe_prepare again. moe_decode does not
- * need it; moe_forward returns MOE_ERR_NOT_PREPARED without it. */
+ * need it; moe_forward returns MOE_ERR_NOT_PREPARED without it.
+ * For router_mode MOE_ROUTER_XWR it also splits W_r into three bf16 terms
+ * t0 + t1 + t2 == W_r exactly (t0 the round-to-nearest bf16 of W_r, t1 of the
+ * remainder, t2 of what is left), which the router GEMM reads; moe_plan and
+ * moe_router_logits return MOE_ERR_NOT_PREPARED without it, and w_router must
+ * not change afterwards without calling moe_prepare again. */
 int moe_prepare(moe_handle *h, void *buf, size_t bytes, void *stream);
 
-/* Host. Scratch bytes `op` (enum moe_op) needs for T tokens; 0 for T == 0. */
+/* Host. Scratch bytes `op` (enum moe_op) needs for T tokens; 0 for T == 0.
+ * MOE_OP_PLAN includes the fp32 logits [T][E] for router_mode MOE_ROUTER_XWR;
+ * MOE_OP_DECODE and MOE_OP_FORWARD include the shared expert's intermediate
+ * (bf16 [T][d_ff], and for decode its fp32 output [T][d_model]) when
+ * has_shared is set. */
 size_t moe_workspace_bytes(const moe_handle *h, int32_t T, int32_t op);
 
 /* Route T tokens: top-k + weights, then the stable per-expert plan.
- * logits: fp32 [T][E] (MOE_ROUTER_LOGITS; x may be NULL) or NULL with x given
- * (MOE_ROUTER_XWR). ws: >= moe_workspace_bytes(h, T, MOE_OP_PLAN).
- * T == 0 is a no-op returning MOE_OK. */
+ * MOE_ROUTER_LOGITS: logits fp32 [T][E] given, x ignored (may be NULL).
+ * MOE_ROUTER_XWR: logits must be NULL and x given (16-byte aligned); the
+ * logits are first computed as in moe_router_logits into the front of ws
+ * (requires moe_prepare). ws: >= moe_workspace_bytes(h, T, MOE_OP_PLAN),
+ * 256-byte aligned when that is non-zero. T == 0 is a no-op returning MOE_OK. */
 int moe_plan(moe_handle *h, int32_t T, const float *logits, const uint16_t *x,
              const moe_plan_buf *plan, void *ws, size_t ws_bytes, void *stream);
 
+/* The router alone (router_mode MOE_ROUTER_XWR): logits fp32 [T][E] =
+ * x . W_r^T with fp32 accumulation, on tensor cores as three bf16 GEMMs
+ * against the W_r terms moe_prepare made (so every product is exact and only
+ * the fp32 accumulation rounds). The router is part of the resident static
+ * tier (Moonshine README, "How the engine works"). x bf16 [T][d_model],
+ * 16-byte aligned; logits caller-owned, 4-byte aligned. No workspace.
+ * Returns MOE_ERR_INVALID_ARG for router_mode MOE_ROUTER_LOGITS and
+ * MOE_ERR_NOT_PREPARED before moe_prepare. */
+int moe_router_logits(moe_handle *h, int32_t T, const uint16_t *x, float *logits, void *stream);
+
 /* Layer-major expert FFN for a planned batch (prefill): grouped block-scaled
  * MXFP4 GEMMs on tcgen05 tensor cores (gate/up with SwiGLU, then down with
- * the weighted scatter), finalised to bf16 out [T][d_model].
+ * the weighted scatter), finalised to bf16 out [T][d_model]. With has_shared
+ * the shared expert (bf16 tensor-core GEMMs, SwiGLU, weight 1.0) is added
+ * before the bf16 rounding.
  * Requires moe_prepare. ws: >= moe_workspace_bytes(h, T, MOE_OP_FORWARD),
  * 256-byte aligned. */
 int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
@@ -180,7 +209,8 @@ int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf 
 
 /* Token-major expert FFN (decode, any T; intended for T <= 16): streams only
  * the active experts' packed codes with 128-bit loads and reduces on CUDA
- * cores in fp32, then combines deterministically in top-k order.
+ * cores in fp32, then combines deterministically in top-k order (the shared
+ * expert's output, with has_shared, added last).
  * ws: >= moe_workspace_bytes(h, T, MOE_OP_DECODE). */
 int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
                uint16_t *out, void *ws, size_t ws_bytes, void *stream);
@@ -199,7 +229,9 @@ int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *
  * stream capture. All calls share the array: calls whose kernels overlap on
  * the GPU (other streams, other threads) race on it and must be serialised by
  * the caller. Same inputs, outputs and results as moe_decode; the plan comes
- * from moe_plan, which needs no workspace for T <= 64. */
+ * from moe_plan, which needs no workspace for T <= 64 with router_mode
+ * MOE_ROUTER_LOGITS. Layers with has_shared return MOE_ERR_UNSUPPORTED (the
+ * fixed array has no room for the shared expert's intermediates). */
 int moe_decode_noalloc(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
                        uint16_t *out, void *stream);
 

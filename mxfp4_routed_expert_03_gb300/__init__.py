@@ -34,7 +34,8 @@ MOE_OP_DECODE = 2
 
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_create", "moe_destroy", "moe_expert_bytes", "moe_prepared_bytes", "moe_prepare",
-           "moe_workspace_bytes", "moe_plan", "moe_forward", "moe_decode", "moe_decode_noalloc",
+           "moe_workspace_bytes", "moe_plan", "moe_router_logits", "moe_forward", "moe_decode",
+           "moe_decode_noalloc",
            "moe_profile_kernel", "moe_status", "moe_strerror")
 
 MOE_PROF_NONE = 0
@@ -42,6 +43,9 @@ MOE_PROF_DECODE_GATEUP = 1
 MOE_PROF_DECODE_DOWN = 2
 MOE_PROF_FORWARD_GEMM1 = 3
 MOE_PROF_FORWARD_GEMM2 = 4
+MOE_PROF_ROUTER = 5
+MOE_PROF_SHARED_GATEUP = 6
+MOE_PROF_SHARED_DOWN = 7
 
 
 class moe_desc(ctypes.Structure):
@@ -94,6 +98,8 @@ def lib() -> ctypes.CDLL:
         L.moe_workspace_bytes.restype = sz
         L.moe_plan.argtypes = [p, i32, p, p, ctypes.POINTER(moe_plan_buf), p, sz, p]
         L.moe_plan.restype = ctypes.c_int
+        L.moe_router_logits.argtypes = [p, i32, p, p, p]
+        L.moe_router_logits.restype = ctypes.c_int
         for fn in (L.moe_forward, L.moe_decode):
             fn.argtypes = [p, i32, p, ctypes.POINTER(moe_plan_buf), p, p, sz, p]
             fn.restype = ctypes.c_int
@@ -161,6 +167,10 @@ def moe_workspace_bytes(h: int, T: int, op: int) -> int:
 def moe_plan(h, T, logits, x, plan: moe_plan_buf, ws, ws_bytes, stream=None) -> int:
     return lib().moe_plan(h, T, _ptr(logits), _ptr(x), ctypes.byref(plan), _ptr(ws), ws_bytes,
                           _stream(stream))
+
+
+def moe_router_logits(h, T, x, logits, stream=None) -> int:
+    return lib().moe_router_logits(h, T, _ptr(x), _ptr(logits), _stream(stream))
 
 
 def moe_forward(h, T, x, plan: moe_plan_buf, out, ws, ws_bytes, stream=None) -> int:

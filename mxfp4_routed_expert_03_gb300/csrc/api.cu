@@ -15,7 +15,10 @@ struct moe_handle {
     int num_sms;
     int *status;  // device word: first error code recorded by a kernel
     CUtensorMap map_gate, map_up, map_down;  // TMA views of the packed E2M1 weights
+    CUtensorMap map_sh_gate, map_sh_up, map_sh_down;  // bf16 shared expert (has_shared)
+    CUtensorMap map_wr[3];  // the three bf16 terms of W_r (router_mode XWR, after prepare)
     const uint8_t *atoms;  // caller buffer filled by moe_prepare (NULL until then)
+    bool wr_ready;         // W_r terms written by moe_prepare
     MoeProf prof;          // optional timing events (moe_profile_kernel)
 };
 
@@ -63,11 +66,11 @@ static bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base
 // their scale blocks, h as the down GEMM's B tiles and its scale blocks, the
 // fp32 output accumulator and the token-tile schedule.
 struct FwdLayout {
-    size_t xq_hi, xq_lo, xs_hi, xs_lo, xb, xa, hb, ha, acc, prefix, total;
+    size_t xq_hi, xq_lo, xs_hi, xs_lo, xb, xa, hb, ha, acc, prefix, hsh, total;
     int max_tt;
 };
 
-static FwdLayout fwd_layout(int T, int D, int F, int E, int k) {
+static FwdLayout fwd_layout(int T, int D, int F, int E, int k, bool shared) {
     FwdLayout L;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -88,8 +91,17 @@ static FwdLayout fwd_layout(int T, int D, int F, int E, int k) {
     L.ha = take((size_t)L.max_tt * (F / 128) * 1024);
     L.acc = take((size_t)T * D * sizeof(float));
     L.prefix = take((size_t)(E + 1) * sizeof(int32_t));
+    L.hsh = take(shared ? (size_t)T * F * 2 : 0);  // shared expert's bf16 h [T][F]
     L.total = off;
     return L;
+}
+
+// TMA view of a row-major bf16 matrix [rows][cols]: boxes of 64 columns
+// (one 128-byte swizzled row) x box_rows rows.
+static bool make_map_bf16(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
+                          uint32_t box_rows) {
+    return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, cols, rows, cols * 2, 64,
+                       box_rows);
 }
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -139,7 +151,9 @@ MOE_API int moe_create(const moe_desc *d, const moe_weights *w, moe_handle **out
         return MOE_ERR_INVALID_ARG;  // TMA of packed E2M1 needs 32-byte aligned bases
     if (d->router_mode == MOE_ROUTER_XWR && !w->w_router) return MOE_ERR_INVALID_ARG;
     if (d->has_shared && (!w->sh_gate || !w->sh_up || !w->sh_down)) return MOE_ERR_INVALID_ARG;
-    if (d->router_mode == MOE_ROUTER_XWR || d->has_shared) return MOE_ERR_UNSUPPORTED;
+    if (d->has_shared && ((uintptr_t)w->sh_gate | (uintptr_t)w->sh_up | (uintptr_t)w->sh_down) & 15u)
+        return MOE_ERR_INVALID_ARG;  // TMA bases must be 16-byte aligned
+    if (d->router_mode == MOE_ROUTER_XWR && ((uintptr_t)w->w_router & 3u)) return MOE_ERR_INVALID_ARG;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -167,6 +181,13 @@ MOE_API int moe_create(const moe_desc *d, const moe_weights *w, moe_handle **out
             free(h);
             return MOE_ERR_CUDA;
         }
+        if (d->has_shared &&
+            (!make_map_bf16(&h->map_sh_gate, w->sh_gate, D, F, 64) ||
+             !make_map_bf16(&h->map_sh_up, w->sh_up, D, F, 64) ||
+             !make_map_bf16(&h->map_sh_down, w->sh_down, F, D, 128))) {
+            free(h);
+            return MOE_ERR_CUDA;
+        }
     }
     if (cudaMalloc(&h->status, sizeof(int)) != cudaSuccess) {
         free(h);
@@ -187,14 +208,90 @@ MOE_API void moe_destroy(moe_handle *h) {
     free(h);
 }
 
+// Router logits region at the front of moe_plan's workspace (router_mode XWR).
+static size_t router_ws_bytes(const moe_handle *h, int T) {
+    if (h->desc.router_mode != MOE_ROUTER_XWR) return 0;
+    return align_up((size_t)T * h->desc.n_experts * sizeof(float), 256);
+}
+
+// Shared-expert regions at the end of moe_decode's workspace: bf16 h [T][F]
+// and the fp32 shared output [T][D].
+static size_t shared_ws_bytes(const moe_handle *h, int T) {
+    if (!h->desc.has_shared) return 0;
+    return align_up((size_t)T * h->desc.d_ff * 2, 256) +
+           align_up((size_t)T * h->desc.d_model * sizeof(float), 256);
+}
+
+static int dense_grid(const moe_handle *h, int epi, int M, int N) {
+    const int tiles = moe_dense_tiles(epi, M, N);
+    return tiles < h->num_sms ? tiles : h->num_sms;
+}
+
+static MoeDenseArgs dense_args(const moe_handle *h, int M, int N, int K, int ldo) {
+    MoeDenseArgs a;
+    memset(&a, 0, sizeof(a));
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ldo = ldo;
+    a.status = h->status;
+    a.timeout_cycles = kTimeoutCycles;
+    return a;
+}
+
+// logits[T][E] = x . W_r^T in fp32 on tensor cores (three bf16 terms of W_r).
+static int run_router(moe_handle *h, int T, const uint16_t *x, float *logits, cudaStream_t st) {
+    const moe_desc &d = h->desc;
+    CUtensorMap mx;
+    if (!make_map_bf16(&mx, x, d.d_model, T, MOE_DENSE_NTILE)) return MOE_ERR_CUDA;
+    MoeDenseArgs a = dense_args(h, d.n_experts, T, d.d_model, d.n_experts);
+    a.out_f32 = logits;
+    h->prof.before(MOE_PROF_ROUTER, st);
+    cudaError_t err = moe_launch_dense(MOE_DENSE_ROUTER, &h->map_wr[0], &h->map_wr[1],
+                                       &h->map_wr[2], &mx, &a,
+                                       dense_grid(h, MOE_DENSE_ROUTER, d.n_experts, T), st);
+    h->prof.after(MOE_PROF_ROUTER, st);
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Shared expert: hsh = bf16(silu(x . Ws_gate^T) * (x . Ws_up^T)) [T][F], then
+// out[T][D] = hsh . Ws_down^T in fp32 (written, not added).
+static int run_shared(moe_handle *h, int T, const uint16_t *x, uint16_t *hsh, float *out,
+                      cudaStream_t st) {
+    const moe_desc &d = h->desc;
+    const int D = d.d_model, F = d.d_ff;
+    CUtensorMap mx, mh;
+    if (!make_map_bf16(&mx, x, D, T, MOE_DENSE_NTILE) ||
+        !make_map_bf16(&mh, hsh, F, T, MOE_DENSE_NTILE))
+        return MOE_ERR_CUDA;
+    MoeDenseArgs g = dense_args(h, F, T, D, F);
+    g.out_bf16 = hsh;
+    h->prof.before(MOE_PROF_SHARED_GATEUP, st);
+    cudaError_t err = moe_launch_dense(MOE_DENSE_SWIGLU, &h->map_sh_gate, &h->map_sh_up,
+                                       &h->map_sh_gate, &mx, &g,
+                                       dense_grid(h, MOE_DENSE_SWIGLU, F, T), st);
+    h->prof.after(MOE_PROF_SHARED_GATEUP, st);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    MoeDenseArgs o = dense_args(h, D, T, F, D);
+    o.out_f32 = out;
+    h->prof.before(MOE_PROF_SHARED_DOWN, st);
+    err = moe_launch_dense(MOE_DENSE_STORE, &h->map_sh_down, &h->map_sh_down, &h->map_sh_down, &mh,
+                           &o, dense_grid(h, MOE_DENSE_STORE, D, T), st);
+    h->prof.after(MOE_PROF_SHARED_DOWN, st);
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 MOE_API size_t moe_workspace_bytes(const moe_handle *h, int32_t T, int32_t op) {
     if (!h || T <= 0) return 0;
     const moe_desc &d = h->desc;
     switch (op) {
-        case MOE_OP_PLAN: return align_up(moe_plan_ws_bytes(T, d.n_experts), 256);
-        case MOE_OP_DECODE: return align_up(moe_decode_ws_bytes(T, d.d_model, d.d_ff, d.top_k), 256);
+        case MOE_OP_PLAN:
+            return router_ws_bytes(h, T) + align_up(moe_plan_ws_bytes(T, d.n_experts), 256);
+        case MOE_OP_DECODE:
+            return align_up(moe_decode_ws_bytes(T, d.d_model, d.d_ff, d.top_k), 256) +
+                   shared_ws_bytes(h, T);
         case MOE_OP_FORWARD:
-            return fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k).total;
+            return fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k, d.has_shared).total;
         default: return 0;
     }
 }
@@ -209,14 +306,38 @@ MOE_API int moe_plan(moe_handle *h, int32_t T, const float *logits, const uint16
     if (!h || T < 0) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
     if (!plan_ok(plan)) return MOE_ERR_INVALID_ARG;
-    if (h->desc.router_mode == MOE_ROUTER_LOGITS && !logits) return MOE_ERR_INVALID_ARG;
+    const bool xwr = h->desc.router_mode == MOE_ROUTER_XWR;
+    if (!xwr && !logits) return MOE_ERR_INVALID_ARG;
+    if (xwr && (logits || !x || !aligned16(x))) return MOE_ERR_INVALID_ARG;
     if ((int64_t)T * h->desc.top_k > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)T * h->desc.n_experts > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+    if (xwr && !h->wr_ready) return MOE_ERR_NOT_PREPARED;
     size_t need = moe_workspace_bytes(h, T, MOE_OP_PLAN);
     if (ws_bytes < need || (need && !ws)) return MOE_ERR_WORKSPACE;
-    (void)x;
-    cudaError_t err = moe_launch_plan(T, h->desc.n_experts, h->desc.top_k, logits, plan, ws,
-                                      h->status, (cudaStream_t)stream);
+    if (need && ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t lg_bytes = router_ws_bytes(h, T);
+    if (xwr) {
+        float *lg = (float *)ws;
+        int rc = run_router(h, T, x, lg, st);
+        if (rc != MOE_OK) return rc;
+        logits = lg;
+    }
+    void *pws = lg_bytes ? (void *)((unsigned char *)ws + lg_bytes) : ws;
+    cudaError_t err = moe_launch_plan(T, h->desc.n_experts, h->desc.top_k, logits, plan, pws,
+                                      h->status, st);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+MOE_API int moe_router_logits(moe_handle *h, int32_t T, const uint16_t *x, float *logits,
+                              void *stream) {
+    if (!h || T < 0) return MOE_ERR_INVALID_ARG;
+    if (h->desc.router_mode != MOE_ROUTER_XWR) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !logits || !aligned16(x) || ((uintptr_t)logits & 3u)) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)T * h->desc.n_experts > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+    if (!h->wr_ready) return MOE_ERR_NOT_PREPARED;
+    return run_router(h, T, x, logits, (cudaStream_t)stream);
 }
 
 MOE_API int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
@@ -229,8 +350,18 @@ MOE_API int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_pl
     size_t need = moe_workspace_bytes(h, T, MOE_OP_DECODE);
     if (ws_bytes < need || !ws || !aligned16(ws)) return MOE_ERR_WORKSPACE;
     const moe_desc &d = h->desc;
+    cudaStream_t st = (cudaStream_t)stream;
+    float *sh_out = nullptr;
+    if (d.has_shared) {
+        unsigned char *p = (unsigned char *)ws +
+                           align_up(moe_decode_ws_bytes(T, d.d_model, d.d_ff, d.top_k), 256);
+        uint16_t *hsh = (uint16_t *)p;
+        sh_out = (float *)(p + align_up((size_t)T * d.d_ff * 2, 256));
+        int rc = run_shared(h, T, x, hsh, sh_out, st);
+        if (rc != MOE_OK) return rc;
+    }
     cudaError_t err = moe_launch_decode(T, d.d_model, d.d_ff, d.n_experts, d.top_k, x, plan, &h->w,
-                                        out, ws, h->status, h->prof, (cudaStream_t)stream);
+                                        sh_out, out, ws, h->status, h->prof, st);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -241,6 +372,7 @@ MOE_API int moe_decode_noalloc(moe_handle *h, int32_t T, const uint16_t *x,
     if (!x || !out || !plan_ok(plan)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
     const moe_desc &d = h->desc;
+    if (d.has_shared) return MOE_ERR_UNSUPPORTED;  // the fixed scratch has no shared-expert room
     if ((int64_t)T * d.top_k > MOE_NOALLOC_MAX_ROWS || d.d_ff > MOE_NOALLOC_MAX_DFF ||
         d.d_model > MOE_NOALLOC_MAX_DMODEL ||
         moe_decode_ws_bytes(T, d.d_model, d.d_ff, d.top_k) > moe_noalloc_scratch_bytes())
@@ -251,7 +383,8 @@ MOE_API int moe_decode_noalloc(moe_handle *h, int32_t T, const uint16_t *x,
     void *scratch = nullptr;
     if (moe_noalloc_scratch(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
     cudaError_t err = moe_launch_decode(T, d.d_model, d.d_ff, d.n_experts, d.top_k, x, plan, &h->w,
-                                        out, scratch, h->status, h->prof, (cudaStream_t)stream);
+                                        nullptr, out, scratch, h->status, h->prof,
+                                        (cudaStream_t)stream);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -264,7 +397,7 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     if ((int64_t)T * h->desc.top_k > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
     if (!h->atoms) return MOE_ERR_NOT_PREPARED;
     const moe_desc &d = h->desc;
-    const FwdLayout L = fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k);
+    const FwdLayout L = fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k, d.has_shared);
     if (ws_bytes < L.total || !ws || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     unsigned char *base = (unsigned char *)ws;
@@ -311,7 +444,14 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         err = moe_launch_gemm(MOE_GEMM_GATEUP, &h->map_gate, &h->map_up, &g1, h->num_sms, st);
         h->prof.after(MOE_PROF_FORWARD_GEMM1, st);
     }
-    if (err == cudaSuccess) err = cudaMemsetAsync(acc, 0, (size_t)T * D * sizeof(float), st);
+    if (err == cudaSuccess) {
+        if (d.has_shared) {  // the shared expert writes acc; the routed rows add onto it
+            if (run_shared(h, T, x, (uint16_t *)(base + L.hsh), acc, st) != MOE_OK)
+                err = cudaErrorLaunchFailure;
+        } else {
+            err = cudaMemsetAsync(acc, 0, (size_t)T * D * sizeof(float), st);
+        }
+    }
     if (err == cudaSuccess) {
         MoeGemmArgs g2 = a;
         g2.M = D;
@@ -330,10 +470,19 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+static size_t atoms_bytes(const moe_desc &d) {
+    return align_up(3 * ((size_t)d.n_experts * d.d_model * d.d_ff / 32), 256);
+}
+
+static size_t wr_terms_bytes(const moe_desc &d) {
+    return d.router_mode == MOE_ROUTER_XWR
+               ? align_up((size_t)d.n_experts * d.d_model * 2, 256) * 3
+               : 0;
+}
+
 MOE_API size_t moe_prepared_bytes(const moe_handle *h) {
     if (!h) return 0;
-    const moe_desc &d = h->desc;
-    return 3 * ((size_t)d.n_experts * d.d_model * d.d_ff / 32);
+    return atoms_bytes(h->desc) + wr_terms_bytes(h->desc);
 }
 
 MOE_API int moe_prepare(moe_handle *h, void *buf, size_t bytes, void *stream) {
@@ -350,12 +499,23 @@ MOE_API int moe_prepare(moe_handle *h, void *buf, size_t bytes, void *stream) {
     if (err == cudaSuccess)
         err = moe_launch_prepare_atoms(E, D, F, 128, h->w.down_s, nullptr, out + 2 * per, st);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
+    if (d.router_mode == MOE_ROUTER_XWR) {
+        // W_r = t0 + t1 + t2 exactly, three bf16 [E][D] arrays after the scale atoms
+        const size_t tb = wr_terms_bytes(d) / 3;
+        uint16_t *t[3];
+        for (int i = 0; i < 3; ++i) t[i] = (uint16_t *)(out + atoms_bytes(d) + i * tb);
+        if (moe_launch_split3((int64_t)E * D, h->w.w_router, t[0], t[1], t[2], st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        for (int i = 0; i < 3; ++i)
+            if (!make_map_bf16(&h->map_wr[i], t[i], D, E, 128)) return MOE_ERR_CUDA;
+        h->wr_ready = true;
+    }
     h->atoms = out;
     return MOE_OK;
 }
 
 MOE_API int moe_profile_kernel(moe_handle *h, int32_t which, void *ev_start, void *ev_stop) {
-    if (!h || which < MOE_PROF_NONE || which > MOE_PROF_FORWARD_GEMM2) return MOE_ERR_INVALID_ARG;
+    if (!h || which < MOE_PROF_NONE || which > MOE_PROF_SHARED_DOWN) return MOE_ERR_INVALID_ARG;
     if (which != MOE_PROF_NONE && (!ev_start || !ev_stop)) return MOE_ERR_INVALID_ARG;
     h->prof.which = which;
     h->prof.start = (cudaEvent_t)ev_start;

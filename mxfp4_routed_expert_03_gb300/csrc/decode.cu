@@ -346,12 +346,14 @@ __global__ void __launch_bounds__(256, 2) moe_decode_down_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Combine: out[t][d] = bf16( sum_j w[t][j] * y[inv[t*k+j]][d] ), j ascending.
+// Combine: out[t][d] = bf16( sum_j w[t][j] * y[inv[t*k+j]][d] [+ shared[t][d]] ),
+// j ascending, the shared expert's output (weight 1.0) added last.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) moe_combine_slots_kernel(int T, int D, int k, int n_rows,
                                                                 const float *__restrict__ topk_w,
                                                                 const int32_t *__restrict__ inv,
                                                                 const float *__restrict__ y,
+                                                                const float *__restrict__ shared,
                                                                 uint16_t *__restrict__ out,
                                                                 int *status) {
     int t = blockIdx.y;
@@ -367,6 +369,13 @@ __global__ void __launch_bounds__(256) moe_combine_slots_kernel(int T, int D, in
         acc.y = fmaf(w, v.y, acc.y);
         acc.z = fmaf(w, v.z, acc.z);
         acc.w = fmaf(w, v.w, acc.w);
+    }
+    if (shared) {
+        const float4 v = ((const float4 *)(shared + (size_t)t * D))[d4];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
     }
     uint2 o;
     o.x = (uint32_t)f32_to_bf16_bits(acc.x) | ((uint32_t)f32_to_bf16_bits(acc.y) << 16);
@@ -460,8 +469,9 @@ const down_fn kDown[9] = {nullptr, launch_down<1>, launch_down<2>, launch_down<3
 }  // namespace
 
 cudaError_t moe_launch_decode(int T, int D, int F, int E, int k, const uint16_t *x,
-                              const moe_plan_buf *p, const moe_weights *w, uint16_t *out,
-                              void *ws, int *status, const MoeProf &prof, cudaStream_t st) {
+                              const moe_plan_buf *p, const moe_weights *w,
+                              const float *shared_out, uint16_t *out, void *ws, int *status,
+                              const MoeProf &prof, cudaStream_t st) {
     const int n_rows = T * k;
     const DecodeLayout L = decode_layout(T, D, F, k);
     unsigned char *base = (unsigned char *)ws;
@@ -478,6 +488,7 @@ cudaError_t moe_launch_decode(int T, int D, int F, int E, int k, const uint16_t 
     kDown[pf](grid, st, D, F, E, n_rows, p, w, h16, hexp, y, status);
     prof.after(MOE_PROF_DECODE_DOWN, st);
     dim3 g((D / 4 + 255) / 256, T);
-    moe_combine_slots_kernel<<<g, 256, 0, st>>>(T, D, k, n_rows, p->topk_w, p->inv, y, out, status);
+    moe_combine_slots_kernel<<<g, 256, 0, st>>>(T, D, k, n_rows, p->topk_w, p->inv, y, shared_out,
+                                                     out, status);
     return cudaGetLastError();
 }

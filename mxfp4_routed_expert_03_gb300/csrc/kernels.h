@@ -29,9 +29,11 @@ cudaError_t moe_launch_plan(int T, int E, int k, const float *logits, const moe_
 // decode.cu
 int moe_decode_per_lane(int K);
 size_t moe_decode_ws_bytes(int T, int D, int F, int k);
+// shared_out: optional fp32 [T][D] added to every token's combine (NULL: none)
 cudaError_t moe_launch_decode(int T, int D, int F, int E, int k, const uint16_t *x,
-                              const moe_plan_buf *p, const moe_weights *w, uint16_t *out,
-                              void *ws, int *status, const MoeProf &prof, cudaStream_t st);
+                              const moe_plan_buf *p, const moe_weights *w,
+                              const float *shared_out, uint16_t *out, void *ws, int *status,
+                              const MoeProf &prof, cudaStream_t st);
 
 // noalloc.cu: fixed scratch of moe_decode_noalloc
 #define MOE_NOALLOC_MAX_ROWS 256     // tokens x top_k
@@ -83,3 +85,27 @@ cudaError_t moe_launch_prepare_atoms(int E, int M, int K, int mrows, const uint8
                                      const uint8_t *s2, uint8_t *out, cudaStream_t st);
 cudaError_t moe_launch_gemm(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
                             const MoeGemmArgs *args, int grid, cudaStream_t st);
+
+// dense_gemm.cu: bf16 tcgen05 GEMMs of the router and the shared expert
+#define MOE_DENSE_ROUTER 0  // 3 bf16 terms of W_r, fp32 store out_f32[t][m] (m < M)
+#define MOE_DENSE_SWIGLU 1  // gate/up (64 + 64 rows per tile), bf16 store out_bf16[t][f]
+#define MOE_DENSE_STORE 2   // 1 term, fp32 store out_f32[t][m] (m < M)
+#define MOE_DENSE_NTILE 192  // tokens per tile
+
+struct MoeDenseArgs {
+    int M;          // output rows (experts, d_ff or d_model)
+    int N;          // tokens
+    int K;          // reduction length, a multiple of 64
+    int ldo;        // row stride of the output (elements)
+    float *out_f32;
+    uint16_t *out_bf16;
+    int *status;
+    long long timeout_cycles;
+};
+
+cudaError_t moe_launch_split3(int64_t n, const float *w, uint16_t *t0, uint16_t *t1, uint16_t *t2,
+                              cudaStream_t st);
+int moe_dense_tiles(int epi, int M, int N);
+cudaError_t moe_launch_dense(int epi, const CUtensorMap *a0, const CUtensorMap *a1,
+                             const CUtensorMap *a2, const CUtensorMap *b,
+                             const MoeDenseArgs *args, int grid, cudaStream_t st);

@@ -7,9 +7,10 @@ from __future__ import annotations
 
 import torch
 
-from . import (MOE_OP_DECODE, MOE_OP_FORWARD, MOE_OP_PLAN, check, moe_create, moe_decode,
-               moe_desc, moe_destroy, moe_forward, moe_plan, moe_plan_buf, moe_prepare,
-               moe_prepared_bytes, moe_status, moe_weights, moe_workspace_bytes)
+from . import (MOE_OP_DECODE, MOE_OP_FORWARD, MOE_OP_PLAN, MOE_ROUTER_XWR, check, moe_create,
+               moe_decode, moe_desc, moe_destroy, moe_forward, moe_plan, moe_plan_buf,
+               moe_prepare, moe_prepared_bytes, moe_router_logits, moe_status, moe_weights,
+               moe_workspace_bytes)
 
 WEIGHT_NAMES = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
 
@@ -49,6 +50,7 @@ class Layer:
     def __init__(self, D: int, F: int, E: int, k: int, weights: dict, router_mode: int = 0,
                  w_router=None, shared=None):
         self.D, self.F, self.E, self.k = D, F, E, k
+        self.router_mode = router_mode
         self.weights = weights
         self.w_router = w_router
         self.shared = shared
@@ -63,7 +65,7 @@ class Layer:
         self.atoms = None
 
     def prepare(self, stream=None) -> None:
-        """One-time weight-scale re-layout for the tensor-core path."""
+        """One-time weight-scale re-layout (and W_r split) for the tensor-core paths."""
         if self.atoms is None:
             n = moe_prepared_bytes(self.h)
             self.atoms = torch.empty(n, dtype=torch.uint8, device="cuda")
@@ -86,7 +88,13 @@ class Layer:
             self._ws = torch.empty(max(n, 256), dtype=torch.uint8, device="cuda")
         return self._ws, n
 
+    def router_logits(self, T, x, logits, stream=None) -> int:
+        self.prepare(stream)
+        return moe_router_logits(self.h, T, x, logits, stream)
+
     def plan(self, T, logits, x, plan: Plan, stream=None) -> int:
+        if self.router_mode == MOE_ROUTER_XWR:
+            self.prepare(stream)
         ws, n = self.workspace(T, MOE_OP_PLAN)
         return moe_plan(self.h, T, logits, x, plan.buf, ws, ws.numel(), stream)
 

@@ -54,3 +54,12 @@ def device_layer_weights(w: synth.Workload, device="cuda") -> dict:
                          torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     return weights
+
+
+def router_and_shared(w: synth.Workload, shared: bool = True, device="cuda"):
+    """Device copies of the workload's fp32 W_r [E][D] and bf16 shared expert (host-generated)."""
+    wr = torch.from_numpy(synth.make_w_router(w)).to(device)
+    if not shared:
+        return wr, None
+    sh = {k: to_dev_bf16(v, device) for k, v in synth.make_shared(w).items()}
+    return wr, sh

@@ -81,5 +81,6 @@ def test_null_handle_calls_are_rejected(L):
     assert L.moe_plan(None, 1, None, None, plan, None, 0) == L.MOE_ERR_INVALID_ARG
     assert L.moe_decode(None, 1, None, plan, None, None, 0) == L.MOE_ERR_INVALID_ARG
     assert L.moe_forward(None, 1, None, plan, None, None, 0) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_router_logits(None, 1, None, None) == L.MOE_ERR_INVALID_ARG
     assert L.moe_workspace_bytes(None, 16, L.MOE_OP_DECODE) == 0
     L.moe_destroy(None)
