@@ -66,6 +66,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall-time budget of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=N_EXPERTS,
+                    help="experts in the layer (default 896); fewer only for profiling small "
+                         "cases, and the line is then marked as such")
     return ap.parse_args()
 
 
@@ -214,6 +217,7 @@ def run_ours(args):
                                               moe_profile_kernel)
     from mxfp4_routed_expert_03_gb300.layer import Layer, Plan, alloc_weights
 
+    n_exp = args.experts
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -230,19 +234,20 @@ def run_ours(args):
     base = synth.WORKLOADS["decode1"] if args.workload == "decode" else synth.WORKLOADS[args.workload]
 
     # weights: the full layer, generated in HBM by the device half of the generator
-    weights = alloc_weights(N_EXPERTS, D_MODEL, D_FF)
-    synth.dev_fill_layer(base.seed, N_EXPERTS, D_MODEL, D_FF,
+    weights = alloc_weights(n_exp, D_MODEL, D_FF)
+    synth.dev_fill_layer(base.seed, n_exp, D_MODEL, D_FF,
                          {k: v.data_ptr() for k, v in weights.items()},
                          torch.cuda.current_stream().cuda_stream)
     use_router = bool(wl.get("router"))
     n_sets = wl.get("sets", N_SETS)
     if use_router:
-        w_router = torch.from_numpy(synth.make_w_router(base)).to(dev)
+        import dataclasses
+        w_router = torch.from_numpy(synth.make_w_router(dataclasses.replace(base, E=n_exp))).to(dev)
         shared = {k: torch.from_numpy(v.view(np.int16)).to(dev)
                   for k, v in synth.make_shared(base).items()}
-        layer = Layer(D_MODEL, D_FF, N_EXPERTS, TOP_K, weights, MOE_ROUTER_XWR, w_router, shared)
+        layer = Layer(D_MODEL, D_FF, n_exp, TOP_K, weights, MOE_ROUTER_XWR, w_router, shared)
     else:
-        layer = Layer(D_MODEL, D_FF, N_EXPERTS, TOP_K, weights)
+        layer = Layer(D_MODEL, D_FF, n_exp, TOP_K, weights)
     if path == "forward" or use_router:
         layer.prepare()
     stream = torch.cuda.current_stream()
@@ -251,20 +256,20 @@ def run_ours(args):
     # when the library computes the logits)
     batches = []
     for T in wl["Ts"]:
-        w = synth.Workload(base.name, T=T, D=D_MODEL, F=D_FF, E=N_EXPERTS, k=TOP_K,
+        w = synth.Workload(base.name, T=T, D=D_MODEL, F=D_FF, E=n_exp, k=TOP_K,
                            seed=base.seed, zipf_s=base.zipf_s)
         xs_h = [synth.make_x(w, rank * 97 + i) for i in range(n_sets)]
-        ls_h = [np.zeros((T, N_EXPERTS), np.float32) if use_router else
+        ls_h = [np.zeros((T, n_exp), np.float32) if use_router else
                 synth.make_logits(w, rank * 97 + i) for i in range(n_sets)]
         xs = [torch.from_numpy(a.view(np.int16)).to(dev) for a in xs_h]
         ls = [torch.from_numpy(a).to(dev) for a in ls_h]
         pin_x = [torch.from_numpy(a.view(np.int16)).pin_memory() for a in xs_h]
         pin_l = [torch.from_numpy(a).pin_memory() for a in ls_h]
         batches.append({"T": T, "x": xs, "l": ls, "px": pin_x, "pl": pin_l,
-                        "plan": Plan(T, N_EXPERTS, TOP_K),
+                        "plan": Plan(T, n_exp, TOP_K),
                         "out": torch.empty((T, D_MODEL), dtype=torch.int16, device=dev),
                         "dx": torch.empty((T, D_MODEL), dtype=torch.int16, device=dev),
-                        "dl": torch.empty((T, N_EXPERTS), dtype=torch.float32, device=dev),
+                        "dl": torch.empty((T, n_exp), dtype=torch.float32, device=dev),
                         "hout": torch.empty((T, D_MODEL), dtype=torch.int16).pin_memory()})
     for b in batches:  # size the workspace once for the largest call
         layer.workspace(b["T"], 2 if path == "decode" else 1)
@@ -420,8 +425,10 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (>=280 MB of expert weights per batch, "
                          "8 rotating logit sets)", "parallelism": f"replicas x{world}"},
         "roofline": roof,
+        **({"profiling_case": f"{n_exp} experts instead of {N_EXPERTS}; not a bench value"}
+           if n_exp != N_EXPERTS else {}),
         "e2e": {"value": e2e_value, "unit": "tokens/s",
-                "h2d_bytes_per_step": sum(T * D_MODEL * 2 + (0 if use_router else T * N_EXPERTS * 4)
+                "h2d_bytes_per_step": sum(T * D_MODEL * 2 + (0 if use_router else T * n_exp * 4)
                                           for T in wl["Ts"]),
                 "d2h_bytes_per_step": sum(T * D_MODEL * 2 for T in wl["Ts"])},
         "gpu_launches": launches_per_call * len(wl["Ts"]) * args.steps,

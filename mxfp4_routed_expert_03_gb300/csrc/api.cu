@@ -149,6 +149,8 @@ MOE_API int moe_create(const moe_desc *d, const moe_weights *w, moe_handle **out
         if (!p) return MOE_ERR_INVALID_ARG;
     if (((uintptr_t)w->gate_q | (uintptr_t)w->up_q | (uintptr_t)w->down_q) & 31u)
         return MOE_ERR_INVALID_ARG;  // TMA of packed E2M1 needs 32-byte aligned bases
+    if (((uintptr_t)w->gate_s | (uintptr_t)w->up_s | (uintptr_t)w->down_s) & 15u)
+        return MOE_ERR_INVALID_ARG;  // bulk copies of scale rows need 16-byte aligned bases
     if (d->router_mode == MOE_ROUTER_XWR && !w->w_router) return MOE_ERR_INVALID_ARG;
     if (d->has_shared && (!w->sh_gate || !w->sh_up || !w->sh_down)) return MOE_ERR_INVALID_ARG;
     if (d->has_shared && ((uintptr_t)w->sh_gate | (uintptr_t)w->sh_up | (uintptr_t)w->sh_down) & 15u)
