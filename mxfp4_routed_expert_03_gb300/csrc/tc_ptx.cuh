@@ -45,6 +45,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to `ns` nanoseconds while the
+// phase is incomplete (it resumes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for waits expected to be long: the waiting warp sleeps inside
+// try_wait instead of spinning, so it takes no issue slots from warps that
+// have work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, long long limit_cycles,
+                                                volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > limit_cycles) return false;
+    }
+}
+
 // Bounded wait on phase `parity`: gives up after `limit_cycles` SM clocks
 // (or as soon as *abort becomes non-zero) and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long limit_cycles,
