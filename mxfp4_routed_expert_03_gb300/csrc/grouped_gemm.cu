@@ -31,10 +31,14 @@
 // to both CTAs' release barriers, so a stage is refilled only once both have
 // consumed it.
 //
+// A pipeline stage carries KS = 2 consecutive 128-wide K blocks (all data
+// layouts stay per 128-wide block), so each wait, commit and loop step of the
+// single MMA-issuing thread is shared by 8 MMAs instead of 4.
+//
 // One persistent CTA per SM, 7 warps:
 //   warp 0      weight producer (one thread): weight tile(s) by TMA (packed
 //               E2M1 expanded to the 8-bit MMA layout) and the prepared
-//               512-byte scale atom by bulk copy
+//               512-byte scale atoms by bulk copy
 //   warp 1      activation producer (one thread): the token tile's prepared
 //               [hi; lo] B tile and its scales, each one contiguous bulk copy
 //               per chunk; TMEM allocator
@@ -51,7 +55,8 @@
 
 namespace {
 
-constexpr int BK = 128;                  // K elements per stage
+constexpr int BK = 128;                  // K elements per block (data-layout unit)
+constexpr int KS = 2;                    // blocks per pipeline stage
 constexpr int NTMAX = MOE_GEMM_NTMAX;    // token rows per tile
 constexpr int A_BYTES = 128 * BK;        // smem bytes of the 128-row weight tile (E2M1 -> 8 bit)
 constexpr int A_TX = 128 * BK / 2;       // bytes the TMA moves for it (packed)
@@ -61,20 +66,23 @@ constexpr int BSF_BYTES = 1024;          // activation scales of one chunk (256 
 constexpr int NUM_THREADS = 224;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 2 * NTMAX;  // [hi | lo] accumulator columns per buffer
-constexpr uint32_t SF_TMEM_COL = 448;     // scale atoms: 2 slots x (4 A + 8 B) columns
+constexpr uint32_t SF_TMEM_COL = 464;     // scales: 2 slots x KS blocks x (4 A + 8 B) columns
+constexpr uint32_t SF_SLOT = KS * 12;     // columns per slot
+constexpr uint32_t SF_SUB = 12;           // columns per block within a slot
 constexpr int CL = MOE_GEMM_CLUSTER;      // CTAs per cluster sharing activation chunks
 constexpr uint16_t CL_MASK = (1u << CL) - 1;
 
 template <int MODE>
 struct Cfg {
     static constexpr int MROWS = (MODE == MOE_GEMM_GATEUP) ? 64 : 128;  // weight rows per tile
-    static constexpr int SA = 4;                                          // weight ring stages
-    static constexpr int SB = 4;                                          // activation stages
-    static constexpr int A_STAGE = (A_BYTES + SF_BYTES + 1023) / 1024 * 1024;
-    static constexpr int A_SF = A_BYTES;
-    static constexpr int B_STAGE = B_BYTES + 4 * BSF_BYTES;  // scales replicated per quadrant
+    static constexpr int SA = 2;  // weight ring stages (KS blocks each)
+    static constexpr int SB = 2;  // activation ring stages
+    static constexpr int A_STAGE = (KS * (A_BYTES + SF_BYTES) + 1023) / 1024 * 1024;
+    static constexpr int A_SF = KS * A_BYTES;  // KS consecutive scale atoms
+    // B: KS blocks of [hi; lo] rows, then KS x 4 scale copies (one per TMEM quadrant)
+    static constexpr int B_STAGE = KS * (B_BYTES + 4 * BSF_BYTES);
     static constexpr int B_BASE = SA * A_STAGE;
-    static constexpr int B_SF = B_BYTES;
+    static constexpr int B_SF = KS * B_BYTES;
     static constexpr int BAR_BASE = B_BASE + SB * B_STAGE;
     static constexpr int N_BARS = 2 * SA + 2 * SB + 4;
     static constexpr int PREFIX_BASE = BAR_BASE + N_BARS * 8 + 16;  // int [active + 1]
@@ -240,20 +248,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                 }
                 const int row0 = t.e * args.M + t.mt * C::MROWS;
                 const size_t atom0 = ((size_t)t.e * MT + t.mt) * KC;
-                for (int kc = 0; kc < KC; ++kc, ++it) {
+                for (int kc = 0; kc < KC; kc += KS, ++it) {
                     const int s = it % C::SA, round = it / C::SA;
+                    const int nsub = min(KS, KC - kc);
                     if (round > 0 && !tc::mbar_wait(&emptyA[s], (round - 1) & 1, LIMIT, abort_p)) {
                         fail();
                         ok = false;
                         break;
                     }
                     unsigned char *st = smem + s * C::A_STAGE;
-                    tc::mbar_arrive_expect_tx(&fullA[s], (uint32_t)(A_TX + SF_BYTES));
-                    tc::tma_load_2d(st, &mapA, &fullA[s], kc * BK, row0, pol_w);
-                    if (MODE == MOE_GEMM_GATEUP)  // up rows fill lanes 64..127
-                        tc::tma_load_2d(st + 64 * BK, &mapA2, &fullA[s], kc * BK, row0, pol_w);
+                    tc::mbar_arrive_expect_tx(&fullA[s], (uint32_t)(nsub * (A_TX + SF_BYTES)));
+                    for (int sub = 0; sub < nsub; ++sub) {
+                        unsigned char *sa = st + sub * A_BYTES;
+                        tc::tma_load_2d(sa, &mapA, &fullA[s], (kc + sub) * BK, row0, pol_w);
+                        if (MODE == MOE_GEMM_GATEUP)  // up rows fill lanes 64..127
+                            tc::tma_load_2d(sa + 64 * BK, &mapA2, &fullA[s], (kc + sub) * BK, row0,
+                                            pol_w);
+                    }
                     tc::bulk_copy_g2s(st + C::A_SF, args.a_atoms + (atom0 + kc) * SF_BYTES,
-                                      SF_BYTES, &fullA[s], pol_w);
+                                      nsub * SF_BYTES, &fullA[s], pol_w);
                 }
             }
         }
@@ -268,24 +281,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                 if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, t)) continue;
                 const uint32_t tile_bytes = (uint32_t)(2 * t.nmma * BK);
                 const size_t blk0 = (size_t)t.tt * KC;
-                for (int kc = 0; kc < KC; ++kc, ++it) {
+                for (int kc = 0; kc < KC; kc += KS, ++it) {
                     const int s = it % C::SB, round = it / C::SB;
+                    const int nsub = min(KS, KC - kc);
                     if (round > 0 && !tc::mbar_wait(&emptyB[s], (round - 1) & 1, LIMIT, abort_p)) {
                         fail();
                         ok = false;
                         break;
                     }
                     unsigned char *st = smem + C::B_BASE + s * C::B_STAGE;
-                    // the whole chunk lands here; this CTA fetches its 1/CL share for all
-                    tc::mbar_arrive_expect_tx(&fullB[s], tile_bytes + 4 * BSF_BYTES);
+                    // the whole stage lands here; this CTA fetches its 1/CL share for all
+                    tc::mbar_arrive_expect_tx(&fullB[s], (uint32_t)nsub * (tile_bytes + 4 * BSF_BYTES));
                     const uint32_t part = tile_bytes / CL;
-                    tc::bulk_copy_g2s_multicast(
-                        st + rank * part, args.b_tiles + (blk0 + kc) * MOE_GEMM_BTILE + rank * part,
-                        part, &fullB[s], CL_MASK, pol_x);
-                    for (int qd = rank; qd < 4; qd += CL)  // one copy per TMEM lane quadrant
-                        tc::bulk_copy_g2s_multicast(st + C::B_SF + qd * BSF_BYTES,
-                                                    args.b_atoms + (blk0 + kc) * BSF_BYTES,
-                                                    BSF_BYTES, &fullB[s], CL_MASK, pol_x);
+                    for (int sub = 0; sub < nsub; ++sub) {
+                        const size_t blk = blk0 + kc + sub;
+                        tc::bulk_copy_g2s_multicast(
+                            st + sub * B_BYTES + rank * part,
+                            args.b_tiles + blk * MOE_GEMM_BTILE + rank * part, part, &fullB[s],
+                            CL_MASK, pol_x);
+                        for (int qd = rank; qd < 4; qd += CL)  // one copy per TMEM lane quadrant
+                            tc::bulk_copy_g2s_multicast(
+                                st + C::B_SF + (sub * 4 + qd) * BSF_BYTES,
+                                args.b_atoms + blk * BSF_BYTES, BSF_BYTES, &fullB[s], CL_MASK, pol_x);
+                    }
                 }
             }
         }
@@ -310,29 +328,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                 }
                 tc::tc_fence_after();
                 const uint32_t acc = tmem + buf * ACC_COLS;
-                for (int kc = 0; kc < KC; ++kc, ++it) {
+                uint32_t idesc[4];  // scale byte k of each column for K step k
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    idesc[k] = tc::idesc_mxf8f6f4(tc::FMT_E2M1, tc::FMT_E4M3, 128, 2 * t.nmma, k, k);
+                for (int kc = 0; kc < KC; kc += KS, ++it) {
                     const int sa = it % C::SA, ra = it / C::SA;
                     const int sb = it % C::SB, rb = it / C::SB;
+                    const int nsub = min(KS, KC - kc);
                     if (!tc::mbar_wait(&fullA[sa], ra & 1, LIMIT, abort_p) ||
                         !tc::mbar_wait(&fullB[sb], rb & 1, LIMIT, abort_p)) {
                         fail();
                         ok = false;
                         break;
                     }
-                    unsigned char *sta = smem + sa * C::A_STAGE;
-                    unsigned char *stb = smem + C::B_BASE + sb * C::B_STAGE;
-                    const uint32_t sfa = tmem + SF_TMEM_COL + (uint32_t)(it & 1) * 12;
-                    const uint32_t sfb = sfa + 4;
-                    tc::tmem_cp_32x128b_warpx4(sfa, tc::sdesc_plain_32x16(tc::smem_u32(sta + C::A_SF)));
-                    tc::tmem_cp_128x256b(sfb, tc::sdesc_plain_128x32(tc::smem_u32(stb + C::B_SF)));
-                    const uint32_t a_s = tc::smem_u32(sta), b_s = tc::smem_u32(stb);
+                    const uint32_t a_s = tc::smem_u32(smem + sa * C::A_STAGE);
+                    const uint32_t b_s = tc::smem_u32(smem + C::B_BASE + sb * C::B_STAGE);
+                    const uint32_t slot = tmem + SF_TMEM_COL + (uint32_t)(it & 1) * SF_SLOT;
+                    for (int sub = 0; sub < nsub; ++sub) {
+                        const uint32_t sfa = slot + sub * SF_SUB, sfb = sfa + 4;
+                        tc::tmem_cp_32x128b_warpx4(
+                            sfa, tc::sdesc_plain_32x16(a_s + C::A_SF + sub * SF_BYTES));
+                        tc::tmem_cp_128x256b(
+                            sfb, tc::sdesc_plain_128x32(b_s + C::B_SF + sub * 4 * BSF_BYTES));
+                        const uint32_t as = a_s + sub * A_BYTES, bs = b_s + sub * B_BYTES;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t idesc =
-                            tc::idesc_mxf8f6f4(tc::FMT_E2M1, tc::FMT_E4M3, 128, 2 * t.nmma, k, k);
-                        tc::mma_mxf8f6f4(acc, tc::sdesc_sw128(a_s + 32 * k),
-                                         tc::sdesc_sw128(b_s + 32 * k), idesc, sfa, sfb,
-                                         (kc > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < 4; ++k)
+                            tc::mma_mxf8f6f4(acc, tc::sdesc_sw128(as + 32 * k),
+                                             tc::sdesc_sw128(bs + 32 * k), idesc[k], sfa, sfb,
+                                             (kc > 0 || sub > 0 || k > 0) ? 1u : 0u);
                     }
                     tc::mma_commit(&emptyA[sa]);
                     tc::mma_commit_multicast(&emptyB[sb], CL_MASK);  // every CTA's copy is free
