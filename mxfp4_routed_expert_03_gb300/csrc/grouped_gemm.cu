@@ -112,23 +112,23 @@ struct Tile {
 // consecutive cluster tiles (weight tile group major, token tile minor); the
 // CTA of cluster rank `rank` takes weight tile mg * CL + rank of the group.
 // s_prefix, s_expert and s_seg are the shared-memory copies of the token-tile
-// prefix, the active experts and their (first slot, rows) segments.
+// prefix, the active experts and their (first slot, rows) segments. Each
+// role visits its tiles in increasing order, so `a` (the caller's cursor,
+// starting at 0) only moves forward: a few shared-memory reads per tile.
 __device__ __forceinline__ bool tile_at(int ct, int n_active, int MTG, int rank,
                                         const int *s_prefix, const int *s_expert,
-                                        const int2 *s_seg, Tile &t) {
-    int lo = 0, hi = n_active - 1;
-    while (lo < hi) {  // last a with MTG * prefix[a] <= ct
-        int mid = (lo + hi + 1) >> 1;
-        if (MTG * s_prefix[mid] <= ct) lo = mid;
-        else hi = mid - 1;
-    }
-    const int a = lo;
+                                        const int2 *s_seg, int &a, Tile &t) {
+    while (a + 1 < n_active && MTG * s_prefix[a + 1] <= ct) ++a;  // last a with MTG*prefix[a] <= ct
     const int ntt = s_prefix[a + 1] - s_prefix[a];
     if (ntt <= 0 || s_expert[a] < 0) return false;
     const int local = ct - MTG * s_prefix[a];
     const int mg = local / ntt, j = local % ntt;
     const int2 seg = s_seg[a];
-    const int r0 = (int)((long long)j * seg.y / ntt), r1 = (int)((long long)(j + 1) * seg.y / ntt);
+    // token rows of the expert split evenly over its ntt tiles (32-bit
+    // arithmetic unless the product is too large for it)
+    const long long p0 = (long long)j * seg.y, p1 = p0 + seg.y;
+    const int r0 = p1 <= 0x7FFFFFFFLL ? (int)p0 / ntt : (int)(p0 / ntt);
+    const int r1 = p1 <= 0x7FFFFFFFLL ? (int)p1 / ntt : (int)(p1 / ntt);
     t.e = s_expert[a];
     t.mt = mg * CL + rank;
     t.s0 = seg.x + r0;
@@ -240,9 +240,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
             const uint64_t pol_w = tc::policy_evict_first();
             int it = 0;
             bool ok = true;
+            int cur = 0;
             for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
                 Tile t;
-                if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, t)) {
+                if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) {
                     moe_flag(args.status, MOE_ERR_BAD_INDEX);
                     continue;
                 }
@@ -276,9 +277,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
             const uint64_t pol_x = tc::policy_evict_last();
             int it = 0;
             bool ok = true;
+            int cur = 0;
             for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
                 Tile t;
-                if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, t)) continue;
+                if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) continue;
                 const uint32_t tile_bytes = (uint32_t)(2 * t.nmma * BK);
                 const size_t blk0 = (size_t)t.tt * KC;
                 for (int kc = 0; kc < KC; kc += KS, ++it) {
@@ -316,9 +318,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
             bool ok = true;
             uint64_t *lastA = nullptr, *lastB = nullptr;
             uint32_t parA = 0, parB = 0;
+            int cur = 0;
             for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
                 Tile t;
-                if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, t)) continue;
+                if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) continue;
                 const int buf = lt & 1, use = lt >> 1;
                 ++lt;
                 if (use > 0 && !tc::mbar_wait(&tempty[buf], (use - 1) & 1, LIMIT, abort_p)) {
@@ -378,13 +381,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
         // ------------------------------------------ epilogue (warps 3..6)
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        int lt = 0;
+        int lt = 0, cur = 0;
         for (int tile = cluster_id; tile < total_tiles; tile += n_clusters) {
             Tile t;
-            if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, t))
+            if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t))
                 continue;
             const int buf = lt & 1, use = lt >> 1;
             ++lt;
+            // GEMM2: the tile's token rows and routing weights, read before the
+            // accumulator is ready (column lane + 32 i of the tile in pf[i], pw[i])
+            int pf[NTMAX / 32 + 1];
+            float pw[NTMAX / 32 + 1];
+            if (MODE == MOE_GEMM_DOWN) {
+#pragma unroll
+                for (int i = 0; i <= NTMAX / 32; ++i) {
+                    const int col = lane + 32 * i;
+                    pf[i] = -1;
+                    pw[i] = 0.f;
+                    if (col < t.n) {
+                        const int fl = args.perm[t.s0 + col];
+                        if (fl < 0 || fl >= args.n_rows) {
+                            moe_flag(args.status, MOE_ERR_BAD_INDEX);
+                        } else {
+                            pf[i] = fl;
+                            pw[i] = args.topk_w[fl];
+                        }
+                    }
+                }
+            }
             if (!tc::mbar_wait(&tfull[buf], use & 1, LIMIT, abort_p)) {
                 if (lane == 0) fail();
                 break;
@@ -450,27 +474,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                     // weighted values -> warp staging [16 columns][32 rows], then each
                     // lane adds 4 consecutive rows of one column with one vector reduction
                     float *stg = (float *)(smem + C::EPI_BASE) + (warp - 3) * 16 * 32;
-                    int fl = -1;
-                    float wv = 0.f;
-                    if (lane < 16 && c0 + lane < t.n) {
-                        fl = args.perm[t.s0 + c0 + lane];
-                        if (fl < 0 || fl >= args.n_rows) {
-                            moe_flag(args.status, MOE_ERR_BAD_INDEX);
-                            fl = -1;
-                        } else {
-                            wv = args.topk_w[fl];
+                    // columns c0 .. c0 + 15 live in pf/pw[c0 / 32] of lanes c0 % 32 + j
+                    const int ci = c0 >> 5, cl = c0 & 31;
+                    int fl = pf[0];
+                    float wv = pw[0];
+#pragma unroll
+                    for (int i = 1; i <= NTMAX / 32; ++i)
+                        if (ci == i) {
+                            fl = pf[i];
+                            wv = pw[i];
                         }
-                    }
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        stg[j * 32 + lane] = __shfl_sync(0xFFFFFFFFu, wv, j) * v[j];
+                        stg[j * 32 + lane] = __shfl_sync(0xFFFFFFFFu, wv, cl + j) * v[j];
                     __syncwarp();
                     const int d0 = t.mt * 128 + q * 32;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int i = lane + 32 * u;  // float4 index: column i/8, rows 4*(i%8)..+3
                         const int j = i >> 3, g = i & 7;
-                        const int flj = __shfl_sync(0xFFFFFFFFu, fl, j);
+                        const int flj = __shfl_sync(0xFFFFFFFFu, fl, cl + j);
                         if (c0 + j < t.n && flj >= 0) {
                             const float4 w4 = *(const float4 *)(stg + j * 32 + 4 * g);
                             float *dst = args.acc + (size_t)(flj / args.k) * args.Dout + d0 + 4 * g;
