@@ -149,19 +149,24 @@ void moe_destroy(moe_handle *h);
 int64_t moe_expert_bytes(int32_t d_model, int32_t d_ff);
 
 /* Host. Bytes of the buffer moe_prepare fills: the three weight-scale arrays
- * (3 * n_experts * d_model * d_ff / 32 bytes, 924 MB for the 896-expert K3
- * layer, rounded up to 256) plus, for router_mode MOE_ROUTER_XWR, three bf16
+ * (3 * n_experts * d_model * d_ff / 32 bytes when d_model and d_ff are
+ * multiples of 256, 924 MB for the 896-expert K3 layer; a K chunk pair is
+ * padded when the chunk count is odd; rounded up to 256) plus, for router_mode MOE_ROUTER_XWR, three bf16
  * copies of W_r's shape (3 * n_experts * d_model * 2 bytes, each rounded up to
  * 256; 38.5 MB for K3). */
 size_t moe_prepared_bytes(const moe_handle *h);
 
 /* One-time weight-layout preparation for moe_forward (asynchronous on
  * `stream`). Re-lays the E8M0 weight scales into the order the tensor cores
- * consume them: for each (expert, 128-row tile, 128-wide K chunk) one
- * contiguous 512-byte block, row m of the tile and 32-wide K block c at byte
- * (m % 32) * 16 + (m / 32) * 4 + c. `buf` is caller-owned device memory of at
- * least moe_prepared_bytes(h) bytes, 256-byte aligned; the handle keeps the
- * pointer, so it must outlive the handle, and the weight scales must not
+ * consume them: for each (expert, 128-row weight tile, pair of 128-wide K
+ * chunks) one contiguous 1 KB block, the layout of one TMEM lane quadrant of
+ * a 128x256b tensor-memory copy (lane l < 32, column j < 8 at byte
+ * (l / 8) * 256 + (j / 4) * 128 + (l % 8) * 16 + (j % 4) * 4; column j holds
+ * the four block scales of tile row 32 * (j % 4) + l in K chunk
+ * 2 * pair + j / 4). Gate/up tiles are 64 gate rows over the same 64 up
+ * rows, down tiles 128 consecutive rows. `buf` is caller-owned device memory
+ * of at least moe_prepared_bytes(h) bytes, 256-byte aligned; the handle keeps
+ * the pointer, so it must outlive the handle, and the weight scales must not
  * change afterwards without calling moe_prepare again. moe_decode does not
  * need it; moe_forward returns MOE_ERR_NOT_PREPARED without it.
  * For router_mode MOE_ROUTER_XWR it also splits W_r into three bf16 terms

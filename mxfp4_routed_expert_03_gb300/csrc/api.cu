@@ -108,6 +108,16 @@ static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// prepared weight scales: gate/up tiles (64 + 64 rows), then down tiles (128 rows)
+static size_t gu_atoms_bytes(const moe_desc &d) {
+    return moe_prepared_atoms_bytes(d.n_experts, d.d_ff, d.d_model, 64);
+}
+
+static size_t atoms_bytes(const moe_desc &d) {
+    return align_up(gu_atoms_bytes(d) + moe_prepared_atoms_bytes(d.n_experts, d.d_model, d.d_ff, 128),
+                    256);
+}
+
 MOE_API int64_t moe_expert_bytes(int32_t d_model, int32_t d_ff) {
     if (d_model <= 0 || d_ff <= 0 || d_model % 32 || d_ff % 32) return -1;
     int64_t n = (int64_t)d_model * d_ff;
@@ -460,7 +470,7 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         g2.MT = D / 128;
         g2.K = F;
         g2.KC = F / 128;
-        g2.a_atoms = h->atoms + 2 * ((size_t)E * F * D / 32);
+        g2.a_atoms = h->atoms + gu_atoms_bytes(d);
         g2.b_tiles = hb;
         g2.b_atoms = ha;
         g2.acc = acc;
@@ -470,10 +480,6 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     }
     if (err == cudaSuccess) err = moe_launch_finalize(T, D, acc, out, st);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-}
-
-static size_t atoms_bytes(const moe_desc &d) {
-    return align_up(3 * ((size_t)d.n_experts * d.d_model * d.d_ff / 32), 256);
 }
 
 static size_t wr_terms_bytes(const moe_desc &d) {
@@ -494,12 +500,12 @@ MOE_API int moe_prepare(moe_handle *h, void *buf, size_t bytes, void *stream) {
     const moe_desc &d = h->desc;
     const int E = d.n_experts, D = d.d_model, F = d.d_ff;
     uint8_t *out = (uint8_t *)buf;
-    const size_t per = (size_t)E * F * D / 32;
     cudaStream_t st = (cudaStream_t)stream;
     // gate/up tiles: 64 gate rows over the same 64 up rows; down tiles: 128 rows
     cudaError_t err = moe_launch_prepare_atoms(E, F, D, 64, h->w.gate_s, h->w.up_s, out, st);
     if (err == cudaSuccess)
-        err = moe_launch_prepare_atoms(E, D, F, 128, h->w.down_s, nullptr, out + 2 * per, st);
+        err = moe_launch_prepare_atoms(E, D, F, 128, h->w.down_s, nullptr, out + gu_atoms_bytes(d),
+                                       st);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     if (d.router_mode == MOE_ROUTER_XWR) {
         // W_r = t0 + t1 + t2 exactly, three bf16 [E][D] arrays after the scale atoms

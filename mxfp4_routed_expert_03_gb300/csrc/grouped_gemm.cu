@@ -37,15 +37,16 @@
 //
 // One persistent CTA per SM, 7 warps:
 //   warp 0      weight producer (one thread): weight tile(s) by TMA (packed
-//               E2M1 expanded to the 8-bit MMA layout) and the prepared
-//               512-byte scale atoms by bulk copy
+//               E2M1 expanded to the 8-bit MMA layout) and the prepared 1 KB
+//               scale block of the stage's two K blocks, once per TMEM quadrant
 //   warp 1      activation producer (one thread): the token tile's prepared
 //               [hi; lo] B tile and its scales, each one contiguous bulk copy
 //               per chunk; TMEM allocator
 //   warp 2      MMA issuer (one thread): tcgen05.cp scales, tcgen05.mma
 //   warps 3-6   epilogue, one 32-lane TMEM quadrant each
-// Weights and activations stream through separate mbarrier rings; the
-// accumulator is double-buffered in TMEM so the epilogue of tile i overlaps
+// Weights and activations share one "full" barrier per stage (both producers
+// arrive on it; the cluster peer's multicast bytes complete on it too) and
+// have separate release barriers; the accumulator is double-buffered in TMEM so the epilogue of tile i overlaps
 // the MMAs of tile i+1. Every wait is bounded: on expiry the CTA records
 // MOE_ERR_DEVICE_TIMEOUT and winds down.
 #include "common.cuh"
@@ -61,14 +62,13 @@ constexpr int NTMAX = MOE_GEMM_NTMAX;    // token rows per tile
 constexpr int A_BYTES = 128 * BK;        // smem bytes of the 128-row weight tile (E2M1 -> 8 bit)
 constexpr int A_TX = 128 * BK / 2;       // bytes the TMA moves for it (packed)
 constexpr int B_BYTES = 2 * NTMAX * BK;  // smem bytes of [hi; lo] activation rows
-constexpr int SF_BYTES = 512;            // one 128-row x 4-block scale atom
+constexpr int SF_BYTES = 1024;           // weight scales of one stage: 128 rows x 2 x 4 blocks
 constexpr int BSF_BYTES = 1024;          // activation scales of one chunk (256 B rows, 4 blocks)
 constexpr int NUM_THREADS = 224;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 2 * NTMAX;  // [hi | lo] accumulator columns per buffer
-constexpr uint32_t SF_TMEM_COL = 464;     // scales: 2 slots x KS blocks x (4 A + 8 B) columns
-constexpr uint32_t SF_SLOT = KS * 12;     // columns per slot
-constexpr uint32_t SF_SUB = 12;           // columns per block within a slot
+constexpr uint32_t SF_TMEM_COL = 464;     // scales: 2 slots x (KS x 4 A + KS x 8 B) columns
+constexpr uint32_t SF_SLOT = KS * 12;     // columns per slot: A blocks at 0, 4; B blocks at 8, 16
 constexpr int CL = MOE_GEMM_CLUSTER;      // CTAs per cluster sharing activation chunks
 constexpr uint16_t CL_MASK = (1u << CL) - 1;
 
@@ -77,14 +77,14 @@ struct Cfg {
     static constexpr int MROWS = (MODE == MOE_GEMM_GATEUP) ? 64 : 128;  // weight rows per tile
     static constexpr int SA = 2;  // weight ring stages (KS blocks each)
     static constexpr int SB = 2;  // activation ring stages
-    static constexpr int A_STAGE = (KS * (A_BYTES + SF_BYTES) + 1023) / 1024 * 1024;
-    static constexpr int A_SF = KS * A_BYTES;  // KS consecutive scale atoms
+    static constexpr int A_STAGE = KS * A_BYTES + 4 * SF_BYTES;  // scales once per TMEM quadrant
+    static constexpr int A_SF = KS * A_BYTES;
     // B: KS blocks of [hi; lo] rows, then KS x 4 scale copies (one per TMEM quadrant)
     static constexpr int B_STAGE = KS * (B_BYTES + 4 * BSF_BYTES);
     static constexpr int B_BASE = SA * A_STAGE;
     static constexpr int B_SF = KS * B_BYTES;
     static constexpr int BAR_BASE = B_BASE + SB * B_STAGE;
-    static constexpr int N_BARS = 2 * SA + 2 * SB + 4;
+    static constexpr int N_BARS = 3 * SA + 4;  // full, emptyA, emptyB per stage; tfull, tempty x2
     static constexpr int PREFIX_BASE = BAR_BASE + N_BARS * 8 + 16;  // int [active + 1]
     static constexpr int EXPERT_BASE = (PREFIX_BASE + (MOE_MAX_EXPERTS + 1) * 4 + 15) / 16 * 16;
     static constexpr int SEG_BASE = (EXPERT_BASE + MOE_MAX_EXPERTS * 4 + 15) / 16 * 16;  // int2
@@ -97,6 +97,7 @@ struct Cfg {
                       SEG_BASE % 16 == 0 && EPI_BASE % 16 == 0,
                   "shared-memory regions must be 16-byte aligned (int2 / float4 accesses)");
     static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(SA == SB, "one full barrier per stage serves both operands");
 };
 
 struct Tile {
@@ -169,10 +170,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t *fullA = (uint64_t *)(smem + C::BAR_BASE);
-    uint64_t *emptyA = fullA + C::SA;
-    uint64_t *fullB = emptyA + C::SA;
-    uint64_t *emptyB = fullB + C::SB;
+    uint64_t *full = (uint64_t *)(smem + C::BAR_BASE);
+    uint64_t *emptyA = full + C::SA;
+    uint64_t *emptyB = emptyA + C::SA;
     uint64_t *tfull = emptyB + C::SB;
     uint64_t *tempty = tfull + 2;
     uint32_t *tmem_slot = (uint32_t *)(tempty + 2);
@@ -201,11 +201,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
     if (tid == 0) {
         *abort_flag = 0;
         for (int s = 0; s < C::SA; ++s) {
-            tc::mbar_init(&fullA[s], 1);
+            tc::mbar_init(&full[s], 2);      // the weight and the activation producer
             tc::mbar_init(&emptyA[s], 1);
-        }
-        for (int s = 0; s < C::SB; ++s) {
-            tc::mbar_init(&fullB[s], 1);
             tc::mbar_init(&emptyB[s], CL);  // released by every CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
@@ -248,7 +245,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                     continue;
                 }
                 const int row0 = t.e * args.M + t.mt * C::MROWS;
-                const size_t atom0 = ((size_t)t.e * MT + t.mt) * KC;
+                const size_t atom0 = ((size_t)t.e * MT + t.mt) * ((KC + KS - 1) / KS);
                 for (int kc = 0; kc < KC; kc += KS, ++it) {
                     const int s = it % C::SA, round = it / C::SA;
                     const int nsub = min(KS, KC - kc);
@@ -258,16 +255,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                         break;
                     }
                     unsigned char *st = smem + s * C::A_STAGE;
-                    tc::mbar_arrive_expect_tx(&fullA[s], (uint32_t)(nsub * (A_TX + SF_BYTES)));
+                    tc::mbar_arrive_expect_tx(&full[s], (uint32_t)(nsub * A_TX + 4 * SF_BYTES));
                     for (int sub = 0; sub < nsub; ++sub) {
                         unsigned char *sa = st + sub * A_BYTES;
-                        tc::tma_load_2d(sa, &mapA, &fullA[s], (kc + sub) * BK, row0, pol_w);
+                        tc::tma_load_2d(sa, &mapA, &full[s], (kc + sub) * BK, row0, pol_w);
                         if (MODE == MOE_GEMM_GATEUP)  // up rows fill lanes 64..127
-                            tc::tma_load_2d(sa + 64 * BK, &mapA2, &fullA[s], (kc + sub) * BK, row0,
+                            tc::tma_load_2d(sa + 64 * BK, &mapA2, &full[s], (kc + sub) * BK, row0,
                                             pol_w);
                     }
-                    tc::bulk_copy_g2s(st + C::A_SF, args.a_atoms + (atom0 + kc) * SF_BYTES,
-                                      nsub * SF_BYTES, &fullA[s], pol_w);
+                    const uint8_t *sf = args.a_atoms + (atom0 + kc / KS) * SF_BYTES;
+                    for (int qd = 0; qd < 4; ++qd)  // one copy per TMEM lane quadrant
+                        tc::bulk_copy_g2s(st + C::A_SF + qd * SF_BYTES, sf, SF_BYTES, &full[s], pol_w);
                 }
             }
         }
@@ -293,18 +291,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                     }
                     unsigned char *st = smem + C::B_BASE + s * C::B_STAGE;
                     // the whole stage lands here; this CTA fetches its 1/CL share for all
-                    tc::mbar_arrive_expect_tx(&fullB[s], (uint32_t)nsub * (tile_bytes + 4 * BSF_BYTES));
+                    tc::mbar_arrive_expect_tx(&full[s], (uint32_t)nsub * (tile_bytes + 4 * BSF_BYTES));
                     const uint32_t part = tile_bytes / CL;
                     for (int sub = 0; sub < nsub; ++sub) {
                         const size_t blk = blk0 + kc + sub;
                         tc::bulk_copy_g2s_multicast(
                             st + sub * B_BYTES + rank * part,
-                            args.b_tiles + blk * MOE_GEMM_BTILE + rank * part, part, &fullB[s],
+                            args.b_tiles + blk * MOE_GEMM_BTILE + rank * part, part, &full[s],
                             CL_MASK, pol_x);
                         for (int qd = rank; qd < 4; qd += CL)  // one copy per TMEM lane quadrant
                             tc::bulk_copy_g2s_multicast(
                                 st + C::B_SF + (sub * 4 + qd) * BSF_BYTES,
-                                args.b_atoms + blk * BSF_BYTES, BSF_BYTES, &fullB[s], CL_MASK, pol_x);
+                                args.b_atoms + blk * BSF_BYTES, BSF_BYTES, &full[s], CL_MASK, pol_x);
                     }
                 }
             }
@@ -339,8 +337,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                     const int sa = it % C::SA, ra = it / C::SA;
                     const int sb = it % C::SB, rb = it / C::SB;
                     const int nsub = min(KS, KC - kc);
-                    if (!tc::mbar_wait(&fullA[sa], ra & 1, LIMIT, abort_p) ||
-                        !tc::mbar_wait(&fullB[sb], rb & 1, LIMIT, abort_p)) {
+                    if (!tc::mbar_wait(&full[sa], ra & 1, LIMIT, abort_p)) {
                         fail();
                         ok = false;
                         break;
@@ -348,10 +345,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                     const uint32_t a_s = tc::smem_u32(smem + sa * C::A_STAGE);
                     const uint32_t b_s = tc::smem_u32(smem + C::B_BASE + sb * C::B_STAGE);
                     const uint32_t slot = tmem + SF_TMEM_COL + (uint32_t)(it & 1) * SF_SLOT;
+                    // both blocks' weight scales in one copy: columns slot .. slot + 7
+                    tc::tmem_cp_128x256b(slot, tc::sdesc_plain_128x32(a_s + C::A_SF));
                     for (int sub = 0; sub < nsub; ++sub) {
-                        const uint32_t sfa = slot + sub * SF_SUB, sfb = sfa + 4;
-                        tc::tmem_cp_32x128b_warpx4(
-                            sfa, tc::sdesc_plain_32x16(a_s + C::A_SF + sub * SF_BYTES));
+                        const uint32_t sfa = slot + 4 * sub, sfb = slot + 8 + 8 * sub;
                         tc::tmem_cp_128x256b(
                             sfb, tc::sdesc_plain_128x32(b_s + C::B_SF + sub * 4 * BSF_BYTES));
                         const uint32_t as = a_s + sub * A_BYTES, bs = b_s + sub * B_BYTES;
@@ -520,25 +517,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
     tc::cluster_sync();  // no CTA leaves while a peer may still multicast into it
 }
 
-// Weight scales re-laid as 512-byte tensor-core scale atoms, one per
-// (expert, weight tile, 128-wide K chunk): tile row m, 32-wide block c at byte
-// (m % 32) * 16 + (m / 32) * 4 + c. For the gate/up GEMM a tile's rows 0..63
-// are gate rows mt*64 .. and rows 64..127 the same up rows; for the down GEMM
-// a tile is 128 consecutive rows. One thread per 4-byte word.
+// Weight scales re-laid for the tensor cores: one 1 KB block per (expert,
+// weight tile, pair of 128-wide K blocks), in the layout a 128x256b
+// tcgen05.cp reads for one TMEM lane quadrant (8-row x 16-byte core
+// matrices): lane l (0..31), 32-bit column j (0..7) at byte
+// (l / 8) * 256 + (j / 4) * 128 + (l % 8) * 16 + (j % 4) * 4. Column j holds
+// the four 32-wide block scales of tile row 32 * (j % 4) + l in K block
+// 2 * pair + j / 4 (zero past the last block). For the gate/up GEMM a tile's
+// rows 0..63 are gate rows mt*64 .. and rows 64..127 the same up rows; for
+// the down GEMM a tile is 128 consecutive rows. One thread per 4-byte word.
 __global__ void __launch_bounds__(256) moe_prepare_atoms_kernel(int64_t words, int M, int K,
                                                                 int mrows, const uint8_t *__restrict__ s,
                                                                 const uint8_t *__restrict__ s2,
                                                                 uint32_t *__restrict__ out) {
     int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (w >= words) return;
-    const int MT = M / mrows, KC = K / BK, ksb = K / 32;
-    int64_t atom = w / 128;
-    int j = (int)(w % 128);
-    int m = (j % 4) * 32 + j / 4;  // inverse of the word index (m % 32) * 4 + m / 32
-    int kc = (int)(atom % KC);
-    int64_t em = atom / KC;  // e * MT + mt
-    int mt = (int)(em % MT);
-    int64_t e = em / MT;
+    const int MT = M / mrows, KC = K / BK, NP = (KC + KS - 1) / KS, ksb = K / 32;
+    const int64_t blk = w / 256;
+    const int wi = (int)(w % 256);
+    const int l = (wi / 64) * 8 + (wi % 32) / 4;   // lane
+    const int j = ((wi % 64) / 32) * 4 + wi % 4;   // column
+    const int m = 32 * (j % 4) + l;                // tile row
+    const int pair = (int)(blk % NP);
+    const int64_t em = blk / NP;  // e * MT + mt
+    const int mt = (int)(em % MT);
+    const int64_t e = em / MT;
+    const int kc = KS * pair + j / 4;
+    if (kc >= KC) {
+        out[w] = 0u;
+        return;
+    }
     const uint8_t *src;
     if (s2 && m >= 64) src = s2 + ((e * M + (int64_t)mt * mrows + (m - 64)) * ksb + kc * 4);
     else src = s + ((e * M + (int64_t)mt * mrows + m) * ksb + kc * 4);
@@ -552,10 +560,14 @@ size_t moe_gemm_smem_bytes(int mode) {
     return mode == MOE_GEMM_GATEUP ? Cfg<MOE_GEMM_GATEUP>::SMEM : Cfg<MOE_GEMM_DOWN>::SMEM;
 }
 
+size_t moe_prepared_atoms_bytes(int E, int M, int K, int mrows) {
+    const int KC = K / BK, NP = (KC + KS - 1) / KS;
+    return (size_t)E * (M / mrows) * NP * SF_BYTES;
+}
+
 cudaError_t moe_launch_prepare_atoms(int E, int M, int K, int mrows, const uint8_t *s,
                                      const uint8_t *s2, uint8_t *out, cudaStream_t st) {
-    const int64_t rows = s2 ? 2 * (int64_t)M : (int64_t)M;  // gate and up together
-    int64_t words = (int64_t)E * rows * (K / 32) / 4;
+    const int64_t words = (int64_t)(moe_prepared_atoms_bytes(E, M, K, mrows) / 4);
     moe_prepare_atoms_kernel<<<(unsigned)((words + 255) / 256), 256, 0, st>>>(
         words, M, K, mrows, s, s2, (uint32_t *)out);
     return cudaGetLastError();

@@ -68,7 +68,7 @@ struct MoeGemmArgs {
     int Dout;                // row stride of the fp32 output accumulator (d_model)
     const int32_t *offsets, *perm, *active, *tt_prefix;
     const float *topk_w;
-    const uint8_t *a_atoms;  // weight scale atoms [E][weight tiles][K/128][512 B]
+    const uint8_t *a_atoms;  // weight scale blocks [E][weight tiles][K/256][1 KB]
     const uint8_t *b_tiles;  // activation B tiles [token tile][K/128][2*NTMAX rows][128 B]:
                              // rows [0, nmma) the hi term, [nmma, 2 nmma) the lo term,
                              // each 128-byte row pre-swizzled (16-byte chunk c at c ^ row % 8)
@@ -81,6 +81,7 @@ struct MoeGemmArgs {
 };
 
 size_t moe_gemm_smem_bytes(int mode);
+size_t moe_prepared_atoms_bytes(int E, int M, int K, int mrows);
 cudaError_t moe_launch_prepare_atoms(int E, int M, int K, int mrows, const uint8_t *s,
                                      const uint8_t *s2, uint8_t *out, cudaStream_t st);
 cudaError_t moe_launch_gemm(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
