@@ -3,8 +3,10 @@
 
 Default workload: one K3-shaped routed layer (d_model 7168, d_ff 1536, 896
 experts, top-16, MXFP4 weights resident in HBM), decode batches of T = 1, 4
-and 16 tokens; one step = moe_plan + moe_decode for each of the three
-batches (21 tokens). `--workload prefill4k|skewed8k` times moe_plan +
+and 16 tokens; one step = moe_plan + the expert FFN for each of the three
+batches (21 tokens). The FFN call follows the decode/prefill crossover at 8
+tokens: moe_decode (CUDA-core streaming) for T <= 8, moe_forward (tcgen05
+grouped GEMMs) above; `--path decode|forward` forces one of them. `--workload prefill4k|skewed8k` times moe_plan +
 moe_forward on one prefill batch instead; `--workload router16k` times the
 long prefill whose logits come from the library's own fp32 router (x . W_r)
 and which adds one bf16 shared expert.
@@ -39,9 +41,10 @@ EXPERT_BYTES = 17547264            # one expert's three MXFP4 matrices (codes + 
 GATEUP_BYTES = 2 * (D_FF * D_MODEL // 2 + D_FF * D_MODEL // 32)
 DOWN_BYTES = D_MODEL * D_FF // 2 + D_MODEL * D_FF // 32
 N_SETS = 8
+CROSSOVER_T = 8   # largest batch the CUDA-core decode path takes under --path auto
 
 BENCH_WORKLOADS = {
-    "decode": {"Ts": [1, 4, 16], "path": "decode",
+    "decode": {"Ts": [1, 4, 16], "path": "auto",
                "desc": "K3 routed layer decode, T=1,4,16 (d_model 7168, d_ff 1536, 896 experts, top-16, MXFP4)"},
     "prefill4k": {"Ts": [4096], "path": "forward",
                   "desc": "K3 routed layer prefill, T=4096, uniform routing"},
@@ -61,8 +64,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default="decode")
-    ap.add_argument("--path", choices=["decode", "forward"], default=None,
-                    help="entry point for the batches (default: decode for decode, forward for prefill)")
+    ap.add_argument("--path", choices=["decode", "forward", "auto"], default=None,
+                    help="entry point for the batches (default: auto for decode -- moe_decode "
+                         "up to 8 tokens, moe_forward above -- and forward for prefill)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall-time budget of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -192,9 +196,11 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-def kernel_traffic(name: str, source: str):
-    """dram bytes per launch of `name` from the committed ncu summary, or None
-    when the summary was taken on a different version of the kernel source."""
+def kernel_traffic(name: str, source: str, workload: str):
+    """DRAM bytes per launch of `name` in `workload` from the committed ncu
+    summary (profiles/traffic.txt: name, sha256[:16] of the kernel source,
+    workload, bytes), or None when it was taken on another version of the
+    kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     src = os.path.join(ROOT, "mxfp4_routed_expert_03_gb300", "csrc", source)
     if not (os.path.exists(path) and os.path.exists(src)):
@@ -202,7 +208,7 @@ def kernel_traffic(name: str, source: str):
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     for line in open(path):
         parts = line.split()
-        if len(parts) == 4 and parts[0] == name and parts[1] == sha:
+        if len(parts) == 4 and parts[0] == name and parts[1] == sha and parts[2] == workload:
             return float(parts[3])
     return None
 
@@ -248,7 +254,11 @@ def run_ours(args):
         layer = Layer(D_MODEL, D_FF, n_exp, TOP_K, weights, MOE_ROUTER_XWR, w_router, shared)
     else:
         layer = Layer(D_MODEL, D_FF, n_exp, TOP_K, weights)
-    if path == "forward" or use_router:
+    def path_of(T):
+        if path == "auto":
+            return "decode" if T <= CROSSOVER_T else "forward"
+        return path
+    if use_router or any(path_of(T) == "forward" for T in wl["Ts"]):
         layer.prepare()
     stream = torch.cuda.current_stream()
 
@@ -270,18 +280,22 @@ def run_ours(args):
                         "out": torch.empty((T, D_MODEL), dtype=torch.int16, device=dev),
                         "dx": torch.empty((T, D_MODEL), dtype=torch.int16, device=dev),
                         "dl": torch.empty((T, n_exp), dtype=torch.float32, device=dev),
-                        "hout": torch.empty((T, D_MODEL), dtype=torch.int16).pin_memory()})
+                        "hout": torch.empty((T, D_MODEL), dtype=torch.int16).pin_memory(),
+                        "path": path_of(T)})
     for b in batches:  # size the workspace once for the largest call
-        layer.workspace(b["T"], 2 if path == "decode" else 1)
-    run = layer.decode if path == "decode" else layer.forward
-    prof_kind = MOE_PROF_DECODE_GATEUP if path == "decode" else MOE_PROF_FORWARD_GEMM1
+        for op in (0, 1, 2):
+            layer.workspace(b["T"], op)
+    # the kernel whose launches are timed in each batch: the path's main one
+    main_kind = {"decode": MOE_PROF_DECODE_GATEUP, "forward": MOE_PROF_FORWARD_GEMM1}
 
-    def step(i, events=None, e2e=False, prof_kind=prof_kind):
+    def step(i, events=None, e2e=False, prof_kind=None):
         for bi, b in enumerate(batches):
             s = i % n_sets
+            run = layer.decode if b["path"] == "decode" else layer.forward
             if events is not None:
                 ev0, ev1 = events[bi]
-                check(moe_profile_kernel(layer.h, prof_kind, ev0, ev1), "profile")
+                kind = prof_kind if prof_kind is not None else main_kind[b["path"]]
+                check(moe_profile_kernel(layer.h, kind, ev0, ev1), "profile")
             if e2e:
                 b["dx"].copy_(b["px"][s], non_blocking=True)
                 if not use_router:
@@ -293,7 +307,7 @@ def run_ours(args):
                 check(layer.plan(b["T"], None, x, b["plan"], stream), "moe_plan")
             else:
                 check(layer.plan(b["T"], lg, None, b["plan"], stream), "moe_plan")
-            check(run(b["T"], x, b["plan"], b["out"], stream), "moe_" + path)
+            check(run(b["T"], x, b["plan"], b["out"], stream), "moe_" + b["path"])
             if e2e:
                 b["hout"].copy_(b["out"], non_blocking=True)
 
@@ -351,9 +365,11 @@ def run_ours(args):
 
     # per-kernel breakdown (separate untimed pass, one kernel bracketed at a time)
     breakdown = {}
-    kinds = ([("decode_gateup", moe.MOE_PROF_DECODE_GATEUP), ("decode_down", moe.MOE_PROF_DECODE_DOWN)]
-             if path == "decode" else
-             [("gemm1_gateup", moe.MOE_PROF_FORWARD_GEMM1), ("gemm2_down", moe.MOE_PROF_FORWARD_GEMM2)])
+    kinds = []
+    if any(b["path"] == "decode" for b in batches):
+        kinds += [("decode_gateup", moe.MOE_PROF_DECODE_GATEUP), ("decode_down", moe.MOE_PROF_DECODE_DOWN)]
+    if any(b["path"] == "forward" for b in batches):
+        kinds += [("gemm1_gateup", moe.MOE_PROF_FORWARD_GEMM1), ("gemm2_down", moe.MOE_PROF_FORWARD_GEMM2)]
     if use_router:
         kinds += [("router", moe.MOE_PROF_ROUTER), ("shared_gateup", moe.MOE_PROF_SHARED_GATEUP),
                   ("shared_down", moe.MOE_PROF_SHARED_DOWN)]
@@ -368,58 +384,82 @@ def run_ours(args):
         for i in range(n_bd):
             step(i, events=ev[i], prof_kind=kid)
         torch.cuda.synchronize()
-        breakdown[name] = float(np.mean([a.elapsed_time(b) for row in ev for (a, b) in row]))
+        # mean per call of the batches that launch this kernel
+        used = [bi for bi, b in enumerate(batches)
+                if (b["path"] == "decode") == name.startswith("decode") or name in
+                ("router", "shared_gateup", "shared_down")]
+        breakdown[name] = float(np.mean([ev[i][bi][0].elapsed_time(ev[i][bi][1])
+                                         for i in range(n_bd) for bi in used]))
     check(moe_profile_kernel(layer.h, MOE_PROF_NONE), "profile")
     tokens_step = sum(wl["Ts"])
     value = world * tokens_step * args.steps / (elapsed_ms * 1e-3)
     e2e_value = world * tokens_step * args.steps / (e2e_ms * 1e-3)
 
-    # roofline of the dominant kernel (algorithmic bytes or flops per launch)
+    # roofline of the dominant kernel: the timed kernel (per batch, its path's
+    # main kernel) with the largest share of the timed region; its bound is
+    # the one its arithmetic intensity puts it under
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
         if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    fp8_peak = 2.0 * peaks.get("bf16_tflops", 1900.0)  # kind::mxf8f6f4 runs at the FP8 rate
     act = [int(b["plan"].active[0].item()) for b in batches]
-    tot_k_ms = float(np.sum(kern_ms))
-    n_launch = args.steps * n_b
-    if path == "decode":
+    per_batch_ms = np.mean(np.array(kern_ms), axis=0)   # mean launch time per batch
+    kinds_t = {}
+    for bi, b in enumerate(batches):
+        kinds_t.setdefault(b["path"], []).append(bi)
+    dom = max(kinds_t, key=lambda k: sum(per_batch_ms[bi] for bi in kinds_t[k]))
+    bis = kinds_t[dom]
+    ms_avg = float(np.mean([per_batch_ms[bi] for bi in bis]))
+    if dom == "decode":
         # gate/up kernel: active experts' gate+up codes and scales, f16 x rows read,
-        # f16 h and its exponents written. Active counts vary per step; the
-        # expected count is taken from the last step's plans.
-        per_launch = [a * GATEUP_BYTES + T * D_MODEL * 2 + T * TOP_K * (D_FF * 2 + D_FF // 32)
-                      for a, T in zip(act, wl["Ts"])]
-        achieved = sum(per_launch) / len(per_launch) / (tot_k_ms / n_launch * 1e-3) / 1e9
-        peak = peaks.get("hbm_gbs", 6800.0)
-        roof = {"bound": "hbm", "kernel": "moe_decode_gateup_kernel", "achieved": achieved,
-                "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
-                "bytes_per_launch": sum(per_launch) / len(per_launch),
-                "traffic": kernel_traffic("moe_decode_gateup_kernel", "decode.cu")}
+        # f16 h and its exponents written (active counts from the last step's plans)
+        nbytes = [act[bi] * GATEUP_BYTES + wl["Ts"][bi] * D_MODEL * 2 +
+                  wl["Ts"][bi] * TOP_K * (D_FF * 2 + D_FF // 32) for bi in bis]
+        nflop = [2.0 * wl["Ts"][bi] * TOP_K * 2 * D_MODEL * D_FF for bi in bis]
+        kname, src, tkey = "moe_decode_gateup_kernel", "decode.cu", args.workload
     else:
-        flops = [2.0 * T * TOP_K * 2 * D_MODEL * D_FF for T in wl["Ts"]]
-        achieved = sum(flops) / len(flops) / (tot_k_ms / n_launch * 1e-3) / 1e12
-        # kind::mxf8f6f4 runs at the FP8 tensor rate: measured bf16 x (4.5 / 2.25 nominal)
-        peak = 2.0 * peaks.get("bf16_tflops", 1900.0)
-        roof = {"bound": "tensor", "kernel": "moe_grouped_gemm_kernel<gate/up>", "achieved": achieved,
-                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "frac_of_fp4_peak": achieved / (6.0 * peaks.get("bf16_tflops", 1900.0)),
-                "peak_source": ("measured bf16 x 2 (fp8 rate); the two-term activation split "
-                                "issues 2 MMAs per algorithmic one, so frac <= 0.5")
-                if "bf16_tflops" in peaks else "fallback",
-                "traffic": kernel_traffic("moe_grouped_gemm_kernel<0>", "grouped_gemm.cu")}
+        # GEMM1: active experts' gate+up weights, two-term activation tiles in,
+        # two-term h tiles out (one byte per term and element)
+        nbytes = [act[bi] * GATEUP_BYTES + wl["Ts"][bi] * TOP_K * (2 * D_MODEL + 2 * D_FF)
+                  for bi in bis]
+        nflop = [2.0 * wl["Ts"][bi] * TOP_K * 2 * D_MODEL * D_FF for bi in bis]
+        kname, src, tkey = "moe_grouped_gemm_kernel<0>", "grouped_gemm.cu", args.workload
+    b_avg, f_avg = float(np.mean(nbytes)), float(np.mean(nflop))
+    gbs = b_avg / (ms_avg * 1e-3) / 1e9
+    tfs = f_avg / (ms_avg * 1e-3) / 1e12
+    mem_bound = (b_avg / hbm_peak) >= (f_avg / 1e3 / fp8_peak)  # time at peak: bytes vs flops
+    src_peak = "measured" if peaks else "fallback"
+    if mem_bound:
+        roof = {"bound": "hbm", "kernel": kname, "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": gbs / hbm_peak, "peak_source": src_peak + " (copy bandwidth)",
+                "bytes_per_launch": b_avg, "tensor_TFLOPs": tfs, "frac_of_fp8_peak": tfs / fp8_peak}
+    else:
+        roof = {"bound": "tensor", "kernel": kname, "achieved": tfs, "peak": fp8_peak,
+                "unit": "TFLOP/s", "frac": tfs / fp8_peak,
+                "peak_source": src_peak + " bf16 x 2 (FP8 rate; the two-term activation split "
+                               "issues 2 MMAs per algorithmic one, so frac <= 0.5)",
+                "flop_per_launch": f_avg, "hbm_GBs": gbs, "frac_of_hbm": gbs / hbm_peak}
+    roof["frac_of_fp4_peak"] = tfs / (6.0 * peaks.get("bf16_tflops", 1900.0))
+    roof["traffic"] = kernel_traffic(kname, src, tkey)
 
     # plan: one fused kernel for T <= 64, else top-k, count, scan, scatter;
     # decode: gate/up, down, combine; forward: quant, schedule, gather, two GEMMs, finalize
-    launches_per_call = 1 if max(wl["Ts"]) <= 64 else 4
-    launches_per_call += 3 if path == "decode" else 6
-    if use_router:
-        launches_per_call += 1 + 2   # router GEMM; shared gate/up and down GEMMs
+    launches = 0
+    for b in batches:
+        launches += 1 if b["T"] <= 64 else 4
+        launches += 3 if b["path"] == "decode" else 6
+        if use_router:
+            launches += 1 + 2   # router GEMM; shared gate/up and down GEMMs
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "mxfp4 x f16 -> f32" if path == "decode" else "mxfp4 x 2-term e4m3 -> f32",
+        "dtype": " / ".join(sorted({"mxfp4 x f16 -> f32" if b["path"] == "decode" else
+                                    "mxfp4 x 2-term e4m3 -> f32" for b in batches})),
         "data": "synthetic (seeded Philox weights, N(0,1) activations and logits)",
         "config": {"workload": wl["desc"],
-                   "path": ("moe_plan (router) + moe_" if use_router else "moe_plan + moe_") + path,
+                   "path": ("moe_plan (router)" if use_router else "moe_plan") + " + " +
+                           ", ".join(f"moe_{b['path']} (T={b['T']})" for b in batches),
                    "tokens_per_step": tokens_step, "active_experts_last_step": act,
                    "kernel_ms_per_call": breakdown,
                    "l2": "inputs larger than L2 (>=280 MB of expert weights per batch, "
@@ -431,7 +471,7 @@ def run_ours(args):
                 "h2d_bytes_per_step": sum(T * D_MODEL * 2 + (0 if use_router else T * n_exp * 4)
                                           for T in wl["Ts"]),
                 "d2h_bytes_per_step": sum(T * D_MODEL * 2 for T in wl["Ts"])},
-        "gpu_launches": launches_per_call * len(wl["Ts"]) * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -453,7 +453,7 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         g1.h_tiles = hb;
         g1.h_atoms = ha;
         h->prof.before(MOE_PROF_FORWARD_GEMM1, st);
-        err = moe_launch_gemm(MOE_GEMM_GATEUP, &h->map_gate, &h->map_up, &g1, h->num_sms, st);
+        err = moe_launch_gemm(MOE_GEMM_GATEUP, &h->map_gate, &h->map_up, &g1, T, h->num_sms, st);
         h->prof.after(MOE_PROF_FORWARD_GEMM1, st);
     }
     if (err == cudaSuccess) {
@@ -475,7 +475,7 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         g2.b_atoms = ha;
         g2.acc = acc;
         h->prof.before(MOE_PROF_FORWARD_GEMM2, st);
-        err = moe_launch_gemm(MOE_GEMM_DOWN, &h->map_down, &h->map_down, &g2, h->num_sms, st);
+        err = moe_launch_gemm(MOE_GEMM_DOWN, &h->map_down, &h->map_down, &g2, T, h->num_sms, st);
         h->prof.after(MOE_PROF_FORWARD_GEMM2, st);
     }
     if (err == cudaSuccess) err = moe_launch_finalize(T, D, acc, out, st);

@@ -58,10 +58,9 @@ namespace {
 
 constexpr int BK = 128;                  // K elements per block (data-layout unit)
 constexpr int KS = 2;                    // blocks per pipeline stage
-constexpr int NTMAX = MOE_GEMM_NTMAX;    // token rows per tile
+constexpr int NTMAX = MOE_GEMM_NTMAX;    // token rows per tile (wide variant)
 constexpr int A_BYTES = 128 * BK;        // smem bytes of the 128-row weight tile (E2M1 -> 8 bit)
 constexpr int A_TX = 128 * BK / 2;       // bytes the TMA moves for it (packed)
-constexpr int B_BYTES = 2 * NTMAX * BK;  // smem bytes of [hi; lo] activation rows
 constexpr int SF_BYTES = 1024;           // weight scales of one stage: 128 rows x 2 x 4 blocks
 constexpr int BSF_BYTES = 1024;          // activation scales of one chunk (256 B rows, 4 blocks)
 constexpr int NUM_THREADS = 224;
@@ -72,15 +71,25 @@ constexpr uint32_t SF_SLOT = KS * 12;     // columns per slot: A blocks at 0, 4;
 constexpr int CL = MOE_GEMM_CLUSTER;      // CTAs per cluster sharing activation chunks
 constexpr uint16_t CL_MASK = (1u << CL) - 1;
 
-template <int MODE>
+// NT: token rows per tile. The wide variant (NT = NTMAX) serves prefill; the
+// narrow one (NT = MOE_GEMM_NT_NARROW, when no expert has more than NT routed
+// rows) spends the activation ring's shared memory on a deeper weight ring,
+// since with few tokens per expert the GEMM streams weights and is bound by
+// the weight bytes it keeps in flight.
+template <int MODE, int NT>
 struct Cfg {
     static constexpr int MROWS = (MODE == MOE_GEMM_GATEUP) ? 64 : 128;  // weight rows per tile
-    static constexpr int SA = 2;  // weight ring stages (KS blocks each)
-    static constexpr int SB = 2;  // activation ring stages
+    static constexpr int SA = NT <= 16 ? 4 : 2;  // weight ring stages (KS blocks each)
+    static constexpr int SB = SA;                // activation ring stages
     static constexpr int A_STAGE = KS * A_BYTES + 4 * SF_BYTES;  // scales once per TMEM quadrant
     static constexpr int A_SF = KS * A_BYTES;
-    // B: KS blocks of [hi; lo] rows, then KS x 4 scale copies (one per TMEM quadrant)
-    static constexpr int B_STAGE = KS * (B_BYTES + 4 * BSF_BYTES);
+    static constexpr int B_BYTES = 2 * NT * BK;  // smem bytes of [hi; lo] activation rows
+    // Activation scales per block: B rows < 128 need TMEM columns 0..3 only,
+    // which one 32x128b.warpx4 copy of the 1 KB block fills in every lane
+    // quadrant; wider tiles take four copies of the block and one 128x256b copy.
+    static constexpr int BSF_COPIES = 2 * NT <= 128 ? 1 : 4;
+    // B: KS blocks of [hi; lo] rows, then KS x BSF_COPIES scale blocks
+    static constexpr int B_STAGE = KS * (B_BYTES + BSF_COPIES * BSF_BYTES);
     static constexpr int B_BASE = SA * A_STAGE;
     static constexpr int B_SF = KS * B_BYTES;
     static constexpr int BAR_BASE = B_BASE + SB * B_STAGE;
@@ -116,6 +125,7 @@ struct Tile {
 // prefix, the active experts and their (first slot, rows) segments. Each
 // role visits its tiles in increasing order, so `a` (the caller's cursor,
 // starting at 0) only moves forward: a few shared-memory reads per tile.
+template <int NT>
 __device__ __forceinline__ bool tile_at(int ct, int n_active, int MTG, int rank,
                                         const int *s_prefix, const int *s_expert,
                                         const int2 *s_seg, int &a, Tile &t) {
@@ -136,7 +146,7 @@ __device__ __forceinline__ bool tile_at(int ct, int n_active, int MTG, int rank,
     t.n = r1 - r0;
     t.nmma = (t.n + 15) & ~15;
     t.tt = s_prefix[a] + j;
-    return t.n > 0 && t.n <= NTMAX;
+    return t.n > 0 && t.n <= NT;
 }
 
 // Position of (row m, 32-wide K block c) inside a 128-row x 4-block scale atom.
@@ -162,11 +172,11 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" :::
 
 }  // namespace
 
-template <int MODE>
+template <int MODE, int NT>
 __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
     const MoeGemmArgs args) {
-    using C = Cfg<MODE>;
+    using C = Cfg<MODE, NT>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
             int cur = 0;
             for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
                 Tile t;
-                if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) {
+                if (!tile_at<NT>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) {
                     moe_flag(args.status, MOE_ERR_BAD_INDEX);
                     continue;
                 }
@@ -278,7 +288,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
             int cur = 0;
             for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
                 Tile t;
-                if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) continue;
+                if (!tile_at<NT>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) continue;
                 const uint32_t tile_bytes = (uint32_t)(2 * t.nmma * BK);
                 const size_t blk0 = (size_t)t.tt * KC;
                 for (int kc = 0; kc < KC; kc += KS, ++it) {
@@ -291,17 +301,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                     }
                     unsigned char *st = smem + C::B_BASE + s * C::B_STAGE;
                     // the whole stage lands here; this CTA fetches its 1/CL share for all
-                    tc::mbar_arrive_expect_tx(&full[s], (uint32_t)nsub * (tile_bytes + 4 * BSF_BYTES));
+                    tc::mbar_arrive_expect_tx(
+                        &full[s], (uint32_t)nsub * (tile_bytes + C::BSF_COPIES * BSF_BYTES));
                     const uint32_t part = tile_bytes / CL;
                     for (int sub = 0; sub < nsub; ++sub) {
                         const size_t blk = blk0 + kc + sub;
                         tc::bulk_copy_g2s_multicast(
-                            st + sub * B_BYTES + rank * part,
+                            st + sub * C::B_BYTES + rank * part,
                             args.b_tiles + blk * MOE_GEMM_BTILE + rank * part, part, &full[s],
                             CL_MASK, pol_x);
-                        for (int qd = rank; qd < 4; qd += CL)  // one copy per TMEM lane quadrant
+                        for (int qd = rank; qd < C::BSF_COPIES; qd += CL)
                             tc::bulk_copy_g2s_multicast(
-                                st + C::B_SF + (sub * 4 + qd) * BSF_BYTES,
+                                st + C::B_SF + (sub * C::BSF_COPIES + qd) * BSF_BYTES,
                                 args.b_atoms + blk * BSF_BYTES, BSF_BYTES, &full[s], CL_MASK, pol_x);
                     }
                 }
@@ -319,7 +330,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
             int cur = 0;
             for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
                 Tile t;
-                if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) continue;
+                if (!tile_at<NT>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) continue;
                 const int buf = lt & 1, use = lt >> 1;
                 ++lt;
                 if (use > 0 && !tc::mbar_wait(&tempty[buf], (use - 1) & 1, LIMIT, abort_p)) {
@@ -349,9 +360,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                     tc::tmem_cp_128x256b(slot, tc::sdesc_plain_128x32(a_s + C::A_SF));
                     for (int sub = 0; sub < nsub; ++sub) {
                         const uint32_t sfa = slot + 4 * sub, sfb = slot + 8 + 8 * sub;
-                        tc::tmem_cp_128x256b(
-                            sfb, tc::sdesc_plain_128x32(b_s + C::B_SF + sub * 4 * BSF_BYTES));
-                        const uint32_t as = a_s + sub * A_BYTES, bs = b_s + sub * B_BYTES;
+                        const uint32_t bsf = b_s + C::B_SF + sub * C::BSF_COPIES * BSF_BYTES;
+                        if (C::BSF_COPIES == 1)  // columns 0..3 (B rows < 128), all quadrants
+                            tc::tmem_cp_32x128b_warpx4(sfb, tc::sdesc_plain_32x16_groups256(bsf));
+                        else
+                            tc::tmem_cp_128x256b(sfb, tc::sdesc_plain_128x32(bsf));
+                        const uint32_t as = a_s + sub * A_BYTES, bs = b_s + sub * C::B_BYTES;
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             tc::mma_mxf8f6f4(acc, tc::sdesc_sw128(as + 32 * k),
@@ -381,17 +395,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
         int lt = 0, cur = 0;
         for (int tile = cluster_id; tile < total_tiles; tile += n_clusters) {
             Tile t;
-            if (!tile_at(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t))
+            if (!tile_at<NT>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t))
                 continue;
             const int buf = lt & 1, use = lt >> 1;
             ++lt;
             // GEMM2: the tile's token rows and routing weights, read before the
             // accumulator is ready (column lane + 32 i of the tile in pf[i], pw[i])
-            int pf[NTMAX / 32 + 1];
-            float pw[NTMAX / 32 + 1];
+            int pf[NT / 32 + 1];
+            float pw[NT / 32 + 1];
             if (MODE == MOE_GEMM_DOWN) {
 #pragma unroll
-                for (int i = 0; i <= NTMAX / 32; ++i) {
+                for (int i = 0; i <= NT / 32; ++i) {
                     const int col = lane + 32 * i;
                     pf[i] = -1;
                     pw[i] = 0.f;
@@ -476,7 +490,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                     int fl = pf[0];
                     float wv = pw[0];
 #pragma unroll
-                    for (int i = 1; i <= NTMAX / 32; ++i)
+                    for (int i = 1; i <= NT / 32; ++i)
                         if (ci == i) {
                             fl = pf[i];
                             wv = pw[i];
@@ -556,8 +570,12 @@ __global__ void __launch_bounds__(256) moe_prepare_atoms_kernel(int64_t words, i
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-size_t moe_gemm_smem_bytes(int mode) {
-    return mode == MOE_GEMM_GATEUP ? Cfg<MOE_GEMM_GATEUP>::SMEM : Cfg<MOE_GEMM_DOWN>::SMEM;
+size_t moe_gemm_smem_bytes(int mode, int narrow) {
+    if (narrow)
+        return mode == MOE_GEMM_GATEUP ? Cfg<MOE_GEMM_GATEUP, MOE_GEMM_NT_NARROW>::SMEM
+                                       : Cfg<MOE_GEMM_DOWN, MOE_GEMM_NT_NARROW>::SMEM;
+    return mode == MOE_GEMM_GATEUP ? Cfg<MOE_GEMM_GATEUP, NTMAX>::SMEM
+                                   : Cfg<MOE_GEMM_DOWN, NTMAX>::SMEM;
 }
 
 size_t moe_prepared_atoms_bytes(int E, int M, int K, int mrows) {
@@ -574,11 +592,11 @@ cudaError_t moe_launch_prepare_atoms(int E, int M, int K, int mrows, const uint8
 }
 
 namespace {
-template <int MODE>
+template <int MODE, int NT>
 cudaError_t launch_clustered(const CUtensorMap *mA, const CUtensorMap *mA2,
                              const MoeGemmArgs *args, int max_ctas, cudaStream_t st) {
-    auto kern = moe_grouped_gemm_kernel<MODE>;
-    const size_t sm = Cfg<MODE>::SMEM;
+    auto kern = moe_grouped_gemm_kernel<MODE, NT>;
+    const size_t sm = Cfg<MODE, NT>::SMEM;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
@@ -592,15 +610,15 @@ cudaError_t launch_clustered(const CUtensorMap *mA, const CUtensorMap *mA2,
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    static int clusters[2] = {0, 0};  // co-resident clusters, per mode
-    if (!clusters[MODE]) {
+    static int clusters = 0;  // co-resident clusters of this instantiation
+    if (!clusters) {
         cfg.gridDim = dim3(max_ctas / CL * CL);
         int n = 0;
         err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
         if (err != cudaSuccess) return err;
-        clusters[MODE] = n > 0 ? n : 1;
+        clusters = n > 0 ? n : 1;
     }
-    int grid = clusters[MODE] * CL;
+    int grid = clusters * CL;
     if (grid > max_ctas / CL * CL) grid = max_ctas / CL * CL;
     cfg.gridDim = dim3(grid);
     return cudaLaunchKernelEx(&cfg, kern, *mA, *mA2, *args);
@@ -608,8 +626,13 @@ cudaError_t launch_clustered(const CUtensorMap *mA, const CUtensorMap *mA2,
 }  // namespace
 
 cudaError_t moe_launch_gemm(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
-                            const MoeGemmArgs *args, int grid, cudaStream_t st) {
+                            const MoeGemmArgs *args, int max_rows, int grid, cudaStream_t st) {
     if (args->MT % CL) return cudaErrorInvalidValue;
-    return mode == MOE_GEMM_GATEUP ? launch_clustered<MOE_GEMM_GATEUP>(mA, mA2, args, grid, st)
-                                   : launch_clustered<MOE_GEMM_DOWN>(mA, mA2, args, grid, st);
+    constexpr int NN = MOE_GEMM_NT_NARROW;
+    if (max_rows <= NN)
+        return mode == MOE_GEMM_GATEUP
+                   ? launch_clustered<MOE_GEMM_GATEUP, NN>(mA, mA2, args, grid, st)
+                   : launch_clustered<MOE_GEMM_DOWN, NN>(mA, mA2, args, grid, st);
+    return mode == MOE_GEMM_GATEUP ? launch_clustered<MOE_GEMM_GATEUP, NTMAX>(mA, mA2, args, grid, st)
+                                   : launch_clustered<MOE_GEMM_DOWN, NTMAX>(mA, mA2, args, grid, st);
 }

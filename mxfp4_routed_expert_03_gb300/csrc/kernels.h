@@ -59,6 +59,7 @@ cudaError_t moe_launch_gather_x(int max_tt, int E, int k, int n_rows, int D, int
 #define MOE_GEMM_GATEUP 0
 #define MOE_GEMM_DOWN 1
 #define MOE_GEMM_NTMAX 112
+#define MOE_GEMM_NT_NARROW 16  // token rows per tile of the narrow variant
 #define MOE_GEMM_CLUSTER 2  // CTAs per cluster sharing the activation operand
 #define MOE_GEMM_BTILE (2 * MOE_GEMM_NTMAX * 128)  // bytes of one activation B tile block
 
@@ -80,12 +81,14 @@ struct MoeGemmArgs {
     long long timeout_cycles;
 };
 
-size_t moe_gemm_smem_bytes(int mode);
+size_t moe_gemm_smem_bytes(int mode, int narrow);
 size_t moe_prepared_atoms_bytes(int E, int M, int K, int mrows);
 cudaError_t moe_launch_prepare_atoms(int E, int M, int K, int mrows, const uint8_t *s,
                                      const uint8_t *s2, uint8_t *out, cudaStream_t st);
+// max_rows: bound on any expert's routed rows (T for distinct top-k experts);
+// at most MOE_GEMM_NT_NARROW selects the narrow-tile variant.
 cudaError_t moe_launch_gemm(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
-                            const MoeGemmArgs *args, int grid, cudaStream_t st);
+                            const MoeGemmArgs *args, int max_rows, int grid, cudaStream_t st);
 
 // dense_gemm.cu: bf16 tcgen05 GEMMs of the router and the shared expert
 #define MOE_DENSE_ROUTER 0  // 3 bf16 terms of W_r, fp32 store out_f32[t][m] (m < M)

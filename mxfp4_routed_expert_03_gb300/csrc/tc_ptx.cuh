@@ -299,6 +299,19 @@ __device__ __forceinline__ uint64_t sdesc_plain_32x16(uint32_t saddr) {
     return d;
 }
 
+// Descriptor of 32 rows x 16 bytes for tcgen05.cp.32x128b whose 8-row core
+// matrices lie 256 bytes apart (the first 16 bytes of each row of a 1 KB
+// 128x256b-layout block). Both offset fields carry the 256-byte stride; the
+// block has a single 16-byte core matrix along K.
+__device__ __forceinline__ uint64_t sdesc_plain_32x16_groups256(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(256u >> 4) << 16;
+    d |= (uint64_t)(256u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
 // Descriptor of a plain (unswizzled) 128-row x 32-byte block for
 // tcgen05.cp.128x256b: K-major core matrices of 8 rows x 16 bytes, the two
 // 16-byte halves of a row 128 bytes apart, 8-row groups 256 bytes apart.

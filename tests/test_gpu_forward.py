@@ -53,14 +53,15 @@ def test_tiny_shapes_ragged_and_multi_tile_segments(tiny_weights, T):
     print("tiny forward T=%d" % T, e)
 
 
-def test_tiny_one_expert_holds_all_rows(tiny_weights):
+@pytest.mark.parametrize("T", [16, 500])
+def test_tiny_one_expert_holds_all_rows(tiny_weights, T):
+    """T = 16 fills one narrow (16-row) token tile; T = 500 spans several wide ones."""
     w = synth.WORKLOADS["tiny"]
-    T = 500
     x, lg = synth.make_x(w, 5, T=T), synth.make_logits(w, 5, T=T)
     lg[:, 9] = 60.0
     got, plan = _run(w, tiny_weights, x, lg)
     assert plan.counts.cpu().numpy()[9] == T
-    tok = np.arange(0, T, 11)
+    tok = np.arange(0, T, 11) if T > 16 else np.arange(T)
     assert_close(got[tok], reference(w, x, lg, tokens=tok)["out"])
 
 
