@@ -63,11 +63,7 @@ constexpr int A_BYTES = 128 * BK;        // smem bytes of the 128-row weight til
 constexpr int A_TX = 128 * BK / 2;       // bytes the TMA moves for it (packed)
 constexpr int SF_BYTES = 1024;           // weight scales of one stage: 128 rows x 2 x 4 blocks
 constexpr int BSF_BYTES = 1024;          // activation scales of one chunk (256 B rows, 4 blocks)
-constexpr int NUM_THREADS = 224;
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COLS = 2 * NTMAX;  // [hi | lo] accumulator columns per buffer
-constexpr uint32_t SF_TMEM_COL = 464;     // scales: 2 slots x (KS x 4 A + KS x 8 B) columns
-constexpr uint32_t SF_SLOT = KS * 12;     // columns per slot: A blocks at 0, 4; B blocks at 8, 16
+constexpr uint32_t SF_SLOT = KS * 12;     // scale columns per stage: A blocks at 0, 4; B at 8, 16
 constexpr int CL = MOE_GEMM_CLUSTER;      // CTAs per cluster sharing activation chunks
 constexpr uint16_t CL_MASK = (1u << CL) - 1;
 
@@ -78,6 +74,18 @@ constexpr uint16_t CL_MASK = (1u << CL) - 1;
 // the weight bytes it keeps in flight.
 template <int MODE, int NT>
 struct Cfg {
+    // MMA-issuing warps. One thread issues a block-scaled MMA every ~90 cycles
+    // when the scale selection changes from MMA to MMA (every K step), which
+    // is slower than the tensor pipe for narrow tiles; the narrow variant
+    // therefore has two issuers, each taking every other K stage of a tile
+    // into its own accumulator, and the epilogue adds the two.
+    static constexpr int NSPLIT = NT <= 16 ? 2 : 1;
+    static constexpr int THREADS = 224 + 32 * (NSPLIT - 1);  // warp 7: second issuer
+    static constexpr uint32_t ACC_COLS = 2 * NT;             // [hi | lo] columns of one accumulator
+    static constexpr uint32_t BUF_COLS = NSPLIT * ACC_COLS;  // one of two accumulator buffers
+    static constexpr uint32_t SF_TMEM_COL = 2 * BUF_COLS;    // then 2 scale slots per issuer
+    static constexpr uint32_t TMEM_COLS = NT <= 16 ? 256 : 512;
+    static_assert(SF_TMEM_COL + 2 * NSPLIT * SF_SLOT <= TMEM_COLS, "tensor memory budget");
     static constexpr int MROWS = (MODE == MOE_GEMM_GATEUP) ? 64 : 128;  // weight rows per tile
     static constexpr int SA = NT <= 16 ? 4 : 2;  // weight ring stages (KS blocks each)
     static constexpr int SB = SA;                // activation ring stages
@@ -173,7 +181,7 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" :::
 }  // namespace
 
 template <int MODE, int NT>
-__global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
+__global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
     const MoeGemmArgs args) {
     using C = Cfg<MODE, NT>;
@@ -195,8 +203,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
     const int E = args.E;
     int n_active = args.active[0];
     if (n_active < 0 || n_active > E) n_active = 0;
-    for (int i = tid; i <= n_active; i += NUM_THREADS) s_prefix[i] = args.tt_prefix[i];
-    for (int a = tid; a < n_active; a += NUM_THREADS) {
+    for (int i = tid; i <= n_active; i += C::THREADS) s_prefix[i] = args.tt_prefix[i];
+    for (int a = tid; a < n_active; a += C::THREADS) {
         const int e = args.active[1 + a];
         int sb = 0, cnt = 0;
         if (e >= 0 && e < E) {
@@ -216,13 +224,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
             tc::mbar_init(&emptyB[s], CL);  // released by every CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(&tfull[b], 1);
+            tc::mbar_init(&tfull[b], C::NSPLIT);  // every issuer commits its half
             tc::mbar_init(&tempty[b], 4);
         }
         tc::fence_mbar_init();
     }
     if (warp == 1) {
-        tc::tmem_alloc(tmem_slot, TMEM_COLS);
+        tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
         tc::tmem_relinquish();
     }
     tc::tc_fence_before();
@@ -318,12 +326,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                 }
             }
         }
-    } else if (warp == 2) {
-        // ------------------------------------------ MMA issuer (one thread)
+    } else if (warp == 2 || warp == 7) {
+        // ------------------------------------------ MMA issuer(s) (one thread each)
         // The whole loop runs on one thread: reconverging the warp around every
         // chunk's issue costs about as much as the chunk's MMAs themselves.
+        // With two issuers, issuer `split` takes the tile's stages j with
+        // j % 2 == split into accumulator `split` of the buffer.
         if (lane == 0) {
-            int it = 0, lt = 0;
+            const int split = warp == 2 ? 0 : 1;
+            int it = 0, lt = 0, mine = 0;
             bool ok = true;
             uint64_t *lastA = nullptr, *lastB = nullptr;
             uint32_t parA = 0, parB = 0;
@@ -339,12 +350,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                     break;
                 }
                 tc::tc_fence_after();
-                const uint32_t acc = tmem + buf * ACC_COLS;
+                const uint32_t acc = tmem + buf * C::BUF_COLS + split * C::ACC_COLS;
                 uint32_t idesc[4];  // scale byte k of each column for K step k
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     idesc[k] = tc::idesc_mxf8f6f4(tc::FMT_E2M1, tc::FMT_E4M3, 128, 2 * t.nmma, k, k);
-                for (int kc = 0; kc < KC; kc += KS, ++it) {
+                bool first = true;
+                for (int kc = 0, j = 0; kc < KC; kc += KS, ++it, ++j) {
+                    if (C::NSPLIT > 1 && (j & 1) != split) continue;  // the other issuer's stage
                     const int sa = it % C::SA, ra = it / C::SA;
                     const int sb = it % C::SB, rb = it / C::SB;
                     const int nsub = min(KS, KC - kc);
@@ -355,7 +368,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                     }
                     const uint32_t a_s = tc::smem_u32(smem + sa * C::A_STAGE);
                     const uint32_t b_s = tc::smem_u32(smem + C::B_BASE + sb * C::B_STAGE);
-                    const uint32_t slot = tmem + SF_TMEM_COL + (uint32_t)(it & 1) * SF_SLOT;
+                    const uint32_t slot =
+                        tmem + C::SF_TMEM_COL + (uint32_t)(2 * split + (mine & 1)) * SF_SLOT;
+                    ++mine;
                     // both blocks' weight scales in one copy: columns slot .. slot + 7
                     tc::tmem_cp_128x256b(slot, tc::sdesc_plain_128x32(a_s + C::A_SF));
                     for (int sub = 0; sub < nsub; ++sub) {
@@ -370,8 +385,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                         for (int k = 0; k < 4; ++k)
                             tc::mma_mxf8f6f4(acc, tc::sdesc_sw128(as + 32 * k),
                                              tc::sdesc_sw128(bs + 32 * k), idesc[k], sfa, sfb,
-                                             (kc > 0 || sub > 0 || k > 0) ? 1u : 0u);
+                                             (!first || sub > 0 || k > 0) ? 1u : 0u);
                     }
+                    first = false;
                     tc::mma_commit(&emptyA[sa]);
                     tc::mma_commit_multicast(&emptyB[sb], CL_MASK);  // every CTA's copy is free
                     lastA = &emptyA[sa];
@@ -390,6 +406,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
         __syncwarp();
     } else {
         // ------------------------------------------ epilogue (warps 3..6)
+        // (warp 7, when present, is the second MMA issuer above)
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         int lt = 0, cur = 0;
@@ -425,7 +442,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                 break;
             }
             tc::tc_fence_after();
-            const uint32_t acc = tmem + lane_base + buf * ACC_COLS;
+            const uint32_t acc = tmem + lane_base + buf * C::BUF_COLS;
+            // the second issuer's accumulator holds something only if the tile has >= 2 stages
+            const bool two = C::NSPLIT > 1 && KC > KS;
             for (int c0 = 0; c0 < t.n; c0 += 16) {
                 uint32_t rh[16], rl[16];
                 tc::tmem_ld_32x32b_x16(acc + c0, rh);
@@ -434,6 +453,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
                 float v[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+                if (two) {
+                    tc::tmem_ld_32x32b_x16(acc + C::ACC_COLS + c0, rh);
+                    tc::tmem_ld_32x32b_x16(acc + C::ACC_COLS + t.nmma + c0, rl);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        v[j] += __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+                }
                 if (MODE == MOE_GEMM_GATEUP) {
                     // Lanes 0..63 hold gate rows f0 + r, lanes 64..127 the same up rows.
                     // Gate warps finish columns 0..7 of the chunk, up warps 8..15; each
@@ -526,7 +553,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_grouped_gemm_kernel(
     __syncthreads();
     if (warp == 1) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, TMEM_COLS);
+        tc::tmem_dealloc(tmem, C::TMEM_COLS);
     }
     tc::cluster_sync();  // no CTA leaves while a peer may still multicast into it
 }
@@ -605,7 +632,7 @@ cudaError_t launch_clustered(const CUtensorMap *mA, const CUtensorMap *mA2,
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.blockDim = dim3(Cfg<MODE, NT>::THREADS);
     cfg.dynamicSmemBytes = sm;
     cfg.stream = st;
     cfg.attrs = attr;
