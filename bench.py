@@ -4,9 +4,10 @@
 Default workload: one K3-shaped routed layer (d_model 7168, d_ff 1536, 896
 experts, top-16, MXFP4 weights resident in HBM), decode batches of T = 1, 4
 and 16 tokens; one step = moe_plan + the expert FFN for each of the three
-batches (21 tokens). The FFN call follows the decode/prefill crossover at 8
-tokens: moe_decode (CUDA-core streaming) for T <= 8, moe_forward (tcgen05
-grouped GEMMs) above; `--path decode|forward` forces one of them. `--workload prefill4k|skewed8k` times moe_plan +
+batches (21 tokens). The FFN call of each batch takes the faster entry point
+as measured on GB300: moe_decode (CUDA-core streaming) for a single token,
+moe_forward (tcgen05 grouped GEMMs) from 2 tokens up; `--path
+decode|forward` forces one of them. `--workload prefill4k|skewed8k` times moe_plan +
 moe_forward on one prefill batch instead; `--workload router16k` times the
 long prefill whose logits come from the library's own fp32 router (x . W_r)
 and which adds one bf16 shared expert.
@@ -41,7 +42,7 @@ EXPERT_BYTES = 17547264            # one expert's three MXFP4 matrices (codes + 
 GATEUP_BYTES = 2 * (D_FF * D_MODEL // 2 + D_FF * D_MODEL // 32)
 DOWN_BYTES = D_MODEL * D_FF // 2 + D_MODEL * D_FF // 32
 N_SETS = 8
-CROSSOVER_T = 8   # largest batch the CUDA-core decode path takes under --path auto
+CROSSOVER_T = 1   # largest batch the CUDA-core decode path takes under --path auto
 
 BENCH_WORKLOADS = {
     "decode": {"Ts": [1, 4, 16], "path": "auto",
@@ -66,7 +67,7 @@ def parse_args():
     ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default="decode")
     ap.add_argument("--path", choices=["decode", "forward", "auto"], default=None,
                     help="entry point for the batches (default: auto for decode -- moe_decode "
-                         "up to 8 tokens, moe_forward above -- and forward for prefill)")
+                         "for one token, moe_forward above -- and forward for prefill)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall-time budget of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
