@@ -31,22 +31,25 @@
 // to both CTAs' release barriers, so a stage is refilled only once both have
 // consumed it.
 //
-// A pipeline stage carries KS = 2 consecutive 128-wide K blocks (all data
-// layouts stay per 128-wide block), so each wait, commit and loop step of the
-// single MMA-issuing thread is shared by 8 MMAs instead of 4.
+// Two tile widths (template NT): the wide variant (112 token rows) for
+// prefill, with 2-stage rings; the narrow variant (16 rows, chosen when no
+// expert has more rows) with 4-stage rings and two MMA issuers. A pipeline
+// stage carries two 128-wide K blocks; data layouts stay per K block.
 //
-// One persistent CTA per SM, 7 warps:
+// One persistent CTA per SM, 7 warps (8 for the narrow variant):
 //   warp 0      weight producer (one thread): weight tile(s) by TMA (packed
 //               E2M1 expanded to the 8-bit MMA layout) and the prepared 1 KB
-//               scale block of the stage's two K blocks, once per TMEM quadrant
+//               scale block holding the stage's K block(s)
 //   warp 1      activation producer (one thread): the token tile's prepared
-//               [hi; lo] B tile and its scales, each one contiguous bulk copy
-//               per chunk; TMEM allocator
+//               [hi; lo] B tile and its 1 KB scale block, each one contiguous
+//               bulk copy per K block; TMEM allocator
 //   warp 2      MMA issuer (one thread): tcgen05.cp scales, tcgen05.mma
 //   warps 3-6   epilogue, one 32-lane TMEM quadrant each
-// Weights and activations share one "full" barrier per stage (both producers
-// arrive on it; the cluster peer's multicast bytes complete on it too) and
-// have separate release barriers; the accumulator is double-buffered in TMEM so the epilogue of tile i overlaps
+//   warp 7      (narrow) second MMA issuer
+// Each operand ring has its own "full" barrier per stage (one barrier serves
+// both when the rings are equally deep; the cluster peer's multicast bytes
+// complete on the activation one) and its own release barrier; the
+// accumulator is double-buffered in TMEM so the epilogue of tile i overlaps
 // the MMAs of tile i+1. Every wait is bounded: on expiry the CTA records
 // MOE_ERR_DEVICE_TIMEOUT and winds down.
 #include "common.cuh"
@@ -57,13 +60,12 @@
 namespace {
 
 constexpr int BK = 128;                  // K elements per block (data-layout unit)
-constexpr int KS = 2;                    // blocks per pipeline stage
+constexpr int ATOM_BLOCKS = 2;           // K blocks per prepared weight-scale block
 constexpr int NTMAX = MOE_GEMM_NTMAX;    // token rows per tile (wide variant)
 constexpr int A_BYTES = 128 * BK;        // smem bytes of the 128-row weight tile (E2M1 -> 8 bit)
 constexpr int A_TX = 128 * BK / 2;       // bytes the TMA moves for it (packed)
-constexpr int SF_BYTES = 1024;           // weight scales of one stage: 128 rows x 2 x 4 blocks
+constexpr int SF_BYTES = 1024;           // one prepared weight-scale block: 128 rows x 2 K blocks
 constexpr int BSF_BYTES = 1024;          // activation scales of one chunk (256 B rows, 4 blocks)
-constexpr uint32_t SF_SLOT = KS * 12;     // scale columns per stage: A blocks at 0, 4; B at 8, 16
 constexpr int CL = MOE_GEMM_CLUSTER;      // CTAs per cluster sharing activation chunks
 constexpr uint16_t CL_MASK = (1u << CL) - 1;
 
@@ -71,37 +73,46 @@ constexpr uint16_t CL_MASK = (1u << CL) - 1;
 // narrow one (NT = MOE_GEMM_NT_NARROW, when no expert has more than NT routed
 // rows) spends the activation ring's shared memory on a deeper weight ring,
 // since with few tokens per expert the GEMM streams weights and is bound by
-// the weight bytes it keeps in flight.
+// the weight bytes it keeps in flight. Scale blocks (1 KB per K block pair
+// of weights, per K block of activations) land in shared memory once
+// (narrow: read into tensor memory by 32x128b.warpx4 copies, which fill every
+// lane quadrant) or once per lane quadrant (wide: one 128x256b copy reads
+// all four, fewer instructions for the single issuer).
 template <int MODE, int NT>
 struct Cfg {
+    static constexpr bool NARROW = NT <= 16;
     // MMA-issuing warps. One thread issues a block-scaled MMA every ~90 cycles
     // when the scale selection changes from MMA to MMA (every K step), which
     // is slower than the tensor pipe for narrow tiles; the narrow variant
     // therefore has two issuers, each taking every other K stage of a tile
     // into its own accumulator, and the epilogue adds the two.
-    static constexpr int NSPLIT = NT <= 16 ? 2 : 1;
+    static constexpr int NSPLIT = NARROW ? 2 : 1;
     static constexpr int THREADS = 224 + 32 * (NSPLIT - 1);  // warp 7: second issuer
     static constexpr uint32_t ACC_COLS = 2 * NT;             // [hi | lo] columns of one accumulator
     static constexpr uint32_t BUF_COLS = NSPLIT * ACC_COLS;  // one of two accumulator buffers
     static constexpr uint32_t SF_TMEM_COL = 2 * BUF_COLS;    // then 2 scale slots per issuer
-    static constexpr uint32_t TMEM_COLS = NT <= 16 ? 256 : 512;
+    static constexpr uint32_t TMEM_COLS = NARROW ? 256 : 512;
+    // K blocks per pipeline stage: each wait, commit and loop step of an
+    // issuer is shared by 8 MMAs. (Single-block stages with deeper rings
+    // measured slower for the wide variant: the issuer's per-stage waits cost
+    // more than the extra depth returned.)
+    static constexpr int KS = 2;
+    static constexpr uint32_t SF_SLOT = KS * 12;  // per stage: A 4 columns per block, then B 8
+    static constexpr int SCALE_REP = NARROW ? 1 : 4;  // copies of each scale block in smem
     static_assert(SF_TMEM_COL + 2 * NSPLIT * SF_SLOT <= TMEM_COLS, "tensor memory budget");
     static constexpr int MROWS = (MODE == MOE_GEMM_GATEUP) ? 64 : 128;  // weight rows per tile
-    static constexpr int SA = NT <= 16 ? 4 : 2;  // weight ring stages (KS blocks each)
-    static constexpr int SB = SA;                // activation ring stages
-    static constexpr int A_STAGE = KS * A_BYTES + 4 * SF_BYTES;  // scales once per TMEM quadrant
+    static constexpr int SA = NARROW ? 4 : 2;  // weight ring stages (KS blocks each)
+    static constexpr int SB = SA;              // activation ring stages
+    static constexpr bool MERGED = SA == SB;   // one full barrier per stage for both operands
+    static constexpr int A_STAGE = KS * A_BYTES + SCALE_REP * SF_BYTES;  // tiles, then scales
     static constexpr int A_SF = KS * A_BYTES;
     static constexpr int B_BYTES = 2 * NT * BK;  // smem bytes of [hi; lo] activation rows
-    // Activation scales per block: B rows < 128 need TMEM columns 0..3 only,
-    // which one 32x128b.warpx4 copy of the 1 KB block fills in every lane
-    // quadrant; wider tiles take four copies of the block and one 128x256b copy.
-    static constexpr int BSF_COPIES = 2 * NT <= 128 ? 1 : 4;
-    // B: KS blocks of [hi; lo] rows, then KS x BSF_COPIES scale blocks
-    static constexpr int B_STAGE = KS * (B_BYTES + BSF_COPIES * BSF_BYTES);
+    static constexpr int B_STAGE = KS * (B_BYTES + SCALE_REP * BSF_BYTES);  // tiles, then scales
     static constexpr int B_BASE = SA * A_STAGE;
     static constexpr int B_SF = KS * B_BYTES;
     static constexpr int BAR_BASE = B_BASE + SB * B_STAGE;
-    static constexpr int N_BARS = 3 * SA + 4;  // full, emptyA, emptyB per stage; tfull, tempty x2
+    static constexpr int N_FULL = MERGED ? SA : SA + SB;
+    static constexpr int N_BARS = N_FULL + SA + SB + 4;  // full(s), emptyA, emptyB; tfull, tempty x2
     static constexpr int PREFIX_BASE = BAR_BASE + N_BARS * 8 + 16;  // int [active + 1]
     static constexpr int EXPERT_BASE = (PREFIX_BASE + (MOE_MAX_EXPERTS + 1) * 4 + 15) / 16 * 16;
     static constexpr int SEG_BASE = (EXPERT_BASE + MOE_MAX_EXPERTS * 4 + 15) / 16 * 16;  // int2
@@ -109,12 +120,11 @@ struct Cfg {
     // GEMM1: u values of 16 columns x 64 rows; GEMM2: 4 warps x 16 columns x 32 rows
     static constexpr int EPI_BYTES = (MODE == MOE_GEMM_GATEUP) ? 16 * 64 * 4 : 4 * 16 * 32 * 4;
     static constexpr int SMEM = 1024 + EPI_BASE + EPI_BYTES;
-    static_assert(B_STAGE % 1024 == 0, "activation stage must keep 1 KB alignment");
+    static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0, "stages must keep 1 KB alignment");
     static_assert(BAR_BASE % 8 == 0 && PREFIX_BASE % 16 == 0 && EXPERT_BASE % 16 == 0 &&
                       SEG_BASE % 16 == 0 && EPI_BASE % 16 == 0,
                   "shared-memory regions must be 16-byte aligned (int2 / float4 accesses)");
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert(SA == SB, "one full barrier per stage serves both operands");
 };
 
 struct Tile {
@@ -188,8 +198,9 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t *full = (uint64_t *)(smem + C::BAR_BASE);
-    uint64_t *emptyA = full + C::SA;
+    uint64_t *fullA = (uint64_t *)(smem + C::BAR_BASE);
+    uint64_t *fullB = C::MERGED ? fullA : fullA + C::SA;
+    uint64_t *emptyA = fullA + C::N_FULL;
     uint64_t *emptyB = emptyA + C::SA;
     uint64_t *tfull = emptyB + C::SB;
     uint64_t *tempty = tfull + 2;
@@ -219,8 +230,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
     if (tid == 0) {
         *abort_flag = 0;
         for (int s = 0; s < C::SA; ++s) {
-            tc::mbar_init(&full[s], 2);      // the weight and the activation producer
+            tc::mbar_init(&fullA[s], C::MERGED ? 2 : 1);  // merged: both producers arrive
             tc::mbar_init(&emptyA[s], 1);
+        }
+        for (int s = 0; s < C::SB; ++s) {
+            if (!C::MERGED) tc::mbar_init(&fullB[s], 1);
             tc::mbar_init(&emptyB[s], CL);  // released by every CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
@@ -263,27 +277,29 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                     continue;
                 }
                 const int row0 = t.e * args.M + t.mt * C::MROWS;
-                const size_t atom0 = ((size_t)t.e * MT + t.mt) * ((KC + KS - 1) / KS);
-                for (int kc = 0; kc < KC; kc += KS, ++it) {
+                const size_t atom0 = ((size_t)t.e * MT + t.mt) * ((KC + ATOM_BLOCKS - 1) / ATOM_BLOCKS);
+                for (int kc = 0; kc < KC; kc += C::KS, ++it) {
                     const int s = it % C::SA, round = it / C::SA;
-                    const int nsub = min(KS, KC - kc);
+                    const int nsub = min(C::KS, KC - kc);
                     if (round > 0 && !tc::mbar_wait(&emptyA[s], (round - 1) & 1, LIMIT, abort_p)) {
                         fail();
                         ok = false;
                         break;
                     }
                     unsigned char *st = smem + s * C::A_STAGE;
-                    tc::mbar_arrive_expect_tx(&full[s], (uint32_t)(nsub * A_TX + 4 * SF_BYTES));
+                    tc::mbar_arrive_expect_tx(&fullA[s],
+                                              (uint32_t)(nsub * A_TX + C::SCALE_REP * SF_BYTES));
                     for (int sub = 0; sub < nsub; ++sub) {
                         unsigned char *sa = st + sub * A_BYTES;
-                        tc::tma_load_2d(sa, &mapA, &full[s], (kc + sub) * BK, row0, pol_w);
+                        tc::tma_load_2d(sa, &mapA, &fullA[s], (kc + sub) * BK, row0, pol_w);
                         if (MODE == MOE_GEMM_GATEUP)  // up rows fill lanes 64..127
-                            tc::tma_load_2d(sa + 64 * BK, &mapA2, &full[s], (kc + sub) * BK, row0,
+                            tc::tma_load_2d(sa + 64 * BK, &mapA2, &fullA[s], (kc + sub) * BK, row0,
                                             pol_w);
                     }
-                    const uint8_t *sf = args.a_atoms + (atom0 + kc / KS) * SF_BYTES;
-                    for (int qd = 0; qd < 4; ++qd)  // one copy per TMEM lane quadrant
-                        tc::bulk_copy_g2s(st + C::A_SF + qd * SF_BYTES, sf, SF_BYTES, &full[s], pol_w);
+                    // the scale block holding this stage's K block(s)
+                    const uint8_t *sf = args.a_atoms + (atom0 + kc / ATOM_BLOCKS) * SF_BYTES;
+                    for (int qd = 0; qd < C::SCALE_REP; ++qd)
+                        tc::bulk_copy_g2s(st + C::A_SF + qd * SF_BYTES, sf, SF_BYTES, &fullA[s], pol_w);
                 }
             }
         }
@@ -299,9 +315,9 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                 if (!tile_at<NT>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) continue;
                 const uint32_t tile_bytes = (uint32_t)(2 * t.nmma * BK);
                 const size_t blk0 = (size_t)t.tt * KC;
-                for (int kc = 0; kc < KC; kc += KS, ++it) {
+                for (int kc = 0; kc < KC; kc += C::KS, ++it) {
                     const int s = it % C::SB, round = it / C::SB;
-                    const int nsub = min(KS, KC - kc);
+                    const int nsub = min(C::KS, KC - kc);
                     if (round > 0 && !tc::mbar_wait(&emptyB[s], (round - 1) & 1, LIMIT, abort_p)) {
                         fail();
                         ok = false;
@@ -310,18 +326,20 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                     unsigned char *st = smem + C::B_BASE + s * C::B_STAGE;
                     // the whole stage lands here; this CTA fetches its 1/CL share for all
                     tc::mbar_arrive_expect_tx(
-                        &full[s], (uint32_t)nsub * (tile_bytes + C::BSF_COPIES * BSF_BYTES));
+                        &fullB[s], (uint32_t)nsub * (tile_bytes + C::SCALE_REP * BSF_BYTES));
                     const uint32_t part = tile_bytes / CL;
                     for (int sub = 0; sub < nsub; ++sub) {
                         const size_t blk = blk0 + kc + sub;
                         tc::bulk_copy_g2s_multicast(
                             st + sub * C::B_BYTES + rank * part,
-                            args.b_tiles + blk * MOE_GEMM_BTILE + rank * part, part, &full[s],
+                            args.b_tiles + blk * MOE_GEMM_BTILE + rank * part, part, &fullB[s],
                             CL_MASK, pol_x);
-                        for (int qd = rank; qd < C::BSF_COPIES; qd += CL)
-                            tc::bulk_copy_g2s_multicast(
-                                st + C::B_SF + (sub * C::BSF_COPIES + qd) * BSF_BYTES,
-                                args.b_atoms + blk * BSF_BYTES, BSF_BYTES, &full[s], CL_MASK, pol_x);
+                        for (int qd = 0; qd < C::SCALE_REP; ++qd)  // each copy fetched by one CTA
+                            if ((sub * C::SCALE_REP + qd) % CL == rank)
+                                tc::bulk_copy_g2s_multicast(
+                                    st + C::B_SF + (sub * C::SCALE_REP + qd) * BSF_BYTES,
+                                    args.b_atoms + blk * BSF_BYTES, BSF_BYTES, &fullB[s], CL_MASK,
+                                    pol_x);
                     }
                 }
             }
@@ -356,12 +374,13 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                 for (int k = 0; k < 4; ++k)
                     idesc[k] = tc::idesc_mxf8f6f4(tc::FMT_E2M1, tc::FMT_E4M3, 128, 2 * t.nmma, k, k);
                 bool first = true;
-                for (int kc = 0, j = 0; kc < KC; kc += KS, ++it, ++j) {
+                for (int kc = 0, j = 0; kc < KC; kc += C::KS, ++it, ++j) {
                     if (C::NSPLIT > 1 && (j & 1) != split) continue;  // the other issuer's stage
                     const int sa = it % C::SA, ra = it / C::SA;
                     const int sb = it % C::SB, rb = it / C::SB;
-                    const int nsub = min(KS, KC - kc);
-                    if (!tc::mbar_wait(&full[sa], ra & 1, LIMIT, abort_p)) {
+                    const int nsub = min(C::KS, KC - kc);
+                    if (!tc::mbar_wait(&fullA[sa], ra & 1, LIMIT, abort_p) ||
+                        (!C::MERGED && !tc::mbar_wait(&fullB[sb], rb & 1, LIMIT, abort_p))) {
                         fail();
                         ok = false;
                         break;
@@ -369,17 +388,25 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                     const uint32_t a_s = tc::smem_u32(smem + sa * C::A_STAGE);
                     const uint32_t b_s = tc::smem_u32(smem + C::B_BASE + sb * C::B_STAGE);
                     const uint32_t slot =
-                        tmem + C::SF_TMEM_COL + (uint32_t)(2 * split + (mine & 1)) * SF_SLOT;
+                        tmem + C::SF_TMEM_COL + (uint32_t)(2 * split + (mine & 1)) * C::SF_SLOT;
                     ++mine;
-                    // both blocks' weight scales in one copy: columns slot .. slot + 7
-                    tc::tmem_cp_128x256b(slot, tc::sdesc_plain_128x32(a_s + C::A_SF));
+                    if (C::SCALE_REP == 4)  // both blocks' weight scales: columns slot .. slot + 7
+                        tc::tmem_cp_128x256b(slot, tc::sdesc_plain_128x32(a_s + C::A_SF));
                     for (int sub = 0; sub < nsub; ++sub) {
-                        const uint32_t sfa = slot + 4 * sub, sfb = slot + 8 + 8 * sub;
-                        const uint32_t bsf = b_s + C::B_SF + sub * C::BSF_COPIES * BSF_BYTES;
-                        if (C::BSF_COPIES == 1)  // columns 0..3 (B rows < 128), all quadrants
-                            tc::tmem_cp_32x128b_warpx4(sfb, tc::sdesc_plain_32x16_groups256(bsf));
-                        else
+                        const uint32_t sfa = slot + 4 * sub, sfb = slot + 4 * C::KS + 8 * sub;
+                        const uint32_t bsf = b_s + C::B_SF + sub * C::SCALE_REP * BSF_BYTES;
+                        if (C::SCALE_REP == 4) {
                             tc::tmem_cp_128x256b(sfb, tc::sdesc_plain_128x32(bsf));
+                        } else {
+                            // weight scales of K block kc + sub: its half of the block
+                            tc::tmem_cp_32x128b_warpx4(
+                                sfa, tc::sdesc_plain_32x16_groups256(a_s + C::A_SF + 128 * ((kc + sub) & 1)));
+                            // activation scales: B rows 0..127 (columns 0..3)
+                            tc::tmem_cp_32x128b_warpx4(sfb, tc::sdesc_plain_32x16_groups256(bsf));
+                            if (2 * t.nmma > 128)  // rows 128.. (columns 4..7)
+                                tc::tmem_cp_32x128b_warpx4(sfb + 4,
+                                                           tc::sdesc_plain_32x16_groups256(bsf + 128));
+                        }
                         const uint32_t as = a_s + sub * A_BYTES, bs = b_s + sub * C::B_BYTES;
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
@@ -444,7 +471,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
             tc::tc_fence_after();
             const uint32_t acc = tmem + lane_base + buf * C::BUF_COLS;
             // the second issuer's accumulator holds something only if the tile has >= 2 stages
-            const bool two = C::NSPLIT > 1 && KC > KS;
+            const bool two = C::NSPLIT > 1 && KC > C::KS;
             for (int c0 = 0; c0 < t.n; c0 += 16) {
                 uint32_t rh[16], rl[16];
                 tc::tmem_ld_32x32b_x16(acc + c0, rh);
@@ -573,7 +600,7 @@ __global__ void __launch_bounds__(256) moe_prepare_atoms_kernel(int64_t words, i
                                                                 uint32_t *__restrict__ out) {
     int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (w >= words) return;
-    const int MT = M / mrows, KC = K / BK, NP = (KC + KS - 1) / KS, ksb = K / 32;
+    const int MT = M / mrows, KC = K / BK, NP = (KC + ATOM_BLOCKS - 1) / ATOM_BLOCKS, ksb = K / 32;
     const int64_t blk = w / 256;
     const int wi = (int)(w % 256);
     const int l = (wi / 64) * 8 + (wi % 32) / 4;   // lane
@@ -583,7 +610,7 @@ __global__ void __launch_bounds__(256) moe_prepare_atoms_kernel(int64_t words, i
     const int64_t em = blk / NP;  // e * MT + mt
     const int mt = (int)(em % MT);
     const int64_t e = em / MT;
-    const int kc = KS * pair + j / 4;
+    const int kc = ATOM_BLOCKS * pair + j / 4;
     if (kc >= KC) {
         out[w] = 0u;
         return;
@@ -606,7 +633,7 @@ size_t moe_gemm_smem_bytes(int mode, int narrow) {
 }
 
 size_t moe_prepared_atoms_bytes(int E, int M, int K, int mrows) {
-    const int KC = K / BK, NP = (KC + KS - 1) / KS;
+    const int KC = K / BK, NP = (KC + ATOM_BLOCKS - 1) / ATOM_BLOCKS;
     return (size_t)E * (M / mrows) * NP * SF_BYTES;
 }
 
