@@ -74,6 +74,9 @@ def parse_args():
     ap.add_argument("--experts", type=int, default=N_EXPERTS,
                     help="experts in the layer (default 896); fewer only for profiling small "
                          "cases, and the line is then marked as such")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="one batch of this many tokens instead of the workload's batches; only "
+                         "for profiling small cases (the line is then marked as such)")
     return ap.parse_args()
 
 
@@ -236,7 +239,9 @@ def run_ours(args):
     else:
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
-    wl = BENCH_WORKLOADS[args.workload]
+    wl = dict(BENCH_WORKLOADS[args.workload])
+    if args.tokens:
+        wl["Ts"] = [args.tokens]
     path = args.path or wl["path"]
     base = synth.WORKLOADS["decode1"] if args.workload == "decode" else synth.WORKLOADS[args.workload]
 
@@ -466,8 +471,8 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (>=280 MB of expert weights per batch, "
                          "8 rotating logit sets)", "parallelism": f"replicas x{world}"},
         "roofline": roof,
-        **({"profiling_case": f"{n_exp} experts instead of {N_EXPERTS}; not a bench value"}
-           if n_exp != N_EXPERTS else {}),
+        **({"profiling_case": f"{n_exp} experts, batches {wl['Ts']}; not a bench value"}
+           if n_exp != N_EXPERTS or args.tokens else {}),
         "e2e": {"value": e2e_value, "unit": "tokens/s",
                 "h2d_bytes_per_step": sum(T * D_MODEL * 2 + (0 if use_router else T * n_exp * 4)
                                           for T in wl["Ts"]),

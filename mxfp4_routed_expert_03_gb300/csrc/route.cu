@@ -128,11 +128,18 @@ __device__ __forceinline__ void warp_stable_scatter(const int32_t *idx, int64_t 
 __global__ void __launch_bounds__(1024) moe_plan_small_kernel(
     int T, int E, int k, const float *__restrict__ logits, int32_t *topk_idx, float *topk_w,
     int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *active, int *status) {
+    // T <= 64 tokens, k <= 32: the selections stay in shared memory, and each
+    // expert keeps a bit mask of the tokens that chose it. A token chooses an
+    // expert at most once, so the stable position of flat entry t*k+j (expert
+    // e) is offsets[e] + the number of tokens before t that chose e.
     __shared__ int s_cnt[MOE_MAX_EXPERTS];
+    __shared__ unsigned long long s_mask[MOE_MAX_EXPERTS];
+    __shared__ int s_idx[64 * MOE_MAX_TOPK];
     __shared__ int s_tot[33];
     __shared__ int s_nan;
     int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     s_cnt[tid] = 0;
+    s_mask[tid] = 0ull;
     if (tid == 0) s_nan = 0;
     __syncthreads();
     for (int t = wid; t < T; t += 32) {
@@ -144,7 +151,9 @@ __global__ void __launch_bounds__(1024) moe_plan_small_kernel(
         if (lane < k) {
             topk_idx[(int64_t)t * k + lane] = my_e;
             topk_w[(int64_t)t * k + lane] = w;
+            s_idx[t * k + lane] = my_e;
             atomicAdd(&s_cnt[my_e], 1);
+            atomicOr(&s_mask[my_e], 1ull << t);
         }
         if (__any_sync(FULL_MASK, nan_seen) && lane == 0) s_nan = 1;
     }
@@ -166,7 +175,12 @@ __global__ void __launch_bounds__(1024) moe_plan_small_kernel(
     __syncthreads();
     if (tid < E) s_cnt[tid] = off;
     __syncthreads();
-    if (wid == 0) warp_stable_scatter(topk_idx, 0, (int64_t)T * k, E, s_cnt, perm, inv, status);
+    for (int f = tid; f < T * k; f += blockDim.x) {
+        const int t = f / k, e = s_idx[f];
+        const int pos = s_cnt[e] + __popcll(s_mask[e] & ((1ull << t) - 1ull));
+        perm[pos] = f;
+        inv[f] = pos;
+    }
 }
 
 // ---------------------------------------------------------------------------
