@@ -15,46 +15,105 @@
 
 namespace {
 
-// Warp-cooperative top-k of one token's logits. On return lane j < k holds
-// the j-th selection (expert index, logit). NaN logits count as -inf and set
-// *nan_seen. Lane l owns experts l, l+32, ... (coalesced loads).
+// Order-preserving 32-bit key of a logit: a larger key is a larger value;
+// -0 and +0 share a key (they compare equal). NaN is mapped to -inf first.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+    const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_logit(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+}
+
+// Warp-cooperative top-k of one token's logits (k <= 32, k <= E <= 1024).
+// On return lane j < k holds the j-th selection (expert index, logit):
+// descending logit, ties to the lower expert index. NaN logits count as -inf
+// and set nan_seen. Lane l owns experts l, l + 32, ... (coalesced loads).
+// `scratch` is k entries of warp-private shared memory.
+//
+// Selection by threshold rather than k rounds of arg-max: a 32-step bitwise
+// search finds the k-th largest key t (the largest x with at least k keys
+// >= x); every key > t is selected, and of the keys equal to t the lowest
+// expert indices fill the remaining places. The k winners are then ranked by
+// (key, index) within the warp.
 __device__ __forceinline__ void warp_topk(const float *row, int E, int k, int lane, int &my_e,
-                                          float &my_v, bool &nan_seen) {
-    float v[32];
-    uint32_t taken = 0;
+                                          float &my_v, bool &nan_seen, uint2 *scratch) {
+    uint32_t key[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        int e = lane + 32 * i;
-        float t = -INFINITY;
+        const int e = lane + 32 * i;
+        uint32_t kk = 0u;  // below every real key: never selected (E >= k)
         if (e < E) {
-            t = row[e];
-            if (t != t) { nan_seen = true; t = -INFINITY; }
-        } else {
-            taken |= 1u << i;
+            float t = row[e];
+            if (t != t) {
+                nan_seen = true;
+                t = -INFINITY;
+            }
+            kk = logit_key(t);
         }
-        v[i] = t;
+        key[i] = kk;
     }
+    uint32_t thr = 0u;
+    for (int b = 31; b >= 0; --b) {
+        const uint32_t cand = thr | (1u << b);
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) c += key[i] >= cand ? 1 : 0;
+        if ((int)__reduce_add_sync(FULL_MASK, (unsigned)c) >= k) thr = cand;
+    }
+    uint32_t sel = 0u;
+    int gt = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (key[i] > thr) {
+            sel |= 1u << i;
+            ++gt;
+        }
+    int need = k - (int)__reduce_add_sync(FULL_MASK, (unsigned)gt);  // ties at thr to take
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        if (need > 0) {  // warp-uniform
+            // chunk i holds experts 32 i + lane: lower lane = lower index
+            const uint32_t m = __ballot_sync(FULL_MASK, key[i] == thr);
+            const int take = min(need, __popc(m));
+            if (((m >> lane) & 1u) && __popc(m & lanemask_lt()) < take) sel |= 1u << i;
+            need -= take;
+        }
+    }
+    // compact the k selections into scratch, then rank them
+    const int mine = __popc(sel);
+    int pos = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(FULL_MASK, pos, off);
+        if (lane >= off) pos += o;
+    }
+    pos -= mine;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if ((sel >> i) & 1u) scratch[pos++] = make_uint2(key[i], (uint32_t)(lane + 32 * i));
+    __syncwarp();
+    uint2 me = make_uint2(0u, 0u);
+    int r = 0;
+    if (lane < k) {
+        me = scratch[lane];
+        for (int q = 0; q < k; ++q) {
+            const uint2 o = scratch[q];
+            r += (o.x > me.x || (o.x == me.x && o.y < me.y)) ? 1 : 0;
+        }
+    }
+    __syncwarp();
+    if (lane < k) scratch[r] = me;
+    __syncwarp();
     my_e = -1;
     my_v = -INFINITY;
-    for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int be = -1;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            // Within a lane the expert index grows with i, so a strict '>'
-            // keeps the lowest index among equal logits (+0 == -0 here).
-            if (!((taken >> i) & 1u) && (be < 0 || v[i] > bv)) { bv = v[i]; be = lane + 32 * i; }
-        }
-#pragma unroll
-        for (int off = 16; off; off >>= 1) {
-            float ov = __shfl_xor_sync(FULL_MASK, bv, off);
-            int oe = __shfl_xor_sync(FULL_MASK, be, off);
-            bool better = oe >= 0 && (be < 0 || ov > bv || (ov == bv && oe < be));
-            if (better) { bv = ov; be = oe; }
-        }
-        if (be >= 0 && (be & 31) == lane) taken |= 1u << (be >> 5);
-        if (lane == j) { my_e = be; my_v = bv; }
+    if (lane < k) {
+        const uint2 w = scratch[lane];
+        my_e = (int)w.y;
+        my_v = key_logit(w.x);
     }
+    __syncwarp();
 }
 
 // Softmax over the k selected logits held by lanes 0..k-1.
@@ -135,6 +194,7 @@ __global__ void __launch_bounds__(1024) moe_plan_small_kernel(
     __shared__ int s_cnt[MOE_MAX_EXPERTS];
     __shared__ unsigned long long s_mask[MOE_MAX_EXPERTS];
     __shared__ int s_idx[64 * MOE_MAX_TOPK];
+    __shared__ uint2 s_scratch[32][MOE_MAX_TOPK];
     __shared__ int s_tot[33];
     __shared__ int s_nan;
     int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -146,7 +206,7 @@ __global__ void __launch_bounds__(1024) moe_plan_small_kernel(
         int my_e;
         float my_v;
         bool nan_seen = false;
-        warp_topk(logits + (int64_t)t * E, E, k, lane, my_e, my_v, nan_seen);
+        warp_topk(logits + (int64_t)t * E, E, k, lane, my_e, my_v, nan_seen, s_scratch[wid]);
         float w = warp_select_weight(my_v, k, lane);
         if (lane < k) {
             topk_idx[(int64_t)t * k + lane] = my_e;
@@ -190,13 +250,14 @@ __global__ void __launch_bounds__(256) moe_topk_kernel(int T, int E, int k,
                                                        const float *__restrict__ logits,
                                                        int32_t *topk_idx, float *topk_w,
                                                        int *status) {
+    __shared__ uint2 s_scratch[8][MOE_MAX_TOPK];
     int lane = threadIdx.x & 31;
     int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
     int my_e;
     float my_v;
     bool nan_seen = false;
-    warp_topk(logits + (int64_t)t * E, E, k, lane, my_e, my_v, nan_seen);
+    warp_topk(logits + (int64_t)t * E, E, k, lane, my_e, my_v, nan_seen, s_scratch[threadIdx.x >> 5]);
     float w = warp_select_weight(my_v, k, lane);
     if (lane < k) {
         topk_idx[(int64_t)t * k + lane] = my_e;
