@@ -23,7 +23,7 @@
 //     A tile (two 64-row TMA boxes), so one MMA per 32-wide K step covers
 //     gate and up; the epilogue pairs TMEM lanes r and 64 + r.
 //
-// CTAs run in clusters of CL = 2 on neighbouring SMs. The two CTAs of a
+// Wide-variant CTAs run in clusters of CL = 2 on neighbouring SMs. The two CTAs of a
 // cluster take adjacent weight tiles of the same expert and token tile, so
 // they consume identical activation chunks: each CTA fetches half of every
 // chunk and multicasts it into both CTAs' shared memory, halving the L2
@@ -66,8 +66,6 @@ constexpr int A_BYTES = 128 * BK;        // smem bytes of the 128-row weight til
 constexpr int A_TX = 128 * BK / 2;       // bytes the TMA moves for it (packed)
 constexpr int SF_BYTES = 1024;           // one prepared weight-scale block: 128 rows x 2 K blocks
 constexpr int BSF_BYTES = 1024;          // activation scales of one chunk (256 B rows, 4 blocks)
-constexpr int CL = MOE_GEMM_CLUSTER;      // CTAs per cluster sharing activation chunks
-constexpr uint16_t CL_MASK = (1u << CL) - 1;
 
 // NT: token rows per tile. The wide variant (NT = NTMAX) serves prefill; the
 // narrow one (NT = MOE_GEMM_NT_NARROW, when no expert has more than NT routed
@@ -98,21 +96,38 @@ struct Cfg {
     // more than the extra depth returned.)
     static constexpr int KS = 2;
     static constexpr uint32_t SF_SLOT = KS * 12;  // per stage: A 4 columns per block, then B 8
-    static constexpr int SCALE_REP = NARROW ? 1 : 4;  // copies of each scale block in smem
+    // Copies of each scale block in smem: four let one 128x256b copy fill all
+    // lane quadrants (weights: both K blocks of a stage at once), which costs
+    // the wide variant's single issuer fewer operations. The narrow variant
+    // is bound by shared-memory traffic (E2M1 tiles land expanded to 8 bits,
+    // and every 128 x 32 MMA reads 4 KB of weights and 1 KB of tokens), so
+    // it keeps one copy of each block and fills the lane quadrants with
+    // 32x128b.warpx4 copies.
+    static constexpr int SCALE_REP_A = NARROW ? 1 : 4;
+    static constexpr int SCALE_REP_B = NARROW ? 1 : 4;
     static_assert(SF_TMEM_COL + 2 * NSPLIT * SF_SLOT <= TMEM_COLS, "tensor memory budget");
     static constexpr int MROWS = (MODE == MOE_GEMM_GATEUP) ? 64 : 128;  // weight rows per tile
+    // CTAs per cluster sharing (multicasting) the activation tile. The wide
+    // variant's 64 KB activation stages are worth sharing; the narrow
+    // variant's 10 KB are not worth the cluster-wide release, whose
+    // multicast commit costs the issuing thread several hundred cycles per
+    // stage (measured), so narrow CTAs run alone.
+    static constexpr int CL = NARROW ? 1 : MOE_GEMM_CLUSTER;
+    static constexpr uint16_t CL_MASK = (uint16_t)((1u << CL) - 1);
     static constexpr int SA = NARROW ? 4 : 2;  // weight ring stages (KS blocks each)
     static constexpr int SB = SA;              // activation ring stages
     static constexpr bool MERGED = SA == SB;   // one full barrier per stage for both operands
-    static constexpr int A_STAGE = KS * A_BYTES + SCALE_REP * SF_BYTES;  // tiles, then scales
+    static constexpr int A_STAGE = KS * A_BYTES + SCALE_REP_A * SF_BYTES;  // tiles, then scales
     static constexpr int A_SF = KS * A_BYTES;
     static constexpr int B_BYTES = 2 * NT * BK;  // smem bytes of [hi; lo] activation rows
-    static constexpr int B_STAGE = KS * (B_BYTES + SCALE_REP * BSF_BYTES);  // tiles, then scales
+    static constexpr int B_STAGE = KS * (B_BYTES + SCALE_REP_B * BSF_BYTES);  // tiles, then scales
     static constexpr int B_BASE = SA * A_STAGE;
     static constexpr int B_SF = KS * B_BYTES;
     static constexpr int BAR_BASE = B_BASE + SB * B_STAGE;
     static constexpr int N_FULL = MERGED ? SA : SA + SB;
-    static constexpr int N_BARS = N_FULL + SA + SB + 4;  // full(s), emptyA, emptyB; tfull, tempty x2
+    // merged rings also share one release barrier per stage (one commit)
+    static constexpr int N_EMPTY = MERGED ? SA : SA + SB;
+    static constexpr int N_BARS = N_FULL + N_EMPTY + 4;  // full(s), empty(s); tfull, tempty x2
     static constexpr int PREFIX_BASE = BAR_BASE + N_BARS * 8 + 16;  // int [active + 1]
     static constexpr int EXPERT_BASE = (PREFIX_BASE + (MOE_MAX_EXPERTS + 1) * 4 + 15) / 16 * 16;
     static constexpr int SEG_BASE = (EXPERT_BASE + MOE_MAX_EXPERTS * 4 + 15) / 16 * 16;  // int2
@@ -121,6 +136,7 @@ struct Cfg {
     static constexpr int EPI_BYTES = (MODE == MOE_GEMM_GATEUP) ? 16 * 64 * 4 : 4 * 16 * 32 * 4;
     static constexpr int SMEM = 1024 + EPI_BASE + EPI_BYTES;
     static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0, "stages must keep 1 KB alignment");
+    static_assert(NARROW || SCALE_REP_B == 4, "wide tiles need B scale columns 0..7");
     static_assert(BAR_BASE % 8 == 0 && PREFIX_BASE % 16 == 0 && EXPERT_BASE % 16 == 0 &&
                       SEG_BASE % 16 == 0 && EPI_BASE % 16 == 0,
                   "shared-memory regions must be 16-byte aligned (int2 / float4 accesses)");
@@ -143,7 +159,7 @@ struct Tile {
 // prefix, the active experts and their (first slot, rows) segments. Each
 // role visits its tiles in increasing order, so `a` (the caller's cursor,
 // starting at 0) only moves forward: a few shared-memory reads per tile.
-template <int NT>
+template <int NT, int CL>
 __device__ __forceinline__ bool tile_at(int ct, int n_active, int MTG, int rank,
                                         const int *s_prefix, const int *s_expert,
                                         const int2 *s_seg, int &a, Tile &t) {
@@ -201,8 +217,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
     uint64_t *fullA = (uint64_t *)(smem + C::BAR_BASE);
     uint64_t *fullB = C::MERGED ? fullA : fullA + C::SA;
     uint64_t *emptyA = fullA + C::N_FULL;
-    uint64_t *emptyB = emptyA + C::SA;
-    uint64_t *tfull = emptyB + C::SB;
+    uint64_t *emptyB = C::MERGED ? emptyA : emptyA + C::SA;
+    uint64_t *tfull = emptyA + C::N_EMPTY;
     uint64_t *tempty = tfull + 2;
     uint32_t *tmem_slot = (uint32_t *)(tempty + 2);
     int *abort_flag = (int *)(tmem_slot + 1);
@@ -231,11 +247,12 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
         *abort_flag = 0;
         for (int s = 0; s < C::SA; ++s) {
             tc::mbar_init(&fullA[s], C::MERGED ? 2 : 1);  // merged: both producers arrive
-            tc::mbar_init(&emptyA[s], 1);
+            tc::mbar_init(&emptyA[s], C::MERGED ? C::CL : 1);
         }
         for (int s = 0; s < C::SB; ++s) {
-            if (!C::MERGED) tc::mbar_init(&fullB[s], 1);
-            tc::mbar_init(&emptyB[s], CL);  // released by every CTA of the cluster
+            if (C::MERGED) continue;
+            tc::mbar_init(&fullB[s], 1);
+            tc::mbar_init(&emptyB[s], C::CL);  // released by every CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&tfull[b], C::NSPLIT);  // every issuer commits its half
@@ -252,8 +269,10 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
     tc::cluster_sync();  // peers' barriers are initialised before any multicast lands
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    constexpr int CL = C::CL;
+    constexpr uint16_t CL_MASK = C::CL_MASK;
     const int MT = args.MT, KC = args.KC, MTG = MT / CL;
-    const int rank = (int)tc::cluster_ctarank();
+    const int rank = CL > 1 ? (int)tc::cluster_ctarank() : 0;
     const int cluster_id = blockIdx.x / CL, n_clusters = gridDim.x / CL;
     const int total_tiles = n_active > 0 ? s_prefix[n_active] * MTG : 0;
     const long long LIMIT = args.timeout_cycles;
@@ -272,7 +291,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
             int cur = 0;
             for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
                 Tile t;
-                if (!tile_at<NT>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) {
+                if (!tile_at<NT, C::CL>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) {
                     moe_flag(args.status, MOE_ERR_BAD_INDEX);
                     continue;
                 }
@@ -288,7 +307,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                     }
                     unsigned char *st = smem + s * C::A_STAGE;
                     tc::mbar_arrive_expect_tx(&fullA[s],
-                                              (uint32_t)(nsub * A_TX + C::SCALE_REP * SF_BYTES));
+                                              (uint32_t)(nsub * A_TX + C::SCALE_REP_A * SF_BYTES));
                     for (int sub = 0; sub < nsub; ++sub) {
                         unsigned char *sa = st + sub * A_BYTES;
                         tc::tma_load_2d(sa, &mapA, &fullA[s], (kc + sub) * BK, row0, pol_w);
@@ -298,7 +317,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                     }
                     // the scale block holding this stage's K block(s)
                     const uint8_t *sf = args.a_atoms + (atom0 + kc / ATOM_BLOCKS) * SF_BYTES;
-                    for (int qd = 0; qd < C::SCALE_REP; ++qd)
+                    for (int qd = 0; qd < C::SCALE_REP_A; ++qd)
                         tc::bulk_copy_g2s(st + C::A_SF + qd * SF_BYTES, sf, SF_BYTES, &fullA[s], pol_w);
                 }
             }
@@ -312,7 +331,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
             int cur = 0;
             for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
                 Tile t;
-                if (!tile_at<NT>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) continue;
+                if (!tile_at<NT, C::CL>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) continue;
                 const uint32_t tile_bytes = (uint32_t)(2 * t.nmma * BK);
                 const size_t blk0 = (size_t)t.tt * KC;
                 for (int kc = 0; kc < KC; kc += C::KS, ++it) {
@@ -326,20 +345,25 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                     unsigned char *st = smem + C::B_BASE + s * C::B_STAGE;
                     // the whole stage lands here; this CTA fetches its 1/CL share for all
                     tc::mbar_arrive_expect_tx(
-                        &fullB[s], (uint32_t)nsub * (tile_bytes + C::SCALE_REP * BSF_BYTES));
+                        &fullB[s], (uint32_t)nsub * (tile_bytes + C::SCALE_REP_B * BSF_BYTES));
                     const uint32_t part = tile_bytes / CL;
                     for (int sub = 0; sub < nsub; ++sub) {
                         const size_t blk = blk0 + kc + sub;
-                        tc::bulk_copy_g2s_multicast(
-                            st + sub * C::B_BYTES + rank * part,
-                            args.b_tiles + blk * MOE_GEMM_BTILE + rank * part, part, &fullB[s],
-                            CL_MASK, pol_x);
-                        for (int qd = 0; qd < C::SCALE_REP; ++qd)  // each copy fetched by one CTA
-                            if ((sub * C::SCALE_REP + qd) % CL == rank)
-                                tc::bulk_copy_g2s_multicast(
-                                    st + C::B_SF + (sub * C::SCALE_REP + qd) * BSF_BYTES,
-                                    args.b_atoms + blk * BSF_BYTES, BSF_BYTES, &fullB[s], CL_MASK,
-                                    pol_x);
+                        unsigned char *dst = st + sub * C::B_BYTES + rank * part;
+                        const uint8_t *src = args.b_tiles + blk * MOE_GEMM_BTILE + rank * part;
+                        if (CL > 1)
+                            tc::bulk_copy_g2s_multicast(dst, src, part, &fullB[s], CL_MASK, pol_x);
+                        else
+                            tc::bulk_copy_g2s(dst, src, part, &fullB[s], pol_x);
+                        for (int qd = 0; qd < C::SCALE_REP_B; ++qd) {  // each copy fetched by one CTA
+                            if ((sub * C::SCALE_REP_B + qd) % CL != rank) continue;
+                            unsigned char *sd = st + C::B_SF + (sub * C::SCALE_REP_B + qd) * BSF_BYTES;
+                            const uint8_t *ss = args.b_atoms + blk * BSF_BYTES;
+                            if (CL > 1)
+                                tc::bulk_copy_g2s_multicast(sd, ss, BSF_BYTES, &fullB[s], CL_MASK, pol_x);
+                            else
+                                tc::bulk_copy_g2s(sd, ss, BSF_BYTES, &fullB[s], pol_x);
+                        }
                     }
                 }
             }
@@ -359,7 +383,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
             int cur = 0;
             for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
                 Tile t;
-                if (!tile_at<NT>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) continue;
+                if (!tile_at<NT, C::CL>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) continue;
                 const int buf = lt & 1, use = lt >> 1;
                 ++lt;
                 if (use > 0 && !tc::mbar_wait(&tempty[buf], (use - 1) & 1, LIMIT, abort_p)) {
@@ -390,23 +414,18 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                     const uint32_t slot =
                         tmem + C::SF_TMEM_COL + (uint32_t)(2 * split + (mine & 1)) * C::SF_SLOT;
                     ++mine;
-                    if (C::SCALE_REP == 4)  // both blocks' weight scales: columns slot .. slot + 7
+                    if (C::SCALE_REP_A == 4)  // both blocks' weight scales: columns slot .. slot + 7
                         tc::tmem_cp_128x256b(slot, tc::sdesc_plain_128x32(a_s + C::A_SF));
                     for (int sub = 0; sub < nsub; ++sub) {
                         const uint32_t sfa = slot + 4 * sub, sfb = slot + 4 * C::KS + 8 * sub;
-                        const uint32_t bsf = b_s + C::B_SF + sub * C::SCALE_REP * BSF_BYTES;
-                        if (C::SCALE_REP == 4) {
-                            tc::tmem_cp_128x256b(sfb, tc::sdesc_plain_128x32(bsf));
-                        } else {
-                            // weight scales of K block kc + sub: its half of the block
+                        if (C::SCALE_REP_A == 1)  // K block kc + sub: its half of the scale block
                             tc::tmem_cp_32x128b_warpx4(
                                 sfa, tc::sdesc_plain_32x16_groups256(a_s + C::A_SF + 128 * ((kc + sub) & 1)));
-                            // activation scales: B rows 0..127 (columns 0..3)
+                        const uint32_t bsf = b_s + C::B_SF + sub * C::SCALE_REP_B * BSF_BYTES;
+                        if (C::SCALE_REP_B == 4)
+                            tc::tmem_cp_128x256b(sfb, tc::sdesc_plain_128x32(bsf));
+                        else  // B rows 0..127 (columns 0..3; the narrow tile has at most 32)
                             tc::tmem_cp_32x128b_warpx4(sfb, tc::sdesc_plain_32x16_groups256(bsf));
-                            if (2 * t.nmma > 128)  // rows 128.. (columns 4..7)
-                                tc::tmem_cp_32x128b_warpx4(sfb + 4,
-                                                           tc::sdesc_plain_32x16_groups256(bsf + 128));
-                        }
                         const uint32_t as = a_s + sub * A_BYTES, bs = b_s + sub * C::B_BYTES;
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
@@ -415,8 +434,14 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                                              (!first || sub > 0 || k > 0) ? 1u : 0u);
                     }
                     first = false;
-                    tc::mma_commit(&emptyA[sa]);
-                    tc::mma_commit_multicast(&emptyB[sb], CL_MASK);  // every CTA's copy is free
+                    if (C::MERGED && CL == 1) {  // one release for both rings
+                        tc::mma_commit(&emptyA[sa]);
+                    } else if (C::MERGED) {  // ... in every CTA of the cluster
+                        tc::mma_commit_multicast(&emptyA[sa], CL_MASK);
+                    } else {
+                        tc::mma_commit(&emptyA[sa]);
+                        tc::mma_commit_multicast(&emptyB[sb], CL_MASK);  // every CTA's copy is free
+                    }
                     lastA = &emptyA[sa];
                     parA = ra & 1;
                     lastB = &emptyB[sb];
@@ -439,7 +464,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
         int lt = 0, cur = 0;
         for (int tile = cluster_id; tile < total_tiles; tile += n_clusters) {
             Tile t;
-            if (!tile_at<NT>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t))
+            if (!tile_at<NT, C::CL>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t))
                 continue;
             const int buf = lt & 1, use = lt >> 1;
             ++lt;
@@ -464,7 +489,9 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                     }
                 }
             }
-            if (!tc::mbar_wait(&tfull[buf], use & 1, LIMIT, abort_p)) {
+            // a long wait (the tile's MMAs): sleep in try_wait rather than
+            // spin, leaving issue slots to the producer and issuer warps
+            if (!tc::mbar_wait_sleep(&tfull[buf], use & 1, LIMIT, abort_p)) {
                 if (lane == 0) fail();
                 break;
             }
@@ -649,17 +676,20 @@ namespace {
 template <int MODE, int NT>
 cudaError_t launch_clustered(const CUtensorMap *mA, const CUtensorMap *mA2,
                              const MoeGemmArgs *args, int max_ctas, cudaStream_t st) {
+    using C = Cfg<MODE, NT>;
+    constexpr int CL = C::CL;
     auto kern = moe_grouped_gemm_kernel<MODE, NT>;
-    const size_t sm = Cfg<MODE, NT>::SMEM;
+    const size_t sm = C::SMEM;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (err != cudaSuccess) return err;
+    if (args->MT % CL) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(Cfg<MODE, NT>::THREADS);
+    cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = sm;
     cfg.stream = st;
     cfg.attrs = attr;
@@ -681,7 +711,6 @@ cudaError_t launch_clustered(const CUtensorMap *mA, const CUtensorMap *mA2,
 
 cudaError_t moe_launch_gemm(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
                             const MoeGemmArgs *args, int max_rows, int grid, cudaStream_t st) {
-    if (args->MT % CL) return cudaErrorInvalidValue;
     constexpr int NN = MOE_GEMM_NT_NARROW;
     if (max_rows <= NN)
         return mode == MOE_GEMM_GATEUP
