@@ -127,8 +127,9 @@ struct Cfg {
     static constexpr int N_FULL = MERGED ? SA : SA + SB;
     // merged rings also share one release barrier per stage (one commit)
     static constexpr int N_EMPTY = MERGED ? SA : SA + SB;
-    static constexpr int N_BARS = N_FULL + N_EMPTY + 4;  // full(s), empty(s); tfull, tempty x2
-    static constexpr int PREFIX_BASE = BAR_BASE + N_BARS * 8 + 16;  // int [active + 1]
+    // full(s), empty(s); tfull, tempty x2; one drain barrier per issuer
+    static constexpr int N_BARS = N_FULL + N_EMPTY + 4 + NSPLIT;
+    static constexpr int PREFIX_BASE = (BAR_BASE + N_BARS * 8 + 16 + 15) / 16 * 16;  // int [active + 1]
     static constexpr int EXPERT_BASE = (PREFIX_BASE + (MOE_MAX_EXPERTS + 1) * 4 + 15) / 16 * 16;
     static constexpr int SEG_BASE = (EXPERT_BASE + MOE_MAX_EXPERTS * 4 + 15) / 16 * 16;  // int2
     static constexpr int EPI_BASE = (SEG_BASE + MOE_MAX_EXPERTS * 8 + 15) / 16 * 16;
@@ -220,7 +221,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
     uint64_t *emptyB = C::MERGED ? emptyA : emptyA + C::SA;
     uint64_t *tfull = emptyA + C::N_EMPTY;
     uint64_t *tempty = tfull + 2;
-    uint32_t *tmem_slot = (uint32_t *)(tempty + 2);
+    uint64_t *drain = tempty + 2;  // per issuer: its MMAs in flight, waited on when giving up
+    uint32_t *tmem_slot = (uint32_t *)(drain + C::NSPLIT);
     int *abort_flag = (int *)(tmem_slot + 1);
     int *s_prefix = (int *)(smem + C::PREFIX_BASE);
     int *s_expert = (int *)(smem + C::EXPERT_BASE);
@@ -254,6 +256,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
             tc::mbar_init(&fullB[s], 1);
             tc::mbar_init(&emptyB[s], C::CL);  // released by every CTA of the cluster
         }
+        for (int i = 0; i < C::NSPLIT; ++i) tc::mbar_init(&drain[i], 1);
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&tfull[b], C::NSPLIT);  // every issuer commits its half
             tc::mbar_init(&tempty[b], 4);
@@ -454,6 +457,13 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
             if (ok && lastA &&
                 (!tc::mbar_wait(lastA, parA, LIMIT, abort_p) || !tc::mbar_wait(lastB, parB, LIMIT, abort_p)))
                 fail();
+            if (!ok || *abort_p) {
+                // giving up: this thread's MMAs must finish before tensor memory
+                // is freed (their operands are in shared memory, so they do)
+                int never = 0;
+                tc::mma_commit(&drain[split]);
+                tc::mbar_wait(&drain[split], 0, LIMIT / 100, &never);
+            }
         }
         __syncwarp();
     } else {
@@ -603,6 +613,12 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
         }
     }
 
+    if (*abort_p && tid == 0) {
+        // wound down early: give bulk copies still in flight (issued for stages
+        // nobody consumed) time to land before the shared memory is released
+        const long long t0 = clock64();
+        while (clock64() - t0 < LIMIT / 5000) __nanosleep(1000);
+    }
     tc::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
