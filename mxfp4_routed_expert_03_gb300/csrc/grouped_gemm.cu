@@ -125,8 +125,12 @@ struct Cfg {
     static constexpr int B_SF = KS * B_BYTES;
     static constexpr int BAR_BASE = B_BASE + SB * B_STAGE;
     static constexpr int N_FULL = MERGED ? SA : SA + SB;
-    // merged rings also share one release barrier per stage (one commit)
-    static constexpr int N_EMPTY = MERGED ? SA : SA + SB;
+    // Without a cluster, merged rings also share one release barrier per
+    // stage (one commit). In a cluster the weight ring keeps a local release
+    // so that a CTA refills its own weights without waiting for its peer
+    // (measured faster for the wide variant than one shared release).
+    static constexpr bool SHARED_EMPTY = MERGED && CL == 1;
+    static constexpr int N_EMPTY = SHARED_EMPTY ? SA : SA + SB;
     // full(s), empty(s); tfull, tempty x2; one drain barrier per issuer
     static constexpr int N_BARS = N_FULL + N_EMPTY + 4 + NSPLIT;
     static constexpr int PREFIX_BASE = (BAR_BASE + N_BARS * 8 + 16 + 15) / 16 * 16;  // int [active + 1]
@@ -218,7 +222,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
     uint64_t *fullA = (uint64_t *)(smem + C::BAR_BASE);
     uint64_t *fullB = C::MERGED ? fullA : fullA + C::SA;
     uint64_t *emptyA = fullA + C::N_FULL;
-    uint64_t *emptyB = C::MERGED ? emptyA : emptyA + C::SA;
+    uint64_t *emptyB = C::SHARED_EMPTY ? emptyA : emptyA + C::SA;
     uint64_t *tfull = emptyA + C::N_EMPTY;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;  // per issuer: its MMAs in flight, waited on when giving up
@@ -249,12 +253,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
         *abort_flag = 0;
         for (int s = 0; s < C::SA; ++s) {
             tc::mbar_init(&fullA[s], C::MERGED ? 2 : 1);  // merged: both producers arrive
-            tc::mbar_init(&emptyA[s], C::MERGED ? C::CL : 1);
+            tc::mbar_init(&emptyA[s], 1);
         }
         for (int s = 0; s < C::SB; ++s) {
-            if (C::MERGED) continue;
-            tc::mbar_init(&fullB[s], 1);
-            tc::mbar_init(&emptyB[s], C::CL);  // released by every CTA of the cluster
+            if (!C::MERGED) tc::mbar_init(&fullB[s], 1);
+            if (!C::SHARED_EMPTY) tc::mbar_init(&emptyB[s], C::CL);  // every CTA of the cluster
         }
         for (int i = 0; i < C::NSPLIT; ++i) tc::mbar_init(&drain[i], 1);
         for (int b = 0; b < 2; ++b) {
@@ -437,10 +440,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                                              (!first || sub > 0 || k > 0) ? 1u : 0u);
                     }
                     first = false;
-                    if (C::MERGED && CL == 1) {  // one release for both rings
+                    if (C::SHARED_EMPTY) {  // one release for both rings
                         tc::mma_commit(&emptyA[sa]);
-                    } else if (C::MERGED) {  // ... in every CTA of the cluster
-                        tc::mma_commit_multicast(&emptyA[sa], CL_MASK);
                     } else {
                         tc::mma_commit(&emptyA[sa]);
                         tc::mma_commit_multicast(&emptyB[sb], CL_MASK);  // every CTA's copy is free
