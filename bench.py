@@ -5,8 +5,9 @@ Default workload: one K3-shaped routed layer (d_model 7168, d_ff 1536, 896
 experts, top-16, MXFP4 weights resident in HBM), decode batches of T = 1, 4
 and 16 tokens; one step = moe_plan + the expert FFN for each of the three
 batches (21 tokens). The FFN call of each batch takes the faster entry point
-as measured on GB300: moe_decode (CUDA-core streaming) for a single token,
-moe_forward (tcgen05 grouped GEMMs) from 2 tokens up; `--path
+as measured on GB300, which is moe_forward (tcgen05 grouped GEMMs) at every
+batch size, down to one token (89 vs 101 us for moe_decode, the CUDA-core
+streaming path); CROSSOVER_T keeps the rule explicit, and `--path
 decode|forward` forces one of them. `--workload prefill4k|skewed8k` times moe_plan +
 moe_forward on one prefill batch instead; `--workload router16k` times the
 long prefill whose logits come from the library's own fp32 router (x . W_r)
@@ -42,7 +43,7 @@ EXPERT_BYTES = 17547264            # one expert's three MXFP4 matrices (codes + 
 GATEUP_BYTES = 2 * (D_FF * D_MODEL // 2 + D_FF * D_MODEL // 32)
 DOWN_BYTES = D_MODEL * D_FF // 2 + D_MODEL * D_FF // 32
 N_SETS = 8
-CROSSOVER_T = 1   # largest batch the CUDA-core decode path takes under --path auto
+CROSSOVER_T = 0   # largest batch the CUDA-core decode path takes under --path auto
 
 BENCH_WORKLOADS = {
     "decode": {"Ts": [1, 4, 16], "path": "auto",
@@ -66,8 +67,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default="decode")
     ap.add_argument("--path", choices=["decode", "forward", "auto"], default=None,
-                    help="entry point for the batches (default: auto for decode -- moe_decode "
-                         "for one token, moe_forward above -- and forward for prefill)")
+                    help="entry point for the batches (default: auto -- moe_decode up to "
+                         "CROSSOVER_T tokens, moe_forward above; measured fastest: forward throughout)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall-time budget of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -449,11 +450,12 @@ def run_ours(args):
     roof["traffic"] = kernel_traffic(kname, src, tkey)
 
     # plan: one fused kernel for T <= 64, else top-k, count, scan, scatter;
-    # decode: gate/up, down, combine; forward: quant, schedule, gather, two GEMMs, finalize
+    # decode: gate/up, down, combine; forward: quant, schedule, gather, two GEMMs,
+    # finalize (T <= 16: one fused quant/gather kernel, two GEMMs, finalize)
     launches = 0
     for b in batches:
         launches += 1 if b["T"] <= 64 else 4
-        launches += 3 if b["path"] == "decode" else 6
+        launches += 3 if b["path"] == "decode" else (4 if b["T"] <= 16 else 6)
         if use_router:
             launches += 1 + 2   # router GEMM; shared gate/up and down GEMMs
     line = {

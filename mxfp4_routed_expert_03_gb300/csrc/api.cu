@@ -420,14 +420,23 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     float *acc = (float *)(base + L.acc);
     int32_t *prefix = (int32_t *)(base + L.prefix);
 
-    cudaError_t err = moe_launch_quant_x(T, D, x, xq_hi, xq_lo, xs_hi, xs_lo, st);
-    if (err == cudaSuccess)
-        err = moe_launch_schedule(E, MOE_GEMM_NTMAX, plan->offsets, plan->active, prefix,
-                                  h->status, st);
-    if (err == cudaSuccess)
-        err = moe_launch_gather_x(L.max_tt, E, k, rows, D, MOE_GEMM_NTMAX, plan->offsets,
-                                  plan->perm, plan->active, prefix, xq_hi, xq_lo, xs_hi, xs_lo,
-                                  xb, xa, h->status, st);
+    // Small batches (every expert one token tile): quantise, gather, schedule
+    // and zero the accumulator in one launch; larger ones in four.
+    const bool small = T <= MOE_GEMM_NT_NARROW;
+    cudaError_t err;
+    if (small) {
+        err = moe_launch_prep_small(T, E, k, D, plan->offsets, plan->perm, plan->active, x, prefix,
+                                    xb, xa, d.has_shared ? nullptr : acc, h->status, st);
+    } else {
+        err = moe_launch_quant_x(T, D, x, xq_hi, xq_lo, xs_hi, xs_lo, st);
+        if (err == cudaSuccess)
+            err = moe_launch_schedule(E, MOE_GEMM_NTMAX, plan->offsets, plan->active, prefix,
+                                      h->status, st);
+        if (err == cudaSuccess)
+            err = moe_launch_gather_x(L.max_tt, E, k, rows, D, MOE_GEMM_NTMAX, plan->offsets,
+                                      plan->perm, plan->active, prefix, xq_hi, xq_lo, xs_hi,
+                                      xs_lo, xb, xa, h->status, st);
+    }
     MoeGemmArgs a;
     memset(&a, 0, sizeof(a));
     a.E = E;
@@ -460,7 +469,7 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         if (d.has_shared) {  // the shared expert writes acc; the routed rows add onto it
             if (run_shared(h, T, x, (uint16_t *)(base + L.hsh), acc, st) != MOE_OK)
                 err = cudaErrorLaunchFailure;
-        } else {
+        } else if (!small) {  // (small batches zeroed it in the first launch)
             err = cudaMemsetAsync(acc, 0, (size_t)T * D * sizeof(float), st);
         }
     }

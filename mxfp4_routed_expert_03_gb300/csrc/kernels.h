@@ -47,6 +47,12 @@ cudaError_t moe_launch_quant_x(int T, int D, const uint16_t *x, uint8_t *q_hi, u
                                uint8_t *s_hi, uint8_t *s_lo, cudaStream_t st);
 cudaError_t moe_launch_schedule(int E, int ntmax, const int32_t *offsets, const int32_t *active,
                                 int32_t *tt_prefix, int *status, cudaStream_t st);
+// T <= MOE_GEMM_NT_NARROW: quantise + gather + identity schedule (+ zero acc
+// when acc is not null) in one launch.
+cudaError_t moe_launch_prep_small(int T, int E, int k, int D, const int32_t *offsets,
+                                  const int32_t *perm, const int32_t *active, const uint16_t *x,
+                                  int32_t *tt_prefix, uint8_t *tiles, uint8_t *atoms, float *acc,
+                                  int *status, cudaStream_t st);
 cudaError_t moe_launch_finalize(int T, int D, const float *acc, uint16_t *out, cudaStream_t st);
 cudaError_t moe_launch_gather_x(int max_tt, int E, int k, int n_rows, int D, int ntmax,
                                 const int32_t *offsets, const int32_t *perm, const int32_t *active,

@@ -7,16 +7,13 @@
 
 #define FULL_MASK 0xFFFFFFFFu
 
-// One thread per 32-element block of x: hi/lo E4M3 bytes and their E8M0 scales.
-__global__ void __launch_bounds__(256) moe_quant_x_kernel(int64_t n_blocks, int D,
-                                                          const uint16_t *__restrict__ x,
-                                                          uint8_t *__restrict__ q_hi,
-                                                          uint8_t *__restrict__ q_lo,
-                                                          uint8_t *__restrict__ s_hi,
-                                                          uint8_t *__restrict__ s_lo) {
-    int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    if (b >= n_blocks) return;
-    const uint4 *src = (const uint4 *)(x + b * 32);
+// Two-term MXFP8 split of 32 consecutive bf16 values: hi = E4M3(v / 2^sh),
+// lo = E4M3((v - hi 2^sh) / 2^sl), sh and sl the E8M0 exponents of the block
+// maxima; hw / lw receive the 32 hi / lo bytes (element 2i in the low byte of
+// each pair).
+__device__ __forceinline__ void split_block32(const uint16_t *__restrict__ src16, uint32_t (&hw)[8],
+                                              uint32_t (&lw)[8], int &sh, int &sl) {
+    const uint4 *src = (const uint4 *)src16;
     float v[32];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -31,9 +28,8 @@ __global__ void __launch_bounds__(256) moe_quant_x_kernel(int64_t n_blocks, int 
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    int sh = mx8::scale_exp(amax);
+    sh = mx8::scale_exp(amax);
     float inv_h = mx8::exp2i(-sh), sc_h = mx8::exp2i(sh);
-    uint32_t hw[8];
     float r[32];
     float ramax = 0.f;
 #pragma unroll
@@ -46,15 +42,28 @@ __global__ void __launch_bounds__(256) moe_quant_x_kernel(int64_t n_blocks, int 
         if (i % 2 == 0) hw[i / 2] = p;
         else hw[i / 2] |= p << 16;
     }
-    int sl = mx8::scale_exp(ramax);
+    sl = mx8::scale_exp(ramax);
     float inv_l = mx8::exp2i(-sl);
-    uint32_t lw[8];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         uint32_t p = mx8::to_e4m3x2(r[2 * i] * inv_l, r[2 * i + 1] * inv_l);
         if (i % 2 == 0) lw[i / 2] = p;
         else lw[i / 2] |= p << 16;
     }
+}
+
+// One thread per 32-element block of x: hi/lo E4M3 bytes and their E8M0 scales.
+__global__ void __launch_bounds__(256) moe_quant_x_kernel(int64_t n_blocks, int D,
+                                                          const uint16_t *__restrict__ x,
+                                                          uint8_t *__restrict__ q_hi,
+                                                          uint8_t *__restrict__ q_lo,
+                                                          uint8_t *__restrict__ s_hi,
+                                                          uint8_t *__restrict__ s_lo) {
+    int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (b >= n_blocks) return;
+    uint32_t hw[8], lw[8];
+    int sh, sl;
+    split_block32(x + b * 32, hw, lw, sh, sl);
     uint4 *dh = (uint4 *)(q_hi + b * 32), *dl = (uint4 *)(q_lo + b * 32);
     dh[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     dh[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
@@ -198,6 +207,80 @@ __global__ void __launch_bounds__(256) moe_gather_x_kernel(
         atoms[at + off(r, c)] = s_hi[(size_t)s_tok[r] * nb + b];
         atoms[at + off(nmma + r, c)] = s_lo[(size_t)s_tok[r] * nb + b];
     }
+}
+
+// Batches of at most MOE_GEMM_NT_NARROW tokens: every active expert has one
+// token tile (a token chooses an expert at most once), so token tile a is
+// active expert a and the schedule is the identity. One block per active
+// expert quantises its tokens' x rows straight into the B tile and scale
+// block layout the gather kernel writes (same split as moe_quant_x_kernel,
+// same bytes), writes tt_prefix[a] = a, and every block zeroes its share of
+// the fp32 accumulator when one is given. Replaces quant, schedule, gather
+// and the accumulator memset of larger batches.
+__global__ void __launch_bounds__(256) moe_prep_small_kernel(
+    int E, int k, int n_rows, int D, int T, const int32_t *__restrict__ offsets,
+    const int32_t *__restrict__ perm, const int32_t *__restrict__ active,
+    const uint16_t *__restrict__ x, int32_t *__restrict__ tt_prefix, uint8_t *__restrict__ tiles,
+    uint8_t *__restrict__ atoms, float *__restrict__ acc, int *status) {
+    __shared__ int s_tok[MOE_GEMM_NT_NARROW];
+    if (acc) {  // zero this block's share of acc [T][D]
+        const int64_t n4 = (int64_t)T * D / 4, per = (n4 + gridDim.x - 1) / gridDim.x;
+        const int64_t i0 = (int64_t)blockIdx.x * per, i1 = min(i0 + per, n4);
+        for (int64_t i = i0 + threadIdx.x; i < i1; i += blockDim.x)
+            ((float4 *)acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    int n_active = active[0];
+    if (n_active < 0 || n_active > E) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) moe_flag(status, MOE_ERR_BAD_INDEX);
+        return;
+    }
+    const int a = blockIdx.x;
+    if (a == 0 && threadIdx.x == 0) tt_prefix[n_active] = n_active;
+    if (a >= n_active) return;
+    if (threadIdx.x == 0) tt_prefix[a] = a;
+    const int e = active[1 + a];
+    if (e < 0 || e >= E) { if (threadIdx.x == 0) moe_flag(status, MOE_ERR_BAD_INDEX); return; }
+    const int sb = offsets[e], n = offsets[e + 1] - sb;
+    if (sb < 0 || n <= 0 || n > MOE_GEMM_NT_NARROW || sb + n > n_rows) {
+        if (threadIdx.x == 0) moe_flag(status, MOE_ERR_BAD_INDEX);
+        return;
+    }
+    for (int r = threadIdx.x; r < n; r += blockDim.x) {
+        int fl = perm[sb + r];
+        if (fl < 0 || fl >= n_rows) { moe_flag(status, MOE_ERR_BAD_INDEX); fl = 0; }
+        s_tok[r] = fl / k;
+    }
+    __syncthreads();
+    const int KC = D / 128, nb = D / 32, nmma = (n + 15) & ~15;
+    auto off = [](int row, int c) {
+        const int i = row & 31, j = row >> 5;
+        return (i >> 3) * 256 + (j >> 2) * 128 + (i & 7) * 16 + (j & 3) * 4 + c;
+    };
+    for (int i = threadIdx.x; i < n * nb; i += blockDim.x) {
+        const int r = i / nb, b = i % nb, kc = b >> 2, c = b & 3;
+        uint32_t hw[8], lw[8];
+        int sh, sl;
+        split_block32(x + (size_t)s_tok[r] * D + (size_t)b * 32, hw, lw, sh, sl);
+        uint8_t *blk = tiles + ((size_t)a * KC + kc) * MOE_GEMM_BTILE;
+        const int rl = nmma + r, p0 = 2 * c, p1 = 2 * c + 1;  // 16-byte pieces of the row
+        *(uint4 *)(blk + r * 128 + ((p0 ^ (r & 7)) * 16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *(uint4 *)(blk + r * 128 + ((p1 ^ (r & 7)) * 16)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+        *(uint4 *)(blk + rl * 128 + ((p0 ^ (rl & 7)) * 16)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        *(uint4 *)(blk + rl * 128 + ((p1 ^ (rl & 7)) * 16)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+        const size_t at = ((size_t)a * KC + kc) * 1024;
+        atoms[at + off(r, c)] = (uint8_t)(sh + 127);
+        atoms[at + off(rl, c)] = (uint8_t)(sl + 127);
+    }
+}
+
+cudaError_t moe_launch_prep_small(int T, int E, int k, int D, const int32_t *offsets,
+                                  const int32_t *perm, const int32_t *active, const uint16_t *x,
+                                  int32_t *tt_prefix, uint8_t *tiles, uint8_t *atoms, float *acc,
+                                  int *status, cudaStream_t st) {
+    const int grid = min(T * k, E);  // an upper bound on the active experts
+    moe_prep_small_kernel<<<grid, 256, 0, st>>>(E, k, T * k, D, T, offsets, perm, active, x,
+                                                tt_prefix, tiles, atoms, acc, status);
+    return cudaGetLastError();
 }
 
 cudaError_t moe_launch_gather_x(int max_tt, int E, int k, int n_rows, int D, int ntmax,
