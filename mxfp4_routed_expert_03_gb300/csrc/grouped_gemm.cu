@@ -540,35 +540,64 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                     const int f = t.mt * 64 + rr;  // intermediate row of this lane
                     const size_t at_base = ((size_t)t.tt * (F / 128) + f / 128) * BSF_BYTES;
                     const int cblk = (f & 127) >> 5;
+                    // Eight independent columns, each step over all eight before the
+                    // next, so that reductions and conversions overlap instead of
+                    // forming one long chain per column. SiLU in fast math: its
+                    // ~1e-6 relative error is far below the E4M3 split that follows.
+                    float h[8], rr8[8];
+                    int sh[8], sl[8];
+                    uint32_t hb[8], lb[8];
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj) {
                         const int j = gate ? jj : jj + 8;
                         const float g = gate ? v[j] : stg[j * 64 + rr];
                         const float u = gate ? stg[j * 64 + rr] : v[j];
-                        const float h = g / (1.f + expf(-g)) * u;
-                        // two-term E4M3 split over this warp's 32 rows (one MX block along F)
-                        const float amax = __uint_as_float(
-                            __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(h))));
-                        const int sh = mx8::scale_exp(amax);
-                        const uint32_t hb = mx8::to_e4m3x2(h * mx8::exp2i(-sh), 0.f) & 0xFF;
-                        const float r = h - mx8::from_e4m3x2(hb).x * mx8::exp2i(sh);
-                        const float ramax = __uint_as_float(
-                            __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(r))));
-                        const int sl = mx8::scale_exp(ramax);
-                        const uint32_t lb = mx8::to_e4m3x2(r * mx8::exp2i(-sl), 0.f) & 0xFF;
+                        h[jj] = __fdividef(g, 1.f + __expf(-g)) * u;
+                    }
+                    // two-term E4M3 split over this warp's 32 rows (one MX block along F)
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj)
+                        sh[jj] = mx8::scale_exp(__uint_as_float(
+                            __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(h[jj])))));
+#pragma unroll
+                    for (int jj = 0; jj < 8; jj += 2) {
+                        const uint32_t p = mx8::to_e4m3x2(h[jj] * mx8::exp2i(-sh[jj]),
+                                                          h[jj + 1] * mx8::exp2i(-sh[jj + 1]));
+                        const float2 back = mx8::from_e4m3x2(p);
+                        hb[jj] = p & 0xFF;
+                        hb[jj + 1] = (p >> 8) & 0xFF;
+                        rr8[jj] = h[jj] - back.x * mx8::exp2i(sh[jj]);
+                        rr8[jj + 1] = h[jj + 1] - back.y * mx8::exp2i(sh[jj + 1]);
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj)
+                        sl[jj] = mx8::scale_exp(__uint_as_float(
+                            __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(rr8[jj])))));
+#pragma unroll
+                    for (int jj = 0; jj < 8; jj += 2) {
+                        const uint32_t p = mx8::to_e4m3x2(rr8[jj] * mx8::exp2i(-sl[jj]),
+                                                          rr8[jj + 1] * mx8::exp2i(-sl[jj + 1]));
+                        lb[jj] = p & 0xFF;
+                        lb[jj + 1] = (p >> 8) & 0xFF;
+                    }
+                    uint8_t *hblk =
+                        args.h_tiles + ((size_t)t.tt * (F / 128) + f / 128) * MOE_GEMM_BTILE;
+                    const int cb = f & 127;
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const int j = gate ? jj : jj + 8;
                         if (c0 + j < t.n) {
                             // GEMM2 B tile of chunk f / 128: rows r (hi) and nmma + r (lo),
                             // byte f % 128 of the row, pre-swizzled
-                            uint8_t *blk = args.h_tiles +
-                                           ((size_t)t.tt * (F / 128) + f / 128) * MOE_GEMM_BTILE;
-                            const int r = c0 + j, rlo = t.nmma + r, cb = f & 127;
-                            blk[r * 128 + (((cb >> 4) ^ (r & 7)) << 4) + (cb & 15)] = (uint8_t)hb;
-                            blk[rlo * 128 + (((cb >> 4) ^ (rlo & 7)) << 4) + (cb & 15)] = (uint8_t)lb;
+                            const int r = c0 + j, rlo = t.nmma + r;
+                            hblk[r * 128 + (((cb >> 4) ^ (r & 7)) << 4) + (cb & 15)] = (uint8_t)hb[jj];
+                            hblk[rlo * 128 + (((cb >> 4) ^ (rlo & 7)) << 4) + (cb & 15)] =
+                                (uint8_t)lb[jj];
                             if (lane == 0) {
                                 // GEMM2 chunk f / 128, block (f % 128) / 32; B rows hi r, lo nmma + r
-                                args.h_atoms[at_base + bsf_off(c0 + j, cblk)] = (uint8_t)(sh + 127);
+                                args.h_atoms[at_base + bsf_off(c0 + j, cblk)] = (uint8_t)(sh[jj] + 127);
                                 args.h_atoms[at_base + bsf_off(t.nmma + c0 + j, cblk)] =
-                                    (uint8_t)(sl + 127);
+                                    (uint8_t)(sl[jj] + 127);
                             }
                         }
                     }
