@@ -240,6 +240,57 @@ int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *
 int moe_decode_noalloc(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
                        uint16_t *out, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * Expert streaming: the routed experts stay in a large slow tier and the ones
+ * a batch selects are copied into a fixed number of per-layer slots with
+ * online least-recently-used replacement, reading the route union once per
+ * batch (Moonshine README, "How the engine works"; Moonshine GitHub README,
+ * "Decode"). On GB300
+ * the slow tier is host memory that the GPU reads directly (pinned host
+ * allocations are device-addressable; over NVLink-C2C on Grace) and the slots
+ * are HBM. The cache is managed on the device: no host round trip per call.
+ *
+ * Replacement rule (exact, so that callers and tests can predict it): each
+ * moe_forward call advances a clock; every active expert of the plan that is
+ * resident gets its slot stamped with the clock (a hit); the missing experts,
+ * in increasing expert index, take the slots not stamped by this call in
+ * increasing (stamp, slot) order (empty slots carry stamp 0, so they go
+ * first), evicting the experts held there.
+ * ------------------------------------------------------------------------- */
+
+/* Host. Bytes of the device cache-state buffer for a streaming handle:
+ * clock, counters, slot_of [n_experts], expert_of / stamp [n_slots], last
+ * miss lists. */
+size_t moe_stream_state_bytes(int32_t n_experts, int32_t n_slots);
+
+/* Host. Like moe_create for a layer whose routed experts live in host memory.
+ *   host_w  gate/up/down codes and scales of all n_experts experts (layouts of
+ *           moe_weights), host memory the device can read (e.g. cudaHostAlloc);
+ *           each array 16-byte aligned; w_router / sh_* are ignored here.
+ *   slot_w  device arrays in the same layouts holding n_slots experts (the
+ *           cache; 32-byte aligned codes, 16-byte aligned scales), plus the
+ *           resident-tier pointers w_router / sh_gate / sh_up / sh_down as for
+ *           moe_create.
+ *   n_slots 1..min(n_experts, 1024).
+ *   state   device buffer of moe_stream_state_bytes(n_experts, n_slots) bytes,
+ *           caller-owned, zero-initialised by this call (stream 0, synchronous).
+ * moe_prepared_bytes then sizes the prepared buffer for n_slots experts;
+ * moe_prepare re-lays only the resident tier (W_r) and records the buffer:
+ * slots are prepared as experts arrive. moe_forward makes every active expert
+ * of the plan resident before its GEMMs (misses copied from host memory) and
+ * returns MOE_ERR_UNSUPPORTED when T * top_k exceeds n_slots while n_experts
+ * does too (the plan could then need more slots than exist). moe_decode and
+ * moe_decode_noalloc return MOE_ERR_UNSUPPORTED on a streaming handle. */
+int moe_create_streaming(const moe_desc *desc, const moe_weights *host_w,
+                         const moe_weights *slot_w, int32_t n_slots, void *state,
+                         moe_handle **out);
+
+/* Host. Synchronises `stream` and reads the cache counters of a streaming
+ * handle: total hits and misses (experts) over all calls, and the misses of
+ * the last call. MOE_ERR_INVALID_ARG for other handles. */
+int moe_stream_stats(moe_handle *h, int64_t *hits, int64_t *misses, int32_t *last_misses,
+                     void *stream);
+
 /* Host. Instrumentation for timing one kernel on the library's own stream:
  * while `which` names a kernel (enum moe_prof_kernel), every later call that
  * launches it records ev_start (a cudaEvent_t) immediately before that launch

@@ -35,8 +35,8 @@ MOE_OP_DECODE = 2
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_create", "moe_destroy", "moe_expert_bytes", "moe_prepared_bytes", "moe_prepare",
            "moe_workspace_bytes", "moe_plan", "moe_router_logits", "moe_forward", "moe_decode",
-           "moe_decode_noalloc",
-           "moe_profile_kernel", "moe_status", "moe_strerror")
+           "moe_decode_noalloc", "moe_stream_state_bytes", "moe_create_streaming",
+           "moe_stream_stats", "moe_profile_kernel", "moe_status", "moe_strerror")
 
 MOE_PROF_NONE = 0
 MOE_PROF_DECODE_GATEUP = 1
@@ -111,6 +111,14 @@ def lib() -> ctypes.CDLL:
         L.moe_status.restype = ctypes.c_int
         L.moe_strerror.argtypes = [ctypes.c_int]
         L.moe_strerror.restype = ctypes.c_char_p
+        L.moe_stream_state_bytes.argtypes = [i32, i32]
+        L.moe_stream_state_bytes.restype = sz
+        L.moe_create_streaming.argtypes = [ctypes.POINTER(moe_desc), ctypes.POINTER(moe_weights),
+                                           ctypes.POINTER(moe_weights), i32, p, ctypes.POINTER(p)]
+        L.moe_create_streaming.restype = ctypes.c_int
+        L.moe_stream_stats.argtypes = [p, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                       ctypes.POINTER(i32), p]
+        L.moe_stream_stats.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -146,6 +154,32 @@ def moe_create(desc: moe_desc, weights: moe_weights) -> int:
     if rc != MOE_OK:
         raise MoeError(rc, "moe_create")
     return h.value
+
+
+def moe_stream_state_bytes(n_experts: int, n_slots: int) -> int:
+    return lib().moe_stream_state_bytes(n_experts, n_slots)
+
+
+def moe_create_streaming(desc: moe_desc, host_weights: moe_weights, slot_weights: moe_weights,
+                         n_slots: int, state) -> int:
+    """host_weights: pinned host arrays of all experts; slot_weights: device cache arrays."""
+    h = ctypes.c_void_p()
+    rc = lib().moe_create_streaming(ctypes.byref(desc), ctypes.byref(host_weights),
+                                    ctypes.byref(slot_weights), n_slots, _ptr(state),
+                                    ctypes.byref(h))
+    if rc != MOE_OK:
+        raise MoeError(rc, "moe_create_streaming")
+    return h.value
+
+
+def moe_stream_stats(h, stream=None) -> tuple:
+    """(hits, misses, last_misses) of a streaming handle; synchronises the stream."""
+    hits, misses, last = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+    rc = lib().moe_stream_stats(h, ctypes.byref(hits), ctypes.byref(misses), ctypes.byref(last),
+                                _stream(stream))
+    if rc != MOE_OK:
+        raise MoeError(rc, "moe_stream_stats")
+    return hits.value, misses.value, last.value
 
 
 def moe_destroy(h: int) -> None:

@@ -20,6 +20,10 @@ struct moe_handle {
     const uint8_t *atoms;  // caller buffer filled by moe_prepare (NULL until then)
     bool wr_ready;         // W_r terms written by moe_prepare
     MoeProf prof;          // optional timing events (moe_profile_kernel)
+    int wE;                // experts held by the weight arrays w.* (n_slots when streaming)
+    bool streaming;        // expert streaming: w.* are the slot cache, host_w the store
+    moe_weights host_w;    // streaming: all experts, host memory the device can read
+    void *sstate;          // streaming: device cache state (moe_stream_state_bytes)
 };
 
 // Device-side waits give up after this many SM clocks (about one second).
@@ -108,14 +112,14 @@ static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// prepared weight scales: gate/up tiles (64 + 64 rows), then down tiles (128 rows)
-static size_t gu_atoms_bytes(const moe_desc &d) {
-    return moe_prepared_atoms_bytes(d.n_experts, d.d_ff, d.d_model, 64);
+// prepared weight scales of the wE experts in the weight arrays: gate/up
+// tiles (64 + 64 rows), then down tiles (128 rows)
+static size_t gu_atoms_bytes(const moe_desc &d, int wE) {
+    return moe_prepared_atoms_bytes(wE, d.d_ff, d.d_model, 64);
 }
 
-static size_t atoms_bytes(const moe_desc &d) {
-    return align_up(gu_atoms_bytes(d) + moe_prepared_atoms_bytes(d.n_experts, d.d_model, d.d_ff, 128),
-                    256);
+static size_t atoms_bytes(const moe_desc &d, int wE) {
+    return align_up(gu_atoms_bytes(d, wE) + moe_prepared_atoms_bytes(wE, d.d_model, d.d_ff, 128), 256);
 }
 
 MOE_API int64_t moe_expert_bytes(int32_t d_model, int32_t d_ff) {
@@ -139,7 +143,9 @@ MOE_API const char *moe_strerror(int code) {
     }
 }
 
-MOE_API int moe_create(const moe_desc *d, const moe_weights *w, moe_handle **out) {
+// moe_create for weight arrays holding wE experts (wE = n_experts, or the
+// slot count of a streaming layer).
+static int create_impl(const moe_desc *d, const moe_weights *w, int wE, moe_handle **out) {
     if (!out) return MOE_ERR_INVALID_ARG;
     *out = NULL;
     if (!d || !w) return MOE_ERR_INVALID_ARG;
@@ -179,13 +185,14 @@ MOE_API int moe_create(const moe_desc *d, const moe_weights *w, moe_handle **out
     if (!h) return MOE_ERR_INVALID_ARG;
     h->desc = *d;
     h->w = *w;
+    h->wE = wE;
     h->device = dev;
     if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         free(h);
         return MOE_ERR_CUDA;
     }
     {
-        const uint64_t D = d->d_model, F = d->d_ff, E = d->n_experts;
+        const uint64_t D = d->d_model, F = d->d_ff, E = wE;  // experts in the weight arrays
         const CUtensorMapDataType fp4 = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
         if (!make_map_2d(&h->map_gate, fp4, w->gate_q, D, E * F, D / 2, 128, 64) ||
             !make_map_2d(&h->map_up, fp4, w->up_q, D, E * F, D / 2, 128, 64) ||
@@ -212,6 +219,96 @@ MOE_API int moe_create(const moe_desc *d, const moe_weights *w, moe_handle **out
     }
     *out = h;
     return MOE_OK;
+}
+
+MOE_API int moe_create(const moe_desc *d, const moe_weights *w, moe_handle **out) {
+    return create_impl(d, w, d ? d->n_experts : 0, out);
+}
+
+MOE_API size_t moe_stream_state_bytes(int32_t n_experts, int32_t n_slots) {
+    if (n_experts <= 0 || n_slots <= 0 || n_experts > MOE_MAX_EXPERTS || n_slots > 1024) return 0;
+    return moe_stream_state_size(n_experts, n_slots);
+}
+
+MOE_API int moe_create_streaming(const moe_desc *d, const moe_weights *host_w,
+                                 const moe_weights *slot_w, int32_t n_slots, void *state,
+                                 moe_handle **out) {
+    if (!out) return MOE_ERR_INVALID_ARG;
+    *out = NULL;
+    if (!d || !host_w || !slot_w || !state) return MOE_ERR_INVALID_ARG;
+    if (d->n_experts <= 0 || n_slots < 1 || n_slots > d->n_experts || n_slots > 1024)
+        return MOE_ERR_INVALID_ARG;
+    const void *hp[] = {host_w->gate_q, host_w->gate_s, host_w->up_q,
+                        host_w->up_s, host_w->down_q, host_w->down_s};
+    for (const void *p : hp) {
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+        // the copy kernel reads these through the same addresses: require
+        // registered (pinned) host memory mapped at the host address
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_INVALID_ARG;
+        }
+        if (at.type != cudaMemoryTypeHost || at.devicePointer != p) return MOE_ERR_INVALID_ARG;
+    }
+    if ((uintptr_t)state & 15u) return MOE_ERR_INVALID_ARG;
+    moe_handle *h = nullptr;
+    int rc = create_impl(d, slot_w, n_slots, &h);
+    if (rc != MOE_OK) return rc;
+    h->streaming = true;
+    h->host_w = *host_w;
+    h->sstate = state;
+    if (moe_launch_stream_init(d->n_experts, n_slots, state, 0) != cudaSuccess ||
+        cudaStreamSynchronize(0) != cudaSuccess) {
+        cudaFree(h->status);
+        free(h);
+        return MOE_ERR_CUDA;
+    }
+    *out = h;
+    return MOE_OK;
+}
+
+MOE_API int moe_stream_stats(moe_handle *h, int64_t *hits, int64_t *misses, int32_t *last_misses,
+                             void *stream) {
+    if (!h || !h->streaming) return MOE_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+    MoeStreamHdr hdr;
+    if (cudaMemcpy(&hdr, h->sstate, sizeof(hdr), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (hits) *hits = (int64_t)hdr.hits;
+    if (misses) *misses = (int64_t)hdr.misses;
+    if (last_misses) *last_misses = hdr.last_miss;
+    return MOE_OK;
+}
+
+// Expert streaming: make every active expert of the plan resident (device-side
+// replacement, copies of the misses from host memory, their scale blocks).
+static cudaError_t stream_fill(moe_handle *h, const moe_plan_buf *plan, cudaStream_t st) {
+    const moe_desc &d = h->desc;
+    const int E = d.n_experts, S = h->wE, D = d.d_model, F = d.d_ff;
+    cudaError_t err = moe_launch_stream_lru(E, S, plan->active, h->sstate, h->status, st);
+    MoeStreamCopy c;
+    const moe_weights &hw = h->host_w, &sw = h->w;
+    const uint8_t *hs[6] = {hw.gate_q, hw.gate_s, hw.up_q, hw.up_s, hw.down_q, hw.down_s};
+    const uint8_t *ss[6] = {sw.gate_q, sw.gate_s, sw.up_q, sw.up_s, sw.down_q, sw.down_s};
+    const int64_t n = (int64_t)D * F;
+    const int64_t by[6] = {n / 2, n / 32, n / 2, n / 32, n / 2, n / 32};
+    for (int i = 0; i < 6; ++i) {
+        c.host[i] = hs[i];
+        c.slot[i] = const_cast<uint8_t *>(ss[i]);
+        c.bytes[i] = by[i];
+    }
+    if (err == cudaSuccess) err = moe_launch_stream_copy(E, S, h->sstate, &c, h->num_sms, st);
+    const MoeStreamView v = moe_stream_view(h->sstate, E, S);
+    uint8_t *atoms = const_cast<uint8_t *>(h->atoms);
+    if (err == cudaSuccess)
+        err = moe_launch_prepare_atoms_slots(F, D, 64, sw.gate_s, sw.up_s, atoms, &v.hdr->last_miss,
+                                             v.miss_s, h->num_sms, st);
+    if (err == cudaSuccess)
+        err = moe_launch_prepare_atoms_slots(D, F, 128, sw.down_s, nullptr,
+                                             atoms + gu_atoms_bytes(d, S), &v.hdr->last_miss,
+                                             v.miss_s, h->num_sms, st);
+    return err;
 }
 
 MOE_API void moe_destroy(moe_handle *h) {
@@ -355,6 +452,7 @@ MOE_API int moe_router_logits(moe_handle *h, int32_t T, const uint16_t *x, float
 MOE_API int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
                        uint16_t *out, void *ws, size_t ws_bytes, void *stream) {
     if (!h || T < 0) return MOE_ERR_INVALID_ARG;
+    if (h->streaming) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
     if (!x || !out || !plan_ok(plan)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
@@ -380,6 +478,7 @@ MOE_API int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_pl
 MOE_API int moe_decode_noalloc(moe_handle *h, int32_t T, const uint16_t *x,
                                const moe_plan_buf *plan, uint16_t *out, void *stream) {
     if (!h || T < 0) return MOE_ERR_INVALID_ARG;
+    if (h->streaming) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
     if (!x || !out || !plan_ok(plan)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
@@ -409,6 +508,9 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     if ((int64_t)T * h->desc.top_k > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
     if (!h->atoms) return MOE_ERR_NOT_PREPARED;
     const moe_desc &d = h->desc;
+    // a streaming layer must be able to hold every expert a plan can select
+    if (h->streaming && (int64_t)T * d.top_k > h->wE && d.n_experts > h->wE)
+        return MOE_ERR_UNSUPPORTED;
     const FwdLayout L = fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k, d.has_shared);
     if (ws_bytes < L.total || !ws || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
@@ -450,6 +552,11 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     a.topk_w = plan->topk_w;
     a.status = h->status;
     a.timeout_cycles = kTimeoutCycles;
+    if (h->streaming) {  // experts resident first; the GEMMs then address their slots
+        if (err == cudaSuccess) err = stream_fill(h, plan, st);
+        a.w_index = moe_stream_view(h->sstate, E, h->wE).slot_of;
+        a.n_wexp = h->wE;
+    }
     if (err == cudaSuccess) {
         MoeGemmArgs g1 = a;
         g1.M = F;
@@ -479,7 +586,7 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         g2.MT = D / 128;
         g2.K = F;
         g2.KC = F / 128;
-        g2.a_atoms = h->atoms + gu_atoms_bytes(d);
+        g2.a_atoms = h->atoms + gu_atoms_bytes(d, h->wE);
         g2.b_tiles = hb;
         g2.b_atoms = ha;
         g2.acc = acc;
@@ -499,7 +606,7 @@ static size_t wr_terms_bytes(const moe_desc &d) {
 
 MOE_API size_t moe_prepared_bytes(const moe_handle *h) {
     if (!h) return 0;
-    return atoms_bytes(h->desc) + wr_terms_bytes(h->desc);
+    return atoms_bytes(h->desc, h->wE) + wr_terms_bytes(h->desc);
 }
 
 MOE_API int moe_prepare(moe_handle *h, void *buf, size_t bytes, void *stream) {
@@ -511,16 +618,20 @@ MOE_API int moe_prepare(moe_handle *h, void *buf, size_t bytes, void *stream) {
     uint8_t *out = (uint8_t *)buf;
     cudaStream_t st = (cudaStream_t)stream;
     // gate/up tiles: 64 gate rows over the same 64 up rows; down tiles: 128 rows
-    cudaError_t err = moe_launch_prepare_atoms(E, F, D, 64, h->w.gate_s, h->w.up_s, out, st);
-    if (err == cudaSuccess)
-        err = moe_launch_prepare_atoms(E, D, F, 128, h->w.down_s, nullptr, out + gu_atoms_bytes(d),
-                                       st);
+    // (a streaming layer's slots are prepared as experts arrive)
+    cudaError_t err = cudaSuccess;
+    if (!h->streaming) {
+        err = moe_launch_prepare_atoms(E, F, D, 64, h->w.gate_s, h->w.up_s, out, st);
+        if (err == cudaSuccess)
+            err = moe_launch_prepare_atoms(E, D, F, 128, h->w.down_s, nullptr,
+                                           out + gu_atoms_bytes(d, h->wE), st);
+    }
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     if (d.router_mode == MOE_ROUTER_XWR) {
         // W_r = t0 + t1 + t2 exactly, three bf16 [E][D] arrays after the scale atoms
         const size_t tb = wr_terms_bytes(d) / 3;
         uint16_t *t[3];
-        for (int i = 0; i < 3; ++i) t[i] = (uint16_t *)(out + atoms_bytes(d) + i * tb);
+        for (int i = 0; i < 3; ++i) t[i] = (uint16_t *)(out + atoms_bytes(d, h->wE) + i * tb);
         if (moe_launch_split3((int64_t)E * D, h->w.w_router, t[0], t[1], t[2], st) != cudaSuccess)
             return MOE_ERR_CUDA;
         for (int i = 0; i < 3; ++i)

@@ -301,8 +301,16 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                     moe_flag(args.status, MOE_ERR_BAD_INDEX);
                     continue;
                 }
-                const int row0 = t.e * args.M + t.mt * C::MROWS;
-                const size_t atom0 = ((size_t)t.e * MT + t.mt) * ((KC + ATOM_BLOCKS - 1) / ATOM_BLOCKS);
+                int we = t.e;  // weight slot of the expert
+                if (args.w_index) {
+                    we = args.w_index[t.e];
+                    if (we < 0 || we >= args.n_wexp) {  // not resident: flag, stay in bounds
+                        moe_flag(args.status, MOE_ERR_BAD_INDEX);
+                        we = 0;
+                    }
+                }
+                const int row0 = we * args.M + t.mt * C::MROWS;
+                const size_t atom0 = ((size_t)we * MT + t.mt) * ((KC + ATOM_BLOCKS - 1) / ATOM_BLOCKS);
                 for (int kc = 0; kc < KC; kc += C::KS, ++it) {
                     const int s = it % C::SA, round = it / C::SA;
                     const int nsub = min(C::KS, KC - kc);
@@ -667,31 +675,51 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
 // 2 * pair + j / 4 (zero past the last block). For the gate/up GEMM a tile's
 // rows 0..63 are gate rows mt*64 .. and rows 64..127 the same up rows; for
 // the down GEMM a tile is 128 consecutive rows. One thread per 4-byte word.
+__device__ __forceinline__ uint32_t atom_word(int64_t e, int mt, int pair, int wi, int M, int K,
+                                              int mrows, const uint8_t *__restrict__ s,
+                                              const uint8_t *__restrict__ s2) {
+    const int KC = K / BK, ksb = K / 32;
+    const int l = (wi / 64) * 8 + (wi % 32) / 4;   // lane
+    const int j = ((wi % 64) / 32) * 4 + wi % 4;   // column
+    const int m = 32 * (j % 4) + l;                // tile row
+    const int kc = ATOM_BLOCKS * pair + j / 4;
+    if (kc >= KC) return 0u;
+    const uint8_t *src;
+    if (s2 && m >= 64) src = s2 + ((e * M + (int64_t)mt * mrows + (m - 64)) * ksb + kc * 4);
+    else src = s + ((e * M + (int64_t)mt * mrows + m) * ksb + kc * 4);
+    return *(const uint32_t *)src;
+}
+
 __global__ void __launch_bounds__(256) moe_prepare_atoms_kernel(int64_t words, int M, int K,
                                                                 int mrows, const uint8_t *__restrict__ s,
                                                                 const uint8_t *__restrict__ s2,
                                                                 uint32_t *__restrict__ out) {
     int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (w >= words) return;
-    const int MT = M / mrows, KC = K / BK, NP = (KC + ATOM_BLOCKS - 1) / ATOM_BLOCKS, ksb = K / 32;
+    const int MT = M / mrows, NP = (K / BK + ATOM_BLOCKS - 1) / ATOM_BLOCKS;
     const int64_t blk = w / 256;
-    const int wi = (int)(w % 256);
-    const int l = (wi / 64) * 8 + (wi % 32) / 4;   // lane
-    const int j = ((wi % 64) / 32) * 4 + wi % 4;   // column
-    const int m = 32 * (j % 4) + l;                // tile row
     const int pair = (int)(blk % NP);
     const int64_t em = blk / NP;  // e * MT + mt
-    const int mt = (int)(em % MT);
-    const int64_t e = em / MT;
-    const int kc = ATOM_BLOCKS * pair + j / 4;
-    if (kc >= KC) {
-        out[w] = 0u;
-        return;
+    out[w] = atom_word(em / MT, (int)(em % MT), pair, (int)(w % 256), M, K, mrows, s, s2);
+}
+
+// The same blocks for the experts just copied into slots miss_slot[0 .. *n_miss)
+// (expert streaming), read from and written for those slots only.
+__global__ void __launch_bounds__(256) moe_prepare_atoms_slots_kernel(
+    int M, int K, int mrows, const uint8_t *__restrict__ s, const uint8_t *__restrict__ s2,
+    uint32_t *__restrict__ out, const int *__restrict__ n_miss, const int32_t *__restrict__ miss_slot) {
+    const int MT = M / mrows, NP = (K / BK + ATOM_BLOCKS - 1) / ATOM_BLOCKS;
+    const int64_t per = (int64_t)MT * NP * 256;  // words per expert
+    const int64_t total = per * (*n_miss);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int m = (int)(i / per);
+        const int64_t w = i - (int64_t)m * per;
+        const int64_t slot = miss_slot[m];
+        const int64_t blk = w / 256;
+        const int pair = (int)(blk % NP), mt = (int)(blk / NP);
+        out[slot * per + w] = atom_word(slot, mt, pair, (int)(w % 256), M, K, mrows, s, s2);
     }
-    const uint8_t *src;
-    if (s2 && m >= 64) src = s2 + ((e * M + (int64_t)mt * mrows + (m - 64)) * ksb + kc * 4);
-    else src = s + ((e * M + (int64_t)mt * mrows + m) * ksb + kc * 4);
-    out[w] = *(const uint32_t *)src;
 }
 
 // ---------------------------------------------------------------------------
@@ -708,6 +736,14 @@ size_t moe_gemm_smem_bytes(int mode, int narrow) {
 size_t moe_prepared_atoms_bytes(int E, int M, int K, int mrows) {
     const int KC = K / BK, NP = (KC + ATOM_BLOCKS - 1) / ATOM_BLOCKS;
     return (size_t)E * (M / mrows) * NP * SF_BYTES;
+}
+
+cudaError_t moe_launch_prepare_atoms_slots(int M, int K, int mrows, const uint8_t *s,
+                                           const uint8_t *s2, uint8_t *out, const int *n_miss,
+                                           const int32_t *miss_slot, int nsm, cudaStream_t st) {
+    moe_prepare_atoms_slots_kernel<<<nsm * 4, 256, 0, st>>>(M, K, mrows, s, s2, (uint32_t *)out,
+                                                            n_miss, miss_slot);
+    return cudaGetLastError();
 }
 
 cudaError_t moe_launch_prepare_atoms(int E, int M, int K, int mrows, const uint8_t *s,

@@ -75,6 +75,8 @@ struct MoeGemmArgs {
     int Dout;                // row stride of the fp32 output accumulator (d_model)
     const int32_t *offsets, *perm, *active, *tt_prefix;
     const float *topk_w;
+    const int32_t *w_index;  // weight slot of expert e (expert streaming), or NULL: e itself
+    int n_wexp;              // experts held by the weight arrays (bound for w_index values)
     const uint8_t *a_atoms;  // weight scale blocks [E][weight tiles][K/256][1 KB]
     const uint8_t *b_tiles;  // activation B tiles [token tile][K/128][2*NTMAX rows][128 B]:
                              // rows [0, nmma) the hi term, [nmma, 2 nmma) the lo term,
@@ -95,6 +97,37 @@ cudaError_t moe_launch_prepare_atoms(int E, int M, int K, int mrows, const uint8
 // at most MOE_GEMM_NT_NARROW selects the narrow-tile variant.
 cudaError_t moe_launch_gemm(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
                             const MoeGemmArgs *args, int max_rows, int grid, cudaStream_t st);
+
+// stream.cu: expert streaming (HBM slot cache in front of host memory)
+struct MoeStreamHdr {
+    int clock;       // calls so far
+    int last_miss;   // misses of the last call (entries of miss_e / miss_s)
+    int pad[2];
+    unsigned long long hits, misses;  // totals over all calls
+};
+struct MoeStreamView {
+    MoeStreamHdr *hdr;
+    int32_t *slot_of;    // [E] slot holding expert e, or -1
+    int32_t *expert_of;  // [S] expert held by slot s, or -1
+    int32_t *stamp;      // [S] clock of the slot's last use (0: never)
+    int32_t *miss_e, *miss_s;  // [S] the last call's missing experts and their slots
+};
+struct MoeStreamCopy {  // gate_q, gate_s, up_q, up_s, down_q, down_s
+    const uint8_t *host[6];
+    uint8_t *slot[6];
+    int64_t bytes[6];  // per expert, multiples of 16
+};
+size_t moe_stream_state_size(int E, int S);
+MoeStreamView moe_stream_view(void *state, int E, int S);
+cudaError_t moe_launch_stream_init(int E, int S, void *state, cudaStream_t st);
+cudaError_t moe_launch_stream_lru(int E, int S, const int32_t *active, void *state, int *status,
+                                  cudaStream_t st);
+cudaError_t moe_launch_stream_copy(int E, int S, void *state, const MoeStreamCopy *c, int nsm,
+                                   cudaStream_t st);
+// grouped_gemm.cu: prepared scale blocks of the slots listed in miss_s[0 .. *n_miss)
+cudaError_t moe_launch_prepare_atoms_slots(int M, int K, int mrows, const uint8_t *s,
+                                           const uint8_t *s2, uint8_t *out, const int *n_miss,
+                                           const int32_t *miss_slot, int nsm, cudaStream_t st);
 
 // dense_gemm.cu: bf16 tcgen05 GEMMs of the router and the shared expert
 #define MOE_DENSE_ROUTER 0  // 3 bf16 terms of W_r, fp32 store out_f32[t][m] (m < M)

@@ -8,9 +8,9 @@ from __future__ import annotations
 import torch
 
 from . import (MOE_OP_DECODE, MOE_OP_FORWARD, MOE_OP_PLAN, MOE_ROUTER_XWR, check, moe_create,
-               moe_decode, moe_desc, moe_destroy, moe_forward, moe_plan, moe_plan_buf,
-               moe_prepare, moe_prepared_bytes, moe_router_logits, moe_status, moe_weights,
-               moe_workspace_bytes)
+               moe_create_streaming, moe_decode, moe_desc, moe_destroy, moe_forward, moe_plan,
+               moe_plan_buf, moe_prepare, moe_prepared_bytes, moe_router_logits, moe_status,
+               moe_stream_state_bytes, moe_stream_stats, moe_weights, moe_workspace_bytes)
 
 WEIGHT_NAMES = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
 
@@ -109,3 +109,45 @@ class Layer:
 
     def status(self, stream=None) -> int:
         return moe_status(self.h, stream)
+
+
+class StreamingLayer(Layer):
+    """A routed layer whose experts stay in pinned host memory; the library
+    keeps an HBM cache of n_slots of them (expert streaming). host_weights:
+    CPU tensors in the library's layouts, pinned (tensor.pin_memory())."""
+
+    def __init__(self, D: int, F: int, E: int, k: int, host_weights: dict, n_slots: int,
+                 router_mode: int = 0, w_router=None, shared=None):
+        self.D, self.F, self.E, self.k = D, F, E, k
+        self.router_mode = router_mode
+        self.host_weights = host_weights
+        self.n_slots = n_slots
+        self.weights = alloc_weights(n_slots, D, F)  # the slot cache
+        self.w_router = w_router
+        self.shared = shared
+        ptr = lambda t: None if t is None else t.data_ptr()
+        sh = shared or {}
+        self.desc = moe_desc(D, F, E, k, router_mode, 1 if shared else 0)
+        self.hdesc = moe_weights(*[host_weights[n].data_ptr() for n in WEIGHT_NAMES], None,
+                                 None, None, None)
+        self.wdesc = moe_weights(*[self.weights[n].data_ptr() for n in WEIGHT_NAMES],
+                                 ptr(w_router), ptr(sh.get("sh_gate")), ptr(sh.get("sh_up")),
+                                 ptr(sh.get("sh_down")))
+        self.state = torch.empty(moe_stream_state_bytes(E, n_slots), dtype=torch.uint8,
+                                 device="cuda")
+        self.h = moe_create_streaming(self.desc, self.hdesc, self.wdesc, n_slots, self.state)
+        self._ws = None
+        self.atoms = None
+
+    def stats(self, stream=None) -> tuple:
+        """(hits, misses, misses of the last call)."""
+        return moe_stream_stats(self.h, stream)
+
+    def cache_state(self) -> dict:
+        """slot_of [E] and expert_of / stamp [S] read back from the device."""
+        import numpy as np
+        raw = self.state.cpu().numpy()
+        words = raw[32:].view(np.int32)
+        E, S = self.E, self.n_slots
+        return {"clock": int(raw[:4].view(np.int32)[0]), "slot_of": words[:E].copy(),
+                "expert_of": words[E:E + S].copy(), "stamp": words[E + S:E + 2 * S].copy()}
