@@ -55,6 +55,9 @@ BENCH_WORKLOADS = {
     "router16k": {"Ts": [16384], "path": "forward", "router": True, "sets": 2,
                   "desc": "K3 routed layer long prefill, T=16384, in-library fp32 router "
                           "(x . W_r) + one bf16 shared expert"},
+    "decode_stream": {"Ts": [1, 4, 16], "path": "forward", "stream_slots": 448,
+                      "desc": "K3 routed layer decode, T=1,4,16, all 896 experts in pinned host "
+                              "memory behind a 448-slot HBM expert cache (expert streaming)"},
 }
 
 
@@ -93,7 +96,7 @@ def oracle_tokens_per_s(workload_name: str, budget_s: float):
     from oracle.run import reference
     oracle.build()
     wl = BENCH_WORKLOADS[workload_name]
-    base = synth.WORKLOADS["decode1"] if workload_name == "decode" else synth.WORKLOADS[workload_name]
+    base = synth.WORKLOADS["decode1"] if workload_name.startswith("decode") else synth.WORKLOADS[workload_name]
     done, t0 = 0, time.perf_counter()
     it = 0
     while True:
@@ -244,7 +247,7 @@ def run_ours(args):
     if args.tokens:
         wl["Ts"] = [args.tokens]
     path = args.path or wl["path"]
-    base = synth.WORKLOADS["decode1"] if args.workload == "decode" else synth.WORKLOADS[args.workload]
+    base = synth.WORKLOADS["decode1"] if args.workload.startswith("decode") else synth.WORKLOADS[args.workload]
 
     # weights: the full layer, generated in HBM by the device half of the generator
     weights = alloc_weights(n_exp, D_MODEL, D_FF)
@@ -252,6 +255,7 @@ def run_ours(args):
                          {k: v.data_ptr() for k, v in weights.items()},
                          torch.cuda.current_stream().cuda_stream)
     use_router = bool(wl.get("router"))
+    n_slots = wl.get("stream_slots")
     n_sets = wl.get("sets", N_SETS)
     if use_router:
         import dataclasses
@@ -259,6 +263,15 @@ def run_ours(args):
         shared = {k: torch.from_numpy(v.view(np.int16)).to(dev)
                   for k, v in synth.make_shared(base).items()}
         layer = Layer(D_MODEL, D_FF, n_exp, TOP_K, weights, MOE_ROUTER_XWR, w_router, shared)
+    elif n_slots:
+        # the store: all experts in pinned host memory; the layer caches n_slots in HBM
+        from mxfp4_routed_expert_03_gb300.layer import StreamingLayer
+        host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in weights.items()}
+        for k, v in weights.items():
+            host[k].copy_(v)
+        del weights
+        torch.cuda.empty_cache()
+        layer = StreamingLayer(D_MODEL, D_FF, n_exp, TOP_K, host, min(n_slots, n_exp))
     else:
         layer = Layer(D_MODEL, D_FF, n_exp, TOP_K, weights)
     def path_of(T):
@@ -293,7 +306,8 @@ def run_ours(args):
         for op in (0, 1, 2):
             layer.workspace(b["T"], op)
     # the kernel whose launches are timed in each batch: the path's main one
-    main_kind = {"decode": MOE_PROF_DECODE_GATEUP, "forward": MOE_PROF_FORWARD_GEMM1}
+    main_kind = {"decode": MOE_PROF_DECODE_GATEUP,
+                 "forward": moe.MOE_PROF_STREAM_COPY if n_slots else MOE_PROF_FORWARD_GEMM1}
 
     def step(i, events=None, e2e=False, prof_kind=None):
         for bi, b in enumerate(batches):
@@ -338,6 +352,7 @@ def run_ours(args):
             a.record()
             b.record()
     torch.cuda.synchronize()
+    stats0 = layer.stats() if n_slots else None
     t_start = time.time()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
@@ -347,6 +362,7 @@ def run_ours(args):
     barrier()
     t_end = time.time()
     check(moe_profile_kernel(layer.h, MOE_PROF_NONE), "profile")
+    stats1 = layer.stats() if n_slots else None
     elapsed_ms = e0.elapsed_time(e1)
     kern_ms = [[a.elapsed_time(b) for (a, b) in row] for row in kev]
     check(layer.status(), "device status")
@@ -377,6 +393,8 @@ def run_ours(args):
         kinds += [("decode_gateup", moe.MOE_PROF_DECODE_GATEUP), ("decode_down", moe.MOE_PROF_DECODE_DOWN)]
     if any(b["path"] == "forward" for b in batches):
         kinds += [("gemm1_gateup", moe.MOE_PROF_FORWARD_GEMM1), ("gemm2_down", moe.MOE_PROF_FORWARD_GEMM2)]
+    if n_slots:
+        kinds += [("stream_copy", moe.MOE_PROF_STREAM_COPY)]
     if use_router:
         kinds += [("router", moe.MOE_PROF_ROUTER), ("shared_gateup", moe.MOE_PROF_SHARED_GATEUP),
                   ("shared_down", moe.MOE_PROF_SHARED_DOWN)]
@@ -448,6 +466,38 @@ def run_ours(args):
                 "flop_per_launch": f_avg, "hbm_GBs": gbs, "frac_of_hbm": gbs / hbm_peak}
     roof["frac_of_fp4_peak"] = tfs / (6.0 * peaks.get("bf16_tflops", 1900.0))
     roof["traffic"] = kernel_traffic(kname, src, tkey)
+    stream_info = None
+    if n_slots:
+        # the copy of the missing experts is bound by the host-to-device link:
+        # miss bytes in the timed region over the summed copy-kernel time, against
+        # the link's copy bandwidth measured here (pinned host -> device, 2 GiB)
+        hits = stats1[0] - stats0[0]
+        misses = stats1[1] - stats0[1]
+        copy_ms = float(np.sum(np.array(kern_ms)))
+        link = torch.empty(1 << 31, dtype=torch.uint8, pin_memory=True)
+        dst = torch.empty(1 << 31, dtype=torch.uint8, device=dev)
+        best = None
+        for _ in range(3):
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record()
+            dst.copy_(link, non_blocking=True)
+            a1.record()
+            torch.cuda.synchronize()
+            t = a0.elapsed_time(a1)
+            best = t if best is None else min(best, t)
+        h2d = (1 << 31) / (best * 1e-3) / 1e9
+        del link, dst
+        gbs_c = misses * EXPERT_BYTES / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else 0.0
+        roof = {"bound": "host-to-device link", "kernel": "moe_stream_copy_kernel",
+                "achieved": gbs_c, "peak": h2d, "unit": "GB/s",
+                "frac": gbs_c / h2d if h2d else None,
+                "peak_source": "measured in this run: cudaMemcpyAsync of 2 GiB pinned host memory "
+                               "to the device",
+                "bytes_per_launch": misses * EXPERT_BYTES / max(1, args.steps * len(batches)),
+                "traffic": None}
+        stream_info = {"slots": layer.n_slots, "hit_rate": hits / max(1, hits + misses),
+                       "misses_per_step": misses / args.steps,
+                       "copy_ms_per_step": copy_ms / args.steps}
 
     # plan: one fused kernel for T <= 64, else top-k, count, scan, scatter;
     # decode: gate/up, down, combine; forward: quant, schedule, gather, two GEMMs,
@@ -456,6 +506,8 @@ def run_ours(args):
     for b in batches:
         launches += 1 if b["T"] <= 64 else 4
         launches += 3 if b["path"] == "decode" else (4 if b["T"] <= 16 else 6)
+        if n_slots:
+            launches += 4   # cache: replacement, copy of the misses, two scale re-layouts
         if use_router:
             launches += 1 + 2   # router GEMM; shared gate/up and down GEMMs
     line = {
@@ -470,6 +522,7 @@ def run_ours(args):
                            ", ".join(f"moe_{b['path']} (T={b['T']})" for b in batches),
                    "tokens_per_step": tokens_step, "active_experts_last_step": act,
                    "kernel_ms_per_call": breakdown,
+                   **({"expert_cache": stream_info} if stream_info else {}),
                    "l2": "inputs larger than L2 (>=280 MB of expert weights per batch, "
                          "8 rotating logit sets)", "parallelism": f"replicas x{world}"},
         "roofline": roof,

@@ -89,7 +89,8 @@ enum moe_prof_kernel {
     MOE_PROF_FORWARD_GEMM2 = 4,   /* moe_forward: grouped down GEMM + weighted scatter */
     MOE_PROF_ROUTER = 5,          /* moe_plan / moe_router_logits: x . W_r GEMM */
     MOE_PROF_SHARED_GATEUP = 6,   /* shared expert: gate/up GEMM + SwiGLU */
-    MOE_PROF_SHARED_DOWN = 7      /* shared expert: down GEMM */
+    MOE_PROF_SHARED_DOWN = 7,     /* shared expert: down GEMM */
+    MOE_PROF_STREAM_COPY = 8      /* expert streaming: copy of the missing experts from host memory */
 };
 
 /* Layer shape. Supported envelope: d_model a multiple of 256, d_ff of 128,

@@ -46,6 +46,7 @@ MOE_PROF_FORWARD_GEMM2 = 4
 MOE_PROF_ROUTER = 5
 MOE_PROF_SHARED_GATEUP = 6
 MOE_PROF_SHARED_DOWN = 7
+MOE_PROF_STREAM_COPY = 8
 
 
 class moe_desc(ctypes.Structure):

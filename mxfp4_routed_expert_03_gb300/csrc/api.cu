@@ -298,7 +298,11 @@ static cudaError_t stream_fill(moe_handle *h, const moe_plan_buf *plan, cudaStre
         c.slot[i] = const_cast<uint8_t *>(ss[i]);
         c.bytes[i] = by[i];
     }
-    if (err == cudaSuccess) err = moe_launch_stream_copy(E, S, h->sstate, &c, h->num_sms, st);
+    if (err == cudaSuccess) {
+        h->prof.before(MOE_PROF_STREAM_COPY, st);
+        err = moe_launch_stream_copy(E, S, h->sstate, &c, h->num_sms, st);
+        h->prof.after(MOE_PROF_STREAM_COPY, st);
+    }
     const MoeStreamView v = moe_stream_view(h->sstate, E, S);
     uint8_t *atoms = const_cast<uint8_t *>(h->atoms);
     if (err == cudaSuccess)
@@ -643,7 +647,7 @@ MOE_API int moe_prepare(moe_handle *h, void *buf, size_t bytes, void *stream) {
 }
 
 MOE_API int moe_profile_kernel(moe_handle *h, int32_t which, void *ev_start, void *ev_stop) {
-    if (!h || which < MOE_PROF_NONE || which > MOE_PROF_SHARED_DOWN) return MOE_ERR_INVALID_ARG;
+    if (!h || which < MOE_PROF_NONE || which > MOE_PROF_STREAM_COPY) return MOE_ERR_INVALID_ARG;
     if (which != MOE_PROF_NONE && (!ev_start || !ev_stop)) return MOE_ERR_INVALID_ARG;
     h->prof.which = which;
     h->prof.start = (cudaEvent_t)ev_start;
