@@ -85,6 +85,24 @@ def parse_args():
 
 
 # ---------------------------------------------------------------------------
+# Replicas: every rank runs the same workload on its own GPU; the job's time is
+# the slowest rank's, and its throughput counts the tokens of all ranks.
+# ---------------------------------------------------------------------------
+def max_over_ranks(times_ms: list, dist=None, device="cpu") -> list:
+    """Element-wise maximum of per-rank times (all ranks get the result)."""
+    import torch
+    t = torch.tensor(times_ms, dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tokens_per_s(world: int, tokens_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: tokens of all ranks over the (slowest rank's) time."""
+    return world * tokens_per_step * steps / (ms * 1e-3)
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle leg (the reference arm and the cpu_baseline object)
 # ---------------------------------------------------------------------------
 def oracle_tokens_per_s(workload_name: str, budget_s: float):
@@ -381,10 +399,7 @@ def run_ours(args):
     sampler.stop()
     clocks = sampler.summary(t_start, t_end)
 
-    times = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    elapsed_ms, e2e_ms = times.tolist()
+    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], dist, dev)
 
     # per-kernel breakdown (separate untimed pass, one kernel bracketed at a time)
     breakdown = {}
@@ -417,8 +432,8 @@ def run_ours(args):
                                          for i in range(n_bd) for bi in used]))
     check(moe_profile_kernel(layer.h, MOE_PROF_NONE), "profile")
     tokens_step = sum(wl["Ts"])
-    value = world * tokens_step * args.steps / (elapsed_ms * 1e-3)
-    e2e_value = world * tokens_step * args.steps / (e2e_ms * 1e-3)
+    value = job_tokens_per_s(world, tokens_step, args.steps, elapsed_ms)
+    e2e_value = job_tokens_per_s(world, tokens_step, args.steps, e2e_ms)
 
     # roofline of the dominant kernel: the timed kernel (per batch, its path's
     # main kernel) with the largest share of the timed region; its bound is

@@ -93,3 +93,17 @@ def test_crossover_decode_and_forward_agree(k3_layer, T):
     ef = assert_close(got_f, ref)
     ed = assert_close(got_d, ref)
     print("crossover T=%d forward" % T, ef, "decode", ed)
+
+
+def test_zero_tokens_is_a_noop(tiny_weights):
+    from mxfp4_routed_expert_03_gb300.layer import Layer, Plan
+    w = synth.WORKLOADS["tiny"]
+    layer = Layer(w.D, w.F, w.E, w.k, tiny_weights)
+    plan = Plan(0, w.E, w.k)
+    x = torch.empty((1, w.D), dtype=torch.int16, device="cuda")
+    out = torch.full((1, w.D), 7, dtype=torch.int16, device="cuda")
+    assert layer.forward(0, x, plan, out) == 0
+    assert layer.decode(0, x, plan, out) == 0
+    assert int(out[0, 0].item()) == 7   # nothing written
+    assert layer.status() == 0
+    layer.close()
