@@ -33,8 +33,11 @@
 //
 // Two tile widths (template NT): the wide variant (112 token rows) for
 // prefill, with 2-stage rings; the narrow variant (16 rows, chosen when no
-// expert has more rows) with 4-stage rings and two MMA issuers. A pipeline
-// stage carries two 128-wide K blocks; data layouts stay per K block.
+// expert has more rows) with 4-stage rings, two MMA issuers and no cluster
+// (its CTAs load their own small activation tiles and release a stage with
+// one local commit). A pipeline stage carries two 128-wide K blocks; data
+// layouts stay per K block. With expert streaming the weight producer
+// addresses the expert's slot (args.w_index).
 //
 // One persistent CTA per SM, 7 warps (8 for the narrow variant):
 //   warp 0      weight producer (one thread): weight tile(s) by TMA (packed
@@ -46,12 +49,13 @@
 //   warp 2      MMA issuer (one thread): tcgen05.cp scales, tcgen05.mma
 //   warps 3-6   epilogue, one 32-lane TMEM quadrant each
 //   warp 7      (narrow) second MMA issuer
-// Each operand ring has its own "full" barrier per stage (one barrier serves
-// both when the rings are equally deep; the cluster peer's multicast bytes
-// complete on the activation one) and its own release barrier; the
+// One "full" barrier per stage serves both operand rings when they are
+// equally deep (the cluster peer's multicast bytes complete on it too);
+// releases are one local barrier per stage without a cluster, or a local
+// weight release plus a cluster-wide activation release with one. The
 // accumulator is double-buffered in TMEM so the epilogue of tile i overlaps
 // the MMAs of tile i+1. Every wait is bounded: on expiry the CTA records
-// MOE_ERR_DEVICE_TIMEOUT and winds down.
+// MOE_ERR_DEVICE_TIMEOUT, drains its MMAs and winds down.
 #include "common.cuh"
 #include "kernels.h"
 #include "mx8.cuh"
@@ -188,9 +192,6 @@ __device__ __forceinline__ bool tile_at(int ct, int n_active, int MTG, int rank,
     return t.n > 0 && t.n <= NT;
 }
 
-// Position of (row m, 32-wide K block c) inside a 128-row x 4-block scale atom.
-__device__ __forceinline__ int atom_off(int m, int c) { return (m & 31) * 16 + (m >> 5) * 4 + c; }
-
 // Position of (B row n < 256, 32-wide K block c) inside the 1 KB activation
 // scale block of one chunk: 32 lanes x 8 columns, lane n % 32 column n / 32,
 // stored as the K-major core matrices (8 rows x 16 bytes) that
@@ -198,12 +199,6 @@ __device__ __forceinline__ int atom_off(int m, int c) { return (m & 31) * 16 + (
 __device__ __forceinline__ int bsf_off(int n, int c) {
     const int i = n & 31, j = n >> 5;
     return (i >> 3) * 256 + (j >> 2) * 128 + (i & 7) * 16 + (j & 3) * 4 + c;
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int off = 16; off; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
-    return v;
 }
 
 // The four epilogue warps (128 threads) meet at named barrier 1.
