@@ -106,3 +106,46 @@ def test_k3_shaped_streaming_sampled_tokens():
         np.testing.assert_array_equal(st["expert_of"], model.expert_of)
         print("k3 streaming call %d" % i, e, layer.stats())
     layer.close()
+
+
+def test_streaming_wide_tiles_and_full_cache():
+    """T = 100 takes the wide (112-row, clustered) GEMM variant through the
+    slot index; 32 slots for 32 experts, so every expert is resident after
+    the first call and the second call is all hits."""
+    from mxfp4_routed_expert_03_gb300.layer import StreamingLayer
+    w = synth.WORKLOADS["tiny"]
+    layer = StreamingLayer(w.D, w.F, w.E, w.k, _host_copy(host_layer_weights(w)), w.E)
+    for i, T in enumerate([100, 130]):
+        x, lg = synth.make_x(w, 90 + i, T=T), synth.make_logits(w, 90 + i, T=T)
+        got, active = _run(layer, w, x, lg)
+        assert layer.status() == 0
+        tok = np.arange(0, T, 7)
+        e = assert_close(got[tok], reference(w, x, lg, tokens=tok)["out"])
+        print("wide streaming T=%d" % T, e, layer.stats())
+    hits, misses, last = layer.stats()
+    assert misses <= w.E   # with a slot per expert each expert is copied at most once
+    layer.close()
+
+
+def test_streaming_with_router_and_shared_expert():
+    from mxfp4_routed_expert_03_gb300 import MOE_ROUTER_XWR, check
+    from mxfp4_routed_expert_03_gb300.layer import Plan, StreamingLayer
+    from harness import router_and_shared
+    w = synth.Workload("tiny_xwr", T=5, D=256, F=128, E=32, k=4, seed=0, router="xwr",
+                       shared=True)
+    wr, sh = router_and_shared(w)
+    layer = StreamingLayer(w.D, w.F, w.E, w.k, _host_copy(host_layer_weights(w)), 20,
+                           MOE_ROUTER_XWR, wr, sh)
+    for T in (5, 1):   # inputs with no near-tie in the router logits (as in the router tests)
+        x_np = synth.make_x(w, 7, T=T)
+        plan = Plan(T, w.E, w.k)
+        x = to_dev_bf16(x_np)
+        check(layer.plan(T, None, x, plan), "plan")
+        out = torch.empty((T, w.D), dtype=torch.int16, device="cuda")
+        check(layer.forward(T, x, plan, out), "forward")
+        assert layer.status() == 0
+        ref = reference(w, x_np, None)
+        np.testing.assert_array_equal(plan.topk_idx.cpu().numpy(), ref["idx"])
+        e = assert_close(bf16_dev_to_f64(out), ref["out"])
+        print("streaming router+shared T=%d" % T, e)
+    layer.close()
