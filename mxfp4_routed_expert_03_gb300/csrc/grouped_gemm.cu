@@ -33,7 +33,7 @@
 //
 // Two tile widths (template NT): the wide variant (112 token rows) for
 // prefill, with 2-stage rings; the narrow variant (16 rows, chosen when no
-// expert has more rows) with 4-stage rings, two MMA issuers and no cluster
+// expert has more rows) with 5-stage rings, two MMA issuers and no cluster
 // (its CTAs load their own small activation tiles and release a stage with
 // one local commit). A pipeline stage carries two 128-wide K blocks; data
 // layouts stay per K block. With expert streaming the weight producer
@@ -118,7 +118,7 @@ struct Cfg {
     // stage (measured), so narrow CTAs run alone.
     static constexpr int CL = NARROW ? 1 : MOE_GEMM_CLUSTER;
     static constexpr uint16_t CL_MASK = (uint16_t)((1u << CL) - 1);
-    static constexpr int SA = NARROW ? 4 : 2;  // weight ring stages (KS blocks each)
+    static constexpr int SA = NARROW ? 5 : 2;  // weight ring stages (KS blocks each)
     static constexpr int SB = SA;              // activation ring stages
     static constexpr bool MERGED = SA == SB;   // one full barrier per stage for both operands
     static constexpr int A_STAGE = KS * A_BYTES + SCALE_REP_A * SF_BYTES;  // tiles, then scales
@@ -135,12 +135,22 @@ struct Cfg {
     // (measured faster for the wide variant than one shared release).
     static constexpr bool SHARED_EMPTY = MERGED && CL == 1;
     static constexpr int N_EMPTY = SHARED_EMPTY ? SA : SA + SB;
+    // two issuers order their full waits by the one release of each stage
+    static_assert(NSPLIT == 1 || SHARED_EMPTY, "split issue needs one release barrier per stage");
     // full(s), empty(s); tfull, tempty x2; one drain barrier per issuer
     static constexpr int N_BARS = N_FULL + N_EMPTY + 4 + NSPLIT;
+    // Tile lookup. Wide: shared-memory copies of the token-tile prefix, the
+    // active experts and their row segments (NTAB entries). Narrow: every
+    // expert has one token tile, so tile ct is active expert ct / MTG; the
+    // CTA's own tiles are decoded once into a list of TLIST entries (direct
+    // loads from the plan past that), which frees the room for a 5th stage.
+    static constexpr int NTAB = NARROW ? 0 : MOE_MAX_EXPERTS;
+    static constexpr int TLIST = NARROW ? 256 : 0;
     static constexpr int PREFIX_BASE = (BAR_BASE + N_BARS * 8 + 16 + 15) / 16 * 16;  // int [active + 1]
-    static constexpr int EXPERT_BASE = (PREFIX_BASE + (MOE_MAX_EXPERTS + 1) * 4 + 15) / 16 * 16;
-    static constexpr int SEG_BASE = (EXPERT_BASE + MOE_MAX_EXPERTS * 4 + 15) / 16 * 16;  // int2
-    static constexpr int EPI_BASE = (SEG_BASE + MOE_MAX_EXPERTS * 8 + 15) / 16 * 16;
+    static constexpr int EXPERT_BASE = (PREFIX_BASE + (NTAB ? (NTAB + 1) * 4 : 0) + 15) / 16 * 16;
+    static constexpr int SEG_BASE = (EXPERT_BASE + NTAB * 4 + 15) / 16 * 16;  // int2
+    static constexpr int LIST_BASE = (SEG_BASE + NTAB * 8 + 15) / 16 * 16;   // int2 [TLIST]
+    static constexpr int EPI_BASE = (LIST_BASE + TLIST * 8 + 15) / 16 * 16;
     // GEMM1: u values of 16 columns x 64 rows; GEMM2: 4 warps x 16 columns x 32 rows
     static constexpr int EPI_BYTES = (MODE == MOE_GEMM_GATEUP) ? 16 * 64 * 4 : 4 * 16 * 32 * 4;
     static constexpr int SMEM = 1024 + EPI_BASE + EPI_BYTES;
@@ -192,6 +202,39 @@ __device__ __forceinline__ bool tile_at(int ct, int n_active, int MTG, int rank,
     return t.n > 0 && t.n <= NT;
 }
 
+// Narrow tiles: tile ct of this CTA (the i-th it visits) from the CTA's tile
+// list (x = expert | rows << 22, y = first slot; x < 0 when invalid) or, past
+// the list, straight from the plan. Active expert a = ct / MTG owns tiles
+// a * MTG .. a * MTG + MTG - 1, one per weight tile group.
+template <int NT, int CL, int TLIST>
+__device__ __forceinline__ bool tile_at_list(int ct, int cluster_id, int n_clusters, int MTG,
+                                             int rank, const int2 *s_list, const MoeGemmArgs &args,
+                                             Tile &t) {
+    const int a = ct / MTG, mg = ct - a * MTG;
+    const int i = (ct - cluster_id) / n_clusters;
+    int e, sb, cnt;
+    if (i < TLIST) {
+        const int2 v = s_list[i];
+        if (v.x < 0) return false;
+        e = v.x & 0x3FFFFF;
+        cnt = v.x >> 22;
+        sb = v.y;
+    } else {
+        e = args.active[1 + a];
+        if (e < 0 || e >= args.E) return false;
+        sb = args.offsets[e];
+        cnt = args.offsets[e + 1] - sb;
+        if (sb < 0 || sb + cnt > args.n_rows) return false;
+    }
+    t.e = e;
+    t.mt = mg * CL + rank;
+    t.s0 = sb;
+    t.n = cnt;
+    t.nmma = (cnt + 15) & ~15;
+    t.tt = a;
+    return cnt > 0 && cnt <= NT;
+}
+
 // Position of (B row n < 256, 32-wide K block c) inside the 1 KB activation
 // scale block of one chunk: 32 lanes x 8 columns, lane n % 32 column n / 32,
 // stored as the K-major core matrices (8 rows x 16 bytes) that
@@ -226,13 +269,32 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
     int *s_prefix = (int *)(smem + C::PREFIX_BASE);
     int *s_expert = (int *)(smem + C::EXPERT_BASE);
     int2 *s_seg = (int2 *)(smem + C::SEG_BASE);
+    int2 *s_list = (int2 *)(smem + C::LIST_BASE);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = args.E;
     int n_active = args.active[0];
     if (n_active < 0 || n_active > E) n_active = 0;
-    for (int i = tid; i <= n_active; i += C::THREADS) s_prefix[i] = args.tt_prefix[i];
-    for (int a = tid; a < n_active; a += C::THREADS) {
+    if (C::NARROW) {  // this CTA's tiles: ct = blockIdx.x + i * gridDim.x (no cluster)
+        const long long n_tiles = (long long)n_active * args.MT;
+        for (int i = tid; i < C::TLIST; i += C::THREADS) {
+            const long long ct = (long long)blockIdx.x + (long long)i * gridDim.x;
+            int2 v = make_int2(-1, 0);
+            if (ct < n_tiles) {
+                const int a = (int)(ct / args.MT);
+                const int e = args.active[1 + a];
+                if (e >= 0 && e < E) {
+                    const int sb = args.offsets[e], cnt = args.offsets[e + 1] - sb;
+                    if (sb >= 0 && cnt > 0 && cnt <= NT && sb + cnt <= args.n_rows)
+                        v = make_int2(e | (cnt << 22), sb);
+                }
+                if (v.x < 0) moe_flag(args.status, MOE_ERR_BAD_INDEX);
+            }
+            s_list[i] = v;
+        }
+    }
+    for (int i = tid; C::NTAB && i <= n_active; i += C::THREADS) s_prefix[i] = args.tt_prefix[i];
+    for (int a = tid; C::NTAB && a < n_active; a += C::THREADS) {
         const int e = args.active[1 + a];
         int sb = 0, cnt = 0;
         if (e >= 0 && e < E) {
@@ -275,7 +337,15 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
     const int MT = args.MT, KC = args.KC, MTG = MT / CL;
     const int rank = CL > 1 ? (int)tc::cluster_ctarank() : 0;
     const int cluster_id = blockIdx.x / CL, n_clusters = gridDim.x / CL;
-    const int total_tiles = n_active > 0 ? s_prefix[n_active] * MTG : 0;
+    const int total_tiles =
+        n_active <= 0 ? 0 : (C::NARROW ? n_active * MTG : s_prefix[n_active] * MTG);
+    auto get_tile = [&](int ct, int &cur, Tile &t) -> bool {
+        if constexpr (C::NARROW)
+            return tile_at_list<NT, CL, C::TLIST>(ct, cluster_id, n_clusters, MTG, rank, s_list,
+                                                  args, t);
+        else
+            return tile_at<NT, CL>(ct, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t);
+    };
     const long long LIMIT = args.timeout_cycles;
     volatile int *abort_p = abort_flag;
     auto fail = [&](void) {
@@ -292,7 +362,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
             int cur = 0;
             for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
                 Tile t;
-                if (!tile_at<NT, C::CL>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) {
+                if (!get_tile(tile, cur, t)) {
                     moe_flag(args.status, MOE_ERR_BAD_INDEX);
                     continue;
                 }
@@ -340,7 +410,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
             int cur = 0;
             for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
                 Tile t;
-                if (!tile_at<NT, C::CL>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) continue;
+                if (!get_tile(tile, cur, t)) continue;
                 const uint32_t tile_bytes = (uint32_t)(2 * t.nmma * BK);
                 const size_t blk0 = (size_t)t.tt * KC;
                 for (int kc = 0; kc < KC; kc += C::KS, ++it) {
@@ -392,7 +462,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
             int cur = 0;
             for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
                 Tile t;
-                if (!tile_at<NT, C::CL>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t)) continue;
+                if (!get_tile(tile, cur, t)) continue;
                 const int buf = lt & 1, use = lt >> 1;
                 ++lt;
                 if (use > 0 && !tc::mbar_wait(&tempty[buf], (use - 1) & 1, LIMIT, abort_p)) {
@@ -412,6 +482,19 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                     const int sa = it % C::SA, ra = it / C::SA;
                     const int sb = it % C::SB, rb = it / C::SB;
                     const int nsub = min(C::KS, KC - kc);
+                    // With two issuers the slot's previous fill may have been the
+                    // other issuer's, still in flight: a parity wait on full[sa]
+                    // could then match the phase before it. The slot's release
+                    // of round ra - 1 comes after that fill landed and before the
+                    // producer refills it, so once it is seen the full wait can
+                    // only mean round ra (and it costs nothing: the fill of round
+                    // ra waits for that release anyway).
+                    if (C::NSPLIT > 1 && ra > 0 &&
+                        !tc::mbar_wait(&emptyA[sa], (ra - 1) & 1, LIMIT, abort_p)) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
                     if (!tc::mbar_wait(&fullA[sa], ra & 1, LIMIT, abort_p) ||
                         (!C::MERGED && !tc::mbar_wait(&fullB[sb], rb & 1, LIMIT, abort_p))) {
                         fail();
@@ -478,7 +561,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
         int lt = 0, cur = 0;
         for (int tile = cluster_id; tile < total_tiles; tile += n_clusters) {
             Tile t;
-            if (!tile_at<NT, C::CL>(tile, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t))
+            if (!get_tile(tile, cur, t))
                 continue;
             const int buf = lt & 1, use = lt >> 1;
             ++lt;
