@@ -4,7 +4,8 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg may import this package. It loads ``liboracle.so`` built from
 ``moe_oracle.c`` (plain C, fp64, OpenMP across rows) and shares no code with
 the CUDA library. See ``moe_oracle.c`` for what each function computes and the
-passage it follows.
+passage it follows. ``oracle.store`` (``store_oracle.c``) is the oracle of the
+compressed expert store.
 
 Every function here is pinned by ``tests/test_oracle_*.py``; none is
 "parity unpinned".
@@ -24,7 +25,10 @@ _lib = None
 
 
 def build(force: bool = False) -> None:
-    """Compile liboracle.so with gcc (building the checker is not using it)."""
+    """Compile liboracle.so and libstore_oracle.so with gcc (building the
+    checker is not using it)."""
+    from . import store
+    store.build(force)
     if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
         return
     subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",

@@ -21,7 +21,7 @@ def store_for(w: synth.Workload, experts) -> dict:
           "up_q": np.empty((S, F, D // 2), np.uint8), "up_s": np.empty((S, F, D // 32), np.uint8),
           "down_q": np.empty((S, D, F // 2), np.uint8), "down_s": np.empty((S, D, F // 32), np.uint8)}
     for i, e in enumerate(experts):
-        ew = synth.expert_weights(w.seed, int(e), D, F)
+        ew = synth.expert_weights(w.seed, int(e), D, F, dist=w.codes)
         for nm, a in ew.items():
             st[nm][i] = a
     return st

@@ -31,6 +31,9 @@ X, LOGITS, WR, ZIPF, SH_GATE, SH_UP, SH_DOWN = 7, 8, 9, 10, 11, 12, 13
 
 # E8M0 scale bytes uniform over 2^-4 .. 2^0  ->  {123, ..., 127}
 SCALE_LO, SCALE_N = 123, 5
+# E2M1 code distributions: uniform over the 16 codes, or "peaked" (shaped like
+# block-scaled normal weights, half of the zeros negative; see philox.h).
+CODES_UNIFORM, CODES_PEAKED = 0, 1
 
 
 def _newer(target, sources):
@@ -69,6 +72,8 @@ def _host_lib():
         L.synth_philox.argtypes = [p, p, p]
         L.synth_mx_codes.argtypes = [u64, u32, u32, i64, i64, p]
         L.synth_mx_codes.restype = i32
+        L.synth_mx_codes_dist.argtypes = [u64, u32, u32, i64, i64, i32, p]
+        L.synth_mx_codes_dist.restype = i32
         L.synth_mx_scales.argtypes = [u64, u32, u32, i64, i64, i32, i32, p]
         L.synth_mx_scales.restype = i32
         L.synth_normal_f32.argtypes = [u64, u32, i64, i64, ctypes.c_double, ctypes.c_double, p]
@@ -88,6 +93,8 @@ def _dev_lib():
                                  ctypes.c_int, ctypes.c_void_p)
         L.synth_dev_mx_codes.argtypes = [u64, u32, u32, i64, i64, i64, p, p]
         L.synth_dev_mx_codes.restype = i32
+        L.synth_dev_mx_codes_dist.argtypes = [u64, u32, u32, i64, i64, i64, i32, p, p]
+        L.synth_dev_mx_codes_dist.restype = i32
         L.synth_dev_mx_scales.argtypes = [u64, u32, u32, i64, i64, i64, i32, i32, p, p]
         L.synth_dev_mx_scales.restype = i32
         _dev = L
@@ -108,11 +115,12 @@ def philox(ctr, key):
     return [int(v) for v in o]
 
 
-def mx_codes(seed: int, tensor: int, expert: int, rows: int, K: int) -> np.ndarray:
+def mx_codes(seed: int, tensor: int, expert: int, rows: int, K: int,
+             dist: int = CODES_UNIFORM) -> np.ndarray:
     """Packed E2M1 codes of one expert matrix: uint8 [rows, K/2]."""
     out = np.empty((rows, K // 2), dtype=np.uint8)
-    if _host_lib().synth_mx_codes(seed, tensor, expert, rows, K, _ptr(out)) != 0:
-        raise ValueError("K must be a multiple of 32")
+    if _host_lib().synth_mx_codes_dist(seed, tensor, expert, rows, K, dist, _ptr(out)) != 0:
+        raise ValueError("K must be a multiple of 32 and dist 0 or 1")
     return out
 
 
@@ -125,12 +133,13 @@ def mx_scales(seed: int, tensor: int, expert: int, rows: int, K: int,
     return out
 
 
-def expert_weights(seed: int, e: int, D: int, F: int, lo: int = SCALE_LO, n: int = SCALE_N):
+def expert_weights(seed: int, e: int, D: int, F: int, lo: int = SCALE_LO, n: int = SCALE_N,
+                   dist: int = CODES_UNIFORM):
     """All six byte arrays of expert e (gate/up: [F, D]; down: [D, F])."""
     return {
-        "gate_q": mx_codes(seed, GATE_Q, e, F, D), "gate_s": mx_scales(seed, GATE_S, e, F, D, lo, n),
-        "up_q": mx_codes(seed, UP_Q, e, F, D), "up_s": mx_scales(seed, UP_S, e, F, D, lo, n),
-        "down_q": mx_codes(seed, DOWN_Q, e, D, F), "down_s": mx_scales(seed, DOWN_S, e, D, F, lo, n),
+        "gate_q": mx_codes(seed, GATE_Q, e, F, D, dist), "gate_s": mx_scales(seed, GATE_S, e, F, D, lo, n),
+        "up_q": mx_codes(seed, UP_Q, e, F, D, dist), "up_s": mx_scales(seed, UP_S, e, F, D, lo, n),
+        "down_q": mx_codes(seed, DOWN_Q, e, D, F, dist), "down_s": mx_scales(seed, DOWN_S, e, D, F, lo, n),
     }
 
 
@@ -157,7 +166,7 @@ def zipf_bias(seed: int, E: int, s: float):
 
 
 def dev_fill_layer(seed: int, E: int, D: int, F: int, bufs: dict, stream: int = 0,
-                   lo: int = SCALE_LO, n: int = SCALE_N) -> None:
+                   lo: int = SCALE_LO, n: int = SCALE_N, dist: int = CODES_UNIFORM) -> None:
     """Fill a whole layer's weights on the GPU.
 
     ``bufs`` maps gate_q/gate_s/up_q/up_s/down_q/down_s to device pointers of
@@ -166,7 +175,7 @@ def dev_fill_layer(seed: int, E: int, D: int, F: int, bufs: dict, stream: int = 
     L = _dev_lib()
     plan = [("gate_q", GATE_Q, F, D), ("up_q", UP_Q, F, D), ("down_q", DOWN_Q, D, F)]
     for name, tid, rows, K in plan:
-        if L.synth_dev_mx_codes(seed, tid, 0, E, rows, K, bufs[name], stream) != 0:
+        if L.synth_dev_mx_codes_dist(seed, tid, 0, E, rows, K, dist, bufs[name], stream) != 0:
             raise RuntimeError("synth_dev_mx_codes failed for " + name)
     plan = [("gate_s", GATE_S, F, D), ("up_s", UP_S, F, D), ("down_s", DOWN_S, D, F)]
     for name, tid, rows, K in plan:
@@ -190,6 +199,7 @@ class Workload:
     router: str = "logits"       # "logits" (fp32 input) or "xwr" (in-library x . W_r)
     zipf_s: float = 0.0          # > 0: Zipf popularity bias on the logits
     shared: bool = False         # one bf16 shared expert added to the combine
+    codes: int = CODES_UNIFORM   # E2M1 code distribution of the expert weights
     extra: dict = field(default_factory=dict)
 
 

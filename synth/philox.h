@@ -69,6 +69,41 @@ SYNTH_HD uint32_t synth_uniform_int(uint32_t w, uint32_t lo, uint32_t n) {
     return lo + (uint32_t)(((uint64_t)w * (uint64_t)n) >> 32);
 }
 
+/* Second code distribution ("peaked"): E2M1 codes shaped like those of
+ * block-scaled normal weights rather than uniform, so that the bytes carry the
+ * redundancy a trained layer's do. Magnitude codes 0..7 are drawn from a fixed
+ * table (parts of 2^15: 3260, 6318, 5757, 4928, 5580, 4299, 2218, 408; close
+ * to a standard normal binned at 0.125, 0.375, 0.625, 0.875, 1.25, 1.75, 2.5)
+ * and the sign bit uniformly, so half of the zero codes are negative zeros.
+ * One 16-bit draw per code: bit 0 the sign, bits 1..15 the magnitude. */
+SYNTH_HD uint32_t synth_peaked_code(uint32_t h16) {
+    const uint32_t u = (h16 >> 1) & 0x7FFFu;
+    uint32_t m = 0;
+    m += u >= 3260u;
+    m += u >= 9578u;
+    m += u >= 15335u;
+    m += u >= 20263u;
+    m += u >= 25843u;
+    m += u >= 30142u;
+    m += u >= 32360u;
+    return ((h16 & 1u) << 3) | m;
+}
+
+/* 16 bytes (32 codes) of row `row`, block `blk` under the peaked distribution:
+ * four Philox calls (blocks 4 blk .. 4 blk + 3), code n from the 16-bit half
+ * n % 2 of word n / 2; byte j holds code 2j in its low nibble. */
+SYNTH_HD void synth_peaked_block(uint64_t seed, uint32_t tensor, uint32_t expert, uint32_t row,
+                                 uint32_t blk, uint8_t out[16]) {
+    for (int q = 0; q < 4; ++q) {
+        synth_u32x4 w = synth_block(seed, tensor, expert, row, 4u * blk + (uint32_t)q);
+        for (int i = 0; i < 4; ++i) {  /* word i of call q: codes 8q + 2i, 8q + 2i + 1 */
+            const uint32_t lo = synth_peaked_code(w.v[i] & 0xFFFFu);
+            const uint32_t hi = synth_peaked_code(w.v[i] >> 16);
+            out[4 * q + i] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
 /* Tensor ids (the Philox key's second word). */
 enum {
     SYNTH_T_GATE_Q = 1, SYNTH_T_UP_Q = 2, SYNTH_T_DOWN_Q = 3,

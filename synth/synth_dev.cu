@@ -22,6 +22,21 @@ __global__ void synth_codes_kernel(uint64_t seed, uint32_t tensor, uint32_t e0, 
     }
 }
 
+// Peaked code distribution: one thread per 16-byte block of one row.
+__global__ void synth_codes_peaked_kernel(uint64_t seed, uint32_t tensor, uint32_t e0, int64_t rows,
+                                          int64_t nblk, int64_t n_experts, uint4 *out) {
+    int64_t total = n_experts * rows * nblk;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        int64_t b = i % nblk;
+        int64_t r = (i / nblk) % rows;
+        int64_t e = i / (nblk * rows);
+        union { uint8_t b[16]; uint4 v; } u;
+        synth_peaked_block(seed, tensor, e0 + (uint32_t)e, (uint32_t)r, (uint32_t)b, u.b);
+        out[i] = u.v;
+    }
+}
+
 // One thread per group of four scale bytes of one row.
 __global__ void synth_scales_kernel(uint64_t seed, uint32_t tensor, uint32_t e0, int64_t rows,
                                     int64_t ns, int64_t n_experts, uint32_t lo, uint32_t n,
@@ -49,6 +64,18 @@ SYNTH_API int synth_dev_mx_codes(uint64_t seed, uint32_t tensor, uint32_t e0, in
     int64_t nblk = K / 32;  // 16-byte blocks per row
     synth_codes_kernel<<<152 * 8, 256, 0, (cudaStream_t)stream>>>(seed, tensor, e0, rows, nblk,
                                                                    n_experts, (uint4 *)out);
+    return cudaGetLastError() == cudaSuccess ? 0 : -2;
+}
+
+// codes under distribution `dist` (0 uniform, 1 peaked).
+SYNTH_API int synth_dev_mx_codes_dist(uint64_t seed, uint32_t tensor, uint32_t e0,
+                                      int64_t n_experts, int64_t rows, int64_t K, int dist,
+                                      void *out, void *stream) {
+    if (dist == 0) return synth_dev_mx_codes(seed, tensor, e0, n_experts, rows, K, out, stream);
+    if (dist != 1 || K % 32 != 0 || rows <= 0 || n_experts <= 0 || ((uintptr_t)out & 15))
+        return -1;
+    synth_codes_peaked_kernel<<<152 * 8, 256, 0, (cudaStream_t)stream>>>(
+        seed, tensor, e0, rows, K / 32, n_experts, (uint4 *)out);
     return cudaGetLastError() == cudaSuccess ? 0 : -2;
 }
 

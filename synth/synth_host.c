@@ -49,6 +49,20 @@ SYNTH_API int synth_mx_codes(uint64_t seed, uint32_t tensor, uint32_t expert,
     return 0;
 }
 
+/* Packed E2M1 codes under distribution `dist` (0: uniform, as synth_mx_codes;
+ * 1: peaked, see philox.h). */
+SYNTH_API int synth_mx_codes_dist(uint64_t seed, uint32_t tensor, uint32_t expert,
+                                  int64_t rows, int64_t K, int dist, uint8_t *out) {
+    if (dist == 0) return synth_mx_codes(seed, tensor, expert, rows, K, out);
+    if (dist != 1 || K % 32 != 0 || rows < 0) return -1;
+    int64_t nb = K / 2;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb / 16; ++b)
+            synth_peaked_block(seed, tensor, expert, (uint32_t)r, (uint32_t)b, out + r * nb + b * 16);
+    return 0;
+}
+
 /* E8M0 scale bytes: rows x (K/32) bytes, each uniform over {lo .. lo+n-1}. */
 SYNTH_API int synth_mx_scales(uint64_t seed, uint32_t tensor, uint32_t expert,
                               int64_t rows, int64_t K, int lo, int n, uint8_t *out) {

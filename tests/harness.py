@@ -41,7 +41,7 @@ def host_layer_weights(w: synth.Workload, device="cuda") -> dict:
     from mxfp4_routed_expert_03_gb300.layer import alloc_weights
     weights = alloc_weights(w.E, w.D, w.F, device)
     for e in range(w.E):
-        for name, arr in synth.expert_weights(w.seed, e, w.D, w.F).items():
+        for name, arr in synth.expert_weights(w.seed, e, w.D, w.F, dist=w.codes).items():
             weights[name][e].copy_(torch.from_numpy(arr))
     return weights
 
@@ -51,7 +51,7 @@ def device_layer_weights(w: synth.Workload, device="cuda") -> dict:
     from mxfp4_routed_expert_03_gb300.layer import alloc_weights
     weights = alloc_weights(w.E, w.D, w.F, device)
     synth.dev_fill_layer(w.seed, w.E, w.D, w.F, {k: v.data_ptr() for k, v in weights.items()},
-                         torch.cuda.current_stream().cuda_stream)
+                         torch.cuda.current_stream().cuda_stream, dist=w.codes)
     torch.cuda.synchronize()
     return weights
 

@@ -63,15 +63,16 @@ def test_tiny_one_expert_holds_all_rows(tiny_weights):
     assert_close(got, reference(w, x, lg)["out"], DECODE_MAX_REL, DECODE_MAE_REL)
 
 
-def test_device_generator_matches_host():
+@pytest.mark.parametrize("dist", [synth.CODES_UNIFORM, synth.CODES_PEAKED])
+def test_device_generator_matches_host(dist):
     w = synth.WORKLOADS["decode1"]
     from mxfp4_routed_expert_03_gb300.layer import alloc_weights
     E = 3
     wts = alloc_weights(E, w.D, w.F)
-    synth.dev_fill_layer(w.seed, E, w.D, w.F, {k: v.data_ptr() for k, v in wts.items()})
+    synth.dev_fill_layer(w.seed, E, w.D, w.F, {k: v.data_ptr() for k, v in wts.items()}, dist=dist)
     torch.cuda.synchronize()
     for e in range(E):
-        host = synth.expert_weights(w.seed, e, w.D, w.F)
+        host = synth.expert_weights(w.seed, e, w.D, w.F, dist=dist)
         for name, arr in host.items():
             np.testing.assert_array_equal(wts[name][e].cpu().numpy(), arr, err_msg=name)
 

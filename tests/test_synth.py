@@ -41,3 +41,20 @@ def test_normals():
     b = synth.normal_bf16(1, synth.X, 200, 1000)
     xf = (b.astype(np.uint32) << 16).view(np.float32)
     assert np.max(np.abs(xf - x)) <= np.max(np.abs(x)) * 2.0 ** -8
+
+
+def test_peaked_code_distribution():
+    """Magnitudes follow the stated table (parts of 2^15) and the sign bit is
+    uniform, so half of the zero codes are negative zeros."""
+    q = synth.mx_codes(0, synth.GATE_Q, 3, 512, 1024, dist=synth.CODES_PEAKED)
+    codes = np.concatenate([q & 15, q >> 4]).ravel()
+    table = np.array([3260, 6318, 5757, 4928, 5580, 4299, 2218, 408]) / 32768.0
+    mag = np.bincount(codes & 7, minlength=8) / codes.size
+    assert np.all(np.abs(mag - table) < 4 * np.sqrt(table / codes.size) + 1e-4)
+    neg = (codes >> 3).mean()
+    assert abs(neg - 0.5) < 0.005
+    z = codes[(codes & 7) == 0]
+    assert abs((z == 8).mean() - 0.5) < 0.01
+    # the uniform distribution is unchanged by the new entry point
+    np.testing.assert_array_equal(synth.mx_codes(0, synth.GATE_Q, 3, 8, 64),
+                                  synth.mx_codes(0, synth.GATE_Q, 3, 8, 64, dist=synth.CODES_UNIFORM))
