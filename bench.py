@@ -58,6 +58,12 @@ BENCH_WORKLOADS = {
     "decode_stream": {"Ts": [1, 4, 16], "path": "forward", "stream_slots": 448,
                       "desc": "K3 routed layer decode, T=1,4,16, all 896 experts in pinned host "
                               "memory behind a 448-slot HBM expert cache (expert streaming)"},
+    "decode_stream_store": {"Ts": [1, 4, 16], "path": "forward", "stream_slots": 448,
+                            "store": True, "codes": 1,   # synth.CODES_PEAKED
+                            "desc": "K3 routed layer decode, T=1,4,16, all 896 experts rANS-coded "
+                                    "in pinned host memory (compressed expert store; peaked E2M1 "
+                                    "codes) behind a 448-slot HBM expert cache, misses decoded "
+                                    "on the GPU"},
 }
 
 
@@ -120,7 +126,8 @@ def oracle_tokens_per_s(workload_name: str, budget_s: float):
     while True:
         T = wl["Ts"][it % len(wl["Ts"])]
         w = synth.Workload(base.name, T=T, D=base.D, F=base.F, E=base.E, k=base.k, seed=base.seed,
-                           zipf_s=base.zipf_s, router=base.router, shared=base.shared)
+                           zipf_s=base.zipf_s, router=base.router, shared=base.shared,
+                           codes=wl.get("codes", synth.CODES_UNIFORM))
         x = synth.make_x(w, it % N_SETS)
         lg = None if w.router == "xwr" else synth.make_logits(w, it % N_SETS)
         reference(w, x, lg, tokens=[it % T])
@@ -271,9 +278,11 @@ def run_ours(args):
     weights = alloc_weights(n_exp, D_MODEL, D_FF)
     synth.dev_fill_layer(base.seed, n_exp, D_MODEL, D_FF,
                          {k: v.data_ptr() for k, v in weights.items()},
-                         torch.cuda.current_stream().cuda_stream)
+                         torch.cuda.current_stream().cuda_stream,
+                         dist=wl.get("codes", synth.CODES_UNIFORM))
     use_router = bool(wl.get("router"))
     n_slots = wl.get("stream_slots")
+    store_info = None
     n_sets = wl.get("sets", N_SETS)
     if use_router:
         import dataclasses
@@ -289,7 +298,18 @@ def run_ours(args):
             host[k].copy_(v)
         del weights
         torch.cuda.empty_cache()
-        layer = StreamingLayer(D_MODEL, D_FF, n_exp, TOP_K, host, min(n_slots, n_exp))
+        if wl.get("store"):
+            # the compressed store, built by the library's host encoder
+            from mxfp4_routed_expert_03_gb300.layer import ExpertStore
+            t_enc = time.perf_counter()
+            store = ExpertStore(n_exp, D_MODEL, D_FF, host)
+            store_info = {"encode_s": time.perf_counter() - t_enc,
+                          "stored_over_raw": store.blob_bytes / store.raw_bytes}
+            del host
+            layer = StreamingLayer(D_MODEL, D_FF, n_exp, TOP_K, None, min(n_slots, n_exp),
+                                   store=store)
+        else:
+            layer = StreamingLayer(D_MODEL, D_FF, n_exp, TOP_K, host, min(n_slots, n_exp))
     else:
         layer = Layer(D_MODEL, D_FF, n_exp, TOP_K, weights)
     def path_of(T):
@@ -502,17 +522,26 @@ def run_ours(args):
             best = t if best is None else min(best, t)
         h2d = (1 << 31) / (best * 1e-3) / 1e9
         del link, dst
-        gbs_c = misses * EXPERT_BYTES / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else 0.0
-        roof = {"bound": "host-to-device link", "kernel": "moe_stream_copy_kernel",
+        # bytes crossing the link per missing expert: the expert itself, or
+        # from a store its stored tiles (the store's mean per expert)
+        store = getattr(layer, "store", None)
+        link_bytes = store.blob_bytes / n_exp if store is not None else EXPERT_BYTES
+        gbs_c = misses * link_bytes / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else 0.0
+        roof = {"bound": "host-to-device link",
+                "kernel": "moe_store_decode_kernel" if store is not None else "moe_stream_copy_kernel",
                 "achieved": gbs_c, "peak": h2d, "unit": "GB/s",
                 "frac": gbs_c / h2d if h2d else None,
                 "peak_source": "measured in this run: cudaMemcpyAsync of 2 GiB pinned host memory "
                                "to the device",
-                "bytes_per_launch": misses * EXPERT_BYTES / max(1, args.steps * len(batches)),
+                "bytes_per_launch": misses * link_bytes / max(1, args.steps * len(batches)),
                 "traffic": None}
         stream_info = {"slots": layer.n_slots, "hit_rate": hits / max(1, hits + misses),
                        "misses_per_step": misses / args.steps,
                        "copy_ms_per_step": copy_ms / args.steps}
+        if store is not None:
+            roof["decoded_GBs"] = misses * EXPERT_BYTES / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else 0.0
+            roof["link_bytes_per_expert"] = "stored bytes, the store's mean per expert"
+            stream_info["store"] = store_info
 
     # plan: one fused kernel for T <= 64, else top-k, count, scan, scatter;
     # decode: gate/up, down, combine; forward: quant, schedule, gather, two GEMMs,

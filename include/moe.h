@@ -66,7 +66,10 @@ enum moe_status_code {
     MOE_ERR_DEVICE_TIMEOUT = -5,  /* a device-side wait hit its iteration limit */
     MOE_ERR_NAN_LOGIT = -6,       /* a router logit was NaN (treated as -inf) */
     MOE_ERR_BAD_INDEX = -7,       /* out-of-range expert / row index in a plan */
-    MOE_ERR_NOT_PREPARED = -8     /* moe_forward before moe_prepare */
+    MOE_ERR_NOT_PREPARED = -8,    /* moe_forward before moe_prepare */
+    MOE_ERR_CORRUPT_TILE = -9     /* a compressed-store tile failed its checks (record, table,
+                                     final coder states, word count or Adler-32); the bytes
+                                     of its slot are then undefined */
 };
 
 enum moe_router_mode {
@@ -90,7 +93,8 @@ enum moe_prof_kernel {
     MOE_PROF_ROUTER = 5,          /* moe_plan / moe_router_logits: x . W_r GEMM */
     MOE_PROF_SHARED_GATEUP = 6,   /* shared expert: gate/up GEMM + SwiGLU */
     MOE_PROF_SHARED_DOWN = 7,     /* shared expert: down GEMM */
-    MOE_PROF_STREAM_COPY = 8      /* expert streaming: copy of the missing experts from host memory */
+    MOE_PROF_STREAM_COPY = 8      /* expert streaming: copy (or, from a compressed store, decode)
+                                     of the missing experts from host memory */
 };
 
 /* Layer shape. Supported envelope: d_model a multiple of 256, d_ff of 128,
@@ -291,6 +295,96 @@ int moe_create_streaming(const moe_desc *desc, const moe_weights *host_w,
  * the last call. MOE_ERR_INVALID_ARG for other handles. */
 int moe_stream_stats(moe_handle *h, int64_t *hits, int64_t *misses, int32_t *last_misses,
                      void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Compressed expert store: the slow tier holds the experts rANS-coded in
+ * independent 16 KiB tiles, and the GPU decodes the missing experts of a call
+ * straight into ordinary cache slots (Moonshine GitHub README, "Expert-stream
+ * compression" / "MZG2 production store": redundant MXFP4 negative zeros
+ * canonicalised, independently bounded 16 KiB tiles, a checksum per tile and
+ * a check of the coder's final state, decode on the GPU into decoded cache
+ * slots). The pages fix no byte format; this library's format:
+ *  - An expert's arrays in the order gate_q, gate_s, up_q, up_s, down_q,
+ *    down_s (layouts of moe_weights; D*F/2 bytes per code array, D*F/32 per
+ *    scale array). Canonical bytes: every E2M1 code 0x8 (negative zero) in
+ *    the code arrays becomes 0x0 (same value); scale bytes unchanged.
+ *  - One frequency table per (expert, array): f[256] (uint16), summing to
+ *    4096; f[b] = 0 for bytes absent from the array, else
+ *    max(1, floor(count * 4096 / n)), after which, while the sum exceeds 4096,
+ *    the largest entry (lowest byte value among equals) loses one, and while
+ *    it falls short, the largest gains one. cum[b] = f[0] + ... + f[b-1].
+ *  - Each array is cut into 16384-byte tiles (the last may be shorter); an
+ *    expert has moe_store_tiles_per_expert() tiles, arrays in order. A tile
+ *    of n bytes is coded by 32 interleaved rANS coders (byte i to coder i % 32,
+ *    step i / 32) with 32-bit states in [2^16, 2^32) and 16-bit words.
+ *    Decoding, steps in increasing order: each coder with a byte in the step
+ *    takes q = x % 4096, the byte b with cum[b] <= q < cum[b] + f[b], sets
+ *    x = f[b] * (x / 4096) + q - cum[b] and, if x < 2^16, reads the next word
+ *    (x = x * 2^16 + w; within a step, coders in increasing order). Encoding
+ *    is the exact reverse, starting every coder at 2^16; a sound tile ends
+ *    with every state at 2^16 and every word read.
+ *  - Stored tile: the 32 final states (uint32, coder 0 first) then the words
+ *    (uint16) in read order, when 128 + 2 * words < n; otherwise the n
+ *    canonical bytes (raw). Zero-padded to a multiple of 16 bytes, back to back.
+ * ------------------------------------------------------------------------- */
+
+/* One tile's record (32 bytes). */
+typedef struct moe_tile_rec {
+    uint32_t offset_lo, offset_hi;  /* bytes from the start of the blob; multiple of 16 */
+    uint32_t n_bytes;               /* decoded bytes, 1..16384 */
+    uint32_t n_words;               /* 16-bit words of a coded tile; 0 when raw */
+    uint32_t adler;                 /* Adler-32 (zlib's definition) of the canonical bytes */
+    uint32_t flags;                 /* bit 0: stored raw */
+    uint32_t reserved[2];           /* 0 */
+} moe_tile_rec;
+
+/* A store as the device reads it. */
+typedef struct moe_store {
+    const uint8_t *blob;         /* host memory the device can read (cudaHostAlloc or
+                                    registered, mapped at the host address), 16-byte aligned */
+    int64_t blob_bytes;
+    const moe_tile_rec *tiles;   /* device, [n_experts][tiles per expert], 16-byte aligned */
+    const uint16_t *tables;      /* device, [n_experts][6][256], 16-byte aligned */
+} moe_store;
+
+/* Host. Tiles of one expert: sum over the six arrays of ceil(bytes / 16384);
+ * -1 unless d_model and d_ff are positive multiples of 32. 1071 for K3. */
+int32_t moe_store_tiles_per_expert(int32_t d_model, int32_t d_ff);
+
+/* Host. Blob capacity moe_store_encode needs: every tile at its raw size
+ * rounded up to 16 bytes, for n_experts experts (the encoder first lays each
+ * expert out at that stride, then packs the blob). -1 on bad sizes. */
+int64_t moe_store_blob_bound(int32_t n_experts, int32_t d_model, int32_t d_ff);
+
+/* Host. Builds the store of experts 0..n_experts-1 from HOST weight arrays
+ * (host_w: gate/up/down codes and scales in the layouts of moe_weights; any
+ * host memory; other fields ignored). Writes blob (host, blob_cap >=
+ * moe_store_blob_bound bytes; *blob_bytes receives the packed size), tiles
+ * (host, n_experts * tiles-per-expert records) and tables (host,
+ * n_experts * 6 * 256). n_threads host threads (<= 0: one per core). Copy
+ * tiles and tables to the device and keep the blob in device-readable host
+ * memory for moe_create_streaming_store / moe_store_decode. */
+int moe_store_encode(int32_t n_experts, int32_t d_model, int32_t d_ff, const moe_weights *host_w,
+                     uint8_t *blob, int64_t blob_cap, int64_t *blob_bytes, moe_tile_rec *tiles,
+                     uint16_t *tables, int32_t n_threads);
+
+/* Decodes experts[i] of the store into slot slots[i] of the arrays in slot_w
+ * (device arrays holding n_slots experts, layouts of moe_weights), i < n.
+ * experts and slots are device int32 [n]; status a device int32 that receives
+ * the first error (MOE_ERR_BAD_INDEX for an expert or slot out of range,
+ * MOE_ERR_CORRUPT_TILE for a tile that fails a check; the kernel skips that
+ * tile and never reads or writes out of bounds). Asynchronous on `stream`. */
+int moe_store_decode(int32_t n_experts, int32_t d_model, int32_t d_ff, const moe_store *store,
+                     const int32_t *experts, const int32_t *slots, int32_t n,
+                     const moe_weights *slot_w, int32_t n_slots, int32_t *status, void *stream);
+
+/* Host. moe_create_streaming with the routed experts in a compressed store:
+ * moe_forward decodes each call's missing experts from the store into their
+ * slots (instead of copying them). Same slot_w, n_slots and state rules;
+ * the store's arrays must outlive the handle. */
+int moe_create_streaming_store(const moe_desc *desc, const moe_store *store,
+                               const moe_weights *slot_w, int32_t n_slots, void *state,
+                               moe_handle **out);
 
 /* Host. Instrumentation for timing one kernel on the library's own stream:
  * while `which` names a kernel (enum moe_prof_kernel), every later call that

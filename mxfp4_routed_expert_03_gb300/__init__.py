@@ -24,6 +24,7 @@ MOE_ERR_DEVICE_TIMEOUT = -5
 MOE_ERR_NAN_LOGIT = -6
 MOE_ERR_BAD_INDEX = -7
 MOE_ERR_NOT_PREPARED = -8
+MOE_ERR_CORRUPT_TILE = -9
 
 MOE_ROUTER_LOGITS = 0
 MOE_ROUTER_XWR = 1
@@ -36,7 +37,9 @@ MOE_OP_DECODE = 2
 EXPORTS = ("moe_create", "moe_destroy", "moe_expert_bytes", "moe_prepared_bytes", "moe_prepare",
            "moe_workspace_bytes", "moe_plan", "moe_router_logits", "moe_forward", "moe_decode",
            "moe_decode_noalloc", "moe_stream_state_bytes", "moe_create_streaming",
-           "moe_stream_stats", "moe_profile_kernel", "moe_status", "moe_strerror")
+           "moe_stream_stats", "moe_store_tiles_per_expert", "moe_store_blob_bound",
+           "moe_store_encode", "moe_store_decode", "moe_create_streaming_store",
+           "moe_profile_kernel", "moe_status", "moe_strerror")
 
 MOE_PROF_NONE = 0
 MOE_PROF_DECODE_GATEUP = 1
@@ -53,6 +56,18 @@ class moe_desc(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("router_mode", ctypes.c_int32), ("has_shared", ctypes.c_int32)]
+
+
+class moe_tile_rec(ctypes.Structure):
+    _fields_ = [("offset_lo", ctypes.c_uint32), ("offset_hi", ctypes.c_uint32),
+                ("n_bytes", ctypes.c_uint32), ("n_words", ctypes.c_uint32),
+                ("adler", ctypes.c_uint32), ("flags", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32 * 2)]
+
+
+class moe_store(ctypes.Structure):
+    _fields_ = [("blob", ctypes.c_void_p), ("blob_bytes", ctypes.c_int64),
+                ("tiles", ctypes.c_void_p), ("tables", ctypes.c_void_p)]
 
 
 class moe_weights(ctypes.Structure):
@@ -120,6 +135,21 @@ def lib() -> ctypes.CDLL:
         L.moe_stream_stats.argtypes = [p, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                        ctypes.POINTER(i32), p]
         L.moe_stream_stats.restype = ctypes.c_int
+        L.moe_store_tiles_per_expert.argtypes = [i32, i32]
+        L.moe_store_tiles_per_expert.restype = i32
+        L.moe_store_blob_bound.argtypes = [i32, i32, i32]
+        L.moe_store_blob_bound.restype = i64
+        L.moe_store_encode.argtypes = [i32, i32, i32, ctypes.POINTER(moe_weights), p, i64,
+                                       ctypes.POINTER(i64), p, p, i32]
+        L.moe_store_encode.restype = ctypes.c_int
+        L.moe_store_decode.argtypes = [i32, i32, i32, ctypes.POINTER(moe_store), p, p, i32,
+                                       ctypes.POINTER(moe_weights), i32, p, p]
+        L.moe_store_decode.restype = ctypes.c_int
+        L.moe_create_streaming_store.argtypes = [ctypes.POINTER(moe_desc),
+                                                 ctypes.POINTER(moe_store),
+                                                 ctypes.POINTER(moe_weights), i32, p,
+                                                 ctypes.POINTER(p)]
+        L.moe_create_streaming_store.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -170,6 +200,47 @@ def moe_create_streaming(desc: moe_desc, host_weights: moe_weights, slot_weights
                                     ctypes.byref(h))
     if rc != MOE_OK:
         raise MoeError(rc, "moe_create_streaming")
+    return h.value
+
+
+def moe_store_tiles_per_expert(d_model: int, d_ff: int) -> int:
+    return lib().moe_store_tiles_per_expert(d_model, d_ff)
+
+
+def moe_store_blob_bound(n_experts: int, d_model: int, d_ff: int) -> int:
+    return lib().moe_store_blob_bound(n_experts, d_model, d_ff)
+
+
+def moe_store_encode(n_experts: int, d_model: int, d_ff: int, host_weights: moe_weights,
+                     blob, blob_cap: int, tiles, tables, n_threads: int = 0) -> int:
+    """Host encoder; blob, tiles, tables are host buffers (pointers or tensors).
+    Returns the packed blob size."""
+    nbytes = ctypes.c_int64(0)
+    rc = lib().moe_store_encode(n_experts, d_model, d_ff, ctypes.byref(host_weights), _ptr(blob),
+                                blob_cap, ctypes.byref(nbytes), _ptr(tiles), _ptr(tables),
+                                n_threads)
+    if rc != MOE_OK:
+        raise MoeError(rc, "moe_store_encode")
+    return nbytes.value
+
+
+def moe_store_decode(n_experts: int, d_model: int, d_ff: int, store: moe_store, experts, slots,
+                     n: int, slot_weights: moe_weights, n_slots: int, status, stream=None) -> int:
+    return lib().moe_store_decode(n_experts, d_model, d_ff, ctypes.byref(store), _ptr(experts),
+                                  _ptr(slots), n, ctypes.byref(slot_weights), n_slots,
+                                  _ptr(status), _stream(stream))
+
+
+def moe_create_streaming_store(desc: moe_desc, store: moe_store, slot_weights: moe_weights,
+                               n_slots: int, state) -> int:
+    """store: the compressed store (blob in pinned host memory, records and tables on the
+    device); slot_weights: device cache arrays."""
+    h = ctypes.c_void_p()
+    rc = lib().moe_create_streaming_store(ctypes.byref(desc), ctypes.byref(store),
+                                          ctypes.byref(slot_weights), n_slots, _ptr(state),
+                                          ctypes.byref(h))
+    if rc != MOE_OK:
+        raise MoeError(rc, "moe_create_streaming_store")
     return h.value
 
 

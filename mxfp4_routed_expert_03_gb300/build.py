@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libmoe.so")
 OBJDIR = os.path.join(HERE, "_build")
 SOURCES = ["api.cu", "route.cu", "decode.cu", "quant.cu", "grouped_gemm.cu", "dense_gemm.cu",
-           "noalloc.cu", "stream.cu"]
+           "noalloc.cu", "stream.cu", "store.cu", "store_enc.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
               "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", os.path.join(ROOT, "include")]
 
@@ -60,7 +60,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(o)
     if force or jobs or _stale(LIB, objs):
         subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-shared",
-                               "-o", LIB, *objs, "-lcudart"])
+                               "-o", LIB, *objs, "-lcudart", "-lpthread"])
     return LIB
 
 

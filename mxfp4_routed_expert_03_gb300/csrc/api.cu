@@ -24,6 +24,8 @@ struct moe_handle {
     bool streaming;        // expert streaming: w.* are the slot cache, host_w the store
     moe_weights host_w;    // streaming: all experts, host memory the device can read
     void *sstate;          // streaming: device cache state (moe_stream_state_bytes)
+    bool from_store;       // streaming from a compressed store (store) instead of host_w
+    moe_store store;
 };
 
 // Device-side waits give up after this many SM clocks (about one second).
@@ -139,6 +141,7 @@ MOE_API const char *moe_strerror(int code) {
         case MOE_ERR_NAN_LOGIT: return "NaN router logit";
         case MOE_ERR_BAD_INDEX: return "out-of-range index in plan";
         case MOE_ERR_NOT_PREPARED: return "moe_prepare has not been called on this handle";
+        case MOE_ERR_CORRUPT_TILE: return "a compressed-store tile failed its checks";
         default: return "unknown status code";
     }
 }
@@ -225,6 +228,16 @@ MOE_API int moe_create(const moe_desc *d, const moe_weights *w, moe_handle **out
     return create_impl(d, w, d ? d->n_experts : 0, out);
 }
 
+// Host memory the device reads through the same address (pinned and mapped).
+static bool device_readable_host(const void *p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost && at.devicePointer == p;
+}
+
 MOE_API size_t moe_stream_state_bytes(int32_t n_experts, int32_t n_slots) {
     if (n_experts <= 0 || n_slots <= 0 || n_experts > MOE_MAX_EXPERTS || n_slots > 1024) return 0;
     return moe_stream_state_size(n_experts, n_slots);
@@ -241,15 +254,9 @@ MOE_API int moe_create_streaming(const moe_desc *d, const moe_weights *host_w,
     const void *hp[] = {host_w->gate_q, host_w->gate_s, host_w->up_q,
                         host_w->up_s, host_w->down_q, host_w->down_s};
     for (const void *p : hp) {
-        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
         // the copy kernel reads these through the same addresses: require
         // registered (pinned) host memory mapped at the host address
-        cudaPointerAttributes at;
-        if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
-            cudaGetLastError();
-            return MOE_ERR_INVALID_ARG;
-        }
-        if (at.type != cudaMemoryTypeHost || at.devicePointer != p) return MOE_ERR_INVALID_ARG;
+        if (!p || !aligned16(p) || !device_readable_host(p)) return MOE_ERR_INVALID_ARG;
     }
     if ((uintptr_t)state & 15u) return MOE_ERR_INVALID_ARG;
     moe_handle *h = nullptr;
@@ -266,6 +273,82 @@ MOE_API int moe_create_streaming(const moe_desc *d, const moe_weights *host_w,
     }
     *out = h;
     return MOE_OK;
+}
+
+MOE_API int moe_create_streaming_store(const moe_desc *d, const moe_store *store,
+                                       const moe_weights *slot_w, int32_t n_slots, void *state,
+                                       moe_handle **out) {
+    if (!out) return MOE_ERR_INVALID_ARG;
+    *out = NULL;
+    if (!d || !store || !slot_w || !state) return MOE_ERR_INVALID_ARG;
+    if (d->n_experts <= 0 || n_slots < 1 || n_slots > d->n_experts || n_slots > 1024)
+        return MOE_ERR_INVALID_ARG;
+    MoeStoreJob probe;
+    if (!moe_store_job_shape(d->d_model, d->d_ff, probe)) return MOE_ERR_INVALID_ARG;
+    if (!store->blob || !aligned16(store->blob) || store->blob_bytes <= 0 || !store->tiles ||
+        !aligned16(store->tiles) || !store->tables || !aligned16(store->tables) ||
+        !device_readable_host(store->blob))
+        return MOE_ERR_INVALID_ARG;
+    if ((uintptr_t)state & 15u) return MOE_ERR_INVALID_ARG;
+    moe_handle *h = nullptr;
+    int rc = create_impl(d, slot_w, n_slots, &h);
+    if (rc != MOE_OK) return rc;
+    h->streaming = true;
+    h->from_store = true;
+    h->store = *store;
+    h->sstate = state;
+    if (moe_launch_stream_init(d->n_experts, n_slots, state, 0) != cudaSuccess ||
+        cudaStreamSynchronize(0) != cudaSuccess) {
+        cudaFree(h->status);
+        free(h);
+        return MOE_ERR_CUDA;
+    }
+    *out = h;
+    return MOE_OK;
+}
+
+// Fills a decode job's store and slot fields.
+static void store_job(MoeStoreJob &j, const moe_store &s, int E, const moe_weights &dst,
+                      int n_slots, int *status) {
+    j.blob = s.blob;
+    j.blob_bytes = s.blob_bytes;
+    j.tiles = s.tiles;
+    j.tables = s.tables;
+    j.E = E;
+    j.n_slots = n_slots;
+    const uint8_t *d6[6] = {dst.gate_q, dst.gate_s, dst.up_q, dst.up_s, dst.down_q, dst.down_s};
+    for (int a = 0; a < 6; ++a) j.dst[a] = const_cast<uint8_t *>(d6[a]);
+    j.status = status;
+}
+
+MOE_API int moe_store_decode(int32_t n_experts, int32_t d_model, int32_t d_ff,
+                             const moe_store *store, const int32_t *experts, const int32_t *slots,
+                             int32_t n, const moe_weights *slot_w, int32_t n_slots, int32_t *status,
+                             void *stream) {
+    MoeStoreJob j;
+    if (n_experts <= 0 || n_experts > MOE_MAX_EXPERTS || n < 0 || n_slots < 1 || !store ||
+        !slot_w || !status || !moe_store_job_shape(d_model, d_ff, j))
+        return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    if (!experts || !slots || !store->blob || !aligned16(store->blob) || store->blob_bytes <= 0 ||
+        !store->tiles || !aligned16(store->tiles) || !store->tables || !aligned16(store->tables))
+        return MOE_ERR_INVALID_ARG;
+    const uint8_t *d6[6] = {slot_w->gate_q, slot_w->gate_s, slot_w->up_q,
+                            slot_w->up_s, slot_w->down_q, slot_w->down_s};
+    for (const uint8_t *p : d6)
+        if (!p) return MOE_ERR_INVALID_ARG;
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    store_job(j, *store, n_experts, *slot_w, n_slots, status);
+    j.experts = experts;
+    j.slots = slots;
+    j.n_dev = nullptr;
+    j.n_host = n;
+    j.max_items = n;
+    return moe_launch_store_decode(j, nsm, (cudaStream_t)stream) == cudaSuccess ? MOE_OK
+                                                                                : MOE_ERR_CUDA;
 }
 
 MOE_API int moe_stream_stats(moe_handle *h, int64_t *hits, int64_t *misses, int32_t *last_misses,
@@ -298,12 +381,24 @@ static cudaError_t stream_fill(moe_handle *h, const moe_plan_buf *plan, cudaStre
         c.slot[i] = const_cast<uint8_t *>(ss[i]);
         c.bytes[i] = by[i];
     }
+    const MoeStreamView v = moe_stream_view(h->sstate, E, S);
     if (err == cudaSuccess) {
         h->prof.before(MOE_PROF_STREAM_COPY, st);
-        err = moe_launch_stream_copy(E, S, h->sstate, &c, h->num_sms, st);
+        if (h->from_store) {  // decode the misses from the compressed store
+            MoeStoreJob j;
+            moe_store_job_shape(D, F, j);
+            store_job(j, h->store, E, sw, S, h->status);
+            j.experts = v.miss_e;
+            j.slots = v.miss_s;
+            j.n_dev = &v.hdr->last_miss;
+            j.n_host = 0;
+            j.max_items = S;
+            err = moe_launch_store_decode(j, h->num_sms, st);
+        } else {
+            err = moe_launch_stream_copy(E, S, h->sstate, &c, h->num_sms, st);
+        }
         h->prof.after(MOE_PROF_STREAM_COPY, st);
     }
-    const MoeStreamView v = moe_stream_view(h->sstate, E, S);
     uint8_t *atoms = const_cast<uint8_t *>(h->atoms);
     if (err == cudaSuccess)
         err = moe_launch_prepare_atoms_slots(F, D, 64, sw.gate_s, sw.up_s, atoms, &v.hdr->last_miss,

@@ -124,6 +124,26 @@ cudaError_t moe_launch_stream_lru(int E, int S, const int32_t *active, void *sta
                                   cudaStream_t st);
 cudaError_t moe_launch_stream_copy(int E, int S, void *state, const MoeStreamCopy *c, int nsm,
                                    cudaStream_t st);
+// store.cu: decode of compressed-store experts into cache slots. Items are the
+// pairs (experts[m], slots[m]), m < count, where count is *n_dev when n_dev is
+// set (clamped to [0, max_items]) and n_host otherwise.
+struct MoeStoreJob {
+    const uint8_t *blob;
+    int64_t blob_bytes;
+    const moe_tile_rec *tiles;
+    const uint16_t *tables;
+    int E, tpe, n_slots;
+    int64_t bytes[6];  // per expert and array
+    int first[7];      // first tile of each array within an expert
+    uint8_t *dst[6];   // slot arrays (n_slots experts each)
+    const int32_t *experts, *slots;
+    const int32_t *n_dev;
+    int n_host, max_items;
+    int *status;
+};
+// Fills bytes/first/tpe from the layer shape; false on a bad shape.
+bool moe_store_job_shape(int D, int F, MoeStoreJob &j);
+cudaError_t moe_launch_store_decode(const MoeStoreJob &j, int nsm, cudaStream_t st);
 // grouped_gemm.cu: prepared scale blocks of the slots listed in miss_s[0 .. *n_miss)
 cudaError_t moe_launch_prepare_atoms_slots(int M, int K, int mrows, const uint8_t *s,
                                            const uint8_t *s2, uint8_t *out, const int *n_miss,

@@ -8,9 +8,11 @@ from __future__ import annotations
 import torch
 
 from . import (MOE_OP_DECODE, MOE_OP_FORWARD, MOE_OP_PLAN, MOE_ROUTER_XWR, check, moe_create,
-               moe_create_streaming, moe_decode, moe_desc, moe_destroy, moe_forward, moe_plan,
-               moe_plan_buf, moe_prepare, moe_prepared_bytes, moe_router_logits, moe_status,
-               moe_stream_state_bytes, moe_stream_stats, moe_weights, moe_workspace_bytes)
+               moe_create_streaming, moe_create_streaming_store, moe_decode, moe_desc,
+               moe_destroy, moe_forward, moe_plan, moe_plan_buf, moe_prepare, moe_prepared_bytes,
+               moe_router_logits, moe_status, moe_store, moe_store_blob_bound, moe_store_encode,
+               moe_store_tiles_per_expert, moe_stream_state_bytes, moe_stream_stats, moe_weights,
+               moe_workspace_bytes)
 
 WEIGHT_NAMES = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
 
@@ -111,16 +113,56 @@ class Layer:
         return moe_status(self.h, stream)
 
 
+class ExpertStore:
+    """The compressed expert store of a layer: blob in pinned host memory,
+    tile records and frequency tables on the device, built by the library's
+    host encoder from host weight arrays (CPU tensors or numpy arrays in the
+    library's layouts)."""
+
+    def __init__(self, E: int, D: int, F: int, host_weights: dict, n_threads: int = 0,
+                 device="cuda"):
+        import numpy as np
+        self.E, self.D, self.F = E, D, F
+        self.tpe = moe_store_tiles_per_expert(D, F)
+        cap = moe_store_blob_bound(E, D, F)
+        if self.tpe <= 0 or cap <= 0:
+            raise ValueError("bad layer shape for a store")
+        arrays = {n: host_weights[n] for n in WEIGHT_NAMES}
+        ptrs = []
+        for n in WEIGHT_NAMES:
+            a = arrays[n]
+            ptrs.append(a.data_ptr() if isinstance(a, torch.Tensor) else a.ctypes.data)
+        hw = moe_weights(*ptrs, None, None, None, None)
+        blob = torch.empty(cap, dtype=torch.uint8, pin_memory=True)
+        tiles = np.zeros((E, self.tpe, 8), np.uint32)
+        tables = np.zeros((E, 6, 256), np.uint16)
+        self.blob_bytes = moe_store_encode(E, D, F, hw, blob.data_ptr(), cap, tiles.ctypes.data,
+                                           tables.ctypes.data, n_threads)
+        self.blob = blob
+        self.raw_bytes = sum(int(arrays[n].numel() if isinstance(arrays[n], torch.Tensor)
+                                 else arrays[n].size) for n in WEIGHT_NAMES)
+        self.tiles = torch.from_numpy(tiles).to(device)
+        self.tables = torch.from_numpy(tables.view(np.int16)).to(device)
+        self.records = tiles
+
+    def desc(self) -> moe_store:
+        return moe_store(self.blob.data_ptr(), self.blob_bytes, self.tiles.data_ptr(),
+                         self.tables.data_ptr())
+
+
 class StreamingLayer(Layer):
     """A routed layer whose experts stay in pinned host memory; the library
     keeps an HBM cache of n_slots of them (expert streaming). host_weights:
     CPU tensors in the library's layouts, pinned (tensor.pin_memory())."""
 
-    def __init__(self, D: int, F: int, E: int, k: int, host_weights: dict, n_slots: int,
-                 router_mode: int = 0, w_router=None, shared=None):
+    def __init__(self, D: int, F: int, E: int, k: int, host_weights: dict | None, n_slots: int,
+                 router_mode: int = 0, w_router=None, shared=None, store: ExpertStore | None = None):
+        """host_weights: pinned CPU tensors of all experts, or None with `store`
+        (an ExpertStore): the misses are then decoded from the store."""
         self.D, self.F, self.E, self.k = D, F, E, k
         self.router_mode = router_mode
         self.host_weights = host_weights
+        self.store = store
         self.n_slots = n_slots
         self.weights = alloc_weights(n_slots, D, F)  # the slot cache
         self.w_router = w_router
@@ -128,14 +170,19 @@ class StreamingLayer(Layer):
         ptr = lambda t: None if t is None else t.data_ptr()
         sh = shared or {}
         self.desc = moe_desc(D, F, E, k, router_mode, 1 if shared else 0)
-        self.hdesc = moe_weights(*[host_weights[n].data_ptr() for n in WEIGHT_NAMES], None,
-                                 None, None, None)
         self.wdesc = moe_weights(*[self.weights[n].data_ptr() for n in WEIGHT_NAMES],
                                  ptr(w_router), ptr(sh.get("sh_gate")), ptr(sh.get("sh_up")),
                                  ptr(sh.get("sh_down")))
         self.state = torch.empty(moe_stream_state_bytes(E, n_slots), dtype=torch.uint8,
                                  device="cuda")
-        self.h = moe_create_streaming(self.desc, self.hdesc, self.wdesc, n_slots, self.state)
+        if store is not None:
+            self.sdesc = store.desc()
+            self.h = moe_create_streaming_store(self.desc, self.sdesc, self.wdesc, n_slots,
+                                                self.state)
+        else:
+            self.hdesc = moe_weights(*[host_weights[n].data_ptr() for n in WEIGHT_NAMES], None,
+                                     None, None, None)
+            self.h = moe_create_streaming(self.desc, self.hdesc, self.wdesc, n_slots, self.state)
         self._ws = None
         self.atoms = None
 

@@ -223,7 +223,7 @@ ORACLE_API int64_t oracle_store_build(int64_t E, int64_t D, int64_t F, const uin
                                       uint8_t *blob, int64_t cap, uint32_t *rec, uint16_t *tab) {
     int64_t nb[6];
     const int64_t tpe = arrays(D, F, nb);
-    if (E <= 0 || D <= 0 || F <= 0 || (D * F) % 32) return -1;
+    if (E <= 0 || D <= 0 || F <= 0 || D % 32 || F % 32) return -1;  /* MXFP4 layouts */
     uint8_t *canon = (uint8_t *)malloc((size_t)nb[0]);
     uint8_t *tile = (uint8_t *)malloc(128 + 2 * TILE);
     int64_t off = 0;
