@@ -38,10 +38,29 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s + % roofline (decode HBM GB/s; prefill FP4 TFLOP/s), 1xGB300"
-D_MODEL, D_FF, N_EXPERTS, TOP_K = 7168, 1536, 896, 16
+K3_SHAPE = (7168, 1536, 896, 16)   # d_model, d_ff, experts, top-k
+D_MODEL, D_FF, N_EXPERTS, TOP_K = K3_SHAPE
 EXPERT_BYTES = 17547264            # one expert's three MXFP4 matrices (codes + scales)
 GATEUP_BYTES = 2 * (D_FF * D_MODEL // 2 + D_FF * D_MODEL // 32)
 DOWN_BYTES = D_MODEL * D_FF // 2 + D_MODEL * D_FF // 32
+
+
+def use_shape(wl: dict) -> None:
+    """Layer shape of the chosen workload (K3 unless it names another)."""
+    global D_MODEL, D_FF, N_EXPERTS, TOP_K, EXPERT_BYTES, GATEUP_BYTES, DOWN_BYTES
+    D_MODEL, D_FF, N_EXPERTS, TOP_K = wl.get("shape", K3_SHAPE)
+    GATEUP_BYTES = 2 * (D_FF * D_MODEL // 2 + D_FF * D_MODEL // 32)
+    DOWN_BYTES = D_MODEL * D_FF // 2 + D_MODEL * D_FF // 32
+    EXPERT_BYTES = GATEUP_BYTES + DOWN_BYTES
+
+
+def base_workload(name: str):
+    """The seeded generator's workload a bench workload draws its inputs from."""
+    import synth
+    wl = BENCH_WORKLOADS[name]
+    if "base" in wl:
+        return synth.WORKLOADS[wl["base"]]
+    return synth.WORKLOADS["decode1"] if name.startswith("decode") else synth.WORKLOADS[name]
 N_SETS = 8
 CROSSOVER_T = 0   # largest batch the CUDA-core decode path takes under --path auto
 
@@ -64,6 +83,17 @@ BENCH_WORKLOADS = {
                                     "in pinned host memory (compressed expert store; peaked E2M1 "
                                     "codes) behind a 448-slot HBM expert cache, misses decoded "
                                     "on the GPU"},
+    # MiMo V2.6 Flash lane: 256 experts, top-8, the same MXFP4 expert FFN; its
+    # hidden sizes are not on the pages (d_model 4096, d_ff 2048 give the
+    # stated 310B total over 48 layers)
+    "mimo_decode": {"Ts": [1, 4, 16], "path": "forward", "shape": (4096, 2048, 256, 8),
+                    "base": "mimo_decode",
+                    "desc": "MiMo-shaped routed layer decode, T=1,4,16 (d_model 4096, d_ff 2048, "
+                            "256 experts, top-8, MXFP4)"},
+    "mimo_prefill4k": {"Ts": [4096], "path": "forward", "shape": (4096, 2048, 256, 8),
+                       "base": "mimo_prefill4k",
+                       "desc": "MiMo-shaped routed layer prefill, T=4096, uniform routing "
+                               "(d_model 4096, d_ff 2048, 256 experts, top-8, MXFP4)"},
 }
 
 
@@ -81,8 +111,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall-time budget of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--experts", type=int, default=N_EXPERTS,
-                    help="experts in the layer (default 896); fewer only for profiling small "
+    ap.add_argument("--experts", type=int, default=None,
+                    help="experts in the layer (default: the workload's); fewer only for profiling small "
                          "cases, and the line is then marked as such")
     ap.add_argument("--tokens", type=int, default=None,
                     help="one batch of this many tokens instead of the workload's batches; only "
@@ -120,7 +150,7 @@ def oracle_tokens_per_s(workload_name: str, budget_s: float):
     from oracle.run import reference
     oracle.build()
     wl = BENCH_WORKLOADS[workload_name]
-    base = synth.WORKLOADS["decode1"] if workload_name.startswith("decode") else synth.WORKLOADS[workload_name]
+    base = base_workload(workload_name)
     done, t0 = 0, time.perf_counter()
     it = 0
     while True:
@@ -256,7 +286,7 @@ def run_ours(args):
                                               moe_profile_kernel)
     from mxfp4_routed_expert_03_gb300.layer import Layer, Plan, alloc_weights
 
-    n_exp = args.experts
+    n_exp = args.experts or N_EXPERTS
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -272,7 +302,7 @@ def run_ours(args):
     if args.tokens:
         wl["Ts"] = [args.tokens]
     path = args.path or wl["path"]
-    base = synth.WORKLOADS["decode1"] if args.workload.startswith("decode") else synth.WORKLOADS[args.workload]
+    base = base_workload(args.workload)
 
     # weights: the full layer, generated in HBM by the device half of the generator
     weights = alloc_weights(n_exp, D_MODEL, D_FF)
@@ -567,8 +597,11 @@ def run_ours(args):
                    "tokens_per_step": tokens_step, "active_experts_last_step": act,
                    "kernel_ms_per_call": breakdown,
                    **({"expert_cache": stream_info} if stream_info else {}),
-                   "l2": "inputs larger than L2 (>=280 MB of expert weights per batch, "
-                         "8 rotating logit sets)", "parallelism": f"replicas x{world}"},
+                   "l2": f"inputs larger than L2: a step reads {sum(act) * EXPERT_BYTES / 1e6:.0f} MB "
+                         f"of expert weights (L2 129 MB) before any batch recurs, and "
+                         f"{wl.get('sets', N_SETS)} rotating logit sets change the experts of "
+                         "each batch from step to step",
+                   "parallelism": f"replicas x{world}"},
         "roofline": roof,
         **({"profiling_case": f"{n_exp} experts, batches {wl['Ts']}; not a bench value"}
            if n_exp != N_EXPERTS or args.tokens else {}),
@@ -596,8 +629,9 @@ def run_ours(args):
 
 def main():
     args = parse_args()
+    use_shape(BENCH_WORKLOADS[args.workload])
     if args.steps is None:
-        args.steps = 1000 if args.workload == "decode" else 60
+        args.steps = 1000 if args.workload in ("decode", "mimo_decode") else 60
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

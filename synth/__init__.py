@@ -212,6 +212,10 @@ WORKLOADS = {
     "skewed8k": Workload("skewed8k", T=8192, D=7168, F=1536, E=896, k=16, zipf_s=1.1),
     "router16k": Workload("router16k", T=16384, D=7168, F=1536, E=896, k=16, router="xwr",
                           shared=True),
+    # MiMo V2.6 Flash lane: 256 experts, top-8 (d_model 4096, d_ff 2048: a
+    # reading, the hidden sizes are not stated)
+    "mimo_decode": Workload("mimo_decode", T=1, D=4096, F=2048, E=256, k=8),
+    "mimo_prefill4k": Workload("mimo_prefill4k", T=4096, D=4096, F=2048, E=256, k=8),
 }
 
 # Seeds of the per-call activation / logit draws (weights use Workload.seed).
