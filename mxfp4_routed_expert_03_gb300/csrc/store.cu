@@ -235,13 +235,10 @@ bool moe_store_job_shape(int D, int F, MoeStoreJob &j) {
 }
 
 cudaError_t moe_launch_store_decode(const MoeStoreJob &j, int nsm, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(moe_store_decode_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SD_SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    // set on every launch (a host-side call): per device and thread-safe
+    cudaError_t e = cudaFuncSetAttribute(moe_store_decode_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SD_SMEM);
+    if (e != cudaSuccess) return e;
     moe_store_decode_kernel<<<nsm, SD_WARPS * 32, SD_SMEM, st>>>(j);
     return cudaGetLastError();
 }
