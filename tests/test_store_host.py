@@ -88,3 +88,21 @@ def test_encoder_rejects_bad_arguments():
     with pytest.raises(m.MoeError):   # shape
         m.moe_store_encode(E, D, 100, hw, blob.ctypes.data, cap, tiles.ctypes.data,
                            tabs.ctypes.data)
+
+
+@pytest.mark.parametrize("D,F", [(32, 32), (96, 64), (32, 1024), (2048, 96), (288, 160)])
+def test_library_encoder_matches_oracle_on_irregular_shapes(D, F):
+    """Multiples of 32 that are not multiples of 128: arrays far below one
+    tile, scale arrays of a few dozen bytes, ragged last tiles."""
+    import mxfp4_routed_expert_03_gb300 as m
+    E = 3
+    w = _weights(E, D, F, synth.CODES_PEAKED, seed=21)
+    ref = S.build_store(w, E, D, F)
+    got = _encode(m, w, E, D, F, threads=2)
+    np.testing.assert_array_equal(got["tables"], ref["tables"])
+    np.testing.assert_array_equal(got["records"], ref["records"])
+    np.testing.assert_array_equal(got["blob"], ref["blob"])
+    back = S.decode_store(ref, E, D, F)
+    for a, nm in enumerate(S.NAMES):
+        want = S.canonical(w[nm]) if a % 2 == 0 else w[nm]
+        np.testing.assert_array_equal(back[nm], want.reshape(back[nm].shape))
