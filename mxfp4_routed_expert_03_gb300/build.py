@@ -60,7 +60,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(o)
     if force or jobs or _stale(LIB, objs):
         subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-shared",
-                               "-o", LIB, *objs, "-lcudart", "-lpthread"])
+                               "-o", LIB, *objs, "-lcudart", "-lpthread", "-ldl"])
     return LIB
 
 

@@ -3,10 +3,21 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
 #define MOE_API extern "C" __attribute__((visibility("default")))
+
+// NVTX range over one entry point (host side; shows each call in profiler
+// timelines, does nothing when no profiling tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 struct moe_handle {
     moe_desc desc;
@@ -325,6 +336,7 @@ MOE_API int moe_store_decode(int32_t n_experts, int32_t d_model, int32_t d_ff,
                              const moe_store *store, const int32_t *experts, const int32_t *slots,
                              int32_t n, const moe_weights *slot_w, int32_t n_slots, int32_t *status,
                              void *stream) {
+    NvtxRange nvtx_range("moe_store_decode");
     MoeStoreJob j;
     if (n_experts <= 0 || n_experts > MOE_MAX_EXPERTS || n < 0 || n_slots < 1 || !store ||
         !slot_w || !status || !moe_store_job_shape(d_model, d_ff, j))
@@ -511,6 +523,7 @@ static bool plan_ok(const moe_plan_buf *p) {
 
 MOE_API int moe_plan(moe_handle *h, int32_t T, const float *logits, const uint16_t *x,
                      const moe_plan_buf *plan, void *ws, size_t ws_bytes, void *stream) {
+    NvtxRange nvtx_range("moe_plan");
     if (!h || T < 0) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
     if (!plan_ok(plan)) return MOE_ERR_INVALID_ARG;
@@ -539,6 +552,7 @@ MOE_API int moe_plan(moe_handle *h, int32_t T, const float *logits, const uint16
 
 MOE_API int moe_router_logits(moe_handle *h, int32_t T, const uint16_t *x, float *logits,
                               void *stream) {
+    NvtxRange nvtx_range("moe_router_logits");
     if (!h || T < 0) return MOE_ERR_INVALID_ARG;
     if (h->desc.router_mode != MOE_ROUTER_XWR) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
@@ -550,6 +564,7 @@ MOE_API int moe_router_logits(moe_handle *h, int32_t T, const uint16_t *x, float
 
 MOE_API int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
                        uint16_t *out, void *ws, size_t ws_bytes, void *stream) {
+    NvtxRange nvtx_range("moe_decode");
     if (!h || T < 0) return MOE_ERR_INVALID_ARG;
     if (h->streaming) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
@@ -576,6 +591,7 @@ MOE_API int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_pl
 
 MOE_API int moe_decode_noalloc(moe_handle *h, int32_t T, const uint16_t *x,
                                const moe_plan_buf *plan, uint16_t *out, void *stream) {
+    NvtxRange nvtx_range("moe_decode_noalloc");
     if (!h || T < 0) return MOE_ERR_INVALID_ARG;
     if (h->streaming) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
@@ -600,6 +616,7 @@ MOE_API int moe_decode_noalloc(moe_handle *h, int32_t T, const uint16_t *x,
 
 MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *plan,
                         uint16_t *out, void *ws, size_t ws_bytes, void *stream) {
+    NvtxRange nvtx_range("moe_forward");
     if (!h || T < 0) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
     if (!x || !out || !plan_ok(plan)) return MOE_ERR_INVALID_ARG;
@@ -709,6 +726,7 @@ MOE_API size_t moe_prepared_bytes(const moe_handle *h) {
 }
 
 MOE_API int moe_prepare(moe_handle *h, void *buf, size_t bytes, void *stream) {
+    NvtxRange nvtx_range("moe_prepare");
     if (!h || !buf) return MOE_ERR_INVALID_ARG;
     if (bytes < moe_prepared_bytes(h)) return MOE_ERR_WORKSPACE;
     if ((uintptr_t)buf & 255u) return MOE_ERR_INVALID_ARG;
