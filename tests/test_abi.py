@@ -84,3 +84,25 @@ def test_null_handle_calls_are_rejected(L):
     assert L.moe_router_logits(None, 1, None, None) == L.MOE_ERR_INVALID_ARG
     assert L.moe_workspace_bytes(None, 16, L.MOE_OP_DECODE) == 0
     L.moe_destroy(None)
+
+
+def test_store_entry_points_check_arguments_on_the_host(L):
+    """Argument errors of the compressed-store calls come back before anything
+    reaches the device (these run without a GPU)."""
+    w = L.moe_weights()
+    st = L.moe_store(None, 0, None, None)
+    # decode: null status, bad shape, negative count; zero items is a no-op
+    assert L.moe_store_decode(4, 256, 128, st, None, None, 1, w, 1, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_store_decode(4, 256, 100, st, None, None, 1, w, 1, 1) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_store_decode(4, 256, 128, st, None, None, -1, w, 1, 1) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_store_decode(0, 256, 128, st, None, None, 1, w, 1, 1) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_store_decode(4, 256, 128, st, None, None, 0, w, 1, 1) == L.MOE_OK
+    assert L.moe_store_decode(4, 256, 128, st, None, None, 1, w, 1, 1) == L.MOE_ERR_INVALID_ARG
+    # streaming from a store: null store arrays, bad slot counts
+    desc = L.moe_desc(256, 128, 8, 2, 0, 0)
+    with pytest.raises(L.MoeError):
+        L.moe_create_streaming_store(desc, st, w, 4, 16)
+    for n_slots in (0, 9):
+        with pytest.raises(L.MoeError):
+            L.moe_create_streaming_store(desc, st, w, n_slots, 16)
+    assert L.moe_strerror(L.MOE_ERR_CORRUPT_TILE) == "a compressed-store tile failed its checks"
