@@ -235,7 +235,8 @@ int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_plan_buf *
  * which loads the library holds until the process exits). It fits T * top_k
  * <= 256 routed rows for d_ff <= 2048 and d_model <= 8192; larger calls
  * return MOE_ERR_WORKSPACE. The first call on a device looks up the array's
- * device address (cudaGetSymbolAddress), so make that first call before any
+ * device address (cudaGetSymbolAddress; again after the device's context
+ * changed, e.g. after cudaDeviceReset), so make that first call before any
  * stream capture. All calls share the array: calls whose kernels overlap on
  * the GPU (other streams, other threads) race on it and must be serialised by
  * the caller. Same inputs, outputs and results as moe_decode; the plan comes
@@ -392,6 +393,29 @@ int moe_create_streaming_store(const moe_desc *desc, const moe_store *store,
  * and ev_stop immediately after it, on the call's stream. The caller owns the
  * events and may swap them between calls; MOE_PROF_NONE turns it off. */
 int moe_profile_kernel(moe_handle *h, int32_t which, void *ev_start, void *ev_stop);
+
+/* Test hooks for the device-side timeout path. Every wait inside the
+ * library's kernels is bounded; when one runs out the kernel records
+ * MOE_ERR_DEVICE_TIMEOUT, stops its work, waits (bounded) for its own copies
+ * and MMAs in flight, releases its tensor memory and returns, so the context
+ * stays usable and the next call runs normally. The pages' counterpart is a
+ * system that refuses or reports rather than half-running or hanging
+ * (Moonshine GitHub README, MiMo section: memory guards and request
+ * deadlines; MeshMoE Cell page: failure detection); they describe no such
+ * hook. Off by default; meant for tests only. */
+enum moe_inject {
+    MOE_INJECT_NONE = 0,
+    MOE_INJECT_GEMM_STALL = 1  /* moe_forward's gate/up GEMM: in every CTA the first MMA issuer
+                                  waits on a barrier that nothing signals, so that wait runs
+                                  out with operand copies in flight */
+};
+
+/* Host. Sets the handle's injection mode (enum moe_inject) and the limit of
+ * every device-side wait of its later calls, in SM clock cycles
+ * (timeout_cycles <= 0: the default, 2e9 cycles, about one second; otherwise
+ * at least 1e5). Returns MOE_ERR_INVALID_ARG for an unknown mode or a limit
+ * below 1e5. */
+int moe_set_fault_injection(moe_handle *h, int32_t mode, int64_t timeout_cycles);
 
 /* Host. Synchronises `stream`, returns the first device-side error recorded
  * since the last call (MOE_OK if none) and clears it. */

@@ -39,7 +39,10 @@ EXPORTS = ("moe_create", "moe_destroy", "moe_expert_bytes", "moe_prepared_bytes"
            "moe_decode_noalloc", "moe_stream_state_bytes", "moe_create_streaming",
            "moe_stream_stats", "moe_store_tiles_per_expert", "moe_store_blob_bound",
            "moe_store_encode", "moe_store_decode", "moe_create_streaming_store",
-           "moe_profile_kernel", "moe_status", "moe_strerror")
+           "moe_profile_kernel", "moe_set_fault_injection", "moe_status", "moe_strerror")
+
+MOE_INJECT_NONE = 0
+MOE_INJECT_GEMM_STALL = 1
 
 MOE_PROF_NONE = 0
 MOE_PROF_DECODE_GATEUP = 1
@@ -123,6 +126,8 @@ def lib() -> ctypes.CDLL:
         L.moe_decode_noalloc.restype = ctypes.c_int
         L.moe_profile_kernel.argtypes = [p, i32, p, p]
         L.moe_profile_kernel.restype = ctypes.c_int
+        L.moe_set_fault_injection.argtypes = [p, i32, i64]
+        L.moe_set_fault_injection.restype = ctypes.c_int
         L.moe_status.argtypes = [p, p]
         L.moe_status.restype = ctypes.c_int
         L.moe_strerror.argtypes = [ctypes.c_int]
@@ -301,6 +306,11 @@ def moe_profile_kernel(h, which: int, ev_start=None, ev_stop=None) -> int:
 def moe_decode_noalloc(h, T, x, plan: moe_plan_buf, out, stream=None) -> int:
     """moe_decode with the library's fixed scratch (no workspace argument)."""
     return lib().moe_decode_noalloc(h, T, _ptr(x), ctypes.byref(plan), _ptr(out), _stream(stream))
+
+
+def moe_set_fault_injection(h, mode: int, timeout_cycles: int = 0) -> int:
+    """Test hook: injection mode (MOE_INJECT_*) and device-wait limit in SM cycles (0: default)."""
+    return lib().moe_set_fault_injection(h, mode, timeout_cycles)
 
 
 def moe_status(h, stream=None) -> int:

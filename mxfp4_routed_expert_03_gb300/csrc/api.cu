@@ -37,6 +37,8 @@ struct moe_handle {
     void *sstate;          // streaming: device cache state (moe_stream_state_bytes)
     bool from_store;       // streaming from a compressed store (store) instead of host_w
     moe_store store;
+    long long timeout;     // limit of every device-side wait (SM clock cycles)
+    int inject;            // enum moe_inject (test hook; MOE_INJECT_NONE by default)
 };
 
 // Device-side waits give up after this many SM clocks (about one second).
@@ -201,6 +203,8 @@ static int create_impl(const moe_desc *d, const moe_weights *w, int wE, moe_hand
     h->w = *w;
     h->wE = wE;
     h->device = dev;
+    h->timeout = kTimeoutCycles;
+    h->inject = MOE_INJECT_NONE;
     if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         free(h);
         return MOE_ERR_CUDA;
@@ -455,7 +459,7 @@ static MoeDenseArgs dense_args(const moe_handle *h, int M, int N, int K, int ldo
     a.K = K;
     a.ldo = ldo;
     a.status = h->status;
-    a.timeout_cycles = kTimeoutCycles;
+    a.timeout_cycles = h->timeout;
     return a;
 }
 
@@ -667,7 +671,8 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     a.tt_prefix = prefix;
     a.topk_w = plan->topk_w;
     a.status = h->status;
-    a.timeout_cycles = kTimeoutCycles;
+    a.timeout_cycles = h->timeout;
+    a.inject = MOE_INJECT_NONE;
     if (h->streaming) {  // experts resident first; the GEMMs then address their slots
         if (err == cudaSuccess) err = stream_fill(h, plan, st);
         a.w_index = moe_stream_view(h->sstate, E, h->wE).slot_of;
@@ -684,6 +689,7 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         g1.b_atoms = xa;
         g1.h_tiles = hb;
         g1.h_atoms = ha;
+        g1.inject = h->inject;
         h->prof.before(MOE_PROF_FORWARD_GEMM1, st);
         err = moe_launch_gemm(MOE_GEMM_GATEUP, &h->map_gate, &h->map_up, &g1, T, h->num_sms, st);
         h->prof.after(MOE_PROF_FORWARD_GEMM1, st);
@@ -765,6 +771,14 @@ MOE_API int moe_profile_kernel(moe_handle *h, int32_t which, void *ev_start, voi
     h->prof.which = which;
     h->prof.start = (cudaEvent_t)ev_start;
     h->prof.stop = (cudaEvent_t)ev_stop;
+    return MOE_OK;
+}
+
+MOE_API int moe_set_fault_injection(moe_handle *h, int32_t mode, int64_t timeout_cycles) {
+    if (!h || (mode != MOE_INJECT_NONE && mode != MOE_INJECT_GEMM_STALL)) return MOE_ERR_INVALID_ARG;
+    if (timeout_cycles > 0 && timeout_cycles < 100000) return MOE_ERR_INVALID_ARG;
+    h->inject = mode;
+    h->timeout = timeout_cycles > 0 ? (long long)timeout_cycles : kTimeoutCycles;
     return MOE_OK;
 }
 

@@ -44,7 +44,7 @@ struct DCfg {
     static constexpr int EPI_BYTES = (EPI == MOE_DENSE_SWIGLU) ? 16 * 64 * 4 : 0;
     static constexpr int SMEM = 1024 + EPI_BASE + EPI_BYTES;
     static_assert(STAGE % 1024 == 0, "stage alignment (128-byte swizzle atoms)");
-    static_assert((2 * S + 4) * 8 + 8 <= 256, "barrier area");
+    static_assert((2 * S + 5) * 8 + 12 <= 256, "barrier area");
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert(DN % 16 == 0 && DN <= 256 && 2 * DN <= (int)DTMEM_COLS, "tile width");
 };
@@ -83,11 +83,14 @@ __global__ void __launch_bounds__(DTHREADS, 1) moe_dense_gemm_kernel(
     uint64_t *empty = full + C::S;
     uint64_t *tfull = empty + C::S;
     uint64_t *tempty = tfull + 2;
-    uint32_t *tmem_slot = (uint32_t *)(tempty + 2);
+    uint64_t *drain = tempty + 2;  // the issuer's MMAs in flight, waited on when giving up
+    uint32_t *tmem_slot = (uint32_t *)(drain + 1);
     int *abort_flag = (int *)(tmem_slot + 1);
+    int *s_issued = abort_flag + 1;  // stages the producer filled
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         *abort_flag = 0;
+        *s_issued = 0;
         for (int s = 0; s < C::S; ++s) {
             tc::mbar_init(&full[s], 1);
             tc::mbar_init(&empty[s], 1);
@@ -96,6 +99,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) moe_dense_gemm_kernel(
             tc::mbar_init(&tfull[b], 1);
             tc::mbar_init(&tempty[b], 4);
         }
+        tc::mbar_init(drain, 1);
         tc::fence_mbar_init();
     }
     if (warp == 1) {
@@ -124,7 +128,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) moe_dense_gemm_kernel(
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const int mt = tile % MT, nt = tile / MT;
-                for (int kc = 0; kc < KC; ++kc, ++it) {
+                for (int kc = 0; kc < KC; ++kc) {
                     const int s = it % C::S, round = it / C::S;
                     if (round > 0 && !tc::mbar_wait(&empty[s], (round - 1) & 1, LIMIT, abort_p)) {
                         fail();
@@ -134,6 +138,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) moe_dense_gemm_kernel(
                     unsigned char *st = smem + s * C::STAGE;
                     tc::mbar_arrive_expect_tx(&full[s],
                                               (uint32_t)(C::NTERMS * D_A_BYTES + D_B_BYTES));
+                    ++it;  // a fill of this stage is now in flight
                     const int row0 = mt * C::MROWS;
                     tc::tma_load_2d(st, &mA0, &full[s], kc * DK, row0, pol);
                     if (EPI == MOE_DENSE_SWIGLU)  // the matching up rows under the gate rows
@@ -142,6 +147,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) moe_dense_gemm_kernel(
                                     pol);
                 }
             }
+            *s_issued = it;
         }
     } else if (warp == 2) {
         if (lane == 0) {
@@ -182,6 +188,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) moe_dense_gemm_kernel(
             }
             // the last MMAs must finish before the CTA releases TMEM
             if (ok && last && !tc::mbar_wait(last, last_par, LIMIT, abort_p)) fail();
+            if (!ok || *abort_p) tc::drain_mmas(drain, LIMIT);
         }
         __syncwarp();
     } else if (warp >= 3) {
@@ -243,6 +250,8 @@ __global__ void __launch_bounds__(DTHREADS, 1) moe_dense_gemm_kernel(
             if (lane == 0) tc::mbar_arrive(&tempty[buf]);
         }
     }
+    __syncthreads();
+    if (*abort_p && tid == 0) tc::wait_issued_fills(full, C::S, *s_issued, LIMIT);
     tc::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -280,11 +289,15 @@ __global__ void __launch_bounds__(RTHREADS, 1) moe_router_gemm_kernel(
     uint64_t *empty = full + R_S;
     uint64_t *cfull = empty + R_S;  // chunk accumulator c % 2 holds chunk c
     uint64_t *cempty = cfull + 2;
-    uint32_t *tmem_slot = (uint32_t *)(cempty + 2);
+    uint64_t *drain = cempty + 2;  // the issuer's MMAs in flight, waited on when giving up
+    uint32_t *tmem_slot = (uint32_t *)(drain + 1);
     int *abort_flag = (int *)(tmem_slot + 1);
+    int *s_issued = abort_flag + 1;  // stages the producer filled
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         *abort_flag = 0;
+        *s_issued = 0;
+        tc::mbar_init(drain, 1);
         for (int s = 0; s < R_S; ++s) {
             tc::mbar_init(&full[s], 1);
             tc::mbar_init(&empty[s], 1);
@@ -318,7 +331,7 @@ __global__ void __launch_bounds__(RTHREADS, 1) moe_router_gemm_kernel(
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const int mt = tile % MT, nt = tile / MT;
-                for (int kc = 0; kc < KC; ++kc, ++it) {
+                for (int kc = 0; kc < KC; ++kc) {
                     const int s = it % R_S, round = it / R_S;
                     if (round > 0 && !tc::mbar_wait(&empty[s], (round - 1) & 1, LIMIT, abort_p)) {
                         fail();
@@ -327,12 +340,14 @@ __global__ void __launch_bounds__(RTHREADS, 1) moe_router_gemm_kernel(
                     }
                     unsigned char *st = smem + s * R_STAGE;
                     tc::mbar_arrive_expect_tx(&full[s], (uint32_t)R_STAGE);
+                    ++it;  // a fill of this stage is now in flight
                     tc::tma_load_2d(st, &mT0, &full[s], kc * DK, mt * 128, pol);
                     tc::tma_load_2d(st + D_A_BYTES, &mT1, &full[s], kc * DK, mt * 128, pol);
                     tc::tma_load_2d(st + 2 * D_A_BYTES, &mT2, &full[s], kc * DK, mt * 128, pol);
                     tc::tma_load_2d(st + 3 * D_A_BYTES, &mX, &full[s], kc * DK, nt * DN, pol);
                 }
             }
+            *s_issued = it;
         }
     } else if (warp == 2) {
         if (lane == 0) {
@@ -373,6 +388,7 @@ __global__ void __launch_bounds__(RTHREADS, 1) moe_router_gemm_kernel(
             }
             // the last MMAs must finish before the CTA releases TMEM
             if (ok && last && !tc::mbar_wait(last, last_par, LIMIT, abort_p)) fail();
+            if (!ok || *abort_p) tc::drain_mmas(drain, LIMIT);
         }
         __syncwarp();
     } else if (warp >= 3) {
@@ -423,6 +439,8 @@ __global__ void __launch_bounds__(RTHREADS, 1) moe_router_gemm_kernel(
             }
         }
     }
+    __syncthreads();
+    if (*abort_p && tid == 0) tc::wait_issued_fills(full, R_S, *s_issued, LIMIT);
     tc::tc_fence_before();
     __syncthreads();
     if (warp == 1) {

@@ -23,19 +23,16 @@
 //     A tile (two 64-row TMA boxes), so one MMA per 32-wide K step covers
 //     gate and up; the epilogue pairs TMEM lanes r and 64 + r.
 //
-// Wide-variant CTAs run in clusters of CL = 2 on neighbouring SMs. The two CTAs of a
-// cluster take adjacent weight tiles of the same expert and token tile, so
-// they consume identical activation chunks: each CTA fetches half of every
-// chunk and multicasts it into both CTAs' shared memory, halving the L2
-// traffic of the activation operand; each CTA's MMA completion is multicast
-// to both CTAs' release barriers, so a stage is refilled only once both have
-// consumed it.
+// Every CTA runs alone (no clusters): it fetches the whole activation chunk
+// of its tile into its own shared memory and releases each stage with one
+// local commit. The CTAs that work on one expert's token tile at the same
+// time take adjacent weight tiles, so the activation chunk they all read is
+// served from L2 after the first fetch.
 //
 // Two tile widths (template NT): the wide variant (112 token rows) for
 // prefill, with 2-stage rings; the narrow variant (16 rows, chosen when no
-// expert has more rows) with 5-stage rings, two MMA issuers and no cluster
-// (its CTAs load their own small activation tiles and release a stage with
-// one local commit). A pipeline stage carries two 128-wide K blocks; data
+// expert has more rows) with 5-stage rings and two MMA issuers. A pipeline
+// stage carries two 128-wide K blocks; data
 // layouts stay per K block. With expert streaming the weight producer
 // addresses the expert's slot (args.w_index).
 //
@@ -49,13 +46,14 @@
 //   warp 2      MMA issuer (one thread): tcgen05.cp scales, tcgen05.mma
 //   warps 3-6   epilogue, one 32-lane TMEM quadrant each
 //   warp 7      (narrow) second MMA issuer
-// One "full" barrier per stage serves both operand rings when they are
-// equally deep (the cluster peer's multicast bytes complete on it too);
-// releases are one local barrier per stage without a cluster, or a local
-// weight release plus a cluster-wide activation release with one. The
-// accumulator is double-buffered in TMEM so the epilogue of tile i overlaps
-// the MMAs of tile i+1. Every wait is bounded: on expiry the CTA records
-// MOE_ERR_DEVICE_TIMEOUT, drains its MMAs and winds down.
+// One "full" barrier per stage serves both operand rings (both producers
+// arrive on it) and one "empty" barrier per stage releases it (one commit of
+// the issuer that consumed it). The accumulator is double-buffered in TMEM so
+// the epilogue of tile i overlaps the MMAs of tile i+1. Every wait is
+// bounded: on expiry the CTA records MOE_ERR_DEVICE_TIMEOUT, each issuer
+// drains its MMAs, and before the CTA leaves it waits (bounded) for every
+// operand copy it issued to land, so nothing writes into shared memory the
+// CTA no longer owns.
 #include "common.cuh"
 #include "kernels.h"
 #include "mx8.cuh"
@@ -80,7 +78,14 @@ constexpr int BSF_BYTES = 1024;          // activation scales of one chunk (256 
 // (narrow: read into tensor memory by 32x128b.warpx4 copies, which fill every
 // lane quadrant) or once per lane quadrant (wide: one 128x256b copy reads
 // all four, fewer instructions for the single issuer).
-template <int MODE, int NT>
+//
+// FP4 selects the FP4 x FP4 mode (kind::mxf4): the activations are one MXFP4
+// term (E2M1 with an E8M0 scale per 32) instead of two E4M3 terms, and both
+// operands stay packed in shared memory, two elements per byte, so a stage's
+// two K blocks are one 128-byte row per weight or token row and one MMA
+// covers 64 K. A stage is half the bytes of the E4M3 path, so the rings are
+// deeper.
+template <int MODE, int NT, bool FP4>
 struct Cfg {
     static constexpr bool NARROW = NT <= 16;
     // MMA-issuing warps. One thread issues a block-scaled MMA every ~90 cycles
@@ -90,14 +95,15 @@ struct Cfg {
     // into its own accumulator, and the epilogue adds the two.
     static constexpr int NSPLIT = NARROW ? 2 : 1;
     static constexpr int THREADS = 224 + 32 * (NSPLIT - 1);  // warp 7: second issuer
-    static constexpr uint32_t ACC_COLS = 2 * NT;             // [hi | lo] columns of one accumulator
+    static constexpr int TERMS = FP4 ? 1 : 2;  // activation terms stacked along N
+    static constexpr uint32_t ACC_COLS = TERMS * NT;         // [hi | lo] columns of one accumulator
     static constexpr uint32_t BUF_COLS = NSPLIT * ACC_COLS;  // one of two accumulator buffers
     static constexpr uint32_t SF_TMEM_COL = 2 * BUF_COLS;    // then 2 scale slots per issuer
     static constexpr uint32_t TMEM_COLS = NARROW ? 256 : 512;
     // K blocks per pipeline stage: each wait, commit and loop step of an
-    // issuer is shared by 8 MMAs. (Single-block stages with deeper rings
-    // measured slower for the wide variant: the issuer's per-stage waits cost
-    // more than the extra depth returned.)
+    // issuer is shared by 8 MMAs (4 in the FP4 mode). (Single-block stages
+    // with deeper rings measured slower for the wide variant: the issuer's
+    // per-stage waits cost more than the extra depth returned.)
     static constexpr int KS = 2;
     static constexpr uint32_t SF_SLOT = KS * 12;  // per stage: A 4 columns per block, then B 8
     // Copies of each scale block in smem: four let one 128x256b copy fill all
@@ -106,42 +112,40 @@ struct Cfg {
     // is bound by shared-memory traffic (E2M1 tiles land expanded to 8 bits,
     // and every 128 x 32 MMA reads 4 KB of weights and 1 KB of tokens), so
     // it keeps one copy of each block and fills the lane quadrants with
-    // 32x128b.warpx4 copies.
-    static constexpr int SCALE_REP_A = NARROW ? 1 : 4;
-    static constexpr int SCALE_REP_B = NARROW ? 1 : 4;
+    // 32x128b.warpx4 copies. The FP4 mode issues half the MMAs per stage and
+    // spends the room of the extra copies on ring depth.
+    static constexpr int SCALE_REP_A = (NARROW || FP4) ? 1 : 4;
+    static constexpr int SCALE_REP_B = (NARROW || FP4) ? 1 : 4;
     static_assert(SF_TMEM_COL + 2 * NSPLIT * SF_SLOT <= TMEM_COLS, "tensor memory budget");
     static constexpr int MROWS = (MODE == MOE_GEMM_GATEUP) ? 64 : 128;  // weight rows per tile
-    // CTAs per cluster sharing (multicasting) the activation tile. The wide
-    // variant's 64 KB activation stages are worth sharing; the narrow
-    // variant's 10 KB are not worth the cluster-wide release, whose
-    // multicast commit costs the issuing thread several hundred cycles per
-    // stage (measured), so narrow CTAs run alone.
-    static constexpr int CL = NARROW ? 1 : MOE_GEMM_CLUSTER;
-    static constexpr uint16_t CL_MASK = (uint16_t)((1u << CL) - 1);
-    static constexpr int SA = NARROW ? 5 : 2;  // weight ring stages (KS blocks each)
+    // ring stages (KS blocks each)
+    static constexpr int SA = NARROW ? (FP4 ? 10 : 5) : (FP4 ? 6 : 2);
     static constexpr int SB = SA;              // activation ring stages
-    static constexpr bool MERGED = SA == SB;   // one full barrier per stage for both operands
-    static constexpr int A_STAGE = KS * A_BYTES + SCALE_REP_A * SF_BYTES;  // tiles, then scales
-    static constexpr int A_SF = KS * A_BYTES;
-    static constexpr int B_BYTES = 2 * NT * BK;  // smem bytes of [hi; lo] activation rows
-    static constexpr int B_STAGE = KS * (B_BYTES + SCALE_REP_B * BSF_BYTES);  // tiles, then scales
+    // one full barrier per stage for both operands (both producers arrive)
+    // and one release barrier per stage (one commit)
+    static constexpr bool MERGED = SA == SB;
+    static_assert(MERGED, "the rings share their barriers");
+    // weight tile of a stage in shared memory: FP4 packed 128-byte rows, else
+    // one 128 x 128-byte tile per K block (E2M1 expanded to 8-bit containers)
+    static constexpr int A_TILE = FP4 ? 128 * 128 : KS * A_BYTES;
+    static constexpr int A_STAGE = A_TILE + SCALE_REP_A * SF_BYTES;  // tiles, then scales
+    static constexpr int A_SF = A_TILE;
+    static constexpr int B_BYTES = 2 * NT * BK;  // smem bytes of one K block's [hi; lo] rows
+    // activation tile of a stage: FP4 one 128-byte row per token, else [hi; lo]
+    // rows per K block
+    static constexpr int B_TILE = FP4 ? NT * 128 : KS * B_BYTES;
+    static constexpr int B_STAGE = B_TILE + KS * SCALE_REP_B * BSF_BYTES;  // tiles, then scales
     static constexpr int B_BASE = SA * A_STAGE;
-    static constexpr int B_SF = KS * B_BYTES;
+    static constexpr int B_SF = B_TILE;
     static constexpr int BAR_BASE = B_BASE + SB * B_STAGE;
-    static constexpr int N_FULL = MERGED ? SA : SA + SB;
-    // Without a cluster, merged rings also share one release barrier per
-    // stage (one commit). In a cluster the weight ring keeps a local release
-    // so that a CTA refills its own weights without waiting for its peer
-    // (measured faster for the wide variant than one shared release).
-    static constexpr bool SHARED_EMPTY = MERGED && CL == 1;
-    static constexpr int N_EMPTY = SHARED_EMPTY ? SA : SA + SB;
-    // two issuers order their full waits by the one release of each stage
-    static_assert(NSPLIT == 1 || SHARED_EMPTY, "split issue needs one release barrier per stage");
+    static constexpr int N_FULL = SA;
+    static constexpr int N_EMPTY = SA;
     // full(s), empty(s); tfull, tempty x2; one drain barrier per issuer
     static constexpr int N_BARS = N_FULL + N_EMPTY + 4 + NSPLIT;
+    // after the barriers: TMEM address, abort flag, fills issued by each producer
     // Tile lookup. Wide: shared-memory copies of the token-tile prefix, the
     // active experts and their row segments (NTAB entries). Narrow: every
-    // expert has one token tile, so tile ct is active expert ct / MTG; the
+    // expert has one token tile, so tile ct is active expert ct / MT; the
     // CTA's own tiles are decoded once into a list of TLIST entries (direct
     // loads from the plan past that), which frees the room for a 5th stage.
     static constexpr int NTAB = NARROW ? 0 : MOE_MAX_EXPERTS;
@@ -155,7 +159,8 @@ struct Cfg {
     static constexpr int EPI_BYTES = (MODE == MOE_GEMM_GATEUP) ? 16 * 64 * 4 : 4 * 16 * 32 * 4;
     static constexpr int SMEM = 1024 + EPI_BASE + EPI_BYTES;
     static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0, "stages must keep 1 KB alignment");
-    static_assert(NARROW || SCALE_REP_B == 4, "wide tiles need B scale columns 0..7");
+    static_assert(NARROW || FP4 || SCALE_REP_B == 4, "wide two-term tiles need B scale columns 0..7");
+    static_assert(TERMS * NT <= 128 || SCALE_REP_B == 4, "B rows past 127 need the 128x256b copy");
     static_assert(BAR_BASE % 8 == 0 && PREFIX_BASE % 16 == 0 && EXPERT_BASE % 16 == 0 &&
                       SEG_BASE % 16 == 0 && EPI_BASE % 16 == 0,
                   "shared-memory regions must be 16-byte aligned (int2 / float4 accesses)");
@@ -171,21 +176,19 @@ struct Tile {
     int tt;     // global token-tile index (activation / h scale atoms)
 };
 
-// Cluster tile `ct` of the schedule: active expert a owns MTG * ntt(a)
-// consecutive cluster tiles (weight tile group major, token tile minor); the
-// CTA of cluster rank `rank` takes weight tile mg * CL + rank of the group.
-// s_prefix, s_expert and s_seg are the shared-memory copies of the token-tile
-// prefix, the active experts and their (first slot, rows) segments. Each
-// role visits its tiles in increasing order, so `a` (the caller's cursor,
-// starting at 0) only moves forward: a few shared-memory reads per tile.
-template <int NT, int CL>
-__device__ __forceinline__ bool tile_at(int ct, int n_active, int MTG, int rank,
-                                        const int *s_prefix, const int *s_expert,
-                                        const int2 *s_seg, int &a, Tile &t) {
-    while (a + 1 < n_active && MTG * s_prefix[a + 1] <= ct) ++a;  // last a with MTG*prefix[a] <= ct
+// Tile `ct` of the schedule: active expert a owns MT * ntt(a) consecutive
+// tiles (weight tile major, token tile minor). s_prefix, s_expert and s_seg
+// are the shared-memory copies of the token-tile prefix, the active experts
+// and their (first slot, rows) segments. Each role visits its tiles in
+// increasing order, so `a` (the caller's cursor, starting at 0) only moves
+// forward: a few shared-memory reads per tile.
+template <int NT>
+__device__ __forceinline__ bool tile_at(int ct, int n_active, int MT, const int *s_prefix,
+                                        const int *s_expert, const int2 *s_seg, int &a, Tile &t) {
+    while (a + 1 < n_active && MT * s_prefix[a + 1] <= ct) ++a;  // last a with MT*prefix[a] <= ct
     const int ntt = s_prefix[a + 1] - s_prefix[a];
     if (ntt <= 0 || s_expert[a] < 0) return false;
-    const int local = ct - MTG * s_prefix[a];
+    const int local = ct - MT * s_prefix[a];
     const int mg = local / ntt, j = local % ntt;
     const int2 seg = s_seg[a];
     // token rows of the expert split evenly over its ntt tiles (32-bit
@@ -194,7 +197,7 @@ __device__ __forceinline__ bool tile_at(int ct, int n_active, int MTG, int rank,
     const int r0 = p1 <= 0x7FFFFFFFLL ? (int)p0 / ntt : (int)(p0 / ntt);
     const int r1 = p1 <= 0x7FFFFFFFLL ? (int)p1 / ntt : (int)(p1 / ntt);
     t.e = s_expert[a];
-    t.mt = mg * CL + rank;
+    t.mt = mg;
     t.s0 = seg.x + r0;
     t.n = r1 - r0;
     t.nmma = (t.n + 15) & ~15;
@@ -204,14 +207,13 @@ __device__ __forceinline__ bool tile_at(int ct, int n_active, int MTG, int rank,
 
 // Narrow tiles: tile ct of this CTA (the i-th it visits) from the CTA's tile
 // list (x = expert | rows << 22, y = first slot; x < 0 when invalid) or, past
-// the list, straight from the plan. Active expert a = ct / MTG owns tiles
-// a * MTG .. a * MTG + MTG - 1, one per weight tile group.
-template <int NT, int CL, int TLIST>
-__device__ __forceinline__ bool tile_at_list(int ct, int cluster_id, int n_clusters, int MTG,
-                                             int rank, const int2 *s_list, const MoeGemmArgs &args,
-                                             Tile &t) {
-    const int a = ct / MTG, mg = ct - a * MTG;
-    const int i = (ct - cluster_id) / n_clusters;
+// the list, straight from the plan. Active expert a = ct / MT owns tiles
+// a * MT .. a * MT + MT - 1, one per weight tile.
+template <int NT, int TLIST>
+__device__ __forceinline__ bool tile_at_list(int ct, int MT, const int2 *s_list,
+                                             const MoeGemmArgs &args, Tile &t) {
+    const int a = ct / MT, mg = ct - a * MT;
+    const int i = (ct - (int)blockIdx.x) / (int)gridDim.x;
     int e, sb, cnt;
     if (i < TLIST) {
         const int2 v = s_list[i];
@@ -227,7 +229,7 @@ __device__ __forceinline__ bool tile_at_list(int ct, int cluster_id, int n_clust
         if (sb < 0 || sb + cnt > args.n_rows) return false;
     }
     t.e = e;
-    t.mt = mg * CL + rank;
+    t.mt = mg;
     t.s0 = sb;
     t.n = cnt;
     t.nmma = (cnt + 15) & ~15;
@@ -250,22 +252,21 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" :::
 }  // namespace
 
 template <int MODE, int NT>
-__global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_kernel(
+__global__ void __launch_bounds__(Cfg<MODE, NT, false>::THREADS, 1) moe_grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
     const MoeGemmArgs args) {
-    using C = Cfg<MODE, NT>;
+    using C = Cfg<MODE, NT, false>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t *fullA = (uint64_t *)(smem + C::BAR_BASE);
-    uint64_t *fullB = C::MERGED ? fullA : fullA + C::SA;
-    uint64_t *emptyA = fullA + C::N_FULL;
-    uint64_t *emptyB = C::SHARED_EMPTY ? emptyA : emptyA + C::SA;
-    uint64_t *tfull = emptyA + C::N_EMPTY;
+    uint64_t *full = (uint64_t *)(smem + C::BAR_BASE);  // both operands of stage s landed
+    uint64_t *empty = full + C::N_FULL;                  // stage s consumed
+    uint64_t *tfull = empty + C::N_EMPTY;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;  // per issuer: its MMAs in flight, waited on when giving up
     uint32_t *tmem_slot = (uint32_t *)(drain + C::NSPLIT);
     int *abort_flag = (int *)(tmem_slot + 1);
+    int *s_issued = abort_flag + 1;  // stages filled by the weight [0] / activation [1] producer
     int *s_prefix = (int *)(smem + C::PREFIX_BASE);
     int *s_expert = (int *)(smem + C::EXPERT_BASE);
     int2 *s_seg = (int2 *)(smem + C::SEG_BASE);
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
     const int E = args.E;
     int n_active = args.active[0];
     if (n_active < 0 || n_active > E) n_active = 0;
-    if (C::NARROW) {  // this CTA's tiles: ct = blockIdx.x + i * gridDim.x (no cluster)
+    if (C::NARROW) {  // this CTA's tiles: ct = blockIdx.x + i * gridDim.x
         const long long n_tiles = (long long)n_active * args.MT;
         for (int i = tid; i < C::TLIST; i += C::THREADS) {
             const long long ct = (long long)blockIdx.x + (long long)i * gridDim.x;
@@ -308,13 +309,10 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
     }
     if (tid == 0) {
         *abort_flag = 0;
+        s_issued[0] = s_issued[1] = 0;
         for (int s = 0; s < C::SA; ++s) {
-            tc::mbar_init(&fullA[s], C::MERGED ? 2 : 1);  // merged: both producers arrive
-            tc::mbar_init(&emptyA[s], 1);
-        }
-        for (int s = 0; s < C::SB; ++s) {
-            if (!C::MERGED) tc::mbar_init(&fullB[s], 1);
-            if (!C::SHARED_EMPTY) tc::mbar_init(&emptyB[s], C::CL);  // every CTA of the cluster
+            tc::mbar_init(&full[s], 2);  // both producers arrive
+            tc::mbar_init(&empty[s], 1);
         }
         for (int i = 0; i < C::NSPLIT; ++i) tc::mbar_init(&drain[i], 1);
         for (int b = 0; b < 2; ++b) {
@@ -329,22 +327,16 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
     }
     tc::tc_fence_before();
     __syncthreads();
-    tc::cluster_sync();  // peers' barriers are initialised before any multicast lands
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    constexpr int CL = C::CL;
-    constexpr uint16_t CL_MASK = C::CL_MASK;
-    const int MT = args.MT, KC = args.KC, MTG = MT / CL;
-    const int rank = CL > 1 ? (int)tc::cluster_ctarank() : 0;
-    const int cluster_id = blockIdx.x / CL, n_clusters = gridDim.x / CL;
+    const int MT = args.MT, KC = args.KC;
     const int total_tiles =
-        n_active <= 0 ? 0 : (C::NARROW ? n_active * MTG : s_prefix[n_active] * MTG);
+        n_active <= 0 ? 0 : (C::NARROW ? n_active * MT : s_prefix[n_active] * MT);
     auto get_tile = [&](int ct, int &cur, Tile &t) -> bool {
         if constexpr (C::NARROW)
-            return tile_at_list<NT, CL, C::TLIST>(ct, cluster_id, n_clusters, MTG, rank, s_list,
-                                                  args, t);
+            return tile_at_list<NT, C::TLIST>(ct, MT, s_list, args, t);
         else
-            return tile_at<NT, CL>(ct, n_active, MTG, rank, s_prefix, s_expert, s_seg, cur, t);
+            return tile_at<NT>(ct, n_active, MT, s_prefix, s_expert, s_seg, cur, t);
     };
     const long long LIMIT = args.timeout_cycles;
     volatile int *abort_p = abort_flag;
@@ -360,7 +352,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
             int it = 0;
             bool ok = true;
             int cur = 0;
-            for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
                 Tile t;
                 if (!get_tile(tile, cur, t)) {
                     moe_flag(args.status, MOE_ERR_BAD_INDEX);
@@ -376,30 +368,32 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                 }
                 const int row0 = we * args.M + t.mt * C::MROWS;
                 const size_t atom0 = ((size_t)we * MT + t.mt) * ((KC + ATOM_BLOCKS - 1) / ATOM_BLOCKS);
-                for (int kc = 0; kc < KC; kc += C::KS, ++it) {
+                for (int kc = 0; kc < KC; kc += C::KS) {
                     const int s = it % C::SA, round = it / C::SA;
                     const int nsub = min(C::KS, KC - kc);
-                    if (round > 0 && !tc::mbar_wait(&emptyA[s], (round - 1) & 1, LIMIT, abort_p)) {
+                    if (round > 0 && !tc::mbar_wait(&empty[s], (round - 1) & 1, LIMIT, abort_p)) {
                         fail();
                         ok = false;
                         break;
                     }
                     unsigned char *st = smem + s * C::A_STAGE;
-                    tc::mbar_arrive_expect_tx(&fullA[s],
+                    tc::mbar_arrive_expect_tx(&full[s],
                                               (uint32_t)(nsub * A_TX + C::SCALE_REP_A * SF_BYTES));
+                    ++it;  // a fill of this stage is now in flight
                     for (int sub = 0; sub < nsub; ++sub) {
                         unsigned char *sa = st + sub * A_BYTES;
-                        tc::tma_load_2d(sa, &mapA, &fullA[s], (kc + sub) * BK, row0, pol_w);
+                        tc::tma_load_2d(sa, &mapA, &full[s], (kc + sub) * BK, row0, pol_w);
                         if (MODE == MOE_GEMM_GATEUP)  // up rows fill lanes 64..127
-                            tc::tma_load_2d(sa + 64 * BK, &mapA2, &fullA[s], (kc + sub) * BK, row0,
+                            tc::tma_load_2d(sa + 64 * BK, &mapA2, &full[s], (kc + sub) * BK, row0,
                                             pol_w);
                     }
                     // the scale block holding this stage's K block(s)
                     const uint8_t *sf = args.a_atoms + (atom0 + kc / ATOM_BLOCKS) * SF_BYTES;
                     for (int qd = 0; qd < C::SCALE_REP_A; ++qd)
-                        tc::bulk_copy_g2s(st + C::A_SF + qd * SF_BYTES, sf, SF_BYTES, &fullA[s], pol_w);
+                        tc::bulk_copy_g2s(st + C::A_SF + qd * SF_BYTES, sf, SF_BYTES, &full[s], pol_w);
                 }
             }
+            s_issued[0] = it;
         }
     } else if (warp == 1) {
         // ------------------------------------------ activation producer (one thread)
@@ -408,44 +402,35 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
             int it = 0;
             bool ok = true;
             int cur = 0;
-            for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
                 Tile t;
                 if (!get_tile(tile, cur, t)) continue;
                 const uint32_t tile_bytes = (uint32_t)(2 * t.nmma * BK);
                 const size_t blk0 = (size_t)t.tt * KC;
-                for (int kc = 0; kc < KC; kc += C::KS, ++it) {
+                for (int kc = 0; kc < KC; kc += C::KS) {
                     const int s = it % C::SB, round = it / C::SB;
                     const int nsub = min(C::KS, KC - kc);
-                    if (round > 0 && !tc::mbar_wait(&emptyB[s], (round - 1) & 1, LIMIT, abort_p)) {
+                    if (round > 0 && !tc::mbar_wait(&empty[s], (round - 1) & 1, LIMIT, abort_p)) {
                         fail();
                         ok = false;
                         break;
                     }
                     unsigned char *st = smem + C::B_BASE + s * C::B_STAGE;
-                    // the whole stage lands here; this CTA fetches its 1/CL share for all
                     tc::mbar_arrive_expect_tx(
-                        &fullB[s], (uint32_t)nsub * (tile_bytes + C::SCALE_REP_B * BSF_BYTES));
-                    const uint32_t part = tile_bytes / CL;
+                        &full[s], (uint32_t)nsub * (tile_bytes + C::SCALE_REP_B * BSF_BYTES));
+                    ++it;
                     for (int sub = 0; sub < nsub; ++sub) {
                         const size_t blk = blk0 + kc + sub;
-                        unsigned char *dst = st + sub * C::B_BYTES + rank * part;
-                        const uint8_t *src = args.b_tiles + blk * MOE_GEMM_BTILE + rank * part;
-                        if (CL > 1)
-                            tc::bulk_copy_g2s_multicast(dst, src, part, &fullB[s], CL_MASK, pol_x);
-                        else
-                            tc::bulk_copy_g2s(dst, src, part, &fullB[s], pol_x);
-                        for (int qd = 0; qd < C::SCALE_REP_B; ++qd) {  // each copy fetched by one CTA
-                            if ((sub * C::SCALE_REP_B + qd) % CL != rank) continue;
-                            unsigned char *sd = st + C::B_SF + (sub * C::SCALE_REP_B + qd) * BSF_BYTES;
-                            const uint8_t *ss = args.b_atoms + blk * BSF_BYTES;
-                            if (CL > 1)
-                                tc::bulk_copy_g2s_multicast(sd, ss, BSF_BYTES, &fullB[s], CL_MASK, pol_x);
-                            else
-                                tc::bulk_copy_g2s(sd, ss, BSF_BYTES, &fullB[s], pol_x);
-                        }
+                        tc::bulk_copy_g2s(st + sub * C::B_BYTES, args.b_tiles + blk * MOE_GEMM_BTILE,
+                                          tile_bytes, &full[s], pol_x);
+                        const uint8_t *ss = args.b_atoms + blk * BSF_BYTES;
+                        for (int qd = 0; qd < C::SCALE_REP_B; ++qd)
+                            tc::bulk_copy_g2s(st + C::B_SF + (sub * C::SCALE_REP_B + qd) * BSF_BYTES,
+                                              ss, BSF_BYTES, &full[s], pol_x);
                     }
                 }
             }
+            s_issued[1] = it;
         }
     } else if (warp == 2 || warp == 7) {
         // ------------------------------------------ MMA issuer(s) (one thread each)
@@ -457,10 +442,19 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
             const int split = warp == 2 ? 0 : 1;
             int it = 0, lt = 0, mine = 0;
             bool ok = true;
-            uint64_t *lastA = nullptr, *lastB = nullptr;
-            uint32_t parA = 0, parB = 0;
+            uint64_t *last = nullptr;
+            uint32_t last_par = 0;
             int cur = 0;
-            for (int tile = cluster_id; tile < total_tiles && ok; tile += n_clusters) {
+            // Test hook (off unless the host asks for it): the first issuer
+            // waits on its drain barrier, which nothing signals before the
+            // wind-down, so the wait runs out and the CTA takes the timeout
+            // path below with operand copies in flight.
+            if (args.inject == MOE_INJECT_GEMM_STALL && split == 0 &&
+                !tc::mbar_wait(&drain[0], 0, LIMIT, abort_p)) {
+                fail();
+                ok = false;
+            }
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
                 Tile t;
                 if (!get_tile(tile, cur, t)) continue;
                 const int buf = lt & 1, use = lt >> 1;
@@ -479,30 +473,28 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                 bool first = true;
                 for (int kc = 0, j = 0; kc < KC; kc += C::KS, ++it, ++j) {
                     if (C::NSPLIT > 1 && (j & 1) != split) continue;  // the other issuer's stage
-                    const int sa = it % C::SA, ra = it / C::SA;
-                    const int sb = it % C::SB, rb = it / C::SB;
+                    const int s = it % C::SA, round = it / C::SA;
                     const int nsub = min(C::KS, KC - kc);
                     // With two issuers the slot's previous fill may have been the
-                    // other issuer's, still in flight: a parity wait on full[sa]
+                    // other issuer's, still in flight: a parity wait on full[s]
                     // could then match the phase before it. The slot's release
-                    // of round ra - 1 comes after that fill landed and before the
-                    // producer refills it, so once it is seen the full wait can
-                    // only mean round ra (and it costs nothing: the fill of round
-                    // ra waits for that release anyway).
-                    if (C::NSPLIT > 1 && ra > 0 &&
-                        !tc::mbar_wait(&emptyA[sa], (ra - 1) & 1, LIMIT, abort_p)) {
+                    // of round - 1 comes after that fill landed and before the
+                    // producers refill it, so once it is seen the full wait can
+                    // only mean this round (and it costs nothing: the fill of
+                    // this round waits for that release anyway).
+                    if (C::NSPLIT > 1 && round > 0 &&
+                        !tc::mbar_wait(&empty[s], (round - 1) & 1, LIMIT, abort_p)) {
                         fail();
                         ok = false;
                         break;
                     }
-                    if (!tc::mbar_wait(&fullA[sa], ra & 1, LIMIT, abort_p) ||
-                        (!C::MERGED && !tc::mbar_wait(&fullB[sb], rb & 1, LIMIT, abort_p))) {
+                    if (!tc::mbar_wait(&full[s], round & 1, LIMIT, abort_p)) {
                         fail();
                         ok = false;
                         break;
                     }
-                    const uint32_t a_s = tc::smem_u32(smem + sa * C::A_STAGE);
-                    const uint32_t b_s = tc::smem_u32(smem + C::B_BASE + sb * C::B_STAGE);
+                    const uint32_t a_s = tc::smem_u32(smem + s * C::A_STAGE);
+                    const uint32_t b_s = tc::smem_u32(smem + C::B_BASE + s * C::B_STAGE);
                     const uint32_t slot =
                         tmem + C::SF_TMEM_COL + (uint32_t)(2 * split + (mine & 1)) * C::SF_SLOT;
                     ++mine;
@@ -526,31 +518,18 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                                              (!first || sub > 0 || k > 0) ? 1u : 0u);
                     }
                     first = false;
-                    if (C::SHARED_EMPTY) {  // one release for both rings
-                        tc::mma_commit(&emptyA[sa]);
-                    } else {
-                        tc::mma_commit(&emptyA[sa]);
-                        tc::mma_commit_multicast(&emptyB[sb], CL_MASK);  // every CTA's copy is free
-                    }
-                    lastA = &emptyA[sa];
-                    parA = ra & 1;
-                    lastB = &emptyB[sb];
-                    parB = rb & 1;
+                    tc::mma_commit(&empty[s]);  // the stage is free once these MMAs are done
+                    last = &empty[s];
+                    last_par = round & 1;
                 }
                 if (!ok) break;
                 tc::mma_commit(&tfull[buf]);
             }
-            // the last stage releases must land before the CTA can exit
-            if (ok && lastA &&
-                (!tc::mbar_wait(lastA, parA, LIMIT, abort_p) || !tc::mbar_wait(lastB, parB, LIMIT, abort_p)))
-                fail();
-            if (!ok || *abort_p) {
-                // giving up: this thread's MMAs must finish before tensor memory
-                // is freed (their operands are in shared memory, so they do)
-                int never = 0;
-                tc::mma_commit(&drain[split]);
-                tc::mbar_wait(&drain[split], 0, LIMIT / 100, &never);
-            }
+            // the last stage release must land before the CTA can exit
+            if (ok && last && !tc::mbar_wait(last, last_par, LIMIT, abort_p)) fail();
+            // giving up: this thread's MMAs must finish before tensor memory is
+            // freed (their operands are in shared memory, so they do)
+            if (!ok || *abort_p) tc::drain_mmas(&drain[split], LIMIT);
         }
         __syncwarp();
     } else {
@@ -559,7 +538,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         int lt = 0, cur = 0;
-        for (int tile = cluster_id; tile < total_tiles; tile += n_clusters) {
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
             Tile t;
             if (!get_tile(tile, cur, t))
                 continue;
@@ -587,9 +566,12 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
                 }
             }
             // a long wait (the tile's MMAs): sleep in try_wait rather than
-            // spin, leaving issue slots to the producer and issuer warps
-            if (!tc::mbar_wait_sleep(&tfull[buf], use & 1, LIMIT, abort_p)) {
-                if (lane == 0) fail();
+            // spin, leaving issue slots to the producer and issuer warps. The
+            // four warps then decide together, so none of them is left at a
+            // later epilogue barrier by a warp that gave up.
+            const bool got = tc::mbar_wait_sleep(&tfull[buf], use & 1, LIMIT, abort_p);
+            if (!tc::bar_and(1, 128, got)) {
+                if (!got && lane == 0) fail();
                 break;
             }
             tc::tc_fence_after();
@@ -729,11 +711,26 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
         }
     }
 
+    // Wind-down after a timeout: every operand copy this CTA issued must land
+    // before its shared memory is released. A stage filled in round r has
+    // completed its full barrier phase r once both producers' arrivals and
+    // bytes are in. The producers stop at most one round apart on a stage
+    // (a fill of round r waited for the release of round r - 1, which needed
+    // both fills of that round), so where only one of them filled the last
+    // round, the missing arrival is made here and the wait then ends when the
+    // issued bytes have landed.
+    __syncthreads();
     if (*abort_p && tid == 0) {
-        // wound down early: give bulk copies still in flight (issued for stages
-        // nobody consumed) time to land before the shared memory is released
-        const long long t0 = clock64();
-        while (clock64() - t0 < LIMIT / 5000) __nanosleep(1000);
+        int never = 0;
+        const int na = s_issued[0], nb = s_issued[1];
+        for (int s = 0; s < C::SA; ++s) {
+            const int ra = na > s ? (na - s + C::SA - 1) / C::SA : 0;  // rounds of slot s filled
+            const int rb = nb > s ? (nb - s + C::SA - 1) / C::SA : 0;
+            const int r = max(ra, rb);
+            if (r == 0 || ra - rb > 1 || rb - ra > 1) continue;
+            if (ra != rb) tc::mbar_arrive(&full[s]);
+            tc::mbar_wait(&full[s], (uint32_t)((r - 1) & 1), LIMIT / 100 + 100000, &never);
+        }
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -741,7 +738,6 @@ __global__ void __launch_bounds__(Cfg<MODE, NT>::THREADS, 1) moe_grouped_gemm_ke
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    tc::cluster_sync();  // no CTA leaves while a peer may still multicast into it
 }
 
 // Weight scales re-laid for the tensor cores: one 1 KB block per (expert,
@@ -805,10 +801,10 @@ __global__ void __launch_bounds__(256) moe_prepare_atoms_slots_kernel(
 // ---------------------------------------------------------------------------
 size_t moe_gemm_smem_bytes(int mode, int narrow) {
     if (narrow)
-        return mode == MOE_GEMM_GATEUP ? Cfg<MOE_GEMM_GATEUP, MOE_GEMM_NT_NARROW>::SMEM
-                                       : Cfg<MOE_GEMM_DOWN, MOE_GEMM_NT_NARROW>::SMEM;
-    return mode == MOE_GEMM_GATEUP ? Cfg<MOE_GEMM_GATEUP, NTMAX>::SMEM
-                                   : Cfg<MOE_GEMM_DOWN, NTMAX>::SMEM;
+        return mode == MOE_GEMM_GATEUP ? Cfg<MOE_GEMM_GATEUP, MOE_GEMM_NT_NARROW, false>::SMEM
+                                       : Cfg<MOE_GEMM_DOWN, MOE_GEMM_NT_NARROW, false>::SMEM;
+    return mode == MOE_GEMM_GATEUP ? Cfg<MOE_GEMM_GATEUP, NTMAX, false>::SMEM
+                                   : Cfg<MOE_GEMM_DOWN, NTMAX, false>::SMEM;
 }
 
 size_t moe_prepared_atoms_bytes(int E, int M, int K, int mrows) {
@@ -833,39 +829,19 @@ cudaError_t moe_launch_prepare_atoms(int E, int M, int K, int mrows, const uint8
 }
 
 namespace {
+// One persistent CTA per SM (grid = max_ctas, the SM count): the kernel's
+// shared memory admits exactly one CTA per SM.
 template <int MODE, int NT>
-cudaError_t launch_clustered(const CUtensorMap *mA, const CUtensorMap *mA2,
-                             const MoeGemmArgs *args, int max_ctas, cudaStream_t st) {
-    using C = Cfg<MODE, NT>;
-    constexpr int CL = C::CL;
+cudaError_t launch_gemm_t(const CUtensorMap *mA, const CUtensorMap *mA2, const MoeGemmArgs *args,
+                          int max_ctas, cudaStream_t st) {
+    using C = Cfg<MODE, NT, false>;
     auto kern = moe_grouped_gemm_kernel<MODE, NT>;
-    const size_t sm = C::SMEM;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (err != cudaSuccess) return err;
-    if (args->MT % CL) return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(C::THREADS);
-    cfg.dynamicSmemBytes = sm;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    static int clusters = 0;  // co-resident clusters of this instantiation
-    if (!clusters) {
-        cfg.gridDim = dim3(max_ctas / CL * CL);
-        int n = 0;
-        err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-        if (err != cudaSuccess) return err;
-        clusters = n > 0 ? n : 1;
-    }
-    int grid = clusters * CL;
-    if (grid > max_ctas / CL * CL) grid = max_ctas / CL * CL;
-    cfg.gridDim = dim3(grid);
-    return cudaLaunchKernelEx(&cfg, kern, *mA, *mA2, *args);
+    if (max_ctas < 1) return cudaErrorInvalidValue;
+    kern<<<max_ctas, C::THREADS, C::SMEM, st>>>(*mA, *mA2, *args);
+    return cudaGetLastError();
 }
 }  // namespace
 
@@ -873,9 +849,8 @@ cudaError_t moe_launch_gemm(int mode, const CUtensorMap *mA, const CUtensorMap *
                             const MoeGemmArgs *args, int max_rows, int grid, cudaStream_t st) {
     constexpr int NN = MOE_GEMM_NT_NARROW;
     if (max_rows <= NN)
-        return mode == MOE_GEMM_GATEUP
-                   ? launch_clustered<MOE_GEMM_GATEUP, NN>(mA, mA2, args, grid, st)
-                   : launch_clustered<MOE_GEMM_DOWN, NN>(mA, mA2, args, grid, st);
-    return mode == MOE_GEMM_GATEUP ? launch_clustered<MOE_GEMM_GATEUP, NTMAX>(mA, mA2, args, grid, st)
-                                   : launch_clustered<MOE_GEMM_DOWN, NTMAX>(mA, mA2, args, grid, st);
+        return mode == MOE_GEMM_GATEUP ? launch_gemm_t<MOE_GEMM_GATEUP, NN>(mA, mA2, args, grid, st)
+                                       : launch_gemm_t<MOE_GEMM_DOWN, NN>(mA, mA2, args, grid, st);
+    return mode == MOE_GEMM_GATEUP ? launch_gemm_t<MOE_GEMM_GATEUP, NTMAX>(mA, mA2, args, grid, st)
+                                   : launch_gemm_t<MOE_GEMM_DOWN, NTMAX>(mA, mA2, args, grid, st);
 }

@@ -66,7 +66,6 @@ cudaError_t moe_launch_gather_x(int max_tt, int E, int k, int n_rows, int D, int
 #define MOE_GEMM_DOWN 1
 #define MOE_GEMM_NTMAX 112
 #define MOE_GEMM_NT_NARROW 16  // token rows per tile of the narrow variant
-#define MOE_GEMM_CLUSTER 2  // CTAs per cluster sharing the activation operand
 #define MOE_GEMM_BTILE (2 * MOE_GEMM_NTMAX * 128)  // bytes of one activation B tile block
 
 struct MoeGemmArgs {
@@ -87,6 +86,7 @@ struct MoeGemmArgs {
     float *acc;                        // GEMM2 output
     int *status;
     long long timeout_cycles;
+    int inject;              // MOE_INJECT_NONE, or a test hook (see moe_set_fault_injection)
 };
 
 size_t moe_gemm_smem_bytes(int mode, int narrow);

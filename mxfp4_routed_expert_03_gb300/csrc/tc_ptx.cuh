@@ -151,32 +151,6 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
         : "memory");
 }
 
-// The same bulk copy delivered to the same shared-memory offset of every CTA
-// in cta_mask (within this cluster); each destination's mbarrier at bar's
-// offset receives the completed bytes.
-__device__ __forceinline__ void bulk_copy_g2s_multicast(void *dst, const void *src, uint32_t bytes,
-                                                        uint64_t *bar, uint16_t cta_mask,
-                                                        uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1], %2, [%3], %4, %5;" ::"r"(smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "h"(cta_mask), "l"(policy)
-        : "memory");
-}
-
-// ---------------------------------------------------------------- clusters
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// All threads of all CTAs of the cluster.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-}
-
 // ---------------------------------------------------------------- cp.async
 __device__ __forceinline__ void cp_async_4(void *dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
@@ -237,15 +211,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
         : "memory");
 }
 
-// As mma_commit, arriving on the mbarrier at bar's offset in every CTA of cta_mask.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
 // 32 rows x 128 bits from smem (descriptor) into TMEM at taddr, replicated to
 // all four 32-lane quadrants.
 __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
@@ -273,6 +238,29 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- wind-down
+// After a timeout: wait until every MMA this thread issued has completed
+// (one commit to `bar`, a barrier used for nothing else, then a bounded wait
+// on its first phase), so that tensor memory can be released.
+__device__ __forceinline__ void drain_mmas(uint64_t *bar, long long limit) {
+    int never = 0;
+    mma_commit(bar);
+    mbar_wait(bar, 0, limit / 100 + 100000, &never);
+}
+
+// After a timeout: wait (bounded) until every fill a single producer issued
+// into a ring of n_slots stages has landed. Fill i went to stage i % n_slots
+// in round i / n_slots; with one arrival per phase the last round of each
+// stage completes once its bytes are in.
+__device__ __forceinline__ void wait_issued_fills(uint64_t *full, int n_slots, int issued,
+                                                  long long limit) {
+    int never = 0;
+    for (int s = 0; s < n_slots; ++s) {
+        const int rounds = issued > s ? (issued - s + n_slots - 1) / n_slots : 0;
+        if (rounds > 0) mbar_wait(&full[s], (uint32_t)((rounds - 1) & 1), limit / 100 + 100000, &never);
+    }
 }
 
 // ---------------------------------------------------------------- descriptors
