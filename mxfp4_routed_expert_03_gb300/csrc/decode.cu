@@ -12,11 +12,15 @@
 // Arithmetic: an E2M1 pair is converted to f16x2 exactly (cvt.rn.f16x2.e2m1x2);
 // each 32-element block is reduced with exact f16 x f16 products accumulated
 // in fp32 (fma.rn.f32.f16), multiplied by its E8M0 scale and added to the
-// row's fp32 sum. Activations enter as f16 (bf16 -> f16 is exact for |x| in
-// [2^-14, 65504), the range of these inputs). The intermediate h is stored as
-// f16 with one power-of-two exponent per 32 consecutive rows of F (so it
-// cannot overflow; 11 significant bits per element), which lets the down
-// projection use the same exact f16 x f16 -> fp32 inner loop.
+// row's fp32 sum. Activations enter as f16 with one power-of-two exponent per
+// 32-element block of x, chosen so that the block's largest magnitude lands in
+// [2^14, 2^15): every bf16 value, from subnormals to 3.4e38, then fits f16
+// without overflow, and every element within 2^-28 of its block's maximum
+// converts exactly (bf16 has 8 significant bits, f16 11). The block's
+// exponent multiplies its partial sum together with the weight scale. The
+// intermediate h is stored the same way, as f16 with one power-of-two
+// exponent per 32 consecutive rows of F, which lets the down projection use
+// the same exact f16 x f16 -> fp32 inner loop.
 //
 // Work split: persistent grids, each CTA walking a contiguous range of the
 // (active expert, row) space, so every weight row is read exactly once and
@@ -96,9 +100,24 @@ __device__ __forceinline__ bool segment_of(int a, int E, int n_rows, const int32
 
 // Shared-memory activation rows: each 32-element block (64 bytes of f16) is
 // stored with 16 bytes of padding, so the 16-byte reads of eight consecutive
-// lanes (one block each) fall in distinct bank groups.
+// lanes (one block each) fall in distinct bank groups. For x the padding's
+// first 4 bytes hold the block's scale 2^ex (fp32).
 constexpr int kBlkStride = 80;   // bytes per staged block
+constexpr int kBlkScale = 64;    // byte offset of a staged x block's scale
 constexpr int kStageTok = 4;     // tokens staged at once
+
+// Exponent ex (clamped to [-126, 113]) with amax * 2^-ex in [2^14, 2^15) for a
+// finite non-zero amax; 0 for zero, infinity or NaN.
+__device__ __forceinline__ int f16_block_exp(float amax) {
+    const int e = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+    if (amax == 0.f || e == 255) return 0;
+    int ex = (e == 0 ? -126 : e - 127) - 14;  // fp32 subnormal amax: below 2^-126
+    return max(-126, min(113, ex));
+}
+
+__device__ __forceinline__ float exp2_int(int ex) {  // 2^ex for ex in [-126, 127]
+    return __uint_as_float((uint32_t)(ex + 127) << 23);
+}
 
 // ---------------------------------------------------------------------------
 // Gate/up + SwiGLU. The (active expert, 32-row block of F) steps are split
@@ -144,22 +163,43 @@ __global__ void __launch_bounds__(256, 2) moe_decode_gateup_kernel(
             const int ns = min(kStageTok, n - g0);
             if (a != staged_a || g0 != staged_g0) {
                 __syncthreads();
-                // 8 bf16 -> 8 f16 per thread iteration; chunk c of block b of token j
-                for (int i = threadIdx.x; i < ns * nblk * 4; i += blockDim.x) {
-                    const int j = i / (nblk * 4), r = i % (nblk * 4);
+                // one 32-element block of token j per thread iteration: 32 bf16
+                // -> 32 f16 scaled by 2^-ex, and the block's scale 2^ex
+                for (int i = threadIdx.x; i < ns * nblk; i += blockDim.x) {
+                    const int j = i / nblk, b = i % nblk;
                     int fl = perm[s0 + g0 + j];
                     if (fl < 0 || fl >= n_rows) { moe_flag(status, MOE_ERR_BAD_INDEX); fl = 0; }
-                    const uint4 v = __ldg((const uint4 *)(x + (size_t)(fl / k) * D) + r);
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                    uint32_t o[4];
+                    const uint4 *src = (const uint4 *)(x + (size_t)(fl / k) * D) + 4 * b;
+                    uint32_t w[16];
+                    float amax = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        __half2 hh = __floats2half2_rn(__uint_as_float(w4[q] << 16),
-                                                       __uint_as_float(w4[q] & 0xFFFF0000u));
-                        o[q] = *reinterpret_cast<uint32_t *>(&hh);
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 v = __ldg(src + c);
+                        w[4 * c] = v.x;
+                        w[4 * c + 1] = v.y;
+                        w[4 * c + 2] = v.z;
+                        w[4 * c + 3] = v.w;
                     }
-                    *(uint4 *)(xs + ((size_t)j * nblk + r / 4) * kBlkStride + (r % 4) * 16) =
-                        make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[q] << 16)),
+                                                 fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
+                    const int ex = f16_block_exp(amax);
+                    const float inv = exp2_int(-ex);  // exact: a power of two times bf16
+                    unsigned char *dst = xs + ((size_t)j * nblk + b) * kBlkStride;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t u = w[4 * c + q];
+                            __half2 hh = __floats2half2_rn(__uint_as_float(u << 16) * inv,
+                                                           __uint_as_float(u & 0xFFFF0000u) * inv);
+                            o[q] = *reinterpret_cast<uint32_t *>(&hh);
+                        }
+                        *(uint4 *)(dst + 16 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                    *(float *)(dst + kBlkScale) = exp2_int(ex);
                 }
                 __syncthreads();
                 staged_a = a;
@@ -188,10 +228,12 @@ __global__ void __launch_bounds__(256, 2) moe_decode_gateup_kernel(
                         if (j < nt) {
 #pragma unroll
                             for (int p = 0; p < PER_LANE; ++p) {
-                                const uint4 *xb = (const uint4 *)(
-                                    xs + ((size_t)(j0 + j) * nblk + sub + LPR * p) * kBlkStride);
-                                ag[j] = fmaf(block_dot_f16(gqv[p], xb), gsc[p], ag[j]);
-                                au[j] = fmaf(block_dot_f16(uqv[p], xb), usc[p], au[j]);
+                                const unsigned char *xbb =
+                                    xs + ((size_t)(j0 + j) * nblk + sub + LPR * p) * kBlkStride;
+                                const uint4 *xb = (const uint4 *)xbb;
+                                const float xsc = *(const float *)(xbb + kBlkScale);
+                                ag[j] = fmaf(block_dot_f16(gqv[p], xb), gsc[p] * xsc, ag[j]);
+                                au[j] = fmaf(block_dot_f16(uqv[p], xb), usc[p] * xsc, au[j]);
                             }
                         }
                     }
