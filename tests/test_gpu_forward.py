@@ -53,29 +53,61 @@ def test_tiny_shapes_ragged_and_multi_tile_segments(tiny_weights, T):
     print("tiny forward T=%d" % T, e)
 
 
-@pytest.mark.parametrize("T", [16, 500])
+@pytest.mark.parametrize("T", [16, 111, 112, 113, 224, 500])
 def test_tiny_one_expert_holds_all_rows(tiny_weights, T):
-    """T = 16 fills one narrow (16-row) token tile; T = 500 spans several wide ones."""
+    """T = 16 fills one narrow (16-row) token tile; 111..113 and 224 sit at
+    the wide tile's 112 rows and its multiples; 500 spans five wide tiles."""
     w = synth.WORKLOADS["tiny"]
     x, lg = synth.make_x(w, 5, T=T), synth.make_logits(w, 5, T=T)
     lg[:, 9] = 60.0
     got, plan = _run(w, tiny_weights, x, lg)
     assert plan.counts.cpu().numpy()[9] == T
-    tok = np.arange(0, T, 11) if T > 16 else np.arange(T)
+    tok = np.arange(T) if T <= 16 else np.unique(np.r_[np.arange(0, T, 11), 110, 111, 112,
+                                                            T - 2, T - 1])
+    tok = tok[tok < T]
     assert_close(got[tok], reference(w, x, lg, tokens=tok)["out"])
+
+
+NT_WIDE = 112   # token rows per tile of the prefill GEMMs
+
+
+def tile_edge_tokens(perm: np.ndarray, offsets: np.ndarray, k: int, e: int) -> np.ndarray:
+    """Tokens at the edges of expert e's token tiles: the GEMMs split a segment
+    of c rows into ceil(c / 112) tiles of near-equal size (rows j*c/ntt ..),
+    so these are the first and last row of every tile, the last tile being
+    the partial one when c is not a multiple of 112."""
+    s0, c = int(offsets[e]), int(offsets[e + 1] - offsets[e])
+    ntt = -(-c // NT_WIDE)
+    rows = set()
+    for j in range(ntt):
+        r0, r1 = j * c // ntt, (j + 1) * c // ntt
+        rows.update((r0, r1 - 1))
+    return np.array(sorted({int(perm[s0 + r]) // k for r in rows}), dtype=np.int64)
 
 
 @pytest.mark.parametrize("name,n_check", [("prefill4k", 16), ("skewed8k", 16)])
 def test_k3_prefill_sampled_tokens(k3_layer, name, n_check):
+    """Random tokens plus the tokens at the tile edges of the longest segment
+    (skewed8k: the most popular Zipf expert, several tiles, the last partial)
+    and of one segment with a single tile."""
     w = synth.WORKLOADS[name]
     x, lg = synth.make_x(w), synth.make_logits(w)
     got, plan = _run(w, k3_layer, x, lg)
-    tok = np.random.default_rng(1).choice(w.T, n_check, replace=False)
+    perm, offsets = plan.perm.cpu().numpy(), plan.offsets.cpu().numpy()
+    counts = np.diff(offsets)
+    longest = int(np.argmax(counts))
+    single = int(np.flatnonzero((counts > 0) & (counts <= NT_WIDE))[0])
+    edges = np.concatenate([tile_edge_tokens(perm, offsets, w.k, longest),
+                            tile_edge_tokens(perm, offsets, w.k, single)])
+    rnd = np.random.default_rng(1).choice(w.T, n_check, replace=False)
+    tok = np.unique(np.concatenate([rnd, edges]))
+    if name == "skewed8k":
+        assert counts[longest] > 2 * NT_WIDE and counts[longest] % NT_WIDE != 0
     ref = reference(w, x, lg, tokens=tok)
-    np.testing.assert_array_equal(plan.perm.cpu().numpy(), ref["plan"]["perm"])
+    np.testing.assert_array_equal(perm, ref["plan"]["perm"])
     e = assert_close(got[tok], ref["out"])
     assert np.all(np.isfinite(got))
-    print(name, e)
+    print(name, "longest segment", counts[longest], "tokens checked", len(tok), e)
 
 
 @pytest.mark.parametrize("T", [1, 4, 8, 16])
