@@ -1,17 +1,22 @@
 #!/usr/bin/env python3
 """Benchmark of the GB300 routed-expert FFN library: prints one JSON line.
 
-Default workload: one K3-shaped routed layer (d_model 7168, d_ff 1536, 896
-experts, top-16, MXFP4 weights resident in HBM), decode batches of T = 1, 4
-and 16 tokens; one step = moe_plan + the expert FFN for each of the three
-batches (21 tokens). The FFN call of each batch takes the faster entry point
-as measured on GB300, which is moe_forward (tcgen05 grouped GEMMs) at every
-batch size, down to one token (89 vs 101 us for moe_decode, the CUDA-core
-streaming path); CROSSOVER_T keeps the rule explicit, and `--path
-decode|forward` forces one of them. `--workload prefill4k|skewed8k` times moe_plan +
-moe_forward on one prefill batch instead; `--workload router16k` times the
-long prefill whose logits come from the library's own fp32 router (x . W_r)
-and which adds one bf16 shared expert.
+Default workload (the headline): one K3-shaped routed layer (d_model 7168,
+d_ff 1536, 896 experts, top-16, MXFP4 weights resident in HBM), decode
+batches of T = 1, 4 and 16 tokens; one step = moe_plan + the expert FFN for
+each of the three batches (21 tokens). The FFN call of each batch takes the
+faster entry point as measured on GB300, which is moe_forward (tcgen05
+grouped GEMMs) at every batch size, down to one token; CROSSOVER_T keeps the
+rule explicit, and `--path decode|forward` forces one of them.
+
+The default run adds, in the same line under "workloads", one record per
+workload measured on the same generated layer: decode_T1, decode_T4,
+decode_T16, prefill4k (T = 4096, uniform routing), skewed8k (T = 8192,
+Zipf-skewed routing) and router16k (T = 16384, the library's own fp32 router
+x . W_r plus one bf16 shared expert). Each record has its time per step,
+tokens/s (device-resident inputs and end to end), its dominant kernel's mean
+launch time with the roofline that bounds it, and the clocks of its timed
+window. `--workload NAME` times one workload alone.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -67,6 +72,10 @@ CROSSOVER_T = 0   # largest batch the CUDA-core decode path takes under --path a
 BENCH_WORKLOADS = {
     "decode": {"Ts": [1, 4, 16], "path": "auto",
                "desc": "K3 routed layer decode, T=1,4,16 (d_model 7168, d_ff 1536, 896 experts, top-16, MXFP4)"},
+    "decode_T1": {"Ts": [1], "path": "forward",
+                  "desc": "K3 routed layer decode, T=1 (one token per step)"},
+    "decode_T4": {"Ts": [4], "path": "forward", "desc": "K3 routed layer decode, T=4"},
+    "decode_T16": {"Ts": [16], "path": "forward", "desc": "K3 routed layer decode, T=16"},
     "prefill4k": {"Ts": [4096], "path": "forward",
                   "desc": "K3 routed layer prefill, T=4096, uniform routing"},
     "skewed8k": {"Ts": [8192], "path": "forward",
@@ -111,6 +120,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall-time budget of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-records", action="store_true",
+                    help="the headline workload only (no per-workload records)")
     ap.add_argument("--experts", type=int, default=None,
                     help="experts in the layer (default: the workload's); fewer only for profiling small "
                          "cases, and the line is then marked as such")
@@ -213,7 +224,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", gpu_id, "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()
         except (OSError, ValueError):
@@ -276,106 +287,199 @@ def kernel_traffic(name: str, source: str, workload: str):
     return None
 
 
-def run_ours(args):
+# ---------------------------------------------------------------------------
+# GPU arm: one generated layer, shared by every workload measured in the run
+# ---------------------------------------------------------------------------
+class Ctx:
+    """Device state of a run: the routed layer's weights (generated in HBM
+    once, by the device half of the seeded generator) and the library handles
+    built over them."""
+
+    def __init__(self, args, n_exp, dev, rank, world, dist):
+        self.args, self.n_exp, self.dev = args, n_exp, dev
+        self.rank, self.world, self.dist = rank, world, dist
+        self.weights = {}     # code distribution -> weight tensors
+        self.layers = {}      # kind -> Layer
+
+    def layer_weights(self, codes, seed):
+        import torch
+        import synth
+        from mxfp4_routed_expert_03_gb300.layer import alloc_weights
+        if codes not in self.weights:
+            w = alloc_weights(self.n_exp, D_MODEL, D_FF)
+            synth.dev_fill_layer(seed, self.n_exp, D_MODEL, D_FF,
+                                 {k: v.data_ptr() for k, v in w.items()},
+                                 torch.cuda.current_stream().cuda_stream, dist=codes)
+            self.weights[codes] = w
+        return self.weights[codes]
+
+    def barrier(self):
+        import torch
+        torch.cuda.synchronize()
+        if self.dist is not None:
+            self.dist.barrier()
+        torch.cuda.synchronize()
+
+    def close(self):
+        for layer in self.layers.values():
+            layer.close()
+        self.layers.clear()
+
+
+def make_layer(ctx, wl, base):
+    """The library handle a workload runs on (built once per kind and kept)."""
+    import dataclasses
     import numpy as np
     import torch
     import synth
-    import mxfp4_routed_expert_03_gb300 as moe
-    from mxfp4_routed_expert_03_gb300 import (MOE_PROF_DECODE_GATEUP, MOE_PROF_FORWARD_GEMM1,
-                                              MOE_PROF_NONE, MOE_ROUTER_XWR, check,
-                                              moe_profile_kernel)
-    from mxfp4_routed_expert_03_gb300.layer import Layer, Plan, alloc_weights
-
-    n_exp = args.experts or N_EXPERTS
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.device("cuda", torch.cuda.current_device())
-    wl = dict(BENCH_WORKLOADS[args.workload])
-    if args.tokens:
-        wl["Ts"] = [args.tokens]
-    path = args.path or wl["path"]
-    base = base_workload(args.workload)
-
-    # weights: the full layer, generated in HBM by the device half of the generator
-    weights = alloc_weights(n_exp, D_MODEL, D_FF)
-    synth.dev_fill_layer(base.seed, n_exp, D_MODEL, D_FF,
-                         {k: v.data_ptr() for k, v in weights.items()},
-                         torch.cuda.current_stream().cuda_stream,
-                         dist=wl.get("codes", synth.CODES_UNIFORM))
-    use_router = bool(wl.get("router"))
+    from mxfp4_routed_expert_03_gb300 import MOE_ROUTER_XWR
+    from mxfp4_routed_expert_03_gb300.layer import Layer
+    codes = wl.get("codes", synth.CODES_UNIFORM)
     n_slots = wl.get("stream_slots")
-    store_info = None
-    n_sets = wl.get("sets", N_SETS)
-    if use_router:
-        import dataclasses
-        w_router = torch.from_numpy(synth.make_w_router(dataclasses.replace(base, E=n_exp))).to(dev)
-        shared = {k: torch.from_numpy(v.view(np.int16)).to(dev)
+    kind = ("router" if wl.get("router") else "stream_store" if wl.get("store") else
+            "stream" if n_slots else "plain", codes)
+    if kind in ctx.layers:
+        return ctx.layers[kind], None
+    weights = ctx.layer_weights(codes, base.seed)
+    info = None
+    if wl.get("router"):
+        w_router = torch.from_numpy(
+            synth.make_w_router(dataclasses.replace(base, E=ctx.n_exp))).to(ctx.dev)
+        shared = {k: torch.from_numpy(v.view(np.int16)).to(ctx.dev)
                   for k, v in synth.make_shared(base).items()}
-        layer = Layer(D_MODEL, D_FF, n_exp, TOP_K, weights, MOE_ROUTER_XWR, w_router, shared)
+        layer = Layer(D_MODEL, D_FF, ctx.n_exp, TOP_K, weights, MOE_ROUTER_XWR, w_router, shared)
     elif n_slots:
-        # the store: all experts in pinned host memory; the layer caches n_slots in HBM
+        # the slow tier: all experts in pinned host memory; the layer caches
+        # n_slots of them in HBM
         from mxfp4_routed_expert_03_gb300.layer import StreamingLayer
         host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in weights.items()}
         for k, v in weights.items():
             host[k].copy_(v)
-        del weights
-        torch.cuda.empty_cache()
         if wl.get("store"):
-            # the compressed store, built by the library's host encoder
             from mxfp4_routed_expert_03_gb300.layer import ExpertStore
             t_enc = time.perf_counter()
-            store = ExpertStore(n_exp, D_MODEL, D_FF, host)
-            store_info = {"encode_s": time.perf_counter() - t_enc,
-                          "stored_over_raw": store.blob_bytes / store.raw_bytes}
+            store = ExpertStore(ctx.n_exp, D_MODEL, D_FF, host)
+            info = {"encode_s": time.perf_counter() - t_enc,
+                    "stored_over_raw": store.blob_bytes / store.raw_bytes}
             del host
-            layer = StreamingLayer(D_MODEL, D_FF, n_exp, TOP_K, None, min(n_slots, n_exp),
-                                   store=store)
+            layer = StreamingLayer(D_MODEL, D_FF, ctx.n_exp, TOP_K, None,
+                                   min(n_slots, ctx.n_exp), store=store)
         else:
-            layer = StreamingLayer(D_MODEL, D_FF, n_exp, TOP_K, host, min(n_slots, n_exp))
+            layer = StreamingLayer(D_MODEL, D_FF, ctx.n_exp, TOP_K, host, min(n_slots, ctx.n_exp))
     else:
-        layer = Layer(D_MODEL, D_FF, n_exp, TOP_K, weights)
+        layer = Layer(D_MODEL, D_FF, ctx.n_exp, TOP_K, weights)
+    layer.prepare()
+    ctx.layers[kind] = layer
+    return layer, info
+
+
+def make_batches(ctx, wl, base, path_of, use_router):
+    """Seeded (x, logits) sets per batch size, resident in HBM (x only when the
+    library computes the logits), their pinned host copies for the end-to-end
+    pass, plan and output buffers."""
+    import numpy as np
+    import torch
+    import synth
+    from mxfp4_routed_expert_03_gb300.layer import Plan
+    n_sets = wl.get("sets", N_SETS)
+    batches = []
+    for T in wl["Ts"]:
+        w = synth.Workload(base.name, T=T, D=D_MODEL, F=D_FF, E=ctx.n_exp, k=TOP_K,
+                           seed=base.seed, zipf_s=base.zipf_s)
+        xs_h = [synth.make_x(w, ctx.rank * 97 + i) for i in range(n_sets)]
+        ls_h = [np.zeros((T, ctx.n_exp), np.float32) if use_router else
+                synth.make_logits(w, ctx.rank * 97 + i) for i in range(n_sets)]
+        dev = ctx.dev
+        batches.append({"T": T,
+                        "x": [torch.from_numpy(a.view(np.int16)).to(dev) for a in xs_h],
+                        "l": [torch.from_numpy(a).to(dev) for a in ls_h],
+                        "px": [torch.from_numpy(a.view(np.int16)).pin_memory() for a in xs_h],
+                        "pl": [torch.from_numpy(a).pin_memory() for a in ls_h],
+                        "plan": Plan(T, ctx.n_exp, TOP_K),
+                        "out": torch.empty((T, D_MODEL), dtype=torch.int16, device=dev),
+                        "dx": torch.empty((T, D_MODEL), dtype=torch.int16, device=dev),
+                        "dl": torch.empty((T, ctx.n_exp), dtype=torch.float32, device=dev),
+                        "hout": torch.empty((T, D_MODEL), dtype=torch.int16).pin_memory(),
+                        "path": path_of(T)})
+    return batches
+
+
+def kernel_work(path: str, T: int, active: int):
+    """Algorithmic bytes and flops of one launch of a batch's dominant kernel:
+    the gate/up GEMM of moe_forward (active experts' gate+up weights, the
+    two-term activation rows in and the two-term h rows out, one byte per
+    term and element) or the gate/up kernel of moe_decode (the same weights,
+    bf16 x rows in, f16 h rows and their exponents out)."""
+    flop = 2.0 * T * TOP_K * 2 * D_MODEL * D_FF
+    if path == "decode":
+        nbytes = active * GATEUP_BYTES + T * D_MODEL * 2 + T * TOP_K * (D_FF * 2 + D_FF // 32)
+    else:
+        nbytes = active * GATEUP_BYTES + T * TOP_K * (2 * D_MODEL + 2 * D_FF)
+    return float(nbytes), flop
+
+
+def roofline(path, nbytes, flop, ms, peaks, workload, store=None):
+    """Roofline of the dominant kernel: achieved algorithmic bytes or flops per
+    launch over its mean launch time, against the measured peak of the bound
+    its arithmetic intensity puts it under."""
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    fp8_peak = 2.0 * peaks.get("bf16_tflops", 1900.0)  # kind::mxf8f6f4 runs at the FP8 rate
+    fp4_peak = 6.0 * peaks.get("bf16_tflops", 1900.0)  # kind::mxf4 (nominal 13.5 / 2.25)
+    src = "measured" if peaks else "fallback"
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    tfs = flop / (ms * 1e-3) / 1e12
+    if path == "decode":
+        kname, csrc = "moe_decode_gateup_kernel", "decode.cu"
+        tensor_time = 0.0   # CUDA cores: bound by bytes
+    else:
+        kname, csrc = "moe_grouped_gemm_kernel<0>", "grouped_gemm.cu"
+        tensor_time = 2.0 * flop / 1e12 / fp8_peak   # two MMAs per algorithmic one
+    mem_bound = nbytes / 1e9 / hbm_peak >= tensor_time
+    if mem_bound:
+        r = {"bound": "hbm", "kernel": kname, "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+             "frac": gbs / hbm_peak, "peak_source": src + " (copy bandwidth)"}
+    else:
+        r = {"bound": "tensor", "kernel": kname, "achieved": tfs, "peak": fp8_peak,
+             "unit": "TFLOP/s", "frac": tfs / fp8_peak,
+             "peak_source": src + " bf16 x 2 (FP8 rate; the two-term activation split issues 2 "
+                                  "MMAs per algorithmic one, so frac <= 0.5)",
+             "hbm_GBs": gbs, "frac_of_hbm": gbs / hbm_peak}
+    r.update({"bytes_per_launch": nbytes, "flop_per_launch": flop, "kernel_ms": ms,
+              "tensor_TFLOPs": tfs, "frac_of_fp8_peak": tfs / fp8_peak,
+              "frac_of_fp4_peak": tfs / fp4_peak,
+              "binding_roof_ms": max(nbytes / 1e9 / hbm_peak, tensor_time) * 1e3,
+              "traffic": kernel_traffic(kname, csrc, workload)})
+    r["frac_of_binding_roof"] = r["binding_roof_ms"] / ms
+    return r
+
+
+def measure(ctx, name, wl, steps, warmup, sampler, peaks, breakdown=True, path_override=None):
+    """Time `steps` steps of workload `name` (after `warmup` untimed ones) on
+    device-resident inputs, then the same steps end to end (host inputs copied
+    in and the output read back inside the timed region). Returns the
+    workload's record and the figures the headline line adds."""
+    import numpy as np
+    import torch
+    import mxfp4_routed_expert_03_gb300 as moe
+    from mxfp4_routed_expert_03_gb300 import check, moe_profile_kernel
+    base = base_workload(name)
+    layer, store_info = make_layer(ctx, wl, base)
+    use_router = bool(wl.get("router"))
+    n_slots = wl.get("stream_slots")
+    path = path_override or wl["path"]
+
     def path_of(T):
         if path == "auto":
             return "decode" if T <= CROSSOVER_T else "forward"
         return path
-    if use_router or any(path_of(T) == "forward" for T in wl["Ts"]):
-        layer.prepare()
-    stream = torch.cuda.current_stream()
-
-    # inputs: seeded (x, logits) sets per batch size, resident in HBM (x only
-    # when the library computes the logits)
-    batches = []
-    for T in wl["Ts"]:
-        w = synth.Workload(base.name, T=T, D=D_MODEL, F=D_FF, E=n_exp, k=TOP_K,
-                           seed=base.seed, zipf_s=base.zipf_s)
-        xs_h = [synth.make_x(w, rank * 97 + i) for i in range(n_sets)]
-        ls_h = [np.zeros((T, n_exp), np.float32) if use_router else
-                synth.make_logits(w, rank * 97 + i) for i in range(n_sets)]
-        xs = [torch.from_numpy(a.view(np.int16)).to(dev) for a in xs_h]
-        ls = [torch.from_numpy(a).to(dev) for a in ls_h]
-        pin_x = [torch.from_numpy(a.view(np.int16)).pin_memory() for a in xs_h]
-        pin_l = [torch.from_numpy(a).pin_memory() for a in ls_h]
-        batches.append({"T": T, "x": xs, "l": ls, "px": pin_x, "pl": pin_l,
-                        "plan": Plan(T, n_exp, TOP_K),
-                        "out": torch.empty((T, D_MODEL), dtype=torch.int16, device=dev),
-                        "dx": torch.empty((T, D_MODEL), dtype=torch.int16, device=dev),
-                        "dl": torch.empty((T, n_exp), dtype=torch.float32, device=dev),
-                        "hout": torch.empty((T, D_MODEL), dtype=torch.int16).pin_memory(),
-                        "path": path_of(T)})
+    batches = make_batches(ctx, wl, base, path_of, use_router)
+    n_sets = wl.get("sets", N_SETS)
     for b in batches:  # size the workspace once for the largest call
         for op in (0, 1, 2):
             layer.workspace(b["T"], op)
-    # the kernel whose launches are timed in each batch: the path's main one
-    main_kind = {"decode": MOE_PROF_DECODE_GATEUP,
-                 "forward": moe.MOE_PROF_STREAM_COPY if n_slots else MOE_PROF_FORWARD_GEMM1}
+    stream = torch.cuda.current_stream()
+    main_kind = {"decode": moe.MOE_PROF_DECODE_GATEUP,
+                 "forward": moe.MOE_PROF_STREAM_COPY if n_slots else moe.MOE_PROF_FORWARD_GEMM1}
 
     def step(i, events=None, e2e=False, prof_kind=None):
         for bi, b in enumerate(batches):
@@ -400,182 +504,117 @@ def run_ours(args):
             if e2e:
                 b["hout"].copy_(b["out"], non_blocking=True)
 
-    def barrier():
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
+    def events(n_rows):
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in batches] for _ in range(n_rows)]
+        for row in ev:
+            for a, b in row:
+                a.record()
+                b.record()
+        return ev
 
-    gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    sampler = ClockSampler(gpu_id)
-    for i in range(args.warmup):
+    for i in range(warmup):
         step(i)
-    barrier()
-    # per-launch events of the dominant kernel over the timed region
-    n_b = len(batches)
-    kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(n_b)] for _ in range(args.steps)]
-    for row in kev:
-        for a, b in row:
-            a.record()
-            b.record()
+    ctx.barrier()
+    kev = events(steps)   # per-launch events of each batch's dominant kernel
     torch.cuda.synchronize()
     stats0 = layer.stats() if n_slots else None
     t_start = time.time()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for i in range(args.steps):
-        step(args.warmup + i, events=kev[i])
+    for i in range(steps):
+        step(warmup + i, events=kev[i])
     e1.record()
-    barrier()
+    ctx.barrier()
     t_end = time.time()
-    check(moe_profile_kernel(layer.h, MOE_PROF_NONE), "profile")
+    check(moe_profile_kernel(layer.h, moe.MOE_PROF_NONE), "profile")
     stats1 = layer.stats() if n_slots else None
     elapsed_ms = e0.elapsed_time(e1)
     kern_ms = [[a.elapsed_time(b) for (a, b) in row] for row in kev]
     check(layer.status(), "device status")
 
-    # end to end through the same calls with host buffers (copies inside the region)
-    for i in range(args.warmup):
+    for i in range(warmup):  # end to end through the same calls, host buffers
         step(i, e2e=True)
-    barrier()
+    ctx.barrier()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record()
-    for i in range(args.steps):
-        step(args.warmup + i, e2e=True)
+    for i in range(steps):
+        step(warmup + i, e2e=True)
     f1.record()
-    barrier()
+    ctx.barrier()
     e2e_ms = f0.elapsed_time(f1)
-    sampler.stop()
     clocks = sampler.summary(t_start, t_end)
-
-    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], dist, dev)
+    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], ctx.dist, ctx.dev)
 
     # per-kernel breakdown (separate untimed pass, one kernel bracketed at a time)
-    breakdown = {}
-    kinds = []
-    if any(b["path"] == "decode" for b in batches):
-        kinds += [("decode_gateup", moe.MOE_PROF_DECODE_GATEUP), ("decode_down", moe.MOE_PROF_DECODE_DOWN)]
-    if any(b["path"] == "forward" for b in batches):
-        kinds += [("gemm1_gateup", moe.MOE_PROF_FORWARD_GEMM1), ("gemm2_down", moe.MOE_PROF_FORWARD_GEMM2)]
-    if n_slots:
-        kinds += [("stream_copy", moe.MOE_PROF_STREAM_COPY)]
-    if use_router:
-        kinds += [("router", moe.MOE_PROF_ROUTER), ("shared_gateup", moe.MOE_PROF_SHARED_GATEUP),
-                  ("shared_down", moe.MOE_PROF_SHARED_DOWN)]
-    n_bd = min(args.steps, 5)
-    for name, kid in kinds:
-        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(n_b)] for _ in range(n_bd)]
-        for row in ev:
-            for a, b in row:
-                a.record()
-                b.record()
-        for i in range(n_bd):
-            step(i, events=ev[i], prof_kind=kid)
-        torch.cuda.synchronize()
-        # mean per call of the batches that launch this kernel
-        used = [bi for bi, b in enumerate(batches)
-                if (b["path"] == "decode") == name.startswith("decode") or name in
-                ("router", "shared_gateup", "shared_down")]
-        breakdown[name] = float(np.mean([ev[i][bi][0].elapsed_time(ev[i][bi][1])
-                                         for i in range(n_bd) for bi in used]))
-    check(moe_profile_kernel(layer.h, MOE_PROF_NONE), "profile")
-    tokens_step = sum(wl["Ts"])
-    value = job_tokens_per_s(world, tokens_step, args.steps, elapsed_ms)
-    e2e_value = job_tokens_per_s(world, tokens_step, args.steps, e2e_ms)
+    bd = {}
+    if breakdown:
+        kinds = []
+        if any(b["path"] == "decode" for b in batches):
+            kinds += [("decode_gateup", moe.MOE_PROF_DECODE_GATEUP),
+                      ("decode_down", moe.MOE_PROF_DECODE_DOWN)]
+        if any(b["path"] == "forward" for b in batches):
+            kinds += [("gemm1_gateup", moe.MOE_PROF_FORWARD_GEMM1),
+                      ("gemm2_down", moe.MOE_PROF_FORWARD_GEMM2)]
+        if n_slots:
+            kinds += [("stream_copy", moe.MOE_PROF_STREAM_COPY)]
+        if use_router:
+            kinds += [("router", moe.MOE_PROF_ROUTER), ("shared_gateup", moe.MOE_PROF_SHARED_GATEUP),
+                      ("shared_down", moe.MOE_PROF_SHARED_DOWN)]
+        n_bd = min(steps, 5)
+        for kname, kid in kinds:
+            ev = events(n_bd)
+            for i in range(n_bd):
+                step(i, events=ev[i], prof_kind=kid)
+            torch.cuda.synchronize()
+            used = [bi for bi, b in enumerate(batches)
+                    if (b["path"] == "decode") == kname.startswith("decode") or kname in
+                    ("router", "shared_gateup", "shared_down", "stream_copy")]
+            bd[kname] = float(np.mean([ev[i][bi][0].elapsed_time(ev[i][bi][1])
+                                       for i in range(n_bd) for bi in used]))
+        check(moe_profile_kernel(layer.h, moe.MOE_PROF_NONE), "profile")
 
-    # roofline of the dominant kernel: the timed kernel (per batch, its path's
-    # main kernel) with the largest share of the timed region; its bound is
-    # the one its arithmetic intensity puts it under
-    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
-        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
-    hbm_peak = peaks.get("hbm_gbs", 6800.0)
-    fp8_peak = 2.0 * peaks.get("bf16_tflops", 1900.0)  # kind::mxf8f6f4 runs at the FP8 rate
+    tokens_step = sum(wl["Ts"])
+    value = job_tokens_per_s(ctx.world, tokens_step, steps, elapsed_ms)
+    e2e_value = job_tokens_per_s(ctx.world, tokens_step, steps, e2e_ms)
     act = [int(b["plan"].active[0].item()) for b in batches]
     per_batch_ms = np.mean(np.array(kern_ms), axis=0)   # mean launch time per batch
-    kinds_t = {}
+    by_path = {}
     for bi, b in enumerate(batches):
-        kinds_t.setdefault(b["path"], []).append(bi)
-    dom = max(kinds_t, key=lambda k: sum(per_batch_ms[bi] for bi in kinds_t[k]))
-    bis = kinds_t[dom]
+        by_path.setdefault(b["path"], []).append(bi)
+    dom = max(by_path, key=lambda k: sum(per_batch_ms[bi] for bi in by_path[k]))
+    bis = by_path[dom]
     ms_avg = float(np.mean([per_batch_ms[bi] for bi in bis]))
-    if dom == "decode":
-        # gate/up kernel: active experts' gate+up codes and scales, f16 x rows read,
-        # f16 h and its exponents written (active counts from the last step's plans)
-        nbytes = [act[bi] * GATEUP_BYTES + wl["Ts"][bi] * D_MODEL * 2 +
-                  wl["Ts"][bi] * TOP_K * (D_FF * 2 + D_FF // 32) for bi in bis]
-        nflop = [2.0 * wl["Ts"][bi] * TOP_K * 2 * D_MODEL * D_FF for bi in bis]
-        kname, src, tkey = "moe_decode_gateup_kernel", "decode.cu", args.workload
-    else:
-        # GEMM1: active experts' gate+up weights, two-term activation tiles in,
-        # two-term h tiles out (one byte per term and element)
-        nbytes = [act[bi] * GATEUP_BYTES + wl["Ts"][bi] * TOP_K * (2 * D_MODEL + 2 * D_FF)
-                  for bi in bis]
-        nflop = [2.0 * wl["Ts"][bi] * TOP_K * 2 * D_MODEL * D_FF for bi in bis]
-        kname, src, tkey = "moe_grouped_gemm_kernel<0>", "grouped_gemm.cu", args.workload
-    b_avg, f_avg = float(np.mean(nbytes)), float(np.mean(nflop))
-    gbs = b_avg / (ms_avg * 1e-3) / 1e9
-    tfs = f_avg / (ms_avg * 1e-3) / 1e12
-    mem_bound = (b_avg / hbm_peak) >= (f_avg / 1e3 / fp8_peak)  # time at peak: bytes vs flops
-    src_peak = "measured" if peaks else "fallback"
-    if mem_bound:
-        roof = {"bound": "hbm", "kernel": kname, "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                "frac": gbs / hbm_peak, "peak_source": src_peak + " (copy bandwidth)",
-                "bytes_per_launch": b_avg, "tensor_TFLOPs": tfs, "frac_of_fp8_peak": tfs / fp8_peak}
-    else:
-        roof = {"bound": "tensor", "kernel": kname, "achieved": tfs, "peak": fp8_peak,
-                "unit": "TFLOP/s", "frac": tfs / fp8_peak,
-                "peak_source": src_peak + " bf16 x 2 (FP8 rate; the two-term activation split "
-                               "issues 2 MMAs per algorithmic one, so frac <= 0.5)",
-                "flop_per_launch": f_avg, "hbm_GBs": gbs, "frac_of_hbm": gbs / hbm_peak}
-    roof["frac_of_fp4_peak"] = tfs / (6.0 * peaks.get("bf16_tflops", 1900.0))
-    roof["traffic"] = kernel_traffic(kname, src, tkey)
+    work = [kernel_work(dom, wl["Ts"][bi], act[bi]) for bi in bis]
+    nbytes, nflop = float(np.mean([w_[0] for w_ in work])), float(np.mean([w_[1] for w_ in work]))
+    roof = roofline(dom, nbytes, nflop, ms_avg, peaks, name)
     stream_info = None
     if n_slots:
-        # the copy of the missing experts is bound by the host-to-device link:
-        # miss bytes in the timed region over the summed copy-kernel time, against
-        # the link's copy bandwidth measured here (pinned host -> device, 2 GiB)
-        hits = stats1[0] - stats0[0]
-        misses = stats1[1] - stats0[1]
-        copy_ms = float(np.sum(np.array(kern_ms)))
-        link = torch.empty(1 << 31, dtype=torch.uint8, pin_memory=True)
-        dst = torch.empty(1 << 31, dtype=torch.uint8, device=dev)
-        best = None
-        for _ in range(3):
-            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a0.record()
-            dst.copy_(link, non_blocking=True)
-            a1.record()
-            torch.cuda.synchronize()
-            t = a0.elapsed_time(a1)
-            best = t if best is None else min(best, t)
-        h2d = (1 << 31) / (best * 1e-3) / 1e9
-        del link, dst
-        # bytes crossing the link per missing expert: the expert itself, or
-        # from a store its stored tiles (the store's mean per expert)
-        store = getattr(layer, "store", None)
-        link_bytes = store.blob_bytes / n_exp if store is not None else EXPERT_BYTES
-        gbs_c = misses * link_bytes / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else 0.0
-        roof = {"bound": "host-to-device link",
-                "kernel": "moe_store_decode_kernel" if store is not None else "moe_stream_copy_kernel",
-                "achieved": gbs_c, "peak": h2d, "unit": "GB/s",
-                "frac": gbs_c / h2d if h2d else None,
-                "peak_source": "measured in this run: cudaMemcpyAsync of 2 GiB pinned host memory "
-                               "to the device",
-                "bytes_per_launch": misses * link_bytes / max(1, args.steps * len(batches)),
-                "traffic": None}
-        stream_info = {"slots": layer.n_slots, "hit_rate": hits / max(1, hits + misses),
-                       "misses_per_step": misses / args.steps,
-                       "copy_ms_per_step": copy_ms / args.steps}
-        if store is not None:
-            roof["decoded_GBs"] = misses * EXPERT_BYTES / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else 0.0
-            roof["link_bytes_per_expert"] = "stored bytes, the store's mean per expert"
-            stream_info["store"] = store_info
-
-    # plan: one fused kernel for T <= 64, else top-k, count, scan, scatter;
-    # decode: gate/up, down, combine; forward: quant, schedule, gather, two GEMMs,
-    # finalize (T <= 16: one fused quant/gather kernel, two GEMMs, finalize)
+        roof, stream_info = stream_roofline(ctx, layer, stats0, stats1, kern_ms, steps,
+                                            len(batches), store_info)
+    h2d = sum(T * D_MODEL * 2 + (0 if use_router else T * ctx.n_exp * 4) for T in wl["Ts"])
+    d2h = sum(T * D_MODEL * 2 for T in wl["Ts"])
+    record = {
+        "workload": wl["desc"], "T": wl["Ts"],
+        "path": ("moe_plan (router)" if use_router else "moe_plan") + " + " +
+                ", ".join(f"moe_{b['path']} (T={b['T']})" for b in batches),
+        "steps": steps, "warmup": warmup, "ms_per_step": elapsed_ms / steps,
+        "tokens_per_s": value,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "active_experts_last_step": act,
+        "dominant_kernel_ms": ms_avg,
+        "roofline": roof,
+        "clocks": clocks,
+    }
+    if bd:
+        record["kernel_ms_per_call"] = bd
+    if stream_info:
+        record["expert_cache"] = stream_info
+    # launches of the library's kernels per step: plan (one fused kernel for
+    # T <= 64, else top-k, count, scan, scatter); decode: gate/up, down,
+    # combine; forward: quant, schedule, gather, two GEMMs, finalize (T <= 16:
+    # one fused quant/gather kernel, two GEMMs, finalize)
     launches = 0
     for b in batches:
         launches += 1 if b["T"] <= 64 else 4
@@ -584,34 +623,119 @@ def run_ours(args):
             launches += 4   # cache: replacement, copy of the misses, two scale re-layouts
         if use_router:
             launches += 1 + 2   # router GEMM; shared gate/up and down GEMMs
+    record["gpu_launches_per_step"] = launches
+    for b in batches:
+        del b["x"], b["l"]
+    torch.cuda.empty_cache()
+    return record
+
+
+def stream_roofline(ctx, layer, stats0, stats1, kern_ms, steps, n_batches, store_info):
+    """Expert streaming: the copy (or store decode) of the missing experts is
+    bound by the host-to-device link; miss bytes in the timed region over the
+    summed copy-kernel time, against the link's copy bandwidth measured here
+    (pinned host -> device, 2 GiB)."""
+    import numpy as np
+    import torch
+    hits = stats1[0] - stats0[0]
+    misses = stats1[1] - stats0[1]
+    copy_ms = float(np.sum(np.array(kern_ms)))
+    link = torch.empty(1 << 31, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(1 << 31, dtype=torch.uint8, device=ctx.dev)
+    best = None
+    for _ in range(3):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        dst.copy_(link, non_blocking=True)
+        a1.record()
+        torch.cuda.synchronize()
+        t = a0.elapsed_time(a1)
+        best = t if best is None else min(best, t)
+    h2d = (1 << 31) / (best * 1e-3) / 1e9
+    del link, dst
+    # bytes crossing the link per missing expert: the expert itself, or from a
+    # store its stored tiles (the store's mean per expert)
+    store = getattr(layer, "store", None)
+    link_bytes = store.blob_bytes / ctx.n_exp if store is not None else EXPERT_BYTES
+    gbs_c = misses * link_bytes / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else 0.0
+    roof = {"bound": "host-to-device link",
+            "kernel": "moe_store_decode_kernel" if store is not None else "moe_stream_copy_kernel",
+            "achieved": gbs_c, "peak": h2d, "unit": "GB/s",
+            "frac": gbs_c / h2d if h2d else None,
+            "peak_source": "measured in this run: cudaMemcpyAsync of 2 GiB pinned host memory "
+                           "to the device",
+            "bytes_per_launch": misses * link_bytes / max(1, steps * n_batches),
+            "traffic": None}
+    info = {"slots": layer.n_slots, "hit_rate": hits / max(1, hits + misses),
+            "misses_per_step": misses / steps, "copy_ms_per_step": copy_ms / steps}
+    if store is not None:
+        roof["decoded_GBs"] = misses * EXPERT_BYTES / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else 0.0
+        roof["link_bytes_per_expert"] = "stored bytes, the store's mean per expert"
+        info["store"] = store_info
+    return roof, info
+
+
+# Workloads that get a record of their own in the default run's line.
+RECORDS = ("decode_T1", "decode_T4", "decode_T16", "prefill4k", "skewed8k", "router16k")
+
+
+def run_ours(args):
+    import torch
+    n_exp = args.experts or N_EXPERTS
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ctx = Ctx(args, n_exp, dev, rank, world, dist)
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    sampler = ClockSampler("GPU-" + str(torch.cuda.get_device_properties(dev).uuid))
+    wl = dict(BENCH_WORKLOADS[args.workload])
+    if args.tokens:
+        wl["Ts"] = [args.tokens]
+    head = measure(ctx, args.workload, wl, args.steps, args.warmup, sampler, peaks,
+                   path_override=args.path)
+    records = {}
+    if args.workload == "decode" and not (args.no_records or args.experts or args.tokens):
+        rec_steps = min(args.steps, 100)   # keeps the default run within a few minutes
+        for name in RECORDS:
+            records[name] = measure(ctx, name, BENCH_WORKLOADS[name], rec_steps, args.warmup,
+                                    sampler, peaks)
+    sampler.stop()
+    config = {"workload": wl["desc"], "path": head["path"],
+              "tokens_per_step": sum(wl["Ts"]),
+              "active_experts_last_step": head["active_experts_last_step"],
+              "kernel_ms_per_call": head.get("kernel_ms_per_call", {}),
+              **({"expert_cache": head["expert_cache"]} if "expert_cache" in head else {}),
+              "l2": "inputs larger than L2: every step reads at least 280 MB of expert weights "
+                    "(L2 129 MB) and the inputs rotate through "
+                    f"{wl.get('sets', N_SETS)} pre-generated sets, so the selected experts "
+                    "change from step to step",
+              "parallelism": f"replicas x{world}"}
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "metric": METRIC, "value": head["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": " / ".join(sorted({"mxfp4 x f16 -> f32" if b["path"] == "decode" else
-                                    "mxfp4 x 2-term e4m3 -> f32" for b in batches})),
+        "dtype": "mxfp4 x f16 -> f32" if (args.path or wl["path"]) == "decode" and CROSSOVER_T
+                 else "mxfp4 x 2-term e4m3 -> f32",
         "data": "synthetic (seeded Philox weights, N(0,1) activations and logits)",
-        "config": {"workload": wl["desc"],
-                   "path": ("moe_plan (router)" if use_router else "moe_plan") + " + " +
-                           ", ".join(f"moe_{b['path']} (T={b['T']})" for b in batches),
-                   "tokens_per_step": tokens_step, "active_experts_last_step": act,
-                   "kernel_ms_per_call": breakdown,
-                   **({"expert_cache": stream_info} if stream_info else {}),
-                   "l2": f"inputs larger than L2: a step reads {sum(act) * EXPERT_BYTES / 1e6:.0f} MB "
-                         f"of expert weights (L2 129 MB) before any batch recurs, and "
-                         f"{wl.get('sets', N_SETS)} rotating logit sets change the experts of "
-                         "each batch from step to step",
-                   "parallelism": f"replicas x{world}"},
-        "roofline": roof,
+        "config": config,
+        "roofline": head["roofline"],
         **({"profiling_case": f"{n_exp} experts, batches {wl['Ts']}; not a bench value"}
            if n_exp != N_EXPERTS or args.tokens else {}),
-        "e2e": {"value": e2e_value, "unit": "tokens/s",
-                "h2d_bytes_per_step": sum(T * D_MODEL * 2 + (0 if use_router else T * n_exp * 4)
-                                          for T in wl["Ts"]),
-                "d2h_bytes_per_step": sum(T * D_MODEL * 2 for T in wl["Ts"])},
-        "gpu_launches": launches * args.steps,
-        "clocks": clocks,
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches_per_step"] * args.steps,
+        "clocks": head["clocks"],
     }
+    if records:
+        line["workloads"] = records
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, tok, el, threads = oracle_tokens_per_s(args.workload, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": threads,
@@ -621,7 +745,7 @@ def run_ours(args):
                                           "of the sampled token, fp64)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    layer.close()
+    ctx.close()
     if dist is not None:
         dist.destroy_process_group()
     return 0

@@ -42,3 +42,24 @@ def test_traffic_lookup_requires_the_current_kernel_source():
         got = bench.kernel_traffic(name, "grouped_gemm.cu", wl)
         assert got == (float(nbytes) if h == sha else None)
     assert bench.kernel_traffic("moe_grouped_gemm_kernel<0>", "grouped_gemm.cu", "no-such") is None
+
+
+def test_default_run_records_and_their_roofline_arithmetic():
+    bench.use_shape({})
+    assert set(bench.RECORDS) <= set(bench.BENCH_WORKLOADS)
+    for name in bench.RECORDS:
+        assert bench.base_workload(name).D == 7168
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0}
+    # a one-token forward: 16 experts' gate/up weights, far below the tensor roof
+    nbytes, flop = bench.kernel_work("forward", 1, 16)
+    assert nbytes == 16 * bench.GATEUP_BYTES + 16 * (2 * 7168 + 2 * 1536)
+    assert flop == 2.0 * 16 * 2 * 7168 * 1536
+    r = bench.roofline("forward", nbytes, flop, nbytes / 6000e9 * 1e3 * 2, peaks, "x")
+    assert r["bound"] == "hbm" and abs(r["frac"] - 0.5) < 1e-12
+    assert abs(r["frac_of_binding_roof"] - 0.5) < 1e-12
+    # 16384 tokens over every expert: two MMAs per algorithmic one at the FP8 rate bind
+    nbytes, flop = bench.kernel_work("forward", 16384, 896)
+    tensor_ms = 2 * flop / 4000e12 * 1e3
+    r = bench.roofline("forward", nbytes, flop, 4 * tensor_ms, peaks, "x")
+    assert r["bound"] == "tensor" and abs(r["frac_of_binding_roof"] - 0.25) < 1e-12
+    assert abs(r["frac"] - 0.125) < 1e-12   # of the FP8 peak, two-term work counted once
