@@ -126,7 +126,8 @@ __device__ __forceinline__ float warp_select_weight(float my_v, int k, int lane)
     return ex / s;
 }
 
-// Exclusive block scan of one int per thread (blockDim.x == 1024).
+// Exclusive block scan of one int per thread over a block of NW warps.
+template <int NW>
 __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &total) {
     int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     int inc = v;
@@ -138,7 +139,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &t
     if (lane == 31) warp_tot[wid] = inc;
     __syncthreads();
     if (wid == 0) {
-        int t = warp_tot[lane];
+        int t = lane < NW ? warp_tot[lane] : 0;
         int ti = t;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -183,8 +184,15 @@ __device__ __forceinline__ void warp_stable_scatter(const int32_t *idx, int64_t 
 
 // ---------------------------------------------------------------------------
 // Small batches: one CTA does top-k, histogram, scan and the stable scatter.
+// 512 threads (16 warps): each warp selects for its tokens with the 32 keys
+// of a lane in registers (a 1024-thread block would cap a thread at 64
+// registers and push the keys to local memory, which made the one-token
+// selection latency-bound); the scans take two experts per thread.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) moe_plan_small_kernel(
+constexpr int kPlanSmallThreads = 512;
+constexpr int kPlanSmallWarps = kPlanSmallThreads / 32;
+
+__global__ void __launch_bounds__(kPlanSmallThreads) moe_plan_small_kernel(
     int T, int E, int k, const float *__restrict__ logits, int32_t *topk_idx, float *topk_w,
     int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *active, int *status) {
     // T <= 64 tokens, k <= 32: the selections stay in shared memory, and each
@@ -194,15 +202,18 @@ __global__ void __launch_bounds__(1024) moe_plan_small_kernel(
     __shared__ int s_cnt[MOE_MAX_EXPERTS];
     __shared__ unsigned long long s_mask[MOE_MAX_EXPERTS];
     __shared__ int s_idx[64 * MOE_MAX_TOPK];
-    __shared__ uint2 s_scratch[32][MOE_MAX_TOPK];
+    __shared__ uint2 s_scratch[kPlanSmallWarps][MOE_MAX_TOPK];
     __shared__ int s_tot[33];
     __shared__ int s_nan;
+    static_assert(2 * kPlanSmallThreads == MOE_MAX_EXPERTS, "two experts per thread in the scans");
     int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    s_cnt[tid] = 0;
-    s_mask[tid] = 0ull;
+    for (int e = tid; e < MOE_MAX_EXPERTS; e += kPlanSmallThreads) {
+        s_cnt[e] = 0;
+        s_mask[e] = 0ull;
+    }
     if (tid == 0) s_nan = 0;
     __syncthreads();
-    for (int t = wid; t < T; t += 32) {
+    for (int t = wid; t < T; t += kPlanSmallWarps) {
         int my_e;
         float my_v;
         bool nan_seen = false;
@@ -219,23 +230,32 @@ __global__ void __launch_bounds__(1024) moe_plan_small_kernel(
     }
     __syncthreads();
     if (tid == 0 && s_nan) moe_flag(status, MOE_ERR_NAN_LOGIT);
-    int c = tid < E ? s_cnt[tid] : 0;
+    // experts e0 = 2 tid and e0 + 1 (counts are zero past E)
+    const int e0 = 2 * tid;
+    const int c0 = e0 < E ? s_cnt[e0] : 0, c1 = e0 + 1 < E ? s_cnt[e0 + 1] : 0;
     int total;
-    int off = block_exclusive_scan(c, s_tot, total);
-    int a = block_exclusive_scan(c > 0 ? 1 : 0, s_tot, total);
-    if (tid < E) {
-        counts[tid] = c;
-        offsets[tid] = off;
-        if (c > 0) active[1 + a] = tid;
+    const int off = block_exclusive_scan<kPlanSmallWarps>(c0 + c1, s_tot, total);
+    const int a0 = c0 > 0 ? 1 : 0, a1 = c1 > 0 ? 1 : 0;
+    const int a = block_exclusive_scan<kPlanSmallWarps>(a0 + a1, s_tot, total);
+    if (e0 < E) {
+        counts[e0] = c0;
+        offsets[e0] = off;
+        if (a0) active[1 + a] = e0;
+    }
+    if (e0 + 1 < E) {
+        counts[e0 + 1] = c1;
+        offsets[e0 + 1] = off + c0;
+        if (a1) active[1 + a + a0] = e0 + 1;
     }
     if (tid == 0) {
         offsets[E] = T * k;
         active[0] = total;
     }
     __syncthreads();
-    if (tid < E) s_cnt[tid] = off;
+    if (e0 < E) s_cnt[e0] = off;
+    if (e0 + 1 < E) s_cnt[e0 + 1] = off + c0;
     __syncthreads();
-    for (int f = tid; f < T * k; f += blockDim.x) {
+    for (int f = tid; f < T * k; f += kPlanSmallThreads) {
         const int t = f / k, e = s_idx[f];
         const int pos = s_cnt[e] + __popcll(s_mask[e] & ((1ull << t) - 1ull));
         perm[pos] = f;
@@ -306,8 +326,8 @@ __global__ void __launch_bounds__(1024) moe_plan_scan_kernel(int T, int E, int k
         }
     }
     int total;
-    int off = block_exclusive_scan(run, s_tot, total);
-    int a = block_exclusive_scan(run > 0 ? 1 : 0, s_tot, total);
+    int off = block_exclusive_scan<32>(run, s_tot, total);
+    int a = block_exclusive_scan<32>(run > 0 ? 1 : 0, s_tot, total);
     if (e < E) {
         counts[e] = run;
         offsets[e] = off;
@@ -350,7 +370,7 @@ size_t moe_plan_ws_bytes(int T, int E) {
 cudaError_t moe_launch_plan(int T, int E, int k, const float *logits, const moe_plan_buf *p,
                             void *ws, int *status, cudaStream_t st) {
     if (moe_plan_is_small(T)) {
-        moe_plan_small_kernel<<<1, 1024, 0, st>>>(T, E, k, logits, p->topk_idx, p->topk_w,
+        moe_plan_small_kernel<<<1, kPlanSmallThreads, 0, st>>>(T, E, k, logits, p->topk_idx, p->topk_w,
                                                   p->counts, p->offsets, p->perm, p->inv,
                                                   p->active, status);
         return cudaGetLastError();
