@@ -78,6 +78,13 @@ BENCH_WORKLOADS = {
     "decode_T16": {"Ts": [16], "path": "forward", "desc": "K3 routed layer decode, T=16"},
     "prefill4k": {"Ts": [4096], "path": "forward",
                   "desc": "K3 routed layer prefill, T=4096, uniform routing"},
+    "prefill4k_fp4": {"Ts": [4096], "path": "forward", "act": 1, "base": "prefill4k",
+                      "desc": "K3 routed layer prefill, T=4096, uniform routing, FP4 x FP4 mode "
+                              "(MXFP4 activations, kind::mxf4; not the parity path)"},
+    "router16k_fp4": {"Ts": [16384], "path": "forward", "router": True, "sets": 2, "act": 1,
+                      "base": "router16k",
+                      "desc": "K3 routed layer long prefill, T=16384, in-library fp32 router + "
+                              "one bf16 shared expert, FP4 x FP4 mode for the routed experts"},
     "skewed8k": {"Ts": [8192], "path": "forward",
                  "desc": "K3 routed layer prefill, T=8192, Zipf(1.1)-skewed routing"},
     "router16k": {"Ts": [16384], "path": "forward", "router": True, "sets": 2,
@@ -336,8 +343,9 @@ def make_layer(ctx, wl, base):
     from mxfp4_routed_expert_03_gb300.layer import Layer
     codes = wl.get("codes", synth.CODES_UNIFORM)
     n_slots = wl.get("stream_slots")
+    act = wl.get("act", 0)
     kind = ("router" if wl.get("router") else "stream_store" if wl.get("store") else
-            "stream" if n_slots else "plain", codes)
+            "stream" if n_slots else "plain", codes, act)
     if kind in ctx.layers:
         return ctx.layers[kind], None
     weights = ctx.layer_weights(codes, base.seed)
@@ -347,7 +355,8 @@ def make_layer(ctx, wl, base):
             synth.make_w_router(dataclasses.replace(base, E=ctx.n_exp))).to(ctx.dev)
         shared = {k: torch.from_numpy(v.view(np.int16)).to(ctx.dev)
                   for k, v in synth.make_shared(base).items()}
-        layer = Layer(D_MODEL, D_FF, ctx.n_exp, TOP_K, weights, MOE_ROUTER_XWR, w_router, shared)
+        layer = Layer(D_MODEL, D_FF, ctx.n_exp, TOP_K, weights, MOE_ROUTER_XWR, w_router, shared,
+                      act_mode=act)
     elif n_slots:
         # the slow tier: all experts in pinned host memory; the layer caches
         # n_slots of them in HBM
@@ -363,11 +372,12 @@ def make_layer(ctx, wl, base):
                     "stored_over_raw": store.blob_bytes / store.raw_bytes}
             del host
             layer = StreamingLayer(D_MODEL, D_FF, ctx.n_exp, TOP_K, None,
-                                   min(n_slots, ctx.n_exp), store=store)
+                                   min(n_slots, ctx.n_exp), store=store, act_mode=act)
         else:
-            layer = StreamingLayer(D_MODEL, D_FF, ctx.n_exp, TOP_K, host, min(n_slots, ctx.n_exp))
+            layer = StreamingLayer(D_MODEL, D_FF, ctx.n_exp, TOP_K, host, min(n_slots, ctx.n_exp),
+                                   act_mode=act)
     else:
-        layer = Layer(D_MODEL, D_FF, ctx.n_exp, TOP_K, weights)
+        layer = Layer(D_MODEL, D_FF, ctx.n_exp, TOP_K, weights, act_mode=act)
     layer.prepare()
     ctx.layers[kind] = layer
     return layer, info
@@ -404,21 +414,25 @@ def make_batches(ctx, wl, base, path_of, use_router):
     return batches
 
 
-def kernel_work(path: str, T: int, active: int):
+def kernel_work(path: str, T: int, active: int, fp4: bool = False):
     """Algorithmic bytes and flops of one launch of a batch's dominant kernel:
     the gate/up GEMM of moe_forward (active experts' gate+up weights, the
     two-term activation rows in and the two-term h rows out, one byte per
-    term and element) or the gate/up kernel of moe_decode (the same weights,
-    bf16 x rows in, f16 h rows and their exponents out)."""
+    term and element; in the FP4 x FP4 mode one MXFP4 term, half a byte per
+    element plus a scale byte per 32) or the gate/up kernel of moe_decode
+    (the same weights, bf16 x rows in, f16 h rows and their exponents out)."""
     flop = 2.0 * T * TOP_K * 2 * D_MODEL * D_FF
     if path == "decode":
         nbytes = active * GATEUP_BYTES + T * D_MODEL * 2 + T * TOP_K * (D_FF * 2 + D_FF // 32)
+    elif fp4:
+        nbytes = active * GATEUP_BYTES + T * TOP_K * (D_MODEL // 2 + D_MODEL // 32 +
+                                                      D_FF // 2 + D_FF // 32)
     else:
         nbytes = active * GATEUP_BYTES + T * TOP_K * (2 * D_MODEL + 2 * D_FF)
     return float(nbytes), flop
 
 
-def roofline(path, nbytes, flop, ms, peaks, workload, store=None):
+def roofline(path, nbytes, flop, ms, peaks, workload, fp4=False):
     """Roofline of the dominant kernel: achieved algorithmic bytes or flops per
     launch over its mean launch time, against the measured peak of the bound
     its arithmetic intensity puts it under."""
@@ -431,6 +445,9 @@ def roofline(path, nbytes, flop, ms, peaks, workload, store=None):
     if path == "decode":
         kname, csrc = "moe_decode_gateup_kernel", "decode.cu"
         tensor_time = 0.0   # CUDA cores: bound by bytes
+    elif fp4:
+        kname, csrc = "moe_grouped_gemm_kernel<0, fp4>", "grouped_gemm.cu"
+        tensor_time = flop / 1e12 / fp4_peak          # one MXFP4 term, kind::mxf4
     else:
         kname, csrc = "moe_grouped_gemm_kernel<0>", "grouped_gemm.cu"
         tensor_time = 2.0 * flop / 1e12 / fp8_peak   # two MMAs per algorithmic one
@@ -438,6 +455,11 @@ def roofline(path, nbytes, flop, ms, peaks, workload, store=None):
     if mem_bound:
         r = {"bound": "hbm", "kernel": kname, "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
              "frac": gbs / hbm_peak, "peak_source": src + " (copy bandwidth)"}
+    elif fp4:
+        r = {"bound": "tensor", "kernel": kname, "achieved": tfs, "peak": fp4_peak,
+             "unit": "TFLOP/s", "frac": tfs / fp4_peak,
+             "peak_source": src + " bf16 x 6 (FP4 rate, nominal 13.5 / 2.25)",
+             "hbm_GBs": gbs, "frac_of_hbm": gbs / hbm_peak}
     else:
         r = {"bound": "tensor", "kernel": kname, "achieved": tfs, "peak": fp8_peak,
              "unit": "TFLOP/s", "frac": tfs / fp8_peak,
@@ -585,9 +607,10 @@ def measure(ctx, name, wl, steps, warmup, sampler, peaks, breakdown=True, path_o
     dom = max(by_path, key=lambda k: sum(per_batch_ms[bi] for bi in by_path[k]))
     bis = by_path[dom]
     ms_avg = float(np.mean([per_batch_ms[bi] for bi in bis]))
-    work = [kernel_work(dom, wl["Ts"][bi], act[bi]) for bi in bis]
+    fp4 = bool(wl.get("act", 0))
+    work = [kernel_work(dom, wl["Ts"][bi], act[bi], fp4) for bi in bis]
     nbytes, nflop = float(np.mean([w_[0] for w_ in work])), float(np.mean([w_[1] for w_ in work]))
-    roof = roofline(dom, nbytes, nflop, ms_avg, peaks, name)
+    roof = roofline(dom, nbytes, nflop, ms_avg, peaks, name, fp4)
     stream_info = None
     if n_slots:
         roof, stream_info = stream_roofline(ctx, layer, stats0, stats1, kern_ms, steps,
@@ -676,7 +699,8 @@ def stream_roofline(ctx, layer, stats0, stats1, kern_ms, steps, n_batches, store
 
 
 # Workloads that get a record of their own in the default run's line.
-RECORDS = ("decode_T1", "decode_T4", "decode_T16", "prefill4k", "skewed8k", "router16k")
+RECORDS = ("decode_T1", "decode_T4", "decode_T16", "prefill4k", "skewed8k", "router16k",
+           "prefill4k_fp4", "router16k_fp4")
 
 
 def run_ours(args):

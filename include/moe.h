@@ -97,6 +97,23 @@ enum moe_prof_kernel {
                                      of the missing experts from host memory */
 };
 
+/* Precision of the activations the tensor cores see in moe_forward.
+ * MOE_ACT_EXACT: x and h as two E4M3 terms with an E8M0 scale per 32 values
+ * each, about bf16's 8 significant bits, within the layer's parity tolerance.
+ * MOE_ACT_MXFP4: the FP4 x FP4 mode, x and h as one MXFP4 term (E2M1 with an
+ * E8M0 scale per 32, converted as OCP MX v1.0 section 6.3 specifies: scale
+ * 2^(floor(log2 max|v|) - 2), elements rounded to nearest even, clamped to
+ * 6), MMAs of kind::mxf4 at the FP4 tensor rate. Its output differs from the
+ * exact layer by far more than bf16 rounding (normwise max error about 0.2 on
+ * N(0,1) inputs at the K3 shape): a separately reported fast mode for the
+ * pages' MXFP4 expert kernels shared by the K3 and MiMo lanes (Moonshine
+ * GitHub README, "Running MiMo V2.6 Flash"), not the parity path. moe_decode
+ * always computes with exact products (it ignores act_mode). */
+enum moe_act_mode {
+    MOE_ACT_EXACT = 0,
+    MOE_ACT_MXFP4 = 1
+};
+
 /* Layer shape. Supported envelope: d_model a multiple of 256, d_ff of 128,
  * d_model <= 16384, d_ff <= 8192, 1 <= top_k <= 32, top_k <= n_experts <= 1024. */
 typedef struct moe_desc {
@@ -106,6 +123,7 @@ typedef struct moe_desc {
     int32_t top_k;
     int32_t router_mode;  /* enum moe_router_mode */
     int32_t has_shared;   /* 1: one always-on bf16 SwiGLU shared expert, weight 1.0 */
+    int32_t act_mode;     /* enum moe_act_mode (moe_forward only) */
 } moe_desc;
 
 /* Device pointers to the layer's weights (see layouts above). Unused fields NULL. */

@@ -26,6 +26,7 @@ struct moe_handle {
     int num_sms;
     int *status;  // device word: first error code recorded by a kernel
     CUtensorMap map_gate, map_up, map_down;  // TMA views of the packed E2M1 weights
+    CUtensorMap map4_gate, map4_up, map4_down;  // the same bytes unexpanded (FP4 x FP4 mode)
     CUtensorMap map_sh_gate, map_sh_up, map_sh_down;  // bf16 shared expert (has_shared)
     CUtensorMap map_wr[3];  // the three bf16 terms of W_r (router_mode XWR, after prepare)
     const uint8_t *atoms;  // caller buffer filled by moe_prepare (NULL until then)
@@ -170,6 +171,7 @@ static int create_impl(const moe_desc *d, const moe_weights *w, int wE, moe_hand
     if (d->router_mode != MOE_ROUTER_LOGITS && d->router_mode != MOE_ROUTER_XWR)
         return MOE_ERR_INVALID_ARG;
     if (d->has_shared != 0 && d->has_shared != 1) return MOE_ERR_INVALID_ARG;
+    if (d->act_mode != MOE_ACT_EXACT && d->act_mode != MOE_ACT_MXFP4) return MOE_ERR_INVALID_ARG;
     if (d->top_k > d->n_experts) return MOE_ERR_INVALID_ARG;
     if (d->d_model % 256 || d->d_ff % 128 || d->d_model > MOE_MAX_DMODEL ||
         d->d_ff > MOE_MAX_DFF || d->top_k > MOE_MAX_TOPK || d->n_experts > MOE_MAX_EXPERTS)
@@ -215,6 +217,15 @@ static int create_impl(const moe_desc *d, const moe_weights *w, int wE, moe_hand
         if (!make_map_2d(&h->map_gate, fp4, w->gate_q, D, E * F, D / 2, 128, 64) ||
             !make_map_2d(&h->map_up, fp4, w->up_q, D, E * F, D / 2, 128, 64) ||
             !make_map_2d(&h->map_down, fp4, w->down_q, F, E * D, F / 2, 128, 128)) {
+            free(h);
+            return MOE_ERR_CUDA;
+        }
+        // FP4 x FP4 mode: 128-byte boxes (two 128-wide K blocks) of packed codes
+        const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        if (d->act_mode == MOE_ACT_MXFP4 &&
+            (!make_map_2d(&h->map4_gate, u8, w->gate_q, D / 2, E * F, D / 2, 128, 64) ||
+             !make_map_2d(&h->map4_up, u8, w->up_q, D / 2, E * F, D / 2, 128, 64) ||
+             !make_map_2d(&h->map4_down, u8, w->down_q, F / 2, E * D, F / 2, 128, 128))) {
             free(h);
             return MOE_ERR_CUDA;
         }
@@ -643,12 +654,24 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     int32_t *prefix = (int32_t *)(base + L.prefix);
 
     // Small batches (every expert one token tile): quantise, gather, schedule
-    // and zero the accumulator in one launch; larger ones in four.
+    // and zero the accumulator in one launch; larger ones in four (the FP4 x
+    // FP4 mode quantises while gathering: three).
     const bool small = T <= MOE_GEMM_NT_NARROW;
+    const bool fp4 = d.act_mode == MOE_ACT_MXFP4;
     cudaError_t err;
-    if (small) {
+    if (small && fp4) {
+        err = moe_launch_prep_small_fp4(T, E, k, D, plan->offsets, plan->perm, plan->active, x,
+                                        prefix, xb, xa, d.has_shared ? nullptr : acc, h->status,
+                                        st);
+    } else if (small) {
         err = moe_launch_prep_small(T, E, k, D, plan->offsets, plan->perm, plan->active, x, prefix,
                                     xb, xa, d.has_shared ? nullptr : acc, h->status, st);
+    } else if (fp4) {
+        err = moe_launch_schedule(E, MOE_GEMM_NTMAX, plan->offsets, plan->active, prefix,
+                                  h->status, st);
+        if (err == cudaSuccess)
+            err = moe_launch_gather_x_fp4(L.max_tt, E, k, rows, D, plan->offsets, plan->perm,
+                                          plan->active, prefix, x, xb, xa, h->status, st);
     } else {
         err = moe_launch_quant_x(T, D, x, xq_hi, xq_lo, xs_hi, xs_lo, st);
         if (err == cudaSuccess)
@@ -691,7 +714,10 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         g1.h_atoms = ha;
         g1.inject = h->inject;
         h->prof.before(MOE_PROF_FORWARD_GEMM1, st);
-        err = moe_launch_gemm(MOE_GEMM_GATEUP, &h->map_gate, &h->map_up, &g1, T, h->num_sms, st);
+        err = fp4 ? moe_launch_gemm(MOE_GEMM_GATEUP, &h->map4_gate, &h->map4_up, &g1, T,
+                                    h->num_sms, 1, st)
+                  : moe_launch_gemm(MOE_GEMM_GATEUP, &h->map_gate, &h->map_up, &g1, T,
+                                    h->num_sms, 0, st);
         h->prof.after(MOE_PROF_FORWARD_GEMM1, st);
     }
     if (err == cudaSuccess) {
@@ -713,7 +739,10 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         g2.b_atoms = ha;
         g2.acc = acc;
         h->prof.before(MOE_PROF_FORWARD_GEMM2, st);
-        err = moe_launch_gemm(MOE_GEMM_DOWN, &h->map_down, &h->map_down, &g2, T, h->num_sms, st);
+        err = fp4 ? moe_launch_gemm(MOE_GEMM_DOWN, &h->map4_down, &h->map4_down, &g2, T,
+                                    h->num_sms, 1, st)
+                  : moe_launch_gemm(MOE_GEMM_DOWN, &h->map_down, &h->map_down, &g2, T,
+                                    h->num_sms, 0, st);
         h->prof.after(MOE_PROF_FORWARD_GEMM2, st);
     }
     if (err == cudaSuccess) err = moe_launch_finalize(T, D, acc, out, st);

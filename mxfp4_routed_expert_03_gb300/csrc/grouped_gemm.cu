@@ -251,11 +251,11 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" :::
 
 }  // namespace
 
-template <int MODE, int NT>
-__global__ void __launch_bounds__(Cfg<MODE, NT, false>::THREADS, 1) moe_grouped_gemm_kernel(
+template <int MODE, int NT, bool FP4>
+__global__ void __launch_bounds__(Cfg<MODE, NT, FP4>::THREADS, 1) moe_grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
     const MoeGemmArgs args) {
-    using C = Cfg<MODE, NT, false>;
+    using C = Cfg<MODE, NT, FP4>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -377,15 +377,28 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, false>::THREADS, 1) moe_grouped_
                         break;
                     }
                     unsigned char *st = smem + s * C::A_STAGE;
-                    tc::mbar_arrive_expect_tx(&full[s],
-                                              (uint32_t)(nsub * A_TX + C::SCALE_REP_A * SF_BYTES));
-                    ++it;  // a fill of this stage is now in flight
-                    for (int sub = 0; sub < nsub; ++sub) {
-                        unsigned char *sa = st + sub * A_BYTES;
-                        tc::tma_load_2d(sa, &mapA, &full[s], (kc + sub) * BK, row0, pol_w);
+                    if constexpr (FP4) {
+                        // one packed 128-byte row per weight row holds the stage's two
+                        // K blocks (a lone last block: the box's second half reads past
+                        // the row end, which the TMA fills with zeros)
+                        tc::mbar_arrive_expect_tx(&full[s],
+                                                  (uint32_t)(C::A_TILE + C::SCALE_REP_A * SF_BYTES));
+                        ++it;  // a fill of this stage is now in flight
+                        tc::tma_load_2d(st, &mapA, &full[s], kc * (BK / 2), row0, pol_w);
                         if (MODE == MOE_GEMM_GATEUP)  // up rows fill lanes 64..127
-                            tc::tma_load_2d(sa + 64 * BK, &mapA2, &full[s], (kc + sub) * BK, row0,
+                            tc::tma_load_2d(st + 64 * 128, &mapA2, &full[s], kc * (BK / 2), row0,
                                             pol_w);
+                    } else {
+                        tc::mbar_arrive_expect_tx(
+                            &full[s], (uint32_t)(nsub * A_TX + C::SCALE_REP_A * SF_BYTES));
+                        ++it;  // a fill of this stage is now in flight
+                        for (int sub = 0; sub < nsub; ++sub) {
+                            unsigned char *sa = st + sub * A_BYTES;
+                            tc::tma_load_2d(sa, &mapA, &full[s], (kc + sub) * BK, row0, pol_w);
+                            if (MODE == MOE_GEMM_GATEUP)  // up rows fill lanes 64..127
+                                tc::tma_load_2d(sa + 64 * BK, &mapA2, &full[s], (kc + sub) * BK,
+                                                row0, pol_w);
+                        }
                     }
                     // the scale block holding this stage's K block(s)
                     const uint8_t *sf = args.a_atoms + (atom0 + kc / ATOM_BLOCKS) * SF_BYTES;
@@ -405,8 +418,10 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, false>::THREADS, 1) moe_grouped_
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
                 Tile t;
                 if (!get_tile(tile, cur, t)) continue;
-                const uint32_t tile_bytes = (uint32_t)(2 * t.nmma * BK);
+                // [hi; lo] rows per K block, or (FP4) one packed row per token per stage
+                const uint32_t tile_bytes = (uint32_t)(FP4 ? t.nmma * 128 : 2 * t.nmma * BK);
                 const size_t blk0 = (size_t)t.tt * KC;
+                const size_t chunk0 = (size_t)t.tt * ((KC + 1) / 2);  // FP4: 256-wide K chunks
                 for (int kc = 0; kc < KC; kc += C::KS) {
                     const int s = it % C::SB, round = it / C::SB;
                     const int nsub = min(C::KS, KC - kc);
@@ -416,13 +431,21 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, false>::THREADS, 1) moe_grouped_
                         break;
                     }
                     unsigned char *st = smem + C::B_BASE + s * C::B_STAGE;
-                    tc::mbar_arrive_expect_tx(
-                        &full[s], (uint32_t)nsub * (tile_bytes + C::SCALE_REP_B * BSF_BYTES));
+                    if constexpr (FP4) {
+                        tc::mbar_arrive_expect_tx(
+                            &full[s], tile_bytes + (uint32_t)nsub * C::SCALE_REP_B * BSF_BYTES);
+                        tc::bulk_copy_g2s(st, args.b_tiles + (chunk0 + kc / 2) * MOE_GEMM_BTILE,
+                                          tile_bytes, &full[s], pol_x);
+                    } else {
+                        tc::mbar_arrive_expect_tx(
+                            &full[s], (uint32_t)nsub * (tile_bytes + C::SCALE_REP_B * BSF_BYTES));
+                    }
                     ++it;
                     for (int sub = 0; sub < nsub; ++sub) {
                         const size_t blk = blk0 + kc + sub;
-                        tc::bulk_copy_g2s(st + sub * C::B_BYTES, args.b_tiles + blk * MOE_GEMM_BTILE,
-                                          tile_bytes, &full[s], pol_x);
+                        if (!FP4)
+                            tc::bulk_copy_g2s(st + sub * C::B_BYTES, args.b_tiles + blk * MOE_GEMM_BTILE,
+                                              tile_bytes, &full[s], pol_x);
                         const uint8_t *ss = args.b_atoms + blk * BSF_BYTES;
                         for (int qd = 0; qd < C::SCALE_REP_B; ++qd)
                             tc::bulk_copy_g2s(st + C::B_SF + (sub * C::SCALE_REP_B + qd) * BSF_BYTES,
@@ -466,10 +489,14 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, false>::THREADS, 1) moe_grouped_
                 }
                 tc::tc_fence_after();
                 const uint32_t acc = tmem + buf * C::BUF_COLS + split * C::ACC_COLS;
-                uint32_t idesc[4];  // scale byte k of each column for K step k
+                // E4M3 path: scale byte k of each column for K step k (32 wide);
+                // FP4: scale bytes 2 k2, 2 k2 + 1 for K step k2 (64 wide)
+                uint32_t idesc[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    idesc[k] = tc::idesc_mxf8f6f4(tc::FMT_E2M1, tc::FMT_E4M3, 128, 2 * t.nmma, k, k);
+                    idesc[k] = FP4 ? tc::idesc_mxf4(128, t.nmma, 2 * (k & 1), 2 * (k & 1))
+                                   : tc::idesc_mxf8f6f4(tc::FMT_E2M1, tc::FMT_E4M3, 128,
+                                                        2 * t.nmma, k, k);
                 bool first = true;
                 for (int kc = 0, j = 0; kc < KC; kc += C::KS, ++it, ++j) {
                     if (C::NSPLIT > 1 && (j & 1) != split) continue;  // the other issuer's stage
@@ -510,12 +537,22 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, false>::THREADS, 1) moe_grouped_
                             tc::tmem_cp_128x256b(sfb, tc::sdesc_plain_128x32(bsf));
                         else  // B rows 0..127 (columns 0..3; the narrow tile has at most 32)
                             tc::tmem_cp_32x128b_warpx4(sfb, tc::sdesc_plain_32x16_groups256(bsf));
-                        const uint32_t as = a_s + sub * A_BYTES, bs = b_s + sub * C::B_BYTES;
+                        if constexpr (FP4) {
+                            // K block sub is bytes 64 sub .. 64 sub + 63 of every packed
+                            // row; two MMAs of 64 K each
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            tc::mma_mxf8f6f4(acc, tc::sdesc_sw128(as + 32 * k),
-                                             tc::sdesc_sw128(bs + 32 * k), idesc[k], sfa, sfb,
-                                             (!first || sub > 0 || k > 0) ? 1u : 0u);
+                            for (int k2 = 0; k2 < 2; ++k2)
+                                tc::mma_mxf4(acc, tc::sdesc_sw128(a_s + 64 * sub + 32 * k2),
+                                             tc::sdesc_sw128(b_s + 64 * sub + 32 * k2), idesc[k2],
+                                             sfa, sfb, (!first || sub > 0 || k2 > 0) ? 1u : 0u);
+                        } else {
+                            const uint32_t as = a_s + sub * A_BYTES, bs = b_s + sub * C::B_BYTES;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                tc::mma_mxf8f6f4(acc, tc::sdesc_sw128(as + 32 * k),
+                                                 tc::sdesc_sw128(bs + 32 * k), idesc[k], sfa, sfb,
+                                                 (!first || sub > 0 || k > 0) ? 1u : 0u);
+                        }
                     }
                     first = false;
                     tc::mma_commit(&empty[s]);  // the stage is free once these MMAs are done
@@ -579,20 +616,22 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, false>::THREADS, 1) moe_grouped_
             // the second issuer's accumulator holds something only if the tile has >= 2 stages
             const bool two = C::NSPLIT > 1 && KC > C::KS;
             for (int c0 = 0; c0 < t.n; c0 += 16) {
+                // columns c0 .. c0 + 15: the hi and lo halves added (FP4: one term)
                 uint32_t rh[16], rl[16];
-                tc::tmem_ld_32x32b_x16(acc + c0, rh);
-                tc::tmem_ld_32x32b_x16(acc + t.nmma + c0, rl);
-                tc::tmem_ld_wait();
                 float v[16];
+                tc::tmem_ld_32x32b_x16(acc + c0, rh);
+                if (!FP4) tc::tmem_ld_32x32b_x16(acc + t.nmma + c0, rl);
+                tc::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+                for (int j = 0; j < 16; ++j)
+                    v[j] = __uint_as_float(rh[j]) + (FP4 ? 0.f : __uint_as_float(rl[j]));
                 if (two) {
                     tc::tmem_ld_32x32b_x16(acc + C::ACC_COLS + c0, rh);
-                    tc::tmem_ld_32x32b_x16(acc + C::ACC_COLS + t.nmma + c0, rl);
+                    if (!FP4) tc::tmem_ld_32x32b_x16(acc + C::ACC_COLS + t.nmma + c0, rl);
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        v[j] += __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+                        v[j] += __uint_as_float(rh[j]) + (FP4 ? 0.f : __uint_as_float(rl[j]));
                 }
                 if (MODE == MOE_GEMM_GATEUP) {
                     // Lanes 0..63 hold gate rows f0 + r, lanes 64..127 the same up rows.
@@ -622,6 +661,33 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, false>::THREADS, 1) moe_grouped_
                         const float u = gate ? stg[j * 64 + rr] : v[j];
                         h[jj] = __fdividef(g, 1.f + __expf(-g)) * u;
                     }
+                    if constexpr (FP4) {
+                        // one MXFP4 term over this warp's 32 rows (one MX block along
+                        // F): the scale from the block maximum, each value to the
+                        // nearest E2M1 code; lanes f and f + 1 share a byte of the
+                        // packed row (f even in the low nibble)
+                        uint32_t nib[8];
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            sh[jj] = mx4::scale_exp(__uint_as_float(
+                                __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(h[jj])))));
+                            nib[jj] = mx4::to_e2m1x2(h[jj] * mx8::exp2i(-sh[jj]), 0.f) & 0xFu;
+                        }
+                        uint8_t *hblk = args.h_tiles +
+                                        ((size_t)t.tt * ((F / 128 + 1) / 2) + f / 256) * MOE_GEMM_BTILE;
+                        const int bi = (f & 255) >> 1;  // byte of the packed row
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const uint32_t up_nib = __shfl_down_sync(0xFFFFFFFFu, nib[jj], 1);
+                            const int j = gate ? jj : jj + 8;
+                            const int r = c0 + j;
+                            if (r < t.n && (lane & 1) == 0)
+                                hblk[r * 128 + (((bi >> 4) ^ (r & 7)) << 4) + (bi & 15)] =
+                                    (uint8_t)(nib[jj] | (up_nib << 4));
+                            if (r < t.n && lane == 0)
+                                args.h_atoms[at_base + bsf_off(r, cblk)] = (uint8_t)(sh[jj] + 127);
+                        }
+                    } else {
                     // two-term E4M3 split over this warp's 32 rows (one MX block along F)
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj)
@@ -669,6 +735,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, false>::THREADS, 1) moe_grouped_
                             }
                         }
                     }
+                    }  // two-term split
                     epi_sync();
                 } else {
                     // weighted values -> warp staging [16 columns][32 rows], then each
@@ -799,14 +866,6 @@ __global__ void __launch_bounds__(256) moe_prepare_atoms_slots_kernel(
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-size_t moe_gemm_smem_bytes(int mode, int narrow) {
-    if (narrow)
-        return mode == MOE_GEMM_GATEUP ? Cfg<MOE_GEMM_GATEUP, MOE_GEMM_NT_NARROW, false>::SMEM
-                                       : Cfg<MOE_GEMM_DOWN, MOE_GEMM_NT_NARROW, false>::SMEM;
-    return mode == MOE_GEMM_GATEUP ? Cfg<MOE_GEMM_GATEUP, NTMAX, false>::SMEM
-                                   : Cfg<MOE_GEMM_DOWN, NTMAX, false>::SMEM;
-}
-
 size_t moe_prepared_atoms_bytes(int E, int M, int K, int mrows) {
     const int KC = K / BK, NP = (KC + ATOM_BLOCKS - 1) / ATOM_BLOCKS;
     return (size_t)E * (M / mrows) * NP * SF_BYTES;
@@ -831,11 +890,11 @@ cudaError_t moe_launch_prepare_atoms(int E, int M, int K, int mrows, const uint8
 namespace {
 // One persistent CTA per SM (grid = max_ctas, the SM count): the kernel's
 // shared memory admits exactly one CTA per SM.
-template <int MODE, int NT>
+template <int MODE, int NT, bool FP4>
 cudaError_t launch_gemm_t(const CUtensorMap *mA, const CUtensorMap *mA2, const MoeGemmArgs *args,
                           int max_ctas, cudaStream_t st) {
-    using C = Cfg<MODE, NT, false>;
-    auto kern = moe_grouped_gemm_kernel<MODE, NT>;
+    using C = Cfg<MODE, NT, FP4>;
+    auto kern = moe_grouped_gemm_kernel<MODE, NT, FP4>;
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (err != cudaSuccess) return err;
@@ -843,14 +902,24 @@ cudaError_t launch_gemm_t(const CUtensorMap *mA, const CUtensorMap *mA2, const M
     kern<<<max_ctas, C::THREADS, C::SMEM, st>>>(*mA, *mA2, *args);
     return cudaGetLastError();
 }
-}  // namespace
 
-cudaError_t moe_launch_gemm(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
+template <bool FP4>
+cudaError_t launch_gemm_fmt(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
                             const MoeGemmArgs *args, int max_rows, int grid, cudaStream_t st) {
     constexpr int NN = MOE_GEMM_NT_NARROW;
     if (max_rows <= NN)
-        return mode == MOE_GEMM_GATEUP ? launch_gemm_t<MOE_GEMM_GATEUP, NN>(mA, mA2, args, grid, st)
-                                       : launch_gemm_t<MOE_GEMM_DOWN, NN>(mA, mA2, args, grid, st);
-    return mode == MOE_GEMM_GATEUP ? launch_gemm_t<MOE_GEMM_GATEUP, NTMAX>(mA, mA2, args, grid, st)
-                                   : launch_gemm_t<MOE_GEMM_DOWN, NTMAX>(mA, mA2, args, grid, st);
+        return mode == MOE_GEMM_GATEUP
+                   ? launch_gemm_t<MOE_GEMM_GATEUP, NN, FP4>(mA, mA2, args, grid, st)
+                   : launch_gemm_t<MOE_GEMM_DOWN, NN, FP4>(mA, mA2, args, grid, st);
+    return mode == MOE_GEMM_GATEUP
+               ? launch_gemm_t<MOE_GEMM_GATEUP, NTMAX, FP4>(mA, mA2, args, grid, st)
+               : launch_gemm_t<MOE_GEMM_DOWN, NTMAX, FP4>(mA, mA2, args, grid, st);
+}
+}  // namespace
+
+cudaError_t moe_launch_gemm(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
+                            const MoeGemmArgs *args, int max_rows, int grid, int fp4,
+                            cudaStream_t st) {
+    return fp4 ? launch_gemm_fmt<true>(mode, mA, mA2, args, max_rows, grid, st)
+               : launch_gemm_fmt<false>(mode, mA, mA2, args, max_rows, grid, st);
 }

@@ -53,6 +53,17 @@ cudaError_t moe_launch_prep_small(int T, int E, int k, int D, const int32_t *off
                                   const int32_t *perm, const int32_t *active, const uint16_t *x,
                                   int32_t *tt_prefix, uint8_t *tiles, uint8_t *atoms, float *acc,
                                   int *status, cudaStream_t st);
+// The FP4 x FP4 mode's counterparts: one MXFP4 term per activation, in the
+// FP4 tile layout (see moe_launch_gemm).
+cudaError_t moe_launch_prep_small_fp4(int T, int E, int k, int D, const int32_t *offsets,
+                                      const int32_t *perm, const int32_t *active,
+                                      const uint16_t *x, int32_t *tt_prefix, uint8_t *tiles,
+                                      uint8_t *atoms, float *acc, int *status, cudaStream_t st);
+cudaError_t moe_launch_gather_x_fp4(int max_tt, int E, int k, int n_rows, int D,
+                                    const int32_t *offsets, const int32_t *perm,
+                                    const int32_t *active, const int32_t *tt_prefix,
+                                    const uint16_t *x, uint8_t *tiles, uint8_t *atoms, int *status,
+                                    cudaStream_t st);
 cudaError_t moe_launch_finalize(int T, int D, const float *acc, uint16_t *out, cudaStream_t st);
 cudaError_t moe_launch_gather_x(int max_tt, int E, int k, int n_rows, int D, int ntmax,
                                 const int32_t *offsets, const int32_t *perm, const int32_t *active,
@@ -89,14 +100,18 @@ struct MoeGemmArgs {
     int inject;              // MOE_INJECT_NONE, or a test hook (see moe_set_fault_injection)
 };
 
-size_t moe_gemm_smem_bytes(int mode, int narrow);
 size_t moe_prepared_atoms_bytes(int E, int M, int K, int mrows);
 cudaError_t moe_launch_prepare_atoms(int E, int M, int K, int mrows, const uint8_t *s,
                                      const uint8_t *s2, uint8_t *out, cudaStream_t st);
 // max_rows: bound on any expert's routed rows (T for distinct top-k experts);
-// at most MOE_GEMM_NT_NARROW selects the narrow-tile variant.
+// at most MOE_GEMM_NT_NARROW selects the narrow-tile variant. fp4: the FP4 x
+// FP4 mode (packed weight maps, MXFP4 activation tiles: one 128-byte row per
+// token per 256-wide K chunk, chunk c of token tile tt at block
+// tt * ceil(K / 256) + c of b_tiles / h_tiles; scale blocks as for the
+// two-term mode, hi rows only).
 cudaError_t moe_launch_gemm(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
-                            const MoeGemmArgs *args, int max_rows, int grid, cudaStream_t st);
+                            const MoeGemmArgs *args, int max_rows, int grid, int fp4,
+                            cudaStream_t st);
 
 // stream.cu: expert streaming (HBM slot cache in front of host memory)
 struct MoeStreamHdr {

@@ -51,3 +51,40 @@ __device__ __forceinline__ float2 from_e4m3x2(uint32_t v) {
 }
 
 }  // namespace mx8
+
+// MXFP4 activations (the FP4 x FP4 mode): E2M1 elements with one E8M0 scale
+// per 32 values, converted as OCP MX v1.0 specifies (section 6.3): the scale
+// is 2^(floor(log2(amax)) - 2), 2 being the largest exponent of E2M1, and
+// each element v / scale rounds to the nearest E2M1 value, ties to even,
+// magnitudes above 6 clamped to 6.
+namespace mx4 {
+
+// floor(log2(amax)) - 2 for amax > 0 finite, clamped to the E8M0 range
+// [-127, 127]; -127 for zero.
+__device__ __forceinline__ int scale_exp(float amax) {
+    const uint32_t b = __float_as_uint(amax);
+    const int e = (int)((b >> 23) & 0xFF);
+    const uint32_t mant = b & 0x7FFFFF;
+    int fl;
+    if (e == 255) return 127;
+    if (e == 0) {
+        if (mant == 0) return -127;
+        fl = (31 - __clz((int)mant)) - 149;  // subnormal: leading bit of the mantissa
+    } else {
+        fl = e - 127;
+    }
+    const int s = fl - 2;
+    return s < -127 ? -127 : (s > 127 ? 127 : s);
+}
+
+// Two fp32 values to one byte of E2M1 codes (round to nearest even,
+// saturating): lo in the low nibble, hi in the high nibble.
+__device__ __forceinline__ uint32_t to_e2m1x2(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+
+}  // namespace mx4

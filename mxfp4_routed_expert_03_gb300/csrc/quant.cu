@@ -273,6 +273,150 @@ __global__ void __launch_bounds__(256) moe_prep_small_kernel(
     }
 }
 
+// ---------------------------------------------------------------------------
+// FP4 x FP4 mode: activations as one MXFP4 term (E2M1 codes, one E8M0 scale
+// per 32 values; OCP MX conversion, see mx8.cuh).
+// ---------------------------------------------------------------------------
+
+// MXFP4 conversion of 32 consecutive bf16 values: 16 bytes of E2M1 codes
+// (element 2i in the low nibble of byte i) and the scale exponent.
+__device__ __forceinline__ void mxfp4_block32(const uint16_t *__restrict__ src16,
+                                              uint32_t (&w)[4], int &s) {
+    const uint4 *src = (const uint4 *)src16;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint4 u = src[i];
+        const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[8 * i + 2 * j] = __uint_as_float(q[j] << 16);
+            v[8 * i + 2 * j + 1] = __uint_as_float(q[j] & 0xFFFF0000u);
+        }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    s = mx4::scale_exp(amax);
+    const float inv = mx8::exp2i(-s);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = 0u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        w[i / 4] |= mx4::to_e2m1x2(v[2 * i] * inv, v[2 * i + 1] * inv) << (8 * (i % 4));
+}
+
+// Row r of a token tile, 32-element block b of its K: the 16 code bytes go to
+// the tile's packed block of K chunk b / 8 (one 128-byte row per token,
+// 16-byte piece b % 8 stored at piece (b % 8) ^ (r % 8), the 128-byte
+// swizzle), the scale to the 1 KB block of K block b / 4 (same placement as
+// the two-term mode's hi rows).
+__device__ __forceinline__ void put_fp4_block(uint8_t *tiles, uint8_t *atoms, size_t tt, int KC2,
+                                              int KC, int r, int b, const uint32_t (&w)[4],
+                                              int s) {
+    uint8_t *blk = tiles + (tt * KC2 + b / 8) * MOE_GEMM_BTILE;
+    *(uint4 *)(blk + r * 128 + (((b & 7) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    const int i = r & 31, j = r >> 5, c = b & 3;
+    atoms[(tt * KC + b / 4) * 1024 + (i >> 3) * 256 + (j >> 2) * 128 + (i & 7) * 16 + (j & 3) * 4 + c] =
+        (uint8_t)(s + 127);
+}
+
+// Small batches in the FP4 mode: as moe_prep_small_kernel (one block per
+// active expert, identity schedule, accumulator zeroed), with one MXFP4 term.
+__global__ void __launch_bounds__(256) moe_prep_small_fp4_kernel(
+    int E, int k, int n_rows, int D, int T, const int32_t *__restrict__ offsets,
+    const int32_t *__restrict__ perm, const int32_t *__restrict__ active,
+    const uint16_t *__restrict__ x, int32_t *__restrict__ tt_prefix, uint8_t *__restrict__ tiles,
+    uint8_t *__restrict__ atoms, float *__restrict__ acc, int *status) {
+    __shared__ int s_tok[MOE_GEMM_NT_NARROW];
+    if (acc) {  // zero this block's share of acc [T][D]
+        const int64_t n4 = (int64_t)T * D / 4, per = (n4 + gridDim.x - 1) / gridDim.x;
+        const int64_t i0 = (int64_t)blockIdx.x * per, i1 = min(i0 + per, n4);
+        for (int64_t i = i0 + threadIdx.x; i < i1; i += blockDim.x)
+            ((float4 *)acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    int n_active = active[0];
+    if (n_active < 0 || n_active > E) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) moe_flag(status, MOE_ERR_BAD_INDEX);
+        return;
+    }
+    const int a = blockIdx.x;
+    if (a == 0 && threadIdx.x == 0) tt_prefix[n_active] = n_active;
+    if (a >= n_active) return;
+    if (threadIdx.x == 0) tt_prefix[a] = a;
+    const int e = active[1 + a];
+    if (e < 0 || e >= E) { if (threadIdx.x == 0) moe_flag(status, MOE_ERR_BAD_INDEX); return; }
+    const int sb = offsets[e], n = offsets[e + 1] - sb;
+    if (sb < 0 || n <= 0 || n > MOE_GEMM_NT_NARROW || sb + n > n_rows) {
+        if (threadIdx.x == 0) moe_flag(status, MOE_ERR_BAD_INDEX);
+        return;
+    }
+    for (int r = threadIdx.x; r < n; r += blockDim.x) {
+        int fl = perm[sb + r];
+        if (fl < 0 || fl >= n_rows) { moe_flag(status, MOE_ERR_BAD_INDEX); fl = 0; }
+        s_tok[r] = fl / k;
+    }
+    __syncthreads();
+    const int nb = D / 32, KC = D / 128, KC2 = (KC + 1) / 2;
+    for (int i = threadIdx.x; i < n * nb; i += blockDim.x) {
+        const int r = i / nb, b = i % nb;
+        uint32_t w[4];
+        int sc;
+        mxfp4_block32(x + (size_t)s_tok[r] * D + (size_t)b * 32, w, sc);
+        put_fp4_block(tiles, atoms, (size_t)a, KC2, KC, r, b, w, sc);
+    }
+}
+
+// Larger batches in the FP4 mode: one block per token tile quantises its
+// rows straight from x into the tile layout (no separate quantise pass).
+__global__ void __launch_bounds__(256) moe_gather_x_fp4_kernel(
+    int E, int k, int n_rows, int D, const int32_t *__restrict__ offsets,
+    const int32_t *__restrict__ perm, const int32_t *__restrict__ active,
+    const int32_t *__restrict__ prefix, const uint16_t *__restrict__ x, uint8_t *__restrict__ tiles,
+    uint8_t *__restrict__ atoms, int *status) {
+    __shared__ int s_tok[MOE_GEMM_NTMAX];
+    const int tt = blockIdx.x;
+    int n_active = active[0];
+    if (n_active < 0 || n_active > E) return;
+    int e, sb, r0, n;
+    if (!token_tile(tt, n_active, prefix, active, offsets, E, n_rows, e, sb, r0, n)) return;
+    if (n > MOE_GEMM_NTMAX) { if (threadIdx.x == 0) moe_flag(status, MOE_ERR_BAD_INDEX); return; }
+    for (int r = threadIdx.x; r < n; r += blockDim.x) {
+        int fl = perm[sb + r0 + r];
+        if (fl < 0 || fl >= n_rows) { moe_flag(status, MOE_ERR_BAD_INDEX); fl = 0; }
+        s_tok[r] = fl / k;
+    }
+    __syncthreads();
+    const int nb = D / 32, KC = D / 128, KC2 = (KC + 1) / 2;
+    for (int i = threadIdx.x; i < n * nb; i += blockDim.x) {
+        const int r = i / nb, b = i % nb;
+        uint32_t w[4];
+        int sc;
+        mxfp4_block32(x + (size_t)s_tok[r] * D + (size_t)b * 32, w, sc);
+        put_fp4_block(tiles, atoms, (size_t)tt, KC2, KC, r, b, w, sc);
+    }
+}
+
+cudaError_t moe_launch_prep_small_fp4(int T, int E, int k, int D, const int32_t *offsets,
+                                      const int32_t *perm, const int32_t *active,
+                                      const uint16_t *x, int32_t *tt_prefix, uint8_t *tiles,
+                                      uint8_t *atoms, float *acc, int *status, cudaStream_t st) {
+    const int grid = min(T * k, E);  // an upper bound on the active experts
+    moe_prep_small_fp4_kernel<<<grid, 256, 0, st>>>(E, k, T * k, D, T, offsets, perm, active, x,
+                                                    tt_prefix, tiles, atoms, acc, status);
+    return cudaGetLastError();
+}
+
+cudaError_t moe_launch_gather_x_fp4(int max_tt, int E, int k, int n_rows, int D,
+                                    const int32_t *offsets, const int32_t *perm,
+                                    const int32_t *active, const int32_t *tt_prefix,
+                                    const uint16_t *x, uint8_t *tiles, uint8_t *atoms, int *status,
+                                    cudaStream_t st) {
+    moe_gather_x_fp4_kernel<<<max_tt, 256, 0, st>>>(E, k, n_rows, D, offsets, perm, active,
+                                                    tt_prefix, x, tiles, atoms, status);
+    return cudaGetLastError();
+}
+
 cudaError_t moe_launch_prep_small(int T, int E, int k, int D, const int32_t *offsets,
                                   const int32_t *perm, const int32_t *active, const uint16_t *x,
                                   int32_t *tt_prefix, uint8_t *tiles, uint8_t *atoms, float *acc,

@@ -203,6 +203,22 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, ui
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] x B[smem]^T, both operands E2M1 packed two per byte
+// (kind::mxf4), 64 K per instruction, one E8M0 scale per 32 K from TMEM
+// (scale_vec::2X: the two scale bytes of a row are the byte pair the sf ids
+// in idesc select, 0 or 2).
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], "
+        "[%6], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
 // Arrive (once) on bar when all prior tcgen05 async ops of this thread finish.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile(
@@ -329,6 +345,13 @@ __host__ __device__ __forceinline__ uint32_t idesc_mxf8f6f4(int a_fmt, int b_fmt
     d |= (uint32_t)((M >> 4) & 0x1F) << 24;
     d |= (uint32_t)(a_sf_id & 3) << 29;
     return d;
+}
+
+// Instruction descriptor of kind::mxf4 block-scaled MMA: the same fields as
+// idesc_mxf8f6f4, with E2M1 coded 1 for both operands in this kind.
+__host__ __device__ __forceinline__ uint32_t idesc_mxf4(int M, int N, int a_sf_id, int b_sf_id) {
+    constexpr int MXF4_E2M1 = 1;
+    return idesc_mxf8f6f4(MXF4_E2M1, MXF4_E2M1, M, N, a_sf_id, b_sf_id);
 }
 
 }  // namespace tc

@@ -50,7 +50,7 @@ class Layer:
     """One routed layer: weights (device tensors) + the library handle."""
 
     def __init__(self, D: int, F: int, E: int, k: int, weights: dict, router_mode: int = 0,
-                 w_router=None, shared=None):
+                 w_router=None, shared=None, act_mode: int = 0):
         self.D, self.F, self.E, self.k = D, F, E, k
         self.router_mode = router_mode
         self.weights = weights
@@ -58,7 +58,7 @@ class Layer:
         self.shared = shared
         ptr = lambda t: None if t is None else t.data_ptr()
         sh = shared or {}
-        self.desc = moe_desc(D, F, E, k, router_mode, 1 if shared else 0)
+        self.desc = moe_desc(D, F, E, k, router_mode, 1 if shared else 0, act_mode)
         self.wdesc = moe_weights(*[weights[n].data_ptr() for n in WEIGHT_NAMES], ptr(w_router),
                                  ptr(sh.get("sh_gate")), ptr(sh.get("sh_up")),
                                  ptr(sh.get("sh_down")))
@@ -156,7 +156,8 @@ class StreamingLayer(Layer):
     CPU tensors in the library's layouts, pinned (tensor.pin_memory())."""
 
     def __init__(self, D: int, F: int, E: int, k: int, host_weights: dict | None, n_slots: int,
-                 router_mode: int = 0, w_router=None, shared=None, store: ExpertStore | None = None):
+                 router_mode: int = 0, w_router=None, shared=None, store: ExpertStore | None = None,
+                 act_mode: int = 0):
         """host_weights: pinned CPU tensors of all experts, or None with `store`
         (an ExpertStore): the misses are then decoded from the store."""
         self.D, self.F, self.E, self.k = D, F, E, k
@@ -169,7 +170,7 @@ class StreamingLayer(Layer):
         self.shared = shared
         ptr = lambda t: None if t is None else t.data_ptr()
         sh = shared or {}
-        self.desc = moe_desc(D, F, E, k, router_mode, 1 if shared else 0)
+        self.desc = moe_desc(D, F, E, k, router_mode, 1 if shared else 0, act_mode)
         self.wdesc = moe_weights(*[self.weights[n].data_ptr() for n in WEIGHT_NAMES],
                                  ptr(w_router), ptr(sh.get("sh_gate")), ptr(sh.get("sh_up")),
                                  ptr(sh.get("sh_down")))

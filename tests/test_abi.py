@@ -64,6 +64,7 @@ def test_create_rejects_bad_descriptors_on_the_host(L):
         (L.moe_desc(7200, 1536, 896, 16, 0, 0), L.MOE_ERR_UNSUPPORTED),
         (L.moe_desc(7168, 1536, 2048, 16, 0, 0), L.MOE_ERR_UNSUPPORTED),
         (L.moe_desc(7168, 1536, 896, 33, 0, 0), L.MOE_ERR_UNSUPPORTED),
+        (L.moe_desc(7168, 1536, 896, 16, 0, 0, 2), L.MOE_ERR_INVALID_ARG),   # act_mode
     ]
     for d, code in cases:
         h = ctypes.c_void_p()
