@@ -78,6 +78,12 @@ BENCH_WORKLOADS = {
     "decode_T16": {"Ts": [16], "path": "forward", "desc": "K3 routed layer decode, T=16"},
     "prefill4k": {"Ts": [4096], "path": "forward",
                   "desc": "K3 routed layer prefill, T=4096, uniform routing"},
+    "decode_fp8": {"Ts": [1, 4, 16], "path": "decode", "fp8": True, "base": "decode1",
+                   "desc": "K3-shaped FP8 (E4M3FN, fp32 scale per 128 x 128) routed layer decode, "
+                           "T=1,4,16, fused CUDA-core GEMV (moe_decode)"},
+    "prefill4k_fp8": {"Ts": [4096], "path": "forward", "fp8": True, "base": "prefill4k",
+                      "desc": "K3-shaped FP8 routed layer prefill, T=4096, bf16 tensor-core GEMMs "
+                              "on the bf16 copy moe_prepare makes (BF16-dequant prefill)"},
     "prefill4k_fp4": {"Ts": [4096], "path": "forward", "act": 1, "base": "prefill4k",
                       "desc": "K3 routed layer prefill, T=4096, uniform routing, FP4 x FP4 mode "
                               "(MXFP4 activations, kind::mxf4; not the parity path)"},
@@ -309,14 +315,21 @@ class Ctx:
         self.layers = {}      # kind -> Layer
 
     def layer_weights(self, codes, seed):
+        """The layer's weights under E2M1 code distribution `codes`, or the FP8
+        lane's (codes == "fp8")."""
         import torch
         import synth
-        from mxfp4_routed_expert_03_gb300.layer import alloc_weights
+        from mxfp4_routed_expert_03_gb300.layer import alloc_fp8_weights, alloc_weights
         if codes not in self.weights:
-            w = alloc_weights(self.n_exp, D_MODEL, D_FF)
-            synth.dev_fill_layer(seed, self.n_exp, D_MODEL, D_FF,
-                                 {k: v.data_ptr() for k, v in w.items()},
-                                 torch.cuda.current_stream().cuda_stream, dist=codes)
+            stream = torch.cuda.current_stream().cuda_stream
+            if codes == "fp8":
+                w = alloc_fp8_weights(self.n_exp, D_MODEL, D_FF)
+                synth.dev_fill_fp8_layer(seed, self.n_exp, D_MODEL, D_FF,
+                                         {k: v.data_ptr() for k, v in w.items()}, stream)
+            else:
+                w = alloc_weights(self.n_exp, D_MODEL, D_FF)
+                synth.dev_fill_layer(seed, self.n_exp, D_MODEL, D_FF,
+                                     {k: v.data_ptr() for k, v in w.items()}, stream, dist=codes)
             self.weights[codes] = w
         return self.weights[codes]
 
@@ -341,9 +354,10 @@ def make_layer(ctx, wl, base):
     import synth
     from mxfp4_routed_expert_03_gb300 import MOE_ROUTER_XWR
     from mxfp4_routed_expert_03_gb300.layer import Layer
-    codes = wl.get("codes", synth.CODES_UNIFORM)
+    codes = "fp8" if wl.get("fp8") else wl.get("codes", synth.CODES_UNIFORM)
     n_slots = wl.get("stream_slots")
     act = wl.get("act", 0)
+    wfmt = 1 if wl.get("fp8") else 0   # MOE_W_FP8 / MOE_W_MXFP4
     kind = ("router" if wl.get("router") else "stream_store" if wl.get("store") else
             "stream" if n_slots else "plain", codes, act)
     if kind in ctx.layers:
@@ -377,8 +391,9 @@ def make_layer(ctx, wl, base):
             layer = StreamingLayer(D_MODEL, D_FF, ctx.n_exp, TOP_K, host, min(n_slots, ctx.n_exp),
                                    act_mode=act)
     else:
-        layer = Layer(D_MODEL, D_FF, ctx.n_exp, TOP_K, weights, act_mode=act)
-    layer.prepare()
+        layer = Layer(D_MODEL, D_FF, ctx.n_exp, TOP_K, weights, act_mode=act, weight_format=wfmt)
+    if wl["path"] != "decode" or not wl.get("fp8"):
+        layer.prepare()   # (the FP8 decode reads the codes; its bf16 copy serves moe_forward)
     ctx.layers[kind] = layer
     return layer, info
 
@@ -414,7 +429,7 @@ def make_batches(ctx, wl, base, path_of, use_router):
     return batches
 
 
-def kernel_work(path: str, T: int, active: int, fp4: bool = False):
+def kernel_work(path: str, T: int, active: int, fp4: bool = False, fp8: bool = False):
     """Algorithmic bytes and flops of one launch of a batch's dominant kernel:
     the gate/up GEMM of moe_forward (active experts' gate+up weights, the
     two-term activation rows in and the two-term h rows out, one byte per
@@ -422,7 +437,17 @@ def kernel_work(path: str, T: int, active: int, fp4: bool = False):
     element plus a scale byte per 32) or the gate/up kernel of moe_decode
     (the same weights, bf16 x rows in, f16 h rows and their exponents out)."""
     flop = 2.0 * T * TOP_K * 2 * D_MODEL * D_FF
-    if path == "decode":
+    if fp8:
+        # FP8 lane: decode streams one code byte per weight (+ its block scales);
+        # the prefill GEMM streams the bf16 copy (2 bytes per weight) and bf16
+        # activation rows in and h rows out
+        nb = lambda n: (n + 127) // 128
+        if path == "decode":
+            wb = 2 * (D_FF * D_MODEL + 4 * nb(D_FF) * nb(D_MODEL))
+            nbytes = active * wb + T * D_MODEL * 2 + T * TOP_K * (D_FF * 2 + D_FF // 32)
+        else:
+            nbytes = active * 2 * D_FF * D_MODEL * 2 + T * TOP_K * (2 * D_MODEL + 2 * D_FF)
+    elif path == "decode":
         nbytes = active * GATEUP_BYTES + T * D_MODEL * 2 + T * TOP_K * (D_FF * 2 + D_FF // 32)
     elif fp4:
         nbytes = active * GATEUP_BYTES + T * TOP_K * (D_MODEL // 2 + D_MODEL // 32 +
@@ -432,7 +457,7 @@ def kernel_work(path: str, T: int, active: int, fp4: bool = False):
     return float(nbytes), flop
 
 
-def roofline(path, nbytes, flop, ms, peaks, workload, fp4=False):
+def roofline(path, nbytes, flop, ms, peaks, workload, fp4=False, fp8=False):
     """Roofline of the dominant kernel: achieved algorithmic bytes or flops per
     launch over its mean launch time, against the measured peak of the bound
     its arithmetic intensity puts it under."""
@@ -442,9 +467,13 @@ def roofline(path, nbytes, flop, ms, peaks, workload, fp4=False):
     src = "measured" if peaks else "fallback"
     gbs = nbytes / (ms * 1e-3) / 1e9
     tfs = flop / (ms * 1e-3) / 1e12
+    bf16_peak = peaks.get("bf16_tflops", 1900.0)
     if path == "decode":
         kname, csrc = "moe_decode_gateup_kernel", "decode.cu"
         tensor_time = 0.0   # CUDA cores: bound by bytes
+    elif fp8:
+        kname, csrc = "moe_grouped_gemm_kernel<0, bf16>", "grouped_gemm.cu"
+        tensor_time = flop / 1e12 / bf16_peak        # kind::f16 on the bf16 copy
     elif fp4:
         kname, csrc = "moe_grouped_gemm_kernel<0, fp4>", "grouped_gemm.cu"
         tensor_time = flop / 1e12 / fp4_peak          # one MXFP4 term, kind::mxf4
@@ -455,6 +484,10 @@ def roofline(path, nbytes, flop, ms, peaks, workload, fp4=False):
     if mem_bound:
         r = {"bound": "hbm", "kernel": kname, "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
              "frac": gbs / hbm_peak, "peak_source": src + " (copy bandwidth)"}
+    elif fp8:
+        r = {"bound": "tensor", "kernel": kname, "achieved": tfs, "peak": bf16_peak,
+             "unit": "TFLOP/s", "frac": tfs / bf16_peak, "peak_source": src + " bf16 (burst)",
+             "hbm_GBs": gbs, "frac_of_hbm": gbs / hbm_peak}
     elif fp4:
         r = {"bound": "tensor", "kernel": kname, "achieved": tfs, "peak": fp4_peak,
              "unit": "TFLOP/s", "frac": tfs / fp4_peak,
@@ -607,10 +640,10 @@ def measure(ctx, name, wl, steps, warmup, sampler, peaks, breakdown=True, path_o
     dom = max(by_path, key=lambda k: sum(per_batch_ms[bi] for bi in by_path[k]))
     bis = by_path[dom]
     ms_avg = float(np.mean([per_batch_ms[bi] for bi in bis]))
-    fp4 = bool(wl.get("act", 0))
-    work = [kernel_work(dom, wl["Ts"][bi], act[bi], fp4) for bi in bis]
+    fp4, fp8 = bool(wl.get("act", 0)), bool(wl.get("fp8"))
+    work = [kernel_work(dom, wl["Ts"][bi], act[bi], fp4, fp8) for bi in bis]
     nbytes, nflop = float(np.mean([w_[0] for w_ in work])), float(np.mean([w_[1] for w_ in work]))
-    roof = roofline(dom, nbytes, nflop, ms_avg, peaks, name, fp4)
+    roof = roofline(dom, nbytes, nflop, ms_avg, peaks, name, fp4, fp8)
     stream_info = None
     if n_slots:
         roof, stream_info = stream_roofline(ctx, layer, stats0, stats1, kern_ms, steps,
@@ -700,7 +733,7 @@ def stream_roofline(ctx, layer, stats0, stats1, kern_ms, steps, n_batches, store
 
 # Workloads that get a record of their own in the default run's line.
 RECORDS = ("decode_T1", "decode_T4", "decode_T16", "prefill4k", "skewed8k", "router16k",
-           "prefill4k_fp4", "router16k_fp4")
+           "prefill4k_fp4", "router16k_fp4", "decode_fp8", "prefill4k_fp8")
 
 
 def run_ours(args):

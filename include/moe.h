@@ -114,6 +114,26 @@ enum moe_act_mode {
     MOE_ACT_MXFP4 = 1
 };
 
+/* Storage format of the routed experts' weights.
+ * MOE_W_MXFP4: the MXFP4 layout above (E2M1 codes + E8M0 scale per 32).
+ * MOE_W_FP8: the FP8 lane (Moonshine GitHub README, "GLM 5.3 Flash status":
+ *   FP8 E4M3FN experts with a fused decode GEMV and a BF16-dequant prefill).
+ *   The pages give no scale layout; here each matrix with N rows and
+ *   reduction length K is
+ *     codes  uint8 [N][K]                        one OCP E4M3FN code per weight
+ *     scales fp32  [ceil(N/128)][ceil(K/128)]    one scale per 128 x 128 block
+ *   weight = value(code) * scale, passed through the same moe_weights fields
+ *   (gate_q / gate_s ...; the scale pointers point at fp32 data, 4-byte
+ *   aligned; codes 16-byte aligned). moe_decode (and moe_decode_noalloc)
+ *   streams the codes on CUDA cores with exact products; moe_forward runs bf16
+ *   tensor-core GEMMs on a bf16 copy of the experts (each weight rounded to
+ *   nearest even) that moe_prepare writes into its caller buffer. act_mode
+ *   must be MOE_ACT_EXACT; expert streaming is not offered for this format. */
+enum moe_weight_format {
+    MOE_W_MXFP4 = 0,
+    MOE_W_FP8 = 1
+};
+
 /* Layer shape. Supported envelope: d_model a multiple of 256, d_ff of 128,
  * d_model <= 16384, d_ff <= 8192, 1 <= top_k <= 32, top_k <= n_experts <= 1024. */
 typedef struct moe_desc {
@@ -121,9 +141,10 @@ typedef struct moe_desc {
     int32_t d_ff;
     int32_t n_experts;
     int32_t top_k;
-    int32_t router_mode;  /* enum moe_router_mode */
-    int32_t has_shared;   /* 1: one always-on bf16 SwiGLU shared expert, weight 1.0 */
-    int32_t act_mode;     /* enum moe_act_mode (moe_forward only) */
+    int32_t router_mode;    /* enum moe_router_mode */
+    int32_t has_shared;     /* 1: one always-on bf16 SwiGLU shared expert, weight 1.0 */
+    int32_t act_mode;       /* enum moe_act_mode (moe_forward only) */
+    int32_t weight_format;  /* enum moe_weight_format */
 } moe_desc;
 
 /* Device pointers to the layer's weights (see layouts above). Unused fields NULL. */
@@ -171,7 +192,11 @@ void moe_destroy(moe_handle *h);
  * d_ff=1536. Returns -1 if either size is not a positive multiple of 32. */
 int64_t moe_expert_bytes(int32_t d_model, int32_t d_ff);
 
-/* Host. Bytes of the buffer moe_prepare fills: the three weight-scale arrays
+/* Host. Bytes of the buffer moe_prepare fills. FP8 layers: the bf16 copy of
+ * every expert's three matrices (3 * n_experts * d_model * d_ff * 2 bytes,
+ * each matrix array rounded up to 256; 59.2 GB for an 896-expert K3-shaped
+ * layer), plus the W_r terms below for router_mode MOE_ROUTER_XWR. MXFP4
+ * layers: the three weight-scale arrays
  * (3 * n_experts * d_model * d_ff / 32 bytes when d_model and d_ff are
  * multiples of 256, 924 MB for the 896-expert K3 layer; a K chunk pair is
  * padded when the chunk count is odd; rounded up to 256) plus, for router_mode MOE_ROUTER_XWR, three bf16

@@ -58,12 +58,15 @@ MOE_PROF_STREAM_COPY = 8
 MOE_ACT_EXACT = 0
 MOE_ACT_MXFP4 = 1
 
+MOE_W_MXFP4 = 0
+MOE_W_FP8 = 1
+
 
 class moe_desc(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("router_mode", ctypes.c_int32), ("has_shared", ctypes.c_int32),
-                ("act_mode", ctypes.c_int32)]
+                ("act_mode", ctypes.c_int32), ("weight_format", ctypes.c_int32)]
 
 
 class moe_tile_rec(ctypes.Structure):

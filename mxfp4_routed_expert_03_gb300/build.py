@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libmoe.so")
 OBJDIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "route.cu", "decode.cu", "quant.cu", "grouped_gemm.cu", "dense_gemm.cu",
+SOURCES = ["api.cu", "route.cu", "decode.cu", "quant.cu", "grouped_gemm.cu", "dense_gemm.cu", "fp8.cu",
            "noalloc.cu", "stream.cu", "store.cu", "store_enc.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
               "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", os.path.join(ROOT, "include")]

@@ -27,6 +27,8 @@ struct moe_handle {
     int *status;  // device word: first error code recorded by a kernel
     CUtensorMap map_gate, map_up, map_down;  // TMA views of the packed E2M1 weights
     CUtensorMap map4_gate, map4_up, map4_down;  // the same bytes unexpanded (FP4 x FP4 mode)
+    CUtensorMap map16_gate, map16_up, map16_down;  // FP8 layers: the bf16 copy (after prepare)
+    bool fp8;              // weight_format MOE_W_FP8
     CUtensorMap map_sh_gate, map_sh_up, map_sh_down;  // bf16 shared expert (has_shared)
     CUtensorMap map_wr[3];  // the three bf16 terms of W_r (router_mode XWR, after prepare)
     const uint8_t *atoms;  // caller buffer filled by moe_prepare (NULL until then)
@@ -90,7 +92,9 @@ struct FwdLayout {
     int max_tt;
 };
 
-static FwdLayout fwd_layout(int T, int D, int F, int E, int k, bool shared) {
+// kdiv: K elements per activation-tile block (128; 64 for the bf16 tiles of
+// FP8 layers).
+static FwdLayout fwd_layout(int T, int D, int F, int E, int k, bool shared, int kdiv = 128) {
     FwdLayout L;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -105,9 +109,9 @@ static FwdLayout fwd_layout(int T, int D, int F, int E, int k, bool shared) {
     L.xq_lo = take((size_t)T * D);
     L.xs_hi = take((size_t)T * D / 32);
     L.xs_lo = take((size_t)T * D / 32);
-    L.xb = take((size_t)L.max_tt * (D / 128) * MOE_GEMM_BTILE);
+    L.xb = take((size_t)L.max_tt * (D / kdiv) * MOE_GEMM_BTILE);
     L.xa = take((size_t)L.max_tt * (D / 128) * 1024);
-    L.hb = take((size_t)L.max_tt * (F / 128) * MOE_GEMM_BTILE);
+    L.hb = take((size_t)L.max_tt * (F / kdiv) * MOE_GEMM_BTILE);
     L.ha = take((size_t)L.max_tt * (F / 128) * 1024);
     L.acc = take((size_t)T * D * sizeof(float));
     L.prefix = take((size_t)(E + 1) * sizeof(int32_t));
@@ -134,7 +138,15 @@ static size_t gu_atoms_bytes(const moe_desc &d, int wE) {
     return moe_prepared_atoms_bytes(wE, d.d_ff, d.d_model, 64);
 }
 
+// Bytes of one bf16 copy of an FP8 layer's matrix array (E x d_model x d_ff).
+static size_t bf16_array_bytes(const moe_desc &d) {
+    return align_up((size_t)d.n_experts * d.d_model * d.d_ff * 2, 256);
+}
+
+// The front of the prepared buffer: MXFP4 layers' re-laid weight scales, or
+// FP8 layers' bf16 copies of gate, up and down.
 static size_t atoms_bytes(const moe_desc &d, int wE) {
+    if (d.weight_format == MOE_W_FP8) return 3 * bf16_array_bytes(d);
     return align_up(gu_atoms_bytes(d, wE) + moe_prepared_atoms_bytes(wE, d.d_model, d.d_ff, 128), 256);
 }
 
@@ -172,6 +184,9 @@ static int create_impl(const moe_desc *d, const moe_weights *w, int wE, moe_hand
         return MOE_ERR_INVALID_ARG;
     if (d->has_shared != 0 && d->has_shared != 1) return MOE_ERR_INVALID_ARG;
     if (d->act_mode != MOE_ACT_EXACT && d->act_mode != MOE_ACT_MXFP4) return MOE_ERR_INVALID_ARG;
+    if (d->weight_format != MOE_W_MXFP4 && d->weight_format != MOE_W_FP8) return MOE_ERR_INVALID_ARG;
+    const bool fp8 = d->weight_format == MOE_W_FP8;
+    if (fp8 && d->act_mode != MOE_ACT_EXACT) return MOE_ERR_UNSUPPORTED;
     if (d->top_k > d->n_experts) return MOE_ERR_INVALID_ARG;
     if (d->d_model % 256 || d->d_ff % 128 || d->d_model > MOE_MAX_DMODEL ||
         d->d_ff > MOE_MAX_DFF || d->top_k > MOE_MAX_TOPK || d->n_experts > MOE_MAX_EXPERTS)
@@ -181,10 +196,10 @@ static int create_impl(const moe_desc *d, const moe_weights *w, int wE, moe_hand
     const void *req[] = {w->gate_q, w->gate_s, w->up_q, w->up_s, w->down_q, w->down_s};
     for (const void *p : req)
         if (!p) return MOE_ERR_INVALID_ARG;
-    if (((uintptr_t)w->gate_q | (uintptr_t)w->up_q | (uintptr_t)w->down_q) & 31u)
-        return MOE_ERR_INVALID_ARG;  // TMA of packed E2M1 needs 32-byte aligned bases
-    if (((uintptr_t)w->gate_s | (uintptr_t)w->up_s | (uintptr_t)w->down_s) & 15u)
-        return MOE_ERR_INVALID_ARG;  // bulk copies of scale rows need 16-byte aligned bases
+    if (((uintptr_t)w->gate_q | (uintptr_t)w->up_q | (uintptr_t)w->down_q) & (fp8 ? 15u : 31u))
+        return MOE_ERR_INVALID_ARG;  // TMA of packed E2M1: 32-byte aligned; FP8 16-byte loads
+    if (((uintptr_t)w->gate_s | (uintptr_t)w->up_s | (uintptr_t)w->down_s) & (fp8 ? 3u : 15u))
+        return MOE_ERR_INVALID_ARG;  // bulk copies of scale rows: 16-byte aligned; FP8 fp32
     if (d->router_mode == MOE_ROUTER_XWR && !w->w_router) return MOE_ERR_INVALID_ARG;
     if (d->has_shared && (!w->sh_gate || !w->sh_up || !w->sh_down)) return MOE_ERR_INVALID_ARG;
     if (d->has_shared && ((uintptr_t)w->sh_gate | (uintptr_t)w->sh_up | (uintptr_t)w->sh_down) & 15u)
@@ -207,11 +222,12 @@ static int create_impl(const moe_desc *d, const moe_weights *w, int wE, moe_hand
     h->device = dev;
     h->timeout = kTimeoutCycles;
     h->inject = MOE_INJECT_NONE;
+    h->fp8 = fp8;
     if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         free(h);
         return MOE_ERR_CUDA;
     }
-    {
+    if (!fp8) {  // (FP8 layers get the maps of their bf16 copy in moe_prepare)
         const uint64_t D = d->d_model, F = d->d_ff, E = wE;  // experts in the weight arrays
         const CUtensorMapDataType fp4 = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
         if (!make_map_2d(&h->map_gate, fp4, w->gate_q, D, E * F, D / 2, 128, 64) ||
@@ -229,6 +245,9 @@ static int create_impl(const moe_desc *d, const moe_weights *w, int wE, moe_hand
             free(h);
             return MOE_ERR_CUDA;
         }
+    }
+    {
+        const uint64_t D = d->d_model, F = d->d_ff;
         if (d->has_shared &&
             (!make_map_bf16(&h->map_sh_gate, w->sh_gate, D, F, 64) ||
              !make_map_bf16(&h->map_sh_up, w->sh_up, D, F, 64) ||
@@ -277,6 +296,7 @@ MOE_API int moe_create_streaming(const moe_desc *d, const moe_weights *host_w,
     if (!d || !host_w || !slot_w || !state) return MOE_ERR_INVALID_ARG;
     if (d->n_experts <= 0 || n_slots < 1 || n_slots > d->n_experts || n_slots > 1024)
         return MOE_ERR_INVALID_ARG;
+    if (d->weight_format != MOE_W_MXFP4) return MOE_ERR_UNSUPPORTED;
     const void *hp[] = {host_w->gate_q, host_w->gate_s, host_w->up_q,
                         host_w->up_s, host_w->down_q, host_w->down_s};
     for (const void *p : hp) {
@@ -309,6 +329,7 @@ MOE_API int moe_create_streaming_store(const moe_desc *d, const moe_store *store
     if (!d || !store || !slot_w || !state) return MOE_ERR_INVALID_ARG;
     if (d->n_experts <= 0 || n_slots < 1 || n_slots > d->n_experts || n_slots > 1024)
         return MOE_ERR_INVALID_ARG;
+    if (d->weight_format != MOE_W_MXFP4) return MOE_ERR_UNSUPPORTED;
     MoeStoreJob probe;
     if (!moe_store_job_shape(d->d_model, d->d_ff, probe)) return MOE_ERR_INVALID_ARG;
     if (!store->blob || !aligned16(store->blob) || store->blob_bytes <= 0 || !store->tiles ||
@@ -526,7 +547,8 @@ MOE_API size_t moe_workspace_bytes(const moe_handle *h, int32_t T, int32_t op) {
             return align_up(moe_decode_ws_bytes(T, d.d_model, d.d_ff, d.top_k), 256) +
                    shared_ws_bytes(h, T);
         case MOE_OP_FORWARD:
-            return fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k, d.has_shared).total;
+            return fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k, d.has_shared,
+                              h->fp8 ? 64 : 128).total;
         default: return 0;
     }
 }
@@ -600,7 +622,7 @@ MOE_API int moe_decode(moe_handle *h, int32_t T, const uint16_t *x, const moe_pl
         if (rc != MOE_OK) return rc;
     }
     cudaError_t err = moe_launch_decode(T, d.d_model, d.d_ff, d.n_experts, d.top_k, x, plan, &h->w,
-                                        sh_out, out, ws, h->status, h->prof, st);
+                                        h->fp8, sh_out, out, ws, h->status, h->prof, st);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -624,7 +646,7 @@ MOE_API int moe_decode_noalloc(moe_handle *h, int32_t T, const uint16_t *x,
     void *scratch = nullptr;
     if (moe_noalloc_scratch(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
     cudaError_t err = moe_launch_decode(T, d.d_model, d.d_ff, d.n_experts, d.top_k, x, plan, &h->w,
-                                        nullptr, out, scratch, h->status, h->prof,
+                                        h->fp8, nullptr, out, scratch, h->status, h->prof,
                                         (cudaStream_t)stream);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -642,7 +664,8 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     // a streaming layer must be able to hold every expert a plan can select
     if (h->streaming && (int64_t)T * d.top_k > h->wE && d.n_experts > h->wE)
         return MOE_ERR_UNSUPPORTED;
-    const FwdLayout L = fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k, d.has_shared);
+    const FwdLayout L = fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k, d.has_shared,
+                                   h->fp8 ? 64 : 128);
     if (ws_bytes < L.total || !ws || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     unsigned char *base = (unsigned char *)ws;
@@ -659,7 +682,16 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     const bool small = T <= MOE_GEMM_NT_NARROW;
     const bool fp4 = d.act_mode == MOE_ACT_MXFP4;
     cudaError_t err;
-    if (small && fp4) {
+    if (h->fp8 && small) {
+        err = moe_launch_prep_small_bf16(T, E, k, D, plan->offsets, plan->perm, plan->active, x,
+                                         prefix, xb, d.has_shared ? nullptr : acc, h->status, st);
+    } else if (h->fp8) {
+        err = moe_launch_schedule(E, MOE_GEMM_NTMAX, plan->offsets, plan->active, prefix,
+                                  h->status, st);
+        if (err == cudaSuccess)
+            err = moe_launch_gather_x_bf16(L.max_tt, E, k, rows, D, plan->offsets, plan->perm,
+                                           plan->active, prefix, x, xb, h->status, st);
+    } else if (small && fp4) {
         err = moe_launch_prep_small_fp4(T, E, k, D, plan->offsets, plan->perm, plan->active, x,
                                         prefix, xb, xa, d.has_shared ? nullptr : acc, h->status,
                                         st);
@@ -705,7 +737,7 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         MoeGemmArgs g1 = a;
         g1.M = F;
         g1.K = D;
-        g1.KC = D / 128;
+        g1.KC = h->fp8 ? D / 64 : D / 128;
         g1.MT = F / 64;  // 64 gate rows + the same 64 up rows per weight tile
         g1.a_atoms = h->atoms;
         g1.b_tiles = xb;
@@ -714,10 +746,12 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         g1.h_atoms = ha;
         g1.inject = h->inject;
         h->prof.before(MOE_PROF_FORWARD_GEMM1, st);
-        err = fp4 ? moe_launch_gemm(MOE_GEMM_GATEUP, &h->map4_gate, &h->map4_up, &g1, T,
-                                    h->num_sms, 1, st)
+        err = h->fp8 ? moe_launch_gemm(MOE_GEMM_GATEUP, &h->map16_gate, &h->map16_up, &g1, T,
+                                       h->num_sms, MOE_AF_BF16, st)
+              : fp4 ? moe_launch_gemm(MOE_GEMM_GATEUP, &h->map4_gate, &h->map4_up, &g1, T,
+                                    h->num_sms, MOE_AF_MXF4, st)
                   : moe_launch_gemm(MOE_GEMM_GATEUP, &h->map_gate, &h->map_up, &g1, T,
-                                    h->num_sms, 0, st);
+                                    h->num_sms, MOE_AF_E4M3X2, st);
         h->prof.after(MOE_PROF_FORWARD_GEMM1, st);
     }
     if (err == cudaSuccess) {
@@ -733,16 +767,18 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         g2.M = D;
         g2.MT = D / 128;
         g2.K = F;
-        g2.KC = F / 128;
+        g2.KC = h->fp8 ? F / 64 : F / 128;
         g2.a_atoms = h->atoms + gu_atoms_bytes(d, h->wE);
         g2.b_tiles = hb;
         g2.b_atoms = ha;
         g2.acc = acc;
         h->prof.before(MOE_PROF_FORWARD_GEMM2, st);
-        err = fp4 ? moe_launch_gemm(MOE_GEMM_DOWN, &h->map4_down, &h->map4_down, &g2, T,
-                                    h->num_sms, 1, st)
+        err = h->fp8 ? moe_launch_gemm(MOE_GEMM_DOWN, &h->map16_down, &h->map16_down, &g2, T,
+                                       h->num_sms, MOE_AF_BF16, st)
+              : fp4 ? moe_launch_gemm(MOE_GEMM_DOWN, &h->map4_down, &h->map4_down, &g2, T,
+                                    h->num_sms, MOE_AF_MXF4, st)
                   : moe_launch_gemm(MOE_GEMM_DOWN, &h->map_down, &h->map_down, &g2, T,
-                                    h->num_sms, 0, st);
+                                    h->num_sms, MOE_AF_E4M3X2, st);
         h->prof.after(MOE_PROF_FORWARD_GEMM2, st);
     }
     if (err == cudaSuccess) err = moe_launch_finalize(T, D, acc, out, st);
@@ -772,7 +808,25 @@ MOE_API int moe_prepare(moe_handle *h, void *buf, size_t bytes, void *stream) {
     // gate/up tiles: 64 gate rows over the same 64 up rows; down tiles: 128 rows
     // (a streaming layer's slots are prepared as experts arrive)
     cudaError_t err = cudaSuccess;
-    if (!h->streaming) {
+    if (h->fp8) {
+        // the bf16 copy the prefill GEMMs stream: gate, up [E][F][D], down [E][D][F]
+        const size_t ab = bf16_array_bytes(d);
+        uint16_t *g16 = (uint16_t *)out, *u16 = (uint16_t *)(out + ab),
+                 *d16 = (uint16_t *)(out + 2 * ab);
+        err = moe_launch_fp8_dequant(E, F, D, h->w.gate_q, (const float *)h->w.gate_s, g16, st);
+        if (err == cudaSuccess)
+            err = moe_launch_fp8_dequant(E, F, D, h->w.up_q, (const float *)h->w.up_s, u16, st);
+        if (err == cudaSuccess)
+            err = moe_launch_fp8_dequant(E, D, F, h->w.down_q, (const float *)h->w.down_s, d16, st);
+        if (err == cudaSuccess &&
+            (!make_map_2d(&h->map16_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g16, D,
+                          (uint64_t)E * F, (uint64_t)D * 2, 64, 64) ||
+             !make_map_2d(&h->map16_up, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u16, D,
+                          (uint64_t)E * F, (uint64_t)D * 2, 64, 64) ||
+             !make_map_2d(&h->map16_down, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d16, F,
+                          (uint64_t)E * D, (uint64_t)F * 2, 64, 128)))
+            return MOE_ERR_CUDA;
+    } else if (!h->streaming) {
         err = moe_launch_prepare_atoms(E, F, D, 64, h->w.gate_s, h->w.up_s, out, st);
         if (err == cudaSuccess)
             err = moe_launch_prepare_atoms(E, D, F, 128, h->w.down_s, nullptr,

@@ -75,6 +75,64 @@ __device__ __forceinline__ float block_dot_f16(const uint4 &q, const uint4 *xs) 
     return a0 + a1;
 }
 
+// The same for four E4M3 codes (one word, element i in byte i): each byte
+// pair converts exactly to f16x2 (E4M3's range and 4 significant bits fit f16).
+__device__ __forceinline__ float word_dot_e4m3(uint32_t w, uint32_t xa, uint32_t xb, float acc) {
+    asm("{\n\t.reg .b16 p0, p1;\n\t.reg .b32 h0, h1;\n\t"
+        ".reg .f16 wl, wh, al, ah;\n\t"
+        "mov.b32 {p0, p1}, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h0, p0;\n\tcvt.rn.f16x2.e4m3x2 h1, p1;\n\t"
+        "mov.b32 {wl, wh}, h0;\n\tmov.b32 {al, ah}, %2;\n\t"
+        "fma.rn.f32.f16 %0, wl, al, %0;\n\tfma.rn.f32.f16 %0, wh, ah, %0;\n\t"
+        "mov.b32 {wl, wh}, h1;\n\tmov.b32 {al, ah}, %3;\n\t"
+        "fma.rn.f32.f16 %0, wl, al, %0;\n\tfma.rn.f32.f16 %0, wh, ah, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w), "r"(xa), "r"(xb));
+    return acc;
+}
+
+// One 32-element block of weights as the kernels load it: 16 bytes of packed
+// E2M1 codes (MXFP4) or 32 bytes of E4M3 codes (FP8), with the block's scale.
+template <bool F8>
+struct WBlock {
+    uint4 q0, q1;  // q1 used by FP8 only
+};
+
+// Block b of a weight row: MXFP4 rows are K/2 bytes with one E8M0 scale byte
+// per block; FP8 rows are K bytes and take the fp32 scale of their
+// 128 x 128 block (sc_row: the row's row of block scales, K/128 entries).
+template <bool F8>
+__device__ __forceinline__ void load_block(const uint8_t *__restrict__ row, const void *sc_row, int b,
+                                           WBlock<F8> &w, float &sc) {
+    if constexpr (F8) {
+        w.q0 = __ldg((const uint4 *)row + 2 * b);
+        w.q1 = __ldg((const uint4 *)row + 2 * b + 1);
+        sc = __ldg((const float *)sc_row + (b >> 2));
+    } else {
+        w.q0 = __ldg((const uint4 *)row + b);
+        sc = e8m0_to_f32(__ldg((const uint8_t *)sc_row + b));
+    }
+}
+
+// Dot product of a weight block with 32 f16 activations (four 16-byte chunks).
+template <bool F8>
+__device__ __forceinline__ float block_dot(const WBlock<F8> &w, const uint4 *xs) {
+    if constexpr (F8) {
+        const uint4 x0 = xs[0], x1 = xs[1], x2 = xs[2], x3 = xs[3];
+        float a0 = word_dot_e4m3(w.q0.x, x0.x, x0.y, 0.f);
+        float a1 = word_dot_e4m3(w.q0.y, x0.z, x0.w, 0.f);
+        a0 = word_dot_e4m3(w.q0.z, x1.x, x1.y, a0);
+        a1 = word_dot_e4m3(w.q0.w, x1.z, x1.w, a1);
+        a0 = word_dot_e4m3(w.q1.x, x2.x, x2.y, a0);
+        a1 = word_dot_e4m3(w.q1.y, x2.z, x2.w, a1);
+        a0 = word_dot_e4m3(w.q1.z, x3.x, x3.y, a0);
+        a1 = word_dot_e4m3(w.q1.w, x3.z, x3.w, a1);
+        return a0 + a1;
+    } else {
+        return block_dot_f16(w.q0, xs);
+    }
+}
+
 __device__ __forceinline__ float2 f16x2_to_float2(uint32_t v) {
     __half2 hv = *reinterpret_cast<__half2 *>(&v);
     return __half22float2(hv);
@@ -127,8 +185,8 @@ __device__ __forceinline__ float exp2_int(int ex) {  // 2^ex for ex in [-126, 12
 // lane owning PER_LANE MX blocks), then one warp per token stores the 32
 // values of h = silu(g) * u as f16 with their shared power-of-two exponent.
 // ---------------------------------------------------------------------------
-template <int PER_LANE>
-__global__ void __launch_bounds__(256, 2) moe_decode_gateup_kernel(
+template <int PER_LANE, bool F8>
+__global__ void __launch_bounds__(256, F8 ? 1 : 2) moe_decode_gateup_kernel(
     int D, int F, int E, int k, int n_rows, const uint16_t *__restrict__ x,
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
     const int32_t *__restrict__ active, const uint8_t *__restrict__ gate_q,
@@ -143,7 +201,9 @@ __global__ void __launch_bounds__(256, 2) moe_decode_gateup_kernel(
     const int LPR = nblk / PER_LANE;
     const int RPW = 32 / LPR;
     const int sub = lane % LPR, grp = lane / LPR;
-    const size_t qrow = (size_t)D / 2, srow = (size_t)nblk;
+    // bytes per weight row; scale entries per row (MXFP4: per 32-block bytes;
+    // FP8: a row of 128 x 128 block scales, shared by 128 rows)
+    const size_t qrow = F8 ? (size_t)D : (size_t)D / 2, srow = F8 ? (size_t)D / 128 : (size_t)nblk;
     int n_active = active[0];
     if (n_active < 0 || n_active > E) {
         if (threadIdx.x == 0) moe_flag(status, MOE_ERR_BAD_INDEX);
@@ -158,7 +218,9 @@ __global__ void __launch_bounds__(256, 2) moe_decode_gateup_kernel(
         int e, s0, n;
         if (!segment_of(a, E, n_rows, active, offsets, e, s0, n, status)) continue;
         const uint8_t *gq = gate_q + (size_t)e * F * qrow, *uq = up_q + (size_t)e * F * qrow;
-        const uint8_t *gs = gate_s + (size_t)e * F * srow, *us = up_s + (size_t)e * F * srow;
+        // the expert's scales: MXFP4 bytes [F][nblk]; FP8 floats [F/128][D/128]
+        const size_t es = F8 ? (size_t)e * (F / 128) * srow * 4 : (size_t)e * F * srow;
+        const uint8_t *gs = gate_s + es, *us = up_s + es;
         for (int g0 = 0; g0 < n; g0 += kStageTok) {
             const int ns = min(kStageTok, n - g0);
             if (a != staged_a || g0 != staged_g0) {
@@ -208,15 +270,14 @@ __global__ void __launch_bounds__(256, 2) moe_decode_gateup_kernel(
             for (int rl = wid * RPW + grp; rl - grp < 32; rl += NW * RPW) {
                 const bool row_ok = rl < 32;
                 const int f = f_base + (row_ok ? rl : 0);
-                uint4 gqv[PER_LANE], uqv[PER_LANE];
+                WBlock<F8> gqv[PER_LANE], uqv[PER_LANE];
                 float gsc[PER_LANE], usc[PER_LANE];
+                const size_t so = F8 ? (size_t)(f / 128) * srow * 4 : (size_t)f * srow;
 #pragma unroll
                 for (int p = 0; p < PER_LANE; ++p) {
                     const int b = sub + LPR * p;
-                    gqv[p] = __ldg((const uint4 *)(gq + (size_t)f * qrow) + b);
-                    uqv[p] = __ldg((const uint4 *)(uq + (size_t)f * qrow) + b);
-                    gsc[p] = e8m0_to_f32(__ldg(gs + (size_t)f * srow + b));
-                    usc[p] = e8m0_to_f32(__ldg(us + (size_t)f * srow + b));
+                    load_block<F8>(gq + (size_t)f * qrow, gs + so, b, gqv[p], gsc[p]);
+                    load_block<F8>(uq + (size_t)f * qrow, us + so, b, uqv[p], usc[p]);
                 }
                 for (int j0 = 0; j0 < ns; j0 += NT) {
                     const int nt = min(NT, ns - j0);
@@ -232,8 +293,8 @@ __global__ void __launch_bounds__(256, 2) moe_decode_gateup_kernel(
                                     xs + ((size_t)(j0 + j) * nblk + sub + LPR * p) * kBlkStride;
                                 const uint4 *xb = (const uint4 *)xbb;
                                 const float xsc = *(const float *)(xbb + kBlkScale);
-                                ag[j] = fmaf(block_dot_f16(gqv[p], xb), gsc[p] * xsc, ag[j]);
-                                au[j] = fmaf(block_dot_f16(uqv[p], xb), usc[p] * xsc, au[j]);
+                                ag[j] = fmaf(block_dot<F8>(gqv[p], xb), gsc[p] * xsc, ag[j]);
+                                au[j] = fmaf(block_dot<F8>(uqv[p], xb), usc[p] * xsc, au[j]);
                             }
                         }
                     }
@@ -280,8 +341,8 @@ __global__ void __launch_bounds__(256, 2) moe_decode_gateup_kernel(
 // changes. Each warp issues all loads of RG groups of RPW rows before any
 // arithmetic.
 // ---------------------------------------------------------------------------
-template <int PER_LANE>
-__global__ void __launch_bounds__(256, 2) moe_decode_down_kernel(
+template <int PER_LANE, bool F8>
+__global__ void __launch_bounds__(256, F8 ? 1 : 2) moe_decode_down_kernel(
     int D, int F, int E, int n_rows, const int32_t *__restrict__ offsets,
     const int32_t *__restrict__ active, const uint8_t *__restrict__ down_q,
     const uint8_t *__restrict__ down_s, const __half *__restrict__ h16,
@@ -294,7 +355,7 @@ __global__ void __launch_bounds__(256, 2) moe_decode_down_kernel(
     const int LPR = nblk / PER_LANE;
     const int RPW = 32 / LPR;
     const int sub = lane % LPR, grp = lane / LPR;
-    const size_t qrow = (size_t)F / 2, srow = (size_t)nblk;
+    const size_t qrow = F8 ? (size_t)F : (size_t)F / 2, srow = F8 ? (size_t)F / 128 : (size_t)nblk;
     int n_active = active[0];
     if (n_active < 0 || n_active > E) {
         if (threadIdx.x == 0) moe_flag(status, MOE_ERR_BAD_INDEX);
@@ -310,22 +371,20 @@ __global__ void __launch_bounds__(256, 2) moe_decode_down_kernel(
         int e, s0, n;
         if (!segment_of(a, E, n_rows, active, offsets, e, s0, n, status)) continue;
         const uint8_t *dq = down_q + (size_t)e * D * qrow;
-        const uint8_t *ds = down_s + (size_t)e * D * srow;
+        const uint8_t *ds = down_s + (F8 ? (size_t)e * (D / 128) * srow * 4 : (size_t)e * D * srow);
         int drow[RG];
         bool ok[RG];
-        uint4 qv[RG][PER_LANE];
+        WBlock<F8> qv[RG][PER_LANE];
         float sc[RG][PER_LANE];
 #pragma unroll
         for (int r = 0; r < RG; ++r) {
             drow[r] = d_base + (wid * RG + r) * RPW + grp;
             ok[r] = drow[r] < D;
             const int d = ok[r] ? drow[r] : 0;
+            const size_t so = F8 ? (size_t)(d / 128) * srow * 4 : (size_t)d * srow;
 #pragma unroll
-            for (int p = 0; p < PER_LANE; ++p) {
-                const int b = sub + LPR * p;
-                qv[r][p] = __ldg((const uint4 *)(dq + (size_t)d * qrow) + b);
-                sc[r][p] = e8m0_to_f32(__ldg(ds + (size_t)d * srow + b));
-            }
+            for (int p = 0; p < PER_LANE; ++p)
+                load_block<F8>(dq + (size_t)d * qrow, ds + so, sub + LPR * p, qv[r][p], sc[r][p]);
         }
         for (int g0 = 0; g0 < n; g0 += kStageTok) {
             const int ns = min(kStageTok, n - g0);
@@ -363,7 +422,7 @@ __global__ void __launch_bounds__(256, 2) moe_decode_down_kernel(
                             const float hsc = s_hsc[j0 + j][b];
 #pragma unroll
                             for (int r = 0; r < RG; ++r)
-                                acc[r][j] = fmaf(block_dot_f16(qv[r][p], hb), sc[r][p] * hsc, acc[r][j]);
+                                acc[r][j] = fmaf(block_dot<F8>(qv[r][p], hb), sc[r][p] * hsc, acc[r][j]);
                         }
                     }
                 }
@@ -476,42 +535,52 @@ int num_sms() {
 size_t moe_decode_ws_bytes(int T, int D, int F, int k) { return decode_layout(T, D, F, k).total; }
 
 namespace {
-template <int P>
+template <int P, bool F8>
 void launch_gateup(int grid, cudaStream_t st, int D, int F, int E, int k, int n_rows,
                    const uint16_t *x, const moe_plan_buf *p, const moe_weights *w, __half *h16,
                    int8_t *hexp, int *status) {
     const size_t sm = (size_t)kStageTok * (D / 32) * kBlkStride;
-    cudaFuncSetAttribute(moe_decode_gateup_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)sm);
-    moe_decode_gateup_kernel<P><<<grid, 256, sm, st>>>(D, F, E, k, n_rows, x, p->offsets, p->perm,
-                                                       p->active, w->gate_q, w->gate_s, w->up_q,
-                                                       w->up_s, h16, hexp, status);
+    cudaFuncSetAttribute(moe_decode_gateup_kernel<P, F8>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    moe_decode_gateup_kernel<P, F8><<<F8 ? grid / 2 : grid, 256, sm, st>>>(
+        D, F, E, k, n_rows, x, p->offsets, p->perm, p->active, w->gate_q, w->gate_s, w->up_q,
+        w->up_s, h16, hexp, status);
 }
 
-template <int P>
+template <int P, bool F8>
 void launch_down(int grid, cudaStream_t st, int D, int F, int E, int n_rows, const moe_plan_buf *p,
                  const moe_weights *w, const __half *h16, const int8_t *hexp, float *y,
                  int *status) {
     const size_t sm = (size_t)kStageTok * (F / 32) * kBlkStride;
-    cudaFuncSetAttribute(moe_decode_down_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(moe_decode_down_kernel<P, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sm);
-    moe_decode_down_kernel<P><<<grid, 256, sm, st>>>(D, F, E, n_rows, p->offsets, p->active,
-                                                     w->down_q, w->down_s, h16, hexp, y, status);
+    moe_decode_down_kernel<P, F8><<<F8 ? grid / 2 : grid, 256, sm, st>>>(D, F, E, n_rows, p->offsets, p->active,
+                                                         w->down_q, w->down_s, h16, hexp, y,
+                                                         status);
 }
 
 typedef void (*gateup_fn)(int, cudaStream_t, int, int, int, int, int, const uint16_t *,
                           const moe_plan_buf *, const moe_weights *, __half *, int8_t *, int *);
 typedef void (*down_fn)(int, cudaStream_t, int, int, int, int, const moe_plan_buf *,
                         const moe_weights *, const __half *, const int8_t *, float *, int *);
-const gateup_fn kGateup[9] = {nullptr, launch_gateup<1>, launch_gateup<2>, launch_gateup<3>,
-                              launch_gateup<4>, launch_gateup<5>, launch_gateup<6>,
-                              launch_gateup<7>, launch_gateup<8>};
-const down_fn kDown[9] = {nullptr, launch_down<1>, launch_down<2>, launch_down<3>, launch_down<4>,
-                          launch_down<5>, launch_down<6>, launch_down<7>, launch_down<8>};
+const gateup_fn kGateup[2][9] = {
+    {nullptr, launch_gateup<1, false>, launch_gateup<2, false>, launch_gateup<3, false>,
+     launch_gateup<4, false>, launch_gateup<5, false>, launch_gateup<6, false>,
+     launch_gateup<7, false>, launch_gateup<8, false>},
+    {nullptr, launch_gateup<1, true>, launch_gateup<2, true>, launch_gateup<3, true>,
+     launch_gateup<4, true>, launch_gateup<5, true>, launch_gateup<6, true>,
+     launch_gateup<7, true>, launch_gateup<8, true>}};
+const down_fn kDown[2][9] = {
+    {nullptr, launch_down<1, false>, launch_down<2, false>, launch_down<3, false>,
+     launch_down<4, false>, launch_down<5, false>, launch_down<6, false>, launch_down<7, false>,
+     launch_down<8, false>},
+    {nullptr, launch_down<1, true>, launch_down<2, true>, launch_down<3, true>,
+     launch_down<4, true>, launch_down<5, true>, launch_down<6, true>, launch_down<7, true>,
+     launch_down<8, true>}};
 }  // namespace
 
 cudaError_t moe_launch_decode(int T, int D, int F, int E, int k, const uint16_t *x,
-                              const moe_plan_buf *p, const moe_weights *w,
+                              const moe_plan_buf *p, const moe_weights *w, int fp8,
                               const float *shared_out, uint16_t *out, void *ws, int *status,
                               const MoeProf &prof, cudaStream_t st) {
     const int n_rows = T * k;
@@ -524,10 +593,10 @@ cudaError_t moe_launch_decode(int T, int D, int F, int E, int k, const uint16_t 
     const int pd = moe_decode_per_lane(D), pf = moe_decode_per_lane(F);
     if (pd < 1 || pd > 8 || pf < 1 || pf > 8) return cudaErrorInvalidValue;
     prof.before(MOE_PROF_DECODE_GATEUP, st);
-    kGateup[pd](grid, st, D, F, E, k, n_rows, x, p, w, h16, hexp, status);
+    kGateup[fp8 ? 1 : 0][pd](grid, st, D, F, E, k, n_rows, x, p, w, h16, hexp, status);
     prof.after(MOE_PROF_DECODE_GATEUP, st);
     prof.before(MOE_PROF_DECODE_DOWN, st);
-    kDown[pf](grid, st, D, F, E, n_rows, p, w, h16, hexp, y, status);
+    kDown[fp8 ? 1 : 0][pf](grid, st, D, F, E, n_rows, p, w, h16, hexp, y, status);
     prof.after(MOE_PROF_DECODE_DOWN, st);
     dim3 g((D / 4 + 255) / 256, T);
     moe_combine_slots_kernel<<<g, 256, 0, st>>>(T, D, k, n_rows, p->topk_w, p->inv, y, shared_out,

@@ -49,22 +49,6 @@ struct DCfg {
     static_assert(DN % 16 == 0 && DN <= 256 && 2 * DN <= (int)DTMEM_COLS, "tile width");
 };
 
-// kind::f16 instruction descriptor: fp32 accumulator (bit 4), bf16 A and B
-// (bits 7-9 and 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // The four epilogue warps (128 threads) meet at named barrier 1.
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -155,7 +139,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) moe_dense_gemm_kernel(
             bool ok = true;
             uint64_t *last = nullptr;
             uint32_t last_par = 0;
-            const uint32_t idesc = idesc_bf16(128, DN);
+            const uint32_t idesc = tc::idesc_bf16(128, DN);
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++lt) {
                 const int buf = lt & 1, use = lt >> 1;
                 if (use > 0 && !tc::mbar_wait(&tempty[buf], (use - 1) & 1, LIMIT, abort_p)) {
@@ -177,7 +161,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) moe_dense_gemm_kernel(
                     const uint32_t b_s = tc::smem_u32(st + C::NTERMS * D_A_BYTES);
 #pragma unroll
                     for (int k = 0; k < DK / 16; ++k)
-                        mma_bf16(acc, tc::sdesc_sw128(tc::smem_u32(st) + 32 * k),
+                        tc::mma_bf16(acc, tc::sdesc_sw128(tc::smem_u32(st) + 32 * k),
                                  tc::sdesc_sw128(b_s + 32 * k), idesc, (kc > 0 || k > 0) ? 1u : 0u);
                     tc::mma_commit(&empty[s]);
                     last = &empty[s];
@@ -351,7 +335,7 @@ __global__ void __launch_bounds__(RTHREADS, 1) moe_router_gemm_kernel(
         }
     } else if (warp == 2) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(128, DN);
+            const uint32_t idesc = tc::idesc_bf16(128, DN);
             int it = 0;
             bool ok = true;
             uint64_t *last = nullptr;
@@ -376,7 +360,7 @@ __global__ void __launch_bounds__(RTHREADS, 1) moe_router_gemm_kernel(
                     for (int term = 2; term >= 0; --term) {
 #pragma unroll
                         for (int k = 0; k < DK / 16; ++k)
-                            mma_bf16(acc, tc::sdesc_sw128(tc::smem_u32(st + term * D_A_BYTES) + 32 * k),
+                            tc::mma_bf16(acc, tc::sdesc_sw128(tc::smem_u32(st + term * D_A_BYTES) + 32 * k),
                                      tc::sdesc_sw128(b_s + 32 * k), idesc,
                                      (k > 0 || term < 2) ? 1u : 0u);
                     }

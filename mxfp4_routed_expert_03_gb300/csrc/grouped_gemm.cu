@@ -85,8 +85,10 @@ constexpr int BSF_BYTES = 1024;          // activation scales of one chunk (256 
 // two K blocks are one 128-byte row per weight or token row and one MMA
 // covers 64 K. A stage is half the bytes of the E4M3 path, so the rings are
 // deeper.
-template <int MODE, int NT, bool FP4>
+template <int MODE, int NT, int AF>
 struct Cfg {
+    static constexpr bool FP4 = AF == MOE_AF_MXF4;
+    static constexpr bool BF16 = AF == MOE_AF_BF16;
     static constexpr bool NARROW = NT <= 16;
     // MMA-issuing warps. One thread issues a block-scaled MMA every ~90 cycles
     // when the scale selection changes from MMA to MMA (every K step), which
@@ -95,7 +97,7 @@ struct Cfg {
     // into its own accumulator, and the epilogue adds the two.
     static constexpr int NSPLIT = NARROW ? 2 : 1;
     static constexpr int THREADS = 224 + 32 * (NSPLIT - 1);  // warp 7: second issuer
-    static constexpr int TERMS = FP4 ? 1 : 2;  // activation terms stacked along N
+    static constexpr int TERMS = (FP4 || BF16) ? 1 : 2;  // activation terms stacked along N
     static constexpr uint32_t ACC_COLS = TERMS * NT;         // [hi | lo] columns of one accumulator
     static constexpr uint32_t BUF_COLS = NSPLIT * ACC_COLS;  // one of two accumulator buffers
     static constexpr uint32_t SF_TMEM_COL = 2 * BUF_COLS;    // then 2 scale slots per issuer
@@ -114,23 +116,25 @@ struct Cfg {
     // it keeps one copy of each block and fills the lane quadrants with
     // 32x128b.warpx4 copies. The FP4 mode issues half the MMAs per stage and
     // spends the room of the extra copies on ring depth.
-    static constexpr int SCALE_REP_A = (NARROW || FP4) ? 1 : 4;
-    static constexpr int SCALE_REP_B = (NARROW || FP4) ? 1 : 4;
+    static constexpr int SCALE_REP_A = BF16 ? 0 : (NARROW || FP4) ? 1 : 4;  // bf16: no scales
+    static constexpr int SCALE_REP_B = BF16 ? 0 : (NARROW || FP4) ? 1 : 4;
     static_assert(SF_TMEM_COL + 2 * NSPLIT * SF_SLOT <= TMEM_COLS, "tensor memory budget");
     static constexpr int MROWS = (MODE == MOE_GEMM_GATEUP) ? 64 : 128;  // weight rows per tile
     // ring stages (KS blocks each)
-    static constexpr int SA = NARROW ? (FP4 ? 10 : 5) : (FP4 ? 6 : 2);
+    static constexpr int SA = NARROW ? (FP4 ? 10 : 5) : (FP4 ? 6 : BF16 ? 3 : 2);
     static constexpr int SB = SA;              // activation ring stages
     // one full barrier per stage for both operands (both producers arrive)
     // and one release barrier per stage (one commit)
     static constexpr bool MERGED = SA == SB;
     static_assert(MERGED, "the rings share their barriers");
     // weight tile of a stage in shared memory: FP4 packed 128-byte rows, else
-    // one 128 x 128-byte tile per K block (E2M1 expanded to 8-bit containers)
+    // one 128 x 128-byte tile per K block (E2M1 expanded to 8-bit containers,
+    // or 64 bf16 per row)
     static constexpr int A_TILE = FP4 ? 128 * 128 : KS * A_BYTES;
     static constexpr int A_STAGE = A_TILE + SCALE_REP_A * SF_BYTES;  // tiles, then scales
     static constexpr int A_SF = A_TILE;
-    static constexpr int B_BYTES = 2 * NT * BK;  // smem bytes of one K block's [hi; lo] rows
+    // smem bytes of one K block's activation rows: [hi; lo] E4M3, or bf16
+    static constexpr int B_BYTES = (BF16 ? 1 : 2) * NT * 128;
     // activation tile of a stage: FP4 one 128-byte row per token, else [hi; lo]
     // rows per K block
     static constexpr int B_TILE = FP4 ? NT * 128 : KS * B_BYTES;
@@ -159,7 +163,8 @@ struct Cfg {
     static constexpr int EPI_BYTES = (MODE == MOE_GEMM_GATEUP) ? 16 * 64 * 4 : 4 * 16 * 32 * 4;
     static constexpr int SMEM = 1024 + EPI_BASE + EPI_BYTES;
     static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0, "stages must keep 1 KB alignment");
-    static_assert(NARROW || FP4 || SCALE_REP_B == 4, "wide two-term tiles need B scale columns 0..7");
+    static_assert(NARROW || FP4 || BF16 || SCALE_REP_B == 4,
+                  "wide two-term tiles need B scale columns 0..7");
     static_assert(TERMS * NT <= 128 || SCALE_REP_B == 4, "B rows past 127 need the 128x256b copy");
     static_assert(BAR_BASE % 8 == 0 && PREFIX_BASE % 16 == 0 && EXPERT_BASE % 16 == 0 &&
                       SEG_BASE % 16 == 0 && EPI_BASE % 16 == 0,
@@ -251,11 +256,12 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" :::
 
 }  // namespace
 
-template <int MODE, int NT, bool FP4>
-__global__ void __launch_bounds__(Cfg<MODE, NT, FP4>::THREADS, 1) moe_grouped_gemm_kernel(
+template <int MODE, int NT, int AF>
+__global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
     const MoeGemmArgs args) {
-    using C = Cfg<MODE, NT, FP4>;
+    using C = Cfg<MODE, NT, AF>;
+    constexpr bool FP4 = C::FP4, BF16 = C::BF16;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -388,6 +394,17 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, FP4>::THREADS, 1) moe_grouped_ge
                         if (MODE == MOE_GEMM_GATEUP)  // up rows fill lanes 64..127
                             tc::tma_load_2d(st + 64 * 128, &mapA2, &full[s], kc * (BK / 2), row0,
                                             pol_w);
+                    } else if constexpr (BF16) {
+                        // one 128 x 64 bf16 tile (128-byte rows) per K block
+                        tc::mbar_arrive_expect_tx(&full[s], (uint32_t)(nsub * A_BYTES));
+                        ++it;  // a fill of this stage is now in flight
+                        for (int sub = 0; sub < nsub; ++sub) {
+                            unsigned char *sa = st + sub * A_BYTES;
+                            tc::tma_load_2d(sa, &mapA, &full[s], (kc + sub) * 64, row0, pol_w);
+                            if (MODE == MOE_GEMM_GATEUP)  // up rows fill lanes 64..127
+                                tc::tma_load_2d(sa + 64 * 128, &mapA2, &full[s], (kc + sub) * 64,
+                                                row0, pol_w);
+                        }
                     } else {
                         tc::mbar_arrive_expect_tx(
                             &full[s], (uint32_t)(nsub * A_TX + C::SCALE_REP_A * SF_BYTES));
@@ -419,7 +436,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, FP4>::THREADS, 1) moe_grouped_ge
                 Tile t;
                 if (!get_tile(tile, cur, t)) continue;
                 // [hi; lo] rows per K block, or (FP4) one packed row per token per stage
-                const uint32_t tile_bytes = (uint32_t)(FP4 ? t.nmma * 128 : 2 * t.nmma * BK);
+                const uint32_t tile_bytes =
+                    (uint32_t)((FP4 || BF16) ? t.nmma * 128 : 2 * t.nmma * BK);
                 const size_t blk0 = (size_t)t.tt * KC;
                 const size_t chunk0 = (size_t)t.tt * ((KC + 1) / 2);  // FP4: 256-wide K chunks
                 for (int kc = 0; kc < KC; kc += C::KS) {
@@ -494,9 +512,10 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, FP4>::THREADS, 1) moe_grouped_ge
                 uint32_t idesc[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    idesc[k] = FP4 ? tc::idesc_mxf4(128, t.nmma, 2 * (k & 1), 2 * (k & 1))
-                                   : tc::idesc_mxf8f6f4(tc::FMT_E2M1, tc::FMT_E4M3, 128,
-                                                        2 * t.nmma, k, k);
+                    idesc[k] = BF16 ? tc::idesc_bf16(128, t.nmma)
+                               : FP4 ? tc::idesc_mxf4(128, t.nmma, 2 * (k & 1), 2 * (k & 1))
+                                     : tc::idesc_mxf8f6f4(tc::FMT_E2M1, tc::FMT_E4M3, 128,
+                                                          2 * t.nmma, k, k);
                 bool first = true;
                 for (int kc = 0, j = 0; kc < KC; kc += C::KS, ++it, ++j) {
                     if (C::NSPLIT > 1 && (j & 1) != split) continue;  // the other issuer's stage
@@ -535,9 +554,17 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, FP4>::THREADS, 1) moe_grouped_ge
                         const uint32_t bsf = b_s + C::B_SF + sub * C::SCALE_REP_B * BSF_BYTES;
                         if (C::SCALE_REP_B == 4)
                             tc::tmem_cp_128x256b(sfb, tc::sdesc_plain_128x32(bsf));
-                        else  // B rows 0..127 (columns 0..3; the narrow tile has at most 32)
+                        else if (C::SCALE_REP_B == 1)  // B rows 0..127 (columns 0..3)
                             tc::tmem_cp_32x128b_warpx4(sfb, tc::sdesc_plain_32x16_groups256(bsf));
-                        if constexpr (FP4) {
+                        if constexpr (BF16) {
+                            // K block sub: 64 bf16 per row, four MMAs of 16 K each
+                            const uint32_t as = a_s + sub * A_BYTES, bs = b_s + sub * C::B_BYTES;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                tc::mma_bf16(acc, tc::sdesc_sw128(as + 32 * k),
+                                             tc::sdesc_sw128(bs + 32 * k), idesc[0],
+                                             (!first || sub > 0 || k > 0) ? 1u : 0u);
+                        } else if constexpr (FP4) {
                             // K block sub is bytes 64 sub .. 64 sub + 63 of every packed
                             // row; two MMAs of 64 K each
 #pragma unroll
@@ -616,22 +643,23 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, FP4>::THREADS, 1) moe_grouped_ge
             // the second issuer's accumulator holds something only if the tile has >= 2 stages
             const bool two = C::NSPLIT > 1 && KC > C::KS;
             for (int c0 = 0; c0 < t.n; c0 += 16) {
-                // columns c0 .. c0 + 15: the hi and lo halves added (FP4: one term)
+                // columns c0 .. c0 + 15: the hi and lo halves added (one term: as is)
+                constexpr bool ONE = C::TERMS == 1;
                 uint32_t rh[16], rl[16];
                 float v[16];
                 tc::tmem_ld_32x32b_x16(acc + c0, rh);
-                if (!FP4) tc::tmem_ld_32x32b_x16(acc + t.nmma + c0, rl);
+                if (!ONE) tc::tmem_ld_32x32b_x16(acc + t.nmma + c0, rl);
                 tc::tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    v[j] = __uint_as_float(rh[j]) + (FP4 ? 0.f : __uint_as_float(rl[j]));
+                    v[j] = __uint_as_float(rh[j]) + (ONE ? 0.f : __uint_as_float(rl[j]));
                 if (two) {
                     tc::tmem_ld_32x32b_x16(acc + C::ACC_COLS + c0, rh);
-                    if (!FP4) tc::tmem_ld_32x32b_x16(acc + C::ACC_COLS + t.nmma + c0, rl);
+                    if (!ONE) tc::tmem_ld_32x32b_x16(acc + C::ACC_COLS + t.nmma + c0, rl);
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        v[j] += __uint_as_float(rh[j]) + (FP4 ? 0.f : __uint_as_float(rl[j]));
+                        v[j] += __uint_as_float(rh[j]) + (ONE ? 0.f : __uint_as_float(rl[j]));
                 }
                 if (MODE == MOE_GEMM_GATEUP) {
                     // Lanes 0..63 hold gate rows f0 + r, lanes 64..127 the same up rows.
@@ -661,7 +689,23 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, FP4>::THREADS, 1) moe_grouped_ge
                         const float u = gate ? stg[j * 64 + rr] : v[j];
                         h[jj] = __fdividef(g, 1.f + __expf(-g)) * u;
                     }
-                    if constexpr (FP4) {
+                    if constexpr (BF16) {
+                        // h in bf16 (round to nearest even) as GEMM2's B tile of K
+                        // block f / 64: row r, bytes 2 (f % 64) .. of its 128-byte row,
+                        // pre-swizzled; lanes f and f + 1 share one 4-byte store
+                        uint8_t *hblk = args.h_tiles + ((size_t)t.tt * (F / 64) + f / 64) * MOE_GEMM_BTILE;
+                        const int bo = (f & 63) * 2;  // byte of the row
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const uint32_t hv = f32_to_bf16_bits(h[jj]);
+                            const uint32_t hn = __shfl_down_sync(0xFFFFFFFFu, hv, 1);
+                            const int j = gate ? jj : jj + 8;
+                            const int r = c0 + j;
+                            if (r < t.n && (lane & 1) == 0)
+                                *(uint32_t *)(hblk + r * 128 + (((bo >> 4) ^ (r & 7)) << 4) + (bo & 15)) =
+                                    hv | (hn << 16);
+                        }
+                    } else if constexpr (FP4) {
                         // one MXFP4 term over this warp's 32 rows (one MX block along
                         // F): the scale from the block maximum, each value to the
                         // nearest E2M1 code; lanes f and f + 1 share a byte of the
@@ -890,11 +934,11 @@ cudaError_t moe_launch_prepare_atoms(int E, int M, int K, int mrows, const uint8
 namespace {
 // One persistent CTA per SM (grid = max_ctas, the SM count): the kernel's
 // shared memory admits exactly one CTA per SM.
-template <int MODE, int NT, bool FP4>
+template <int MODE, int NT, int AF>
 cudaError_t launch_gemm_t(const CUtensorMap *mA, const CUtensorMap *mA2, const MoeGemmArgs *args,
                           int max_ctas, cudaStream_t st) {
-    using C = Cfg<MODE, NT, FP4>;
-    auto kern = moe_grouped_gemm_kernel<MODE, NT, FP4>;
+    using C = Cfg<MODE, NT, AF>;
+    auto kern = moe_grouped_gemm_kernel<MODE, NT, AF>;
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (err != cudaSuccess) return err;
@@ -903,23 +947,27 @@ cudaError_t launch_gemm_t(const CUtensorMap *mA, const CUtensorMap *mA2, const M
     return cudaGetLastError();
 }
 
-template <bool FP4>
+template <int AF>
 cudaError_t launch_gemm_fmt(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
                             const MoeGemmArgs *args, int max_rows, int grid, cudaStream_t st) {
     constexpr int NN = MOE_GEMM_NT_NARROW;
     if (max_rows <= NN)
         return mode == MOE_GEMM_GATEUP
-                   ? launch_gemm_t<MOE_GEMM_GATEUP, NN, FP4>(mA, mA2, args, grid, st)
-                   : launch_gemm_t<MOE_GEMM_DOWN, NN, FP4>(mA, mA2, args, grid, st);
+                   ? launch_gemm_t<MOE_GEMM_GATEUP, NN, AF>(mA, mA2, args, grid, st)
+                   : launch_gemm_t<MOE_GEMM_DOWN, NN, AF>(mA, mA2, args, grid, st);
     return mode == MOE_GEMM_GATEUP
-               ? launch_gemm_t<MOE_GEMM_GATEUP, NTMAX, FP4>(mA, mA2, args, grid, st)
-               : launch_gemm_t<MOE_GEMM_DOWN, NTMAX, FP4>(mA, mA2, args, grid, st);
+               ? launch_gemm_t<MOE_GEMM_GATEUP, NTMAX, AF>(mA, mA2, args, grid, st)
+               : launch_gemm_t<MOE_GEMM_DOWN, NTMAX, AF>(mA, mA2, args, grid, st);
 }
 }  // namespace
 
 cudaError_t moe_launch_gemm(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
-                            const MoeGemmArgs *args, int max_rows, int grid, int fp4,
+                            const MoeGemmArgs *args, int max_rows, int grid, int af,
                             cudaStream_t st) {
-    return fp4 ? launch_gemm_fmt<true>(mode, mA, mA2, args, max_rows, grid, st)
-               : launch_gemm_fmt<false>(mode, mA, mA2, args, max_rows, grid, st);
+    switch (af) {
+        case MOE_AF_E4M3X2: return launch_gemm_fmt<MOE_AF_E4M3X2>(mode, mA, mA2, args, max_rows, grid, st);
+        case MOE_AF_MXF4: return launch_gemm_fmt<MOE_AF_MXF4>(mode, mA, mA2, args, max_rows, grid, st);
+        case MOE_AF_BF16: return launch_gemm_fmt<MOE_AF_BF16>(mode, mA, mA2, args, max_rows, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
 }

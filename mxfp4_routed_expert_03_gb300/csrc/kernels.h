@@ -29,9 +29,11 @@ cudaError_t moe_launch_plan(int T, int E, int k, const float *logits, const moe_
 // decode.cu
 int moe_decode_per_lane(int K);
 size_t moe_decode_ws_bytes(int T, int D, int F, int k);
-// shared_out: optional fp32 [T][D] added to every token's combine (NULL: none)
+// shared_out: optional fp32 [T][D] added to every token's combine (NULL: none).
+// fp8: the weights are FP8 (E4M3FN codes [N][K], fp32 scales per 128 x 128
+// block) instead of MXFP4.
 cudaError_t moe_launch_decode(int T, int D, int F, int E, int k, const uint16_t *x,
-                              const moe_plan_buf *p, const moe_weights *w,
+                              const moe_plan_buf *p, const moe_weights *w, int fp8,
                               const float *shared_out, uint16_t *out, void *ws, int *status,
                               const MoeProf &prof, cudaStream_t st);
 
@@ -71,6 +73,19 @@ cudaError_t moe_launch_gather_x(int max_tt, int E, int k, int n_rows, int D, int
                                 const uint8_t *s_hi, const uint8_t *s_lo, uint8_t *tiles,
                                 uint8_t *atoms, int *status, cudaStream_t st);
 
+// fp8.cu: the FP8 lane's prefill side (bf16 copy of the experts, bf16 tiles)
+cudaError_t moe_launch_fp8_dequant(int E, int N, int K, const uint8_t *codes, const float *scales,
+                                   uint16_t *out, cudaStream_t st);
+cudaError_t moe_launch_prep_small_bf16(int T, int E, int k, int D, const int32_t *offsets,
+                                       const int32_t *perm, const int32_t *active,
+                                       const uint16_t *x, int32_t *tt_prefix, uint8_t *tiles,
+                                       float *acc, int *status, cudaStream_t st);
+cudaError_t moe_launch_gather_x_bf16(int max_tt, int E, int k, int n_rows, int D,
+                                     const int32_t *offsets, const int32_t *perm,
+                                     const int32_t *active, const int32_t *tt_prefix,
+                                     const uint16_t *x, uint8_t *tiles, int *status,
+                                     cudaStream_t st);
+
 // grouped_gemm.cu
 #include <cuda.h>
 #define MOE_GEMM_GATEUP 0
@@ -103,14 +118,24 @@ struct MoeGemmArgs {
 size_t moe_prepared_atoms_bytes(int E, int M, int K, int mrows);
 cudaError_t moe_launch_prepare_atoms(int E, int M, int K, int mrows, const uint8_t *s,
                                      const uint8_t *s2, uint8_t *out, cudaStream_t st);
+// Arithmetic formats of the grouped GEMMs (af):
+//  MOE_AF_E4M3X2  MXFP4 weights (8-bit containers) x two-term E4M3 activations,
+//                 kind::mxf8f6f4; K blocks of 128
+//  MOE_AF_MXF4    the FP4 x FP4 mode: packed MXFP4 weights x one MXFP4 term,
+//                 kind::mxf4; activation tiles hold one 128-byte row per token
+//                 per 256-wide K chunk (chunk c of token tile tt at block
+//                 tt * ceil(K / 256) + c of b_tiles / h_tiles), scale blocks
+//                 as for the two-term format, hi rows only
+//  MOE_AF_BF16    bf16 weights x bf16 activations, kind::f16, no scales; K
+//                 blocks of 64 (one 128-byte row per token and block, block
+//                 kb of token tile tt at tt * (K / 64) + kb); args.KC = K / 64
+#define MOE_AF_E4M3X2 0
+#define MOE_AF_MXF4 1
+#define MOE_AF_BF16 2
 // max_rows: bound on any expert's routed rows (T for distinct top-k experts);
-// at most MOE_GEMM_NT_NARROW selects the narrow-tile variant. fp4: the FP4 x
-// FP4 mode (packed weight maps, MXFP4 activation tiles: one 128-byte row per
-// token per 256-wide K chunk, chunk c of token tile tt at block
-// tt * ceil(K / 256) + c of b_tiles / h_tiles; scale blocks as for the
-// two-term mode, hi rows only).
+// at most MOE_GEMM_NT_NARROW selects the narrow-tile variant.
 cudaError_t moe_launch_gemm(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
-                            const MoeGemmArgs *args, int max_rows, int grid, int fp4,
+                            const MoeGemmArgs *args, int max_rows, int grid, int af,
                             cudaStream_t st);
 
 // stream.cu: expert streaming (HBM slot cache in front of host memory)

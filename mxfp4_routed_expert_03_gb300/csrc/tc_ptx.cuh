@@ -219,6 +219,17 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] x B[smem]^T, bf16 operands (kind::f16), 16 K per
+// instruction, fp32 accumulation.
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive (once) on bar when all prior tcgen05 async ops of this thread finish.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile(
@@ -345,6 +356,13 @@ __host__ __device__ __forceinline__ uint32_t idesc_mxf8f6f4(int a_fmt, int b_fmt
     d |= (uint32_t)((M >> 4) & 0x1F) << 24;
     d |= (uint32_t)(a_sf_id & 3) << 29;
     return d;
+}
+
+// kind::f16 instruction descriptor: fp32 accumulator (bit 4), bf16 A and B
+// (bits 7-9 and 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
 }
 
 // Instruction descriptor of kind::mxf4 block-scaled MMA: the same fields as

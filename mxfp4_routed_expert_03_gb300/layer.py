@@ -29,6 +29,20 @@ def alloc_weights(E: int, D: int, F: int, device="cuda") -> dict:
     }
 
 
+def alloc_fp8_weights(E: int, D: int, F: int, device="cuda") -> dict:
+    """Uninitialised FP8 expert tensors: E4M3FN codes (uint8) and fp32 scales
+    per 128 x 128 block, in the library's layout."""
+    nb = lambda n: (n + 127) // 128
+    return {
+        "gate_q": torch.empty((E, F, D), dtype=torch.uint8, device=device),
+        "gate_s": torch.empty((E, nb(F), nb(D)), dtype=torch.float32, device=device),
+        "up_q": torch.empty((E, F, D), dtype=torch.uint8, device=device),
+        "up_s": torch.empty((E, nb(F), nb(D)), dtype=torch.float32, device=device),
+        "down_q": torch.empty((E, D, F), dtype=torch.uint8, device=device),
+        "down_s": torch.empty((E, nb(D), nb(F)), dtype=torch.float32, device=device),
+    }
+
+
 class Plan:
     def __init__(self, T: int, E: int, k: int, device="cuda"):
         dev = device
@@ -50,7 +64,7 @@ class Layer:
     """One routed layer: weights (device tensors) + the library handle."""
 
     def __init__(self, D: int, F: int, E: int, k: int, weights: dict, router_mode: int = 0,
-                 w_router=None, shared=None, act_mode: int = 0):
+                 w_router=None, shared=None, act_mode: int = 0, weight_format: int = 0):
         self.D, self.F, self.E, self.k = D, F, E, k
         self.router_mode = router_mode
         self.weights = weights
@@ -58,7 +72,7 @@ class Layer:
         self.shared = shared
         ptr = lambda t: None if t is None else t.data_ptr()
         sh = shared or {}
-        self.desc = moe_desc(D, F, E, k, router_mode, 1 if shared else 0, act_mode)
+        self.desc = moe_desc(D, F, E, k, router_mode, 1 if shared else 0, act_mode, weight_format)
         self.wdesc = moe_weights(*[weights[n].data_ptr() for n in WEIGHT_NAMES], ptr(w_router),
                                  ptr(sh.get("sh_gate")), ptr(sh.get("sh_up")),
                                  ptr(sh.get("sh_down")))

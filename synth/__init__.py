@@ -28,6 +28,7 @@ ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # Tensor ids: second word of the Philox key (kept equal to philox.h).
 GATE_Q, UP_Q, DOWN_Q, GATE_S, UP_S, DOWN_S = 1, 2, 3, 4, 5, 6
 X, LOGITS, WR, ZIPF, SH_GATE, SH_UP, SH_DOWN = 7, 8, 9, 10, 11, 12, 13
+F8_GATE_Q, F8_UP_Q, F8_DOWN_Q, F8_GATE_S, F8_UP_S, F8_DOWN_S = 14, 15, 16, 17, 18, 19
 
 # E8M0 scale bytes uniform over 2^-4 .. 2^0  ->  {123, ..., 127}
 SCALE_LO, SCALE_N = 123, 5
@@ -79,6 +80,10 @@ def _host_lib():
         L.synth_normal_f32.argtypes = [u64, u32, i64, i64, ctypes.c_double, ctypes.c_double, p]
         L.synth_normal_bf16.argtypes = [u64, u32, i64, i64, ctypes.c_double, p]
         L.synth_zipf_bias.argtypes = [u64, i32, ctypes.c_double, p, p]
+        L.synth_fp8_codes.argtypes = [u64, u32, u32, i64, i64, p]
+        L.synth_fp8_codes.restype = i32
+        L.synth_fp8_scales.argtypes = [u64, u32, u32, i64, i64, p]
+        L.synth_fp8_scales.restype = i32
         _host = L
     return _host
 
@@ -97,6 +102,10 @@ def _dev_lib():
         L.synth_dev_mx_codes_dist.restype = i32
         L.synth_dev_mx_scales.argtypes = [u64, u32, u32, i64, i64, i64, i32, i32, p, p]
         L.synth_dev_mx_scales.restype = i32
+        L.synth_dev_fp8_codes.argtypes = [u64, u32, u32, i64, i64, i64, p, p]
+        L.synth_dev_fp8_codes.restype = i32
+        L.synth_dev_fp8_scales.argtypes = [u64, u32, u32, i64, i64, i64, p, p]
+        L.synth_dev_fp8_scales.restype = i32
         _dev = L
     return _dev
 
@@ -141,6 +150,36 @@ def expert_weights(seed: int, e: int, D: int, F: int, lo: int = SCALE_LO, n: int
         "up_q": mx_codes(seed, UP_Q, e, F, D, dist), "up_s": mx_scales(seed, UP_S, e, F, D, lo, n),
         "down_q": mx_codes(seed, DOWN_Q, e, D, F, dist), "down_s": mx_scales(seed, DOWN_S, e, D, F, lo, n),
     }
+
+
+def fp8_expert_weights(seed: int, e: int, D: int, F: int) -> dict:
+    """FP8 (E4M3FN) expert e: codes gate/up [F, D], down [D, F] (uint8) and fp32
+    block scales [ceil(rows/128), ceil(K/128)] (see philox.h for the draws)."""
+    L = _host_lib()
+    out = {}
+    for name, tq, ts, rows, K in (("gate", F8_GATE_Q, F8_GATE_S, F, D),
+                                  ("up", F8_UP_Q, F8_UP_S, F, D),
+                                  ("down", F8_DOWN_Q, F8_DOWN_S, D, F)):
+        q = np.empty((rows, K), dtype=np.uint8)
+        sc = np.empty(((rows + 127) // 128, (K + 127) // 128), dtype=np.float32)
+        if L.synth_fp8_codes(seed, tq, e, rows, K, _ptr(q)) != 0 or \
+                L.synth_fp8_scales(seed, ts, e, rows, K, _ptr(sc)) != 0:
+            raise ValueError("K must be a multiple of 16")
+        out[name + "_q"], out[name + "_s"] = q, sc
+    return out
+
+
+def dev_fill_fp8_layer(seed: int, E: int, D: int, F: int, bufs: dict, stream: int = 0) -> None:
+    """Fill a whole FP8 layer on the GPU: ``bufs`` maps gate_q/up_q/down_q
+    (E x rows x K bytes) and gate_s/up_s/down_s (E x ceil(rows/128) x
+    ceil(K/128) fp32) to device pointers."""
+    L = _dev_lib()
+    for name, tq, ts, rows, K in (("gate", F8_GATE_Q, F8_GATE_S, F, D),
+                                  ("up", F8_UP_Q, F8_UP_S, F, D),
+                                  ("down", F8_DOWN_Q, F8_DOWN_S, D, F)):
+        if L.synth_dev_fp8_codes(seed, tq, 0, E, rows, K, bufs[name + "_q"], stream) != 0 or \
+                L.synth_dev_fp8_scales(seed, ts, 0, E, rows, K, bufs[name + "_s"], stream) != 0:
+            raise RuntimeError("synth_dev_fp8 failed for " + name)
 
 
 def normal_f32(seed: int, tensor: int, rows: int, cols: int, mean: float = 0.0,

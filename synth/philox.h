@@ -104,12 +104,29 @@ SYNTH_HD void synth_peaked_block(uint64_t seed, uint32_t tensor, uint32_t expert
     }
 }
 
+/* FP8 expert weights (E4M3FN lane): one byte per weight from one random
+ * byte b: the sign from bit 7 and the magnitude code 0x20 + (b & 0x3F), i.e.
+ * exponent fields 4..11 with every mantissa, values 2^-3 .. 30 spread
+ * log-uniformly over eight binades; never a NaN code. */
+SYNTH_HD uint32_t synth_fp8_code(uint32_t b) {
+    return (b & 0x80u) | (0x20u + (b & 0x3Fu));
+}
+
+/* fp32 bits of an FP8 block scale from one word w: 2^-7 * (1 + m 2^-23) with
+ * the 23 mantissa bits m = w >> 9 (every mantissa occurs; values in
+ * [2^-7, 2^-6)). */
+SYNTH_HD uint32_t synth_fp8_scale_bits(uint32_t w) {
+    return ((uint32_t)(127 - 7) << 23) | (w >> 9);
+}
+
 /* Tensor ids (the Philox key's second word). */
 enum {
     SYNTH_T_GATE_Q = 1, SYNTH_T_UP_Q = 2, SYNTH_T_DOWN_Q = 3,
     SYNTH_T_GATE_S = 4, SYNTH_T_UP_S = 5, SYNTH_T_DOWN_S = 6,
     SYNTH_T_X = 7, SYNTH_T_LOGITS = 8, SYNTH_T_WR = 9, SYNTH_T_ZIPF = 10,
-    SYNTH_T_SH_GATE = 11, SYNTH_T_SH_UP = 12, SYNTH_T_SH_DOWN = 13
+    SYNTH_T_SH_GATE = 11, SYNTH_T_SH_UP = 12, SYNTH_T_SH_DOWN = 13,
+    SYNTH_T_F8_GATE_Q = 14, SYNTH_T_F8_UP_Q = 15, SYNTH_T_F8_DOWN_Q = 16,
+    SYNTH_T_F8_GATE_S = 17, SYNTH_T_F8_UP_S = 18, SYNTH_T_F8_DOWN_S = 19
 };
 
 #endif

@@ -88,3 +88,55 @@ SYNTH_API int synth_dev_mx_scales(uint64_t seed, uint32_t tensor, uint32_t e0, i
         seed, tensor, e0, rows, K / 32, n_experts, (uint32_t)lo, (uint32_t)n, (uint8_t *)out);
     return cudaGetLastError() == cudaSuccess ? 0 : -2;
 }
+
+// FP8 expert codes: one thread per 16-byte Philox block of one row.
+__global__ void synth_fp8_codes_kernel(uint64_t seed, uint32_t tensor, uint32_t e0, int64_t rows,
+                                       int64_t nblk, int64_t n_experts, uint4 *out) {
+    int64_t total = n_experts * rows * nblk;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        int64_t b = i % nblk;
+        int64_t r = (i / nblk) % rows;
+        int64_t e = i / (nblk * rows);
+        synth_u32x4 w = synth_block(seed, tensor, e0 + (uint32_t)e, (uint32_t)r, (uint32_t)b);
+        uint32_t o[4];
+        for (int q = 0; q < 4; ++q) {
+            o[q] = 0;
+            for (int j = 0; j < 4; ++j)
+                o[q] |= synth_fp8_code((w.v[q] >> (8 * j)) & 0xFFu) << (8 * j);
+        }
+        out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// FP8 block scales: one thread per entry.
+__global__ void synth_fp8_scales_kernel(uint64_t seed, uint32_t tensor, uint32_t e0, int64_t nr,
+                                        int64_t nk, int64_t n_experts, uint32_t *out) {
+    int64_t total = n_experts * nr * nk;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        int64_t j = i % nk;
+        int64_t r = (i / nk) % nr;
+        int64_t e = i / (nk * nr);
+        synth_u32x4 w = synth_block(seed, tensor, e0 + (uint32_t)e, (uint32_t)r, (uint32_t)(j / 4));
+        out[i] = synth_fp8_scale_bits(w.v[j % 4]);
+    }
+}
+
+// FP8 codes of n_experts experts from e0: n_experts x rows x K bytes (K % 16 == 0).
+SYNTH_API int synth_dev_fp8_codes(uint64_t seed, uint32_t tensor, uint32_t e0, int64_t n_experts,
+                                  int64_t rows, int64_t K, void *out, void *stream) {
+    if (K % 16 != 0 || rows <= 0 || n_experts <= 0 || ((uintptr_t)out & 15)) return -1;
+    synth_fp8_codes_kernel<<<152 * 8, 256, 0, (cudaStream_t)stream>>>(seed, tensor, e0, rows, K / 16,
+                                                                       n_experts, (uint4 *)out);
+    return cudaGetLastError() == cudaSuccess ? 0 : -2;
+}
+
+// FP8 block scales: n_experts x ceil(rows/128) x ceil(K/128) fp32.
+SYNTH_API int synth_dev_fp8_scales(uint64_t seed, uint32_t tensor, uint32_t e0, int64_t n_experts,
+                                   int64_t rows, int64_t K, void *out, void *stream) {
+    if (rows <= 0 || K <= 0 || n_experts <= 0 || ((uintptr_t)out & 3)) return -1;
+    synth_fp8_scales_kernel<<<152 * 4, 256, 0, (cudaStream_t)stream>>>(
+        seed, tensor, e0, (rows + 127) / 128, (K + 127) / 128, n_experts, (uint32_t *)out);
+    return cudaGetLastError() == cudaSuccess ? 0 : -2;
+}

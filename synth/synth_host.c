@@ -78,6 +78,37 @@ SYNTH_API int synth_mx_scales(uint64_t seed, uint32_t tensor, uint32_t expert,
     return 0;
 }
 
+/* FP8 expert codes: rows x K bytes (K a multiple of 16), byte j of 16-byte
+ * block b of row r from Philox block (r, b), mapped by synth_fp8_code. */
+SYNTH_API int synth_fp8_codes(uint64_t seed, uint32_t tensor, uint32_t expert, int64_t rows,
+                              int64_t K, uint8_t *out) {
+    if (K % 16 != 0 || rows < 0) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < K / 16; ++b) {
+            synth_u32x4 w = synth_block(seed, tensor, expert, (uint32_t)r, (uint32_t)b);
+            for (int j = 0; j < 16; ++j)
+                out[r * K + b * 16 + j] = (uint8_t)synth_fp8_code((w.v[j / 4] >> (8 * (j % 4))) & 0xFFu);
+        }
+    }
+    return 0;
+}
+
+/* FP8 block scales: fp32 [ceil(rows/128)][ceil(K/128)], entry (i, j) from word
+ * j % 4 of Philox block (i, j / 4). */
+SYNTH_API int synth_fp8_scales(uint64_t seed, uint32_t tensor, uint32_t expert, int64_t rows,
+                               int64_t K, float *out) {
+    if (rows < 0 || K < 0) return -1;
+    const int64_t nr = (rows + 127) / 128, nk = (K + 127) / 128;
+    for (int64_t i = 0; i < nr; ++i)
+        for (int64_t j = 0; j < nk; ++j) {
+            synth_u32x4 w = synth_block(seed, tensor, expert, (uint32_t)i, (uint32_t)(j / 4));
+            const uint32_t bits = synth_fp8_scale_bits(w.v[j % 4]);
+            memcpy(&out[i * nk + j], &bits, 4);
+        }
+    return 0;
+}
+
 static double synth_normal_at(uint64_t seed, uint32_t tensor, int64_t r, int64_t c) {
     synth_u32x4 w = synth_block(seed, tensor, 0, (uint32_t)r, (uint32_t)(c / 4));
     int pair = (int)((c % 4) / 2);

@@ -58,3 +58,26 @@ def test_peaked_code_distribution():
     # the uniform distribution is unchanged by the new entry point
     np.testing.assert_array_equal(synth.mx_codes(0, synth.GATE_Q, 3, 8, 64),
                                   synth.mx_codes(0, synth.GATE_Q, 3, 8, 64, dist=synth.CODES_UNIFORM))
+
+
+def test_fp8_expert_draws():
+    """FP8 lane: each code byte comes from one Philox byte b as
+    (b & 0x80) | (0x20 + (b & 0x3F)), each block scale from one word w as the
+    fp32 2^-7 (1 + (w >> 9) 2^-23); recomputed here from the raw stream."""
+    import oracle.fp8 as F8
+    seed, e, D, F = 5, 3, 256, 128
+    w = synth.fp8_expert_weights(seed, e, D, F)
+    assert w["gate_q"].shape == (F, D) and w["down_q"].shape == (D, F)
+    assert w["gate_s"].shape == (1, 2) and w["down_s"].shape == (2, 1)
+    # code bytes of gate row 1, block 2 from the raw Philox block
+    words = synth.philox([2, 1, e, seed >> 32], [seed & 0xFFFFFFFF, synth.F8_GATE_Q])
+    raw = [(wd >> (8 * j)) & 0xFF for wd in words for j in range(4)]
+    want = [(b & 0x80) | (0x20 + (b & 0x3F)) for b in raw]
+    assert w["gate_q"][1, 32:48].tolist() == want
+    # scale (0, 1) of up from word 1 of block (0, 0)
+    wd = synth.philox([0, 0, e, seed >> 32], [seed & 0xFFFFFFFF, synth.F8_UP_S])[1]
+    assert w["up_s"][0, 1] == np.float32(2.0 ** -7 * (1 + (wd >> 9) * 2.0 ** -23))
+    vals = F8.TABLE[w["up_q"]]
+    assert np.all(np.isfinite(vals))
+    assert np.abs(vals).min() == 0.125 and np.abs(vals).max() <= 30.0
+    assert np.all((w["down_s"] >= 2.0 ** -7) & (w["down_s"] < 2.0 ** -6))
