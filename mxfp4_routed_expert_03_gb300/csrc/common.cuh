@@ -35,8 +35,42 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
     return __uint_as_float(b << 23);
 }
 
+// Programmatic dependent launch. A kernel launched with launch_pdl may start
+// while its predecessor in the stream is still running (once every CTA of the
+// predecessor has called grid_dep_launch or exited). grid_dep_wait blocks the
+// calling thread until the predecessor has completed and its memory is
+// visible; before it, a kernel may touch only what no running kernel writes.
+// The library keeps one rule that makes this safe for its chains: a kernel
+// whose predecessor may still run calls grid_dep_wait before it reads that
+// predecessor's output, and calls grid_dep_launch only after its own wait or,
+// in the grouped GEMMs, after reading nothing but the plan and the weights;
+// so when a kernel starts, every kernel two or more launches back has
+// completed. Both are no-ops in an ordinary launch.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
+}
+
+// Host: launch `kern` with programmatic dependent launch allowed (see
+// grid_dep_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }

@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(256) moe_prep_small_bf16_kernel(
     const uint16_t *__restrict__ x, int32_t *__restrict__ tt_prefix, uint8_t *__restrict__ tiles,
     float *__restrict__ acc, int *status) {
     __shared__ int s_tok[MOE_GEMM_NT_NARROW];
+    grid_dep_wait();    // the plan comes from the previous kernel
+    grid_dep_launch();
     if (acc) {  // zero this block's share of acc [T][D]
         const int64_t n4 = (int64_t)T * D / 4, per = (n4 + gridDim.x - 1) / gridDim.x;
         const int64_t i0 = (int64_t)blockIdx.x * per, i1 = min(i0 + per, n4);
@@ -157,9 +159,8 @@ cudaError_t moe_launch_prep_small_bf16(int T, int E, int k, int D, const int32_t
                                        const uint16_t *x, int32_t *tt_prefix, uint8_t *tiles,
                                        float *acc, int *status, cudaStream_t st) {
     const int grid = min(T * k, E);  // an upper bound on the active experts
-    moe_prep_small_bf16_kernel<<<grid, 256, 0, st>>>(E, k, T * k, D, T, offsets, perm, active, x,
-                                                     tt_prefix, tiles, acc, status);
-    return cudaGetLastError();
+    return launch_pdl(moe_prep_small_bf16_kernel, dim3(grid), dim3(256), 0, st, E, k, T * k, D, T,
+                      offsets, perm, active, x, tt_prefix, tiles, acc, status);
 }
 
 cudaError_t moe_launch_gather_x_bf16(int max_tt, int E, int k, int n_rows, int D,

@@ -334,6 +334,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
+    // Launched with programmatic dependent launch: everything so far read the
+    // plan only, which is complete (it is two launches back); the next kernel
+    // may start on SMs this grid leaves, and only the activation producer
+    // waits below for the previous kernel's output.
+    grid_dep_launch();
     const uint32_t tmem = *tmem_slot;
     const int MT = args.MT, KC = args.KC;
     const int total_tiles =
@@ -428,6 +433,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
     } else if (warp == 1) {
         // ------------------------------------------ activation producer (one thread)
         if (lane == 0) {
+            grid_dep_wait();  // the activation (or h) tiles come from the previous kernel
             const uint64_t pol_x = tc::policy_evict_last();
             int it = 0;
             bool ok = true;
@@ -943,8 +949,8 @@ cudaError_t launch_gemm_t(const CUtensorMap *mA, const CUtensorMap *mA2, const M
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (err != cudaSuccess) return err;
     if (max_ctas < 1) return cudaErrorInvalidValue;
-    kern<<<max_ctas, C::THREADS, C::SMEM, st>>>(*mA, *mA2, *args);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(max_ctas), dim3(C::THREADS), (size_t)C::SMEM, st, *mA, *mA2,
+                      *args);
 }
 
 template <int AF>

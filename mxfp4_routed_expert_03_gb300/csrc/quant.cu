@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(1024) moe_schedule_kernel(int E, int ntmax,
 
 __global__ void __launch_bounds__(256) moe_finalize_kernel(int64_t n4, const float *__restrict__ acc,
                                                            uint16_t *__restrict__ out) {
+    grid_dep_wait();    // acc is complete once the down GEMM is
     int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (i >= n4) return;
     float4 v = ((const float4 *)acc)[i];
@@ -223,6 +224,8 @@ __global__ void __launch_bounds__(256) moe_prep_small_kernel(
     const uint16_t *__restrict__ x, int32_t *__restrict__ tt_prefix, uint8_t *__restrict__ tiles,
     uint8_t *__restrict__ atoms, float *__restrict__ acc, int *status) {
     __shared__ int s_tok[MOE_GEMM_NT_NARROW];
+    grid_dep_wait();    // the plan comes from the previous kernel
+    grid_dep_launch();
     if (acc) {  // zero this block's share of acc [T][D]
         const int64_t n4 = (int64_t)T * D / 4, per = (n4 + gridDim.x - 1) / gridDim.x;
         const int64_t i0 = (int64_t)blockIdx.x * per, i1 = min(i0 + per, n4);
@@ -329,6 +332,8 @@ __global__ void __launch_bounds__(256) moe_prep_small_fp4_kernel(
     const uint16_t *__restrict__ x, int32_t *__restrict__ tt_prefix, uint8_t *__restrict__ tiles,
     uint8_t *__restrict__ atoms, float *__restrict__ acc, int *status) {
     __shared__ int s_tok[MOE_GEMM_NT_NARROW];
+    grid_dep_wait();    // the plan comes from the previous kernel
+    grid_dep_launch();
     if (acc) {  // zero this block's share of acc [T][D]
         const int64_t n4 = (int64_t)T * D / 4, per = (n4 + gridDim.x - 1) / gridDim.x;
         const int64_t i0 = (int64_t)blockIdx.x * per, i1 = min(i0 + per, n4);
@@ -402,9 +407,8 @@ cudaError_t moe_launch_prep_small_fp4(int T, int E, int k, int D, const int32_t 
                                       const uint16_t *x, int32_t *tt_prefix, uint8_t *tiles,
                                       uint8_t *atoms, float *acc, int *status, cudaStream_t st) {
     const int grid = min(T * k, E);  // an upper bound on the active experts
-    moe_prep_small_fp4_kernel<<<grid, 256, 0, st>>>(E, k, T * k, D, T, offsets, perm, active, x,
-                                                    tt_prefix, tiles, atoms, acc, status);
-    return cudaGetLastError();
+    return launch_pdl(moe_prep_small_fp4_kernel, dim3(grid), dim3(256), 0, st, E, k, T * k, D, T,
+                      offsets, perm, active, x, tt_prefix, tiles, atoms, acc, status);
 }
 
 cudaError_t moe_launch_gather_x_fp4(int max_tt, int E, int k, int n_rows, int D,
@@ -422,9 +426,8 @@ cudaError_t moe_launch_prep_small(int T, int E, int k, int D, const int32_t *off
                                   int32_t *tt_prefix, uint8_t *tiles, uint8_t *atoms, float *acc,
                                   int *status, cudaStream_t st) {
     const int grid = min(T * k, E);  // an upper bound on the active experts
-    moe_prep_small_kernel<<<grid, 256, 0, st>>>(E, k, T * k, D, T, offsets, perm, active, x,
-                                                tt_prefix, tiles, atoms, acc, status);
-    return cudaGetLastError();
+    return launch_pdl(moe_prep_small_kernel, dim3(grid), dim3(256), 0, st, E, k, T * k, D, T,
+                      offsets, perm, active, x, tt_prefix, tiles, atoms, acc, status);
 }
 
 cudaError_t moe_launch_gather_x(int max_tt, int E, int k, int n_rows, int D, int ntmax,
@@ -454,6 +457,6 @@ cudaError_t moe_launch_schedule(int E, int ntmax, const int32_t *offsets, const 
 
 cudaError_t moe_launch_finalize(int T, int D, const float *acc, uint16_t *out, cudaStream_t st) {
     int64_t n4 = (int64_t)T * D / 4;
-    moe_finalize_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(n4, acc, out);
-    return cudaGetLastError();
+    return launch_pdl(moe_finalize_kernel, dim3((unsigned)((n4 + 255) / 256)), dim3(256), 0, st,
+                      n4, acc, out);
 }

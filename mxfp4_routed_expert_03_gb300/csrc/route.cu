@@ -207,6 +207,8 @@ __global__ void __launch_bounds__(kPlanSmallThreads) moe_plan_small_kernel(
     __shared__ int s_nan;
     static_assert(2 * kPlanSmallThreads == MOE_MAX_EXPERTS, "two experts per thread in the scans");
     int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    grid_dep_wait();    // the logits may come from the previous kernel
+    grid_dep_launch();
     for (int e = tid; e < MOE_MAX_EXPERTS; e += kPlanSmallThreads) {
         s_cnt[e] = 0;
         s_mask[e] = 0ull;
@@ -370,10 +372,9 @@ size_t moe_plan_ws_bytes(int T, int E) {
 cudaError_t moe_launch_plan(int T, int E, int k, const float *logits, const moe_plan_buf *p,
                             void *ws, int *status, cudaStream_t st) {
     if (moe_plan_is_small(T)) {
-        moe_plan_small_kernel<<<1, kPlanSmallThreads, 0, st>>>(T, E, k, logits, p->topk_idx, p->topk_w,
-                                                  p->counts, p->offsets, p->perm, p->inv,
-                                                  p->active, status);
-        return cudaGetLastError();
+        return launch_pdl(moe_plan_small_kernel, dim3(1), dim3(kPlanSmallThreads), 0, st, T, E, k,
+                          logits, p->topk_idx, p->topk_w, p->counts, p->offsets, p->perm, p->inv,
+                          p->active, status);
     }
     int CH = MOE_PLAN_CHUNK;
     int nchunks = (T + CH - 1) / CH;
