@@ -472,10 +472,10 @@ def roofline(path, nbytes, flop, ms, peaks, workload, fp4=False, fp8=False):
         kname, csrc = "moe_decode_gateup_kernel", "decode.cu"
         tensor_time = 0.0   # CUDA cores: bound by bytes
     elif fp8:
-        kname, csrc = "moe_grouped_gemm_kernel<0, bf16>", "grouped_gemm.cu"
+        kname, csrc = "moe_grouped_gemm_kernel<0,bf16>", "grouped_gemm.cu"
         tensor_time = flop / 1e12 / bf16_peak        # kind::f16 on the bf16 copy
     elif fp4:
-        kname, csrc = "moe_grouped_gemm_kernel<0, fp4>", "grouped_gemm.cu"
+        kname, csrc = "moe_grouped_gemm_kernel<0,fp4>", "grouped_gemm.cu"
         tensor_time = flop / 1e12 / fp4_peak          # one MXFP4 term, kind::mxf4
     else:
         kname, csrc = "moe_grouped_gemm_kernel<0>", "grouped_gemm.cu"
