@@ -88,13 +88,14 @@ static bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base
 // their scale blocks, h as the down GEMM's B tiles and its scale blocks, the
 // fp32 output accumulator and the token-tile schedule.
 struct FwdLayout {
-    size_t xq_hi, xq_lo, xs_hi, xs_lo, xb, xa, hb, ha, acc, prefix, hsh, total;
+    size_t xq_hi, xq_lo, xs_hi, xs_lo, xb, xa, hb, ha, acc, prefix, hsh, sk_part, sk_count, total;
     int max_tt;
 };
 
 // kdiv: K elements per activation-tile block (128; 64 for the bf16 tiles of
-// FP8 layers).
-static FwdLayout fwd_layout(int T, int D, int F, int E, int k, bool shared, int kdiv = 128) {
+// FP8 layers); n_ctas: the grouped GEMMs' grid.
+static FwdLayout fwd_layout(int T, int D, int F, int E, int k, bool shared, int n_ctas,
+                            int kdiv = 128) {
     FwdLayout L;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -116,6 +117,11 @@ static FwdLayout fwd_layout(int T, int D, int F, int E, int k, bool shared, int 
     L.acc = take((size_t)T * D * sizeof(float));
     L.prefix = take((size_t)(E + 1) * sizeof(int32_t));
     L.hsh = take(shared ? (size_t)T * F * 2 : 0);  // shared expert's bf16 h [T][F]
+    // small batches (narrow GEMMs): split gate/up tiles meet in 2 slots of
+    // 16 x 128 fp32 per CTA; one arrival counter per gate/up weight tile
+    const bool small = T <= MOE_GEMM_NT_NARROW;
+    L.sk_part = take(small ? (size_t)n_ctas * 2 * 16 * 128 * sizeof(float) : 0);
+    L.sk_count = take(small ? std::min(rows, (size_t)E) * (F / 64) * sizeof(int) : 0);
     L.total = off;
     return L;
 }
@@ -548,7 +554,7 @@ MOE_API size_t moe_workspace_bytes(const moe_handle *h, int32_t T, int32_t op) {
                    shared_ws_bytes(h, T);
         case MOE_OP_FORWARD:
             return fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k, d.has_shared,
-                              h->fp8 ? 64 : 128).total;
+                              h->num_sms, h->fp8 ? 64 : 128).total;
         default: return 0;
     }
 }
@@ -665,7 +671,7 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     if (h->streaming && (int64_t)T * d.top_k > h->wE && d.n_experts > h->wE)
         return MOE_ERR_UNSUPPORTED;
     const FwdLayout L = fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k, d.has_shared,
-                                   h->fp8 ? 64 : 128);
+                                   h->num_sms, h->fp8 ? 64 : 128);
     if (ws_bytes < L.total || !ws || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     unsigned char *base = (unsigned char *)ws;
@@ -675,6 +681,9 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     uint8_t *xb = base + L.xb, *xa = base + L.xa, *hb = base + L.hb, *ha = base + L.ha;
     float *acc = (float *)(base + L.acc);
     int32_t *prefix = (int32_t *)(base + L.prefix);
+    float *sk_part = (float *)(base + L.sk_part);
+    int *sk_count = (int *)(base + L.sk_count);
+    const int n_sk = (int)(std::min((size_t)T * d.top_k, (size_t)d.n_experts) * (d.d_ff / 64));
 
     // Small batches (every expert one token tile): quantise, gather, schedule
     // and zero the accumulator in one launch; larger ones in four (the FP4 x
@@ -684,7 +693,8 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     cudaError_t err;
     if (h->fp8 && small) {
         err = moe_launch_prep_small_bf16(T, E, k, D, plan->offsets, plan->perm, plan->active, x,
-                                         prefix, xb, d.has_shared ? nullptr : acc, h->status, st);
+                                         prefix, xb, d.has_shared ? nullptr : acc, sk_count, n_sk,
+                                         h->status, st);
     } else if (h->fp8) {
         err = moe_launch_schedule(E, MOE_GEMM_NTMAX, plan->offsets, plan->active, prefix,
                                   h->status, st);
@@ -693,11 +703,12 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
                                            plan->active, prefix, x, xb, h->status, st);
     } else if (small && fp4) {
         err = moe_launch_prep_small_fp4(T, E, k, D, plan->offsets, plan->perm, plan->active, x,
-                                        prefix, xb, xa, d.has_shared ? nullptr : acc, h->status,
-                                        st);
+                                        prefix, xb, xa, d.has_shared ? nullptr : acc, sk_count,
+                                        n_sk, h->status, st);
     } else if (small) {
         err = moe_launch_prep_small(T, E, k, D, plan->offsets, plan->perm, plan->active, x, prefix,
-                                    xb, xa, d.has_shared ? nullptr : acc, h->status, st);
+                                    xb, xa, d.has_shared ? nullptr : acc, sk_count, n_sk,
+                                    h->status, st);
     } else if (fp4) {
         err = moe_launch_schedule(E, MOE_GEMM_NTMAX, plan->offsets, plan->active, prefix,
                                   h->status, st);
@@ -728,6 +739,10 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     a.status = h->status;
     a.timeout_cycles = h->timeout;
     a.inject = MOE_INJECT_NONE;
+    if (small) {
+        a.sk_part = sk_part;
+        a.sk_count = sk_count;
+    }
     if (h->streaming) {  // experts resident first; the GEMMs then address their slots
         if (err == cudaSuccess) err = stream_fill(h, plan, st);
         a.w_index = moe_stream_view(h->sstate, E, h->wE).slot_of;

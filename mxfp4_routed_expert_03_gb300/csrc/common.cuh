@@ -58,10 +58,18 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 }
 
 // Host: launch `kern` with programmatic dependent launch allowed (see
-// grid_dep_wait).
+// grid_dep_wait). Every kernel of a chain asks for the largest shared-memory
+// carve-out: an SM's L1 / shared split changes only when the SM is idle, so
+// a small kernel's CTA left on an SM in the default split keeps the next
+// kernel's large-shared-memory CTA (the grouped GEMMs) off that SM until it
+// exits, even where both fit.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t st, Args... args) {
+    cudaError_t err = cudaFuncSetAttribute((const void *)kern,
+                                           cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           (int)cudaSharedmemCarveoutMaxShared);
+    if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(256) moe_prep_small_bf16_kernel(
     int E, int k, int n_rows, int D, int T, const int32_t *__restrict__ offsets,
     const int32_t *__restrict__ perm, const int32_t *__restrict__ active,
     const uint16_t *__restrict__ x, int32_t *__restrict__ tt_prefix, uint8_t *__restrict__ tiles,
-    float *__restrict__ acc, int *status) {
+    float *__restrict__ acc, int *__restrict__ sk_count, int n_sk, int *status) {
     __shared__ int s_tok[MOE_GEMM_NT_NARROW];
     grid_dep_wait();    // the plan comes from the previous kernel
     grid_dep_launch();
@@ -86,6 +86,9 @@ __global__ void __launch_bounds__(256) moe_prep_small_bf16_kernel(
         for (int64_t i = i0 + threadIdx.x; i < i1; i += blockDim.x)
             ((float4 *)acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    // the grouped GEMMs' split-tile counters
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_sk; i += gridDim.x * blockDim.x)
+        sk_count[i] = 0;
     int n_active = active[0];
     if (n_active < 0 || n_active > E) {
         if (blockIdx.x == 0 && threadIdx.x == 0) moe_flag(status, MOE_ERR_BAD_INDEX);
@@ -157,10 +160,11 @@ cudaError_t moe_launch_fp8_dequant(int E, int N, int K, const uint8_t *codes, co
 cudaError_t moe_launch_prep_small_bf16(int T, int E, int k, int D, const int32_t *offsets,
                                        const int32_t *perm, const int32_t *active,
                                        const uint16_t *x, int32_t *tt_prefix, uint8_t *tiles,
-                                       float *acc, int *status, cudaStream_t st) {
+                                       float *acc, int *sk_count, int n_sk, int *status,
+                                       cudaStream_t st) {
     const int grid = min(T * k, E);  // an upper bound on the active experts
     return launch_pdl(moe_prep_small_bf16_kernel, dim3(grid), dim3(256), 0, st, E, k, T * k, D, T,
-                      offsets, perm, active, x, tt_prefix, tiles, acc, status);
+                      offsets, perm, active, x, tt_prefix, tiles, acc, sk_count, n_sk, status);
 }
 
 cudaError_t moe_launch_gather_x_bf16(int max_tt, int E, int k, int n_rows, int D,

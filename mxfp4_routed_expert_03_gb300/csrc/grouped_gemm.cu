@@ -146,7 +146,8 @@ struct Cfg {
     static constexpr int N_EMPTY = SA;
     // full(s), empty(s); tfull, tempty x2; one drain barrier per issuer
     static constexpr int N_BARS = N_FULL + N_EMPTY + 4 + NSPLIT;
-    // after the barriers: TMEM address, abort flag, fills issued by each producer
+    // after the barriers: TMEM address, abort flag, fills issued by each
+    // producer, the epilogue's last-part flag
     // Tile lookup. Wide: shared-memory copies of the token-tile prefix, the
     // active experts and their row segments (NTAB entries). Narrow: every
     // expert has one token tile, so tile ct is active expert ct / MT; the
@@ -154,7 +155,7 @@ struct Cfg {
     // loads from the plan past that), which frees the room for a 5th stage.
     static constexpr int NTAB = NARROW ? 0 : MOE_MAX_EXPERTS;
     static constexpr int TLIST = NARROW ? 256 : 0;
-    static constexpr int PREFIX_BASE = (BAR_BASE + N_BARS * 8 + 16 + 15) / 16 * 16;  // int [active + 1]
+    static constexpr int PREFIX_BASE = (BAR_BASE + N_BARS * 8 + 20 + 15) / 16 * 16;  // int [active + 1]
     static constexpr int EXPERT_BASE = (PREFIX_BASE + (NTAB ? (NTAB + 1) * 4 : 0) + 15) / 16 * 16;
     static constexpr int SEG_BASE = (EXPERT_BASE + NTAB * 4 + 15) / 16 * 16;  // int2
     static constexpr int LIST_BASE = (SEG_BASE + NTAB * 8 + 15) / 16 * 16;   // int2 [TLIST]
@@ -170,6 +171,11 @@ struct Cfg {
                       SEG_BASE % 16 == 0 && EPI_BASE % 16 == 0,
                   "shared-memory regions must be 16-byte aligned (int2 / float4 accesses)");
     static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct Seg {
+    int tile;    // tile index in the schedule
+    int s0, s1;  // its pipeline stages [s0, s1) (K blocks KS s0 .. KS s1 - 1)
 };
 
 struct Tile {
@@ -210,17 +216,17 @@ __device__ __forceinline__ bool tile_at(int ct, int n_active, int MT, const int 
     return t.n > 0 && t.n <= NT;
 }
 
-// Narrow tiles: tile ct of this CTA (the i-th it visits) from the CTA's tile
-// list (x = expert | rows << 22, y = first slot; x < 0 when invalid) or, past
-// the list, straight from the plan. Active expert a = ct / MT owns tiles
-// a * MT .. a * MT + MT - 1, one per weight tile.
+// Narrow tiles: tile ct of this CTA from the CTA's tile list (its tiles
+// t_first, t_first + 1, ...: x = expert | rows << 22, y = first slot; x < 0
+// when invalid) or, past the list, straight from the plan. Active expert
+// a = ct / MT owns tiles a * MT .. a * MT + MT - 1, one per weight tile.
 template <int NT, int TLIST>
-__device__ __forceinline__ bool tile_at_list(int ct, int MT, const int2 *s_list,
+__device__ __forceinline__ bool tile_at_list(int ct, int MT, const int2 *s_list, int t_first,
                                              const MoeGemmArgs &args, Tile &t) {
     const int a = ct / MT, mg = ct - a * MT;
-    const int i = (ct - (int)blockIdx.x) / (int)gridDim.x;
+    const int i = ct - t_first;
     int e, sb, cnt;
-    if (i < TLIST) {
+    if (i >= 0 && i < TLIST) {
         const int2 v = s_list[i];
         if (v.x < 0) return false;
         e = v.x & 0x3FFFFF;
@@ -251,6 +257,12 @@ __device__ __forceinline__ int bsf_off(int n, int c) {
     return (i >> 3) * 256 + (j >> 2) * 128 + (i & 7) * 16 + (j & 3) * 4 + c;
 }
 
+// Stream-K split: the CTA whose stage range [U b / G, U (b + 1) / G) holds
+// stage u (the largest b with floor(U b / G) <= u).
+__device__ __forceinline__ int cta_of(long long U, long long u) {
+    return (int)(((u + 1) * gridDim.x + U - 1) / U - 1);
+}
+
 // The four epilogue warps (128 threads) meet at named barrier 1.
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -273,6 +285,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
     uint32_t *tmem_slot = (uint32_t *)(drain + C::NSPLIT);
     int *abort_flag = (int *)(tmem_slot + 1);
     int *s_issued = abort_flag + 1;  // stages filled by the weight [0] / activation [1] producer
+    volatile int *sk_last = s_issued + 2;  // epilogue: this CTA holds a split tile's last part
     int *s_prefix = (int *)(smem + C::PREFIX_BASE);
     int *s_expert = (int *)(smem + C::EXPERT_BASE);
     int2 *s_seg = (int2 *)(smem + C::SEG_BASE);
@@ -282,10 +295,22 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
     const int E = args.E;
     int n_active = args.active[0];
     if (n_active < 0 || n_active > E) n_active = 0;
-    if (C::NARROW) {  // this CTA's tiles: ct = blockIdx.x + i * gridDim.x
-        const long long n_tiles = (long long)n_active * args.MT;
+    // The CTA's work. Wide: whole tiles ct = blockIdx.x + i * gridDim.x.
+    // Narrow (stream-K): the stages of all tiles in order form one sequence,
+    // and CTA b takes the contiguous range [U b / G, U (b + 1) / G) of it, so
+    // every CTA streams the same weight bytes whatever the tile count. A
+    // tile split between CTAs is finished by the last part to arrive: gate/up
+    // parts meet in global memory (args.sk_part), down parts each add their
+    // own share to the output rows.
+    const int NST = (args.KC + C::KS - 1) / C::KS;  // stages per tile
+    const long long U = C::NARROW ? (long long)n_active * args.MT * NST : 0;
+    const long long u_begin = U * blockIdx.x / gridDim.x;
+    const long long u_end = U * (blockIdx.x + 1) / gridDim.x;
+    const int t_first = C::NARROW ? (int)(u_begin / NST) : 0;  // this CTA's first tile
+    if (C::NARROW) {  // this CTA's tiles: t_first, t_first + 1, .. (tile of stage u_end - 1)
+        const long long n_tiles = u_end > u_begin ? (u_end - 1) / NST + 1 : 0;
         for (int i = tid; i < C::TLIST; i += C::THREADS) {
-            const long long ct = (long long)blockIdx.x + (long long)i * gridDim.x;
+            const long long ct = (long long)t_first + i;
             int2 v = make_int2(-1, 0);
             if (ct < n_tiles) {
                 const int a = (int)(ct / args.MT);
@@ -345,9 +370,49 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
         n_active <= 0 ? 0 : (C::NARROW ? n_active * MT : s_prefix[n_active] * MT);
     auto get_tile = [&](int ct, int &cur, Tile &t) -> bool {
         if constexpr (C::NARROW)
-            return tile_at_list<NT, C::TLIST>(ct, MT, s_list, args, t);
+            return tile_at_list<NT, C::TLIST>(ct, MT, s_list, t_first, args, t);
         else
             return tile_at<NT>(ct, n_active, MT, s_prefix, s_expert, s_seg, cur, t);
+    };
+    // Next piece of this CTA's work: tile sg.tile, stages [sg.s0, sg.s1) of
+    // it (all of them unless a narrow tile is split between CTAs). Every role
+    // walks the same sequence; `u` starts at seg_start. A narrow CTA's range
+    // is at most a partial first tile, whole tiles and a partial last tile;
+    // it takes the partial pieces first, so that joining a split tile's
+    // parts (a few round trips to L2) overlaps the whole tiles' streaming
+    // instead of adding to the end of the launch.
+    const int f_tile = (int)(u_begin / NST), l_tile = (int)((u_end - 1) / NST);
+    const int f_s0 = (int)(u_begin - (long long)f_tile * NST);
+    const int l_s1 = (int)(u_end - (long long)l_tile * NST);
+    const int f_s1 = l_tile == f_tile ? l_s1 : NST;
+    const bool f_part = u_end > u_begin && (f_s0 != 0 || f_s1 != NST);
+    const bool l_part = u_end > u_begin && l_tile != f_tile && l_s1 != NST;
+    const int w_first = f_part ? f_tile + 1 : f_tile;  // whole tiles w_first .. w_last
+    const int w_last = u_end > u_begin ? (l_part ? l_tile - 1 : l_tile) : -1;
+    const long long seg_start = C::NARROW ? 0 : (long long)blockIdx.x;
+    auto seg_next = [&](long long &u, Seg &sg) -> bool {
+        if constexpr (C::NARROW) {
+            int i = (int)u++;  // position in this CTA's order
+            if (f_part && i-- == 0) {
+                sg.tile = f_tile; sg.s0 = f_s0; sg.s1 = f_s1;
+                return true;
+            }
+            if (l_part && i-- == 0) {
+                sg.tile = l_tile; sg.s0 = 0; sg.s1 = l_s1;
+                return true;
+            }
+            if (w_first + i > w_last) return false;
+            sg.tile = w_first + i;
+            sg.s0 = 0;
+            sg.s1 = NST;
+        } else {
+            if (u >= total_tiles) return false;
+            sg.tile = (int)u;
+            sg.s0 = 0;
+            sg.s1 = NST;
+            u += gridDim.x;
+        }
+        return true;
     };
     const long long LIMIT = args.timeout_cycles;
     volatile int *abort_p = abort_flag;
@@ -363,9 +428,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
             int it = 0;
             bool ok = true;
             int cur = 0;
-            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+            long long u = seg_start;
+            Seg sg;
+            while (ok && seg_next(u, sg)) {
                 Tile t;
-                if (!get_tile(tile, cur, t)) {
+                if (!get_tile(sg.tile, cur, t)) {
                     moe_flag(args.status, MOE_ERR_BAD_INDEX);
                     continue;
                 }
@@ -379,7 +446,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
                 }
                 const int row0 = we * args.M + t.mt * C::MROWS;
                 const size_t atom0 = ((size_t)we * MT + t.mt) * ((KC + ATOM_BLOCKS - 1) / ATOM_BLOCKS);
-                for (int kc = 0; kc < KC; kc += C::KS) {
+                const int kend = min(KC, sg.s1 * C::KS);
+                for (int kc = sg.s0 * C::KS; kc < kend; kc += C::KS) {
                     const int s = it % C::SA, round = it / C::SA;
                     const int nsub = min(C::KS, KC - kc);
                     if (round > 0 && !tc::mbar_wait(&empty[s], (round - 1) & 1, LIMIT, abort_p)) {
@@ -438,15 +506,18 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
             int it = 0;
             bool ok = true;
             int cur = 0;
-            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+            long long u = seg_start;
+            Seg sg;
+            while (ok && seg_next(u, sg)) {
                 Tile t;
-                if (!get_tile(tile, cur, t)) continue;
+                if (!get_tile(sg.tile, cur, t)) continue;
                 // [hi; lo] rows per K block, or (FP4) one packed row per token per stage
                 const uint32_t tile_bytes =
                     (uint32_t)((FP4 || BF16) ? t.nmma * 128 : 2 * t.nmma * BK);
                 const size_t blk0 = (size_t)t.tt * KC;
                 const size_t chunk0 = (size_t)t.tt * ((KC + 1) / 2);  // FP4: 256-wide K chunks
-                for (int kc = 0; kc < KC; kc += C::KS) {
+                const int kend = min(KC, sg.s1 * C::KS);
+                for (int kc = sg.s0 * C::KS; kc < kend; kc += C::KS) {
                     const int s = it % C::SB, round = it / C::SB;
                     const int nsub = min(C::KS, KC - kc);
                     if (round > 0 && !tc::mbar_wait(&empty[s], (round - 1) & 1, LIMIT, abort_p)) {
@@ -501,9 +572,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
                 fail();
                 ok = false;
             }
-            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+            long long u = seg_start;
+            Seg sg;
+            while (ok && seg_next(u, sg)) {
                 Tile t;
-                if (!get_tile(tile, cur, t)) continue;
+                if (!get_tile(sg.tile, cur, t)) continue;
                 const int buf = lt & 1, use = lt >> 1;
                 ++lt;
                 if (use > 0 && !tc::mbar_wait(&tempty[buf], (use - 1) & 1, LIMIT, abort_p)) {
@@ -523,7 +596,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
                                      : tc::idesc_mxf8f6f4(tc::FMT_E2M1, tc::FMT_E4M3, 128,
                                                           2 * t.nmma, k, k);
                 bool first = true;
-                for (int kc = 0, j = 0; kc < KC; kc += C::KS, ++it, ++j) {
+                const int kend = min(KC, sg.s1 * C::KS);
+                for (int kc = sg.s0 * C::KS, j = 0; kc < kend; kc += C::KS, ++it, ++j) {
                     if (C::NSPLIT > 1 && (j & 1) != split) continue;  // the other issuer's stage
                     const int s = it % C::SA, round = it / C::SA;
                     const int nsub = min(C::KS, KC - kc);
@@ -608,9 +682,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         int lt = 0, cur = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        long long u = seg_start;
+        Seg sg;
+        while (seg_next(u, sg)) {
             Tile t;
-            if (!get_tile(tile, cur, t))
+            if (!get_tile(sg.tile, cur, t))
                 continue;
             const int buf = lt & 1, use = lt >> 1;
             ++lt;
@@ -646,8 +722,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
             }
             tc::tc_fence_after();
             const uint32_t acc = tmem + lane_base + buf * C::BUF_COLS;
-            // the second issuer's accumulator holds something only if the tile has >= 2 stages
-            const bool two = C::NSPLIT > 1 && KC > C::KS;
+            // the second issuer's accumulator holds something only if the piece has >= 2 stages
+            const bool two = C::NSPLIT > 1 && sg.s1 - sg.s0 >= 2;
             for (int c0 = 0; c0 < t.n; c0 += 16) {
                 // columns c0 .. c0 + 15: the hi and lo halves added (one term: as is)
                 constexpr bool ONE = C::TERMS == 1;
@@ -666,6 +742,50 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         v[j] += __uint_as_float(rh[j]) + (ONE ? 0.f : __uint_as_float(rl[j]));
+                }
+                if constexpr (C::NARROW && MODE == MOE_GEMM_GATEUP) {
+                    // A tile split between CTAs (one 16-column chunk): each part
+                    // stores its sums in its slot and counts itself in; the last
+                    // one adds every part in CTA order (the same sums whichever
+                    // CTA is last) and finishes the tile.
+                    const int c_first = cta_of(U, (long long)sg.tile * NST);
+                    const int c_last = cta_of(U, (long long)sg.tile * NST + NST - 1);
+                    if (c_first != c_last) {
+                        // the parts: CTAs in [c_first, c_last] with a non-empty range
+                        // (fewer stages than CTAs leave some ranges empty)
+                        auto has_part = [&](int c) {
+                            return U * (c + 1) / gridDim.x > U * c / gridDim.x;
+                        };
+                        int n_parts = 0;
+                        for (int c = c_first; c <= c_last; ++c) n_parts += has_part(c) ? 1 : 0;
+                        const int row = q * 32 + lane;
+                        float *mine = args.sk_part +
+                                      ((size_t)blockIdx.x * 2 + (sg.tile == t_first ? 0 : 1)) * (16 * 128);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) mine[j * 128 + row] = v[j];
+                        __threadfence();
+                        epi_sync();
+                        if (warp == 3 && lane == 0)
+                            *sk_last = atomicAdd(&args.sk_count[sg.tile], 1) == n_parts - 1;
+                        epi_sync();
+                        if (!*sk_last) break;  // another part finishes the tile
+                        __threadfence();
+                        float sum[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) sum[j] = 0.f;
+                        for (int c = c_first; c <= c_last; ++c) {
+                            if (!has_part(c)) continue;
+                            // slot 0 holds a CTA's first tile, slot 1 its last
+                            const int slot =
+                                sg.tile == (int)(U * c / gridDim.x / NST) ? 0 : 1;
+                            const float *part = args.sk_part + ((size_t)c * 2 + slot) * (16 * 128);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                sum[j] += c == (int)blockIdx.x ? v[j] : __ldcg(part + j * 128 + row);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] = sum[j];
+                    }
                 }
                 if (MODE == MOE_GEMM_GATEUP) {
                     // Lanes 0..63 hold gate rows f0 + r, lanes 64..127 the same up rows.
@@ -957,6 +1077,9 @@ template <int AF>
 cudaError_t launch_gemm_fmt(int mode, const CUtensorMap *mA, const CUtensorMap *mA2,
                             const MoeGemmArgs *args, int max_rows, int grid, cudaStream_t st) {
     constexpr int NN = MOE_GEMM_NT_NARROW;
+    // the narrow gate/up GEMM meets split tiles in sk_part (2 slots per CTA)
+    if (max_rows <= NN && mode == MOE_GEMM_GATEUP && (!args->sk_part || !args->sk_count))
+        return cudaErrorInvalidValue;
     if (max_rows <= NN)
         return mode == MOE_GEMM_GATEUP
                    ? launch_gemm_t<MOE_GEMM_GATEUP, NN, AF>(mA, mA2, args, grid, st)

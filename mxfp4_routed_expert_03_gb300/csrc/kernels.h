@@ -50,17 +50,19 @@ cudaError_t moe_launch_quant_x(int T, int D, const uint16_t *x, uint8_t *q_hi, u
 cudaError_t moe_launch_schedule(int E, int ntmax, const int32_t *offsets, const int32_t *active,
                                 int32_t *tt_prefix, int *status, cudaStream_t st);
 // T <= MOE_GEMM_NT_NARROW: quantise + gather + identity schedule (+ zero acc
-// when acc is not null) in one launch.
+// when acc is not null, and sk_count[0 .. n_sk), the grouped GEMMs'
+// split-tile counters) in one launch.
 cudaError_t moe_launch_prep_small(int T, int E, int k, int D, const int32_t *offsets,
                                   const int32_t *perm, const int32_t *active, const uint16_t *x,
                                   int32_t *tt_prefix, uint8_t *tiles, uint8_t *atoms, float *acc,
-                                  int *status, cudaStream_t st);
+                                  int *sk_count, int n_sk, int *status, cudaStream_t st);
 // The FP4 x FP4 mode's counterparts: one MXFP4 term per activation, in the
 // FP4 tile layout (see moe_launch_gemm).
 cudaError_t moe_launch_prep_small_fp4(int T, int E, int k, int D, const int32_t *offsets,
                                       const int32_t *perm, const int32_t *active,
                                       const uint16_t *x, int32_t *tt_prefix, uint8_t *tiles,
-                                      uint8_t *atoms, float *acc, int *status, cudaStream_t st);
+                                      uint8_t *atoms, float *acc, int *sk_count, int n_sk,
+                                      int *status, cudaStream_t st);
 cudaError_t moe_launch_gather_x_fp4(int max_tt, int E, int k, int n_rows, int D,
                                     const int32_t *offsets, const int32_t *perm,
                                     const int32_t *active, const int32_t *tt_prefix,
@@ -79,7 +81,8 @@ cudaError_t moe_launch_fp8_dequant(int E, int N, int K, const uint8_t *codes, co
 cudaError_t moe_launch_prep_small_bf16(int T, int E, int k, int D, const int32_t *offsets,
                                        const int32_t *perm, const int32_t *active,
                                        const uint16_t *x, int32_t *tt_prefix, uint8_t *tiles,
-                                       float *acc, int *status, cudaStream_t st);
+                                       float *acc, int *sk_count, int n_sk, int *status,
+                                       cudaStream_t st);
 cudaError_t moe_launch_gather_x_bf16(int max_tt, int E, int k, int n_rows, int D,
                                      const int32_t *offsets, const int32_t *perm,
                                      const int32_t *active, const int32_t *tt_prefix,
@@ -110,6 +113,12 @@ struct MoeGemmArgs {
     uint8_t *h_tiles;        // GEMM1 output: h as GEMM2's B tiles [token tile][M/128][...]
     uint8_t *h_atoms;        // GEMM1 output: h scales [token tile][M/128][1 KB]
     float *acc;                        // GEMM2 output
+    // Narrow variant (stream-K split of the stages over the CTAs): gate/up
+    // tiles split between CTAs meet here. sk_part: per CTA two slots of
+    // 16 x 128 fp32 partial sums (its first and its last tile); sk_count:
+    // per weight tile the parts that arrived, zero before the launch.
+    float *sk_part;
+    int *sk_count;
     int *status;
     long long timeout_cycles;
     int inject;              // MOE_INJECT_NONE, or a test hook (see moe_set_fault_injection)

@@ -104,3 +104,31 @@ def test_plan_zero_tokens_is_noop():
     layer = _layer(32, 4)
     assert layer.plan(0, None, None, Plan(0, 32, 4)) == 0
     layer.close()
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 9, 16])
+def test_plan_small_batches_every_group_size(T):
+    """The small-batch kernel selects each token with a group of 16, 8, 4, 2
+    or 1 warps (by T): normal logits, logits on a coarse grid (many equal
+    keys, more of them than places at the k-th value) and all-equal rows."""
+    _compare(synth.normal_f32(300 + T, synth.LOGITS, T, 896), 16)
+    coarse = np.round(synth.normal_f32(400 + T, synth.LOGITS, T, 896) * 2.0) / 2.0
+    _compare(coarse.astype(np.float32), 16)
+    flat = np.zeros((T, 1024), np.float32)
+    flat[:, 1::3] = -0.0
+    _compare(flat, 32)
+    _compare(synth.normal_f32(500 + T, synth.LOGITS, T, 7), 3)
+
+
+def test_plan_nan_logit_single_token():
+    from mxfp4_routed_expert_03_gb300 import MOE_ERR_NAN_LOGIT
+    lg = synth.normal_f32(3, synth.LOGITS, 1, 896)
+    lg[0, 10] = np.nan
+    layer, plan, st = _run_plan(lg, 16)
+    assert st == MOE_ERR_NAN_LOGIT
+    idx = plan.topk_idx.cpu().numpy()[0]
+    assert len(set(idx.tolist())) == 16 and 10 not in idx.tolist()
+    lg[0, 10] = -np.inf
+    ref, _ = oracle.route(lg.astype(np.float64), 16)
+    np.testing.assert_array_equal(idx, ref[0])
+    layer.close()
