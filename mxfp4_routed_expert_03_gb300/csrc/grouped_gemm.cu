@@ -551,136 +551,158 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
             s_issued[1] = it;
         }
     } else if (warp == 2 || warp == 7) {
-        // ------------------------------------------ MMA issuer(s) (one thread each)
-        // The whole loop runs on one thread: reconverging the warp around every
-        // chunk's issue costs about as much as the chunk's MMAs themselves.
-        // With two issuers, issuer `split` takes the tile's stages j with
+        // ------------------------------------------ MMA issuer(s), one warp each
+        // The whole warp walks the issue loop: the waits, shared-memory
+        // addresses and descriptors are the same in every lane, so they stay
+        // in the warp-uniform registers the tcgen05 instructions read, and
+        // lane 0 issues the instructions. (Run by lane 0 alone, the loop moved
+        // every operand into uniform registers anew for each instruction,
+        // about 80 cycles apiece, and a stage issues 9 to 13 of them.) With two
+        // issuers, issuer `split` takes the piece's stages j with
         // j % 2 == split into accumulator `split` of the buffer.
-        if (lane == 0) {
-            const int split = warp == 2 ? 0 : 1;
-            int it = 0, lt = 0, mine = 0;
-            bool ok = true;
-            uint64_t *last = nullptr;
-            uint32_t last_par = 0;
-            int cur = 0;
-            // Test hook (off unless the host asks for it): the first issuer
-            // waits on its drain barrier, which nothing signals before the
-            // wind-down, so the wait runs out and the CTA takes the timeout
-            // path below with operand copies in flight.
-            if (args.inject == MOE_INJECT_GEMM_STALL && split == 0 &&
-                !tc::mbar_wait(&drain[0], 0, LIMIT, abort_p)) {
-                fail();
+        const int split = warp == 2 ? 0 : 1;
+        const bool leader = lane == 0;
+        // a wait in every lane, decided for the warp: it fails if any lane's ran out
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
+            return __all_sync(0xFFFFFFFFu, tc::mbar_wait(bar, parity, LIMIT, abort_p));
+        };
+        int it = 0, lt = 0, mine = 0;
+        bool ok = true;
+        uint64_t *last = nullptr;
+        uint32_t last_par = 0;
+        int cur = 0;
+        // Test hook (off unless the host asks for it): the first issuer waits
+        // on its drain barrier, which nothing signals before the wind-down, so
+        // the wait runs out and the CTA takes the timeout path below with
+        // operand copies in flight.
+        if (args.inject == MOE_INJECT_GEMM_STALL && split == 0 && !wait_all(&drain[0], 0)) {
+            if (leader) fail();
+            ok = false;
+        }
+        long long u = seg_start;
+        Seg sg;
+        while (ok && seg_next(u, sg)) {
+            Tile t;
+            if (!get_tile(sg.tile, cur, t)) continue;
+            const int buf = lt & 1, use = lt >> 1;
+            ++lt;
+            if (use > 0 && !wait_all(&tempty[buf], (use - 1) & 1)) {
+                if (leader) fail();
                 ok = false;
+                break;
             }
-            long long u = seg_start;
-            Seg sg;
-            while (ok && seg_next(u, sg)) {
-                Tile t;
-                if (!get_tile(sg.tile, cur, t)) continue;
-                const int buf = lt & 1, use = lt >> 1;
-                ++lt;
-                if (use > 0 && !tc::mbar_wait(&tempty[buf], (use - 1) & 1, LIMIT, abort_p)) {
-                    fail();
+            tc::tc_fence_after();
+            const uint32_t acc = tmem + buf * C::BUF_COLS + split * C::ACC_COLS;
+            // E4M3 path: scale byte k of each column for K step k (32 wide);
+            // FP4: scale bytes 2 k2, 2 k2 + 1 for K step k2 (64 wide)
+            uint32_t idesc[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                idesc[k] = BF16 ? tc::idesc_bf16(128, t.nmma)
+                           : FP4 ? tc::idesc_mxf4(128, t.nmma, 2 * (k & 1), 2 * (k & 1))
+                                 : tc::idesc_mxf8f6f4(tc::FMT_E2M1, tc::FMT_E4M3, 128,
+                                                      2 * t.nmma, k, k);
+            bool first = true;
+            const int kend = min(KC, sg.s1 * C::KS);
+            for (int kc = sg.s0 * C::KS, j = 0; kc < kend; kc += C::KS, ++it, ++j) {
+                if (C::NSPLIT > 1 && (j & 1) != split) continue;  // the other issuer's stage
+                const int s = it % C::SA, round = it / C::SA;
+                const int nsub = min(C::KS, KC - kc);
+                // With two issuers the slot's previous fill may have been the
+                // other issuer's, still in flight: a parity wait on full[s]
+                // could then match the phase before it. The slot's release of
+                // round - 1 comes after that fill landed and before the
+                // producers refill it, so once it is seen the full wait can only
+                // mean this round (and it costs nothing: the fill of this round
+                // waits for that release anyway).
+                if (C::NSPLIT > 1 && round > 0 && !wait_all(&empty[s], (round - 1) & 1)) {
+                    if (leader) fail();
                     ok = false;
                     break;
                 }
-                tc::tc_fence_after();
-                const uint32_t acc = tmem + buf * C::BUF_COLS + split * C::ACC_COLS;
-                // E4M3 path: scale byte k of each column for K step k (32 wide);
-                // FP4: scale bytes 2 k2, 2 k2 + 1 for K step k2 (64 wide)
-                uint32_t idesc[4];
+                if (!wait_all(&full[s], round & 1)) {
+                    if (leader) fail();
+                    ok = false;
+                    break;
+                }
+                const uint32_t a_s = tc::smem_u32(smem + s * C::A_STAGE);
+                const uint32_t b_s = tc::smem_u32(smem + C::B_BASE + s * C::B_STAGE);
+                const uint32_t slot =
+                    tmem + C::SF_TMEM_COL + (uint32_t)(2 * split + (mine & 1)) * C::SF_SLOT;
+                ++mine;
+                // descriptors of the stage (offsets in 16-byte units are added
+                // to the start-address field, which cannot carry over: shared
+                // memory addresses stay below 256 KB)
+                const uint64_t ad = tc::sdesc_sw128(a_s), bd = tc::sdesc_sw128(b_s);
+                const uint64_t asf4 = tc::sdesc_plain_128x32(a_s + C::A_SF);
+                uint64_t asf1[C::KS], bsf[C::KS];
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    idesc[k] = BF16 ? tc::idesc_bf16(128, t.nmma)
-                               : FP4 ? tc::idesc_mxf4(128, t.nmma, 2 * (k & 1), 2 * (k & 1))
-                                     : tc::idesc_mxf8f6f4(tc::FMT_E2M1, tc::FMT_E4M3, 128,
-                                                          2 * t.nmma, k, k);
-                bool first = true;
-                const int kend = min(KC, sg.s1 * C::KS);
-                for (int kc = sg.s0 * C::KS, j = 0; kc < kend; kc += C::KS, ++it, ++j) {
-                    if (C::NSPLIT > 1 && (j & 1) != split) continue;  // the other issuer's stage
-                    const int s = it % C::SA, round = it / C::SA;
-                    const int nsub = min(C::KS, KC - kc);
-                    // With two issuers the slot's previous fill may have been the
-                    // other issuer's, still in flight: a parity wait on full[s]
-                    // could then match the phase before it. The slot's release
-                    // of round - 1 comes after that fill landed and before the
-                    // producers refill it, so once it is seen the full wait can
-                    // only mean this round (and it costs nothing: the fill of
-                    // this round waits for that release anyway).
-                    if (C::NSPLIT > 1 && round > 0 &&
-                        !tc::mbar_wait(&empty[s], (round - 1) & 1, LIMIT, abort_p)) {
-                        fail();
-                        ok = false;
-                        break;
-                    }
-                    if (!tc::mbar_wait(&full[s], round & 1, LIMIT, abort_p)) {
-                        fail();
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t a_s = tc::smem_u32(smem + s * C::A_STAGE);
-                    const uint32_t b_s = tc::smem_u32(smem + C::B_BASE + s * C::B_STAGE);
-                    const uint32_t slot =
-                        tmem + C::SF_TMEM_COL + (uint32_t)(2 * split + (mine & 1)) * C::SF_SLOT;
-                    ++mine;
+                for (int sub = 0; sub < C::KS; ++sub) {
+                    asf1[sub] = tc::sdesc_plain_32x16_groups256(a_s + C::A_SF + 128 * ((kc + sub) & 1));
+                    const uint32_t b_sf = b_s + C::B_SF + sub * C::SCALE_REP_B * BSF_BYTES;
+                    bsf[sub] = C::SCALE_REP_B == 4 ? tc::sdesc_plain_128x32(b_sf)
+                                                   : tc::sdesc_plain_32x16_groups256(b_sf);
+                }
+                if (leader) {
                     if (C::SCALE_REP_A == 4)  // both blocks' weight scales: columns slot .. slot + 7
-                        tc::tmem_cp_128x256b(slot, tc::sdesc_plain_128x32(a_s + C::A_SF));
-                    for (int sub = 0; sub < nsub; ++sub) {
+                        tc::tmem_cp_128x256b(slot, asf4);
+#pragma unroll
+                    for (int sub = 0; sub < C::KS; ++sub) {
+                        if (sub >= nsub) break;
                         const uint32_t sfa = slot + 4 * sub, sfb = slot + 4 * C::KS + 8 * sub;
                         if (C::SCALE_REP_A == 1)  // K block kc + sub: its half of the scale block
-                            tc::tmem_cp_32x128b_warpx4(
-                                sfa, tc::sdesc_plain_32x16_groups256(a_s + C::A_SF + 128 * ((kc + sub) & 1)));
-                        const uint32_t bsf = b_s + C::B_SF + sub * C::SCALE_REP_B * BSF_BYTES;
+                            tc::tmem_cp_32x128b_warpx4(sfa, asf1[sub]);
                         if (C::SCALE_REP_B == 4)
-                            tc::tmem_cp_128x256b(sfb, tc::sdesc_plain_128x32(bsf));
+                            tc::tmem_cp_128x256b(sfb, bsf[sub]);
                         else if (C::SCALE_REP_B == 1)  // B rows 0..127 (columns 0..3)
-                            tc::tmem_cp_32x128b_warpx4(sfb, tc::sdesc_plain_32x16_groups256(bsf));
+                            tc::tmem_cp_32x128b_warpx4(sfb, bsf[sub]);
                         if constexpr (BF16) {
                             // K block sub: 64 bf16 per row, four MMAs of 16 K each
-                            const uint32_t as = a_s + sub * A_BYTES, bs = b_s + sub * C::B_BYTES;
+                            const uint64_t as = ad + (uint64_t)((sub * A_BYTES) >> 4);
+                            const uint64_t bs = bd + (uint64_t)((sub * C::B_BYTES) >> 4);
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
-                                tc::mma_bf16(acc, tc::sdesc_sw128(as + 32 * k),
-                                             tc::sdesc_sw128(bs + 32 * k), idesc[0],
+                                tc::mma_bf16(acc, as + 2 * k, bs + 2 * k, idesc[0],
                                              (!first || sub > 0 || k > 0) ? 1u : 0u);
                         } else if constexpr (FP4) {
                             // K block sub is bytes 64 sub .. 64 sub + 63 of every packed
                             // row; two MMAs of 64 K each
 #pragma unroll
                             for (int k2 = 0; k2 < 2; ++k2)
-                                tc::mma_mxf4(acc, tc::sdesc_sw128(a_s + 64 * sub + 32 * k2),
-                                             tc::sdesc_sw128(b_s + 64 * sub + 32 * k2), idesc[k2],
-                                             sfa, sfb, (!first || sub > 0 || k2 > 0) ? 1u : 0u);
+                                tc::mma_mxf4(acc, ad + 4 * sub + 2 * k2, bd + 4 * sub + 2 * k2,
+                                             idesc[k2], sfa, sfb,
+                                             (!first || sub > 0 || k2 > 0) ? 1u : 0u);
                         } else {
-                            const uint32_t as = a_s + sub * A_BYTES, bs = b_s + sub * C::B_BYTES;
+                            const uint64_t as = ad + (uint64_t)((sub * A_BYTES) >> 4);
+                            const uint64_t bs = bd + (uint64_t)((sub * C::B_BYTES) >> 4);
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
-                                tc::mma_mxf8f6f4(acc, tc::sdesc_sw128(as + 32 * k),
-                                                 tc::sdesc_sw128(bs + 32 * k), idesc[k], sfa, sfb,
+                                tc::mma_mxf8f6f4(acc, as + 2 * k, bs + 2 * k, idesc[k], sfa, sfb,
                                                  (!first || sub > 0 || k > 0) ? 1u : 0u);
                         }
                     }
-                    first = false;
                     tc::mma_commit(&empty[s]);  // the stage is free once these MMAs are done
-                    last = &empty[s];
-                    last_par = round & 1;
                 }
-                if (!ok) break;
-                tc::mma_commit(&tfull[buf]);
+                first = false;
+                last = &empty[s];
+                last_par = round & 1;
             }
-            // the last stage release must land before the CTA can exit
-            if (ok && last && !tc::mbar_wait(last, last_par, LIMIT, abort_p)) fail();
-            // giving up: this thread's MMAs must finish before tensor memory is
-            // freed (their operands are in shared memory, so they do)
-            if (!ok || *abort_p) tc::drain_mmas(&drain[split], LIMIT);
+            if (!ok) break;
+            if (leader) tc::mma_commit(&tfull[buf]);
+            __syncwarp();
         }
+        // the last stage release must land before the CTA can exit
+        if (ok && last && !wait_all(last, last_par) && leader) fail();
+        // giving up: this warp's MMAs must finish before tensor memory is
+        // freed (their operands are in shared memory, so they do)
+        if (leader && (!ok || *abort_p)) tc::drain_mmas(&drain[split], LIMIT);
         __syncwarp();
     } else {
         // ------------------------------------------ epilogue (warps 3..6)
         // (warp 7, when present, is the second MMA issuer above)
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const uint64_t pol_acc = tc::policy_evict_last();
         int lt = 0, cur = 0;
         long long u = seg_start;
         Seg sg;
@@ -934,9 +956,12 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
                         if (c0 + j < t.n && flj >= 0) {
                             const float4 w4 = *(const float4 *)(stg + j * 32 + 4 * g);
                             float *dst = args.acc + (size_t)(flj / args.k) * args.Dout + d0 + 4 * g;
-                            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst),
-                                         "f"(w4.x), "f"(w4.y), "f"(w4.z), "f"(w4.w)
-                                         : "memory");
+                            // evict_last: the accumulator rows stay in L2 while
+                            // the weights stream through it (evict_first)
+                            asm volatile(
+                                "red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst),
+                                "f"(w4.x), "f"(w4.y), "f"(w4.z), "f"(w4.w), "l"(pol_acc)
+                                : "memory");
                         }
                     }
                     __syncwarp();
