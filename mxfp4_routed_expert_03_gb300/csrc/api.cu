@@ -88,14 +88,21 @@ static bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base
 // their scale blocks, h as the down GEMM's B tiles and its scale blocks, the
 // fp32 output accumulator and the token-tile schedule.
 struct FwdLayout {
-    size_t xq_hi, xq_lo, xs_hi, xs_lo, xb, xa, hb, ha, acc, prefix, hsh, sk_part, sk_count, total;
+    size_t xq_hi, xq_lo, xs_hi, xs_lo, xb, xa, hb, ha, acc, prefix, hsh, sk_part, sk_count, y, total;
     int max_tt;
 };
 
+// Whether moe_forward's larger batches keep every routed row's output and
+// combine them (the FP4 x FP4 mode) instead of adding into an accumulator.
+static bool row_out_mode(const moe_handle *h) {
+    return h->desc.act_mode == MOE_ACT_MXFP4 && !h->fp8;
+}
+
 // kdiv: K elements per activation-tile block (128; 64 for the bf16 tiles of
-// FP8 layers); n_ctas: the grouped GEMMs' grid.
+// FP8 layers); n_ctas: the grouped GEMMs' grid; row_out: larger batches keep
+// every routed row's output (the FP4 x FP4 mode).
 static FwdLayout fwd_layout(int T, int D, int F, int E, int k, bool shared, int n_ctas,
-                            int kdiv = 128) {
+                            bool row_out, int kdiv = 128) {
     FwdLayout L;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -122,6 +129,9 @@ static FwdLayout fwd_layout(int T, int D, int F, int E, int k, bool shared, int 
     const bool small = T <= MOE_GEMM_NT_NARROW;
     L.sk_part = take(small ? (size_t)n_ctas * 2 * 16 * 128 * sizeof(float) : 0);
     L.sk_count = take(small ? std::min(rows, (size_t)E) * (F / 64) * sizeof(int) : 0);
+    // larger batches in the FP4 x FP4 mode: every routed row's down-projection
+    // output, fp32 [T k][D] in perm order, for the deterministic combine
+    L.y = take(!small && row_out ? rows * D * sizeof(float) : 0);
     L.total = off;
     return L;
 }
@@ -554,7 +564,7 @@ MOE_API size_t moe_workspace_bytes(const moe_handle *h, int32_t T, int32_t op) {
                    shared_ws_bytes(h, T);
         case MOE_OP_FORWARD:
             return fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k, d.has_shared,
-                              h->num_sms, h->fp8 ? 64 : 128).total;
+                              h->num_sms, row_out_mode(h), h->fp8 ? 64 : 128).total;
         default: return 0;
     }
 }
@@ -671,7 +681,7 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     if (h->streaming && (int64_t)T * d.top_k > h->wE && d.n_experts > h->wE)
         return MOE_ERR_UNSUPPORTED;
     const FwdLayout L = fwd_layout(T, d.d_model, d.d_ff, d.n_experts, d.top_k, d.has_shared,
-                                   h->num_sms, h->fp8 ? 64 : 128);
+                                   h->num_sms, row_out_mode(h), h->fp8 ? 64 : 128);
     if (ws_bytes < L.total || !ws || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     unsigned char *base = (unsigned char *)ws;
@@ -683,12 +693,19 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     int32_t *prefix = (int32_t *)(base + L.prefix);
     float *sk_part = (float *)(base + L.sk_part);
     int *sk_count = (int *)(base + L.sk_count);
+    float *y = (float *)(base + L.y);
     const int n_sk = (int)(std::min((size_t)T * d.top_k, (size_t)d.n_experts) * (d.d_ff / 64));
 
     // Small batches (every expert one token tile): quantise, gather, schedule
     // and zero the accumulator in one launch; larger ones in four (the FP4 x
     // FP4 mode quantises while gathering: three).
     const bool small = T <= MOE_GEMM_NT_NARROW;
+    // The FP4 x FP4 mode's down GEMM is bound by its epilogue when it adds
+    // into the fp32 accumulator (it issues half the MMAs of the two-term
+    // path): there the rows go to y and a combine sums them. The two-term
+    // path's down GEMM is bound by its MMA issue, so the reductions cost it
+    // nothing and it keeps the accumulator (no extra traffic).
+    const bool row_out = !small && row_out_mode(h);
     const bool fp4 = d.act_mode == MOE_ACT_MXFP4;
     cudaError_t err;
     if (h->fp8 && small) {
@@ -770,10 +787,13 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         h->prof.after(MOE_PROF_FORWARD_GEMM1, st);
     }
     if (err == cudaSuccess) {
-        if (d.has_shared) {  // the shared expert writes acc; the routed rows add onto it
+        // the shared expert writes acc: the routed rows add onto it, or the
+        // combine adds it last (row_out); without one, small batches zeroed
+        // acc in their first launch and larger ones zero it here
+        if (d.has_shared) {
             if (run_shared(h, T, x, (uint16_t *)(base + L.hsh), acc, st) != MOE_OK)
                 err = cudaErrorLaunchFailure;
-        } else if (!small) {  // (small batches zeroed it in the first launch)
+        } else if (!small && !row_out) {
             err = cudaMemsetAsync(acc, 0, (size_t)T * D * sizeof(float), st);
         }
     }
@@ -787,6 +807,7 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         g2.b_tiles = hb;
         g2.b_atoms = ha;
         g2.acc = acc;
+        if (row_out) g2.y = y;  // plain stores of each row; no accumulator reductions
         h->prof.before(MOE_PROF_FORWARD_GEMM2, st);
         err = h->fp8 ? moe_launch_gemm(MOE_GEMM_DOWN, &h->map16_down, &h->map16_down, &g2, T,
                                        h->num_sms, MOE_AF_BF16, st)
@@ -796,7 +817,11 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
                                     h->num_sms, MOE_AF_E4M3X2, st);
         h->prof.after(MOE_PROF_FORWARD_GEMM2, st);
     }
-    if (err == cudaSuccess) err = moe_launch_finalize(T, D, acc, out, st);
+    if (err == cudaSuccess)
+        err = !row_out ? moe_launch_finalize(T, D, acc, out, st)
+                       : moe_launch_combine_slots(T, D, k, rows, plan->topk_w, plan->inv, y,
+                                                  d.has_shared ? acc : nullptr, out, h->status,
+                                                  st);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

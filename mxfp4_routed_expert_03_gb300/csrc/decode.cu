@@ -457,15 +457,16 @@ __global__ void __launch_bounds__(256) moe_combine_slots_kernel(int T, int D, in
                                                                 const float *__restrict__ shared,
                                                                 uint16_t *__restrict__ out,
                                                                 int *status) {
-    int t = blockIdx.y;
-    int d4 = blockIdx.x * blockDim.x + threadIdx.x;  // group of 4 columns
-    if (t >= T || d4 * 4 >= D) return;
+    grid_dep_wait();  // (a dependent launch after the down GEMM that wrote y)
+    const int d4 = blockIdx.x * blockDim.x + threadIdx.x;  // group of 4 columns
+    if (d4 * 4 >= D) return;
+    for (int t = blockIdx.y; t < T; t += gridDim.y) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
         int slot = inv[(size_t)t * k + j];
         if (slot < 0 || slot >= n_rows) { moe_flag(status, MOE_ERR_BAD_INDEX); continue; }
         float w = topk_w[(size_t)t * k + j];
-        float4 v = ((const float4 *)(y + (size_t)slot * D))[d4];
+        const float4 v = ((const float4 *)(y + (size_t)slot * D))[d4];
         acc.x = fmaf(w, v.x, acc.x);
         acc.y = fmaf(w, v.y, acc.y);
         acc.z = fmaf(w, v.z, acc.z);
@@ -482,6 +483,15 @@ __global__ void __launch_bounds__(256) moe_combine_slots_kernel(int T, int D, in
     o.x = (uint32_t)f32_to_bf16_bits(acc.x) | ((uint32_t)f32_to_bf16_bits(acc.y) << 16);
     o.y = (uint32_t)f32_to_bf16_bits(acc.z) | ((uint32_t)f32_to_bf16_bits(acc.w) << 16);
     ((uint2 *)(out + (size_t)t * D))[d4] = o;
+    }
+}
+
+cudaError_t moe_launch_combine_slots(int T, int D, int k, int n_rows, const float *topk_w,
+                                     const int32_t *inv, const float *y, const float *shared,
+                                     uint16_t *out, int *status, cudaStream_t st) {
+    const dim3 g((unsigned)((D / 4 + 255) / 256), (unsigned)min(T, 65535));
+    return launch_pdl(moe_combine_slots_kernel, g, dim3(256), 0, st, T, D, k, n_rows, topk_w, inv,
+                      y, shared, out, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -598,8 +608,6 @@ cudaError_t moe_launch_decode(int T, int D, int F, int E, int k, const uint16_t 
     prof.before(MOE_PROF_DECODE_DOWN, st);
     kDown[fp8 ? 1 : 0][pf](grid, st, D, F, E, n_rows, p, w, h16, hexp, y, status);
     prof.after(MOE_PROF_DECODE_DOWN, st);
-    dim3 g((D / 4 + 255) / 256, T);
-    moe_combine_slots_kernel<<<g, 256, 0, st>>>(T, D, k, n_rows, p->topk_w, p->inv, y, shared_out,
-                                                     out, status);
-    return cudaGetLastError();
+    return moe_launch_combine_slots(T, D, k, n_rows, p->topk_w, p->inv, y, shared_out, out, status,
+                                    st);
 }

@@ -90,12 +90,14 @@ struct Cfg {
     static constexpr bool FP4 = AF == MOE_AF_MXF4;
     static constexpr bool BF16 = AF == MOE_AF_BF16;
     static constexpr bool NARROW = NT <= 16;
-    // MMA-issuing warps. One thread issues a block-scaled MMA every ~90 cycles
-    // when the scale selection changes from MMA to MMA (every K step), which
-    // is slower than the tensor pipe for narrow tiles; the narrow variant
-    // therefore has two issuers, each taking every other K stage of a tile
-    // into its own accumulator, and the epilogue adds the two.
-    static constexpr int NSPLIT = NARROW ? 2 : 1;
+    // MMA-issuing warps. One issuing thread spends about 75 cycles on each
+    // tcgen05 instruction (MMA, scale copy, commit) whatever the MMA's N,
+    // which is slower than the tensor pipe for the narrow tiles and for the
+    // FP4 mode's one-term tiles; those variants therefore have two issuers,
+    // each taking every other K stage of a tile into its own accumulator, and
+    // the epilogue adds the two. (The two-term wide tiles' accumulators,
+    // 2 x 112 columns, leave no tensor memory for a second pair.)
+    static constexpr int NSPLIT = (NARROW || FP4) ? 2 : 1;
     static constexpr int THREADS = 224 + 32 * (NSPLIT - 1);  // warp 7: second issuer
     static constexpr int TERMS = (FP4 || BF16) ? 1 : 2;  // activation terms stacked along N
     static constexpr uint32_t ACC_COLS = TERMS * NT;         // [hi | lo] columns of one accumulator
@@ -107,7 +109,10 @@ struct Cfg {
     // with deeper rings measured slower for the wide variant: the issuer's
     // per-stage waits cost more than the extra depth returned.)
     static constexpr int KS = 2;
-    static constexpr uint32_t SF_SLOT = KS * 12;  // per stage: A 4 columns per block, then B 8
+    // B scale columns per K block: 8 when B has more than 128 rows (two
+    // 128-row halves), else 4
+    static constexpr uint32_t BSF_COLS = TERMS * NT > 128 ? 8 : 4;
+    static constexpr uint32_t SF_SLOT = KS * (4 + BSF_COLS);  // per stage: A 4 columns per block, then B
     // Copies of each scale block in smem: four let one 128x256b copy fill all
     // lane quadrants (weights: both K blocks of a stage at once), which costs
     // the wide variant's single issuer fewer operations. The narrow variant
@@ -649,7 +654,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
 #pragma unroll
                     for (int sub = 0; sub < C::KS; ++sub) {
                         if (sub >= nsub) break;
-                        const uint32_t sfa = slot + 4 * sub, sfb = slot + 4 * C::KS + 8 * sub;
+                        const uint32_t sfa = slot + 4 * sub, sfb = slot + 4 * C::KS + C::BSF_COLS * sub;
                         if (C::SCALE_REP_A == 1)  // K block kc + sub: its half of the scale block
                             tc::tmem_cp_32x128b_warpx4(sfa, asf1[sub]);
                         if (C::SCALE_REP_B == 4)
@@ -716,7 +721,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
             // accumulator is ready (column lane + 32 i of the tile in pf[i], pw[i])
             int pf[NT / 32 + 1];
             float pw[NT / 32 + 1];
-            if (MODE == MOE_GEMM_DOWN) {
+            if (MODE == MOE_GEMM_DOWN && !args.y) {
 #pragma unroll
                 for (int i = 0; i <= NT / 32; ++i) {
                     const int col = lane + 32 * i;
@@ -929,6 +934,14 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
                     }
                     }  // two-term split
                     epi_sync();
+                } else if (args.y) {
+                    // the rows' unweighted values, one 128-byte line per column
+                    // (token row): y[slot][mt * 128 + 32 q + lane]. (bf16 rows,
+                    // half the bytes, measured slower: 64-byte half lines.)
+                    float *yd = args.y + (size_t)t.s0 * args.Dout + t.mt * 128 + q * 32 + lane;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (c0 + j < t.n) yd[(size_t)(c0 + j) * args.Dout] = v[j];
                 } else {
                     // weighted values -> warp staging [16 columns][32 rows], then each
                     // lane adds 4 consecutive rows of one column with one vector reduction

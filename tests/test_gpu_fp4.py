@@ -89,3 +89,35 @@ def test_k3_layer_fp4_mode(k3_layer, T):
     tok = np.arange(T) if T <= 4 else np.array([0, T // 2, T - 1])
     e_q, e_x = _check(got[tok], _study(w, x, lg, tok))
     print("k3 fp4 T=%d vs quantised" % T, e_q, "vs exact", e_x)
+
+
+@pytest.mark.parametrize("shared", [False, True])
+def test_tiny_fp4_wide_batches_are_deterministic(tiny_weights, shared):
+    """Above the narrow tiles the FP4 mode's down GEMM stores every routed
+    row (fp32) and a combine sums each token's rows in a fixed order: two calls
+    on the same inputs give the same bits, with and without a shared expert
+    (whose fp32 output the combine adds last)."""
+    from mxfp4_routed_expert_03_gb300 import MOE_ACT_MXFP4, check
+    from mxfp4_routed_expert_03_gb300.layer import Layer, Plan
+    w = synth.WORKLOADS["tiny"]
+    T = 300
+    x_np, lg_np = synth.make_x(w, 77, T=T), synth.make_logits(w, 77, T=T)
+    sh = ({k: torch.from_numpy(v.view(np.int16)).cuda() for k, v in synth.make_shared(w).items()}
+          if shared else None)
+    layer = Layer(w.D, w.F, w.E, w.k, tiny_weights, shared=sh, act_mode=MOE_ACT_MXFP4)
+    layer.prepare()
+    plan = Plan(T, w.E, w.k)
+    x = to_dev_bf16(x_np)
+    check(layer.plan(T, torch.from_numpy(lg_np).cuda(), None, plan), "plan")
+    outs = []
+    for _ in range(3):
+        out = torch.empty((T, w.D), dtype=torch.int16, device="cuda")
+        check(layer.forward(T, x, plan, out), "forward fp4")
+        outs.append(out.cpu().numpy())
+    st = layer.status()
+    layer.close()
+    assert st == 0, st
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    if not shared:
+        tok = np.arange(0, T, 7)
+        _check(bf16_dev_to_f64(torch.from_numpy(outs[0]))[tok], _study(w, x_np, lg_np, tok))
