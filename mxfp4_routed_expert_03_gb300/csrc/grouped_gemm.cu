@@ -97,13 +97,17 @@ struct Cfg {
     // each taking every other K stage of a tile into its own accumulator, and
     // the epilogue adds the two. (The two-term wide tiles' accumulators,
     // 2 x 112 columns, leave no tensor memory for a second pair.)
-    static constexpr int NSPLIT = (NARROW || FP4) ? 2 : 1;
-    static constexpr int THREADS = 224 + 32 * (NSPLIT - 1);  // warp 7: second issuer
+    // (Measured on the narrow tiles: a third issuer shortens the down GEMM,
+    // whose pieces are short, by 7 %, and lengthens the gate/up GEMM, whose
+    // epilogue then adds three accumulators, by 2 %.)
+    static constexpr int NSPLIT = NARROW ? (MODE == MOE_GEMM_DOWN ? 3 : 2) : FP4 ? 2 : 1;
+    static constexpr int THREADS = 224 + 32 * (NSPLIT - 1);  // warps 7, 8: further issuers
     static constexpr int TERMS = (FP4 || BF16) ? 1 : 2;  // activation terms stacked along N
     static constexpr uint32_t ACC_COLS = TERMS * NT;         // [hi | lo] columns of one accumulator
     static constexpr uint32_t BUF_COLS = NSPLIT * ACC_COLS;  // one of two accumulator buffers
     static constexpr uint32_t SF_TMEM_COL = 2 * BUF_COLS;    // then 2 scale slots per issuer
-    static constexpr uint32_t TMEM_COLS = NARROW ? 256 : 512;
+    // accumulators and scale slots, rounded up to a power of two
+    static constexpr uint32_t TMEM_COLS = (NARROW && NSPLIT < 3) ? 256 : 512;
     // K blocks per pipeline stage: each wait, commit and loop step of an
     // issuer is shared by 8 MMAs (4 in the FP4 mode). (Single-block stages
     // with deeper rings measured slower for the wide variant: the issuer's
@@ -352,7 +356,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
         }
         for (int i = 0; i < C::NSPLIT; ++i) tc::mbar_init(&drain[i], 1);
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(&tfull[b], C::NSPLIT);  // every issuer commits its half
+            tc::mbar_init(&tfull[b], C::NSPLIT);  // every issuer commits its share
             tc::mbar_init(&tempty[b], 4);
         }
         tc::fence_mbar_init();
@@ -555,17 +559,17 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
             }
             s_issued[1] = it;
         }
-    } else if (warp == 2 || warp == 7) {
+    } else if (warp == 2 || warp >= 7) {
         // ------------------------------------------ MMA issuer(s), one warp each
         // The whole warp walks the issue loop: the waits, shared-memory
         // addresses and descriptors are the same in every lane, so they stay
         // in the warp-uniform registers the tcgen05 instructions read, and
         // lane 0 issues the instructions. (Run by lane 0 alone, the loop moved
         // every operand into uniform registers anew for each instruction,
-        // about 80 cycles apiece, and a stage issues 9 to 13 of them.) With two
-        // issuers, issuer `split` takes the piece's stages j with
-        // j % 2 == split into accumulator `split` of the buffer.
-        const int split = warp == 2 ? 0 : 1;
+        // about 80 cycles apiece, and a stage issues 9 to 13 of them.) With
+        // NSPLIT issuers, issuer `split` takes the piece's stages j with
+        // j % NSPLIT == split into accumulator `split` of the buffer.
+        const int split = warp == 2 ? 0 : warp - 6;
         const bool leader = lane == 0;
         // a wait in every lane, decided for the warp: it fails if any lane's ran out
         auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
@@ -610,7 +614,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
             bool first = true;
             const int kend = min(KC, sg.s1 * C::KS);
             for (int kc = sg.s0 * C::KS, j = 0; kc < kend; kc += C::KS, ++it, ++j) {
-                if (C::NSPLIT > 1 && (j & 1) != split) continue;  // the other issuer's stage
+                if (C::NSPLIT > 1 && j % C::NSPLIT != split) continue;  // another issuer's stage
                 const int s = it % C::SA, round = it / C::SA;
                 const int nsub = min(C::KS, KC - kc);
                 // With two issuers the slot's previous fill may have been the
@@ -749,8 +753,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
             }
             tc::tc_fence_after();
             const uint32_t acc = tmem + lane_base + buf * C::BUF_COLS;
-            // the second issuer's accumulator holds something only if the piece has >= 2 stages
-            const bool two = C::NSPLIT > 1 && sg.s1 - sg.s0 >= 2;
+            // issuer i's accumulator holds something only if the piece has > i stages
+            const int nacc = min(C::NSPLIT, sg.s1 - sg.s0);
             for (int c0 = 0; c0 < t.n; c0 += 16) {
                 // columns c0 .. c0 + 15: the hi and lo halves added (one term: as is)
                 constexpr bool ONE = C::TERMS == 1;
@@ -762,9 +766,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     v[j] = __uint_as_float(rh[j]) + (ONE ? 0.f : __uint_as_float(rl[j]));
-                if (two) {
-                    tc::tmem_ld_32x32b_x16(acc + C::ACC_COLS + c0, rh);
-                    if (!ONE) tc::tmem_ld_32x32b_x16(acc + C::ACC_COLS + t.nmma + c0, rl);
+#pragma unroll
+                for (int i = 1; i < C::NSPLIT; ++i) {
+                    if (i >= nacc) break;
+                    tc::tmem_ld_32x32b_x16(acc + i * C::ACC_COLS + c0, rh);
+                    if (!ONE) tc::tmem_ld_32x32b_x16(acc + i * C::ACC_COLS + t.nmma + c0, rl);
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
