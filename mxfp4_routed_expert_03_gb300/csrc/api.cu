@@ -98,6 +98,17 @@ static bool row_out_mode(const moe_handle *h) {
     return h->desc.act_mode == MOE_ACT_MXFP4 && !h->fp8;
 }
 
+// Rows kept in bf16 (half the bytes for the down GEMM to write and the
+// combine to read) while the experts average at most one wide token tile;
+// beyond that each weight tile meets several token tiles, the down GEMM is
+// bound by its epilogue, and fp32 rows stored straight from the lanes cost
+// it less than the bf16 rows' shared-memory staging (measured: prefill4k,
+// 73 rows per expert, 3.32 -> 3.07 ms per step with bf16; router16k, 292
+// rows, 10.36 ms with fp32 against 10.61).
+static bool row_out_bf16(int T, int k, int E) {
+    return (int64_t)T * k <= (int64_t)E * MOE_GEMM_NTMAX;
+}
+
 // kdiv: K elements per activation-tile block (128; 64 for the bf16 tiles of
 // FP8 layers); n_ctas: the grouped GEMMs' grid; row_out: larger batches keep
 // every routed row's output (the FP4 x FP4 mode).
@@ -130,8 +141,8 @@ static FwdLayout fwd_layout(int T, int D, int F, int E, int k, bool shared, int 
     L.sk_part = take(small ? (size_t)n_ctas * 2 * 16 * 128 * sizeof(float) : 0);
     L.sk_count = take(small ? std::min(rows, (size_t)E) * (F / 64) * sizeof(int) : 0);
     // larger batches in the FP4 x FP4 mode: every routed row's down-projection
-    // output, fp32 [T k][D] in perm order, for the deterministic combine
-    L.y = take(!small && row_out ? rows * D * sizeof(float) : 0);
+    // output [T k][D] in perm order (bf16 or fp32), for the deterministic combine
+    L.y = take(!small && row_out ? rows * D * (row_out_bf16(T, k, E) ? 2 : 4) : 0);
     L.total = off;
     return L;
 }
@@ -693,7 +704,7 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     int32_t *prefix = (int32_t *)(base + L.prefix);
     float *sk_part = (float *)(base + L.sk_part);
     int *sk_count = (int *)(base + L.sk_count);
-    float *y = (float *)(base + L.y);
+    void *y = base + L.y;
     const int n_sk = (int)(std::min((size_t)T * d.top_k, (size_t)d.n_experts) * (d.d_ff / 64));
 
     // Small batches (every expert one token tile): quantise, gather, schedule
@@ -807,7 +818,10 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         g2.b_tiles = hb;
         g2.b_atoms = ha;
         g2.acc = acc;
-        if (row_out) g2.y = y;  // plain stores of each row; no accumulator reductions
+        if (row_out) {  // plain stores of each row; no accumulator reductions
+            g2.y = y;
+            g2.y_bf16 = row_out_bf16(T, k, E) ? 1 : 0;
+        }
         h->prof.before(MOE_PROF_FORWARD_GEMM2, st);
         err = h->fp8 ? moe_launch_gemm(MOE_GEMM_DOWN, &h->map16_down, &h->map16_down, &g2, T,
                                        h->num_sms, MOE_AF_BF16, st)
@@ -819,9 +833,15 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     }
     if (err == cudaSuccess)
         err = !row_out ? moe_launch_finalize(T, D, acc, out, st)
-                       : moe_launch_combine_slots(T, D, k, rows, plan->topk_w, plan->inv, y,
-                                                  d.has_shared ? acc : nullptr, out, h->status,
-                                                  st);
+                       : row_out_bf16(T, k, E)
+                           ? moe_launch_combine_slots_bf16(T, D, k, rows, plan->topk_w, plan->inv,
+                                                           (const uint16_t *)y,
+                                                           d.has_shared ? acc : nullptr, out,
+                                                           h->status, st)
+                           : moe_launch_combine_slots(T, D, k, rows, plan->topk_w, plan->inv,
+                                                      (const float *)y,
+                                                      d.has_shared ? acc : nullptr, out,
+                                                      h->status, st);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -450,10 +450,12 @@ __global__ void __launch_bounds__(256, F8 ? 1 : 2) moe_decode_down_kernel(
 // Combine: out[t][d] = bf16( sum_j w[t][j] * y[inv[t*k+j]][d] [+ shared[t][d]] ),
 // j ascending, the shared expert's output (weight 1.0) added last.
 // ---------------------------------------------------------------------------
+// Y: the row element type, float or bf16 bits (uint16_t).
+template <typename Y>
 __global__ void __launch_bounds__(256) moe_combine_slots_kernel(int T, int D, int k, int n_rows,
                                                                 const float *__restrict__ topk_w,
                                                                 const int32_t *__restrict__ inv,
-                                                                const float *__restrict__ y,
+                                                                const Y *__restrict__ y,
                                                                 const float *__restrict__ shared,
                                                                 uint16_t *__restrict__ out,
                                                                 int *status) {
@@ -466,7 +468,14 @@ __global__ void __launch_bounds__(256) moe_combine_slots_kernel(int T, int D, in
         int slot = inv[(size_t)t * k + j];
         if (slot < 0 || slot >= n_rows) { moe_flag(status, MOE_ERR_BAD_INDEX); continue; }
         float w = topk_w[(size_t)t * k + j];
-        const float4 v = ((const float4 *)(y + (size_t)slot * D))[d4];
+        float4 v;
+        if constexpr (sizeof(Y) == 2) {
+            const uint2 b = ((const uint2 *)(y + (size_t)slot * D))[d4];
+            v = make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xFFFF0000u),
+                            __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xFFFF0000u));
+        } else {
+            v = ((const float4 *)(y + (size_t)slot * D))[d4];
+        }
         acc.x = fmaf(w, v.x, acc.x);
         acc.y = fmaf(w, v.y, acc.y);
         acc.z = fmaf(w, v.z, acc.z);
@@ -490,8 +499,17 @@ cudaError_t moe_launch_combine_slots(int T, int D, int k, int n_rows, const floa
                                      const int32_t *inv, const float *y, const float *shared,
                                      uint16_t *out, int *status, cudaStream_t st) {
     const dim3 g((unsigned)((D / 4 + 255) / 256), (unsigned)min(T, 65535));
-    return launch_pdl(moe_combine_slots_kernel, g, dim3(256), 0, st, T, D, k, n_rows, topk_w, inv,
-                      y, shared, out, status);
+    return launch_pdl(moe_combine_slots_kernel<float>, g, dim3(256), 0, st, T, D, k, n_rows,
+                      topk_w, inv, y, shared, out, status);
+}
+
+cudaError_t moe_launch_combine_slots_bf16(int T, int D, int k, int n_rows, const float *topk_w,
+                                          const int32_t *inv, const uint16_t *y,
+                                          const float *shared, uint16_t *out, int *status,
+                                          cudaStream_t st) {
+    const dim3 g((unsigned)((D / 4 + 255) / 256), (unsigned)min(T, 65535));
+    return launch_pdl(moe_combine_slots_kernel<uint16_t>, g, dim3(256), 0, st, T, D, k, n_rows,
+                      topk_w, inv, y, shared, out, status);
 }
 
 // ---------------------------------------------------------------------------

@@ -940,11 +940,31 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
                     }
                     }  // two-term split
                     epi_sync();
+                } else if (args.y && args.y_bf16) {
+                    // the rows' unweighted values in bf16: the four warps' 128
+                    // rows of columns c0 .. c0 + 15 meet in shared memory (bf16,
+                    // two buffers used in turn, so one barrier per 16 columns),
+                    // then each thread writes 32 contiguous bytes of one token
+                    // row, y[slot][mt * 128 + 16 p ..] (whole 128-byte lines;
+                    // bf16 stored straight from the lanes made 64-byte half
+                    // lines, measured slower than fp32 rows)
+                    uint16_t *yb = (uint16_t *)args.y;
+                    uint16_t *stg = (uint16_t *)(smem + C::EPI_BASE) + ((c0 >> 4) & 1) * (16 * 128);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) stg[j * 128 + q * 32 + lane] = f32_to_bf16_bits(v[j]);
+                    epi_sync();
+                    const int e = (warp - 3) * 32 + lane, j = e >> 3, p = e & 7;
+                    if (c0 + j < t.n) {
+                        const uint4 *src = (const uint4 *)(stg + j * 128 + p * 16);
+                        uint4 *dst = (uint4 *)(yb + (size_t)(t.s0 + c0 + j) * args.Dout +
+                                               t.mt * 128 + p * 16);
+                        dst[0] = src[0];
+                        dst[1] = src[1];
+                    }
                 } else if (args.y) {
-                    // the rows' unweighted values, one 128-byte line per column
-                    // (token row): y[slot][mt * 128 + 32 q + lane]. (bf16 rows,
-                    // half the bytes, measured slower: 64-byte half lines.)
-                    float *yd = args.y + (size_t)t.s0 * args.Dout + t.mt * 128 + q * 32 + lane;
+                    // fp32 rows straight from the lanes, one 128-byte line per
+                    // warp and column (token row): y[slot][mt * 128 + 32 q + lane]
+                    float *yd = (float *)args.y + (size_t)t.s0 * args.Dout + t.mt * 128 + q * 32 + lane;
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         if (c0 + j < t.n) yd[(size_t)(c0 + j) * args.Dout] = v[j];

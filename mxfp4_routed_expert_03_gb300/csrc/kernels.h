@@ -33,10 +33,15 @@ size_t moe_decode_ws_bytes(int T, int D, int F, int k);
 // fp8: the weights are FP8 (E4M3FN codes [N][K], fp32 scales per 128 x 128
 // block) instead of MXFP4.
 // out[t] = bf16(sum_j topk_w[t][j] * y[inv[t k + j]] (+ shared[t])), j ascending:
-// the deterministic combine of per-slot expert rows y [n_rows][D] (fp32).
+// the deterministic combine of per-slot expert rows y [n_rows][D], fp32
+// (moe_decode) or, with the _bf16 form, bf16 (moe_forward's FP4 mode).
 cudaError_t moe_launch_combine_slots(int T, int D, int k, int n_rows, const float *topk_w,
                                      const int32_t *inv, const float *y, const float *shared,
                                      uint16_t *out, int *status, cudaStream_t st);
+cudaError_t moe_launch_combine_slots_bf16(int T, int D, int k, int n_rows, const float *topk_w,
+                                          const int32_t *inv, const uint16_t *y,
+                                          const float *shared, uint16_t *out, int *status,
+                                          cudaStream_t st);
 cudaError_t moe_launch_decode(int T, int D, int F, int E, int k, const uint16_t *x,
                               const moe_plan_buf *p, const moe_weights *w, int fp8,
                               const float *shared_out, uint16_t *out, void *ws, int *status,
@@ -124,11 +129,13 @@ struct MoeGemmArgs {
     // per weight tile the parts that arrived, zero before the launch.
     float *sk_part;
     int *sk_count;
-    // Wide down GEMM, when not null: each routed row's unweighted fp32 output
-    // goes to y[slot][0 .. Dout) (slot: its position in perm order) with plain
-    // stores, one 128-byte line per warp and row, for the deterministic
-    // combine; acc is then unused.
-    float *y;
+    // Wide down GEMM, when not null: each routed row's unweighted output goes
+    // to y[slot][0 .. Dout) (slot: its position in perm order) with plain
+    // stores of whole 128-byte lines, for the deterministic combine; acc is
+    // then unused. y_bf16: bf16 rows (rounded to nearest even) staged through
+    // shared memory, else fp32 rows stored straight from the lanes.
+    void *y;
+    int y_bf16;
     int *status;
     long long timeout_cycles;
     int inject;              // MOE_INJECT_NONE, or a test hook (see moe_set_fault_injection)
