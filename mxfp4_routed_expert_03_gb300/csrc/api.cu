@@ -708,8 +708,9 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
     const int n_sk = (int)(std::min((size_t)T * d.top_k, (size_t)d.n_experts) * (d.d_ff / 64));
 
     // Small batches (every expert one token tile): quantise, gather, schedule
-    // and zero the accumulator in one launch; larger ones in four (the FP4 x
-    // FP4 mode quantises while gathering: three).
+    // and zero the accumulator in one launch; larger ones quantise each token
+    // once, schedule the token tiles and gather them (and zero the
+    // accumulator where it is used).
     const bool small = T <= MOE_GEMM_NT_NARROW;
     // The FP4 x FP4 mode's down GEMM is bound by its epilogue when it adds
     // into the fp32 accumulator (it issues half the MMAs of the two-term
@@ -737,12 +738,15 @@ MOE_API int moe_forward(moe_handle *h, int32_t T, const uint16_t *x, const moe_p
         err = moe_launch_prep_small(T, E, k, D, plan->offsets, plan->perm, plan->active, x, prefix,
                                     xb, xa, d.has_shared ? nullptr : acc, sk_count, n_sk,
                                     h->status, st);
-    } else if (fp4) {
-        err = moe_launch_schedule(E, MOE_GEMM_NTMAX, plan->offsets, plan->active, prefix,
-                                  h->status, st);
+    } else if (fp4) {  // each token quantised once (into the two-term path's buffers)
+        err = moe_launch_quant_x_fp4(T, D, x, xq_hi, xs_hi, st);
+        if (err == cudaSuccess)
+            err = moe_launch_schedule(E, MOE_GEMM_NTMAX, plan->offsets, plan->active, prefix,
+                                      h->status, st);
         if (err == cudaSuccess)
             err = moe_launch_gather_x_fp4(L.max_tt, E, k, rows, D, plan->offsets, plan->perm,
-                                          plan->active, prefix, x, xb, xa, h->status, st);
+                                          plan->active, prefix, xq_hi, xs_hi, xb, xa, h->status,
+                                          st);
     } else {
         err = moe_launch_quant_x(T, D, x, xq_hi, xq_lo, xs_hi, xs_lo, st);
         if (err == cudaSuccess)

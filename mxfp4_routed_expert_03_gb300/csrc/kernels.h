@@ -73,11 +73,15 @@ cudaError_t moe_launch_prep_small_fp4(int T, int E, int k, int D, const int32_t 
                                       const uint16_t *x, int32_t *tt_prefix, uint8_t *tiles,
                                       uint8_t *atoms, float *acc, int *sk_count, int n_sk,
                                       int *status, cudaStream_t st);
+// Larger batches: every token's row once to MXFP4 (q [T][D/2], biased scale
+// bytes s [T][D/32]), then the token tiles gathered from them.
+cudaError_t moe_launch_quant_x_fp4(int T, int D, const uint16_t *x, uint8_t *q, uint8_t *s,
+                                   cudaStream_t st);
 cudaError_t moe_launch_gather_x_fp4(int max_tt, int E, int k, int n_rows, int D,
                                     const int32_t *offsets, const int32_t *perm,
                                     const int32_t *active, const int32_t *tt_prefix,
-                                    const uint16_t *x, uint8_t *tiles, uint8_t *atoms, int *status,
-                                    cudaStream_t st);
+                                    const uint8_t *q, const uint8_t *s, uint8_t *tiles,
+                                    uint8_t *atoms, int *status, cudaStream_t st);
 cudaError_t moe_launch_finalize(int T, int D, const float *acc, uint16_t *out, cudaStream_t st);
 cudaError_t moe_launch_gather_x(int max_tt, int E, int k, int n_rows, int D, int ntmax,
                                 const int32_t *offsets, const int32_t *perm, const int32_t *active,

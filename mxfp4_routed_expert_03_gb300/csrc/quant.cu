@@ -382,11 +382,30 @@ __global__ void __launch_bounds__(256) moe_prep_small_fp4_kernel(
 
 // Larger batches in the FP4 mode: one block per token tile quantises its
 // rows straight from x into the tile layout (no separate quantise pass).
+// Larger batches in the FP4 x FP4 mode, first pass: every token's row once
+// to MXFP4, q [T][D/2] (16 code bytes per 32-element block, element 2i in
+// the low nibble of byte i) and s [T][D/32] (biased E8M0 scale bytes).
+__global__ void __launch_bounds__(256) moe_quant_x_fp4_kernel(int64_t n_blocks, int D,
+                                                              const uint16_t *__restrict__ x,
+                                                              uint8_t *__restrict__ q,
+                                                              uint8_t *__restrict__ s) {
+    const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;  // 32-element block
+    if (i >= n_blocks) return;
+    uint32_t w[4];
+    int sc;
+    mxfp4_block32(x + i * 32, w, sc);
+    *(uint4 *)(q + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    s[i] = (uint8_t)(sc + 127);
+}
+
+// Second pass: token tile tt's rows copied from q / s into the tile layout
+// put_fp4_block writes (one 16-byte piece and one scale byte per block).
 __global__ void __launch_bounds__(256) moe_gather_x_fp4_kernel(
     int E, int k, int n_rows, int D, const int32_t *__restrict__ offsets,
     const int32_t *__restrict__ perm, const int32_t *__restrict__ active,
-    const int32_t *__restrict__ prefix, const uint16_t *__restrict__ x, uint8_t *__restrict__ tiles,
-    uint8_t *__restrict__ atoms, int *status) {
+    const int32_t *__restrict__ prefix, const uint8_t *__restrict__ q,
+    const uint8_t *__restrict__ s, uint8_t *__restrict__ tiles, uint8_t *__restrict__ atoms,
+    int *status) {
     __shared__ int s_tok[MOE_GEMM_NTMAX];
     const int tt = blockIdx.x;
     int n_active = active[0];
@@ -403,10 +422,12 @@ __global__ void __launch_bounds__(256) moe_gather_x_fp4_kernel(
     const int nb = D / 32, KC = D / 128, KC2 = (KC + 1) / 2;
     for (int i = threadIdx.x; i < n * nb; i += blockDim.x) {
         const int r = i / nb, b = i % nb;
-        uint32_t w[4];
-        int sc;
-        mxfp4_block32(x + (size_t)s_tok[r] * D + (size_t)b * 32, w, sc);
-        put_fp4_block(tiles, atoms, (size_t)tt, KC2, KC, r, b, w, sc);
+        const size_t src = (size_t)s_tok[r] * nb + b;
+        uint8_t *blk = tiles + ((size_t)tt * KC2 + b / 8) * MOE_GEMM_BTILE;
+        *(uint4 *)(blk + r * 128 + (((b & 7) ^ (r & 7)) << 4)) = *(const uint4 *)(q + src * 16);
+        const int ri = r & 31, rj = r >> 5;
+        atoms[((size_t)tt * KC + b / 4) * 1024 + (ri >> 3) * 256 + (rj >> 2) * 128 + (ri & 7) * 16 +
+              (rj & 3) * 4 + (b & 3)] = s[src];
     }
 }
 
@@ -421,13 +442,20 @@ cudaError_t moe_launch_prep_small_fp4(int T, int E, int k, int D, const int32_t 
                       status);
 }
 
+cudaError_t moe_launch_quant_x_fp4(int T, int D, const uint16_t *x, uint8_t *q, uint8_t *s,
+                                   cudaStream_t st) {
+    const int64_t nb = (int64_t)T * D / 32;
+    moe_quant_x_fp4_kernel<<<(unsigned)((nb + 255) / 256), 256, 0, st>>>(nb, D, x, q, s);
+    return cudaGetLastError();
+}
+
 cudaError_t moe_launch_gather_x_fp4(int max_tt, int E, int k, int n_rows, int D,
                                     const int32_t *offsets, const int32_t *perm,
                                     const int32_t *active, const int32_t *tt_prefix,
-                                    const uint16_t *x, uint8_t *tiles, uint8_t *atoms, int *status,
-                                    cudaStream_t st) {
+                                    const uint8_t *q, const uint8_t *s, uint8_t *tiles,
+                                    uint8_t *atoms, int *status, cudaStream_t st) {
     moe_gather_x_fp4_kernel<<<max_tt, 256, 0, st>>>(E, k, n_rows, D, offsets, perm, active,
-                                                    tt_prefix, x, tiles, atoms, status);
+                                                    tt_prefix, q, s, tiles, atoms, status);
     return cudaGetLastError();
 }
 
