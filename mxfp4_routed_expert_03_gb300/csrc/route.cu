@@ -124,17 +124,135 @@ __device__ __forceinline__ uint32_t row_key(const float *row, int e, int E, bool
     return logit_key(t);
 }
 
+// Sort value of expert e's logit key: larger is earlier in the selection
+// order (descending logit, then ascending index); all values distinct.
+__device__ __forceinline__ uint64_t sort_value(uint32_t key, int e) {
+    return ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e);
+}
+
+__device__ __forceinline__ uint64_t shfl_xor64(uint64_t v, int m) {
+    const uint32_t lo = __shfl_xor_sync(FULL_MASK, (uint32_t)v, m);
+    const uint32_t hi = __shfl_xor_sync(FULL_MASK, (uint32_t)(v >> 32), m);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+// Sorts P independent sets of 64 values in descending order, interleaved so
+// that their dependent chains overlap: element n = 2 lane + h of set p in
+// v[p][h]. Bitonic network: for block size K = 2 .. 64 and distance
+// J = K / 2 .. 1, element n is paired with n ^ J and the pair ordered
+// descending where (n & K) == 0, ascending elsewhere (the last block, K = 64,
+// orders everything descending).
+template <int P>
+__device__ __forceinline__ void warp_sort64(uint64_t (&v)[P][2], int lane) {
+#pragma unroll
+    for (int K = 2; K <= 64; K <<= 1) {
+#pragma unroll
+        for (int J = K >> 1; J > 0; J >>= 1) {
+            if (J == 1) {  // partners in the same lane
+                const bool desc = ((2 * lane) & K) == 0;
+#pragma unroll
+                for (int q = 0; q < P; ++q) {
+                    const uint64_t a = v[q][0], b = v[q][1];
+                    const uint64_t mx = a > b ? a : b, mn = a > b ? b : a;
+                    v[q][0] = desc ? mx : mn;
+                    v[q][1] = desc ? mn : mx;
+                }
+            } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int n = 2 * lane + h;
+                    const bool take_max = (((n & K) == 0) == ((n & J) == 0));
+#pragma unroll
+                    for (int q = 0; q < P; ++q) {
+                        const uint64_t o = shfl_xor64(v[q][h], J >> 1);
+                        v[q][h] = take_max ? (v[q][h] > o ? v[q][h] : o) : (v[q][h] > o ? o : v[q][h]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Top-k of a warp's keys, as warp_select, by a threshold instead of a
+// bitwise search when it can: the k-th largest of the 32 lanes' maxima is at
+// most the k-th largest key (the k lanes with the largest maxima hold k keys
+// at least that large), so every selected key is >= it. When at most 64 keys
+// are, they are gathered (with their positions) and sorted by one bitonic
+// network, and the first k are the selection. Otherwise (many keys equal or
+// close to it) warp_select decides. About 500 instructions per warp against
+// the bitwise search's 32 compares per lane and bit, which left a batch of
+// one warp per token issue-bound. scratch: 64 x 8 bytes of warp-private
+// shared memory (as uint2: 64 entries).
+template <int NK>
+__device__ __forceinline__ void warp_select_thr(const uint32_t (&key)[NK], int k, int lane,
+                                                uint2 *scratch, int &pos_out, uint32_t &key_out) {
+    uint32_t m = 0u;
+#pragma unroll
+    for (int i = 0; i < NK; ++i) m = key[i] > m ? key[i] : m;
+    // the lane maxima in descending order over the lanes (bitonic, as
+    // warp_sort64 with one value per lane)
+#pragma unroll
+    for (int K = 2; K <= 32; K <<= 1) {
+#pragma unroll
+        for (int J = K >> 1; J > 0; J >>= 1) {
+            const uint32_t o = __shfl_xor_sync(FULL_MASK, m, J);
+            const bool take_max = ((lane & K) == 0) == ((lane & J) == 0);
+            m = take_max ? (m > o ? m : o) : (m > o ? o : m);
+        }
+    }
+    const uint32_t t0 = __shfl_sync(FULL_MASK, m, k - 1);
+    int c[2] = {0, 0};
+#pragma unroll
+    for (int i = 0; i < NK; ++i) c[i & 1] += key[i] >= t0 ? 1 : 0;
+    const int mine = c[0] + c[1];
+    const int total = (int)__reduce_add_sync(FULL_MASK, (unsigned)mine);
+    if (total > 64) {
+        warp_select<NK>(key, k, lane, scratch, pos_out, key_out);
+        return;
+    }
+    int off = mine;  // exclusive prefix of the lanes' counts
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(FULL_MASK, off, d);
+        if (lane >= d) off += o;
+    }
+    off -= mine;
+    uint64_t *cand = reinterpret_cast<uint64_t *>(scratch);
+#pragma unroll
+    for (int i = 0; i < NK; ++i)
+        if (key[i] >= t0) cand[off++] = sort_value(key[i], lane + 32 * i);
+    __syncwarp();
+    uint64_t v[1][2];
+    v[0][0] = 2 * lane < total ? cand[2 * lane] : 0ull;
+    v[0][1] = 2 * lane + 1 < total ? cand[2 * lane + 1] : 0ull;
+    __syncwarp();
+    warp_sort64<1>(v, lane);
+    // selection j is element j of the sorted 64: lane j / 2, half j % 2
+    const int src = (lane >> 1) & 15;
+    const uint32_t lo0 = __shfl_sync(FULL_MASK, (uint32_t)v[0][0], src);
+    const uint32_t hi0 = __shfl_sync(FULL_MASK, (uint32_t)(v[0][0] >> 32), src);
+    const uint32_t lo1 = __shfl_sync(FULL_MASK, (uint32_t)v[0][1], src);
+    const uint32_t hi1 = __shfl_sync(FULL_MASK, (uint32_t)(v[0][1] >> 32), src);
+    pos_out = -1;
+    key_out = 0u;
+    if (lane < k) {
+        pos_out = (int)(0xFFFFFFFFu - ((lane & 1) ? lo1 : lo0));
+        key_out = (lane & 1) ? hi1 : hi0;
+    }
+}
+
 // Warp-cooperative top-k of one token's logits (k <= 32, k <= E <= 1024).
 // On return lane j < k holds the j-th selection (expert index, logit):
 // descending logit, ties to the lower expert index. NaN logits count as -inf
 // and set nan_seen. Lane l owns experts l, l + 32, ... (coalesced loads).
+// scratch: 64 entries of warp-private shared memory.
 __device__ __forceinline__ void warp_topk(const float *row, int E, int k, int lane, int &my_e,
                                           float &my_v, bool &nan_seen, uint2 *scratch) {
     uint32_t key[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) key[i] = row_key(row, lane + 32 * i, E, nan_seen);
     uint32_t kv;
-    warp_select<32>(key, k, lane, scratch, my_e, kv);
+    warp_select_thr<32>(key, k, lane, scratch, my_e, kv);
     my_v = lane < k ? key_logit(kv) : -INFINITY;
 }
 
@@ -202,195 +320,16 @@ __device__ __forceinline__ void warp_stable_scatter(const int32_t *idx, int64_t 
     }
 }
 
-// The W warps of group g (W = 1: the warp itself) meet at named barrier 1 + g.
-__device__ __forceinline__ void group_sync(int g, int W) {
-    if (W == 1) __syncwarp();
-    else asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(32 * W) : "memory");
-}
-
-// Sort value of expert e's logit key: larger is earlier in the selection
-// order (descending logit, then ascending index); all values distinct.
-__device__ __forceinline__ uint64_t sort_value(uint32_t key, int e) {
-    return ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e);
-}
-
-__device__ __forceinline__ uint64_t shfl_xor64(uint64_t v, int m) {
-    const uint32_t lo = __shfl_xor_sync(FULL_MASK, (uint32_t)v, m);
-    const uint32_t hi = __shfl_xor_sync(FULL_MASK, (uint32_t)(v >> 32), m);
-    return ((uint64_t)hi << 32) | lo;
-}
-
-// Sorts P independent sets of 64 values in descending order, interleaved so
-// that their dependent chains overlap: element n = 2 lane + h of set p in
-// v[p][h]. Bitonic network: for block size K = 2 .. 64 and distance
-// J = K / 2 .. 1, element n is paired with n ^ J and the pair ordered
-// descending where (n & K) == 0, ascending elsewhere (the last block, K = 64,
-// orders everything descending).
-template <int P>
-__device__ __forceinline__ void warp_sort64(uint64_t (&v)[P][2], int lane) {
-#pragma unroll
-    for (int K = 2; K <= 64; K <<= 1) {
-#pragma unroll
-        for (int J = K >> 1; J > 0; J >>= 1) {
-            if (J == 1) {  // partners in the same lane
-                const bool desc = ((2 * lane) & K) == 0;
-#pragma unroll
-                for (int q = 0; q < P; ++q) {
-                    const uint64_t a = v[q][0], b = v[q][1];
-                    const uint64_t mx = a > b ? a : b, mn = a > b ? b : a;
-                    v[q][0] = desc ? mx : mn;
-                    v[q][1] = desc ? mn : mx;
-                }
-            } else {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int n = 2 * lane + h;
-                    const bool take_max = (((n & K) == 0) == ((n & J) == 0));
-#pragma unroll
-                    for (int q = 0; q < P; ++q) {
-                        const uint64_t o = shfl_xor64(v[q][h], J >> 1);
-                        v[q][h] = take_max ? (v[q][h] > o ? v[q][h] : o) : (v[q][h] > o ? o : v[q][h]);
-                    }
-                }
-            }
-        }
-    }
-}
-
-// Entries of a descending list L[0 .. 32) greater than x.
-__device__ __forceinline__ int count_greater(const uint64_t *L, uint64_t x) {
-    int lo = 0;
-#pragma unroll
-    for (int step = 16; step > 0; step >>= 1)
-        if (L[lo + step - 1] > x) lo += step;
-    return lo + (L[lo] > x ? 1 : 0);
-}
-
-// Top-k of one token's logits (k <= 32, k <= E <= 1024) by the W warps of
-// group g (one or two tokens), thread j of the group; same result as
-// warp_topk. The experts
-// split into 16 slices of 64 (keys past E are 0, below every real key). A
-// warp sorts a slice (bitonic network over its lanes, two values each) and
-// keeps its k largest as a descending list of 32 (the rest 0): every member
-// of the token's top k is on its slice's list. A candidate's rank is then the
-// number of listed values above it, one binary search per list, and the
-// candidates of rank < k land in selection order. lists: 16 x 32 values;
-// out: k values. On return lane j < k of the group's first warp holds the
-// j-th selection.
-template <int W>
-__device__ __forceinline__ void group_topk(const float *row, int E, int k, int g, int j,
-                                           uint64_t *lists, uint64_t *out, bool &nan_seen,
-                                           int &my_e, float &my_v) {
-    constexpr int SPW = 16 / W;               // slices per warp
-    constexpr int P = SPW < 8 ? SPW : 8;      // slices sorted together
-    const int lane = j & 31, w = j >> 5;
-#pragma unroll
-    for (int s0 = 0; s0 < SPW; s0 += P) {
-        uint64_t v[P][2];
-#pragma unroll
-        for (int q = 0; q < P; ++q) {
-            const int slice = w * SPW + s0 + q;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int e = 64 * slice + 2 * lane + h;
-                v[q][h] = e < E ? sort_value(row_key(row, e, E, nan_seen), e) : 0ull;
-            }
-        }
-        warp_sort64<P>(v, lane);
-#pragma unroll
-        for (int q = 0; q < P; ++q) {
-            uint64_t *L = lists + (w * SPW + s0 + q) * 32;
-            // elements 2 lane + h < 32 form the list: the first k kept
-            if (lane < 16) {
-                L[2 * lane] = 2 * lane < k ? v[q][0] : 0ull;
-                L[2 * lane + 1] = 2 * lane + 1 < k ? v[q][1] : 0ull;
-            }
-        }
-    }
-    group_sync(g, W);
-    for (int c = j; c < 16 * k; c += 32 * W) {
-        const uint64_t x = lists[(c / k) * 32 + c % k];
-        int r = 0;
-#pragma unroll
-        for (int l = 0; l < 16; ++l) r += count_greater(lists + l * 32, x);
-        if (r < k) out[r] = x;
-    }
-    group_sync(g, W);
-    my_e = -1;
-    my_v = -INFINITY;
-    if (w == 0 && lane < k) {
-        const uint64_t x = out[lane];
-        my_e = (int)(0xFFFFFFFFu - (uint32_t)x);
-        my_v = key_logit((uint32_t)(x >> 32));
-    }
-    group_sync(g, W);  // the lists are overwritten by the group's next token
-}
-
-// Top-k of one token's logits by the W warps of group g (3 to 8 tokens),
-// thread j of the group (same result as warp_topk). Warp w selects the k
-// largest of experts [w S, w S + S), S = 1024 / W (keys past E are 0 and
-// never beat a real one); the k W candidates are stored in warp order, each
-// warp's in rank order, so among equal keys a lower candidate position is a
-// lower expert index; the group's first warp then selects the k largest
-// candidates. On return lane j < k of that warp holds the j-th selection.
-// cand_key / cand_exp hold k W entries, scratch k entries per warp.
-template <int W>
-__device__ __forceinline__ void group_topk_sel(const float *row, int E, int k, int g, int j,
-                                               uint32_t *cand_key, int *cand_exp, uint2 *scratch,
-                                               bool &nan_seen, int &my_e, float &my_v) {
-    constexpr int S = 1024 / W, NK1 = S / 32;
-    const int lane = j & 31, w = j >> 5;
-    uint32_t key[NK1];
-#pragma unroll
-    for (int i = 0; i < NK1; ++i) key[i] = row_key(row, w * S + lane + 32 * i, E, nan_seen);
-    int pos;
-    uint32_t kv;
-    warp_select<NK1>(key, k, lane, scratch + w * MOE_MAX_TOPK, pos, kv);
-    if (lane < k) {
-        cand_key[w * k + lane] = kv;
-        cand_exp[w * k + lane] = w * S + pos;
-    }
-    group_sync(g, W);
-    my_e = -1;
-    my_v = -INFINITY;
-    if (w == 0) {
-        uint32_t k2[W];
-#pragma unroll
-        for (int i = 0; i < W; ++i) {
-            const int p = lane + 32 * i;
-            k2[i] = p < W * k ? cand_key[p] : 0u;
-        }
-        warp_select<W>(k2, k, lane, scratch, pos, kv);
-        if (lane < k) {
-            my_e = cand_exp[pos];
-            my_v = key_logit(kv);
-        }
-    }
-    group_sync(g, W);  // the candidates are overwritten by the group's next token
-}
-
 }  // namespace
 
 // ---------------------------------------------------------------------------
 // Small batches: one CTA does top-k, histogram, scan and the stable scatter.
-// 512 threads (16 warps) in G token groups of W = 16 / G warps: one token
-// uses the whole CTA, two tokens 8 warps each, and so on down to a warp per
-// token from 9 tokens up, so few tokens still spread their selection over
-// every warp. (A 1024-thread block would cap a thread at 64 registers and
-// push the keys to local memory.) The scans take two experts per thread.
+// 512 threads (16 warps), one warp per token (warp_topk). (A 1024-thread
+// block would cap a thread at 64 registers and push the keys to local
+// memory.) The scans take two experts per thread.
 // ---------------------------------------------------------------------------
 constexpr int kPlanSmallThreads = 512;
 constexpr int kPlanSmallWarps = kPlanSmallThreads / 32;
-// 64-bit words of shared memory per token group: 16 lists of 32 and k
-// outputs, or (4 warps or fewer) candidate keys, experts and warp scratch
-constexpr int kPlanGroupWords = 16 * 32 + MOE_MAX_TOPK;
-static_assert(4 * MOE_MAX_TOPK * 8 + 4 * MOE_MAX_TOPK * 8 <= kPlanGroupWords * 8,
-              "candidates and scratch of a 4-warp group fit its area");
-
-// Warps per token group for T tokens (T <= 64): as many as 16 warps allow.
-__host__ __device__ __forceinline__ int plan_group_warps(int T) {
-    return T >= 9 ? 1 : T >= 5 ? 2 : T >= 3 ? 4 : T == 2 ? 8 : 16;
-}
 
 __global__ void __launch_bounds__(kPlanSmallThreads) moe_plan_small_kernel(
     int T, int E, int k, const float *__restrict__ logits, int32_t *topk_idx, float *topk_w,
@@ -402,7 +341,7 @@ __global__ void __launch_bounds__(kPlanSmallThreads) moe_plan_small_kernel(
     __shared__ int s_cnt[MOE_MAX_EXPERTS];
     __shared__ unsigned long long s_mask[MOE_MAX_EXPERTS];
     __shared__ int s_idx[64 * MOE_MAX_TOPK];
-    extern __shared__ uint64_t s_lists[];  // per token group: 16 lists of 32, then k outputs
+    __shared__ uint2 s_scr[kPlanSmallWarps][64];  // each warp's top-k scratch
     __shared__ int s_tot[33];
     __shared__ int s_nan;
     static_assert(2 * kPlanSmallThreads == MOE_MAX_EXPERTS, "two experts per thread in the scans");
@@ -415,36 +354,18 @@ __global__ void __launch_bounds__(kPlanSmallThreads) moe_plan_small_kernel(
     }
     if (tid == 0) s_nan = 0;
     __syncthreads();
-    // token groups of W warps (group g: warps g W .. g W + W - 1)
-    const int W = plan_group_warps(T);
-    const int G = kPlanSmallWarps / W, g = wid / W, j = tid - g * 32 * W;
     bool nan_seen = false;
-    for (int t = g; t < T; t += G) {
+    for (int t = wid; t < T; t += kPlanSmallWarps) {
         int my_e;
         float my_v;
-        const float *row = logits + (int64_t)t * E;
-        uint64_t *lists = s_lists + (size_t)g * kPlanGroupWords;
-        uint64_t *out = lists + 16 * 32;
-        // the same group area (kPlanGroupWords words) as candidates for W <= 4
-        uint32_t *ck = (uint32_t *)lists;
-        int *ce = (int *)(ck + W * MOE_MAX_TOPK);
-        uint2 *sc = (uint2 *)(ce + W * MOE_MAX_TOPK);
-        switch (W) {  // the same in the whole block; measured fastest per group size
-            case 16: group_topk<16>(row, E, k, g, j, lists, out, nan_seen, my_e, my_v); break;
-            case 8: group_topk<8>(row, E, k, g, j, lists, out, nan_seen, my_e, my_v); break;
-            case 4: group_topk_sel<4>(row, E, k, g, j, ck, ce, sc, nan_seen, my_e, my_v); break;
-            case 2: group_topk_sel<2>(row, E, k, g, j, ck, ce, sc, nan_seen, my_e, my_v); break;
-            default: warp_topk(row, E, k, lane, my_e, my_v, nan_seen, sc); break;
-        }
-        if (j < 32) {  // the group's first warp holds the selections
-            const float w = warp_select_weight(my_v, k, lane);
-            if (lane < k) {
-                topk_idx[(int64_t)t * k + lane] = my_e;
-                topk_w[(int64_t)t * k + lane] = w;
-                s_idx[t * k + lane] = my_e;
-                atomicAdd(&s_cnt[my_e], 1);
-                atomicOr(&s_mask[my_e], 1ull << t);
-            }
+        warp_topk(logits + (int64_t)t * E, E, k, lane, my_e, my_v, nan_seen, s_scr[wid]);
+        const float w = warp_select_weight(my_v, k, lane);
+        if (lane < k) {
+            topk_idx[(int64_t)t * k + lane] = my_e;
+            topk_w[(int64_t)t * k + lane] = w;
+            s_idx[t * k + lane] = my_e;
+            atomicAdd(&s_cnt[my_e], 1);
+            atomicOr(&s_mask[my_e], 1ull << t);
         }
     }
     if (__any_sync(FULL_MASK, nan_seen) && lane == 0) s_nan = 1;
@@ -490,7 +411,7 @@ __global__ void __launch_bounds__(256) moe_topk_kernel(int T, int E, int k,
                                                        const float *__restrict__ logits,
                                                        int32_t *topk_idx, float *topk_w,
                                                        int *status) {
-    __shared__ uint2 s_scratch[8][MOE_MAX_TOPK];
+    __shared__ uint2 s_scratch[8][64];
     int lane = threadIdx.x & 31;
     int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -590,11 +511,7 @@ size_t moe_plan_ws_bytes(int T, int E) {
 cudaError_t moe_launch_plan(int T, int E, int k, const float *logits, const moe_plan_buf *p,
                             void *ws, int *status, cudaStream_t st) {
     if (moe_plan_is_small(T)) {
-        const int smem = kPlanSmallWarps / plan_group_warps(T) * kPlanGroupWords * 8;
-        cudaError_t err = cudaFuncSetAttribute(moe_plan_small_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (err != cudaSuccess) return err;
-        return launch_pdl(moe_plan_small_kernel, dim3(1), dim3(kPlanSmallThreads), (size_t)smem, st,
+        return launch_pdl(moe_plan_small_kernel, dim3(1), dim3(kPlanSmallThreads), 0, st,
                           T, E, k, logits, p->topk_idx, p->topk_w, p->counts, p->offsets, p->perm,
                           p->inv, p->active, status);
     }

@@ -69,9 +69,10 @@ def tiny_weights():
     return host_layer_weights(synth.WORKLOADS["tiny"])
 
 
-@pytest.mark.parametrize("T", [1, 8, 16, 300])
+@pytest.mark.parametrize("T", [1, 8, 16, 300, 3000])
 def test_tiny_layer_fp4_mode(tiny_weights, T):
-    """T <= 16: narrow tiles; T = 300: wide tiles, several per expert."""
+    """T <= 16: narrow tiles; T = 300: wide tiles, several per expert;
+    T = 3000 (375 rows per expert): four ragged wide tiles per expert."""
     w = synth.WORKLOADS["tiny"]
     x, lg = synth.make_x(w, 80 + T, T=T), synth.make_logits(w, 80 + T, T=T)
     got = _forward_fp4(w, tiny_weights, x, lg)
@@ -80,15 +81,30 @@ def test_tiny_layer_fp4_mode(tiny_weights, T):
     print("tiny fp4 T=%d vs quantised" % T, e_q, "vs exact", e_x)
 
 
-@pytest.mark.parametrize("T", [2, 64])
+@pytest.mark.parametrize("T", [2, 64, 8192])
 def test_k3_layer_fp4_mode(k3_layer, T):
-    """The study's shape (two tokens) and a wide-tile batch."""
+    """The study's shape (two tokens) and wide-tile batches (T = 8192: about
+    146 rows per expert, two tiles each)."""
     w = synth.WORKLOADS["decode4"]
     x, lg = synth.make_x(w, 90 + T, T=T), synth.make_logits(w, 90 + T, T=T)
     got = _forward_fp4(w, k3_layer, x, lg)
-    tok = np.arange(T) if T <= 4 else np.array([0, T // 2, T - 1])
+    tok = (np.arange(T) if T <= 4 else np.array([0, T // 2, T - 1]) if T <= 64
+           else np.array([0, T - 1]))
     e_q, e_x = _check(got[tok], _study(w, x, lg, tok))
     print("k3 fp4 T=%d vs quantised" % T, e_q, "vs exact", e_x)
+
+
+def test_tiny_fp4_one_expert_holds_all_rows(tiny_weights):
+    """Every token picks expert 9 (and three others): its 1000 rows make nine
+    wide tiles of 111 or 112 rows, the others ragged tiles of their own."""
+    w = synth.WORKLOADS["tiny"]
+    T = 1000
+    x, lg = synth.make_x(w, 85, T=T), synth.make_logits(w, 85, T=T)
+    lg[:, 9] = 60.0
+    got = _forward_fp4(w, tiny_weights, x, lg)
+    tok = np.unique(np.r_[np.arange(0, T, 29), 110, 111, 221, 222, T - 1])
+    e_q, e_x = _check(got[tok], _study(w, x, lg, tok))
+    print("tiny fp4 one hot expert vs quantised", e_q, "vs exact", e_x)
 
 
 @pytest.mark.parametrize("T,shared", [(300, False), (300, True), (1000, False)])

@@ -107,11 +107,15 @@ def test_plan_zero_tokens_is_noop():
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 9, 16])
-def test_plan_small_batches_every_group_size(T):
-    """The small-batch kernel selects each token with a group of 16, 8, 4, 2
-    or 1 warps (by T): normal logits, logits on a coarse grid (many equal
-    keys, more of them than places at the k-th value) and all-equal rows."""
+def test_plan_small_batches_threshold_and_fallback(T):
+    """The small-batch kernel selects each token with one warp: the keys at or
+    above the k-th largest lane maximum, sorted, when there are at most 64 of
+    them (normal logits; logits on a fine grid, with ties at and around the
+    k-th value), else the bitwise search (a coarse grid: more equal keys than
+    places at the k-th value; all-equal rows)."""
     _compare(synth.normal_f32(300 + T, synth.LOGITS, T, 896), 16)
+    fine = np.round(synth.normal_f32(450 + T, synth.LOGITS, T, 896) * 16.0) / 16.0
+    _compare(fine.astype(np.float32), 16)
     coarse = np.round(synth.normal_f32(400 + T, synth.LOGITS, T, 896) * 2.0) / 2.0
     _compare(coarse.astype(np.float32), 16)
     flat = np.zeros((T, 1024), np.float32)
