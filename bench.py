@@ -660,7 +660,7 @@ def measure(ctx, name, wl, steps, warmup, sampler, peaks, breakdown=True, path_o
     h2d = sum(T * D_MODEL * 2 + (0 if use_router else T * ctx.n_exp * 4) for T in wl["Ts"])
     d2h = sum(T * D_MODEL * 2 for T in wl["Ts"])
     record = {
-        "workload": wl["desc"], "T": wl["Ts"],
+        "workload": wl["desc"], "T": wl["Ts"], "dtype": dtype_of(wl, path),
         "path": ("moe_plan (router)" if use_router else "moe_plan") + " + " +
                 ", ".join(f"moe_{b['path']} (T={b['T']})" for b in batches),
         "steps": steps, "warmup": warmup, "ms_per_step": elapsed_ms / steps,
@@ -740,6 +740,17 @@ def stream_roofline(ctx, layer, stats0, stats1, kern_ms, steps, n_batches, store
     return roof, info
 
 
+def dtype_of(wl, path):
+    """The arithmetic types a workload's path computes in (operands -> accumulator)."""
+    if wl.get("fp8"):
+        return "e4m3fn x f16 -> f32" if path == "decode" else "bf16 (from e4m3fn) x bf16 -> f32"
+    if wl.get("act", 0):
+        return "mxfp4 x mxfp4 -> f32"
+    if path == "decode":
+        return "mxfp4 x f16 -> f32"
+    return "mxfp4 x 2-term e4m3 -> f32"
+
+
 # Workloads that get a record of their own in the default run's line.
 RECORDS = ("decode_T1", "decode_T4", "decode_T16", "prefill4k", "skewed8k", "router16k",
            "prefill4k_fp4", "router16k_fp4", "decode_fp8", "prefill4k_fp8")
@@ -789,8 +800,7 @@ def run_ours(args):
         "metric": METRIC, "value": head["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "mxfp4 x f16 -> f32" if (args.path or wl["path"]) == "decode" and CROSSOVER_T
-                 else "mxfp4 x 2-term e4m3 -> f32",
+        "dtype": dtype_of(wl, args.path or wl["path"]),
         "data": "synthetic (seeded Philox weights, N(0,1) activations and logits)",
         "config": config,
         "roofline": head["roofline"],
