@@ -401,7 +401,8 @@ def make_layer(ctx, wl, base):
 def make_batches(ctx, wl, base, path_of, use_router):
     """Seeded (x, logits) sets per batch size, resident in HBM (x only when the
     library computes the logits), their pinned host copies for the end-to-end
-    pass, plan and output buffers."""
+    pass (x and logits of a set side by side in one buffer, so one copy moves
+    a step's inputs), plan and output buffers."""
     import numpy as np
     import torch
     import synth
@@ -415,15 +416,26 @@ def make_batches(ctx, wl, base, path_of, use_router):
         ls_h = [np.zeros((T, ctx.n_exp), np.float32) if use_router else
                 synth.make_logits(w, ctx.rank * 97 + i) for i in range(n_sets)]
         dev = ctx.dev
+        xb = T * D_MODEL * 2                              # bytes of x (bf16), a multiple of 16
+        lb = 0 if use_router else T * ctx.n_exp * 4       # bytes of the logits (fp32)
+        pin = []
+        for a, l in zip(xs_h, ls_h):
+            buf = torch.empty(xb + lb, dtype=torch.uint8).pin_memory()
+            buf[:xb] = torch.from_numpy(a.view(np.uint8).reshape(-1))
+            if lb:
+                buf[xb:] = torch.from_numpy(l.view(np.uint8).reshape(-1))
+            pin.append(buf)
+        dxl = torch.empty(xb + lb, dtype=torch.uint8, device=dev)
         batches.append({"T": T,
                         "x": [torch.from_numpy(a.view(np.int16)).to(dev) for a in xs_h],
                         "l": [torch.from_numpy(a).to(dev) for a in ls_h],
-                        "px": [torch.from_numpy(a.view(np.int16)).pin_memory() for a in xs_h],
-                        "pl": [torch.from_numpy(a).pin_memory() for a in ls_h],
+                        "pxl": pin,
                         "plan": Plan(T, ctx.n_exp, TOP_K),
                         "out": torch.empty((T, D_MODEL), dtype=torch.int16, device=dev),
-                        "dx": torch.empty((T, D_MODEL), dtype=torch.int16, device=dev),
-                        "dl": torch.empty((T, ctx.n_exp), dtype=torch.float32, device=dev),
+                        "dxl": dxl,
+                        "dx": dxl[:xb].view(torch.int16).view(T, D_MODEL),
+                        "dl": (dxl[xb:].view(torch.float32).view(T, ctx.n_exp) if lb else
+                               torch.empty((T, ctx.n_exp), dtype=torch.float32, device=dev)),
                         "hout": torch.empty((T, D_MODEL), dtype=torch.int16).pin_memory(),
                         "path": path_of(T)})
     return batches
@@ -545,9 +557,7 @@ def measure(ctx, name, wl, steps, warmup, sampler, peaks, breakdown=True, path_o
                 kind = prof_kind if prof_kind is not None else main_kind[b["path"]]
                 check(moe_profile_kernel(layer.h, kind, ev0, ev1), "profile")
             if e2e:
-                b["dx"].copy_(b["px"][s], non_blocking=True)
-                if not use_router:
-                    b["dl"].copy_(b["pl"][s], non_blocking=True)
+                b["dxl"].copy_(b["pxl"][s], non_blocking=True)  # x (and logits): one copy
                 x, lg = b["dx"], b["dl"]
             else:
                 x, lg = b["x"][s], b["l"][s]
