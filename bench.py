@@ -398,17 +398,27 @@ def make_layer(ctx, wl, base):
     return layer, info
 
 
+def pad256(a):
+    """A byte array zero-padded to a multiple of 256 bytes (keeps every input
+    in the end-to-end step buffer 256-byte aligned)."""
+    import numpy as np
+    return np.concatenate([a, np.zeros((-len(a)) % 256, np.uint8)])
+
+
 def make_batches(ctx, wl, base, path_of, use_router):
     """Seeded (x, logits) sets per batch size, resident in HBM (x only when the
     library computes the logits), their pinned host copies for the end-to-end
-    pass (x and logits of a set side by side in one buffer, so one copy moves
-    a step's inputs), plan and output buffers."""
+    pass, plan and output buffers. For the end-to-end pass the inputs of all
+    of a step's batches (x, then the logits, per batch) sit side by side in
+    one pinned buffer per set and the outputs in one device buffer, so a step
+    moves its inputs with one copy and its outputs with one."""
     import numpy as np
     import torch
     import synth
     from mxfp4_routed_expert_03_gb300.layer import Plan
     n_sets = wl.get("sets", N_SETS)
     batches = []
+    step_in = [[] for _ in range(n_sets)]   # per set: each batch's x and logits bytes
     for T in wl["Ts"]:
         w = synth.Workload(base.name, T=T, D=D_MODEL, F=D_FF, E=ctx.n_exp, k=TOP_K,
                            seed=base.seed, zipf_s=base.zipf_s)
@@ -416,29 +426,41 @@ def make_batches(ctx, wl, base, path_of, use_router):
         ls_h = [np.zeros((T, ctx.n_exp), np.float32) if use_router else
                 synth.make_logits(w, ctx.rank * 97 + i) for i in range(n_sets)]
         dev = ctx.dev
-        xb = T * D_MODEL * 2                              # bytes of x (bf16), a multiple of 16
-        lb = 0 if use_router else T * ctx.n_exp * 4       # bytes of the logits (fp32)
-        pin = []
-        for a, l in zip(xs_h, ls_h):
-            buf = torch.empty(xb + lb, dtype=torch.uint8).pin_memory()
-            buf[:xb] = torch.from_numpy(a.view(np.uint8).reshape(-1))
-            if lb:
-                buf[xb:] = torch.from_numpy(l.view(np.uint8).reshape(-1))
-            pin.append(buf)
-        dxl = torch.empty(xb + lb, dtype=torch.uint8, device=dev)
+        for i, (a, l) in enumerate(zip(xs_h, ls_h)):
+            step_in[i].append(pad256(a.view(np.uint8).reshape(-1)))
+            if not use_router:
+                step_in[i].append(pad256(l.view(np.uint8).reshape(-1)))
         batches.append({"T": T,
                         "x": [torch.from_numpy(a.view(np.int16)).to(dev) for a in xs_h],
                         "l": [torch.from_numpy(a).to(dev) for a in ls_h],
-                        "pxl": pin,
                         "plan": Plan(T, ctx.n_exp, TOP_K),
                         "out": torch.empty((T, D_MODEL), dtype=torch.int16, device=dev),
-                        "dxl": dxl,
-                        "dx": dxl[:xb].view(torch.int16).view(T, D_MODEL),
-                        "dl": (dxl[xb:].view(torch.float32).view(T, ctx.n_exp) if lb else
-                               torch.empty((T, ctx.n_exp), dtype=torch.float32, device=dev)),
-                        "hout": torch.empty((T, D_MODEL), dtype=torch.int16).pin_memory(),
                         "path": path_of(T)})
-    return batches
+    # the end-to-end pass's step buffers (every piece a multiple of 16 bytes)
+    nin = sum(len(p) for p in step_in[0])
+    pin = []
+    for parts in step_in:
+        buf = torch.empty(sum(len(p) for p in parts), dtype=torch.uint8).pin_memory()
+        buf.copy_(torch.from_numpy(np.concatenate(parts)))
+        pin.append(buf)
+    din = torch.empty(pin[0].numel(), dtype=torch.uint8, device=ctx.dev)
+    tot = sum(wl["Ts"])
+    dout = torch.empty((tot, D_MODEL), dtype=torch.int16, device=ctx.dev)
+    hout = torch.empty((tot, D_MODEL), dtype=torch.int16).pin_memory()
+    off, row = 0, 0
+    for b in batches:
+        T = b["T"]
+        xb, lb = T * D_MODEL * 2, (0 if use_router else T * ctx.n_exp * 4)
+        b["dx"] = din[off:off + xb].view(torch.int16).view(T, D_MODEL)
+        off += -(-xb // 256) * 256
+        b["dl"] = (din[off:off + lb].view(torch.float32).view(T, ctx.n_exp) if lb else
+                   torch.empty((T, ctx.n_exp), dtype=torch.float32, device=ctx.dev))
+        off += -(-lb // 256) * 256
+        b["dout"] = dout[row:row + T]
+        row += T
+    assert off == nin == din.numel()
+    step_io = {"pin": pin, "din": din, "dout": dout, "hout": hout}
+    return batches, step_io
 
 
 def kernel_work(path: str, T: int, active: int, fp4: bool = False, fp8: bool = False):
@@ -539,7 +561,7 @@ def measure(ctx, name, wl, steps, warmup, sampler, peaks, breakdown=True, path_o
         if path == "auto":
             return "decode" if T <= CROSSOVER_T else "forward"
         return path
-    batches = make_batches(ctx, wl, base, path_of, use_router)
+    batches, step_io = make_batches(ctx, wl, base, path_of, use_router)
     n_sets = wl.get("sets", N_SETS)
     for b in batches:  # size the workspace once for the largest call
         for op in (0, 1, 2):
@@ -549,6 +571,8 @@ def measure(ctx, name, wl, steps, warmup, sampler, peaks, breakdown=True, path_o
                  "forward": moe.MOE_PROF_STREAM_COPY if n_slots else moe.MOE_PROF_FORWARD_GEMM1}
 
     def step(i, events=None, e2e=False, prof_kind=None):
+        if e2e:  # the step's inputs, all batches: one copy
+            step_io["din"].copy_(step_io["pin"][i % n_sets], non_blocking=True)
         for bi, b in enumerate(batches):
             s = i % n_sets
             run = layer.decode if b["path"] == "decode" else layer.forward
@@ -557,7 +581,6 @@ def measure(ctx, name, wl, steps, warmup, sampler, peaks, breakdown=True, path_o
                 kind = prof_kind if prof_kind is not None else main_kind[b["path"]]
                 check(moe_profile_kernel(layer.h, kind, ev0, ev1), "profile")
             if e2e:
-                b["dxl"].copy_(b["pxl"][s], non_blocking=True)  # x (and logits): one copy
                 x, lg = b["dx"], b["dl"]
             else:
                 x, lg = b["x"][s], b["l"][s]
@@ -565,9 +588,10 @@ def measure(ctx, name, wl, steps, warmup, sampler, peaks, breakdown=True, path_o
                 check(layer.plan(b["T"], None, x, b["plan"], stream), "moe_plan")
             else:
                 check(layer.plan(b["T"], lg, None, b["plan"], stream), "moe_plan")
-            check(run(b["T"], x, b["plan"], b["out"], stream), "moe_" + b["path"])
-            if e2e:
-                b["hout"].copy_(b["out"], non_blocking=True)
+            check(run(b["T"], x, b["plan"], b["dout"] if e2e else b["out"], stream),
+                  "moe_" + b["path"])
+        if e2e:  # and its outputs: one copy
+            step_io["hout"].copy_(step_io["dout"], non_blocking=True)
 
     def events(n_rows):
         ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -667,8 +691,10 @@ def measure(ctx, name, wl, steps, warmup, sampler, peaks, breakdown=True, path_o
     if n_slots:
         roof, stream_info = stream_roofline(ctx, layer, stats0, stats1, kern_ms, steps,
                                             len(batches), store_info)
-    h2d = sum(T * D_MODEL * 2 + (0 if use_router else T * ctx.n_exp * 4) for T in wl["Ts"])
-    d2h = sum(T * D_MODEL * 2 for T in wl["Ts"])
+    # the bytes the end-to-end steps copy: the step's input buffer (x and
+    # logits of every batch, each padded to 256 bytes) and its outputs
+    h2d = step_io["din"].numel()
+    d2h = step_io["dout"].numel() * step_io["dout"].element_size()
     record = {
         "workload": wl["desc"], "T": wl["Ts"], "dtype": dtype_of(wl, path),
         "path": ("moe_plan (router)" if use_router else "moe_plan") + " + " +
