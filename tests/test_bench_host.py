@@ -63,3 +63,23 @@ def test_default_run_records_and_their_roofline_arithmetic():
     r = bench.roofline("forward", nbytes, flop, 4 * tensor_ms, peaks, "x")
     assert r["bound"] == "tensor" and abs(r["frac_of_binding_roof"] - 0.25) < 1e-12
     assert abs(r["frac"] - 0.125) < 1e-12   # of the FP8 peak, two-term work counted once
+
+
+def test_arithmetic_types_follow_the_workload():
+    w = bench.BENCH_WORKLOADS
+    assert bench.dtype_of(w["decode"], w["decode"]["path"]) == "mxfp4 x 2-term e4m3 -> f32"
+    assert bench.dtype_of(w["prefill4k"], "forward") == "mxfp4 x 2-term e4m3 -> f32"
+    assert bench.dtype_of(w["prefill4k_fp4"], "forward") == "mxfp4 x mxfp4 -> f32"
+    assert bench.dtype_of(w["router16k_fp4"], "forward") == "mxfp4 x mxfp4 -> f32"
+    assert bench.dtype_of(w["decode_fp8"], "decode") == "e4m3fn x f16 -> f32"
+    assert bench.dtype_of(w["prefill4k_fp8"], "forward") == "bf16 (from e4m3fn) x bf16 -> f32"
+    assert bench.dtype_of(w["decode"], "decode") == "mxfp4 x f16 -> f32"
+
+
+def test_end_to_end_inputs_keep_every_piece_256_byte_aligned():
+    import numpy as np
+    for n in (0, 1, 15, 16, 255, 256, 257, 14336, 3584):
+        a = np.arange(n, dtype=np.int64).astype(np.uint8)
+        p = bench.pad256(a)
+        assert len(p) % 256 == 0 and len(p) - n < 256
+        assert np.array_equal(p[:n], a) and not p[n:].any()
