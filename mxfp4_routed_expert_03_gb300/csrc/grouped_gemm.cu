@@ -197,19 +197,31 @@ struct Tile {
 };
 
 // Tile `ct` of the schedule: active expert a owns MT * ntt(a) consecutive
-// tiles (weight tile major, token tile minor). s_prefix, s_expert and s_seg
-// are the shared-memory copies of the token-tile prefix, the active experts
-// and their (first slot, rows) segments. Each role visits its tiles in
-// increasing order, so `a` (the caller's cursor, starting at 0) only moves
-// forward: a few shared-memory reads per tile.
-template <int NT>
+// tiles. Normally the token tile varies fastest: the CTAs working on one
+// weight tile run side by side and share it through L2, and so do the
+// activations of the expert's few token tiles. In the gate/up GEMM an expert
+// with more tiles than a wave of the grid (MT * ntt > G CTAs: a popular
+// expert of a skewed batch, dozens of token tiles) takes its weight tiles
+// fastest instead: the CTAs of one token tile share its activation rows (1.6
+// MB at d_model 7168, two terms) while they are in L2, which token-tile-
+// fastest order re-read from DRAM for every pair of weight tiles (skewed
+// prefill, T = 8192: 17.3 -> 13.3 GB per launch). The down GEMM keeps the
+// token tile fastest: there the expert's weights dominate what a token tile
+// would re-read. s_prefix, s_expert and s_seg are the shared-memory copies of
+// the token-tile prefix, the active experts and their (first slot, rows)
+// segments. Each role visits its tiles in increasing order, so `a` (the
+// caller's cursor, starting at 0) only moves forward: a few shared-memory
+// reads per tile.
+template <int NT, bool WM>
 __device__ __forceinline__ bool tile_at(int ct, int n_active, int MT, const int *s_prefix,
                                         const int *s_expert, const int2 *s_seg, int &a, Tile &t) {
     while (a + 1 < n_active && MT * s_prefix[a + 1] <= ct) ++a;  // last a with MT*prefix[a] <= ct
     const int ntt = s_prefix[a + 1] - s_prefix[a];
     if (ntt <= 0 || s_expert[a] < 0) return false;
     const int local = ct - MT * s_prefix[a];
-    const int mg = local / ntt, j = local % ntt;
+    const bool wide_expert = WM && (long long)MT * ntt > (long long)gridDim.x;
+    const int mg = wide_expert ? local % MT : local / ntt;
+    const int j = wide_expert ? local / MT : local % ntt;
     const int2 seg = s_seg[a];
     // token rows of the expert split evenly over its ntt tiles (32-bit
     // arithmetic unless the product is too large for it)
@@ -381,7 +393,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NT, AF>::THREADS, 1) moe_grouped_gem
         if constexpr (C::NARROW)
             return tile_at_list<NT, C::TLIST>(ct, MT, s_list, t_first, args, t);
         else
-            return tile_at<NT>(ct, n_active, MT, s_prefix, s_expert, s_seg, cur, t);
+            return tile_at<NT, MODE == MOE_GEMM_GATEUP>(ct, n_active, MT, s_prefix, s_expert, s_seg,
+                                                        cur, t);
     };
     // Next piece of this CTA's work: tile sg.tile, stages [sg.s0, sg.s1) of
     // it (all of them unless a narrow tile is split between CTAs). Every role
