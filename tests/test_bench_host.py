@@ -34,12 +34,13 @@ def test_store_workload_uses_peaked_codes():
 
 
 def test_traffic_lookup_requires_the_current_kernel_source():
-    src = os.path.join(bench.ROOT, "mxfp4_routed_expert_03_gb300", "csrc", "grouped_gemm.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     lines = [l.split() for l in open(os.path.join(bench.ROOT, "profiles", "traffic.txt"))
              if l.strip() and not l.startswith("#")]
     for name, h, wl, nbytes in lines:
-        got = bench.kernel_traffic(name, "grouped_gemm.cu", wl)
+        source = "decode.cu" if name.startswith("moe_decode") else "grouped_gemm.cu"
+        src = os.path.join(bench.ROOT, "mxfp4_routed_expert_03_gb300", "csrc", source)
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        got = bench.kernel_traffic(name, source, wl)
         assert got == (float(nbytes) if h == sha else None)
     assert bench.kernel_traffic("moe_grouped_gemm_kernel<0>", "grouped_gemm.cu", "no-such") is None
 
