@@ -450,56 +450,89 @@ __global__ void __launch_bounds__(256, F8 ? 1 : 2) moe_decode_down_kernel(
 // Combine: out[t][d] = bf16( sum_j w[t][j] * y[inv[t*k+j]][d] [+ shared[t][d]] ),
 // j ascending, the shared expert's output (weight 1.0) added last.
 // ---------------------------------------------------------------------------
-// Y: the row element type, float or bf16 bits (uint16_t).
+// Y: the row element type, float or bf16 bits (uint16_t). One block of 128
+// threads per (token, 128 x V columns); a thread takes V = 16 bytes of
+// each row (8 bf16 or 4 fp32 columns). The token's k slots and weights are
+// read once per block into shared memory, so each thread's k row loads are
+// independent of one another and issue back to back (the loop is unrolled):
+// the loads of one row per iteration behind a slot read made this kernel
+// latency-bound at ~4 TB/s. D is a multiple of 32 (the ABI's shape check).
 template <typename Y>
-__global__ void __launch_bounds__(256) moe_combine_slots_kernel(int T, int D, int k, int n_rows,
+__global__ void __launch_bounds__(128) moe_combine_slots_kernel(int T, int D, int k, int n_rows,
                                                                 const float *__restrict__ topk_w,
                                                                 const int32_t *__restrict__ inv,
                                                                 const Y *__restrict__ y,
                                                                 const float *__restrict__ shared,
                                                                 uint16_t *__restrict__ out,
                                                                 int *status) {
+    constexpr int V = 16 / (int)sizeof(Y);  // columns per thread
+    __shared__ int s_slot[MOE_MAX_TOPK];
+    __shared__ float s_w[MOE_MAX_TOPK];
     grid_dep_wait();  // (a dependent launch after the down GEMM that wrote y)
-    const int d4 = blockIdx.x * blockDim.x + threadIdx.x;  // group of 4 columns
-    if (d4 * 4 >= D) return;
+    const int c = (blockIdx.x * blockDim.x + threadIdx.x) * V;  // first column of the thread
     for (int t = blockIdx.y; t < T; t += gridDim.y) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-        int slot = inv[(size_t)t * k + j];
-        if (slot < 0 || slot >= n_rows) { moe_flag(status, MOE_ERR_BAD_INDEX); continue; }
-        float w = topk_w[(size_t)t * k + j];
-        float4 v;
-        if constexpr (sizeof(Y) == 2) {
-            const uint2 b = ((const uint2 *)(y + (size_t)slot * D))[d4];
-            v = make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xFFFF0000u),
-                            __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xFFFF0000u));
-        } else {
-            v = ((const float4 *)(y + (size_t)slot * D))[d4];
+        if ((int)threadIdx.x < k) {
+            int slot = inv[(size_t)t * k + threadIdx.x];
+            if (slot < 0 || slot >= n_rows) {
+                moe_flag(status, MOE_ERR_BAD_INDEX);
+                slot = -1;
+            }
+            s_slot[threadIdx.x] = slot;
+            s_w[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
         }
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
-    }
-    if (shared) {
-        const float4 v = ((const float4 *)(shared + (size_t)t * D))[d4];
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
-    }
-    uint2 o;
-    o.x = (uint32_t)f32_to_bf16_bits(acc.x) | ((uint32_t)f32_to_bf16_bits(acc.y) << 16);
-    o.y = (uint32_t)f32_to_bf16_bits(acc.z) | ((uint32_t)f32_to_bf16_bits(acc.w) << 16);
-    ((uint2 *)(out + (size_t)t * D))[d4] = o;
+        __syncthreads();
+        if (c < D) {
+            float acc[V];
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] = 0.f;
+#pragma unroll 8
+            for (int j = 0; j < k; ++j) {
+                const int slot = s_slot[j];
+                if (slot < 0) continue;
+                const float w = s_w[j];
+                const uint4 u = *(const uint4 *)(y + (size_t)slot * D + c);
+                const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+                if constexpr (sizeof(Y) == 2) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[2 * i] = fmaf(w, __uint_as_float(q[i] << 16), acc[2 * i]);
+                        acc[2 * i + 1] = fmaf(w, __uint_as_float(q[i] & 0xFFFF0000u), acc[2 * i + 1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i] = fmaf(w, __uint_as_float(q[i]), acc[i]);
+                }
+            }
+            if (shared) {
+#pragma unroll
+                for (int i = 0; i < V; i += 4) {
+                    const float4 v = *(const float4 *)(shared + (size_t)t * D + c + i);
+                    acc[i] += v.x;
+                    acc[i + 1] += v.y;
+                    acc[i + 2] += v.z;
+                    acc[i + 3] += v.w;
+                }
+            }
+            uint32_t o[V / 2];
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i)
+                o[i] = (uint32_t)f32_to_bf16_bits(acc[2 * i]) |
+                       ((uint32_t)f32_to_bf16_bits(acc[2 * i + 1]) << 16);
+            if constexpr (V == 8)
+                *(uint4 *)(out + (size_t)t * D + c) = make_uint4(o[0], o[1], o[2], o[3]);
+            else
+                *(uint2 *)(out + (size_t)t * D + c) = make_uint2(o[0], o[1]);
+        }
+        __syncthreads();  // the slots of the block's next token
     }
 }
 
 cudaError_t moe_launch_combine_slots(int T, int D, int k, int n_rows, const float *topk_w,
                                      const int32_t *inv, const float *y, const float *shared,
                                      uint16_t *out, int *status, cudaStream_t st) {
-    const dim3 g((unsigned)((D / 4 + 255) / 256), (unsigned)min(T, 65535));
-    return launch_pdl(moe_combine_slots_kernel<float>, g, dim3(256), 0, st, T, D, k, n_rows,
+    if (k < 1 || k > MOE_MAX_TOPK || D % 8) return cudaErrorInvalidValue;
+    const dim3 g((unsigned)((D / 4 + 127) / 128), (unsigned)min(T, 65535));
+    return launch_pdl(moe_combine_slots_kernel<float>, g, dim3(128), 0, st, T, D, k, n_rows,
                       topk_w, inv, y, shared, out, status);
 }
 
@@ -507,8 +540,9 @@ cudaError_t moe_launch_combine_slots_bf16(int T, int D, int k, int n_rows, const
                                           const int32_t *inv, const uint16_t *y,
                                           const float *shared, uint16_t *out, int *status,
                                           cudaStream_t st) {
-    const dim3 g((unsigned)((D / 4 + 255) / 256), (unsigned)min(T, 65535));
-    return launch_pdl(moe_combine_slots_kernel<uint16_t>, g, dim3(256), 0, st, T, D, k, n_rows,
+    if (k < 1 || k > MOE_MAX_TOPK || D % 8) return cudaErrorInvalidValue;
+    const dim3 g((unsigned)((D / 8 + 127) / 128), (unsigned)min(T, 65535));
+    return launch_pdl(moe_combine_slots_kernel<uint16_t>, g, dim3(128), 0, st, T, D, k, n_rows,
                       topk_w, inv, y, shared, out, status);
 }
 
