@@ -186,6 +186,10 @@ __device__ __forceinline__ void warp_sort64(uint64_t (&v)[P][2], int lane) {
 template <int NK>
 __device__ __forceinline__ void warp_select_thr(const uint32_t (&key)[NK], int k, int lane,
                                                 uint2 *scratch, int &pos_out, uint32_t &key_out) {
+    if (k > 16) {  // the k-th largest of 32 maxima bounds too little: nearly always > 64 keys
+        warp_select<NK>(key, k, lane, scratch, pos_out, key_out);
+        return;
+    }
     uint32_t m = 0u;
 #pragma unroll
     for (int i = 0; i < NK; ++i) m = key[i] > m ? key[i] : m;

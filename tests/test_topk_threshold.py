@@ -16,7 +16,10 @@ import pytest
 
 def select_by_threshold(keys, k):
     """keys: [32 * NK] in position order. Returns the k positions, or None
-    when more than 64 keys reach the threshold (the fallback's case)."""
+    when the kernel takes the bitwise search instead: k > 16, or more than 64
+    keys reach the threshold."""
+    if k > 16:
+        return None
     lanes = keys.reshape(-1, 32).T            # lane l: positions l + 32 i
     t0 = np.sort(lanes.max(axis=1))[::-1][k - 1]
     cand = [(int(keys[p]), p) for p in range(len(keys)) if keys[p] >= t0]
@@ -50,7 +53,7 @@ def test_threshold_select_matches_a_full_sort(E, k):
             fallbacks += 1
             continue
         assert got == reference(keys, k)
-    if k <= 16:   # (k = 32: t0 is the smallest lane maximum, so the fallback decides)
+    if k <= 16:   # (k > 16: the bitwise search decides)
         assert fallbacks < 60
 
 
