@@ -226,6 +226,38 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # Clock sampling during the timed region
 # ---------------------------------------------------------------------------
+def bind_host_to_gpu(uuid: str):
+    """Runs this process on the CPU cores NVML names as the GPU's neighbours
+    (a read-only query), so the pinned host buffers of the end-to-end pass are
+    placed in memory next to it. Returns the cores, or None when NVML is not
+    there or names none (the process then keeps its cores)."""
+    import ctypes
+    try:
+        nvml = ctypes.CDLL("libnvidia-ml.so.1")
+    except OSError:
+        return None
+    if nvml.nvmlInit_v2() != 0:
+        return None
+    try:
+        dev = ctypes.c_void_p()
+        if nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(dev)) != 0:
+            return None
+        words = ((os.cpu_count() or 64) + 63) // 64
+        mask = (ctypes.c_ulong * words)()
+        if nvml.nvmlDeviceGetCpuAffinity(dev, ctypes.c_uint(words), mask) != 0:
+            return None
+        cpus = {64 * i + b for i in range(words) for b in range(64) if (mask[i] >> b) & 1}
+        cpus &= os.sched_getaffinity(0)
+        if not cpus:
+            return None
+        os.sched_setaffinity(0, cpus)
+        return sorted(cpus)
+    except (AttributeError, OSError):
+        return None
+    finally:
+        nvml.nvmlShutdown()
+
+
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -809,7 +841,9 @@ def run_ours(args):
     ctx = Ctx(args, n_exp, dev, rank, world, dist)
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
         if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
-    sampler = ClockSampler("GPU-" + str(torch.cuda.get_device_properties(dev).uuid))
+    gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    host_cpus = bind_host_to_gpu(gpu_uuid)
+    sampler = ClockSampler(gpu_uuid)
     wl = dict(BENCH_WORKLOADS[args.workload])
     if args.tokens:
         wl["Ts"] = [args.tokens]
@@ -831,7 +865,9 @@ def run_ours(args):
                     "(L2 129 MB) and the inputs rotate through "
                     f"{wl.get('sets', N_SETS)} pre-generated sets, so the selected experts "
                     "change from step to step",
-              "parallelism": f"replicas x{world}"}
+              "parallelism": f"replicas x{world}",
+              "host_cores": (f"{len(host_cpus)} next to the GPU (NVML affinity)" if host_cpus
+                             else "unbound")}
     line = {
         "metric": METRIC, "value": head["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
