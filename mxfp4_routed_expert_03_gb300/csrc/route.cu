@@ -249,14 +249,22 @@ __device__ __forceinline__ void warp_select_thr(const uint32_t (&key)[NK], int k
 // On return lane j < k holds the j-th selection (expert index, logit):
 // descending logit, ties to the lower expert index. NaN logits count as -inf
 // and set nan_seen. Lane l owns experts l, l + 32, ... (coalesced loads).
-// scratch: 64 entries of warp-private shared memory.
+// THR: the threshold select (fewer dependent steps: the small-batch plan,
+// where one warp's latency is the time); else the bitwise search (fewer
+// instructions: the large-batch kernel, where many warps share each SM and
+// the threshold select measured 1.8x slower). scratch: 64 entries of
+// warp-private shared memory (k entries without THR).
+template <bool THR>
 __device__ __forceinline__ void warp_topk(const float *row, int E, int k, int lane, int &my_e,
                                           float &my_v, bool &nan_seen, uint2 *scratch) {
     uint32_t key[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) key[i] = row_key(row, lane + 32 * i, E, nan_seen);
     uint32_t kv;
-    warp_select_thr<32>(key, k, lane, scratch, my_e, kv);
+    if constexpr (THR)
+        warp_select_thr<32>(key, k, lane, scratch, my_e, kv);
+    else
+        warp_select<32>(key, k, lane, scratch, my_e, kv);
     my_v = lane < k ? key_logit(kv) : -INFINITY;
 }
 
@@ -362,7 +370,7 @@ __global__ void __launch_bounds__(kPlanSmallThreads) moe_plan_small_kernel(
     for (int t = wid; t < T; t += kPlanSmallWarps) {
         int my_e;
         float my_v;
-        warp_topk(logits + (int64_t)t * E, E, k, lane, my_e, my_v, nan_seen, s_scr[wid]);
+        warp_topk<true>(logits + (int64_t)t * E, E, k, lane, my_e, my_v, nan_seen, s_scr[wid]);
         const float w = warp_select_weight(my_v, k, lane);
         if (lane < k) {
             topk_idx[(int64_t)t * k + lane] = my_e;
@@ -415,14 +423,15 @@ __global__ void __launch_bounds__(256) moe_topk_kernel(int T, int E, int k,
                                                        const float *__restrict__ logits,
                                                        int32_t *topk_idx, float *topk_w,
                                                        int *status) {
-    __shared__ uint2 s_scratch[8][64];
+    __shared__ uint2 s_scratch[8][MOE_MAX_TOPK];
     int lane = threadIdx.x & 31;
     int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
     int my_e;
     float my_v;
     bool nan_seen = false;
-    warp_topk(logits + (int64_t)t * E, E, k, lane, my_e, my_v, nan_seen, s_scratch[threadIdx.x >> 5]);
+    warp_topk<false>(logits + (int64_t)t * E, E, k, lane, my_e, my_v, nan_seen,
+                     s_scratch[threadIdx.x >> 5]);
     float w = warp_select_weight(my_v, k, lane);
     if (lane < k) {
         topk_idx[(int64_t)t * k + lane] = my_e;
